@@ -1,0 +1,57 @@
+"""Plant plausible mistakes in the oracle (on the CPU, by monkeypatching) and
+check that a pin catches each one: a dropped term, a wrong sign, a transposed
+operand, a wrong shard index."""
+import numpy as np
+
+from oracle import tp_oracle as O
+from tests import test_oracle_pins as pins
+
+
+def test_dropped_term_in_gelu_prime_is_caught(monkeypatch):
+    bad = lambda x: 0.5 * (1.0 + O._erf(np.asarray(x) / O.SQRT2))  # Phi only, x*phi dropped
+    monkeypatch.setattr(O, "gelu_prime", bad)
+    errs = pins.fd_errors_mlp_gelu(2)
+    assert max(errs.values()) > 1e-3
+
+
+def test_wrong_sign_in_swiglu_grad_is_caught(monkeypatch):
+    def bad(dA, G, U):
+        s = O.sigmoid(G)
+        return dA * U * s * (1.0 - G * (1.0 - s)), dA * G * s
+    monkeypatch.setattr(O, "_swiglu_grads", bad)
+    errs = pins.fd_errors_mlp_swiglu(2)
+    assert max(errs.values()) > 1e-3
+
+
+def test_transposed_weight_grad_is_caught(monkeypatch):
+    real = O.mlp_gelu_bwd
+
+    def bad(X, W1, W2, dZ, N):
+        g = real(X, W1, W2, dZ, N)
+        # dW2 built as dZ^T H instead of H^T dZ, reshaped to fit
+        H = O.gelu(X @ W1)
+        g["dW2"] = (dZ.T @ H).reshape(g["dW2"].shape)
+        return g
+    monkeypatch.setattr(O, "mlp_gelu_bwd", bad)
+    errs = pins.fd_errors_mlp_gelu(2)
+    assert errs["dW2"] > 1e-3
+
+
+def test_wrong_row_shard_is_caught(monkeypatch):
+    real = O.row_shards
+
+    def bad(W, N):
+        s = real(W, N)
+        return s[::-1]  # shard i paired with the wrong row block
+    monkeypatch.setattr(O, "row_shards", bad)
+    r = np.random.default_rng(0)
+    X, W = r.normal(size=(3, 6)), r.normal(size=(6, 5))
+    assert O.rel_err(O.row_linear(X, W, 2), X @ W) > 1e-3
+
+
+def test_tanh_gelu_is_caught(monkeypatch):
+    tanh_gelu = lambda x: 0.5 * np.asarray(x) * (1 + np.tanh(np.sqrt(2 / np.pi) * (x + 0.044715 * np.asarray(x) ** 3)))
+    monkeypatch.setattr(O, "gelu", tanh_gelu)
+    import pytest
+    with pytest.raises(AssertionError):
+        pins.test_gelu_phi_table()
