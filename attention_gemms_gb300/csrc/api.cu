@@ -1,0 +1,355 @@
+// C ABI of libtpmlp: argument validation, workspace carving and the composition
+// of the tensor-parallel linear block out of GEMM / reduction launches.
+#include <cuda_runtime.h>
+
+#include <initializer_list>
+#include <string>
+
+#include "internal.h"
+
+namespace tp {
+
+tp_status check_device();
+void set_debug_hang(int v);
+
+namespace {
+
+bool al16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
+
+tp_status need(bool cond, tp_status s, const char* msg) { return cond ? TP_OK : fail(s, msg); }
+
+tp_status check_aligned(std::initializer_list<const void*> ptrs) {
+  for (const void* p : ptrs)
+    if (p && !al16(p)) return fail(TP_ERR_ALIGNMENT, "device buffers must be 16-byte aligned");
+  return TP_OK;
+}
+
+tp_status check_dtype(tp_dtype dt) {
+  return need(dt == TP_BF16 || dt == TP_F32, TP_ERR_DTYPE, "dtype must be TP_BF16 or TP_F32");
+}
+
+// bf16 tile rules: reduced widths and per-shard widths are whole 64-column blocks
+tp_status check_mlp_shape(int64_t M, int64_t h, int64_t f, int32_t N, tp_dtype dt) {
+  TP_TRY(need(N >= 1, TP_ERR_INVALID_ARG, "shard count N must be >= 1"));
+  TP_TRY(need(M >= 0 && h >= 1 && f >= 1, TP_ERR_INVALID_ARG, "sizes must be positive (M >= 0)"));
+  TP_TRY(need(f % N == 0, TP_ERR_SHAPE, "h' (f) must be divisible by the shard count N"));
+  if (dt == TP_BF16) {
+    TP_TRY(need(h % 64 == 0, TP_ERR_SHAPE, "bf16 path: h must be a multiple of 64"));
+    TP_TRY(need((f / N) % 64 == 0, TP_ERR_SHAPE, "bf16 path: h'/N must be a multiple of 64"));
+  }
+  return TP_OK;
+}
+
+size_t partial_bytes(int64_t M, int64_t n, int32_t N, tp_reduce mode) {
+  return mode == TP_REDUCE_BUFFERS ? static_cast<size_t>(N) * M * n * sizeof(float) : 0;
+}
+
+tp_status col_impl(const void* X, const void* W, const void* Wu, void* Y, void* Yu, void* out,
+                   int64_t M, int64_t h, int64_t f, int32_t N, tp_dtype dt, tp_act act,
+                   cudaStream_t st) {
+  GemmDesc d;
+  d.dtype = dt;
+  d.M = M;
+  d.N = f;
+  d.K = h;
+  d.A[0] = {X, M, h, h};
+  d.B[0] = {W, h, f, f};
+  d.b_mn = true;
+  d.ldo = f;
+  d.shards = N;
+  d.shard_axis = 1;
+  if (act == TP_ACT_NONE) {
+    d.epi = EPI_STORE;
+    d.out[0] = out;
+    d.out_f32 = dt == TP_F32;
+  } else if (act == TP_ACT_GELU) {
+    d.epi = EPI_GELU;
+    d.out[0] = Y;
+    d.out[1] = out;
+  } else {
+    d.paired = true;
+    d.B[1] = {Wu, h, f, f};
+    d.epi = EPI_SWIGLU;
+    d.out[0] = Y;
+    d.out[1] = Yu;
+    d.out[2] = out;
+  }
+  return launch_gemm(d, st);
+}
+
+// out = sum_i Xs_i W_i (+ residual): variant A (partials + reduce) or B (split-K fold)
+tp_status row_impl(const void* Xs, const void* W, const void* residual, void* out, int64_t M,
+                   int64_t k, int64_t n, int32_t N, tp_dtype dt, tp_reduce mode, void* ws,
+                   cudaStream_t st) {
+  GemmDesc d;
+  d.dtype = dt;
+  d.M = M;
+  d.N = n;
+  d.A[0] = {Xs, M, k, k};
+  d.B[0] = {W, k, n, n};
+  d.b_mn = true;
+  d.ldo = n;
+  d.epi = EPI_STORE;
+  if (mode == TP_REDUCE_SPLITK) {
+    d.K = k;
+    d.in[0] = residual;
+    d.out[0] = out;
+    d.out_f32 = dt == TP_F32;
+    return launch_gemm(d, st);
+  }
+  d.K = k / N;
+  d.groups = N;
+  d.out[0] = ws;
+  d.out_f32 = true;
+  d.out_group_stride = M * n;
+  TP_TRY(launch_gemm(d, st));
+  return launch_shard_reduce(static_cast<const float*>(ws), residual, out, N, M, n, dt, st);
+}
+
+// dX = sum_i sum_s dA_s,i B_s,i^T over nseg operand pairs (dY with W1, or dG/dU with Wg/Wu)
+tp_status dx_impl(const void* const* dA, const void* const* Wt, int nseg, void* dX, int64_t M,
+                  int64_t h, int64_t f, int32_t N, tp_dtype dt, tp_reduce mode, void* ws,
+                  cudaStream_t st) {
+  GemmDesc d;
+  d.dtype = dt;
+  d.M = M;
+  d.N = h;
+  d.nseg = nseg;
+  for (int s = 0; s < nseg; ++s) {
+    d.A[s] = {dA[s], M, f, f};   // dY (M, f), K-major
+    d.B[s] = {Wt[s], h, f, f};   // W1 (h, f) read as B(k = f, n = h): K-major
+  }
+  d.ldo = h;
+  d.epi = EPI_STORE;
+  if (mode == TP_REDUCE_SPLITK) {
+    d.K = f;
+    d.out[0] = dX;
+    d.out_f32 = dt == TP_F32;
+    return launch_gemm(d, st);
+  }
+  d.K = f / N;
+  d.groups = N;
+  d.out[0] = ws;
+  d.out_f32 = true;
+  d.out_group_stride = M * h;
+  TP_TRY(launch_gemm(d, st));
+  return launch_shard_reduce(static_cast<const float*>(ws), nullptr, dX, N, M, h, dt, st);
+}
+
+}  // namespace
+}  // namespace tp
+
+using namespace tp;
+
+extern "C" {
+
+void tp_debug_inject_wait_fault(int enable) { set_debug_hang(enable); }
+
+size_t tp_workspace_size(tp_op op, int64_t M, int64_t h, int64_t f, int32_t N, tp_dtype dtype,
+                         tp_act act, tp_reduce mode) {
+  if (N < 1 || M < 0 || h < 1 || f < 1) return 0;
+  if (dtype != TP_BF16 && dtype != TP_F32) return 0;
+  const size_t elt = elem_size(dtype);
+  switch (op) {
+    case TP_OP_COL_LINEAR: return 0;
+    case TP_OP_ROW_LINEAR: return partial_bytes(M, f, N, mode);
+    case TP_OP_MLP_FWD:
+      return align_up(static_cast<size_t>(M) * f * elt, 256) + partial_bytes(M, h, N, mode);
+    case TP_OP_MLP_BWD:
+      return (act == TP_ACT_SWIGLU ? 2 : 1) * align_up(static_cast<size_t>(M) * f * elt, 256) +
+             partial_bytes(M, h, N, mode);
+    default: return 0;
+  }
+}
+
+tp_status tp_col_linear(const void* X, const void* W, const void* W_up, void* Y, void* Y_up,
+                        void* out, int64_t M, int64_t h, int64_t f, int32_t N, tp_dtype dtype,
+                        tp_act act, void* stream) {
+  TP_TRY(check_dtype(dtype));
+  TP_TRY(need(act >= TP_ACT_NONE && act <= TP_ACT_SWIGLU, TP_ERR_INVALID_ARG, "unknown act"));
+  TP_TRY(need(X && W && out, TP_ERR_INVALID_ARG, "X, W and out are required"));
+  TP_TRY(need(act != TP_ACT_SWIGLU || W_up, TP_ERR_INVALID_ARG, "SwiGLU needs W_up"));
+  TP_TRY(check_mlp_shape(M, h, f, N, dtype));
+  TP_TRY(check_aligned({X, W, W_up, Y, Y_up, out}));
+  if (M == 0) return TP_OK;
+  TP_TRY(check_device());
+  return col_impl(X, W, W_up, Y, Y_up, out, M, h, f, N, dtype, act,
+                  static_cast<cudaStream_t>(stream));
+}
+
+tp_status tp_row_linear(const void* Xs, const void* W, const void* residual, void* out, int64_t M,
+                        int64_t k, int64_t n, int32_t N, tp_dtype dtype, tp_reduce mode, void* ws,
+                        size_t ws_bytes, void* stream) {
+  TP_TRY(check_dtype(dtype));
+  TP_TRY(need(mode == TP_REDUCE_BUFFERS || mode == TP_REDUCE_SPLITK, TP_ERR_INVALID_ARG,
+              "unknown reduce mode"));
+  TP_TRY(need(Xs && W && out, TP_ERR_INVALID_ARG, "Xs, W and out are required"));
+  TP_TRY(need(N >= 1, TP_ERR_INVALID_ARG, "shard count N must be >= 1"));
+  TP_TRY(need(M >= 0 && k >= 1 && n >= 1, TP_ERR_INVALID_ARG, "sizes must be positive (M >= 0)"));
+  TP_TRY(need(k % N == 0, TP_ERR_SHAPE, "k must be divisible by the shard count N"));
+  if (dtype == TP_BF16) {
+    TP_TRY(need((k / N) % 64 == 0, TP_ERR_SHAPE, "bf16 path: k/N must be a multiple of 64"));
+    TP_TRY(need(n % 64 == 0, TP_ERR_SHAPE, "bf16 path: n must be a multiple of 64"));
+  }
+  TP_TRY(check_aligned({Xs, W, residual, out, ws}));
+  if (M == 0) return TP_OK;
+  const size_t need_ws = partial_bytes(M, n, N, mode);
+  TP_TRY(need(ws_bytes >= need_ws && (need_ws == 0 || ws), TP_ERR_WORKSPACE,
+              "workspace smaller than tp_workspace_size"));
+  TP_TRY(check_device());
+  return row_impl(Xs, W, residual, out, M, k, n, N, dtype, mode, ws,
+                  static_cast<cudaStream_t>(stream));
+}
+
+tp_status tp_shard_reduce(const float* partials, const void* residual, void* out, int32_t N,
+                          int64_t M, int64_t n, tp_dtype out_dtype, void* stream) {
+  TP_TRY(check_dtype(out_dtype));
+  TP_TRY(need(partials && out, TP_ERR_INVALID_ARG, "partials and out are required"));
+  TP_TRY(need(N >= 1 && M >= 0 && n >= 1, TP_ERR_INVALID_ARG, "need N >= 1, M >= 0, n >= 1"));
+  TP_TRY(check_aligned({partials, residual, out}));
+  if (M == 0) return TP_OK;
+  TP_TRY(check_device());
+  return launch_shard_reduce(partials, residual, out, N, M, n, out_dtype,
+                             static_cast<cudaStream_t>(stream));
+}
+
+tp_status tp_mlp_fwd(const void* X, const void* W1, const void* W1_up, const void* W2,
+                     const void* residual, void* Y, void* Y_up, void* H, void* Z, int64_t M,
+                     int64_t h, int64_t f, int32_t N, tp_dtype dtype, tp_act act, tp_reduce mode,
+                     void* ws, size_t ws_bytes, void* stream) {
+  TP_TRY(check_dtype(dtype));
+  TP_TRY(need(act == TP_ACT_GELU || act == TP_ACT_SWIGLU, TP_ERR_INVALID_ARG,
+              "MLP act must be TP_ACT_GELU or TP_ACT_SWIGLU"));
+  TP_TRY(need(mode == TP_REDUCE_BUFFERS || mode == TP_REDUCE_SPLITK, TP_ERR_INVALID_ARG,
+              "unknown reduce mode"));
+  TP_TRY(need(X && W1 && W2 && Z, TP_ERR_INVALID_ARG, "X, W1, W2 and Z are required"));
+  TP_TRY(need(act != TP_ACT_SWIGLU || W1_up, TP_ERR_INVALID_ARG, "SwiGLU needs W1_up"));
+  TP_TRY(check_mlp_shape(M, h, f, N, dtype));
+  TP_TRY(check_aligned({X, W1, W1_up, W2, residual, Y, Y_up, H, Z, ws}));
+  if (M == 0) return TP_OK;
+  const size_t h_bytes = H ? 0 : align_up(static_cast<size_t>(M) * f * elem_size(dtype), 256);
+  const size_t need_ws = h_bytes + partial_bytes(M, h, N, mode);
+  TP_TRY(need(ws_bytes >= need_ws && (need_ws == 0 || ws), TP_ERR_WORKSPACE,
+              "workspace smaller than tp_workspace_size"));
+  TP_TRY(check_device());
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* Hb = H ? H : ws;
+  void* parts = static_cast<char*>(ws) + h_bytes;
+  TP_TRY(col_impl(X, W1, W1_up, Y, Y_up, Hb, M, h, f, N, dtype, act, st));
+  return row_impl(Hb, W2, residual, Z, M, f, h, N, dtype, mode, parts, st);
+}
+
+tp_status tp_mlp_bwd(const void* X, const void* W1, const void* W1_up, const void* W2,
+                     const void* Y, const void* Y_up, const void* H, const void* dZ, void* dX,
+                     void* dW1, void* dW1_up, void* dW2, int64_t M, int64_t h, int64_t f,
+                     int32_t N, tp_dtype dtype, tp_act act, tp_reduce mode, void* ws,
+                     size_t ws_bytes, void* stream) {
+  TP_TRY(check_dtype(dtype));
+  TP_TRY(need(act == TP_ACT_GELU || act == TP_ACT_SWIGLU, TP_ERR_INVALID_ARG,
+              "MLP act must be TP_ACT_GELU or TP_ACT_SWIGLU"));
+  TP_TRY(need(mode == TP_REDUCE_BUFFERS || mode == TP_REDUCE_SPLITK, TP_ERR_INVALID_ARG,
+              "unknown reduce mode"));
+  const bool sw = act == TP_ACT_SWIGLU;
+  TP_TRY(need(X && W1 && W2 && Y && H && dZ && dX && dW1 && dW2, TP_ERR_INVALID_ARG,
+              "X, W1, W2, Y, H, dZ, dX, dW1 and dW2 are required"));
+  TP_TRY(need(!sw || (W1_up && Y_up && dW1_up), TP_ERR_INVALID_ARG,
+              "SwiGLU needs W1_up, Y_up and dW1_up"));
+  TP_TRY(check_mlp_shape(M, h, f, N, dtype));
+  TP_TRY(check_aligned({X, W1, W1_up, W2, Y, Y_up, H, dZ, dX, dW1, dW1_up, dW2, ws}));
+  if (M == 0) return TP_OK;
+  const size_t elt = elem_size(dtype);
+  const size_t g_one = align_up(static_cast<size_t>(M) * f * elt, 256);
+  const size_t g_bytes = (sw ? 2 : 1) * g_one;
+  const size_t need_ws = g_bytes + partial_bytes(M, h, N, mode);
+  TP_TRY(need(ws_bytes >= need_ws && ws, TP_ERR_WORKSPACE,
+              "workspace smaller than tp_workspace_size"));
+  TP_TRY(check_device());
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* dY = ws;  // GELU: dY; SwiGLU: dG then dU
+  void* dU = static_cast<char*>(ws) + g_one;
+  void* parts = static_cast<char*>(ws) + g_bytes;
+
+  // 1. g-backward is the identity: every shard reads all of dZ.
+  //    dH_i = dZ W2_i^T with the activation derivative fused (row-parallel dX_i = dY W_i^T)
+  {
+    GemmDesc d;
+    d.dtype = dtype;
+    d.M = M;
+    d.N = f;
+    d.K = h;
+    d.A[0] = {dZ, M, h, h};
+    d.B[0] = {W2, f, h, h};  // W2 (f, h) read as B(k = h, n = f): K-major
+    d.ldo = f;
+    d.shards = N;
+    d.shard_axis = 1;
+    if (sw) {
+      d.epi = EPI_DSWIGLU;
+      d.in[0] = Y;
+      d.in[1] = Y_up;
+      d.out[0] = dY;
+      d.out[1] = dU;
+    } else {
+      d.epi = EPI_DGELU;
+      d.in[0] = Y;
+      d.out[0] = dY;
+    }
+    TP_TRY(launch_gemm(d, st));
+  }
+  // 2. dW2_i = H_i^T dZ (row-parallel weight gradient; shard i = row block i)
+  {
+    GemmDesc d;
+    d.dtype = dtype;
+    d.M = f;
+    d.N = h;
+    d.K = M;
+    d.A[0] = {H, M, f, f};
+    d.a_mn = true;
+    d.B[0] = {dZ, M, h, h};
+    d.b_mn = true;
+    d.ldo = h;
+    d.epi = EPI_STORE;
+    d.out[0] = dW2;
+    d.out_f32 = dtype == TP_F32;
+    d.shards = N;
+    d.shard_axis = 0;
+    TP_TRY(launch_gemm(d, st));
+  }
+  // 3. dW1_i = X^T dY_i (column-parallel weight gradient; shard i = column block i)
+  {
+    GemmDesc d;
+    d.dtype = dtype;
+    d.M = h;
+    d.N = f;
+    d.K = M;
+    d.A[0] = {X, M, h, h};
+    d.a_mn = true;
+    d.B[0] = {dY, M, f, f};
+    d.b_mn = true;
+    d.ldo = f;
+    d.shards = N;
+    d.shard_axis = 1;
+    if (sw) {
+      d.paired = true;
+      d.B[1] = {dU, M, f, f};
+      d.epi = EPI_PAIR;
+      d.out[0] = dW1;
+      d.out[1] = dW1_up;
+    } else {
+      d.epi = EPI_STORE;
+      d.out[0] = dW1;
+      d.out_f32 = dtype == TP_F32;
+    }
+    TP_TRY(launch_gemm(d, st));
+  }
+  // 4. f-backward: dX = sum_i dY_i W1_i^T (SwiGLU: + dU_i W1up_i^T)
+  if (sw) {
+    const void* dA[2] = {dY, dU};
+    const void* Wt[2] = {W1, W1_up};
+    return dx_impl(dA, Wt, 2, dX, M, h, f, N, dtype, mode, parts, st);
+  }
+  const void* dA[1] = {dY};
+  const void* Wt[1] = {W1};
+  return dx_impl(dA, Wt, 1, dX, M, h, f, N, dtype, mode, parts, st);
+}
+
+}  // extern "C"

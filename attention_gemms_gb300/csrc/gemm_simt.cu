@@ -1,0 +1,176 @@
+// fp32 GEMM engine on CUDA cores (FFMA, no TF32: TF32's 10-bit mantissa would not
+// hold the fp32 path to 1e-5). Same problem descriptor and epilogues as the
+// tensor-core engine; 64 x 64 output tile per CTA, 4 x 4 per thread, K in steps of 16.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "epi_math.cuh"
+#include "internal.h"
+
+namespace tp {
+namespace {
+
+constexpr int TM = 64, TN = 64, TK = 16;
+
+struct SimtParams {
+  const float* A[2];
+  const float* B[2];
+  int64_t lda[2], ldb[2];
+  int64_t M, N, K;
+  int a_mn, b_mn, nseg, paired;
+  float* out0;
+  float* out1;
+  float* out2;
+  const float* in0;
+  const float* in1;
+  int64_t ldo, out_group_stride;
+};
+
+template <int EPI>
+__device__ __forceinline__ void epi1(const SimtParams& p, int g, int64_t r, int64_t c, float a,
+                                     float b) {
+  const int64_t i = r * p.ldo + c;
+  if constexpr (EPI == EPI_STORE) {
+    p.out0[g * p.out_group_stride + i] = a + (p.in0 ? p.in0[i] : 0.0f);
+  } else if constexpr (EPI == EPI_GELU) {
+    if (p.out0) p.out0[i] = a;
+    p.out1[i] = gelu_f(a);
+  } else if constexpr (EPI == EPI_SWIGLU) {
+    if (p.out0) p.out0[i] = a;
+    if (p.out1) p.out1[i] = b;
+    p.out2[i] = silu_f(a) * b;
+  } else if constexpr (EPI == EPI_DGELU) {
+    p.out0[i] = a * gelu_prime_f(p.in0[i]);
+  } else if constexpr (EPI == EPI_DSWIGLU) {
+    float du;
+    p.out0[i] = dswiglu_f(a, p.in0[i], p.in1[i], du);
+    p.out1[i] = du;
+  } else if constexpr (EPI == EPI_PAIR) {
+    p.out0[i] = a;
+    p.out1[i] = b;
+  }
+}
+
+template <int EPI, bool PAIRED>
+__global__ void __launch_bounds__(256) gemm_simt_kernel(const SimtParams p) {
+  __shared__ float As[TK][TM + 4];
+  __shared__ float Bs[PAIRED ? 2 : 1][TK][TN + 4];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * TM;
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * TN;
+  const int g = blockIdx.z;
+  float acc[4][4] = {}, acc2[4][4] = {};
+  for (int s = 0; s < p.nseg; ++s) {
+    const float* A = p.A[s];
+    const int64_t lda = p.lda[s];
+    for (int64_t k0 = 0; k0 < p.K; k0 += TK) {
+      for (int e = threadIdx.x; e < TM * TK; e += 256) {
+        // consecutive threads walk the contiguous storage dimension
+        const int mm = p.a_mn ? e % TM : e / TK;
+        const int kk = p.a_mn ? e / TM : e % TK;
+        const int64_t gm = m0 + mm, lk = k0 + kk, gk = g * p.K + lk;
+        float v = 0.0f;
+        if (gm < p.M && lk < p.K) v = p.a_mn ? A[gk * lda + gm] : A[gm * lda + gk];
+        As[kk][mm] = v;
+      }
+      for (int h = 0; h < (PAIRED ? 2 : 1); ++h) {
+        const float* B = p.B[PAIRED ? h : s];
+        const int64_t ldb = p.ldb[PAIRED ? h : s];
+        for (int e = threadIdx.x; e < TN * TK; e += 256) {
+          const int nn = p.b_mn ? e % TN : e / TK;
+          const int kk = p.b_mn ? e / TN : e % TK;
+          const int64_t gn = n0 + nn, lk = k0 + kk, gk = g * p.K + lk;
+          float v = 0.0f;
+          if (gn < p.N && lk < p.K) v = p.b_mn ? B[gk * ldb + gn] : B[gn * ldb + gk];
+          Bs[h][kk][nn] = v;
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int kk = 0; kk < TK; ++kk) {
+        float a[4], b[4], b2[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          a[i] = As[kk][ty * 4 + i];
+          b[i] = Bs[0][kk][tx * 4 + i];
+          if constexpr (PAIRED) b2[i] = Bs[PAIRED ? 1 : 0][kk][tx * 4 + i];
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+            if constexpr (PAIRED) acc2[i][j] = fmaf(a[i], b2[j], acc2[i][j]);
+          }
+      }
+      __syncthreads();
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t r = m0 + ty * 4 + i, c = n0 + tx * 4 + j;
+      if (r < p.M && c < p.N) epi1<EPI>(p, g, r, c, acc[i][j], acc2[i][j]);
+    }
+}
+
+template <int EPI, bool PAIRED>
+void launch_k(const SimtParams& p, dim3 grid, cudaStream_t st) {
+  gemm_simt_kernel<EPI, PAIRED><<<grid, 256, 0, st>>>(p);
+}
+
+}  // namespace
+
+tp_status launch_gemm_simt(const GemmDesc& d, cudaStream_t st) {
+  if (d.M <= 0 || d.N <= 0 || d.K <= 0) return TP_OK;
+  SimtParams p{};
+  for (int s = 0; s < 2; ++s) {
+    const int sa = s < d.nseg ? s : 0;
+    const int sb = s < (d.paired ? 2 : d.nseg) ? s : 0;
+    p.A[s] = static_cast<const float*>(d.A[sa].ptr);
+    p.lda[s] = d.A[sa].ld;
+    p.B[s] = static_cast<const float*>(d.B[sb].ptr);
+    p.ldb[s] = d.B[sb].ld;
+  }
+  p.M = d.M;
+  p.N = d.N;
+  p.K = d.K;
+  p.a_mn = d.a_mn;
+  p.b_mn = d.b_mn;
+  p.nseg = d.nseg;
+  p.paired = d.paired;
+  p.out0 = static_cast<float*>(d.out[0]);
+  p.out1 = static_cast<float*>(d.out[1]);
+  p.out2 = static_cast<float*>(d.out[2]);
+  p.in0 = static_cast<const float*>(d.in[0]);
+  p.in1 = static_cast<const float*>(d.in[1]);
+  p.ldo = d.ldo;
+  p.out_group_stride = d.out_group_stride;
+  const int64_t gx = (d.N + TN - 1) / TN, gy = (d.M + TM - 1) / TM;
+  if (gx > 2147483647ll || gy > 65535 || d.groups > 65535)
+    return fail(TP_ERR_SHAPE, "fp32 GEMM grid too large");
+  dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(d.groups));
+  const bool pr = d.paired;
+  switch (d.epi) {
+    case EPI_STORE: launch_k<EPI_STORE, false>(p, grid, st); break;
+    case EPI_GELU: launch_k<EPI_GELU, false>(p, grid, st); break;
+    case EPI_SWIGLU:
+      if (!pr) return fail(TP_ERR_INVALID_ARG, "SwiGLU epilogue needs a paired problem");
+      launch_k<EPI_SWIGLU, true>(p, grid, st);
+      break;
+    case EPI_DGELU: launch_k<EPI_DGELU, false>(p, grid, st); break;
+    case EPI_DSWIGLU: launch_k<EPI_DSWIGLU, false>(p, grid, st); break;
+    case EPI_PAIR:
+      if (!pr) return fail(TP_ERR_INVALID_ARG, "pair epilogue needs a paired problem");
+      launch_k<EPI_PAIR, true>(p, grid, st);
+      break;
+    default: return fail(TP_ERR_INVALID_ARG, "unknown epilogue");
+  }
+  count_launch();
+  TP_CUDA_TRY(cudaGetLastError());
+  return TP_OK;
+}
+
+}  // namespace tp

@@ -1,0 +1,549 @@
+// Tensor-core GEMM engine for sm_103a: TMA -> shared-memory ring -> tcgen05.mma
+// (bf16 in, fp32 accumulate in TMEM) -> fused epilogue from TMEM.
+//
+// One persistent CTA per SM, 6 warps with fixed roles:
+//   warp 0      TMA producer (one lane): fills a STAGES-deep ring of A/B tiles
+//   warp 1      MMA issuer (one lane) and TMEM owner: 128 x BN x 16 MMAs into one
+//               of two TMEM accumulators (double buffer), commits to mbarriers
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator (each warp owns 32 TMEM
+//               lanes = 32 rows), activation / gradient / residual math, stores
+// The tile space is enumerated shard by shard (each virtual rank's slab in turn),
+// and inside a slab in groups of 16 M-tiles so that concurrently running CTAs
+// share operand tiles through L2.
+//
+// Every mbarrier wait is bounded by a time limit; on expiry the CTA records
+// TP_ERR_TIMEOUT in the device status word, waits for its own copies and MMAs
+// in flight, frees its TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "epi_math.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tp {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kThreads = 192;
+constexpr int kGroupM = 16;
+constexpr uint64_t kDrainTimeoutNs = 1000000000ull;
+
+template <int BN>
+struct TcCfg {
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int NBARS = 2 * STAGES + 6;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + NBARS * 8 + 16;
+};
+
+struct TcParams {  // CUtensorMap members carry their own 128-byte alignment
+  CUtensorMap tmA[2];
+  CUtensorMap tmB[2];
+  int64_t M, N, K;  // N counts logical output columns
+  int a_mn, b_mn, nseg, paired, groups;
+  int tiles_m, tiles_n, kb_per_seg;
+  int shards, shard_axis;
+  void* out0;
+  void* out1;
+  void* out2;
+  const void* in0;
+  const void* in1;
+  int64_t ldo;
+  int out_f32;
+  int64_t out_group_stride;
+  int* status;
+  uint64_t timeout_ns;
+  int debug_hang;
+};
+
+struct TileCoord {
+  int g, mt, nt;
+};
+
+__device__ __forceinline__ TileCoord tile_coord(const TcParams& p, int t) {
+  const int tm = p.tiles_m, tn = p.tiles_n;
+  int g = 0;
+  if (p.groups > 1) {
+    g = t / (tm * tn);
+    t -= g * tm * tn;
+  }
+  int slab_m = tm, slab_n = tn, s = 0;
+  if (p.shards > 1) {
+    if (p.shard_axis == 0) slab_m = tm / p.shards;
+    else slab_n = tn / p.shards;
+    s = t / (slab_m * slab_n);
+    t -= s * slab_m * slab_n;
+  }
+  const int grp = t / (kGroupM * slab_n);
+  const int first_m = grp * kGroupM;
+  const int gm = min(slab_m - first_m, kGroupM);
+  const int r = t - grp * kGroupM * slab_n;
+  int mt = first_m + r % gm;
+  int nt = r / gm;
+  if (p.shards > 1) {
+    if (p.shard_axis == 0) mt += s * slab_m;
+    else nt += s * slab_n;
+  }
+  return {g, mt, nt};
+}
+
+__device__ __forceinline__ void record_timeout(int* status) {
+  atomicCAS(status, 0, static_cast<int>(TP_ERR_TIMEOUT));
+  atomicAdd(status + 1, 1);
+}
+
+// ---- bf16 pack / unpack of 8 values (16 bytes)
+__device__ __forceinline__ uint4 pack8(const float* v) {
+  uint4 r;
+  uint32_t* w = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t*>(&b);
+  }
+  return r;
+}
+__device__ __forceinline__ void unpack8(uint4 r, float* v) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(&r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+__device__ __forceinline__ void st8(void* base, int64_t idx, const float* v) {
+  *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(base) + idx) = pack8(v);
+}
+__device__ __forceinline__ void ld8(const void* base, int64_t idx, float* v) {
+  unpack8(__ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(base) + idx)), v);
+}
+
+// Epilogue of 8 consecutive output columns of one row. a: accumulator values,
+// b: the paired half (gate/up second operand) when the problem is paired.
+template <int EPI>
+__device__ __forceinline__ void epi8(const TcParams& p, int g, int64_t row, int64_t col,
+                                     const float* a, const float* b) {
+  const int64_t idx = row * p.ldo + col;
+  float v[8], w[8];
+  if constexpr (EPI == EPI_STORE) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = a[i];
+    if (p.in0) {
+      ld8(p.in0, idx, w);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] += w[i];
+    }
+    if (p.out_f32) {
+      float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out0) +
+                                            g * p.out_group_stride + idx);
+      o[0] = make_float4(v[0], v[1], v[2], v[3]);
+      o[1] = make_float4(v[4], v[5], v[6], v[7]);
+    } else {
+      st8(p.out0, idx, v);
+    }
+  } else if constexpr (EPI == EPI_GELU) {
+    if (p.out0) st8(p.out0, idx, a);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = gelu_f(a[i]);
+    st8(p.out1, idx, v);
+  } else if constexpr (EPI == EPI_SWIGLU) {
+    if (p.out0) st8(p.out0, idx, a);
+    if (p.out1) st8(p.out1, idx, b);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = silu_f(a[i]) * b[i];
+    st8(p.out2, idx, v);
+  } else if constexpr (EPI == EPI_DGELU) {
+    ld8(p.in0, idx, w);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = a[i] * gelu_prime_f(w[i]);
+    st8(p.out0, idx, v);
+  } else if constexpr (EPI == EPI_DSWIGLU) {
+    float gg[8], uu[8], du[8];
+    ld8(p.in0, idx, gg);
+    ld8(p.in1, idx, uu);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = dswiglu_f(a[i], gg[i], uu[i], du[i]);
+    st8(p.out0, idx, v);
+    st8(p.out1, idx, du);
+  } else if constexpr (EPI == EPI_PAIR) {
+    st8(p.out0, idx, a);
+    st8(p.out1, idx, b);
+  }
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
+  using C = TcCfg<BN>;
+  constexpr int S = C::STAGES;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * S + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
+  const uint32_t never_bar = bar0 + 8u * (2 * S + 5);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 4);
+    }
+    mbar_init(drain_bar, 1);
+    mbar_init(never_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmA[0]);
+    tma_prefetch_desc(&p.tmB[0]);
+    if (p.nseg > 1) tma_prefetch_desc(&p.tmA[1]);
+    if (p.nseg > 1 || p.paired) tma_prefetch_desc(&p.tmB[1]);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  const int ntiles = p.tiles_m * p.tiles_n * p.groups;
+  const int nkb = p.nseg * p.kb_per_seg;
+  const int bn_logical = p.paired ? BN / 2 : BN;
+  uint32_t issued = 0;      // producer: loads issued
+  bool mma_issued = false;  // MMA thread: any MMA issued
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      const uint32_t stage_tx = C::STAGE_BYTES;
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const TileCoord tc = tile_coord(p, t);
+        const int m0 = tc.mt * BM;
+        const int n0 = tc.nt * bn_logical;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int seg = kb / p.kb_per_seg;
+          const int k0 = static_cast<int>(tc.g * p.K) + (kb - seg * p.kb_per_seg) * BK;
+          const uint32_t a_dst = sbase + stage * C::STAGE_BYTES;
+          const uint32_t b_dst = a_dst + C::A_BYTES;
+          mbar_arrive_expect_tx(full_bar(stage), stage_tx);
+          if (p.a_mn) {
+            tma_load_2d(a_dst, &p.tmA[seg], full_bar(stage), m0, k0);
+            tma_load_2d(a_dst + 8192, &p.tmA[seg], full_bar(stage), m0 + 64, k0);
+          } else {
+            tma_load_2d(a_dst, &p.tmA[seg], full_bar(stage), k0, m0);
+          }
+          if (p.paired) {
+            constexpr int HALF = BN / 128;  // 64-wide boxes per half
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) {
+              const int half = j / HALF;
+              tma_load_2d(b_dst + j * 8192, &p.tmB[half], full_bar(stage), n0 + 64 * (j % HALF), k0);
+            }
+          } else if (p.b_mn) {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(b_dst + j * 8192, &p.tmB[seg], full_bar(stage), n0 + 64 * j, k0);
+          } else {
+            tma_load_2d(b_dst, &p.tmB[seg], full_bar(stage), k0, n0);
+          }
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) record_timeout(p.status);
+    }
+    __syncwarp();  // reconverge before the block-wide (aligned) barriers below
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      const uint32_t idesc = idesc_bf16_f32(BM, BN, p.a_mn, p.b_mn);
+      const uint32_t a_lbo = p.a_mn ? 8192u : 16u, b_lbo = p.b_mn ? 8192u : 16u;
+      const uint32_t a_kstep = p.a_mn ? 2048u : 32u, b_kstep = p.b_mn ? 2048u : 32u;
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      if (p.debug_hang) ok = mbar_wait(never_bar, 0, p.timeout_ns, abort_flag);
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, p.timeout_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = sbase + stage * C::STAGE_BYTES;
+          const uint32_t b_addr = a_addr + C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = sw128_desc(a_addr + kk * a_kstep, a_lbo, 1024u);
+            const uint64_t bd = sw128_desc(b_addr + kk * b_kstep, b_lbo, 1024u);
+            mma_bf16_ss(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          mma_issued = true;
+          mma_commit(empty_bar(stage));
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(tfull_bar(acc));
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (!ok) record_timeout(p.status);
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int quad = warp & 3;  // TMEM lanes [32*quad, 32*quad + 32)
+    uint32_t acc = 0, acc_phase = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      const TileCoord tc = tile_coord(p, t);
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(tfull_bar(acc), acc_phase, p.timeout_ns, abort_flag) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) {
+        if (lane == 0) record_timeout(p.status);
+        break;
+      }
+      tc_fence_after();
+      const int64_t row = static_cast<int64_t>(tc.mt) * BM + quad * 32 + lane;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+      const int64_t col_base = static_cast<int64_t>(tc.nt) * bn_logical;
+      for (int c = 0; c < bn_logical / 32; ++c) {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(t_row + c * 32, ra);
+        if (p.paired) tmem_ld32(t_row + BN / 2 + c * 32, rb);
+        tmem_ld_wait();
+        if (row < p.M) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int64_t col = col_base + c * 32 + q * 8;
+            if (col < p.N) {
+              float a[8], b[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                a[i] = __uint_as_float(ra[q * 8 + i]);
+                b[i] = __uint_as_float(rb[q * 8 + i]);
+              }
+              epi8<EPI>(p, tc.g, row, col, a, b);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  __syncthreads();
+  if (*abort_flag) {
+    volatile int no_abort = 0;
+    if (warp == 0) {
+      if (lane == 0) {
+        // wait for every copy this CTA issued: the last load into stage s
+        for (int s = 0; s < S; ++s) {
+          if (issued > static_cast<uint32_t>(s)) {
+            const uint32_t last = ((issued - 1u - s) / S) * S + s;
+            mbar_wait(full_bar(s), (last / S) & 1u, kDrainTimeoutNs, &no_abort);
+          }
+        }
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      if (lane == 0 && mma_issued) {
+        mma_commit(drain_bar);
+        mbar_wait(drain_bar, 0, kDrainTimeoutNs, &no_abort);
+      }
+      __syncwarp();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// 2-D bf16 map over a row-major tensor, 128-byte swizzle, zero fill out of bounds.
+tp_status make_map(CUtensorMap* m, const Operand& op, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn enc = get_encoder();
+  if (!enc) return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
+  if (reinterpret_cast<uintptr_t>(op.ptr) % 16 != 0 || (op.ld * 2) % 16 != 0)
+    return fail(TP_ERR_ALIGNMENT, "TMA operand base/pitch not 16-byte aligned");
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(op.cols), static_cast<cuuint64_t>(op.rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(op.ld) * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(op.ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled failed (code " + std::to_string(r) + ")");
+  return TP_OK;
+}
+
+template <int BN, int EPI>
+tp_status launch_bn_epi(const TcParams& prm, int grid, cudaStream_t st) {
+  auto kern = gemm_tc_kernel<BN, EPI>;
+  static bool attr_set = false;  // per instantiation; benign race (idempotent)
+  if (!attr_set) {
+    TP_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     TcCfg<BN>::SMEM_BYTES));
+    attr_set = true;
+  }
+  kern<<<grid, kThreads, TcCfg<BN>::SMEM_BYTES, st>>>(prm);
+  count_launch();
+  TP_CUDA_TRY(cudaGetLastError());
+  return TP_OK;
+}
+
+template <int BN>
+tp_status launch_bn(int epi, const TcParams& prm, int grid, cudaStream_t st) {
+  switch (epi) {
+    case EPI_STORE: return launch_bn_epi<BN, EPI_STORE>(prm, grid, st);
+    case EPI_GELU: return launch_bn_epi<BN, EPI_GELU>(prm, grid, st);
+    case EPI_SWIGLU: return launch_bn_epi<BN, EPI_SWIGLU>(prm, grid, st);
+    case EPI_DGELU: return launch_bn_epi<BN, EPI_DGELU>(prm, grid, st);
+    case EPI_DSWIGLU: return launch_bn_epi<BN, EPI_DSWIGLU>(prm, grid, st);
+    case EPI_PAIR: return launch_bn_epi<BN, EPI_PAIR>(prm, grid, st);
+  }
+  return fail(TP_ERR_INVALID_ARG, "unknown epilogue");
+}
+
+std::atomic<int> g_debug_hang{0};
+
+}  // namespace
+
+void set_debug_hang(int v) { g_debug_hang.store(v); }
+
+tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
+  if (d.M <= 0 || d.N <= 0 || d.K <= 0) return TP_OK;
+  if (d.paired && (!d.b_mn || d.nseg != 1))
+    return fail(TP_ERR_INVALID_ARG, "paired GEMM needs MN-major B and one K segment");
+  if (d.N % 8 != 0) return fail(TP_ERR_SHAPE, "GEMM output width must be a multiple of 8");
+  if (d.groups > 1 && d.K % BK != 0)
+    return fail(TP_ERR_SHAPE, "per-shard K must be a multiple of 64");
+  const int epi = d.epi;
+  // tile width in TMEM columns: 256 unless the problem is narrow
+  const int64_t n_tmem = d.paired ? 2 * d.N : d.N;
+  const int BN = n_tmem >= 256 ? 256 : 128;
+  const int bn_logical = d.paired ? BN / 2 : BN;
+
+  TcParams prm;
+  memset(&prm, 0, sizeof(prm));
+  for (int s = 0; s < d.nseg; ++s) {
+    if (d.a_mn) TP_TRY(make_map(&prm.tmA[s], d.A[s], 64, 64));
+    else TP_TRY(make_map(&prm.tmA[s], d.A[s], 64, BM));
+  }
+  const int nb = d.paired ? 2 : d.nseg;
+  for (int s = 0; s < nb; ++s) {
+    if (d.b_mn) TP_TRY(make_map(&prm.tmB[s], d.B[s], 64, 64));
+    else TP_TRY(make_map(&prm.tmB[s], d.B[s], 64, static_cast<uint32_t>(BN)));
+  }
+  if (d.nseg == 1) prm.tmA[1] = prm.tmA[0];
+  if (nb == 1) prm.tmB[1] = prm.tmB[0];
+  prm.M = d.M;
+  prm.N = d.N;
+  prm.K = d.K;
+  prm.a_mn = d.a_mn;
+  prm.b_mn = d.b_mn;
+  prm.nseg = d.nseg;
+  prm.paired = d.paired;
+  prm.groups = d.groups;
+  prm.tiles_m = static_cast<int>((d.M + BM - 1) / BM);
+  prm.tiles_n = static_cast<int>((d.N + bn_logical - 1) / bn_logical);
+  prm.kb_per_seg = static_cast<int>((d.K + BK - 1) / BK);
+  prm.shards = 1;
+  prm.shard_axis = d.shard_axis;
+  if (d.shards > 1) {
+    const int along = d.shard_axis == 0 ? prm.tiles_m : prm.tiles_n;
+    if (along % d.shards == 0) prm.shards = d.shards;
+  }
+  prm.out0 = d.out[0];
+  prm.out1 = d.out[1];
+  prm.out2 = d.out[2];
+  prm.in0 = d.in[0];
+  prm.in1 = d.in[1];
+  prm.ldo = d.ldo;
+  prm.out_f32 = d.out_f32;
+  prm.out_group_stride = d.out_group_stride;
+  prm.status = device_status_word();
+  if (!prm.status) return fail(TP_ERR_CUDA, "device status word unavailable");
+  prm.timeout_ns = wait_timeout_ns();
+  prm.debug_hang = g_debug_hang.load();
+
+  const int64_t ntiles = static_cast<int64_t>(prm.tiles_m) * prm.tiles_n * prm.groups;
+  if (ntiles > (1ll << 30)) return fail(TP_ERR_SHAPE, "problem too large");
+  const int grid = static_cast<int>(std::min<int64_t>(ntiles, device_sm_count()));
+  return BN == 256 ? launch_bn<256>(epi, prm, grid, st) : launch_bn<128>(epi, prm, grid, st);
+}
+
+}  // namespace tp

@@ -1,0 +1,96 @@
+// Internal interfaces of libtpmlp: the GEMM problem descriptor shared by the
+// tensor-core (tcgen05) and CUDA-core engines, epilogue kinds, launchers and
+// error plumbing. Not part of the public ABI.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+
+#include "../../include/tpmlp.h"
+
+namespace tp {
+
+// ------------------------------------------------------------------ errors
+
+void set_error(const std::string& msg);  // thread-local detail for tp_last_error
+tp_status fail(tp_status s, const std::string& msg);
+tp_status cuda_fail(cudaError_t e, const char* what);
+
+#define TP_CUDA_TRY(expr)                                   \
+  do {                                                      \
+    cudaError_t _e = (expr);                                \
+    if (_e != cudaSuccess) return ::tp::cuda_fail(_e, #expr); \
+  } while (0)
+
+#define TP_TRY(expr)                    \
+  do {                                  \
+    tp_status _s = (expr);              \
+    if (_s != TP_OK) return _s;         \
+  } while (0)
+
+// per-device sticky status word (device address) and the wait limit
+int* device_status_word();             // for the current device; nullptr on failure
+uint64_t wait_timeout_ns();
+int device_sm_count();                 // current device
+void count_launch(int n = 1);
+
+// ------------------------------------------------------------------ GEMM problem
+
+// Epilogue applied to each accumulator tile.
+enum EpiKind : int {
+  EPI_STORE = 0,    // out[0] = acc (+ in[0] residual)
+  EPI_GELU = 1,     // out[0] = acc (pre-activation, optional), out[1] = GELU(acc)
+  EPI_SWIGLU = 2,   // paired: out[0] = g (optional), out[1] = u (optional), out[2] = SiLU(g) u
+  EPI_DGELU = 3,    // out[0] = acc * GELU'(in[0])
+  EPI_DSWIGLU = 4,  // a = acc, g = in[0], u = in[1]: out[0] = dG, out[1] = dU
+  EPI_PAIR = 5,     // paired: out[0] = first half, out[1] = second half
+  EPI_COUNT = 6
+};
+
+// A 2-D row-major tensor in storage order.
+struct Operand {
+  const void* ptr = nullptr;
+  int64_t rows = 0, cols = 0;  // storage extents
+  int64_t ld = 0;              // row pitch, elements
+};
+
+// D (M x N) = sum_{s < nseg} sum_k A_s(m, k) B_s(k, n), per K-group g:
+//   A(m, k) is A.ptr[m * ld + k] (K-major) or A.ptr[k * ld + m] (a_mn: MN-major),
+//   B(k, n) is B.ptr[n * ld + k] (K-major) or B.ptr[k * ld + n] (b_mn: MN-major);
+//   group g reads k in [g*K, (g+1)*K) and writes its output g*out_group_stride
+//   elements further (the per-shard partial buffers of the shard sum).
+// paired: B[0] feeds the first half of every tile's columns and B[1] the second;
+//   logical column n of the output takes B[0](., n) and B[1](., n) (gate/up).
+struct GemmDesc {
+  int64_t M = 0, N = 0, K = 0;
+  bool a_mn = false, b_mn = false;
+  int nseg = 1;
+  Operand A[2], B[2];
+  bool paired = false;
+  int groups = 1;
+  int shards = 1;      // tile order: `shards` equal slabs along shard_axis, slab-major
+  int shard_axis = 1;  // 0 = M, 1 = N
+  int epi = EPI_STORE;
+  void* out[3] = {nullptr, nullptr, nullptr};
+  const void* in[2] = {nullptr, nullptr};
+  int64_t ldo = 0;     // row pitch of outputs and of in[] (elements)
+  bool out_f32 = false;  // EPI_STORE: fp32 output (partials), else the element type
+  int64_t out_group_stride = 0;
+  tp_dtype dtype = TP_BF16;
+};
+
+tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st);    // bf16, tcgen05
+tp_status launch_gemm_simt(const GemmDesc& d, cudaStream_t st);  // fp32, CUDA cores
+tp_status launch_shard_reduce(const float* P, const void* residual, void* out, int N,
+                              int64_t M, int64_t n, tp_dtype out_dtype, cudaStream_t st);
+
+inline tp_status launch_gemm(const GemmDesc& d, cudaStream_t st) {
+  return d.dtype == TP_BF16 ? launch_gemm_tc(d, st) : launch_gemm_simt(d, st);
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline size_t elem_size(tp_dtype t) { return t == TP_BF16 ? 2 : 4; }
+
+}  // namespace tp

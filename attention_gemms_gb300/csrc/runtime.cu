@@ -1,0 +1,125 @@
+// Runtime plumbing of libtpmlp: thread-local error detail, the per-device sticky
+// status word that bounded device waits report into, the wait limit, SM counts
+// and the launch counter.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+#include <string>
+
+#include "internal.h"
+
+namespace tp {
+
+// status[0]: first error code recorded by a kernel; status[1]: how many CTAs gave up.
+__device__ int g_tp_status[4];
+
+namespace {
+thread_local std::string t_err;
+std::atomic<uint64_t> g_timeout_ns{0};
+std::atomic<uint64_t> g_launches{0};
+constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_status_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+}  // namespace
+
+void set_error(const std::string& msg) { t_err = msg; }
+
+tp_status fail(tp_status s, const std::string& msg) {
+  t_err = std::string(tp_status_string(s)) + ": " + msg;
+  return s;
+}
+
+tp_status cuda_fail(cudaError_t e, const char* what) {
+  t_err = std::string("TP_ERR_CUDA: ") + what + ": " + cudaGetErrorString(e);
+  return TP_ERR_CUDA;
+}
+
+int* device_status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_tp_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sm_count[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 1;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+uint64_t wait_timeout_ns() {
+  const uint64_t v = g_timeout_ns.load();
+  return v ? v : kDefaultTimeoutNs;
+}
+
+void count_launch(int n) { g_launches.fetch_add(static_cast<uint64_t>(n)); }
+
+// The kernels are built for sm_103a only.
+tp_status check_device() {
+  int dev = 0, maj = 0, min = 0;
+  TP_CUDA_TRY(cudaGetDevice(&dev));
+  TP_CUDA_TRY(cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev));
+  TP_CUDA_TRY(cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev));
+  if (maj != 10 || min != 3)
+    return fail(TP_ERR_UNSUPPORTED, "device is sm_" + std::to_string(maj) + std::to_string(min) +
+                                        "; this library is built for sm_103a");
+  return TP_OK;
+}
+
+}  // namespace tp
+
+extern "C" {
+
+int tp_version(void) { return TPMLP_VERSION; }
+
+const char* tp_status_string(tp_status s) {
+  switch (s) {
+    case TP_OK: return "TP_OK";
+    case TP_ERR_INVALID_ARG: return "TP_ERR_INVALID_ARG";
+    case TP_ERR_SHAPE: return "TP_ERR_SHAPE";
+    case TP_ERR_DTYPE: return "TP_ERR_DTYPE";
+    case TP_ERR_ALIGNMENT: return "TP_ERR_ALIGNMENT";
+    case TP_ERR_WORKSPACE: return "TP_ERR_WORKSPACE";
+    case TP_ERR_CUDA: return "TP_ERR_CUDA";
+    case TP_ERR_TIMEOUT: return "TP_ERR_TIMEOUT";
+    case TP_ERR_UNSUPPORTED: return "TP_ERR_UNSUPPORTED";
+  }
+  return "TP_ERR_UNKNOWN";
+}
+
+const char* tp_last_error(void) { return tp::t_err.c_str(); }
+
+void tp_set_wait_timeout_ns(uint64_t ns) { tp::g_timeout_ns.store(ns); }
+
+uint64_t tp_launch_count(void) { return tp::g_launches.load(); }
+
+tp_status tp_check_status(void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  TP_CUDA_TRY(cudaStreamSynchronize(st));
+  int* d = tp::device_status_word();
+  if (!d) return tp::fail(TP_ERR_CUDA, "device status word unavailable");
+  int h[4] = {0, 0, 0, 0};
+  TP_CUDA_TRY(cudaMemcpy(h, d, sizeof(h), cudaMemcpyDeviceToHost));
+  if (h[0] == 0) return TP_OK;
+  const int zero[4] = {0, 0, 0, 0};
+  TP_CUDA_TRY(cudaMemcpy(d, zero, sizeof(zero), cudaMemcpyHostToDevice));
+  return tp::fail(static_cast<tp_status>(h[0]),
+                  "a bounded device wait expired in " + std::to_string(h[1]) + " CTA role(s)");
+}
+
+}  // extern "C"

