@@ -162,6 +162,34 @@ size_t tp_workspace_size(tp_op op, int64_t M, int64_t h, int64_t f, int32_t N, t
   }
 }
 
+tp_status tp_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                  int a_trans, int b_trans, tp_dtype dtype, void* stream) {
+  TP_TRY(check_dtype(dtype));
+  TP_TRY(need(A && B && C, TP_ERR_INVALID_ARG, "A, B and C are required"));
+  TP_TRY(need(M >= 0 && N >= 0 && K >= 1, TP_ERR_INVALID_ARG, "need M, N >= 0 and K >= 1"));
+  if (dtype == TP_BF16) {
+    TP_TRY(need(N % 8 == 0 && (a_trans ? M : K) % 8 == 0 && (b_trans ? K : N) % 8 == 0,
+                TP_ERR_SHAPE, "bf16 path: N and the stored row widths must be multiples of 8"));
+  }
+  TP_TRY(check_aligned({A, B, C}));
+  if (M == 0 || N == 0) return TP_OK;
+  TP_TRY(check_device());
+  GemmDesc d;
+  d.dtype = dtype;
+  d.M = M;
+  d.N = N;
+  d.K = K;
+  d.a_mn = a_trans != 0;
+  d.b_mn = b_trans == 0;
+  d.A[0] = a_trans ? Operand{A, K, M, M} : Operand{A, M, K, K};
+  d.B[0] = b_trans ? Operand{B, N, K, K} : Operand{B, K, N, N};
+  d.ldo = N;
+  d.epi = EPI_STORE;
+  d.out[0] = C;
+  d.out_f32 = dtype == TP_F32;
+  return launch_gemm(d, static_cast<cudaStream_t>(stream));
+}
+
 tp_status tp_col_linear(const void* X, const void* W, const void* W_up, void* Y, void* Y_up,
                         void* out, int64_t M, int64_t h, int64_t f, int32_t N, tp_dtype dtype,
                         tp_act act, void* stream) {

@@ -51,16 +51,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase with parity `parity` to complete. Gives up when
-// `deadline` (globaltimer ns) passes or another role of the CTA has already
-// given up (`*abort` != 0); then sets *abort and returns false.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t deadline,
+// Bounded wait for the phase with parity `parity` to complete. Gives up after
+// `timeout_ns` nanoseconds (%globaltimer) of waiting, or as soon as another role
+// of the CTA has given up (`*abort` != 0); sets *abort and returns false then.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
                                           volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() > deadline) {
+    if (globaltimer_ns() - t0 > timeout_ns) {
       *abort = 1;
       return false;
     }

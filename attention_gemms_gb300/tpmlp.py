@@ -74,6 +74,7 @@ _SIGS = {
     "tp_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "tp_launch_count": (ctypes.c_uint64, []),
     "tp_workspace_size": (_SZ, [_ST, _I64, _I64, _I64, _I32, _ST, _ST, _ST]),
+    "tp_gemm": (_ST, [_P, _P, _P, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, _ST, _P]),
     "tp_col_linear": (_ST, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _ST, _ST, _P]),
     "tp_row_linear": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _ST, _ST, _P, _SZ, _P]),
     "tp_shard_reduce": (_ST, [_P, _P, _P, _I32, _I64, _I64, _ST, _P]),
@@ -174,6 +175,11 @@ def tp_debug_inject_wait_fault(enable: bool) -> None:
 
 
 # ---------------------------------------------------------------- layers
+
+def tp_gemm(A, B, C, M, N, K, a_trans, b_trans, dtype, stream=None):
+    _check(lib().tp_gemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, int(bool(a_trans)),
+                         int(bool(b_trans)), int(dtype), _stream(stream)))
+
 
 def tp_col_linear(X, W, W_up, Y, Y_up, out, M, h, f, N, dtype, act, stream=None):
     _check(lib().tp_col_linear(_ptr(X), _ptr(W), _ptr(W_up), _ptr(Y), _ptr(Y_up), _ptr(out),

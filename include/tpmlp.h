@@ -128,6 +128,19 @@ TP_API uint64_t tp_launch_count(void);
 TP_API size_t tp_workspace_size(tp_op op, int64_t M, int64_t h, int64_t f, int32_t N,
                          tp_dtype dtype, tp_act act, tp_reduce mode);
 
+/*
+ * Plain GEMM on the library's engine (tensor cores for bf16, CUDA cores for fp32):
+ *   C (M, N) = A B, fp32 accumulation, C row-major with element type `dtype`.
+ *   A is (M, K) row-major, or -- when a_trans != 0 -- stored as its transpose (K, M);
+ *   B is (K, N) row-major, or -- when b_trans != 0 -- stored as its transpose (N, K).
+ * This is the building block of every layer below (the transposed forms are how the
+ * backward reads X^T, H^T and W^T in place, with no transpose copies).
+ * bf16 rule: the stored row widths (K or M for A, N or K for B) and N are multiples of 8.
+ * Errors: TP_ERR_INVALID_ARG, TP_ERR_SHAPE, TP_ERR_ALIGNMENT, TP_ERR_CUDA.
+ */
+TP_API tp_status tp_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                         int a_trans, int b_trans, tp_dtype dtype, void* stream);
+
 /* ------------------------------------------------------------------ layers */
 
 /*
