@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <initializer_list>
+#include <mutex>
 #include <string>
 
 #include "internal.h"
@@ -381,3 +382,68 @@ tp_status tp_mlp_bwd(const void* X, const void* W1, const void* W1_up, const voi
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ no-allocation variant
+//
+// tp_row_linear_noalloc: the row-parallel linear with per-shard partial buffers
+// (TP_REDUCE_BUFFERS), for callers that cannot allocate device memory -- for
+// example a library loaded into a host process whose device memory is owned by
+// its own pool allocator, or which runs under a fixed device-memory budget, so it
+// can neither call cudaMalloc itself nor hand this library a workspace. The fp32
+// partials live in the fixed array below instead of a caller workspace.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 32u << 20;  // 32 MiB, held by every device that loads the library
+
+__device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+
+// Device address of g_noalloc_scratch on the current device. In host code the
+// symbol's name is only a host-side stand-in, so the address must come from
+// cudaGetSymbolAddress, called with that device current; it is looked up once per
+// device and cached.
+tp_status noalloc_scratch(void** out) {
+  int dev = 0;
+  TP_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(TP_ERR_UNSUPPORTED, "device ordinal above 63");
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    TP_CUDA_TRY(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return TP_OK;
+}
+
+}  // namespace
+
+extern "C" tp_status tp_row_linear_noalloc(const void* Xs, const void* W, const void* residual,
+                                           void* out, int64_t M, int64_t k, int64_t n, int32_t N,
+                                           tp_dtype dtype, void* stream) {
+  TP_TRY(check_dtype(dtype));
+  TP_TRY(need(Xs && W && out, TP_ERR_INVALID_ARG, "Xs, W and out are required"));
+  TP_TRY(need(N >= 1, TP_ERR_INVALID_ARG, "shard count N must be >= 1"));
+  TP_TRY(need(M >= 0 && k >= 1 && n >= 1, TP_ERR_INVALID_ARG, "sizes must be positive (M >= 0)"));
+  TP_TRY(need(k % N == 0, TP_ERR_SHAPE, "k must be divisible by the shard count N"));
+  if (dtype == TP_BF16) {
+    TP_TRY(need((k / N) % 64 == 0, TP_ERR_SHAPE, "bf16 path: k/N must be a multiple of 64"));
+    TP_TRY(need(n % 64 == 0, TP_ERR_SHAPE, "bf16 path: n must be a multiple of 64"));
+  }
+  TP_TRY(check_aligned({Xs, W, residual, out}));
+  if (M == 0) return TP_OK;
+  const size_t need_bytes = partial_bytes(M, n, N, TP_REDUCE_BUFFERS);
+  TP_TRY(need(need_bytes <= kNoAllocScratchBytes, TP_ERR_WORKSPACE,
+              "N*M*n*4 bytes of partials exceed the fixed 32 MiB scratch of tp_row_linear_noalloc"));
+  TP_TRY(check_device());
+  void* scratch = nullptr;
+  TP_TRY(noalloc_scratch(&scratch));
+  // every partial element the reduction reads is written first by the GEMM, so the
+  // previous call's contents need no clearing
+  return row_impl(Xs, W, residual, out, M, k, n, N, dtype, TP_REDUCE_BUFFERS, scratch,
+                  static_cast<cudaStream_t>(stream));
+}
+

@@ -82,6 +82,7 @@ _SIGS = {
                          _ST, _P, _SZ, _P]),
     "tp_mlp_bwd": (_ST, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32,
                          _ST, _ST, _ST, _P, _SZ, _P]),
+    "tp_row_linear_noalloc": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _ST, _P]),
     "tp_debug_inject_wait_fault": (None, [ctypes.c_int]),
 }
 
@@ -209,3 +210,8 @@ def tp_mlp_bwd(X, W1, W1_up, W2, Y, Y_up, H, dZ, dX, dW1, dW1_up, dW2, M, h, f, 
                             _ptr(H), _ptr(dZ), _ptr(dX), _ptr(dW1), _ptr(dW1_up), _ptr(dW2),
                             M, h, f, N, int(dtype), int(act), int(mode), _ptr(ws),
                             int(ws_bytes), _stream(stream)))
+
+
+def tp_row_linear_noalloc(Xs, W, residual, out, M, k, n, N, dtype, stream=None):
+    _check(lib().tp_row_linear_noalloc(_ptr(Xs), _ptr(W), _ptr(residual), _ptr(out), M, k, n, N,
+                                       int(dtype), _stream(stream)))

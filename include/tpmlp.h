@@ -240,6 +240,29 @@ TP_API tp_status tp_mlp_bwd(const void* X, const void* W1, const void* W1_up, co
                      tp_dtype dtype, tp_act act, tp_reduce mode,
                      void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * Row-parallel linear + shard sum with per-shard partial buffers, allocating
+ * nothing. (The pages have no counterpart: this is a deployment variant.)
+ *
+ * Same computation, arguments and errors as tp_row_linear with
+ * mode = TP_REDUCE_BUFFERS, but the N*M*n fp32 partials live in a fixed 32 MiB
+ * device array inside the library instead of a caller workspace. For callers that
+ * cannot allocate device memory -- e.g. code running in a host process whose
+ * device memory is owned by that process's own pool allocator, or under a fixed
+ * memory budget -- and so can neither call cudaMalloc nor supply a workspace.
+ * No cudaMalloc, cudaFree or allocating library routine is called.
+ *   - Sizes with N*M*n*4 > 32 MiB are rejected with TP_ERR_WORKSPACE (nothing launched).
+ *   - Every device that loads the library holds the 32 MiB until the process exits.
+ *   - The first call on each device looks up the array's device address (with that
+ *     device current) and caches it; make that first call before any stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (e.g. on two
+ *     streams at once) race. Nothing in it needs to start at zero: every partial
+ *     that is read is written first by the same call.
+ */
+TP_API tp_status tp_row_linear_noalloc(const void* Xs, const void* W, const void* residual,
+                                       void* out, int64_t M, int64_t k, int64_t n, int32_t N,
+                                       tp_dtype dtype, void* stream);
+
 /* ------------------------------------------------------------------ testing */
 
 /* Failure injection for tests. While enabled (non-zero), every tensor-core GEMM
