@@ -39,6 +39,9 @@ WORKLOADS = {
                b=1, s=8192, h=8192, f=28672, N=4, act="swiglu", cfg=5),
     "c3": dict(desc="mid training erf-GELU MLP fwd+bwd: b=4 s=2048 h=4096 ffn=16384 N=8",
                b=4, s=2048, h=4096, f=16384, N=8, act="gelu", cfg=3),
+    # reduced-token case of c5 for ncu captures (a few GB on the device, inputs > L2)
+    "c5-2k": dict(desc="profiling case: SwiGLU MLP fwd+bwd b=1 s=2048 h=8192 ffn=28672 N=4",
+                  b=1, s=2048, h=8192, f=28672, N=4, act="swiglu", cfg=5),
 }
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -53,6 +56,28 @@ def mlp_flops(w, M=None):
 def col_gemm_flops(w):
     M = w["b"] * w["s"]
     return (4.0 if w["act"] == "swiglu" else 2.0) * M * w["h"] * w["f"]
+
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one column-GEMM launch,
+# from an ncu capture of the full-size workload, valid only for the kernel source it
+# was taken on (sha256 of csrc/gemm_tc.cu); see profiles/.
+COL_GEMM_TRAFFIC = {
+    "c5": {"bytes": 6.55e9 + 1.42e9, "src": "43985879dda58388"},
+    "c3": {"bytes": 755.52e6 + 503.90e6, "src": "43985879dda58388"},
+}
+
+
+def _kernel_source_hash():
+    import hashlib
+    with open(os.path.join(ROOT, "attention_gemms_gb300", "csrc", "gemm_tc.cu"), "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+def col_gemm_traffic(workload):
+    t = COL_GEMM_TRAFFIC.get(workload)
+    if not t or t["src"] != _kernel_source_hash():
+        return None
+    return t["bytes"]
 
 
 def load_peaks():
@@ -287,14 +312,7 @@ def run_ours(args, w):
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     peak_s = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     col_tf = col_gemm_flops(w) / (col_max * 1e-3) / 1e12
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", f"traffic_{args.workload}.json")
-    if os.path.exists(prof):
-        try:
-            with open(prof) as fh:
-                traffic = json.load(fh).get("col_gemm_bytes_per_launch")
-        except Exception:
-            traffic = None
+    traffic = col_gemm_traffic(args.workload)
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws_,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
