@@ -492,9 +492,11 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
   if (d.groups > 1 && d.K % BK != 0)
     return fail(TP_ERR_SHAPE, "per-shard K must be a multiple of 64");
   const int epi = d.epi;
-  // tile width in TMEM columns: 256 unless the problem is narrow
+  // tile width in TMEM columns: 256 unless the problem is narrow, or has so few rows
+  // (decode: M <= 64 tokens, one M-tile) that 128-wide tiles are needed to give
+  // every SM its share of the weight stream
   const int64_t n_tmem = d.paired ? 2 * d.N : d.N;
-  const int BN = n_tmem >= 256 ? 256 : 128;
+  const int BN = (n_tmem >= 256 && d.M > 64) ? 256 : 128;
   const int bn_logical = d.paired ? BN / 2 : BN;
 
   TcParams prm;

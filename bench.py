@@ -44,6 +44,10 @@ WORKLOADS = {
                   b=1, s=2048, h=8192, f=28672, N=4, act="swiglu", cfg=5),
 }
 
+DECODE = dict(desc="decode GEMV sweep: SwiGLU MLP forward, h=8192 ffn=28672 N=8 "
+                   "(W_gate/W_up column-split, W_down row-split), shard sum via fp32 partials",
+              h=8192, f=28672, N=8, tokens=(1, 8, 32, 64), cfg=4)
+
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -337,10 +341,104 @@ def run_ours(args, w):
         "clocks": clk,
         "input_gen_s": round(t_gen, 1),
     }
+    if args.decode:
+        out["decode"] = run_decode(args, device, T)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, hostin, budget_s=args.cpu_budget)
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------------ decode sweep
+
+def decode_bytes(T, h, f, N):
+    """Algorithmic HBM bytes of one decode forward: the three weight matrices once,
+    x in, A = SiLU(x Wg) * (x Wu) out and back in, the fp32 shard partials out and
+    back in, Z out."""
+    weights = 3 * h * f * 2
+    acts = T * h * 2 + 2 * T * f * 2 + T * h * 2
+    partials = 2 * N * T * h * 4
+    return weights + acts + partials, 3 * h * f * 2, 2 * h * f * 2 + T * h * 2 + T * f * 2
+
+
+def run_decode(args, device, T):
+    import torch
+    from attention_gemms_gb300 import synth
+    w = DECODE
+    h, f, N, c = w["h"], w["f"], w["N"], w["cfg"]
+    BF = T.DType.BF16
+    mode = T.Reduce.BUFFERS
+
+    def dev(shape, name, sigma, extra=0):
+        a = synth.normal(shape, synth.seed_of(c, name) + extra, sigma, "bf16")
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+
+    Wg, Wu, Wd = dev((h, f), "Wg", 0.02), dev((h, f), "Wu", 0.02), dev((f, h), "Wd", 0.02)
+    peaks, src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    res = {"workload": w["desc"], "unit": "GB/s", "peak": hbm,
+           "peak_source": f"{src} HBM copy bandwidth", "cuda_graph": True, "per_tokens": {}}
+    stream = torch.cuda.current_stream()
+    for nt in w["tokens"]:
+        X = dev((nt, h), "X", 1.0, nt)
+        A = torch.empty((nt, f), dtype=torch.bfloat16, device=device)
+        Z = torch.empty((nt, h), dtype=torch.bfloat16, device=device)
+        wsb = T.tp_workspace_size(T.Op.ROW_LINEAR, nt, f, h, N, BF, T.Act.NONE, mode)
+        ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=device)
+        def fwd():
+            T.tp_col_linear(X, Wg, Wu, None, None, A, nt, h, f, N, BF, T.Act.SWIGLU)
+            T.tp_row_linear(A, Wd, None, Z, nt, f, h, N, BF, mode, ws, ws.numel())
+
+        for _ in range(args.warmup):
+            fwd()
+        torch.cuda.synchronize()
+        # one step's launches in a CUDA graph (the tensor maps are kernel parameters)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fwd()
+        # warm up for at least 200 ms of replays: clocks (SM and HBM) drop while the
+        # GPU idles, e.g. during the CPU baseline, and take a moment to come back
+        t_w = time.time()
+        n_w = 0
+        while n_w < args.warmup or time.time() - t_w < 0.2:
+            g.replay()
+            n_w += 1
+            if n_w % 50 == 0:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(args.steps):
+            g.replay()
+        t1.record()
+        torch.cuda.synchronize()
+        ms = t0.elapsed_time(t1) / args.steps
+        # the gate/up GEMM alone, launched eagerly between events (weights > L2)
+        col_ms = []
+        for _ in range(args.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            T.tp_col_linear(X, Wg, Wu, None, None, A, nt, h, f, N, BF, T.Act.SWIGLU)
+            e1.record()
+            torch.cuda.synchronize()
+            col_ms.append(e0.elapsed_time(e1))
+        col = float(np.median(col_ms))
+        total, wbytes, col_bytes = decode_bytes(nt, h, f, N)
+        if T.tp_check_status(stream) != 0:
+            raise RuntimeError("device wait timeout in decode: " + T.tp_last_error())
+        gbs = total / (ms * 1e-3) / 1e9
+        res["per_tokens"][str(nt)] = {
+            "ms_per_step": round(ms, 4), "GBps": round(gbs, 1),
+            "pct_of_peak": round(100 * gbs / hbm, 1),
+            "weight_GBps": round(wbytes / (ms * 1e-3) / 1e9, 1),
+            "TFLOPs": round(2 * nt * 3 * h * f / (ms * 1e-3) / 1e12, 2),
+            "roofline": {"bound": "hbm", "kernel": "gemm_tc_kernel (gate/up + SwiGLU)",
+                         "achieved": round(col_bytes / (col * 1e-3) / 1e9, 1), "peak": hbm,
+                         "unit": "GB/s", "frac": round(col_bytes / (col * 1e-3) / 1e9 / hbm, 4),
+                         "avg_launch_ms": round(col, 4), "algorithmic_bytes": col_bytes},
+        }
+        del g
+    return res
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -436,6 +534,9 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode", dest="decode", action="store_true", default=True,
+                    help="also run the decode GEMV sweep (default)")
+    ap.add_argument("--no-decode", dest="decode", action="store_false")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -81,3 +81,31 @@ def test_full_size_parity(workload, mode):
         errs[k] = rel(host(got), ref)
     for k, v in errs.items():
         assert v <= BF16_TOL, (workload, mode, k, v)
+
+
+@pytest.mark.parametrize("T_", [1, 8, 32, 64])
+def test_decode_full_size_parity(T_):
+    """The decode sweep's shapes (h=8192, ffn=28672, N=8, SwiGLU) in bench.py's launch
+    configuration (tp_col_linear -> tp_row_linear with fp32 shard partials); the
+    oracle computes every output."""
+    T.lib()
+    w = bench.DECODE
+    h, f, N, c = w["h"], w["f"], w["N"], w["cfg"]
+    BF = T.DType.BF16
+    dev = torch.device("cuda", 0)
+    arrs = {k: synth.normal(s, synth.seed_of(c, n) + ex, sg, "bf16")
+            for k, s, n, sg, ex in [("X", (T_, h), "X", 1.0, T_), ("Wg", (h, f), "Wg", 0.02, 0),
+                                    ("Wu", (h, f), "Wu", 0.02, 0), ("Wd", (f, h), "Wd", 0.02, 0)]}
+    d = {k: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev) for k, a in arrs.items()}
+    A = torch.empty((T_, f), dtype=torch.bfloat16, device=dev)
+    Z = torch.empty((T_, h), dtype=torch.bfloat16, device=dev)
+    wsb = T.tp_workspace_size(T.Op.ROW_LINEAR, T_, f, h, N, BF, T.Act.NONE, T.Reduce.BUFFERS)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    T.tp_col_linear(d["X"], d["Wg"], d["Wu"], None, None, A, T_, h, f, N, BF, T.Act.SWIGLU)
+    T.tp_row_linear(A, d["Wd"], None, Z, T_, f, h, N, BF, T.Reduce.BUFFERS, ws, wsb)
+    torch.cuda.synchronize()
+    assert T.tp_check_status() == 0
+    f64 = {k: synth.to_f64(a, "bf16") for k, a in arrs.items()}
+    ref = O.mlp_swiglu_fwd(f64["X"], f64["Wg"], f64["Wu"], f64["Wd"], N)
+    assert rel(host(A), ref["A"]) <= BF16_TOL
+    assert rel(host(Z), ref["Z"]) <= BF16_TOL

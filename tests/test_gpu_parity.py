@@ -203,3 +203,27 @@ def test_wait_timeout_reports_and_recovers():
     T.tp_col_linear(X, W, None, None, None, out, M, h, f, N, BF, T.Act.NONE)
     assert T.tp_check_status() == 0
     assert rel(host(out), Xo @ Wo) <= BF16_TOL
+
+
+# ---------------------------------------------------------------- decode-sized forward
+
+@pytest.mark.parametrize("T_", [1, 8, 32, 64])
+@pytest.mark.parametrize("act", [T.Act.GELU, T.Act.SWIGLU])
+@pytest.mark.parametrize("mode", [T.Reduce.BUFFERS, T.Reduce.SPLITK])
+def test_decode_forward(T_, act, mode):
+    M, h, f, N = T_, 256, 1024, 4
+    sw = act == T.Act.SWIGLU
+    Xo, X = tensor((M, h), 801)
+    W1o, W1 = tensor((h, f), 802, 0.05)
+    Wuo, Wu = tensor((h, f), 803, 0.05)
+    W2o, W2 = tensor((f, h), 804, 0.05)
+    H = empty((M, f), bf16)
+    Z, full = guarded((M, h), bf16)
+    ws = _ws(T.tp_workspace_size(T.Op.MLP_FWD, M, h, f, N, BF, act, mode))
+    T.tp_mlp_fwd(X, W1, Wu if sw else None, W2, None, None, None, H, Z, M, h, f, N, BF, act, mode,
+                 ws, ws.numel())
+    torch.cuda.synchronize()
+    ref = O.mlp_swiglu_fwd(Xo, W1o, Wuo, W2o, N) if sw else O.mlp_gelu_fwd(Xo, W1o, W2o, N)
+    assert rel(host(H), ref["A"] if sw else ref["H"]) <= BF16_TOL
+    assert rel(host(Z), ref["Z"]) <= BF16_TOL
+    assert guard_intact(full, M)
