@@ -14,8 +14,8 @@ tp_status check_device();
 void set_debug_hang(int v);
 
 namespace {
-
 bool al16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
+}  // namespace
 
 tp_status need(bool cond, tp_status s, const char* msg) { return cond ? TP_OK : fail(s, msg); }
 
@@ -137,7 +137,6 @@ tp_status dx_impl(const void* const* dA, const void* const* Wt, int nseg, void* 
   return launch_shard_reduce(static_cast<const float*>(ws), nullptr, dX, N, M, h, dt, st);
 }
 
-}  // namespace
 }  // namespace tp
 
 using namespace tp;
@@ -148,7 +147,9 @@ void tp_debug_inject_wait_fault(int enable) { set_debug_hang(enable); }
 
 size_t tp_workspace_size(tp_op op, int64_t M, int64_t h, int64_t f, int32_t N, tp_dtype dtype,
                          tp_act act, tp_reduce mode) {
-  if (N < 1 || M < 0 || h < 1 || f < 1) return 0;
+  if (N < 1 || M < 0 || h < 1 || (f < 1 && op != TP_OP_ATTN_PROJ_FWD && op != TP_OP_ATTN_PROJ_BWD &&
+                                   op != TP_OP_LAYERNORM_BWD))
+    return 0;
   if (dtype != TP_BF16 && dtype != TP_F32) return 0;
   const size_t elt = elem_size(dtype);
   switch (op) {
@@ -159,6 +160,11 @@ size_t tp_workspace_size(tp_op op, int64_t M, int64_t h, int64_t f, int32_t N, t
     case TP_OP_MLP_BWD:
       return (act == TP_ACT_SWIGLU ? 2 : 1) * align_up(static_cast<size_t>(M) * f * elt, 256) +
              partial_bytes(M, h, N, mode);
+    case TP_OP_ATTN_PROJ_FWD: return attn_workspace_size(true, M, h, N, dtype, mode);
+    case TP_OP_ATTN_PROJ_BWD: return attn_workspace_size(false, M, h, N, dtype, mode);
+    case TP_OP_LAYERNORM_BWD: return layernorm_bwd_ws_bytes(M, h);
+    case TP_OP_LAYER_FWD: return layer_workspace_size(true, M, h, f, N, dtype, mode);
+    case TP_OP_LAYER_BWD: return layer_workspace_size(false, M, h, f, N, dtype, mode);
     default: return 0;
   }
 }

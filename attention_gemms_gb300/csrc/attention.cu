@@ -1,0 +1,305 @@
+// Per-head softmax attention of the head-sharded attention block, forward and
+// backward. Heads are independent [张量并行 notes, §Multi-Head Attention 的并行化], so
+// shard i's heads (a contiguous range of grid.y) never exchange data with other
+// shards. Layout: qkv (M, 3h) with M = b*s rows, W_qkv = [W_q | W_k | W_v] so head t
+// of Q, K, V sits at columns t*d, h + t*d, 2h + t*d; o (M, h), head t at t*d;
+// lse (b, heads, s) the log-sum-exp of each score row.
+//   forward:  O = softmax(Q K^T / sqrt(d)) V        [Megatron-LM 实战 04, TPAttention]
+//   backward: P = exp(S - lse), Dr = rowsum(dO * O), dV = P^T dO, dP = dO V^T,
+//             dS = P * (dP - Dr), dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d)
+// At the page-2 layer's sizes (s = 128, d = 16) this is a few MFLOP per head, so
+// the kernels use CUDA cores: one thread per query row (forward, dQ) or key row
+// (dK, dV), 64 rows per CTA, the other operand streamed through shared memory in
+// blocks of 64 rows; softmax statistics in fp32.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "internal.h"
+
+namespace tp {
+namespace {
+
+constexpr int RB = 64;  // rows per CTA and per shared-memory block
+
+__device__ __forceinline__ float ld(const float* p, int64_t i) { return p[i]; }
+__device__ __forceinline__ float ld(const __nv_bfloat16* p, int64_t i) {
+  return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void st(float* p, int64_t i, float v) { p[i] = v; }
+__device__ __forceinline__ void st(__nv_bfloat16* p, int64_t i, float v) {
+  p[i] = __float2bfloat16_rn(v);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(RB) attn_fwd_kernel(const T* __restrict__ qkv, T* __restrict__ o,
+                                                      float* __restrict__ lse, int s, int h,
+                                                      int heads, float scale, int causal) {
+  __shared__ float Ks[RB][D + 1], Vs[RB][D + 1];
+  const int b = blockIdx.z, t = blockIdx.y;
+  const int qi = blockIdx.x * RB + threadIdx.x;
+  const int64_t ldq = 3ll * h;
+  const T* base = qkv + static_cast<int64_t>(b) * s * ldq;
+  const bool valid = qi < s;
+  float q[D], acc[D];
+#pragma unroll
+  for (int d = 0; d < D; ++d) {
+    q[d] = valid ? ld(base + qi * ldq, t * D + d) * scale : 0.0f;
+    acc[d] = 0.0f;
+  }
+  float m = -INFINITY, l = 0.0f;
+  const int kend = causal ? min(s, static_cast<int>(blockIdx.x + 1) * RB) : s;
+  for (int k0 = 0; k0 < kend; k0 += RB) {
+    __syncthreads();
+    const int kj = k0 + threadIdx.x;
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      Ks[threadIdx.x][d] = kj < s ? ld(base + kj * ldq, h + t * D + d) : 0.0f;
+      Vs[threadIdx.x][d] = kj < s ? ld(base + kj * ldq, 2 * h + t * D + d) : 0.0f;
+    }
+    __syncthreads();
+    if (!valid) continue;
+    for (int j0 = 0; j0 < RB; j0 += 32) {
+      float sc[32];
+      float mb = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int key = k0 + j0 + j;
+        float v = -INFINITY;
+        if (key < s && (!causal || key <= qi)) {
+          v = 0.0f;
+#pragma unroll
+          for (int d = 0; d < D; ++d) v = fmaf(q[d], Ks[j0 + j][d], v);
+        }
+        sc[j] = v;
+        mb = fmaxf(mb, v);
+      }
+      const float mn = fmaxf(m, mb);
+      if (mn == -INFINITY) continue;  // every key so far masked
+      const float corr = expf(m - mn);
+      l *= corr;
+#pragma unroll
+      for (int d = 0; d < D; ++d) acc[d] *= corr;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float p = expf(sc[j] - mn);
+        l += p;
+#pragma unroll
+        for (int d = 0; d < D; ++d) acc[d] = fmaf(p, Vs[j0 + j][d], acc[d]);
+      }
+      m = mn;
+    }
+  }
+  if (!valid) return;
+  const float inv = 1.0f / l;
+  T* orow = o + (static_cast<int64_t>(b) * s + qi) * h + t * D;
+#pragma unroll
+  for (int d = 0; d < D; ++d) st(orow, d, acc[d] * inv);
+  lse[(static_cast<int64_t>(b) * heads + t) * s + qi] = m + logf(l);
+}
+
+// dK, dV: one thread per key row; query rows streamed through shared memory
+template <typename T, int D>
+__global__ void __launch_bounds__(RB) attn_bwd_dkdv_kernel(
+    const T* __restrict__ qkv, const T* __restrict__ o, const float* __restrict__ lse,
+    const T* __restrict__ dO, T* __restrict__ dqkv, int s, int h, int heads, float scale,
+    int causal) {
+  __shared__ float Qs[RB][D + 1], dOs[RB][D + 1], Ls[RB], Ds[RB];
+  const int b = blockIdx.z, t = blockIdx.y;
+  const int kj = blockIdx.x * RB + threadIdx.x;
+  const int64_t ldq = 3ll * h;
+  const T* base = qkv + static_cast<int64_t>(b) * s * ldq;
+  const T* obase = o + static_cast<int64_t>(b) * s * h;
+  const T* dobase = dO + static_cast<int64_t>(b) * s * h;
+  const float* lrow = lse + (static_cast<int64_t>(b) * heads + t) * s;
+  const bool valid = kj < s;
+  float k[D], v[D], dk[D], dv[D];
+#pragma unroll
+  for (int d = 0; d < D; ++d) {
+    k[d] = valid ? ld(base + kj * ldq, h + t * D + d) : 0.0f;
+    v[d] = valid ? ld(base + kj * ldq, 2 * h + t * D + d) : 0.0f;
+    dk[d] = 0.0f;
+    dv[d] = 0.0f;
+  }
+  const int qstart = causal ? static_cast<int>(blockIdx.x) * RB : 0;
+  for (int q0 = qstart; q0 < s; q0 += RB) {
+    __syncthreads();
+    const int qi = q0 + threadIdx.x;
+    float dsum = 0.0f;
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      const float qv = qi < s ? ld(base + qi * ldq, t * D + d) : 0.0f;
+      const float dov = qi < s ? ld(dobase + qi * h, t * D + d) : 0.0f;
+      const float ov = qi < s ? ld(obase + qi * h, t * D + d) : 0.0f;
+      Qs[threadIdx.x][d] = qv;
+      dOs[threadIdx.x][d] = dov;
+      dsum = fmaf(dov, ov, dsum);
+    }
+    Ls[threadIdx.x] = qi < s ? lrow[qi] : 0.0f;
+    Ds[threadIdx.x] = dsum;
+    __syncthreads();
+    if (!valid) continue;
+    const int iend = min(RB, s - q0);
+    for (int i = 0; i < iend; ++i) {
+      if (causal && kj > q0 + i) continue;
+      float sc = 0.0f, dp = 0.0f;
+#pragma unroll
+      for (int d = 0; d < D; ++d) {
+        sc = fmaf(Qs[i][d], k[d], sc);
+        dp = fmaf(dOs[i][d], v[d], dp);
+      }
+      const float p = expf(sc * scale - Ls[i]);
+      const float ds = p * (dp - Ds[i]) * scale;
+#pragma unroll
+      for (int d = 0; d < D; ++d) {
+        dv[d] = fmaf(p, dOs[i][d], dv[d]);
+        dk[d] = fmaf(ds, Qs[i][d], dk[d]);
+      }
+    }
+  }
+  if (!valid) return;
+  T* row = dqkv + (static_cast<int64_t>(b) * s + kj) * ldq;
+#pragma unroll
+  for (int d = 0; d < D; ++d) {
+    st(row, h + t * D + d, dk[d]);
+    st(row, 2 * h + t * D + d, dv[d]);
+  }
+}
+
+// dQ: one thread per query row; key rows streamed through shared memory
+template <typename T, int D>
+__global__ void __launch_bounds__(RB) attn_bwd_dq_kernel(
+    const T* __restrict__ qkv, const T* __restrict__ o, const float* __restrict__ lse,
+    const T* __restrict__ dO, T* __restrict__ dqkv, int s, int h, int heads, float scale,
+    int causal) {
+  __shared__ float Ks[RB][D + 1], Vs[RB][D + 1];
+  const int b = blockIdx.z, t = blockIdx.y;
+  const int qi = blockIdx.x * RB + threadIdx.x;
+  const int64_t ldq = 3ll * h;
+  const T* base = qkv + static_cast<int64_t>(b) * s * ldq;
+  const bool valid = qi < s;
+  float q[D], dov[D], dq[D];
+  float dsum = 0.0f, L = 0.0f;
+  if (valid) {
+    const T* orow = o + (static_cast<int64_t>(b) * s + qi) * h + t * D;
+    const T* dorow = dO + (static_cast<int64_t>(b) * s + qi) * h + t * D;
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      q[d] = ld(base + qi * ldq, t * D + d);
+      dov[d] = ld(dorow, d);
+      dsum = fmaf(dov[d], ld(orow, d), dsum);
+      dq[d] = 0.0f;
+    }
+    L = lse[(static_cast<int64_t>(b) * heads + t) * s + qi];
+  } else {
+#pragma unroll
+    for (int d = 0; d < D; ++d) q[d] = dov[d] = dq[d] = 0.0f;
+  }
+  const int kend = causal ? min(s, static_cast<int>(blockIdx.x + 1) * RB) : s;
+  for (int k0 = 0; k0 < kend; k0 += RB) {
+    __syncthreads();
+    const int kj = k0 + threadIdx.x;
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      Ks[threadIdx.x][d] = kj < s ? ld(base + kj * ldq, h + t * D + d) : 0.0f;
+      Vs[threadIdx.x][d] = kj < s ? ld(base + kj * ldq, 2 * h + t * D + d) : 0.0f;
+    }
+    __syncthreads();
+    if (!valid) continue;
+    const int jend = min(RB, s - k0);
+    for (int j = 0; j < jend; ++j) {
+      if (causal && k0 + j > qi) break;
+      float sc = 0.0f, dp = 0.0f;
+#pragma unroll
+      for (int d = 0; d < D; ++d) {
+        sc = fmaf(q[d], Ks[j][d], sc);
+        dp = fmaf(dov[d], Vs[j][d], dp);
+      }
+      const float p = expf(sc * scale - L);
+      const float ds = p * (dp - dsum) * scale;
+#pragma unroll
+      for (int d = 0; d < D; ++d) dq[d] = fmaf(ds, Ks[j][d], dq[d]);
+    }
+  }
+  if (!valid) return;
+  T* row = dqkv + (static_cast<int64_t>(b) * s + qi) * ldq;
+#pragma unroll
+  for (int d = 0; d < D; ++d) st(row, t * D + d, dq[d]);
+}
+
+template <typename T, int D>
+tp_status run_fwd(const void* qkv, void* o, float* lse, int b, int s, int h, int heads,
+                  int causal, cudaStream_t st) {
+  const dim3 grid((s + RB - 1) / RB, heads, b);
+  attn_fwd_kernel<T, D><<<grid, RB, 0, st>>>(static_cast<const T*>(qkv), static_cast<T*>(o), lse,
+                                              s, h, heads, 1.0f / sqrtf(static_cast<float>(D)),
+                                              causal);
+  count_launch();
+  TP_CUDA_TRY(cudaGetLastError());
+  return TP_OK;
+}
+
+template <typename T, int D>
+tp_status run_bwd(const void* qkv, const void* o, const float* lse, const void* dO, void* dqkv,
+                  int b, int s, int h, int heads, int causal, cudaStream_t st) {
+  const dim3 grid((s + RB - 1) / RB, heads, b);
+  const float scale = 1.0f / sqrtf(static_cast<float>(D));
+  attn_bwd_dkdv_kernel<T, D><<<grid, RB, 0, st>>>(
+      static_cast<const T*>(qkv), static_cast<const T*>(o), lse, static_cast<const T*>(dO),
+      static_cast<T*>(dqkv), s, h, heads, scale, causal);
+  attn_bwd_dq_kernel<T, D><<<grid, RB, 0, st>>>(
+      static_cast<const T*>(qkv), static_cast<const T*>(o), lse, static_cast<const T*>(dO),
+      static_cast<T*>(dqkv), s, h, heads, scale, causal);
+  count_launch(2);
+  TP_CUDA_TRY(cudaGetLastError());
+  return TP_OK;
+}
+
+template <typename T>
+tp_status fwd_d(const void* qkv, void* o, float* lse, int b, int s, int h, int heads, int causal,
+                cudaStream_t st) {
+  switch (h / heads) {
+    case 16: return run_fwd<T, 16>(qkv, o, lse, b, s, h, heads, causal, st);
+    case 32: return run_fwd<T, 32>(qkv, o, lse, b, s, h, heads, causal, st);
+    case 64: return run_fwd<T, 64>(qkv, o, lse, b, s, h, heads, causal, st);
+  }
+  return fail(TP_ERR_SHAPE, "head_dim must be 16, 32 or 64");
+}
+
+template <typename T>
+tp_status bwd_d(const void* qkv, const void* o, const float* lse, const void* dO, void* dqkv,
+                int b, int s, int h, int heads, int causal, cudaStream_t st) {
+  switch (h / heads) {
+    case 16: return run_bwd<T, 16>(qkv, o, lse, dO, dqkv, b, s, h, heads, causal, st);
+    case 32: return run_bwd<T, 32>(qkv, o, lse, dO, dqkv, b, s, h, heads, causal, st);
+    case 64: return run_bwd<T, 64>(qkv, o, lse, dO, dqkv, b, s, h, heads, causal, st);
+  }
+  return fail(TP_ERR_SHAPE, "head_dim must be 16, 32 or 64");
+}
+
+}  // namespace
+
+tp_status launch_attention_fwd(const void* qkv, void* o, float* lse, int64_t b, int64_t s,
+                               int64_t h, int heads, int causal, tp_dtype dt, cudaStream_t st) {
+  if (b <= 0 || s <= 0) return TP_OK;
+  if (b > 65535 || heads > 65535 || s > (1 << 24) || h > (1 << 20))
+    return fail(TP_ERR_SHAPE, "attention sizes out of range");
+  const int bi = static_cast<int>(b), si = static_cast<int>(s), hi = static_cast<int>(h);
+  return dt == TP_BF16 ? fwd_d<__nv_bfloat16>(qkv, o, lse, bi, si, hi, heads, causal, st)
+                       : fwd_d<float>(qkv, o, lse, bi, si, hi, heads, causal, st);
+}
+
+tp_status launch_attention_bwd(const void* qkv, const void* o, const float* lse, const void* dO,
+                               void* dqkv, int64_t b, int64_t s, int64_t h, int heads, int causal,
+                               tp_dtype dt, cudaStream_t st) {
+  if (b <= 0 || s <= 0) return TP_OK;
+  if (b > 65535 || heads > 65535 || s > (1 << 24) || h > (1 << 20))
+    return fail(TP_ERR_SHAPE, "attention sizes out of range");
+  const int bi = static_cast<int>(b), si = static_cast<int>(s), hi = static_cast<int>(h);
+  return dt == TP_BF16
+             ? bwd_d<__nv_bfloat16>(qkv, o, lse, dO, dqkv, bi, si, hi, heads, causal, st)
+             : bwd_d<float>(qkv, o, lse, dO, dqkv, bi, si, hi, heads, causal, st);
+}
+
+}  // namespace tp

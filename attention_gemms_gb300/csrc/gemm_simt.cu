@@ -14,9 +14,9 @@ namespace {
 constexpr int TM = 64, TN = 64, TK = 16;
 
 struct SimtParams {
-  const float* A[2];
-  const float* B[2];
-  int64_t lda[2], ldb[2];
+  const float* A[3];
+  const float* B[3];
+  int64_t lda[3], ldb[3], k0[3];
   int64_t M, N, K;
   int a_mn, b_mn, nseg, paired;
   float* out0;
@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const SimtParams p) {
         // consecutive threads walk the contiguous storage dimension
         const int mm = p.a_mn ? e % TM : e / TK;
         const int kk = p.a_mn ? e / TM : e % TK;
-        const int64_t gm = m0 + mm, lk = k0 + kk, gk = g * p.K + lk;
+        const int64_t gm = m0 + mm, lk = k0 + kk, gk = p.k0[s] + g * p.K + lk;
         float v = 0.0f;
         if (gm < p.M && lk < p.K) v = p.a_mn ? A[gk * lda + gm] : A[gm * lda + gk];
         As[kk][mm] = v;
@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const SimtParams p) {
         for (int e = threadIdx.x; e < TN * TK; e += 256) {
           const int nn = p.b_mn ? e % TN : e / TK;
           const int kk = p.b_mn ? e / TN : e % TK;
-          const int64_t gn = n0 + nn, lk = k0 + kk, gk = g * p.K + lk;
+          const int64_t gn = n0 + nn, lk = k0 + kk, gk = p.k0[s] + g * p.K + lk;
           float v = 0.0f;
           if (gn < p.N && lk < p.K) v = p.b_mn ? B[gk * ldb + gn] : B[gn * ldb + gk];
           Bs[h][kk][nn] = v;
@@ -126,9 +126,11 @@ void launch_k(const SimtParams& p, dim3 grid, cudaStream_t st) {
 tp_status launch_gemm_simt(const GemmDesc& d, cudaStream_t st) {
   if (d.M <= 0 || d.N <= 0 || d.K <= 0) return TP_OK;
   SimtParams p{};
-  for (int s = 0; s < 2; ++s) {
+  if (d.nseg < 1 || d.nseg > 3) return fail(TP_ERR_INVALID_ARG, "1 to 3 K segments");
+  for (int s = 0; s < 3; ++s) {
     const int sa = s < d.nseg ? s : 0;
     const int sb = s < (d.paired ? 2 : d.nseg) ? s : 0;
+    p.k0[s] = d.seg_k0[s];
     p.A[s] = static_cast<const float*>(d.A[sa].ptr);
     p.lda[s] = d.A[sa].ld;
     p.B[s] = static_cast<const float*>(d.B[sb].ptr);

@@ -48,10 +48,11 @@ struct TcCfg {
 };
 
 struct TcParams {  // CUtensorMap members carry their own 128-byte alignment
-  CUtensorMap tmA[2];
-  CUtensorMap tmB[2];
+  CUtensorMap tmA[3];
+  CUtensorMap tmB[3];
   int64_t M, N, K;  // N counts logical output columns
   int a_mn, b_mn, nseg, paired, groups;
+  int seg_k0[3];
   int tiles_m, tiles_n, kb_per_seg;
   int shards, shard_axis;
   void* out0;
@@ -221,8 +222,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.tmA[0]);
     tma_prefetch_desc(&p.tmB[0]);
-    if (p.nseg > 1) tma_prefetch_desc(&p.tmA[1]);
-    if (p.nseg > 1 || p.paired) tma_prefetch_desc(&p.tmB[1]);
+    for (int s = 1; s < p.nseg; ++s) {
+      tma_prefetch_desc(&p.tmA[s]);
+      tma_prefetch_desc(&p.tmB[s]);
+    }
+    if (p.paired) tma_prefetch_desc(&p.tmB[1]);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -255,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             break;
           }
           const int seg = kb / p.kb_per_seg;
-          const int k0 = static_cast<int>(tc.g * p.K) + (kb - seg * p.kb_per_seg) * BK;
+          const int k0 = p.seg_k0[seg] + static_cast<int>(tc.g * p.K) + (kb - seg * p.kb_per_seg) * BK;
           const uint32_t a_dst = sbase + stage * C::STAGE_BYTES;
           const uint32_t b_dst = a_dst + C::A_BYTES;
           mbar_arrive_expect_tx(full_bar(stage), stage_tx);
@@ -491,6 +495,10 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
   if (d.N % 8 != 0) return fail(TP_ERR_SHAPE, "GEMM output width must be a multiple of 8");
   if (d.groups > 1 && d.K % BK != 0)
     return fail(TP_ERR_SHAPE, "per-shard K must be a multiple of 64");
+  if (d.nseg < 1 || d.nseg > 3) return fail(TP_ERR_INVALID_ARG, "1 to 3 K segments");
+  for (int s = 0; s < d.nseg; ++s)
+    if (d.seg_k0[s] % BK != 0 || d.seg_k0[s] > (1ll << 30))
+      return fail(TP_ERR_SHAPE, "K segment offsets must be multiples of 64");
   const int epi = d.epi;
   // tile width in TMEM columns: 256 unless the problem is narrow, or has so few rows
   // (decode: M <= 64 tokens, one M-tile) that 128-wide tiles are needed to give
@@ -510,8 +518,9 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
     if (d.b_mn) TP_TRY(make_map(&prm.tmB[s], d.B[s], 64, 64));
     else TP_TRY(make_map(&prm.tmB[s], d.B[s], 64, static_cast<uint32_t>(BN)));
   }
-  if (d.nseg == 1) prm.tmA[1] = prm.tmA[0];
-  if (nb == 1) prm.tmB[1] = prm.tmB[0];
+  for (int s = d.nseg; s < 3; ++s) prm.tmA[s] = prm.tmA[0];
+  for (int s = nb; s < 3; ++s) prm.tmB[s] = prm.tmB[0];
+  for (int s = 0; s < 3; ++s) prm.seg_k0[s] = static_cast<int>(d.seg_k0[s]);
   prm.M = d.M;
   prm.N = d.N;
   prm.K = d.K;

@@ -6,6 +6,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <initializer_list>
 #include <string>
 
 #include "../../include/tpmlp.h"
@@ -56,18 +57,20 @@ struct Operand {
   int64_t ld = 0;              // row pitch, elements
 };
 
-// D (M x N) = sum_{s < nseg} sum_k A_s(m, k) B_s(k, n), per K-group g:
+// D (M x N) = sum_{s < nseg} sum_k A_s(m, k0_s + k) B_s(k0_s + k, n), per K-group g:
 //   A(m, k) is A.ptr[m * ld + k] (K-major) or A.ptr[k * ld + m] (a_mn: MN-major),
 //   B(k, n) is B.ptr[n * ld + k] (K-major) or B.ptr[k * ld + n] (b_mn: MN-major);
-//   group g reads k in [g*K, (g+1)*K) and writes its output g*out_group_stride
-//   elements further (the per-shard partial buffers of the shard sum).
+//   segment s starts at K offset seg_k0[s]; group g reads k in [g*K, (g+1)*K) of
+//   every segment and writes its output g*out_group_stride elements further (the
+//   per-shard partial buffers of the shard sum).
 // paired: B[0] feeds the first half of every tile's columns and B[1] the second;
 //   logical column n of the output takes B[0](., n) and B[1](., n) (gate/up).
 struct GemmDesc {
   int64_t M = 0, N = 0, K = 0;
   bool a_mn = false, b_mn = false;
-  int nseg = 1;
-  Operand A[2], B[2];
+  int nseg = 1;  // <= 3
+  Operand A[3], B[3];
+  int64_t seg_k0[3] = {0, 0, 0};
   bool paired = false;
   int groups = 1;
   int shards = 1;      // tile order: `shards` equal slabs along shard_axis, slab-major
@@ -90,6 +93,36 @@ inline tp_status launch_gemm(const GemmDesc& d, cudaStream_t st) {
   return d.dtype == TP_BF16 ? launch_gemm_tc(d, st) : launch_gemm_simt(d, st);
 }
 
+// ------------------------------------------------------------------ other kernels
+
+tp_status launch_layernorm_fwd(const void* x, const float* gamma, const float* beta, void* y,
+                               float* mean, float* rstd, int64_t M, int64_t h, float eps,
+                               tp_dtype dt, cudaStream_t st);
+tp_status launch_layernorm_bwd(const void* x, const float* gamma, const float* mean,
+                               const float* rstd, const void* dy, const void* dres, void* dx,
+                               float* dgamma, float* dbeta, int64_t M, int64_t h, void* ws,
+                               tp_dtype dt, cudaStream_t st);
+size_t layernorm_bwd_ws_bytes(int64_t M, int64_t h);
+size_t attn_workspace_size(bool fwd, int64_t M, int64_t h, int32_t N, tp_dtype dt,
+                           tp_reduce mode);
+size_t layer_workspace_size(bool fwd, int64_t M, int64_t h, int64_t f, int32_t N, tp_dtype dt,
+                            tp_reduce mode);
+tp_status launch_attention_fwd(const void* qkv, void* o, float* lse, int64_t b, int64_t s,
+                               int64_t h, int heads, int causal, tp_dtype dt, cudaStream_t st);
+tp_status launch_attention_bwd(const void* qkv, const void* o, const float* lse, const void* dO,
+                               void* dqkv, int64_t b, int64_t s, int64_t h, int heads, int causal,
+                               tp_dtype dt, cudaStream_t st);
+
+// ------------------------------------------------------------------ API helpers (api.cu)
+
+tp_status need(bool cond, tp_status s, const char* msg);
+tp_status check_aligned(std::initializer_list<const void*> ptrs);
+tp_status check_dtype(tp_dtype dt);
+tp_status check_device();
+size_t partial_bytes(int64_t M, int64_t n, int32_t N, tp_reduce mode);
+tp_status row_impl(const void* Xs, const void* W, const void* residual, void* out, int64_t M,
+                   int64_t k, int64_t n, int32_t N, tp_dtype dt, tp_reduce mode, void* ws,
+                   cudaStream_t st);
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline size_t elem_size(tp_dtype t) { return t == TP_BF16 ? 2 : 4; }
 

@@ -51,6 +51,33 @@ class Op(enum.IntEnum):
     MLP_BWD = 3
     ATTN_PROJ_FWD = 4
     ATTN_PROJ_BWD = 5
+    LAYERNORM_BWD = 6
+    LAYER_FWD = 7
+    LAYER_BWD = 8
+
+
+class LayerWeights(ctypes.Structure):
+    """tp_layer_weights"""
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("Wqkv", "Wo", "W1", "W2", "gamma1", "beta1", "gamma2", "beta2")]
+
+
+class LayerSaved(ctypes.Structure):
+    """tp_layer_saved"""
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("xn1", "mean1", "rstd1", "qkv", "o", "lse", "x1", "xn2", "mean2", "rstd2",
+                 "y", "hh")]
+
+
+class LayerGrads(ctypes.Structure):
+    """tp_layer_grads"""
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("dWqkv", "dWo", "dW1", "dW2", "dgamma1", "dbeta1", "dgamma2", "dbeta2")]
+
+
+def make_struct(cls, **tensors):
+    """Fill one of the layer structs from tensors / addresses / None by field name."""
+    return cls(**{k: _ptr(v) for k, v in tensors.items()})
 
 
 class TpError(RuntimeError):
@@ -82,6 +109,17 @@ _SIGS = {
                          _ST, _P, _SZ, _P]),
     "tp_mlp_bwd": (_ST, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32,
                          _ST, _ST, _ST, _P, _SZ, _P]),
+    "tp_layernorm_fwd": (_ST, [_P, _P, _P, _P, _P, _P, _I64, _I64, ctypes.c_float, _ST, _P]),
+    "tp_layernorm_bwd": (_ST, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _ST, _P, _SZ, _P]),
+    "tp_attn_proj_fwd": (_ST, [_P] * 12 + [_I64, _I64, _I64, _I32, _I32, ctypes.c_int, _ST, _ST,
+                                           _P, _SZ, _P]),
+    "tp_attn_proj_bwd": (_ST, [_P] * 16 + [_I64, _I64, _I64, _I32, _I32, ctypes.c_int, _ST, _ST,
+                                           _P, _SZ, _P]),
+    "tp_layer_fwd": (_ST, [_P, ctypes.POINTER(LayerWeights), ctypes.POINTER(LayerSaved), _P, _I64,
+                           _I64, _I64, _I64, _I32, _I32, ctypes.c_int, _ST, _ST, _P, _SZ, _P]),
+    "tp_layer_bwd": (_ST, [_P, ctypes.POINTER(LayerWeights), ctypes.POINTER(LayerSaved), _P, _P,
+                           ctypes.POINTER(LayerGrads), _I64, _I64, _I64, _I64, _I32, _I32,
+                           ctypes.c_int, _ST, _ST, _P, _SZ, _P]),
     "tp_row_linear_noalloc": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _ST, _P]),
     "tp_debug_inject_wait_fault": (None, [ctypes.c_int]),
 }
@@ -215,3 +253,50 @@ def tp_mlp_bwd(X, W1, W1_up, W2, Y, Y_up, H, dZ, dX, dW1, dW1_up, dW2, M, h, f, 
 def tp_row_linear_noalloc(Xs, W, residual, out, M, k, n, N, dtype, stream=None):
     _check(lib().tp_row_linear_noalloc(_ptr(Xs), _ptr(W), _ptr(residual), _ptr(out), M, k, n, N,
                                        int(dtype), _stream(stream)))
+
+
+# ---------------------------------------------------------------- attention block and layer
+
+def tp_layernorm_fwd(x, gamma, beta, y, mean, rstd, M, h, eps, dtype, stream=None):
+    _check(lib().tp_layernorm_fwd(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), _ptr(mean),
+                                  _ptr(rstd), M, h, float(eps), int(dtype), _stream(stream)))
+
+
+def tp_layernorm_bwd(x, gamma, mean, rstd, dy, dres, dx, dgamma, dbeta, M, h, dtype, ws, ws_bytes,
+                     stream=None):
+    _check(lib().tp_layernorm_bwd(_ptr(x), _ptr(gamma), _ptr(mean), _ptr(rstd), _ptr(dy),
+                                  _ptr(dres), _ptr(dx), _ptr(dgamma), _ptr(dbeta), M, h,
+                                  int(dtype), _ptr(ws), int(ws_bytes), _stream(stream)))
+
+
+def tp_attn_proj_fwd(x, gamma, beta, Wqkv, Wo, xn, mean, rstd, qkv, o, lse, out, b, s, h, n_heads,
+                     N, causal, dtype, mode, ws, ws_bytes, stream=None):
+    _check(lib().tp_attn_proj_fwd(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(Wqkv), _ptr(Wo), _ptr(xn),
+                                  _ptr(mean), _ptr(rstd), _ptr(qkv), _ptr(o), _ptr(lse), _ptr(out),
+                                  b, s, h, n_heads, N, int(causal), int(dtype), int(mode), _ptr(ws),
+                                  int(ws_bytes), _stream(stream)))
+
+
+def tp_attn_proj_bwd(x, gamma, Wqkv, Wo, xn, mean, rstd, qkv, o, lse, dout, dx, dgamma, dbeta,
+                     dWqkv, dWo, b, s, h, n_heads, N, causal, dtype, mode, ws, ws_bytes,
+                     stream=None):
+    _check(lib().tp_attn_proj_bwd(_ptr(x), _ptr(gamma), _ptr(Wqkv), _ptr(Wo), _ptr(xn), _ptr(mean),
+                                  _ptr(rstd), _ptr(qkv), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dx),
+                                  _ptr(dgamma), _ptr(dbeta), _ptr(dWqkv), _ptr(dWo), b, s, h,
+                                  n_heads, N, int(causal), int(dtype), int(mode), _ptr(ws),
+                                  int(ws_bytes), _stream(stream)))
+
+
+def tp_layer_fwd(x, weights, saved, out, b, s, h, f, n_heads, N, causal, dtype, mode, ws, ws_bytes,
+                 stream=None):
+    _check(lib().tp_layer_fwd(_ptr(x), ctypes.byref(weights), ctypes.byref(saved), _ptr(out), b, s,
+                              h, f, n_heads, N, int(causal), int(dtype), int(mode), _ptr(ws),
+                              int(ws_bytes), _stream(stream)))
+
+
+def tp_layer_bwd(x, weights, saved, dout, dx, grads, b, s, h, f, n_heads, N, causal, dtype, mode, ws,
+                 ws_bytes, stream=None):
+    _check(lib().tp_layer_bwd(_ptr(x), ctypes.byref(weights), ctypes.byref(saved), _ptr(dout),
+                              _ptr(dx), ctypes.byref(grads), b, s, h, f, n_heads, N, int(causal),
+                              int(dtype), int(mode), _ptr(ws), int(ws_bytes), _stream(stream)))
+

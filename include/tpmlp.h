@@ -96,8 +96,51 @@ typedef enum tp_op {
   TP_OP_MLP_FWD = 2,
   TP_OP_MLP_BWD = 3,
   TP_OP_ATTN_PROJ_FWD = 4,
-  TP_OP_ATTN_PROJ_BWD = 5
+  TP_OP_ATTN_PROJ_BWD = 5,
+  TP_OP_LAYERNORM_BWD = 6,
+  TP_OP_LAYER_FWD = 7,
+  TP_OP_LAYER_BWD = 8
 } tp_op;
+
+/* Weights of the pre-LN transformer layer (tp_layer_fwd / tp_layer_bwd). */
+typedef struct tp_layer_weights {
+  const void* Wqkv;     /* (h, 3h) = [W_q | W_k | W_v], head t at columns t*d of each block */
+  const void* Wo;       /* (h, h), row block i = shard i's heads                            */
+  const void* W1;       /* (h, f), column-split                                              */
+  const void* W2;       /* (f, h), row-split                                                 */
+  const float* gamma1;  /* (h) LN1 scale and shift, fp32                                     */
+  const float* beta1;
+  const float* gamma2;  /* (h) LN2                                                           */
+  const float* beta2;
+} tp_layer_weights;
+
+/* State the layer's forward saves for its backward (all written by tp_layer_fwd). */
+typedef struct tp_layer_saved {
+  void* xn1;     /* (M, h) LN1(x)                       */
+  float* mean1;  /* (M) LN1 row mean, fp32              */
+  float* rstd1;  /* (M) LN1 row 1/sqrt(var + eps)       */
+  void* qkv;     /* (M, 3h)                             */
+  void* o;       /* (M, h) attention output, heads concatenated */
+  float* lse;    /* (b, n_heads, s) softmax log-sum-exp */
+  void* x1;      /* (M, h) x + attention block          */
+  void* xn2;     /* (M, h) LN2(x1)                      */
+  float* mean2;
+  float* rstd2;
+  void* y;       /* (M, f) MLP pre-activation           */
+  void* hh;      /* (M, f) GELU(y)                      */
+} tp_layer_saved;
+
+/* Parameter gradients written by tp_layer_bwd. */
+typedef struct tp_layer_grads {
+  void* dWqkv;  /* (h, 3h) */
+  void* dWo;    /* (h, h)  */
+  void* dW1;    /* (h, f)  */
+  void* dW2;    /* (f, h)  */
+  float* dgamma1;
+  float* dbeta1;
+  float* dgamma2;
+  float* dbeta2;
+} tp_layer_grads;
 
 /* ------------------------------------------------------------------ utilities */
 
@@ -123,8 +166,9 @@ TP_API void tp_set_wait_timeout_ns(uint64_t ns);
 TP_API uint64_t tp_launch_count(void);
 
 /* Bytes of workspace `op` needs for these sizes (0 if none). For TP_OP_ROW_LINEAR,
- * h is the reduced width k and f the output width n. For the attention ops,
- * M = b*s, h the hidden width, f = n_heads. Returns 0 on invalid arguments. */
+ * h is the reduced width k and f the output width n. For the attention and
+ * LayerNorm ops, M = b*s and h the hidden width (f is ignored). For the layer ops,
+ * f is the MLP width. Returns 0 on invalid arguments. */
 TP_API size_t tp_workspace_size(tp_op op, int64_t M, int64_t h, int64_t f, int32_t N,
                          tp_dtype dtype, tp_act act, tp_reduce mode);
 
@@ -262,6 +306,93 @@ TP_API tp_status tp_mlp_bwd(const void* X, const void* W1, const void* W1_up, co
 TP_API tp_status tp_row_linear_noalloc(const void* Xs, const void* W, const void* residual,
                                        void* out, int64_t M, int64_t k, int64_t n, int32_t N,
                                        tp_dtype dtype, void* stream);
+
+/* ------------------------------------------------------------------ attention block */
+
+/*
+ * LayerNorm over the full hidden width: y = gamma * (x - mu) / sqrt(var + eps) + beta,
+ * biased variance. [张量并行 notes, §相关分析: LN needs the complete activation, so
+ * it runs replicated after the shard sum]
+ *   x (M, h) read; gamma, beta (h) fp32 read; y (M, h) written;
+ *   mean, rstd (M) fp32 written (NULL = not kept). eps: the pages leave it open; the
+ *   layer entry points use 1e-5.
+ */
+TP_API tp_status tp_layernorm_fwd(const void* x, const float* gamma, const float* beta, void* y,
+                                  float* mean, float* rstd, int64_t M, int64_t h, float eps,
+                                  tp_dtype dtype, void* stream);
+
+/*
+ * LayerNorm backward with an optional residual gradient added:
+ *   dx = dres + rstd * (g - mean(g) - xhat * mean(g * xhat)),  g = dy * gamma
+ *   dgamma = sum_rows dy * xhat, dbeta = sum_rows dy (fp32, deterministic order; the
+ *   rows are replicated on every rank, so they need no all-reduce [张量并行 notes, §相关分析])
+ * dres may be NULL; dgamma/dbeta may be NULL (then no workspace is needed).
+ */
+TP_API tp_status tp_layernorm_bwd(const void* x, const float* gamma, const float* mean,
+                                  const float* rstd, const void* dy, const void* dres, void* dx,
+                                  float* dgamma, float* dbeta, int64_t M, int64_t h,
+                                  tp_dtype dtype, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Head-sharded attention block, forward: out = x + sum_i O_i W_o,i with
+ *   xn = LN(x; gamma, beta), QKV = xn W_qkv, O_t = softmax(Q_t K_t^T / sqrt(d)) V_t.
+ * Shard i owns heads [i*H/N, (i+1)*H/N): its columns of W_q, W_k, W_v (column-parallel)
+ * and row block i of W_o (row-parallel); no gather of heads is needed, the shard
+ * outputs are summed [张量并行 notes, §Multi-Head Attention 的并行化; Infra: Tensor
+ * Parallel, attention; 20260402-parallelism, §1 TP]. n_heads % N == 0 and N <= n_heads
+ * [Infra: Tensor Parallel, attention, the Megatron check]; head_dim = h / n_heads
+ * in {16, 32, 64}. Softmax scale 1/sqrt(d); causal != 0 masks keys after the query.
+ *   x (b*s, h) read (rows of one sequence consecutive); gamma, beta (h) fp32;
+ *   Wqkv (h, 3h) = [W_q | W_k | W_v]; Wo (h, h)
+ *   saved for the backward (written): xn (M, h), mean, rstd (M) fp32, qkv (M, 3h),
+ *   o (M, h), lse (b, n_heads, s) fp32;  out (M, h) written.
+ *   ws: TP_REDUCE_BUFFERS needs N*M*h*4 bytes.
+ * Errors: TP_ERR_INVALID_ARG, TP_ERR_SHAPE (h % heads, heads % N, head_dim, bf16: (h/N) % 64),
+ *         TP_ERR_ALIGNMENT, TP_ERR_WORKSPACE, TP_ERR_CUDA.
+ */
+TP_API tp_status tp_attn_proj_fwd(const void* x, const float* gamma, const float* beta,
+                                  const void* Wqkv, const void* Wo, void* xn, float* mean,
+                                  float* rstd, void* qkv, void* o, float* lse, void* out,
+                                  int64_t b, int64_t s, int64_t h, int32_t n_heads, int32_t N,
+                                  int causal, tp_dtype dtype, tp_reduce mode, void* ws,
+                                  size_t ws_bytes, void* stream);
+
+/*
+ * Attention block backward (dout = d out). dWo_i = O_i^T dout, dO_i = dout W_o,i^T,
+ * per head dV = P^T dO, dS = P * (dO V^T - rowsum(dO * O)), dQ = dS K/sqrt(d),
+ * dK = dS^T Q/sqrt(d); dW_qkv = xn^T dQKV; f-backward dxn = sum_i dQKV_i W_qkv,i^T;
+ * dx = dout + LN'(dxn) (the residual branch).
+ *   inputs: the forward's x, gamma, Wqkv, Wo and saved xn, mean, rstd, qkv, o, lse
+ *   outputs: dx (M, h), dgamma, dbeta (h) fp32, dWqkv (h, 3h), dWo (h, h)
+ *   ws: tp_workspace_size(TP_OP_ATTN_PROJ_BWD, b*s, h, 0, N, dtype, 0, mode)
+ */
+TP_API tp_status tp_attn_proj_bwd(const void* x, const float* gamma, const void* Wqkv,
+                                  const void* Wo, const void* xn, const float* mean,
+                                  const float* rstd, const void* qkv, const void* o,
+                                  const float* lse, const void* dout, void* dx, float* dgamma,
+                                  float* dbeta, void* dWqkv, void* dWo, int64_t b, int64_t s,
+                                  int64_t h, int32_t n_heads, int32_t N, int causal,
+                                  tp_dtype dtype, tp_reduce mode, void* ws, size_t ws_bytes,
+                                  void* stream);
+
+/*
+ * Pre-LN transformer layer with the tensor-parallel attention block and GELU MLP
+ * [Megatron-LM 实战 04 张量并行实现, 核心实现, TPTransformerLayer]:
+ *   x1 = x + Attn(LN1(x)),  out = x1 + MLP(LN2(x1)).
+ * tp_layer_fwd fills every field of *saved; tp_layer_bwd reads them and writes dx and
+ * every field of *grads. Sizes: M = b*s tokens, h hidden, f MLP width, n_heads, N shards.
+ * ws: tp_workspace_size(TP_OP_LAYER_FWD / TP_OP_LAYER_BWD, b*s, h, f, N, dtype, 0, mode).
+ */
+TP_API tp_status tp_layer_fwd(const void* x, const tp_layer_weights* w, const tp_layer_saved* saved,
+                              void* out, int64_t b, int64_t s, int64_t h, int64_t f,
+                              int32_t n_heads, int32_t N, int causal, tp_dtype dtype,
+                              tp_reduce mode, void* ws, size_t ws_bytes, void* stream);
+
+TP_API tp_status tp_layer_bwd(const void* x, const tp_layer_weights* w,
+                              const tp_layer_saved* saved, const void* dout, void* dx,
+                              const tp_layer_grads* grads, int64_t b, int64_t s, int64_t h,
+                              int64_t f, int32_t n_heads, int32_t N, int causal, tp_dtype dtype,
+                              tp_reduce mode, void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------ testing */
 
