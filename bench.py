@@ -39,6 +39,11 @@ WORKLOADS = {
                b=1, s=8192, h=8192, f=28672, N=4, act="swiglu", cfg=5),
     "c3": dict(desc="mid training erf-GELU MLP fwd+bwd: b=4 s=2048 h=4096 ffn=16384 N=8",
                b=4, s=2048, h=4096, f=16384, N=8, act="gelu", cfg=3),
+    "c1": dict(desc="tiny fp32 erf-GELU MLP fwd+bwd: b=2 s=16 h=128 ffn=512 N=2 (CUDA cores, no TF32)",
+               b=2, s=16, h=128, f=512, N=2, act="gelu", cfg=1, dtype="f32"),
+    "c2": dict(desc="page-2-sized pre-LN transformer layer fwd+bwd: b=8 s=128 h=128 heads=8 "
+                    "ffn=512 N=2", b=8, s=128, h=128, f=512, N=2, heads=8, act="gelu", cfg=2,
+               layer=True),
     # reduced-token case of c5 for ncu captures (a few GB on the device, inputs > L2)
     "c5-2k": dict(desc="profiling case: SwiGLU MLP fwd+bwd b=1 s=2048 h=8192 ffn=28672 N=4",
                   b=1, s=2048, h=8192, f=28672, N=4, act="swiglu", cfg=5),
@@ -49,6 +54,14 @@ DECODE = dict(desc="decode GEMV sweep: SwiGLU MLP forward, h=8192 ffn=28672 N=8 
               h=8192, f=28672, N=8, tokens=(1, 8, 32, 64), cfg=4)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def layer_flops(w):
+    """Algorithmic FLOPs of the pre-LN layer forward + backward (backward = 2 x forward):
+    QKV 2*M*h*3h, scores and P V 4*b*heads*s*s*d, W_o 2*M*h*h, MLP 4*M*h*f."""
+    M, h, f = w["b"] * w["s"], w["h"], w["f"]
+    fwd = 6 * M * h * h + 4 * w["b"] * w["s"] * w["s"] * h + 2 * M * h * h + 4 * M * h * f
+    return 3.0 * fwd
 
 
 def mlp_flops(w, M=None):
@@ -200,9 +213,13 @@ def make_inputs(w, rank, device):
     c = w["cfg"]
     off = rank_seed_offset(rank)
 
+    dt = w.get("dtype", "bf16")
+
     def dev(shape, name, sigma, extra=0):
-        a = synth.normal(shape, synth.seed_of(c, name) + extra, sigma, "bf16")
-        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device), a
+        a = synth.normal(shape, synth.seed_of(c, name) + extra, sigma, dt)
+        if dt == "bf16":
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device), a
+        return torch.from_numpy(a).to(device), a
 
     X, Xh = dev((M, h), "X", 1.0, off)
     dZ, dZh = dev((M, h), "dZ", 1.0, off)
@@ -227,12 +244,15 @@ def run_ours(args, w):
     B.build()
     T.lib()
     device = torch.device("cuda", torch.cuda.current_device())
+    if w.get("layer"):
+        return run_layer(args, w, T, device, rank, ws_)
     M, h, f, N = w["b"] * w["s"], w["h"], w["f"], w["N"]
     sw = w["act"] == "swiglu"
     act = T.Act.SWIGLU if sw else T.Act.GELU
     mode = T.Reduce.SPLITK if args.mode == "splitk" else T.Reduce.BUFFERS
-    BF = T.DType.BF16
-    bf = torch.bfloat16
+    f32 = w.get("dtype") == "f32"
+    BF = T.DType.F32 if f32 else T.DType.BF16
+    bf = torch.float32 if f32 else torch.bfloat16
     t_gen = time.time()
     d, hostin = make_inputs(w, rank, device)
     t_gen = time.time() - t_gen
@@ -286,8 +306,12 @@ def run_ours(args, w):
     # end to end: pinned host inputs in, results (Z, dX) out, every step
     Xp = torch.empty((M, h), dtype=bf, pin_memory=True)
     dZp = torch.empty((M, h), dtype=bf, pin_memory=True)
-    Xp.view(torch.int16).numpy()[:] = hostin["X"].view(np.int16)
-    dZp.view(torch.int16).numpy()[:] = hostin["dZ"].view(np.int16)
+    if f32:
+        Xp.numpy()[:] = hostin["X"]
+        dZp.numpy()[:] = hostin["dZ"]
+    else:
+        Xp.view(torch.int16).numpy()[:] = hostin["X"].view(np.int16)
+        dZp.view(torch.int16).numpy()[:] = hostin["dZ"].view(np.int16)
     Zp = torch.empty((M, h), dtype=bf, pin_memory=True)
     dXp = torch.empty((M, h), dtype=bf, pin_memory=True)
     barrier()
@@ -320,7 +344,8 @@ def run_ours(args, w):
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws_,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if f32 else "bf16",
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights; random init)",
         "config": {"workload": w["desc"], "tokens": M, "h": h, "ffn": f, "shards": N,
                    "act": w["act"], "shard_sum": args.mode, "global_batch": w["b"] * ws_,
@@ -335,18 +360,158 @@ def run_ours(args, w):
                      "algorithmic_flops_per_launch": col_gemm_flops(w),
                      "avg_launch_ms": round(col_max, 4)},
         "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": 2 * M * h * 2, "d2h_bytes_per_step": 2 * M * h * 2,
+                "h2d_bytes_per_step": 2 * M * h * (4 if f32 else 2),
+                "d2h_bytes_per_step": 2 * M * h * (4 if f32 else 2),
                 "ms_per_step": round(e2e_max, 4)},
         "gpu_launches": int(launches),
         "clocks": clk,
         "input_gen_s": round(t_gen, 1),
     }
-    if args.decode:
+    if f32:
+        out["roofline"] = {"bound": "alu", "note": "fp32 FFMA path at a latency-bound size; "
+                           "no roofline fraction is claimed", "achieved": None, "peak": None,
+                           "unit": "TFLOP/s", "frac": None, "traffic": None}
+    if args.decode and not f32:
         out["decode"] = run_decode(args, device, T)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, hostin, budget_s=args.cpu_budget)
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------------ page-2 layer
+
+def layer_inputs(w, rank):
+    """Seeded inputs of the pre-LN layer: x, dout ~N(0,1); W_qkv, W_o, W1, W2 ~N(0,0.02^2);
+    LayerNorm gamma = 1, beta = 0 (the framework's initial values)."""
+    from attention_gemms_gb300 import synth
+    b, s, h, f, c = w["b"], w["s"], w["h"], w["f"], w["cfg"]
+    M, off = b * s, rank_seed_offset(rank)
+    g = lambda shape, name, sigma, extra=0: synth.normal(shape, synth.seed_of(c, name) + extra,
+                                                         sigma, "bf16")
+    return {"x": g((M, h), "X", 1.0, off), "dout": g((M, h), "dZ", 1.0, off),
+            "Wqkv": g((h, 3 * h), "Wqkv", 0.02), "Wo": g((h, h), "Wo", 0.02),
+            "W1": g((h, f), "W1", 0.02), "W2": g((f, h), "W2", 0.02),
+            "gamma1": np.ones(h, np.float32), "beta1": np.zeros(h, np.float32),
+            "gamma2": np.ones(h, np.float32), "beta2": np.zeros(h, np.float32)}
+
+
+def run_layer(args, w, T, device, rank, nranks):
+    import torch
+    b, s, h, f, N, heads = w["b"], w["s"], w["h"], w["f"], w["N"], w["heads"]
+    M = b * s
+    BF, bf, f32 = T.DType.BF16, torch.bfloat16, torch.float32
+    mode = T.Reduce.SPLITK if args.mode == "splitk" else T.Reduce.BUFFERS
+    hin = layer_inputs(w, rank)
+    to = lambda a: (torch.from_numpy(a.view(np.int16)).view(bf) if a.dtype == np.uint16
+                    else torch.from_numpy(a)).to(device)
+    d = {k: to(v) for k, v in hin.items()}
+    e = lambda *sh, dty=bf: torch.empty(*sh, dtype=dty, device=device)
+    sv = dict(xn1=e(M, h), mean1=e(M, dty=f32), rstd1=e(M, dty=f32), qkv=e(M, 3 * h), o=e(M, h),
+              lse=e(b, heads, s, dty=f32), x1=e(M, h), xn2=e(M, h), mean2=e(M, dty=f32),
+              rstd2=e(M, dty=f32), y=e(M, f), hh=e(M, f))
+    gr = dict(dWqkv=e(h, 3 * h), dWo=e(h, h), dW1=e(h, f), dW2=e(f, h), dgamma1=e(h, dty=f32),
+              dbeta1=e(h, dty=f32), dgamma2=e(h, dty=f32), dbeta2=e(h, dty=f32))
+    W = T.make_struct(T.LayerWeights, **{k: d[k] for k in ("Wqkv", "Wo", "W1", "W2", "gamma1",
+                                                             "beta1", "gamma2", "beta2")})
+    S = T.make_struct(T.LayerSaved, **sv)
+    G = T.make_struct(T.LayerGrads, **gr)
+    wsb = max(T.tp_workspace_size(T.Op.LAYER_FWD, M, h, f, N, BF, T.Act.GELU, mode),
+              T.tp_workspace_size(T.Op.LAYER_BWD, M, h, f, N, BF, T.Act.GELU, mode))
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=device)
+    out, dx = e(M, h), e(M, h)
+
+    def step():
+        T.tp_layer_fwd(d["x"], W, S, out, b, s, h, f, heads, N, 0, BF, mode, ws, ws.numel())
+        T.tp_layer_bwd(d["x"], W, S, d["dout"], dx, G, b, s, h, f, heads, N, 0, BF, mode, ws,
+                       ws.numel())
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    n0 = T.tp_launch_count()
+    step()
+    per_step_launches = T.tp_launch_count() - n0
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(max(args.warmup, 20)):
+        g.replay()
+    clocks = ClockSampler(device.index)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        g.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    barrier()
+    ms = t0.elapsed_time(t1) / args.steps
+    # end to end through the C ABI: x and dout in from pinned memory, out and dx back
+    xp = torch.empty((M, h), dtype=bf, pin_memory=True)
+    dp = torch.empty((M, h), dtype=bf, pin_memory=True)
+    xp.view(torch.int16).numpy()[:] = hin["x"].view(np.int16)
+    dp.view(torch.int16).numpy()[:] = hin["dout"].view(np.int16)
+    op, dxp = torch.empty_like(xp, pin_memory=True), torch.empty_like(xp, pin_memory=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        d["x"].copy_(xp, non_blocking=True)
+        d["dout"].copy_(dp, non_blocking=True)
+        step()
+        op.copy_(out, non_blocking=True)
+        dxp.copy_(dx, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    clk = clocks.stop()
+    if T.tp_check_status() != 0:
+        raise RuntimeError("device wait timeout in the layer: " + T.tp_last_error())
+    ms_max, e2e_max = max_over_ranks(ms, device), max_over_ranks(e2e_ms, device)
+    fl = layer_flops(w)
+    res = {
+        "metric": METRIC, "value": round(fl * nranks / (ms_max * 1e-3) / 1e12, 3),
+        "unit": "TFLOP/s", "n_gpus": nranks, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; LN gamma=1, beta=0)",
+        "config": {"workload": w["desc"], "tokens": M, "h": h, "ffn": f, "heads": heads,
+                   "shards": N, "shard_sum": args.mode, "replay": "CUDA graph of one step",
+                   "launches_per_step": int(per_step_launches),
+                   "parallelism": f"tp{N} virtual ranks per GPU, dp{nranks}"},
+        "roofline": {"bound": "latency", "note": "launch/latency-bound size (M=1024, h=128): "
+                     "the step time is reported, no roofline fraction is claimed",
+                     "achieved": None, "peak": None, "unit": "TFLOP/s", "frac": None,
+                     "traffic": None},
+        "e2e": {"value": round(fl * nranks / (e2e_max * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": 2 * M * h * 2, "d2h_bytes_per_step": 2 * M * h * 2,
+                "ms_per_step": round(e2e_max, 4), "replay": "eager launches"},
+        "gpu_launches": int(per_step_launches) * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = layer_cpu_baseline(w, hin)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+def layer_cpu_baseline(w, hin, reps=3):
+    from attention_gemms_gb300 import synth
+    from oracle import tp_oracle as O
+    f64 = lambda a: synth.to_f64(a, "bf16") if a.dtype == np.uint16 else a.astype(np.float64)
+    p = {k: f64(hin[k]) for k in ("Wqkv", "Wo", "W1", "W2", "gamma1", "beta1", "gamma2", "beta2")}
+    x, dout = f64(hin["x"]), f64(hin["dout"])
+    c0, t0 = time.process_time(), time.perf_counter()
+    for _ in range(reps):
+        O.layer_bwd(x, w["b"], w["s"], p, w["heads"], w["N"], dout)  # runs the forward too
+    dt, dc = (time.perf_counter() - t0) / reps, (time.process_time() - c0) / reps
+    return {"value": round(layer_flops(w) / dt / 1e12, 6), "unit": "TFLOP/s",
+            "cores": len(os.sched_getaffinity(0)), "threads_effective": round(dc / dt, 1),
+            "kind": "oracle", "sample": f"fp64 oracle layer forward+backward on the whole "
+                                        f"workload, {reps} repetitions, {dt:.2f} s each"}
 
 
 # ------------------------------------------------------------------ decode sweep
@@ -447,8 +612,9 @@ def _oracle_sample(w, hostin, rows, Wf):
     """One forward + backward of the oracle on `rows` token rows (full weights)."""
     from attention_gemms_gb300 import synth
     from oracle import tp_oracle as O
-    X = synth.to_f64(hostin["X"][:rows], "bf16")
-    dZ = synth.to_f64(hostin["dZ"][:rows], "bf16")
+    dt = w.get("dtype", "bf16")
+    X = synth.to_f64(hostin["X"][:rows], dt)
+    dZ = synth.to_f64(hostin["dZ"][:rows], dt)
     if w["act"] == "swiglu":
         O.mlp_swiglu_fwd(X, Wf["W1"], Wf["W1u"], Wf["W2"], w["N"])
         O.mlp_swiglu_bwd(X, Wf["W1"], Wf["W1u"], Wf["W2"], dZ, w["N"])
@@ -457,14 +623,14 @@ def _oracle_sample(w, hostin, rows, Wf):
         O.mlp_gelu_bwd(X, Wf["W1"], Wf["W2"], dZ, w["N"])
 
 
-def _weights_f64(hostin):
+def _weights_f64(hostin, dt="bf16"):
     from attention_gemms_gb300 import synth
-    return {k: (synth.to_f64(hostin[k], "bf16") if hostin[k] is not None else None)
+    return {k: (synth.to_f64(hostin[k], dt) if hostin[k] is not None else None)
             for k in ("W1", "W1u", "W2")}
 
 
 def cpu_baseline(w, hostin, budget_s=15.0):
-    Wf = _weights_f64(hostin)
+    Wf = _weights_f64(hostin, w.get("dtype", "bf16"))
     rows = 8
     while True:
         c0, t0 = time.process_time(), time.perf_counter()
@@ -489,24 +655,38 @@ def run_reference(args, w):
     from attention_gemms_gb300 import synth
     M, h, f = w["b"] * w["s"], w["h"], w["f"]
     c = w["cfg"]
-    hostin = {"X": synth.normal((M, h), synth.seed_of(c, "X"), 1.0, "bf16"),
-              "dZ": synth.normal((M, h), synth.seed_of(c, "dZ"), 1.0, "bf16"),
-              "W1": synth.normal((h, f), synth.seed_of(c, "Wg"), 0.02, "bf16"),
-              "W1u": (synth.normal((h, f), synth.seed_of(c, "Wu"), 0.02, "bf16")
-                      if w["act"] == "swiglu" else None),
-              "W2": synth.normal((f, h), synth.seed_of(c, "Wd"), 0.02, "bf16")}
-    Wf = _weights_f64(hostin)
+    dtp = w.get("dtype", "bf16")
+    if w.get("layer"):
+        from oracle import tp_oracle as O
+        hin = layer_inputs(w, 0)
+        f64 = lambda a: synth.to_f64(a, "bf16") if a.dtype == np.uint16 else a.astype(np.float64)
+        p = {k: f64(hin[k]) for k in ("Wqkv", "Wo", "W1", "W2", "gamma1", "beta1", "gamma2",
+                                      "beta2")}
+        x, dout = f64(hin["x"]), f64(hin["dout"])
+        run = lambda: O.layer_bwd(x, w["b"], w["s"], p, w["heads"], w["N"], dout)
+        flops = layer_flops(w)
+        sample = "fp64 oracle layer forward+backward on the whole workload per step"
+    else:
+        hostin = {"X": synth.normal((M, h), synth.seed_of(c, "X"), 1.0, dtp),
+                  "dZ": synth.normal((M, h), synth.seed_of(c, "dZ"), 1.0, dtp),
+                  "W1": synth.normal((h, f), synth.seed_of(c, "Wg"), 0.02, dtp),
+                  "W1u": (synth.normal((h, f), synth.seed_of(c, "Wu"), 0.02, dtp)
+                          if w["act"] == "swiglu" else None),
+                  "W2": synth.normal((f, h), synth.seed_of(c, "Wd"), 0.02, dtp)}
+        Wf = _weights_f64(hostin, dtp)
+        rows = min(args.ref_rows, M)
+        run = lambda: _oracle_sample(w, hostin, rows, Wf)
+        flops = mlp_flops(w, rows)
+        sample = (f"fp64 oracle forward+backward on {rows} of {M} token rows per step, full "
+                  f"weights; FLOPs scaled by the row fraction")
     t_gen = time.time() - t_gen
-    rows = args.ref_rows
     for _ in range(args.warmup):
-        _oracle_sample(w, hostin, rows, Wf)
+        run()
     c0, t0 = time.process_time(), time.perf_counter()
     for _ in range(args.steps):
-        _oracle_sample(w, hostin, rows, Wf)
+        run()
     dt, dc = (time.perf_counter() - t0) / args.steps, (time.process_time() - c0) / args.steps
-    val = mlp_flops(w, rows) / dt / 1e12
-    sample = (f"fp64 oracle forward+backward on {rows} of {M} token rows per step, full weights; "
-              f"FLOPs scaled by the row fraction")
+    val = flops / dt / 1e12
     print(json.dumps({
         "metric": METRIC, "value": round(val, 6), "unit": "TFLOP/s", "n_gpus": ws_,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 2),
@@ -528,7 +708,9 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="c5", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="c5", choices=sorted(WORKLOADS),
+                    help="c5 (default): large SwiGLU MLP; c3: GELU MLP; c2: page-2 layer; "
+                         "c1: tiny fp32 MLP; c5-2k: profiling case")
     ap.add_argument("--mode", default="splitk", choices=["splitk", "buffers"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-rows", type=int, default=64)
