@@ -68,6 +68,19 @@ struct TcParams {  // CUtensorMap members carry their own 128-byte alignment
   int debug_hang;
 };
 
+// Optional wait-cycle counters (compile with -DTP_GEMM_STATS; off in normal builds):
+// per CTA, [0] producer waiting for a free stage, [1] MMA waiting for data,
+// [2] MMA waiting for a free accumulator, [3] epilogue waiting for an accumulator,
+// [4] epilogue busy, [5] MMA thread lifetime, [6] tiles, [7] producer lifetime.
+#ifdef TP_GEMM_STATS
+__device__ unsigned long long g_gemm_stats[1024][8];
+#define TP_STAT(i, v) atomicAdd(&g_gemm_stats[blockIdx.x][i], static_cast<unsigned long long>(v))
+#define TP_CLK() clock64()
+#else
+#define TP_STAT(i, v) ((void)(v))
+#define TP_CLK() 0ll
+#endif
+
 struct TileCoord {
   int g, mt, nt;
 };
@@ -249,15 +262,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       const uint32_t stage_tx = C::STAGE_BYTES;
       uint32_t stage = 0, phase = 0;
       bool ok = true;
+      [[maybe_unused]] const long long t_start = TP_CLK();
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
         const TileCoord tc = tile_coord(p, t);
         const int m0 = tc.mt * BM;
         const int n0 = tc.nt * bn_logical;
         for (int kb = 0; kb < nkb; ++kb) {
+          [[maybe_unused]] const long long tw = TP_CLK();
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag)) {
             ok = false;
             break;
           }
+          TP_STAT(0, TP_CLK() - tw);
           const int seg = kb / p.kb_per_seg;
           const int k0 = p.seg_k0[seg] + static_cast<int>(tc.g * p.K) + (kb - seg * p.kb_per_seg) * BK;
           const uint32_t a_dst = sbase + stage * C::STAGE_BYTES;
@@ -290,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           }
         }
       }
+      TP_STAT(7, TP_CLK() - t_start);
       if (!ok) record_timeout(p.status);
     }
     __syncwarp();  // reconverge before the block-wide (aligned) barriers below
@@ -302,18 +319,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       if (p.debug_hang) ok = mbar_wait(never_bar, 0, p.timeout_ns, abort_flag);
+      [[maybe_unused]] const long long t_start = TP_CLK();
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        [[maybe_unused]] long long tw = TP_CLK();
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
           ok = false;
           break;
         }
+        TP_STAT(2, TP_CLK() - tw);
+        TP_STAT(6, 1);
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = 0; kb < nkb; ++kb) {
+          tw = TP_CLK();
           if (!mbar_wait(full_bar(stage), phase, p.timeout_ns, abort_flag)) {
             ok = false;
             break;
           }
+          TP_STAT(1, TP_CLK() - tw);
           tc_fence_after();
           const uint32_t a_addr = sbase + stage * C::STAGE_BYTES;
           const uint32_t b_addr = a_addr + C::A_BYTES;
@@ -335,6 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
+      TP_STAT(5, TP_CLK() - t_start);
       if (!ok) record_timeout(p.status);
     }
     __syncwarp();
@@ -345,8 +369,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const TileCoord tc = tile_coord(p, t);
       int ok = 1;
+      [[maybe_unused]] const long long tw = TP_CLK();
       if (lane == 0) ok = mbar_wait(tfull_bar(acc), acc_phase, p.timeout_ns, abort_flag) ? 1 : 0;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      [[maybe_unused]] const long long tb = TP_CLK();
+      if (warp == 2 && lane == 0) TP_STAT(3, tb - tw);
       if (!ok) {
         if (lane == 0) record_timeout(p.status);
         break;
@@ -378,6 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       }
       tc_fence_before();
       __syncwarp();
+      if (warp == 2 && lane == 0) TP_STAT(4, TP_CLK() - tb);
       if (lane == 0) mbar_arrive(tempty_bar(acc));
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
@@ -412,6 +440,288 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ CTA-pair kernel
+//
+// Same roles as gemm_tc_kernel, but two CTAs of a cluster share one 256 x 256 tile
+// through tcgen05.mma.cta_group::2: CTA r of the pair stages A rows [128 r, 128 r + 128)
+// and B columns [128 r, 128 r + 128) of the tile (32 KB per 64-deep K block instead
+// of 48 KB for 128 x 256 on one CTA), and holds D rows [128 r, 128 r + 128) in its
+// TMEM. The even CTA issues the MMAs; its commits arrive on the barriers of both
+// CTAs (multicast). Both CTAs' copies of a stage complete on the even CTA's "full"
+// barrier (pair form of the TMA load), whose producer expects both halves' bytes;
+// the odd CTA's epilogue warps report "accumulator drained" to the even CTA with
+// remote arrives. At exit both CTAs wait for the pair's last MMAs, then for each
+// other, before freeing TMEM.
+
+constexpr int kPairStages = 6;
+constexpr int kPairStageBytes = 2 * 128 * BK * 2;  // A 128 x 64 + B 128 x 64, bf16
+constexpr int kPairBars = 2 * kPairStages + 7;
+constexpr int kPairSmem = kPairStages * kPairStageBytes + 1024 + kPairBars * 8 + 16;
+constexpr uint64_t kPairDrainNs = 20000000ull;
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_constant__ TcParams p) {
+  constexpr int S = kPairStages;
+  constexpr int A_BYTES = 128 * BK * 2;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * kPairStageBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kPairBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * S + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
+  const uint32_t exit_bar = bar0 + 8u * (2 * S + 5);
+  const uint32_t never_bar = bar0 + 8u * (2 * S + 6);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);  // even CTA: its producer's expect-tx; odd CTA: unused
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), leader ? 8 : 1);  // 4 epilogue warps in each CTA
+    }
+    mbar_init(drain_bar, 1);
+    mbar_init(exit_bar, 1);
+    mbar_init(never_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmA[0]);
+    tma_prefetch_desc(&p.tmB[0]);
+    for (int s = 1; s < p.nseg; ++s) {
+      tma_prefetch_desc(&p.tmA[s]);
+      tma_prefetch_desc(&p.tmB[s]);
+    }
+    if (p.paired) tma_prefetch_desc(&p.tmB[1]);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), 512);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // the peer's barriers are initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+  const int ntiles = p.tiles_m * p.tiles_n * p.groups;
+  const int nkb = p.nseg * p.kb_per_seg;
+  const int bn_logical = p.paired ? 128 : 256;
+  uint32_t issued = 0;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer (both CTAs)
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      [[maybe_unused]] const long long t_start = TP_CLK();
+      const uint32_t lead_full0 = mapa_shared(full_bar(0), 0);
+      for (int t = pair; t < ntiles && ok; t += npairs) {
+        const TileCoord tc = tile_coord(p, t);
+        const int m0 = tc.mt * 256 + static_cast<int>(rank) * 128;
+        const int n0 = tc.nt * bn_logical;
+        for (int kb = 0; kb < nkb; ++kb) {
+          [[maybe_unused]] const long long tw = TP_CLK();
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          TP_STAT(0, TP_CLK() - tw);
+          const int seg = kb / p.kb_per_seg;
+          const int k0 =
+              p.seg_k0[seg] + static_cast<int>(tc.g * p.K) + (kb - seg * p.kb_per_seg) * BK;
+          const uint32_t a_dst = sbase + stage * kPairStageBytes;
+          const uint32_t b_dst = a_dst + A_BYTES;
+          const uint32_t fb = lead_full0 + 8u * stage;  // the even CTA's barrier
+          if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * kPairStageBytes);
+          if (p.a_mn) {
+            tma_load_2d_pair(a_dst, &p.tmA[seg], fb, m0, k0);
+            tma_load_2d_pair(a_dst + 8192, &p.tmA[seg], fb, m0 + 64, k0);
+          } else {
+            tma_load_2d_pair(a_dst, &p.tmA[seg], fb, k0, m0);
+          }
+          if (p.paired) {
+            // even CTA: 128 gate columns, odd CTA: the same 128 up columns
+            tma_load_2d_pair(b_dst, &p.tmB[rank], fb, n0, k0);
+            tma_load_2d_pair(b_dst + 8192, &p.tmB[rank], fb, n0 + 64, k0);
+          } else if (p.b_mn) {
+            const int nb = n0 + static_cast<int>(rank) * 128;
+            tma_load_2d_pair(b_dst, &p.tmB[seg], fb, nb, k0);
+            tma_load_2d_pair(b_dst + 8192, &p.tmB[seg], fb, nb + 64, k0);
+          } else {
+            tma_load_2d_pair(b_dst, &p.tmB[seg], fb, k0, n0 + static_cast<int>(rank) * 128);
+          }
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      TP_STAT(7, TP_CLK() - t_start);
+      if (!ok) record_timeout(p.status);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------------------ pair MMA issuer
+      const uint32_t idesc = idesc_bf16_f32(256, 256, p.a_mn, p.b_mn);
+      const uint32_t a_lbo = p.a_mn ? 8192u : 16u, b_lbo = p.b_mn ? 8192u : 16u;
+      const uint32_t a_kstep = p.a_mn ? 2048u : 32u, b_kstep = p.b_mn ? 2048u : 32u;
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      if (p.debug_hang) ok = mbar_wait(never_bar, 0, p.timeout_ns, abort_flag);
+      [[maybe_unused]] const long long t_start = TP_CLK();
+      for (int t = pair; t < ntiles && ok; t += npairs) {
+        [[maybe_unused]] long long tw = TP_CLK();
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        TP_STAT(2, TP_CLK() - tw);
+        TP_STAT(6, 1);
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * 256;
+        for (int kb = 0; kb < nkb; ++kb) {
+          tw = TP_CLK();
+          if (!mbar_wait(full_bar(stage), phase, p.timeout_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          TP_STAT(1, TP_CLK() - tw);
+          tc_fence_after();
+          const uint32_t a_addr = sbase + stage * kPairStageBytes;
+          const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = sw128_desc(a_addr + kk * a_kstep, a_lbo, 1024u);
+            const uint64_t bd = sw128_desc(b_addr + kk * b_kstep, b_lbo, 1024u);
+            mma_bf16_ss_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit_pair(empty_bar(stage), 0x3);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair(tfull_bar(acc), 0x3);
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      TP_STAT(5, TP_CLK() - t_start);
+      if (!ok) record_timeout(p.status);
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- epilogue (both CTAs)
+    const int quad = warp & 3;
+    const uint32_t remote_tempty0 = mapa_shared(tempty_bar(0), 0);
+    uint32_t acc = 0, acc_phase = 0;
+    for (int t = pair; t < ntiles; t += npairs) {
+      const TileCoord tc = tile_coord(p, t);
+      int ok = 1;
+      [[maybe_unused]] const long long tw = TP_CLK();
+      if (lane == 0) ok = mbar_wait(tfull_bar(acc), acc_phase, p.timeout_ns, abort_flag) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      [[maybe_unused]] const long long tb = TP_CLK();
+      if (warp == 2 && lane == 0) TP_STAT(3, tb - tw);
+      if (!ok) {
+        if (lane == 0) record_timeout(p.status);
+        break;
+      }
+      tc_fence_after();
+      const int64_t row =
+          static_cast<int64_t>(tc.mt) * 256 + static_cast<int>(rank) * 128 + quad * 32 + lane;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * 256;
+      const int64_t col_base = static_cast<int64_t>(tc.nt) * bn_logical;
+      for (int c = 0; c < bn_logical / 32; ++c) {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(t_row + c * 32, ra);
+        if (p.paired) tmem_ld32(t_row + 128 + c * 32, rb);
+        tmem_ld_wait();
+        if (row < p.M) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int64_t col = col_base + c * 32 + q * 8;
+            if (col < p.N) {
+              float a[8], b[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                a[i] = __uint_as_float(ra[q * 8 + i]);
+                b[i] = __uint_as_float(rb[q * 8 + i]);
+              }
+              epi8<EPI>(p, tc.g, row, col, a, b);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (warp == 2 && lane == 0) TP_STAT(4, TP_CLK() - tb);
+      if (lane == 0) {
+        if (leader) mbar_arrive(tempty_bar(acc));
+        else mbar_arrive_remote(remote_tempty0 + 8u * acc);
+      }
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  __syncthreads();
+  volatile int no_abort = 0;
+  // after an abort, the even CTA waits (bounded) for the copies of both CTAs, whose
+  // completions land on its barriers; the odd CTA stays until the exit handshake
+  if (*abort_flag && warp == 0 && leader) {
+    if (lane == 0) {
+      for (int s = 0; s < S; ++s) {
+        if (issued > static_cast<uint32_t>(s)) {
+          const uint32_t last = ((issued - 1u - s) / S) * S + s;
+          mbar_wait(full_bar(s), (last / S) & 1u, kPairDrainNs, &no_abort);
+        }
+      }
+    }
+    __syncwarp();
+  }
+  if (warp == 1) {
+    // every MMA of the pair has completed once the even CTA's final commit arrives
+    if (lane == 0) {
+      if (leader) mma_commit_pair(drain_bar, 0x3);
+      mbar_wait(drain_bar, 0, kPairDrainNs, &no_abort);
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // neither CTA leaves while the other may still signal its barriers or read its smem
+    mbar_arrive_remote(mapa_shared(exit_bar, rank ^ 1u));
+    mbar_wait(exit_bar, 0, kPairDrainNs, &no_abort);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, 512);
   }
 }
 
@@ -482,11 +792,56 @@ tp_status launch_bn(int epi, const TcParams& prm, int grid, cudaStream_t st) {
   return fail(TP_ERR_INVALID_ARG, "unknown epilogue");
 }
 
+template <int EPI>
+tp_status launch_pair_epi(const TcParams& prm, int64_t ntiles, cudaStream_t st) {
+  auto kern = gemm_tc2_kernel<EPI>;
+  static int max_pairs = 0;  // per instantiation; benign race (idempotent)
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPairSmem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_pairs == 0) {
+    TP_CUDA_TRY(
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem));
+    cfg.gridDim = dim3(2 * static_cast<unsigned>(device_sm_count() / 2), 1, 1);
+    int n = 0;
+    TP_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, kern, &cfg));
+    if (n <= 0) return fail(TP_ERR_CUDA, "no CTA pair of the GEMM kernel fits on the device");
+    max_pairs = n;
+  }
+  const int pairs = static_cast<int>(std::min<int64_t>(ntiles, max_pairs));
+  cfg.gridDim = dim3(2 * static_cast<unsigned>(pairs), 1, 1);
+  TP_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, prm));
+  count_launch();
+  return TP_OK;
+}
+
+tp_status launch_pair(int epi, const TcParams& prm, int64_t ntiles, cudaStream_t st) {
+  switch (epi) {
+    case EPI_STORE: return launch_pair_epi<EPI_STORE>(prm, ntiles, st);
+    case EPI_GELU: return launch_pair_epi<EPI_GELU>(prm, ntiles, st);
+    case EPI_SWIGLU: return launch_pair_epi<EPI_SWIGLU>(prm, ntiles, st);
+    case EPI_DGELU: return launch_pair_epi<EPI_DGELU>(prm, ntiles, st);
+    case EPI_DSWIGLU: return launch_pair_epi<EPI_DSWIGLU>(prm, ntiles, st);
+    case EPI_PAIR: return launch_pair_epi<EPI_PAIR>(prm, ntiles, st);
+  }
+  return fail(TP_ERR_INVALID_ARG, "unknown epilogue");
+}
+
 std::atomic<int> g_debug_hang{0};
+std::atomic<int> g_pair_mode{1};  // 1: CTA-pair kernel for large tiles, 0: one-CTA kernel only
 
 }  // namespace
 
 void set_debug_hang(int v) { g_debug_hang.store(v); }
+void set_pair_mode(int v) { g_pair_mode.store(v); }
 
 tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
   if (d.M <= 0 || d.N <= 0 || d.K <= 0) return TP_OK;
@@ -506,6 +861,9 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
   const int64_t n_tmem = d.paired ? 2 * d.N : d.N;
   const int BN = (n_tmem >= 256 && d.M > 64) ? 256 : 128;
   const int bn_logical = d.paired ? BN / 2 : BN;
+  // 256 x 256 tiles on CTA pairs once there are at least 256 rows
+  const bool pair = BN == 256 && d.M >= 256 && g_pair_mode.load() != 0;
+  const int tile_m = pair ? 256 : BM;
 
   TcParams prm;
   memset(&prm, 0, sizeof(prm));
@@ -516,7 +874,7 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
   const int nb = d.paired ? 2 : d.nseg;
   for (int s = 0; s < nb; ++s) {
     if (d.b_mn) TP_TRY(make_map(&prm.tmB[s], d.B[s], 64, 64));
-    else TP_TRY(make_map(&prm.tmB[s], d.B[s], 64, static_cast<uint32_t>(BN)));
+    else TP_TRY(make_map(&prm.tmB[s], d.B[s], 64, static_cast<uint32_t>(pair ? 128 : BN)));
   }
   for (int s = d.nseg; s < 3; ++s) prm.tmA[s] = prm.tmA[0];
   for (int s = nb; s < 3; ++s) prm.tmB[s] = prm.tmB[0];
@@ -529,7 +887,7 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
   prm.nseg = d.nseg;
   prm.paired = d.paired;
   prm.groups = d.groups;
-  prm.tiles_m = static_cast<int>((d.M + BM - 1) / BM);
+  prm.tiles_m = static_cast<int>((d.M + tile_m - 1) / tile_m);
   prm.tiles_n = static_cast<int>((d.N + bn_logical - 1) / bn_logical);
   prm.kb_per_seg = static_cast<int>((d.K + BK - 1) / BK);
   prm.shards = 1;
@@ -553,8 +911,21 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
 
   const int64_t ntiles = static_cast<int64_t>(prm.tiles_m) * prm.tiles_n * prm.groups;
   if (ntiles > (1ll << 30)) return fail(TP_ERR_SHAPE, "problem too large");
+  if (pair) return launch_pair(epi, prm, ntiles, st);
   const int grid = static_cast<int>(std::min<int64_t>(ntiles, device_sm_count()));
   return BN == 256 ? launch_bn<256>(epi, prm, grid, st) : launch_bn<128>(epi, prm, grid, st);
 }
 
 }  // namespace tp
+
+#ifdef TP_GEMM_STATS
+// Instrumented builds only: copy out and clear the wait-cycle counters.
+extern "C" TP_API int tp_debug_gemm_stats(unsigned long long* out, int ctas) {
+  if (ctas > 1024) ctas = 1024;
+  if (cudaMemcpyFromSymbol(out, tp::g_gemm_stats, sizeof(unsigned long long) * 8 * ctas) !=
+      cudaSuccess)
+    return 1;
+  static unsigned long long zero[1024][8];
+  return cudaMemcpyToSymbol(tp::g_gemm_stats, zero, sizeof(zero)) == cudaSuccess ? 0 : 1;
+}
+#endif

@@ -162,6 +162,12 @@ TP_API tp_status tp_check_status(void* stream);
  * to launches made after the call, from any thread. 0 restores the default. */
 TP_API void tp_set_wait_timeout_ns(uint64_t ns);
 
+/* Large GEMM tiles (M >= 256 rows, 256 columns) run on CTA pairs (two SMs sharing one
+ * 256 x 256 tile through tcgen05 pair MMAs) when enabled (default 1); 0 restricts every
+ * GEMM to the one-CTA 128 x 256 kernel. Results agree within rounding either way;
+ * this switch exists to compare the two kernels. Applies to launches made after it. */
+TP_API void tp_set_gemm_pair_mode(int enable);
+
 /* Number of kernel launches this library has made in this process (all threads). */
 TP_API uint64_t tp_launch_count(void);
 
