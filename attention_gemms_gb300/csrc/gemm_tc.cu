@@ -33,7 +33,17 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kThreads = 192;
-constexpr int kGroupM = 16;
+#ifndef TP_GROUP_M
+#define TP_GROUP_M 16
+#endif
+#ifndef TP_PAIR_STAGES
+#define TP_PAIR_STAGES 6
+#endif
+#ifndef TP_MN_3D
+#define TP_MN_3D 1
+#endif
+constexpr bool kMn3d = TP_MN_3D != 0;
+constexpr int kGroupM = TP_GROUP_M;
 constexpr uint64_t kDrainTimeoutNs = 1000000000ull;
 
 template <int BN>
@@ -52,6 +62,7 @@ struct TcParams {  // CUtensorMap members carry their own 128-byte alignment
   CUtensorMap tmB[3];
   int64_t M, N, K;  // N counts logical output columns
   int a_mn, b_mn, nseg, paired, groups;
+  int a3d, b3d;  // MN-major operand maps are 3-D (x: 64 columns, y: k, z: 64-column chunk)
   int seg_k0[3];
   int tiles_m, tiles_n, kb_per_seg;
   int shards, shard_axis;
@@ -279,7 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           const uint32_t a_dst = sbase + stage * C::STAGE_BYTES;
           const uint32_t b_dst = a_dst + C::A_BYTES;
           mbar_arrive_expect_tx(full_bar(stage), stage_tx);
-          if (p.a_mn) {
+          if (p.a_mn && p.a3d) {
+            tma_load_3d(a_dst, &p.tmA[seg], full_bar(stage), 0, k0, m0 / 64);
+          } else if (p.a_mn) {
             tma_load_2d(a_dst, &p.tmA[seg], full_bar(stage), m0, k0);
             tma_load_2d(a_dst + 8192, &p.tmA[seg], full_bar(stage), m0 + 64, k0);
           } else {
@@ -287,11 +300,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           }
           if (p.paired) {
             constexpr int HALF = BN / 128;  // 64-wide boxes per half
+            if (p.b3d) {
+              tma_load_3d(b_dst, &p.tmB[0], full_bar(stage), 0, k0, n0 / 64);
+              tma_load_3d(b_dst + HALF * 8192, &p.tmB[1], full_bar(stage), 0, k0, n0 / 64);
+            } else {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) {
-              const int half = j / HALF;
-              tma_load_2d(b_dst + j * 8192, &p.tmB[half], full_bar(stage), n0 + 64 * (j % HALF), k0);
+              for (int j = 0; j < BN / 64; ++j) {
+                const int half = j / HALF;
+                tma_load_2d(b_dst + j * 8192, &p.tmB[half], full_bar(stage), n0 + 64 * (j % HALF),
+                            k0);
+              }
             }
+          } else if (p.b_mn && p.b3d) {
+            tma_load_3d(b_dst, &p.tmB[seg], full_bar(stage), 0, k0, n0 / 64);
           } else if (p.b_mn) {
 #pragma unroll
             for (int j = 0; j < BN / 64; ++j)
@@ -456,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 // remote arrives. At exit both CTAs wait for the pair's last MMAs, then for each
 // other, before freeing TMEM.
 
-constexpr int kPairStages = 6;
+constexpr int kPairStages = TP_PAIR_STAGES;
 constexpr int kPairStageBytes = 2 * 128 * BK * 2;  // A 128 x 64 + B 128 x 64, bf16
 constexpr int kPairBars = 2 * kPairStages + 7;
 constexpr int kPairSmem = kPairStages * kPairStageBytes + 1024 + kPairBars * 8 + 16;
@@ -553,7 +574,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
           const uint32_t b_dst = a_dst + A_BYTES;
           const uint32_t fb = lead_full0 + 8u * stage;  // the even CTA's barrier
           if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * kPairStageBytes);
-          if (p.a_mn) {
+          if (p.a_mn && p.a3d) {
+            tma_load_3d_pair(a_dst, &p.tmA[seg], fb, 0, k0, m0 / 64);
+          } else if (p.a_mn) {
             tma_load_2d_pair(a_dst, &p.tmA[seg], fb, m0, k0);
             tma_load_2d_pair(a_dst + 8192, &p.tmA[seg], fb, m0 + 64, k0);
           } else {
@@ -561,12 +584,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
           }
           if (p.paired) {
             // even CTA: 128 gate columns, odd CTA: the same 128 up columns
-            tma_load_2d_pair(b_dst, &p.tmB[rank], fb, n0, k0);
-            tma_load_2d_pair(b_dst + 8192, &p.tmB[rank], fb, n0 + 64, k0);
+            if (p.b3d) {
+              tma_load_3d_pair(b_dst, &p.tmB[rank], fb, 0, k0, n0 / 64);
+            } else {
+              tma_load_2d_pair(b_dst, &p.tmB[rank], fb, n0, k0);
+              tma_load_2d_pair(b_dst + 8192, &p.tmB[rank], fb, n0 + 64, k0);
+            }
           } else if (p.b_mn) {
             const int nb = n0 + static_cast<int>(rank) * 128;
-            tma_load_2d_pair(b_dst, &p.tmB[seg], fb, nb, k0);
-            tma_load_2d_pair(b_dst + 8192, &p.tmB[seg], fb, nb + 64, k0);
+            if (p.b3d) {
+              tma_load_3d_pair(b_dst, &p.tmB[seg], fb, 0, k0, nb / 64);
+            } else {
+              tma_load_2d_pair(b_dst, &p.tmB[seg], fb, nb, k0);
+              tma_load_2d_pair(b_dst + 8192, &p.tmB[seg], fb, nb + 64, k0);
+            }
           } else {
             tma_load_2d_pair(b_dst, &p.tmB[seg], fb, k0, n0 + static_cast<int>(rank) * 128);
           }
@@ -764,6 +795,26 @@ tp_status make_map(CUtensorMap* m, const Operand& op, uint32_t box_inner, uint32
   return TP_OK;
 }
 
+// 3-D view of an MN-major operand for loading `chunks` 64-column chunks at once:
+// dims (64, rows, cols / 64), strides (ld * 2, 128) bytes, box (64, 64, chunks).
+tp_status make_map_3d(CUtensorMap* m, const Operand& op, uint32_t chunks) {
+  EncodeTiledFn enc = get_encoder();
+  if (!enc) return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
+  if (reinterpret_cast<uintptr_t>(op.ptr) % 16 != 0 || (op.ld * 2) % 16 != 0 || op.cols % 64 != 0)
+    return fail(TP_ERR_ALIGNMENT, "3-D TMA operand not 16-byte aligned or ragged");
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(op.rows),
+                              static_cast<cuuint64_t>(op.cols / 64)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(op.ld) * 2, 128};
+  const cuuint32_t box[3] = {64, 64, chunks};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(op.ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed (code " + std::to_string(r) + ")");
+  return TP_OK;
+}
+
 template <int BN, int EPI>
 tp_status launch_bn_epi(const TcParams& prm, int grid, cudaStream_t st) {
   auto kern = gemm_tc_kernel<BN, EPI>;
@@ -867,15 +918,25 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
 
   TcParams prm;
   memset(&prm, 0, sizeof(prm));
+  const int nb = d.paired ? 2 : d.nseg;
+  // MN-major operands whose rows are whole 64-column chunks use one 3-D load per stage
+  bool a3d = kMn3d && d.a_mn, b3d = kMn3d && d.b_mn;
+  for (int s = 0; s < d.nseg; ++s) a3d = a3d && d.A[s].cols % 64 == 0;
+  for (int s = 0; s < nb; ++s) b3d = b3d && d.B[s].cols % 64 == 0;
+  // B chunks per load: the pair kernel's column half (2), or the whole (half) tile
+  const uint32_t b_chunks = pair ? 2u : static_cast<uint32_t>(d.paired ? BN / 128 : BN / 64);
   for (int s = 0; s < d.nseg; ++s) {
-    if (d.a_mn) TP_TRY(make_map(&prm.tmA[s], d.A[s], 64, 64));
+    if (a3d) TP_TRY(make_map_3d(&prm.tmA[s], d.A[s], 2));
+    else if (d.a_mn) TP_TRY(make_map(&prm.tmA[s], d.A[s], 64, 64));
     else TP_TRY(make_map(&prm.tmA[s], d.A[s], 64, BM));
   }
-  const int nb = d.paired ? 2 : d.nseg;
   for (int s = 0; s < nb; ++s) {
-    if (d.b_mn) TP_TRY(make_map(&prm.tmB[s], d.B[s], 64, 64));
+    if (b3d) TP_TRY(make_map_3d(&prm.tmB[s], d.B[s], b_chunks));
+    else if (d.b_mn) TP_TRY(make_map(&prm.tmB[s], d.B[s], 64, 64));
     else TP_TRY(make_map(&prm.tmB[s], d.B[s], 64, static_cast<uint32_t>(pair ? 128 : BN)));
   }
+  prm.a3d = a3d;
+  prm.b3d = b3d;
   for (int s = d.nseg; s < 3; ++s) prm.tmA[s] = prm.tmA[0];
   for (int s = nb; s < 3; ++s) prm.tmB[s] = prm.tmB[0];
   for (int s = 0; s < 3; ++s) prm.seg_k0[s] = static_cast<int>(d.seg_k0[s]);
