@@ -42,14 +42,33 @@ constexpr int kThreads = 192;
 #ifndef TP_MN_3D
 #define TP_MN_3D 1
 #endif
+// tcgen05.fence::after_thread_sync after every full-stage wait of the MMA thread
+// (copies and MMAs are both async-proxy operations ordered by the mbarrier itself,
+// so the fence is only required once per tile, after the accumulator handoff)
+#ifndef TP_KLOOP_FENCE
+#define TP_KLOOP_FENCE 0
+#endif
 constexpr bool kMn3d = TP_MN_3D != 0;
 constexpr int kGroupM = TP_GROUP_M;
 constexpr uint64_t kDrainTimeoutNs = 1000000000ull;
 
-template <int BN>
+// DEC: decode-sized problems (M <= 64 rows): only the first a_rows (<= 64) rows of
+// each A tile are loaded; the MMA still computes 128 rows, the rest of which read
+// whatever shared memory follows and are never stored (row m of D depends on row m
+// of A only). The smaller stages let two CTAs share an SM.
+// decode configuration: two CTAs per SM of 4 stages each keep more weight bytes in
+// flight than one CTA of 8 (the copies one producer thread keeps outstanding are
+// the limit at these sizes)
+#ifndef TP_DEC_STAGES
+#define TP_DEC_STAGES 4
+#endif
+#ifndef TP_DEC_CTAS_PER_SM
+#define TP_DEC_CTAS_PER_SM 2
+#endif
+template <int BN, bool DEC = false>
 struct TcCfg {
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
-  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int STAGES = DEC ? TP_DEC_STAGES : (BN == 256 ? 4 : 6);
+  static constexpr int A_BYTES = DEC ? 64 * BK * 2 : BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = 2 * BN;
@@ -63,6 +82,7 @@ struct TcParams {  // CUtensorMap members carry their own 128-byte alignment
   int64_t M, N, K;  // N counts logical output columns
   int a_mn, b_mn, nseg, paired, groups;
   int a3d, b3d;  // MN-major operand maps are 3-D (x: 64 columns, y: k, z: 64-column chunk)
+  int a_rows;    // rows of A loaded per tile by the decode configuration
   int seg_k0[3];
   int tiles_m, tiles_n, kb_per_seg;
   int shards, shard_axis;
@@ -84,7 +104,7 @@ struct TcParams {  // CUtensorMap members carry their own 128-byte alignment
 // [2] MMA waiting for a free accumulator, [3] epilogue waiting for an accumulator,
 // [4] epilogue busy, [5] MMA thread lifetime, [6] tiles, [7] producer lifetime.
 #ifdef TP_GEMM_STATS
-__device__ unsigned long long g_gemm_stats[1024][8];
+__device__ unsigned long long g_gemm_stats[1024][16];
 #define TP_STAT(i, v) atomicAdd(&g_gemm_stats[blockIdx.x][i], static_cast<unsigned long long>(v))
 #define TP_CLK() clock64()
 #else
@@ -207,9 +227,9 @@ __device__ __forceinline__ void epi8(const TcParams& p, int g, int64_t row, int6
   }
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool DEC>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
-  using C = TcCfg<BN>;
+  using C = TcCfg<BN, DEC>;
   constexpr int S = C::STAGES;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -217,6 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::STAGE_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+#ifdef TP_GEMM_STATS
+  __shared__ volatile long long issue_clk[8], commit_clk[8];
+#endif
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -270,7 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
-      const uint32_t stage_tx = C::STAGE_BYTES;
+      const uint32_t stage_tx =
+          DEC ? static_cast<uint32_t>(p.a_rows * BK * 2 + C::B_BYTES) : C::STAGE_BYTES;
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       [[maybe_unused]] const long long t_start = TP_CLK();
@@ -289,6 +313,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           const int k0 = p.seg_k0[seg] + static_cast<int>(tc.g * p.K) + (kb - seg * p.kb_per_seg) * BK;
           const uint32_t a_dst = sbase + stage * C::STAGE_BYTES;
           const uint32_t b_dst = a_dst + C::A_BYTES;
+#ifdef TP_GEMM_STATS
+          {
+            const long long now = clock64();
+            if (issued >= static_cast<uint32_t>(S)) TP_STAT(9, now - commit_clk[stage]);
+            issue_clk[stage] = now;
+          }
+#endif
           mbar_arrive_expect_tx(full_bar(stage), stage_tx);
           if (p.a_mn && p.a3d) {
             tma_load_3d(a_dst, &p.tmA[seg], full_bar(stage), 0, k0, m0 / 64);
@@ -358,7 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             break;
           }
           TP_STAT(1, TP_CLK() - tw);
-          tc_fence_after();
+#ifdef TP_GEMM_STATS
+          TP_STAT(8, clock64() - issue_clk[stage]);
+          TP_STAT(10, 1);
+#endif
+          if (TP_KLOOP_FENCE) tc_fence_after();
           const uint32_t a_addr = sbase + stage * C::STAGE_BYTES;
           const uint32_t b_addr = a_addr + C::A_BYTES;
 #pragma unroll
@@ -369,6 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           }
           mma_issued = true;
           mma_commit(empty_bar(stage));
+#ifdef TP_GEMM_STATS
+          commit_clk[stage] = clock64();
+#endif
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
@@ -477,6 +515,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 // remote arrives. At exit both CTAs wait for the pair's last MMAs, then for each
 // other, before freeing TMEM.
 
+#ifndef TP_PAIR_DUAL
+#define TP_PAIR_DUAL 1
+#endif
+// TP_PAIR_DUAL: a second producer warp (warp 6) issues the B copies while warp 0 issues A
+constexpr int kPairThreads = TP_PAIR_DUAL ? 224 : 192;
 constexpr int kPairStages = TP_PAIR_STAGES;
 constexpr int kPairStageBytes = 2 * 128 * BK * 2;  // A 128 x 64 + B 128 x 64, bf16
 constexpr int kPairBars = 2 * kPairStages + 7;
@@ -484,7 +527,7 @@ constexpr int kPairSmem = kPairStages * kPairStageBytes + 1024 + kPairBars * 8 +
 constexpr uint64_t kPairDrainNs = 20000000ull;
 
 template <int EPI>
-__global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(kPairThreads, 1) gemm_tc2_kernel(const __grid_constant__ TcParams p) {
   constexpr int S = kPairStages;
   constexpr int A_BYTES = 128 * BK * 2;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -493,6 +536,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * kPairStageBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kPairBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+#ifdef TP_GEMM_STATS
+  __shared__ volatile long long issue_clk[kPairStages], commit_clk[kPairStages];
+#endif
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -549,7 +595,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
   const int bn_logical = p.paired ? 128 : 256;
   uint32_t issued = 0;
 
-  if (warp == 0) {
+  if (warp == 0 || (TP_PAIR_DUAL && warp == 6)) {
+    const bool load_a = warp == 0;
+    const bool load_b = !TP_PAIR_DUAL || warp == 6;
     if (lane == 0) {
       // ------------------------------------------------------------ producer (both CTAs)
       uint32_t stage = 0, phase = 0;
@@ -573,8 +621,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
           const uint32_t a_dst = sbase + stage * kPairStageBytes;
           const uint32_t b_dst = a_dst + A_BYTES;
           const uint32_t fb = lead_full0 + 8u * stage;  // the even CTA's barrier
-          if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * kPairStageBytes);
-          if (p.a_mn && p.a3d) {
+#ifdef TP_GEMM_STATS
+          if (leader) {
+            const long long now = clock64();
+            if (issued >= static_cast<uint32_t>(S)) TP_STAT(9, now - commit_clk[stage]);
+            issue_clk[stage] = now;
+          }
+#endif
+          if (leader && load_a) mbar_arrive_expect_tx(full_bar(stage), 2 * kPairStageBytes);
+          if (!load_a) {
+          } else if (p.a_mn && p.a3d) {
             tma_load_3d_pair(a_dst, &p.tmA[seg], fb, 0, k0, m0 / 64);
           } else if (p.a_mn) {
             tma_load_2d_pair(a_dst, &p.tmA[seg], fb, m0, k0);
@@ -582,7 +638,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
           } else {
             tma_load_2d_pair(a_dst, &p.tmA[seg], fb, k0, m0);
           }
-          if (p.paired) {
+          if (!load_b) {
+          } else if (p.paired) {
             // even CTA: 128 gate columns, odd CTA: the same 128 up columns
             if (p.b3d) {
               tma_load_3d_pair(b_dst, &p.tmB[rank], fb, 0, k0, n0 / 64);
@@ -639,7 +696,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
             break;
           }
           TP_STAT(1, TP_CLK() - tw);
-          tc_fence_after();
+#ifdef TP_GEMM_STATS
+          TP_STAT(8, clock64() - issue_clk[stage]);
+          TP_STAT(10, 1);
+#endif
+          if (TP_KLOOP_FENCE) tc_fence_after();
           const uint32_t a_addr = sbase + stage * kPairStageBytes;
           const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
@@ -649,6 +710,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
             mma_bf16_ss_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           mma_commit_pair(empty_bar(stage), 0x3);
+#ifdef TP_GEMM_STATS
+          commit_clk[stage] = clock64();
+#endif
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
@@ -663,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc2_kernel(const __grid_cons
       if (!ok) record_timeout(p.status);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 6) {
     // -------------------------------------------------------------- epilogue (both CTAs)
     const int quad = warp & 3;
     const uint32_t remote_tempty0 = mapa_shared(tempty_bar(0), 0);
@@ -815,30 +879,30 @@ tp_status make_map_3d(CUtensorMap* m, const Operand& op, uint32_t chunks) {
   return TP_OK;
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool DEC>
 tp_status launch_bn_epi(const TcParams& prm, int grid, cudaStream_t st) {
-  auto kern = gemm_tc_kernel<BN, EPI>;
+  auto kern = gemm_tc_kernel<BN, EPI, DEC>;
   static bool attr_set = false;  // per instantiation; benign race (idempotent)
   if (!attr_set) {
     TP_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     TcCfg<BN>::SMEM_BYTES));
+                                     TcCfg<BN, DEC>::SMEM_BYTES));
     attr_set = true;
   }
-  kern<<<grid, kThreads, TcCfg<BN>::SMEM_BYTES, st>>>(prm);
+  kern<<<grid, kThreads, TcCfg<BN, DEC>::SMEM_BYTES, st>>>(prm);
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;
 }
 
-template <int BN>
+template <int BN, bool DEC>
 tp_status launch_bn(int epi, const TcParams& prm, int grid, cudaStream_t st) {
   switch (epi) {
-    case EPI_STORE: return launch_bn_epi<BN, EPI_STORE>(prm, grid, st);
-    case EPI_GELU: return launch_bn_epi<BN, EPI_GELU>(prm, grid, st);
-    case EPI_SWIGLU: return launch_bn_epi<BN, EPI_SWIGLU>(prm, grid, st);
-    case EPI_DGELU: return launch_bn_epi<BN, EPI_DGELU>(prm, grid, st);
-    case EPI_DSWIGLU: return launch_bn_epi<BN, EPI_DSWIGLU>(prm, grid, st);
-    case EPI_PAIR: return launch_bn_epi<BN, EPI_PAIR>(prm, grid, st);
+    case EPI_STORE: return launch_bn_epi<BN, EPI_STORE, DEC>(prm, grid, st);
+    case EPI_GELU: return launch_bn_epi<BN, EPI_GELU, DEC>(prm, grid, st);
+    case EPI_SWIGLU: return launch_bn_epi<BN, EPI_SWIGLU, DEC>(prm, grid, st);
+    case EPI_DGELU: return launch_bn_epi<BN, EPI_DGELU, DEC>(prm, grid, st);
+    case EPI_DSWIGLU: return launch_bn_epi<BN, EPI_DSWIGLU, DEC>(prm, grid, st);
+    case EPI_PAIR: return launch_bn_epi<BN, EPI_PAIR, DEC>(prm, grid, st);
   }
   return fail(TP_ERR_INVALID_ARG, "unknown epilogue");
 }
@@ -853,7 +917,7 @@ tp_status launch_pair_epi(const TcParams& prm, int64_t ntiles, cudaStream_t st) 
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(kPairThreads, 1, 1);
   cfg.dynamicSmemBytes = kPairSmem;
   cfg.stream = st;
   cfg.attrs = attr;
@@ -915,6 +979,9 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
   // 256 x 256 tiles on CTA pairs once there are at least 256 rows
   const bool pair = BN == 256 && d.M >= 256 && g_pair_mode.load() != 0;
   const int tile_m = pair ? 256 : BM;
+  // decode configuration: at most 64 K-major rows of A
+  const bool dec = !pair && BN == 128 && !d.a_mn && d.M <= 64;
+  const int a_rows = dec ? static_cast<int>((d.M + 7) / 8 * 8) : BM;
 
   TcParams prm;
   memset(&prm, 0, sizeof(prm));
@@ -928,7 +995,7 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
   for (int s = 0; s < d.nseg; ++s) {
     if (a3d) TP_TRY(make_map_3d(&prm.tmA[s], d.A[s], 2));
     else if (d.a_mn) TP_TRY(make_map(&prm.tmA[s], d.A[s], 64, 64));
-    else TP_TRY(make_map(&prm.tmA[s], d.A[s], 64, BM));
+    else TP_TRY(make_map(&prm.tmA[s], d.A[s], 64, static_cast<uint32_t>(a_rows)));
   }
   for (int s = 0; s < nb; ++s) {
     if (b3d) TP_TRY(make_map_3d(&prm.tmB[s], d.B[s], b_chunks));
@@ -937,6 +1004,7 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
   }
   prm.a3d = a3d;
   prm.b3d = b3d;
+  prm.a_rows = a_rows;
   for (int s = d.nseg; s < 3; ++s) prm.tmA[s] = prm.tmA[0];
   for (int s = nb; s < 3; ++s) prm.tmB[s] = prm.tmB[0];
   for (int s = 0; s < 3; ++s) prm.seg_k0[s] = static_cast<int>(d.seg_k0[s]);
@@ -973,8 +1041,11 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
   const int64_t ntiles = static_cast<int64_t>(prm.tiles_m) * prm.tiles_n * prm.groups;
   if (ntiles > (1ll << 30)) return fail(TP_ERR_SHAPE, "problem too large");
   if (pair) return launch_pair(epi, prm, ntiles, st);
-  const int grid = static_cast<int>(std::min<int64_t>(ntiles, device_sm_count()));
-  return BN == 256 ? launch_bn<256>(epi, prm, grid, st) : launch_bn<128>(epi, prm, grid, st);
+  const int grid = static_cast<int>(
+      std::min<int64_t>(ntiles, static_cast<int64_t>(device_sm_count()) * (dec ? TP_DEC_CTAS_PER_SM : 1)));
+  if (dec) return launch_bn<128, true>(epi, prm, grid, st);
+  return BN == 256 ? launch_bn<256, false>(epi, prm, grid, st)
+                   : launch_bn<128, false>(epi, prm, grid, st);
 }
 
 }  // namespace tp
@@ -983,10 +1054,10 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
 // Instrumented builds only: copy out and clear the wait-cycle counters.
 extern "C" TP_API int tp_debug_gemm_stats(unsigned long long* out, int ctas) {
   if (ctas > 1024) ctas = 1024;
-  if (cudaMemcpyFromSymbol(out, tp::g_gemm_stats, sizeof(unsigned long long) * 8 * ctas) !=
+  if (cudaMemcpyFromSymbol(out, tp::g_gemm_stats, sizeof(unsigned long long) * 16 * ctas) !=
       cudaSuccess)
     return 1;
-  static unsigned long long zero[1024][8];
+  static unsigned long long zero[1024][16];
   return cudaMemcpyToSymbol(tp::g_gemm_stats, zero, sizeof(zero)) == cudaSuccess ? 0 : 1;
 }
 #endif

@@ -85,12 +85,15 @@ struct GemmDesc {
 };
 
 tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st);    // bf16, tcgen05
+bool gemv_eligible(const GemmDesc& d);                             // bf16, M <= 4
+tp_status launch_gemv(const GemmDesc& d, cudaStream_t st);
 tp_status launch_gemm_simt(const GemmDesc& d, cudaStream_t st);  // fp32, CUDA cores
 tp_status launch_shard_reduce(const float* P, const void* residual, void* out, int N,
                               int64_t M, int64_t n, tp_dtype out_dtype, cudaStream_t st);
 
 inline tp_status launch_gemm(const GemmDesc& d, cudaStream_t st) {
-  return d.dtype == TP_BF16 ? launch_gemm_tc(d, st) : launch_gemm_simt(d, st);
+  if (d.dtype != TP_BF16) return launch_gemm_simt(d, st);
+  return gemv_eligible(d) ? launch_gemv(d, st) : launch_gemm_tc(d, st);
 }
 
 // ------------------------------------------------------------------ other kernels

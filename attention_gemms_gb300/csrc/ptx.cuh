@@ -54,15 +54,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Bounded wait for the phase with parity `parity` to complete. Gives up after
 // `timeout_ns` nanoseconds (%globaltimer) of waiting, or as soon as another role
 // of the CTA has given up (`*abort` != 0); sets *abort and returns false then.
+#ifndef TP_WAIT_GLOBALTIMER
+#define TP_WAIT_GLOBALTIMER 0
+#endif
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
                                           volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
+  // fast path: plain polls (each try_wait may suspend the thread until the phase
+  // completes or a short hardware time limit passes)
+#pragma unroll 1
+  for (int i = 0; i < 16; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+#if TP_WAIT_GLOBALTIMER
   const uint64_t t0 = globaltimer_ns();
+#else
+  // the SM clock bounds the wait: timeout_ns at most 2 GHz worth of cycles, so the
+  // limit in wall time is timeout_ns or longer when the clock runs slower
+  const long long c0 = clock64();
+  const long long limit = static_cast<long long>(timeout_ns) * 2;
+#endif
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 31u) == 0) {  // the abort flag and the clock are checked every 32 polls
       if (*abort) return false;
+#if TP_WAIT_GLOBALTIMER
       if (globaltimer_ns() - t0 > timeout_ns) {
+#else
+      if (clock64() - c0 > limit) {
+#endif
         *abort = 1;
         return false;
       }
@@ -90,13 +108,29 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
 // The same load issued by either CTA of a pair, completing on the mbarrier at
 // shared::cluster address `bar`, which may be in the peer CTA (the even CTA's
 // barrier, so that it sees both halves of a stage arrive).
+#ifndef TP_TMA_HINT
+#define TP_TMA_HINT 0
+#endif
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar,
                                                  int32_t x, int32_t y) {
+#if TP_TMA_HINT
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "l"(l2_evict_last_policy())
+      : "memory");
+#else
   asm volatile(
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y)
       : "memory");
+#endif
 }
 
 // 3-D tiled loads (x innermost): used to fetch several 64-wide column chunks of an
@@ -111,11 +145,20 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
 }
 __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar,
                                                  int32_t x, int32_t y, int32_t z) {
+#if TP_TMA_HINT
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z),
+      "l"(l2_evict_last_policy())
+      : "memory");
+#else
   asm volatile(
       "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z)
       : "memory");
+#endif
 }
 
 // ------------------------------------------------------------------ tcgen05
