@@ -79,8 +79,8 @@ def col_gemm_flops(w):
 # from an ncu capture of the full-size workload, valid only for the kernel source it
 # was taken on (sha256 of csrc/gemm_tc.cu); see profiles/.
 COL_GEMM_TRAFFIC = {
-    "c5": {"bytes": 6.55e9 + 1.42e9, "src": "43985879dda58388"},
-    "c3": {"bytes": 755.52e6 + 503.90e6, "src": "43985879dda58388"},
+    "c5": {"bytes": 8.61e9 + 1.41e9, "src": "596f461bf51440fd"},
+    "c3": {"bytes": 1.04e9 + 505.75e6, "src": "596f461bf51440fd"},
 }
 
 
@@ -565,7 +565,7 @@ def run_decode(args, device, T):
         # GPU idles, e.g. during the CPU baseline, and take a moment to come back
         t_w = time.time()
         n_w = 0
-        while n_w < args.warmup or time.time() - t_w < 0.2:
+        while n_w < args.warmup or time.time() - t_w < args.decode_warmup_ms * 1e-3:
             g.replay()
             n_w += 1
             if n_w % 50 == 0:
@@ -604,6 +604,37 @@ def run_decode(args, device, T):
         }
         del g
     return res
+
+
+def run_decode_only(args):
+    """The decode sweep as the main line: value = the lowest GB/s over the token counts."""
+    import torch
+    from attention_gemms_gb300 import build as B
+    from attention_gemms_gb300 import tpmlp as T
+    ws_, rank, local = dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps({"impl": "reference", "unavailable": "the decode sweep has no CPU "
+                              "arm of its own; time --workload c5/c3 for the oracle"}))
+        return
+    if ws_ > 1:
+        torch.cuda.set_device(local)
+    dist_init("nccl")
+    B.build()
+    T.lib()
+    device = torch.device("cuda", torch.cuda.current_device())
+    barrier()
+    d = run_decode(args, device, T)
+    worst = min(v["GBps"] for v in d["per_tokens"].values())
+    worst = max_over_ranks(-worst, device) * -1.0
+    if rank == 0:
+        peak = d["peak"]
+        print(json.dumps({"metric": METRIC, "value": round(worst * ws_, 1), "unit": "GB/s",
+                          "n_gpus": ws_, "steps": args.steps, "warmup": args.warmup,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                          "dtype": "bf16", "data": "synthetic (seeded)",
+                          "config": {"workload": DECODE["desc"], "tokens": list(DECODE["tokens"])},
+                          "pct_of_peak": round(100 * worst / peak, 1), "decode": d}), flush=True)
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -708,9 +739,9 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="c5", choices=sorted(WORKLOADS),
+    ap.add_argument("--workload", default="c5", choices=sorted(WORKLOADS) + ["c4"],
                     help="c5 (default): large SwiGLU MLP; c3: GELU MLP; c2: page-2 layer; "
-                         "c1: tiny fp32 MLP; c5-2k: profiling case")
+                         "c1: tiny fp32 MLP; c4: decode sweep only; c5-2k: profiling case")
     ap.add_argument("--mode", default="splitk", choices=["splitk", "buffers"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-rows", type=int, default=64)
@@ -719,9 +750,13 @@ def main(argv=None):
     ap.add_argument("--decode", dest="decode", action="store_true", default=True,
                     help="also run the decode GEMV sweep (default)")
     ap.add_argument("--no-decode", dest="decode", action="store_false")
+    ap.add_argument("--decode-warmup-ms", type=float, default=200.0,
+                    help="minimum warm-up time of each decode token count (clocks ramp up)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.workload == "c4":
+        return run_decode_only(args)
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
