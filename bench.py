@@ -77,17 +77,22 @@ def col_gemm_flops(w):
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one column-GEMM launch,
 # from an ncu capture of the full-size workload, valid only for the kernel source it
-# was taken on (sha256 of csrc/gemm_tc.cu); see profiles/.
+# was taken on (sha256 of csrc/gemm_tc.cu + csrc/ptx.cuh); see profiles/.
 COL_GEMM_TRAFFIC = {
-    "c5": {"bytes": 8.61e9 + 1.41e9, "src": "596f461bf51440fd"},
-    "c3": {"bytes": 1.04e9 + 505.75e6, "src": "596f461bf51440fd"},
+    "c5": {"bytes": 9.16e9 + 1.41e9, "src": "e04ea258919ab47a"},
+    "c3": {"bytes": 1.05e9 + 505.88e6, "src": "e04ea258919ab47a"},
 }
 
 
 def _kernel_source_hash():
+    """Hash of the tensor-core GEMM's source (kernel and its PTX wrappers): a stored
+    traffic figure is reported only while the kernel it was measured on is unchanged."""
     import hashlib
-    with open(os.path.join(ROOT, "attention_gemms_gb300", "csrc", "gemm_tc.cu"), "rb") as fh:
-        return hashlib.sha256(fh.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for name in ("gemm_tc.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "attention_gemms_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def col_gemm_traffic(workload):
