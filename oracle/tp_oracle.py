@@ -327,6 +327,20 @@ def layernorm_bwd(x, gamma, dy, eps=LN_EPS):
     return dx, (dy * xhat).sum(axis=red), dy.sum(axis=red)
 
 
+def shard_reduce_ln(partials, residual, gamma, beta, eps=LN_EPS):
+    """The shard sum, then LayerNorm of its full-width result.
+
+    x = sum_i Z_i (+ residual) is what the all-reduce leaves on every rank; LN
+    needs the statistics of the whole hidden width, so it can only run after the
+    sum [张量并行 notes, §相关分析, forward bottleneck before LayerNorm]. Shards are
+    summed in order 0..N-1 (`shard_reduce`), then `layernorm_fwd`.
+    Returns (x, y, mu, rstd).
+    """
+    x = shard_reduce(partials, residual)
+    y, mu, rstd = layernorm_fwd(x, gamma, beta, eps)
+    return x, y, mu, rstd
+
+
 # ---------------------------------------------------------------- attention
 
 def softmax_rows(S):

@@ -55,3 +55,28 @@ def test_tanh_gelu_is_caught(monkeypatch):
     import pytest
     with pytest.raises(AssertionError):
         pins.test_gelu_phi_table()
+
+
+def test_ln_before_sum_is_caught(monkeypatch):
+    """LN applied to each shard's partial and the results summed: what the notes
+    rule out (the statistics need the whole sum)."""
+    def bad(partials, residual, gamma, beta, eps=O.LN_EPS):
+        parts = [O.layernorm_fwd(P, gamma, beta, eps)[0] for P in partials]
+        x = O.shard_reduce(partials, residual)
+        _, mu, rs = O.layernorm_fwd(x, gamma, beta, eps)
+        return x, O.shard_reduce(parts, residual), mu, rs
+    monkeypatch.setattr(O, "shard_reduce_ln", bad)
+    import pytest
+    with pytest.raises(AssertionError):
+        pins.test_shard_reduce_ln_bruteforce()
+
+
+def test_residual_dropped_before_ln_is_caught(monkeypatch):
+    def bad(partials, residual, gamma, beta, eps=O.LN_EPS):
+        x = O.shard_reduce(partials, residual)
+        y, mu, rs = O.layernorm_fwd(O.shard_reduce(partials), gamma, beta, eps)
+        return x, y, mu, rs
+    monkeypatch.setattr(O, "shard_reduce_ln", bad)
+    import pytest
+    with pytest.raises(AssertionError):
+        pins.test_shard_reduce_ln_equals_ln_of_unsplit_row_gemm()

@@ -291,6 +291,60 @@ def test_layernorm_bwd_fd():
     assert O.rel_err(db, _fd(loss, beta)) <= 1e-7
 
 
+def _ln_row_loops(v, g, b, eps):
+    """LayerNorm of one row in scalar Python: mean, biased variance, normalise."""
+    n = len(v)
+    mu = sum(v) / n
+    var = sum((t - mu) * (t - mu) for t in v) / n
+    rs = 1.0 / math.sqrt(var + eps)
+    return [g[c] * (v[c] - mu) * rs + b[c] for c in range(n)], mu, rs
+
+
+def test_shard_reduce_ln_bruteforce():
+    """Sum of the shards and LN of the result, element by element in plain loops."""
+    r = _rng(40)
+    N, M, h = 3, 4, 8
+    P = [r.normal(size=(M, h)) for _ in range(N)]
+    R, g, b = r.normal(size=(M, h)), r.normal(size=h), r.normal(size=h)
+    x, y, mu, rstd = O.shard_reduce_ln(P, R, g, b)
+    for m in range(M):
+        row = [sum(P[i][m, c] for i in range(N)) + R[m, c] for c in range(h)]
+        yr, mr, rr = _ln_row_loops(row, g, b, 1e-5)
+        assert max(abs(x[m, c] - row[c]) for c in range(h)) <= 1e-14
+        assert max(abs(y[m, c] - yr[c]) for c in range(h)) <= 1e-12
+        assert abs(mu[m] - mr) <= 1e-14 and abs(rstd[m] - rr) <= 1e-12 * rr
+
+
+def test_shard_reduce_ln_equals_ln_of_unsplit_row_gemm():
+    """LN after the all-reduce of the row-parallel partials = LN of the unsplit
+    product (block identity of the row split, then the same LN)."""
+    r = _rng(41)
+    H, W, R = r.normal(size=(6, 12)), r.normal(size=(12, 8)), r.normal(size=(6, 8))
+    g, b = r.normal(size=8), r.normal(size=8)
+    for N in (1, 2, 3, 4):
+        x, y, _, _ = O.shard_reduce_ln(O.row_partials(H, W, N), R, g, b)
+        Z = H @ W + R
+        assert O.rel_err(x, Z) <= 1e-13
+        yr = np.array([_ln_row_loops(list(Z[m]), g, b, 1e-5)[0] for m in range(6)])
+        assert O.rel_err(y, yr) <= 1e-12
+
+
+def test_shard_reduce_ln_shift_and_constant_rows():
+    """LN ignores a constant added to a whole row (through any shard), and maps a
+    constant row to beta."""
+    r = _rng(42)
+    P = [r.normal(size=(3, 16)) for _ in range(2)]
+    g, b = r.normal(size=16), r.normal(size=16)
+    _, y0, mu0, rs0 = O.shard_reduce_ln(P, None, g, b)
+    Q = [P[0], P[1] + np.array([[5.0], [-2.0], [0.25]])]
+    x1, y1, mu1, rs1 = O.shard_reduce_ln(Q, None, g, b)
+    assert O.rel_err(y1, y0) <= 1e-12 and np.allclose(rs1, rs0, rtol=1e-12)
+    assert np.allclose(mu1 - mu0, [5.0, -2.0, 0.25], atol=1e-13)
+    C = [np.full((2, 16), 0.75), np.full((2, 16), -2.0)]
+    _, yc, muc, _ = O.shard_reduce_ln(C, np.full((2, 16), 0.5), g, b)
+    assert np.allclose(muc, -0.75, atol=1e-15) and np.allclose(yc, b, atol=1e-15)
+
+
 # ---------------------------------------------------------------- attention
 
 def test_attention_closed_forms():
