@@ -502,6 +502,73 @@ def layer_bwd(x, b, s, p, n_heads, N, dout, causal=False):
             "dW1": g["dW1"], "dW2": g["dW2"]}
 
 
+# ---------------------------------------------------------------- sequence parallelism
+
+def seq_slices(M, N):
+    """Rows that virtual rank r holds in the sequence-parallel regions:
+    [r*M/N, (r+1)*M/N). Reading taken: token rows are ordered so that each rank's
+    piece of the sequence is one contiguous block (M % N == 0)."""
+    if M % N:
+        raise ValueError("sequence parallelism needs M % N == 0")
+    m = M // N
+    return [slice(r * m, (r + 1) * m) for r in range(N)]
+
+
+def _sp_mlp(xn, W1, W2, N, act, W1u):
+    if act == "gelu":
+        return mlp_gelu_fwd(xn, W1, W2, N)
+    return mlp_swiglu_fwd(xn, W1, W1u, W2, N)
+
+
+def sp_mlp_block_fwd(x, gamma, beta, W1, W2, N, act="gelu", W1u=None, eps=LN_EPS):
+    """Pre-LN MLP sub-block, out = x + MLP(LN(x)), in its sequence-parallel form
+    [20260402-parallelism, §5 Sequence Parallelism]:
+      rank r holds only its rows x_r of the LayerNorm / residual activations and
+      normalises them (LN on 1/N of the rows); an all-gather assembles the full
+      LN output for the tensor-parallel MLP (column split, then row split); the
+      all-reduce that would end the MLP is split into its reduce-scatter half, so
+      rank r receives only its rows of sum_i Z_i and adds its residual rows.
+    Returns xn (gathered), mean, rstd, the MLP's saved activations and out (the
+    ranks' slices stacked in rank order)."""
+    sl = seq_slices(x.shape[0], N)
+    ln = [layernorm_fwd(x[q], gamma, beta, eps) for q in sl]           # LN(1/N) per rank
+    xn = np.concatenate([t[0] for t in ln], axis=0)                     # all-gather
+    m = _sp_mlp(xn, W1, W2, N, act, W1u)                                # TP MLP, per shard
+    out = np.concatenate([m["Z"][q] + x[q] for q in sl], axis=0)        # reduce-scatter + x_r
+    return {"xn": xn, "mean": np.concatenate([t[1] for t in ln]),
+            "rstd": np.concatenate([t[2] for t in ln]), "mlp": m, "out": out}
+
+
+def sp_mlp_block_bwd(x, gamma, beta, W1, W2, N, dout, act="gelu", W1u=None, eps=LN_EPS):
+    """Backward of `sp_mlp_block_fwd`. The backward of the reduce-scatter is an
+    all-gather of dout (every shard reads the whole dZ); the backward of the
+    all-gather is a reduce-scatter of the MLP's input gradient, so rank r gets
+    dxn_r = (sum_i dX_i)[rows of r]; LN backward runs per rank on its rows, plus
+    the residual's dout_r. Each rank's LN parameters only see its own rows, so
+    the ranks' gamma / beta gradients differ and are summed over the ranks (an
+    all-reduce) -- unlike the replicated LN of plain tensor parallelism, whose
+    gradients agree on every rank [张量并行 notes, §相关分析]."""
+    f = sp_mlp_block_fwd(x, gamma, beta, W1, W2, N, act, W1u, eps)
+    sl = seq_slices(x.shape[0], N)
+    dZ = np.concatenate([dout[q] for q in sl], axis=0)                   # all-gather
+    if act == "gelu":
+        g = mlp_gelu_bwd(f["xn"], W1, W2, dZ, N)
+        res = {"dW1": g["dW1"], "dW2": g["dW2"]}
+    else:
+        g = mlp_swiglu_bwd(f["xn"], W1, W1u, W2, dZ, N)
+        res = {"dW1": g["dWg"], "dW1u": g["dWu"], "dW2": g["dWd"]}
+    dx, dgr, dbr = [], [], []
+    for q in sl:
+        dxr, dg, db = layernorm_bwd(x[q], gamma, g["dX"][q], eps)      # reduce-scatter rows
+        dx.append(dxr + dout[q])
+        dgr.append(dg)
+        dbr.append(db)
+    res.update({"dx": np.concatenate(dx, axis=0), "dgamma_ranks": np.stack(dgr),
+                "dbeta_ranks": np.stack(dbr), "dgamma": shard_reduce(dgr),
+                "dbeta": shard_reduce(dbr)})
+    return res
+
+
 def rel_err(got, ref):
     """max|got - ref| / max|ref| -- the parity metric."""
     got = np.asarray(got, dtype=np.float64)

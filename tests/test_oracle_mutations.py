@@ -80,3 +80,44 @@ def test_residual_dropped_before_ln_is_caught(monkeypatch):
     import pytest
     with pytest.raises(AssertionError):
         pins.test_shard_reduce_ln_equals_ln_of_unsplit_row_gemm()
+
+
+def test_sp_missing_residual_grad_is_caught(monkeypatch):
+    """The block's input gradient without the residual's dout_r term."""
+    real_sp = O.sp_mlp_block_bwd
+
+    def bad(x, gamma, beta, W1, W2, N, dout, act="gelu", W1u=None, eps=O.LN_EPS):
+        res = real_sp(x, gamma, beta, W1, W2, N, dout, act, W1u, eps)
+        res["dx"] = res["dx"] - dout
+        return res
+    monkeypatch.setattr(O, "sp_mlp_block_bwd", bad)
+    import pytest
+    with pytest.raises(AssertionError):
+        pins.test_sp_mlp_block_equals_unsplit_and_fd("gelu", 2)
+
+
+def test_sp_rank_gradient_not_summed_is_caught(monkeypatch):
+    """Taking rank 0's LN gradient as if it were replicated (no sum over ranks)."""
+    real_sp = O.sp_mlp_block_bwd
+
+    def bad(x, gamma, beta, W1, W2, N, dout, act="gelu", W1u=None, eps=O.LN_EPS):
+        res = real_sp(x, gamma, beta, W1, W2, N, dout, act, W1u, eps)
+        res["dgamma"] = res["dgamma_ranks"][0]
+        return res
+    monkeypatch.setattr(O, "sp_mlp_block_bwd", bad)
+    import pytest
+    with pytest.raises(AssertionError):
+        pins.test_sp_mlp_block_equals_unsplit_and_fd("gelu", 2)
+
+
+def test_sp_rank_rows_swapped_is_caught(monkeypatch):
+    """Reduce-scatter handing rank r the rows of rank r+1."""
+    real = O.seq_slices
+
+    def bad(M, N):
+        s = real(M, N)
+        return s[1:] + s[:1]
+    monkeypatch.setattr(O, "seq_slices", bad)
+    import pytest
+    with pytest.raises(AssertionError):
+        pins.test_sp_mlp_block_equals_unsplit_and_fd("gelu", 2)

@@ -425,3 +425,77 @@ def test_qkv_shard_columns_cover_once():
     for N in (1, 2, 4, 8):
         cols = np.concatenate([O.qkv_shard_columns(h, heads, N, i) for i in range(N)])
         assert sorted(cols.tolist()) == list(range(3 * h))
+
+
+# ---------------------------------------------------------------- sequence parallelism
+
+def _block_unsplit(x, g, b, W1, W2, act, W1u):
+    """x + MLP(LN(x)) on one device, written with the plain operators."""
+    mu = x.mean(axis=1, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=1, keepdims=True)
+    xn = g * (x - mu) / np.sqrt(var + 1e-5) + b
+    if act == "gelu":
+        return x + O.gelu(xn @ W1) @ W2
+    return x + (O.silu(xn @ W1) * (xn @ W1u)) @ W2
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+@pytest.mark.parametrize("N", [1, 2, 4])
+def test_sp_mlp_block_equals_unsplit_and_fd(act, N):
+    r = _rng(50)
+    M, h, f = 8, 4, 8
+    x, g, b = r.normal(size=(M, h)), r.normal(size=h), r.normal(size=h)
+    W1, W2, W1u = r.normal(size=(h, f)), r.normal(size=(f, h)), r.normal(size=(h, f))
+    dout = r.normal(size=(M, h))
+    u = W1u if act == "swiglu" else None
+    fw = O.sp_mlp_block_fwd(x, g, b, W1, W2, N, act, u)
+    assert O.rel_err(fw["out"], _block_unsplit(x, g, b, W1, W2, act, u)) <= 1e-13
+    bw = O.sp_mlp_block_bwd(x, g, b, W1, W2, N, dout, act, u)
+    loss = lambda: float(np.sum(_block_unsplit(x, g, b, W1, W2, act, u) * dout))
+    assert O.rel_err(bw["dx"], _fd(loss, x)) <= 1e-7
+    assert O.rel_err(bw["dgamma"], _fd(loss, g)) <= 1e-7
+    assert O.rel_err(bw["dbeta"], _fd(loss, b)) <= 1e-7
+    assert O.rel_err(bw["dW1"], _fd(loss, W1)) <= 1e-7
+    assert O.rel_err(bw["dW2"], _fd(loss, W2)) <= 1e-7
+    if act == "swiglu":
+        assert O.rel_err(bw["dW1u"], _fd(loss, W1u)) <= 1e-7
+
+
+def test_sp_rank_gradients_are_per_rank_parameter_gradients():
+    """dgamma_ranks[r] is the gradient with respect to rank r's own copy of gamma
+    (every rank normalises its rows with its copy), checked by finite differences
+    on a block whose LN uses a separate gamma / beta per row slice."""
+    r = _rng(51)
+    M, h, f, N = 6, 4, 6, 3
+    x, W1, W2 = r.normal(size=(M, h)), r.normal(size=(h, f)), r.normal(size=(f, h))
+    gs, bs = r.normal(size=(N, h)), r.normal(size=(N, h))
+    dout = r.normal(size=(M, h))
+
+    def loss():
+        rows = np.concatenate([np.repeat(gs[k][None], M // N, 0) for k in range(N)])
+        brow = np.concatenate([np.repeat(bs[k][None], M // N, 0) for k in range(N)])
+        return float(np.sum(_block_unsplit(x, rows, brow, W1, W2, "gelu", None) * dout))
+    # with equal copies the per-copy gradients are the oracle's per-rank partials
+    gs[:] = gs[0]
+    bs[:] = bs[0]
+    bw = O.sp_mlp_block_bwd(x, gs[0].copy(), bs[0].copy(), W1, W2, N, dout)
+    assert O.rel_err(bw["dgamma_ranks"], _fd(loss, gs)) <= 1e-7
+    assert O.rel_err(bw["dbeta_ranks"], _fd(loss, bs)) <= 1e-7
+    assert np.allclose(bw["dgamma_ranks"].sum(axis=0), bw["dgamma"], rtol=1e-13, atol=1e-13)
+
+
+def test_sp_output_rows_depend_only_on_own_rank_rows():
+    """LN and the MLP act token by token, so rank r's output rows depend only on
+    its own input rows (the reduce-scatter hands each rank exactly those)."""
+    r = _rng(52)
+    M, h, f, N = 8, 4, 8, 4
+    x, g, b = r.normal(size=(M, h)), r.normal(size=h), r.normal(size=h)
+    W1, W2 = r.normal(size=(h, f)), r.normal(size=(f, h))
+    o0 = O.sp_mlp_block_fwd(x, g, b, W1, W2, N)["out"]
+    x2 = x.copy()
+    x2[2:4] += 1.5  # rank 1's rows
+    o1 = O.sp_mlp_block_fwd(x2, g, b, W1, W2, N)["out"]
+    assert np.array_equal(o0[:2], o1[:2]) and np.array_equal(o0[4:], o1[4:])
+    assert not np.allclose(o0[2:4], o1[2:4])
+    with pytest.raises(ValueError):
+        O.seq_slices(7, 2)
