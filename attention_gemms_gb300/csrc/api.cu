@@ -108,6 +108,35 @@ tp_status row_impl(const void* Xs, const void* W, const void* residual, void* ou
   return launch_shard_reduce(static_cast<const float*>(ws), residual, out, N, M, n, dt, st);
 }
 
+// sum_out = sum_i Xs_i W_i (+ residual), y = LN(sum_out): variant A fuses the LN into
+// the reduction of the partials; variant B folds the sum in the GEMM, then runs LN
+tp_status row_ln_impl(const void* Xs, const void* W, const void* residual, const float* gamma,
+                      const float* beta, void* sum_out, void* y, float* mean, float* rstd,
+                      int64_t M, int64_t k, int64_t n, int32_t N, float eps, tp_dtype dt,
+                      tp_reduce mode, void* ws, cudaStream_t st) {
+  if (mode == TP_REDUCE_SPLITK) {
+    TP_TRY(row_impl(Xs, W, residual, sum_out, M, k, n, N, dt, mode, ws, st));
+    return launch_layernorm_fwd(sum_out, gamma, beta, y, mean, rstd, M, n, eps, dt, st);
+  }
+  GemmDesc d;
+  d.dtype = dt;
+  d.M = M;
+  d.N = n;
+  d.K = k / N;
+  d.groups = N;
+  d.A[0] = {Xs, M, k, k};
+  d.B[0] = {W, k, n, n};
+  d.b_mn = true;
+  d.ldo = n;
+  d.epi = EPI_STORE;
+  d.out[0] = ws;
+  d.out_f32 = true;
+  d.out_group_stride = M * n;
+  TP_TRY(launch_gemm(d, st));
+  return launch_shard_reduce_ln(static_cast<const float*>(ws), residual, gamma, beta, sum_out, y,
+                                mean, rstd, N, M, n, eps, dt, st);
+}
+
 // dX = sum_i sum_s dA_s,i B_s,i^T over nseg operand pairs (dY with W1, or dG/dU with Wg/Wu)
 tp_status dx_impl(const void* const* dA, const void* const* Wt, int nseg, void* dX, int64_t M,
                   int64_t h, int64_t f, int32_t N, tp_dtype dt, tp_reduce mode, void* ws,
@@ -168,6 +197,8 @@ size_t tp_workspace_size(tp_op op, int64_t M, int64_t h, int64_t f, int32_t N, t
     case TP_OP_LAYERNORM_BWD: return layernorm_bwd_ws_bytes(M, h);
     case TP_OP_LAYER_FWD: return layer_workspace_size(true, M, h, f, N, dtype, mode);
     case TP_OP_LAYER_BWD: return layer_workspace_size(false, M, h, f, N, dtype, mode);
+    case TP_OP_SP_MLP_FWD: return sp_mlp_workspace_size(true, M, h, f, N, dtype, act, mode);
+    case TP_OP_SP_MLP_BWD: return sp_mlp_workspace_size(false, M, h, f, N, dtype, act, mode);
     default: return 0;
   }
 }
@@ -249,6 +280,54 @@ tp_status tp_shard_reduce(const float* partials, const void* residual, void* out
   TP_TRY(check_device());
   return launch_shard_reduce(partials, residual, out, N, M, n, out_dtype,
                              static_cast<cudaStream_t>(stream));
+}
+
+tp_status tp_shard_reduce_ln(const float* partials, const void* residual, const float* gamma,
+                             const float* beta, void* sum_out, void* y, float* mean, float* rstd,
+                             int32_t N, int64_t M, int64_t h, float eps, tp_dtype dtype,
+                             void* stream) {
+  TP_TRY(check_dtype(dtype));
+  TP_TRY(need(partials && gamma && beta && y, TP_ERR_INVALID_ARG,
+              "partials, gamma, beta and y are required"));
+  TP_TRY(need(N >= 1 && M >= 0 && h >= 1 && eps >= 0.0f, TP_ERR_INVALID_ARG,
+              "need N >= 1, M >= 0, h >= 1, eps >= 0"));
+  TP_TRY(need(h % 8 == 0 && h <= kReduceLnMaxH, TP_ERR_SHAPE,
+              "fused reduce + LayerNorm: h must be a multiple of 8 and at most 16384"));
+  TP_TRY(check_aligned({partials, residual, gamma, beta, sum_out, y, mean, rstd}));
+  if (M == 0) return TP_OK;
+  TP_TRY(check_device());
+  return launch_shard_reduce_ln(partials, residual, gamma, beta, sum_out, y, mean, rstd, N, M, h,
+                                eps, dtype, static_cast<cudaStream_t>(stream));
+}
+
+tp_status tp_row_linear_ln(const void* Xs, const void* W, const void* residual,
+                           const float* gamma, const float* beta, void* sum_out, void* y,
+                           float* mean, float* rstd, int64_t M, int64_t k, int64_t n, int32_t N,
+                           float eps, tp_dtype dtype, tp_reduce mode, void* ws, size_t ws_bytes,
+                           void* stream) {
+  TP_TRY(check_dtype(dtype));
+  TP_TRY(need(mode == TP_REDUCE_BUFFERS || mode == TP_REDUCE_SPLITK, TP_ERR_INVALID_ARG,
+              "unknown reduce mode"));
+  TP_TRY(need(Xs && W && gamma && beta && sum_out && y, TP_ERR_INVALID_ARG,
+              "Xs, W, gamma, beta, sum_out and y are required"));
+  TP_TRY(need(N >= 1, TP_ERR_INVALID_ARG, "shard count N must be >= 1"));
+  TP_TRY(need(M >= 0 && k >= 1 && n >= 1 && eps >= 0.0f, TP_ERR_INVALID_ARG,
+              "sizes must be positive (M >= 0) and eps >= 0"));
+  TP_TRY(need(k % N == 0, TP_ERR_SHAPE, "k must be divisible by the shard count N"));
+  TP_TRY(need(n % 8 == 0 && n <= kReduceLnMaxH, TP_ERR_SHAPE,
+              "fused reduce + LayerNorm: n must be a multiple of 8 and at most 16384"));
+  if (dtype == TP_BF16) {
+    TP_TRY(need((k / N) % 64 == 0, TP_ERR_SHAPE, "bf16 path: k/N must be a multiple of 64"));
+    TP_TRY(need(n % 64 == 0, TP_ERR_SHAPE, "bf16 path: n must be a multiple of 64"));
+  }
+  TP_TRY(check_aligned({Xs, W, residual, gamma, beta, sum_out, y, mean, rstd, ws}));
+  if (M == 0) return TP_OK;
+  const size_t need_ws = partial_bytes(M, n, N, mode);
+  TP_TRY(need(ws_bytes >= need_ws && (need_ws == 0 || ws), TP_ERR_WORKSPACE,
+              "workspace smaller than tp_workspace_size"));
+  TP_TRY(check_device());
+  return row_ln_impl(Xs, W, residual, gamma, beta, sum_out, y, mean, rstd, M, k, n, N, eps, dtype,
+                     mode, ws, static_cast<cudaStream_t>(stream));
 }
 
 tp_status tp_mlp_fwd(const void* X, const void* W1, const void* W1_up, const void* W2,

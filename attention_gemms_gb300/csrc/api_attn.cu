@@ -66,6 +66,32 @@ size_t layer_workspace_size(bool fwd, int64_t M, int64_t h, int64_t f, int32_t N
   return 2 * a256(M * h * e) + rest;
 }
 
+// Validation and the part of the attention block before W_o: LN1, QKV, attention.
+tp_status attn_core_fwd(const void* x, const float* gamma, const float* beta, const void* Wqkv,
+                        const void* Wo, void* xn, float* mean, float* rstd, void* qkv, void* o,
+                        float* lse, void* out, int64_t b, int64_t s, int64_t h, int32_t n_heads,
+                        int32_t N, int causal, tp_dtype dtype, tp_reduce mode, void* ws,
+                        size_t ws_bytes, void* stream) {
+  TP_TRY(check_dtype(dtype));
+  TP_TRY(need(mode == TP_REDUCE_BUFFERS || mode == TP_REDUCE_SPLITK, TP_ERR_INVALID_ARG,
+              "unknown reduce mode"));
+  TP_TRY(need(x && gamma && beta && Wqkv && Wo && xn && mean && rstd && qkv && o && lse && out,
+              TP_ERR_INVALID_ARG, "all tensors of tp_attn_proj_fwd are required"));
+  TP_TRY(check_attn_shape(b, s, h, n_heads, N, dtype));
+  TP_TRY(check_aligned({x, gamma, beta, Wqkv, Wo, xn, mean, rstd, qkv, o, lse, out, ws}));
+  const int64_t M = b * s;
+  if (M == 0) return TP_OK;
+  const size_t need_ws = partial_bytes(M, h, N, mode);
+  TP_TRY(need(ws_bytes >= need_ws && (need_ws == 0 || ws), TP_ERR_WORKSPACE,
+              "workspace smaller than tp_workspace_size"));
+  TP_TRY(check_device());
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // LN needs the whole hidden width: every shard holds the full x (replicated)
+  TP_TRY(launch_layernorm_fwd(x, gamma, beta, xn, mean, rstd, M, h, 1e-5f, dtype, st));
+  TP_TRY(qkv_fwd(xn, Wqkv, qkv, M, h, dtype, st));
+  return launch_attention_fwd(qkv, o, lse, b, s, h, n_heads, causal, dtype, st);
+}
+
 }  // namespace tp
 
 using namespace tp;
@@ -108,26 +134,12 @@ tp_status tp_attn_proj_fwd(const void* x, const float* gamma, const float* beta,
                            float* lse, void* out, int64_t b, int64_t s, int64_t h,
                            int32_t n_heads, int32_t N, int causal, tp_dtype dtype, tp_reduce mode,
                            void* ws, size_t ws_bytes, void* stream) {
-  TP_TRY(check_dtype(dtype));
-  TP_TRY(need(mode == TP_REDUCE_BUFFERS || mode == TP_REDUCE_SPLITK, TP_ERR_INVALID_ARG,
-              "unknown reduce mode"));
-  TP_TRY(need(x && gamma && beta && Wqkv && Wo && xn && mean && rstd && qkv && o && lse && out,
-              TP_ERR_INVALID_ARG, "all tensors of tp_attn_proj_fwd are required"));
-  TP_TRY(check_attn_shape(b, s, h, n_heads, N, dtype));
-  TP_TRY(check_aligned({x, gamma, beta, Wqkv, Wo, xn, mean, rstd, qkv, o, lse, out, ws}));
-  const int64_t M = b * s;
-  if (M == 0) return TP_OK;
-  const size_t need_ws = partial_bytes(M, h, N, mode);
-  TP_TRY(need(ws_bytes >= need_ws && (need_ws == 0 || ws), TP_ERR_WORKSPACE,
-              "workspace smaller than tp_workspace_size"));
-  TP_TRY(check_device());
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // LN needs the whole hidden width: every shard holds the full x (replicated)
-  TP_TRY(launch_layernorm_fwd(x, gamma, beta, xn, mean, rstd, M, h, 1e-5f, dtype, st));
-  TP_TRY(qkv_fwd(xn, Wqkv, qkv, M, h, dtype, st));
-  TP_TRY(launch_attention_fwd(qkv, o, lse, b, s, h, n_heads, causal, dtype, st));
+  TP_TRY(attn_core_fwd(x, gamma, beta, Wqkv, Wo, xn, mean, rstd, qkv, o, lse, out, b, s, h,
+                       n_heads, N, causal, dtype, mode, ws, ws_bytes, stream));
+  if (b * s == 0) return TP_OK;
   // shard i's O_i feeds row block i of W_o directly (no gather); sum + residual
-  return row_impl(o, Wo, x, out, M, h, h, N, dtype, mode, ws, st);
+  return row_impl(o, Wo, x, out, b * s, h, h, N, dtype, mode, ws,
+                  static_cast<cudaStream_t>(stream));
 }
 
 tp_status tp_attn_proj_bwd(const void* x, const float* gamma, const void* Wqkv, const void* Wo,
@@ -266,12 +278,20 @@ tp_status tp_layer_fwd(const void* x, const tp_layer_weights* w, const tp_layer_
   TP_TRY(need(ws_bytes >= layer_workspace_size(true, b * s, h, f, N, dtype, mode) ||
                   b * s == 0,
               TP_ERR_WORKSPACE, "workspace smaller than tp_workspace_size"));
-  // x1 = x + sum_i O_i W_o,i  with O from LN1(x)
-  TP_TRY(tp_attn_proj_fwd(x, w->gamma1, w->beta1, w->Wqkv, w->Wo, sv->xn1, sv->mean1, sv->rstd1,
-                          sv->qkv, sv->o, sv->lse, sv->x1, b, s, h, n_heads, N, causal, dtype,
-                          mode, ws, ws_bytes, stream));
-  TP_TRY(tp_layernorm_fwd(sv->x1, w->gamma2, w->beta2, sv->xn2, sv->mean2, sv->rstd2, b * s, h,
-                          1e-5f, dtype, stream));
+  // x1 = x + sum_i O_i W_o,i  with O from LN1(x); then xn2 = LN2(x1). The sum and
+  // LN2 run as one pass over the shard partials (buffers mode) or the split-K GEMM
+  // followed by LN2.
+  TP_TRY(need(w->gamma2 && w->beta2, TP_ERR_INVALID_ARG, "gamma2 and beta2 are required"));
+  TP_TRY(need(h % 8 == 0 && h <= kReduceLnMaxH, TP_ERR_SHAPE,
+              "layer: h must be a multiple of 8 and at most 16384"));
+  TP_TRY(check_aligned({w->gamma2, w->beta2, sv->x1, sv->xn2, sv->mean2, sv->rstd2}));
+  TP_TRY(attn_core_fwd(x, w->gamma1, w->beta1, w->Wqkv, w->Wo, sv->xn1, sv->mean1, sv->rstd1,
+                       sv->qkv, sv->o, sv->lse, sv->x1, b, s, h, n_heads, N, causal, dtype, mode,
+                       ws, ws_bytes, stream));
+  if (b * s > 0)
+    TP_TRY(row_ln_impl(sv->o, w->Wo, x, w->gamma2, w->beta2, sv->x1, sv->xn2, sv->mean2,
+                       sv->rstd2, b * s, h, h, N, 1e-5f, dtype, mode, ws,
+                       static_cast<cudaStream_t>(stream)));
   // out = x1 + sum_i GELU(xn2 W1_i) W2_i
   return tp_mlp_fwd(sv->xn2, w->W1, nullptr, w->W2, sv->x1, sv->y, nullptr, sv->hh, out, b * s,
                     h, f, N, dtype, TP_ACT_GELU, mode, ws, ws_bytes, stream);

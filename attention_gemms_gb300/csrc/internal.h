@@ -90,6 +90,13 @@ tp_status launch_gemv(const GemmDesc& d, cudaStream_t st);
 tp_status launch_gemm_simt(const GemmDesc& d, cudaStream_t st);  // fp32, CUDA cores
 tp_status launch_shard_reduce(const float* P, const void* residual, void* out, int N,
                               int64_t M, int64_t n, tp_dtype out_dtype, cudaStream_t st);
+// sum + residual, rounded to dt, then LayerNorm of the rounded row: h % 8 == 0,
+// h <= kReduceLnMaxH, 16-byte aligned buffers
+constexpr int64_t kReduceLnMaxH = 16384;
+tp_status launch_shard_reduce_ln(const float* P, const void* residual, const float* gamma,
+                                 const float* beta, void* sum_out, void* y, float* mean,
+                                 float* rstd, int N, int64_t M, int64_t h, float eps,
+                                 tp_dtype dt, cudaStream_t st);
 
 inline tp_status launch_gemm(const GemmDesc& d, cudaStream_t st) {
   if (d.dtype != TP_BF16) return launch_gemm_simt(d, st);
@@ -105,7 +112,14 @@ tp_status launch_layernorm_bwd(const void* x, const float* gamma, const float* m
                                const float* rstd, const void* dy, const void* dres, void* dx,
                                float* dgamma, float* dbeta, int64_t M, int64_t h, void* ws,
                                tp_dtype dt, cudaStream_t st);
-size_t layernorm_bwd_ws_bytes(int64_t M, int64_t h);
+// LN backward whose parameter gradients are also kept per rank: rank r owns rows
+// [r M / ranks, (r + 1) M / ranks) (M % ranks == 0); dgamma = sum over ranks in order
+tp_status launch_layernorm_bwd_ranks(const void* x, const float* gamma, const float* mean,
+                                     const float* rstd, const void* dy, const void* dres,
+                                     void* dx, float* dgamma, float* dbeta, float* dgamma_ranks,
+                                     float* dbeta_ranks, int64_t M, int64_t h, int ranks,
+                                     void* ws, tp_dtype dt, cudaStream_t st);
+size_t layernorm_bwd_ws_bytes(int64_t M, int64_t h, int ranks = 1);
 size_t attn_workspace_size(bool fwd, int64_t M, int64_t h, int32_t N, tp_dtype dt,
                            tp_reduce mode);
 size_t layer_workspace_size(bool fwd, int64_t M, int64_t h, int64_t f, int32_t N, tp_dtype dt,
@@ -123,9 +137,16 @@ tp_status check_aligned(std::initializer_list<const void*> ptrs);
 tp_status check_dtype(tp_dtype dt);
 tp_status check_device();
 size_t partial_bytes(int64_t M, int64_t n, int32_t N, tp_reduce mode);
+tp_status check_mlp_shape(int64_t M, int64_t h, int64_t f, int32_t N, tp_dtype dt);
+size_t sp_mlp_workspace_size(bool fwd, int64_t M, int64_t h, int64_t f, int32_t N, tp_dtype dt,
+                             tp_act act, tp_reduce mode);
 tp_status row_impl(const void* Xs, const void* W, const void* residual, void* out, int64_t M,
                    int64_t k, int64_t n, int32_t N, tp_dtype dt, tp_reduce mode, void* ws,
                    cudaStream_t st);
+tp_status row_ln_impl(const void* Xs, const void* W, const void* residual, const float* gamma,
+                      const float* beta, void* sum_out, void* y, float* mean, float* rstd,
+                      int64_t M, int64_t k, int64_t n, int32_t N, float eps, tp_dtype dt,
+                      tp_reduce mode, void* ws, cudaStream_t st);
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline size_t elem_size(tp_dtype t) { return t == TP_BF16 ? 2 : 4; }
 

@@ -93,16 +93,22 @@ __global__ void __launch_bounds__(32 * kRowWarps) ln_bwd_dx_kernel(
 constexpr int kColThreads = 256;
 constexpr int kRowsPerChunk = 64;
 
-// partial[chunk][0:h] = sum over the chunk's rows of dy * xhat, partial[chunk][h:2h] = of dy
+// partial[chunk][0:h] = sum over the chunk's rows of dy * xhat, partial[chunk][h:2h] = of dy.
+// Rows are grouped by rank (rank r owns rows [r * rank_rows, (r + 1) * rank_rows), one
+// rank when the LN input is replicated) and each rank's rows are cut into cpr chunks
+// of at most kRowsPerChunk rows; chunk index = r * cpr + c.
 template <typename T>
 __global__ void __launch_bounds__(kColThreads) ln_bwd_param_partial_kernel(
     const T* __restrict__ x, const float* __restrict__ mean, const float* __restrict__ rstd,
-    const T* __restrict__ dy, float* __restrict__ partial, int64_t M, int h) {
+    const T* __restrict__ dy, float* __restrict__ partial, int64_t M, int h, int64_t rank_rows,
+    int cpr) {
   const int c = blockIdx.x * kColThreads + threadIdx.x;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kRowsPerChunk;
+  const int rank = blockIdx.y / cpr, chunk = blockIdx.y - rank * cpr;
+  const int64_t rank_end = min(M, (rank + 1) * rank_rows);
+  const int64_t r0 = rank * rank_rows + static_cast<int64_t>(chunk) * kRowsPerChunk;
   if (c >= h) return;
   float sg = 0.0f, sb = 0.0f;
-  const int64_t r1 = min(M, r0 + kRowsPerChunk);
+  const int64_t r1 = min(rank_end, r0 + kRowsPerChunk);
   for (int64_t r = r0; r < r1; ++r) {
     const float d = ld(dy + r * h, c);
     sg += d * (ld(x + r * h, c) - mean[r]) * rstd[r];
@@ -112,17 +118,27 @@ __global__ void __launch_bounds__(kColThreads) ln_bwd_param_partial_kernel(
   partial[blockIdx.y * 2ll * h + h + c] = sb;
 }
 
+// per rank: the sum of its chunks in order (written to dgamma_ranks / dbeta_ranks
+// (ranks, h) when given); then the sum over the ranks in rank order
 __global__ void __launch_bounds__(kColThreads) ln_bwd_param_final_kernel(
-    const float* __restrict__ partial, int chunks, int h, float* dgamma, float* dbeta) {
+    const float* __restrict__ partial, int ranks, int cpr, int h, float* dgamma, float* dbeta,
+    float* dgamma_ranks, float* dbeta_ranks) {
   const int c = blockIdx.x * kColThreads + threadIdx.x;
   if (c >= h) return;
-  float sg = 0.0f, sb = 0.0f;
-  for (int k = 0; k < chunks; ++k) {
-    sg += partial[k * 2ll * h + c];
-    sb += partial[k * 2ll * h + h + c];
+  float tg = 0.0f, tb = 0.0f;
+  for (int r = 0; r < ranks; ++r) {
+    float sg = 0.0f, sb = 0.0f;
+    for (int k = r * cpr; k < (r + 1) * cpr; ++k) {
+      sg += partial[k * 2ll * h + c];
+      sb += partial[k * 2ll * h + h + c];
+    }
+    if (dgamma_ranks) dgamma_ranks[static_cast<int64_t>(r) * h + c] = sg;
+    if (dbeta_ranks) dbeta_ranks[static_cast<int64_t>(r) * h + c] = sb;
+    tg += sg;
+    tb += sb;
   }
-  if (dgamma) dgamma[c] = sg;
-  if (dbeta) dbeta[c] = sb;
+  if (dgamma) dgamma[c] = tg;
+  if (dbeta) dbeta[c] = tb;
 }
 
 template <typename T>
@@ -139,20 +155,22 @@ tp_status fwd_t(const void* x, const float* gamma, const float* beta, void* y, f
 template <typename T>
 tp_status bwd_t(const void* x, const float* gamma, const float* mean, const float* rstd,
                 const void* dy, const void* dres, void* dx, float* dgamma, float* dbeta,
-                int64_t M, int h, float* ws, cudaStream_t st) {
+                float* dgamma_ranks, float* dbeta_ranks, int64_t M, int h, int ranks, float* ws,
+                cudaStream_t st) {
   const unsigned rblocks = static_cast<unsigned>((M + kRowWarps - 1) / kRowWarps);
   ln_bwd_dx_kernel<T><<<rblocks, 32 * kRowWarps, 0, st>>>(
       static_cast<const T*>(x), gamma, mean, rstd, static_cast<const T*>(dy),
       static_cast<const T*>(dres), static_cast<T*>(dx), M, h);
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
-  if (!dgamma && !dbeta) return TP_OK;
-  const int chunks = static_cast<int>((M + kRowsPerChunk - 1) / kRowsPerChunk);
-  const dim3 g1((h + kColThreads - 1) / kColThreads, chunks);
+  if (!dgamma && !dbeta && !dgamma_ranks && !dbeta_ranks) return TP_OK;
+  const int64_t rank_rows = M / ranks;
+  const int cpr = static_cast<int>((rank_rows + kRowsPerChunk - 1) / kRowsPerChunk);
+  const dim3 g1((h + kColThreads - 1) / kColThreads, ranks * cpr);
   ln_bwd_param_partial_kernel<T><<<g1, kColThreads, 0, st>>>(
-      static_cast<const T*>(x), mean, rstd, static_cast<const T*>(dy), ws, M, h);
+      static_cast<const T*>(x), mean, rstd, static_cast<const T*>(dy), ws, M, h, rank_rows, cpr);
   ln_bwd_param_final_kernel<<<(h + kColThreads - 1) / kColThreads, kColThreads, 0, st>>>(
-      ws, chunks, h, dgamma, dbeta);
+      ws, ranks, cpr, h, dgamma, dbeta, dgamma_ranks, dbeta_ranks);
   count_launch(2);
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;
@@ -160,8 +178,10 @@ tp_status bwd_t(const void* x, const float* gamma, const float* mean, const floa
 
 }  // namespace
 
-size_t layernorm_bwd_ws_bytes(int64_t M, int64_t h) {
-  return static_cast<size_t>((M + kRowsPerChunk - 1) / kRowsPerChunk) * 2 * h * sizeof(float);
+size_t layernorm_bwd_ws_bytes(int64_t M, int64_t h, int ranks) {
+  if (ranks < 1 || M % ranks) return 0;
+  const int64_t cpr = (M / ranks + kRowsPerChunk - 1) / kRowsPerChunk;
+  return static_cast<size_t>(ranks * cpr) * 2 * h * sizeof(float);
 }
 
 tp_status launch_layernorm_fwd(const void* x, const float* gamma, const float* beta, void* y,
@@ -178,14 +198,25 @@ tp_status launch_layernorm_bwd(const void* x, const float* gamma, const float* m
                                const float* rstd, const void* dy, const void* dres, void* dx,
                                float* dgamma, float* dbeta, int64_t M, int64_t h, void* ws,
                                tp_dtype dt, cudaStream_t st) {
+  return launch_layernorm_bwd_ranks(x, gamma, mean, rstd, dy, dres, dx, dgamma, dbeta, nullptr,
+                                    nullptr, M, h, 1, ws, dt, st);
+}
+
+tp_status launch_layernorm_bwd_ranks(const void* x, const float* gamma, const float* mean,
+                                     const float* rstd, const void* dy, const void* dres,
+                                     void* dx, float* dgamma, float* dbeta, float* dgamma_ranks,
+                                     float* dbeta_ranks, int64_t M, int64_t h, int ranks,
+                                     void* ws, tp_dtype dt, cudaStream_t st) {
   if (M <= 0) return TP_OK;
-  if (h > (1 << 24) || (M + kRowsPerChunk - 1) / kRowsPerChunk > 65535)
-    return fail(TP_ERR_SHAPE, "LN too large");
+  if (ranks < 1 || M % ranks) return fail(TP_ERR_SHAPE, "LN rows must split evenly over the ranks");
+  const int64_t cpr = (M / ranks + kRowsPerChunk - 1) / kRowsPerChunk;
+  if (h > (1 << 24) || ranks * cpr > 65535) return fail(TP_ERR_SHAPE, "LN too large");
   float* w = static_cast<float*>(ws);
+  const int hh = static_cast<int>(h);
   return dt == TP_BF16 ? bwd_t<__nv_bfloat16>(x, gamma, mean, rstd, dy, dres, dx, dgamma, dbeta,
-                                              M, static_cast<int>(h), w, st)
-                       : bwd_t<float>(x, gamma, mean, rstd, dy, dres, dx, dgamma, dbeta, M,
-                                      static_cast<int>(h), w, st);
+                                              dgamma_ranks, dbeta_ranks, M, hh, ranks, w, st)
+                       : bwd_t<float>(x, gamma, mean, rstd, dy, dres, dx, dgamma, dbeta,
+                                      dgamma_ranks, dbeta_ranks, M, hh, ranks, w, st);
 }
 
 }  // namespace tp

@@ -54,6 +54,8 @@ class Op(enum.IntEnum):
     LAYERNORM_BWD = 6
     LAYER_FWD = 7
     LAYER_BWD = 8
+    SP_MLP_FWD = 9
+    SP_MLP_BWD = 10
 
 
 class LayerWeights(ctypes.Structure):
@@ -106,6 +108,9 @@ _SIGS = {
     "tp_col_linear": (_ST, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _ST, _ST, _P]),
     "tp_row_linear": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _ST, _ST, _P, _SZ, _P]),
     "tp_shard_reduce": (_ST, [_P, _P, _P, _I32, _I64, _I64, _ST, _P]),
+    "tp_shard_reduce_ln": (_ST, [_P] * 8 + [_I32, _I64, _I64, ctypes.c_float, _ST, _P]),
+    "tp_row_linear_ln": (_ST, [_P] * 9 + [_I64, _I64, _I64, _I32, ctypes.c_float, _ST, _ST, _P,
+                                          _SZ, _P]),
     "tp_mlp_fwd": (_ST, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _ST, _ST,
                          _ST, _P, _SZ, _P]),
     "tp_mlp_bwd": (_ST, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32,
@@ -116,6 +121,8 @@ _SIGS = {
                                            _P, _SZ, _P]),
     "tp_attn_proj_bwd": (_ST, [_P] * 16 + [_I64, _I64, _I64, _I32, _I32, ctypes.c_int, _ST, _ST,
                                            _P, _SZ, _P]),
+    "tp_sp_mlp_fwd": (_ST, [_P] * 13 + [_I64, _I64, _I64, _I32, _ST, _ST, _ST, _P, _SZ, _P]),
+    "tp_sp_mlp_bwd": (_ST, [_P] * 20 + [_I64, _I64, _I64, _I32, _ST, _ST, _ST, _P, _SZ, _P]),
     "tp_layer_fwd": (_ST, [_P, ctypes.POINTER(LayerWeights), ctypes.POINTER(LayerSaved), _P, _I64,
                            _I64, _I64, _I64, _I32, _I32, ctypes.c_int, _ST, _ST, _P, _SZ, _P]),
     "tp_layer_bwd": (_ST, [_P, ctypes.POINTER(LayerWeights), ctypes.POINTER(LayerSaved), _P, _P,
@@ -240,6 +247,21 @@ def tp_shard_reduce(partials, residual, out, N, M, n, out_dtype, stream=None):
                                  int(out_dtype), _stream(stream)))
 
 
+def tp_shard_reduce_ln(partials, residual, gamma, beta, sum_out, y, mean, rstd, N, M, h, eps,
+                       dtype, stream=None):
+    _check(lib().tp_shard_reduce_ln(_ptr(partials), _ptr(residual), _ptr(gamma), _ptr(beta),
+                                    _ptr(sum_out), _ptr(y), _ptr(mean), _ptr(rstd), N, M, h,
+                                    float(eps), int(dtype), _stream(stream)))
+
+
+def tp_row_linear_ln(Xs, W, residual, gamma, beta, sum_out, y, mean, rstd, M, k, n, N, eps,
+                     dtype, mode, ws, ws_bytes, stream=None):
+    _check(lib().tp_row_linear_ln(_ptr(Xs), _ptr(W), _ptr(residual), _ptr(gamma), _ptr(beta),
+                                  _ptr(sum_out), _ptr(y), _ptr(mean), _ptr(rstd), M, k, n, N,
+                                  float(eps), int(dtype), int(mode), _ptr(ws), int(ws_bytes),
+                                  _stream(stream)))
+
+
 def tp_mlp_fwd(X, W1, W1_up, W2, residual, Y, Y_up, H, Z, M, h, f, N, dtype, act, mode, ws,
                ws_bytes, stream=None):
     _check(lib().tp_mlp_fwd(_ptr(X), _ptr(W1), _ptr(W1_up), _ptr(W2), _ptr(residual), _ptr(Y),
@@ -253,6 +275,24 @@ def tp_mlp_bwd(X, W1, W1_up, W2, Y, Y_up, H, dZ, dX, dW1, dW1_up, dW2, M, h, f, 
                             _ptr(H), _ptr(dZ), _ptr(dX), _ptr(dW1), _ptr(dW1_up), _ptr(dW2),
                             M, h, f, N, int(dtype), int(act), int(mode), _ptr(ws),
                             int(ws_bytes), _stream(stream)))
+
+
+def tp_sp_mlp_fwd(x, gamma, beta, W1, W1_up, W2, xn, mean, rstd, Y, Y_up, H, out, M, h, f, N,
+                  dtype, act, mode, ws, ws_bytes, stream=None):
+    _check(lib().tp_sp_mlp_fwd(*[_ptr(t) for t in (x, gamma, beta, W1, W1_up, W2, xn, mean, rstd,
+                                                   Y, Y_up, H, out)],
+                               M, h, f, N, int(dtype), int(act), int(mode), _ptr(ws),
+                               int(ws_bytes), _stream(stream)))
+
+
+def tp_sp_mlp_bwd(x, gamma, W1, W1_up, W2, xn, mean, rstd, Y, Y_up, H, dout, dx, dgamma, dbeta,
+                  dgamma_ranks, dbeta_ranks, dW1, dW1_up, dW2, M, h, f, N, dtype, act, mode, ws,
+                  ws_bytes, stream=None):
+    _check(lib().tp_sp_mlp_bwd(*[_ptr(t) for t in (x, gamma, W1, W1_up, W2, xn, mean, rstd, Y,
+                                                   Y_up, H, dout, dx, dgamma, dbeta, dgamma_ranks,
+                                                   dbeta_ranks, dW1, dW1_up, dW2)],
+                               M, h, f, N, int(dtype), int(act), int(mode), _ptr(ws),
+                               int(ws_bytes), _stream(stream)))
 
 
 def tp_row_linear_noalloc(Xs, W, residual, out, M, k, n, N, dtype, stream=None):

@@ -44,6 +44,9 @@ WORKLOADS = {
     "c2": dict(desc="page-2-sized pre-LN transformer layer fwd+bwd: b=8 s=128 h=128 heads=8 "
                     "ffn=512 N=2", b=8, s=128, h=128, f=512, N=2, heads=8, act="gelu", cfg=2,
                layer=True),
+    "c3-sp": dict(desc="sequence-parallel pre-LN erf-GELU MLP block fwd+bwd (LN on each rank's "
+                       "rows, reduce-scatter + all-gather): b=4 s=2048 h=4096 ffn=16384 N=8",
+                  b=4, s=2048, h=4096, f=16384, N=8, act="gelu", cfg=3, sp=True),
     # reduced-token case of c5 for ncu captures (a few GB on the device, inputs > L2)
     "c5-2k": dict(desc="profiling case: SwiGLU MLP fwd+bwd b=1 s=2048 h=8192 ffn=28672 N=4",
                   b=1, s=2048, h=8192, f=28672, N=4, act="swiglu", cfg=5),
@@ -251,6 +254,8 @@ def run_ours(args, w):
     device = torch.device("cuda", torch.cuda.current_device())
     if w.get("layer"):
         return run_layer(args, w, T, device, rank, ws_)
+    if w.get("sp"):
+        return run_sp(args, w, T, device, rank, ws_)
     M, h, f, N = w["b"] * w["s"], w["h"], w["f"], w["N"]
     sw = w["act"] == "swiglu"
     act = T.Act.SWIGLU if sw else T.Act.GELU
@@ -376,12 +381,141 @@ def run_ours(args, w):
         out["roofline"] = {"bound": "alu", "note": "fp32 FFMA path at a latency-bound size; "
                            "no roofline fraction is claimed", "achieved": None, "peak": None,
                            "unit": "TFLOP/s", "frac": None, "traffic": None}
+    if args.shard_sum:
+        out["reduce_ln"] = run_shard_sum(args, w, device, T)
     if args.decode and not f32:
         out["decode"] = run_decode(args, device, T)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, hostin, budget_s=args.cpu_budget)
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+def run_sp(args, w, T, device, rank, nranks):
+    """The sequence-parallel pre-LN MLP block, forward + backward, per step. The MLP
+    FLOPs are the work counted; the same block without sequence parallelism (LN on
+    the replicated rows, the ordinary all-reduce, replicated LN gradients) is timed
+    beside it, and the column GEMM of the block on its own gives the roofline."""
+    import torch
+    M, h, f, N = w["b"] * w["s"], w["h"], w["f"], w["N"]
+    sw = w["act"] == "swiglu"
+    A = T.Act.SWIGLU if sw else T.Act.GELU
+    mode = T.Reduce.SPLITK if args.mode == "splitk" else T.Reduce.BUFFERS
+    BF, bf, f32 = T.DType.BF16, torch.bfloat16, torch.float32
+    t_gen = time.time()
+    d, hostin = make_inputs(w, rank, device)
+    t_gen = time.time() - t_gen
+    e = lambda *sh, dt=bf: torch.empty(sh, dtype=dt, device=device)
+    g, b = torch.ones(h, device=device), torch.zeros(h, device=device)
+    xn, mean, rstd = e(M, h), e(M, dt=f32), e(M, dt=f32)
+    Y, Yu, H, out, dx = e(M, f), (e(M, f) if sw else None), e(M, f), e(M, h), e(M, h)
+    dg, db, dgr, dbr = e(h, dt=f32), e(h, dt=f32), e(N, h, dt=f32), e(N, h, dt=f32)
+    dW1, dWu, dW2 = e(h, f), (e(h, f) if sw else None), e(f, h)
+    wsb = max(T.tp_workspace_size(T.Op.SP_MLP_FWD, M, h, f, N, BF, A, mode),
+              T.tp_workspace_size(T.Op.SP_MLP_BWD, M, h, f, N, BF, A, mode),
+              T.tp_workspace_size(T.Op.MLP_FWD, M, h, f, N, BF, A, mode),
+              T.tp_workspace_size(T.Op.MLP_BWD, M, h, f, N, BF, A, mode),
+              T.tp_workspace_size(T.Op.LAYERNORM_BWD, M, h, 0, 1, BF))
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=device)
+    dxn = e(M, h)
+    stream = torch.cuda.current_stream()
+    X, W1, W1u, W2, dZ = d["X"], d["W1"], d["W1u"], d["W2"], d["dZ"]
+
+    def sp_step():
+        T.tp_sp_mlp_fwd(X, g, b, W1, W1u, W2, xn, mean, rstd, Y, Yu, H, out, M, h, f, N, BF, A,
+                        mode, ws, ws.numel(), stream)
+        T.tp_sp_mlp_bwd(X, g, W1, W1u, W2, xn, mean, rstd, Y, Yu, H, dZ, dx, dg, db, dgr, dbr,
+                        dW1, dWu, dW2, M, h, f, N, BF, A, mode, ws, ws.numel(), stream)
+
+    def tp_step():  # LN replicated on every rank, all-reduce, replicated LN gradients
+        T.tp_layernorm_fwd(X, g, b, xn, mean, rstd, M, h, 1e-5, BF, stream)
+        T.tp_mlp_fwd(xn, W1, W1u, W2, X, Y, Yu, H, out, M, h, f, N, BF, A, mode, ws, ws.numel(),
+                     stream)
+        T.tp_mlp_bwd(xn, W1, W1u, W2, Y, Yu, H, dZ, dxn, dW1, dWu, dW2, M, h, f, N, BF, A, mode,
+                     ws, ws.numel(), stream)
+        T.tp_layernorm_bwd(X, g, mean, rstd, dxn, dZ, dx, dg, db, M, h, BF, ws, ws.numel(),
+                           stream)
+
+    def timed(fn, steps):
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        z.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(z) / steps
+
+    for _ in range(args.warmup):
+        sp_step()
+        tp_step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(device.index)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    n0 = T.tp_launch_count()
+    ms = timed(sp_step, args.steps)
+    launches = T.tp_launch_count() - n0
+    barrier()
+    tp_ms = timed(tp_step, args.steps)
+    col_ms = timed(lambda: T.tp_col_linear(xn, W1, W1u, Y, Yu, H, M, h, f, N, BF, A, stream),
+                   args.steps)
+    # end to end: x and dout in from pinned host memory, out and dx back, every step
+    pin = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
+    Xp, dZp = pin(hostin["X"]), pin(hostin["dZ"])
+    outp = torch.empty((M, h), dtype=bf, pin_memory=True)
+    dxp = torch.empty((M, h), dtype=bf, pin_memory=True)
+
+    def e2e_step():
+        X.copy_(Xp, non_blocking=True)
+        dZ.copy_(dZp, non_blocking=True)
+        sp_step()
+        outp.copy_(out, non_blocking=True)
+        dxp.copy_(dx, non_blocking=True)
+    barrier()
+    e2e_ms = timed(e2e_step, args.steps)
+    clk = clocks.stop()
+    if T.tp_check_status(stream) != 0:
+        raise RuntimeError("device wait timeout: " + T.tp_last_error())
+    ms_max, e2e_max = max_over_ranks(ms, device), max_over_ranks(e2e_ms, device)
+    tp_max, col_max = max_over_ranks(tp_ms, device), max_over_ranks(col_ms, device)
+    flops = mlp_flops(w)
+    value = flops * nranks / (ms_max * 1e-3) / 1e12
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    col_tf = col_gemm_flops(w) / (col_max * 1e-3) / 1e12
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": nranks,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights; LN gamma=1, beta=0)",
+        "config": {"workload": w["desc"], "tokens": M, "h": h, "ffn": f, "shards": N,
+                   "act": w["act"], "shard_sum": args.mode, "sequence_parallel": True,
+                   "global_batch": w["b"] * nranks, "seq_len": w["s"],
+                   "parallelism": f"tp{N}+sp virtual ranks per GPU, dp{nranks}",
+                   "l2": "inputs larger than L2 (no flush)"},
+        "pct_of_peak": round(100 * value / nranks / peak, 2),
+        "without_sp_ms_per_step": round(tp_max, 4),
+        "roofline": {"bound": "tensor", "kernel": "gemm_tc_kernel (column-parallel GEMM + fused "
+                     + ("SwiGLU" if sw else "GELU") + " epilogue), timed on its own at the "
+                     "block's shape", "achieved": round(col_tf, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(col_tf / peak, 4),
+                     "peak_source": f"{src} bf16 dense (burst)",
+                     "traffic": col_gemm_traffic(args.workload.replace("-sp", "")),
+                     "algorithmic_flops_per_launch": col_gemm_flops(w),
+                     "avg_launch_ms": round(col_max, 4)},
+        "e2e": {"value": round(flops * nranks / (e2e_max * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": 2 * M * h * 2, "d2h_bytes_per_step": 2 * M * h * 2,
+                "ms_per_step": round(e2e_max, 4)},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "input_gen_s": round(t_gen, 1),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, hostin, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
 
 
 # ------------------------------------------------------------------ page-2 layer
@@ -531,6 +665,63 @@ def decode_bytes(T, h, f, N):
     return weights + acts + partials, 3 * h * f * 2, 2 * h * f * 2 + T * h * 2 + T * f * 2
 
 
+def run_shard_sum(args, w, device, T, reps=20):
+    """The shard sum at the workload's size, on its own (variant A's reduction of the
+    fp32 partials) and followed by LayerNorm, fused into one pass and unfused
+    (reduce, then LN reading the sum back). HBM-bound: GB/s of algorithmic bytes
+    against the measured copy bandwidth. Inputs (the partials) are larger than L2."""
+    import torch
+    M, h, N = w["b"] * w["s"], w["h"], w["N"]
+    f32 = w.get("dtype") == "f32"
+    BF = T.DType.F32 if f32 else T.DType.BF16
+    bf = torch.float32 if f32 else torch.bfloat16
+    e = 4 if f32 else 2
+    g = torch.Generator(device=device)
+    g.manual_seed(4242)
+    P = torch.randn((N, M, h), generator=g, device=device, dtype=torch.float32)
+    R = torch.randn((M, h), generator=g, device=device, dtype=torch.float32).to(bf)
+    gamma = torch.ones(h, device=device, dtype=torch.float32)
+    beta = torch.zeros(h, device=device, dtype=torch.float32)
+    S, Y = torch.empty((M, h), device=device, dtype=bf), torch.empty((M, h), device=device, dtype=bf)
+    mean = torch.empty(M, device=device, dtype=torch.float32)
+    rstd = torch.empty(M, device=device, dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+    calls = {
+        "reduce": (lambda: T.tp_shard_reduce(P, R, S, N, M, h, BF, stream),
+                   N * M * h * 4 + 2 * M * h * e),
+        "reduce_ln_fused": (lambda: T.tp_shard_reduce_ln(P, R, gamma, beta, S, Y, mean, rstd, N, M,
+                                                         h, 1e-5, BF, stream),
+                            N * M * h * 4 + 3 * M * h * e + 8 * M),
+        "reduce_then_ln": (lambda: (T.tp_shard_reduce(P, R, S, N, M, h, BF, stream),
+                                    T.tp_layernorm_fwd(S, gamma, beta, Y, mean, rstd, M, h, 1e-5,
+                                                       BF, stream)),
+                           N * M * h * 4 + 3 * M * h * e + 8 * M),
+    }
+    peaks, src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    out = {"unit": "GB/s", "peak": hbm, "peak_source": f"{src} HBM copy",
+           "shape": {"N": N, "M": M, "h": h}, "l2": "partials larger than L2 (no flush)"}
+    for name, (fn, nbytes) in calls.items():
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / reps
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[name] = {"us": round(us, 2), "algorithmic_bytes": int(nbytes), "achieved": round(gbs, 1),
+                     "frac": round(gbs / hbm, 4)}
+    if T.tp_check_status(stream) != 0:
+        raise RuntimeError("device error in the shard-sum measurement: " + T.tp_last_error())
+    del P, R, S, Y
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_decode(args, device, T):
     import torch
     from attention_gemms_gb300 import synth
@@ -651,6 +842,10 @@ def _oracle_sample(w, hostin, rows, Wf):
     dt = w.get("dtype", "bf16")
     X = synth.to_f64(hostin["X"][:rows], dt)
     dZ = synth.to_f64(hostin["dZ"][:rows], dt)
+    if w.get("sp"):  # rows is a multiple of N: each virtual rank holds rows / N of them
+        g, b = np.ones(X.shape[1]), np.zeros(X.shape[1])
+        O.sp_mlp_block_bwd(X, g, b, Wf["W1"], Wf["W2"], w["N"], dZ, w["act"], Wf["W1u"])
+        return
     if w["act"] == "swiglu":
         O.mlp_swiglu_fwd(X, Wf["W1"], Wf["W1u"], Wf["W2"], w["N"])
         O.mlp_swiglu_bwd(X, Wf["W1"], Wf["W1u"], Wf["W2"], dZ, w["N"])
@@ -675,6 +870,7 @@ def cpu_baseline(w, hostin, budget_s=15.0):
         if dt * 2 > budget_s or rows >= w["b"] * w["s"]:
             break
         rows = min(w["b"] * w["s"], int(rows * max(2.0, budget_s / max(dt, 1e-3) * 0.5)))
+        rows -= rows % w["N"] if w.get("sp") else 0
     return {"value": round(mlp_flops(w, rows) / dt / 1e12, 6), "unit": "TFLOP/s",
             "cores": len(os.sched_getaffinity(0)),
             "threads_effective": round(dc / dt, 1), "kind": "oracle",
@@ -711,6 +907,8 @@ def run_reference(args, w):
                   "W2": synth.normal((f, h), synth.seed_of(c, "Wd"), 0.02, dtp)}
         Wf = _weights_f64(hostin, dtp)
         rows = min(args.ref_rows, M)
+        if w.get("sp"):
+            rows = max(w["N"], rows - rows % w["N"])
         run = lambda: _oracle_sample(w, hostin, rows, Wf)
         flops = mlp_flops(w, rows)
         sample = (f"fp64 oracle forward+backward on {rows} of {M} token rows per step, full "
@@ -755,6 +953,8 @@ def main(argv=None):
     ap.add_argument("--decode", dest="decode", action="store_true", default=True,
                     help="also run the decode GEMV sweep (default)")
     ap.add_argument("--no-decode", dest="decode", action="store_false")
+    ap.add_argument("--no-shard-sum", dest="shard_sum", action="store_false", default=True,
+                    help="skip the shard-sum / fused reduce + LayerNorm measurement")
     ap.add_argument("--decode-warmup-ms", type=float, default=200.0,
                     help="minimum warm-up time of each decode token count (clocks ramp up)")
     args = ap.parse_args(argv)

@@ -99,7 +99,9 @@ typedef enum tp_op {
   TP_OP_ATTN_PROJ_BWD = 5,
   TP_OP_LAYERNORM_BWD = 6,
   TP_OP_LAYER_FWD = 7,
-  TP_OP_LAYER_BWD = 8
+  TP_OP_LAYER_BWD = 8,
+  TP_OP_SP_MLP_FWD = 9,
+  TP_OP_SP_MLP_BWD = 10
 } tp_op;
 
 /* Weights of the pre-LN transformer layer (tp_layer_fwd / tp_layer_bwd). */
@@ -245,6 +247,43 @@ TP_API tp_status tp_shard_reduce(const float* partials, const void* residual, vo
                           void* stream);
 
 /*
+ * The shard sum followed by LayerNorm, fused into one pass over the partials:
+ *   x = sum_{i=0}^{N-1} partials[i] (+ residual), shards in that order in fp32, rounded
+ *       to dtype and written to sum_out (the residual stream after the all-reduce);
+ *   y = gamma * (x - mean) * rstd + beta over the full width h of the ROUNDED x,
+ *       biased variance, rstd = 1 / sqrt(var + eps).
+ * The all-reduce has to finish before LayerNorm because its statistics need the
+ * whole hidden width [张量并行 notes, §相关分析, the forward bottleneck before LN];
+ * here the sum is normalised while it is still on chip.
+ *
+ *   partials (N, M, h) fp32 read;  residual (M, h) dtype read or NULL
+ *   gamma, beta (h) fp32 read;  sum_out (M, h) dtype written or NULL
+ *   y (M, h) dtype written;  mean, rstd (M) fp32 written or NULL
+ * Errors: TP_ERR_INVALID_ARG, TP_ERR_DTYPE, TP_ERR_SHAPE (h % 8, h > 16384),
+ * TP_ERR_ALIGNMENT (every buffer 16-byte aligned), TP_ERR_CUDA.
+ */
+TP_API tp_status tp_shard_reduce_ln(const float* partials, const void* residual,
+                                    const float* gamma, const float* beta, void* sum_out,
+                                    void* y, float* mean, float* rstd, int32_t N, int64_t M,
+                                    int64_t h, float eps, tp_dtype dtype, void* stream);
+
+/*
+ * Row-parallel linear whose shard sum feeds LayerNorm:
+ *   sum_out = sum_i Xs_i W_i (+ residual),  y = LN(sum_out; gamma, beta, eps)
+ * with the operands, shard split and modes of tp_row_linear and the LN of
+ * tp_shard_reduce_ln. TP_REDUCE_BUFFERS writes fp32 partials and normalises them in
+ * the fused reduction; TP_REDUCE_SPLITK folds the sum in the GEMM and then runs LN.
+ *   sum_out (M, n) written (required);  y (M, n) written;  mean, rstd (M) or NULL
+ *   ws: tp_workspace_size(TP_OP_ROW_LINEAR, M, k, n, N, dtype, TP_ACT_NONE, mode).
+ * Errors: as tp_row_linear, plus TP_ERR_SHAPE for n % 8 or n > 16384.
+ */
+TP_API tp_status tp_row_linear_ln(const void* Xs, const void* W, const void* residual,
+                                  const float* gamma, const float* beta, void* sum_out, void* y,
+                                  float* mean, float* rstd, int64_t M, int64_t k, int64_t n,
+                                  int32_t N, float eps, tp_dtype dtype, tp_reduce mode, void* ws,
+                                  size_t ws_bytes, void* stream);
+
+/*
  * Tensor-parallel MLP forward: Z = sum_i act(X W1_i) W2_i (+ residual).
  * [张量并行 notes, §MLP 层的并行化, column-then-row formula; Infra: Tensor Parallel, MLP;
  *  20260402-parallelism, §1 TP (W_gate/W_up by column, second layer by row)]
@@ -382,12 +421,59 @@ TP_API tp_status tp_attn_proj_bwd(const void* x, const float* gamma, const void*
                                   void* stream);
 
 /*
+ * Sequence-parallel pre-LN MLP sub-block, out = x + MLP(LN(x))
+ * [20260402-parallelism, §5 Sequence Parallelism]. The rows are split over the N
+ * ranks of the tensor-parallel group along the sequence: rank r holds rows
+ * [r M/N, (r+1) M/N) of x, xn, mean, rstd, out and dx (M % N == 0; sequence-major
+ * rows, so each rank's piece is one contiguous block). Forward: LN on each rank's
+ * rows; all-gather of xn (the ranks' blocks are adjacent in one buffer, so the
+ * gather is the buffer itself); the tensor-parallel MLP of tp_mlp_fwd; the sum
+ * after the row-parallel GEMM is a reduce-scatter: rank r receives its rows of
+ * sum_i Z_i and adds its residual rows x_r. The two collectives move the same
+ * bytes as the all-reduce they replace.
+ *   x (M, h) read;  gamma, beta (h) fp32 read;  W1, W1_up, W2 as tp_mlp_fwd
+ *   xn (M, h), mean, rstd (M) fp32 written (saved for the backward)
+ *   Y, Y_up, H as tp_mlp_fwd (H required here);  out (M, h) written
+ *   ws: tp_workspace_size(TP_OP_SP_MLP_FWD, M, h, f, N, dtype, act, mode)
+ * Errors: as tp_mlp_fwd, plus TP_ERR_SHAPE when M % N != 0.
+ */
+TP_API tp_status tp_sp_mlp_fwd(const void* x, const float* gamma, const float* beta,
+                               const void* W1, const void* W1_up, const void* W2, void* xn,
+                               float* mean, float* rstd, void* Y, void* Y_up, void* H, void* out,
+                               int64_t M, int64_t h, int64_t f, int32_t N, tp_dtype dtype,
+                               tp_act act, tp_reduce mode, void* ws, size_t ws_bytes,
+                               void* stream);
+
+/*
+ * Backward of tp_sp_mlp_fwd. dout's rank blocks are all-gathered (every shard reads
+ * all of it); the MLP's input gradient is reduce-scattered, so rank r gets its rows
+ * of sum_i dX_i; LN backward runs on each rank's rows and adds the residual's dout_r.
+ * Each rank's LN parameters see only that rank's rows, so the per-rank gradients
+ * differ: dgamma_ranks[r] / dbeta_ranks[r] (N, h) fp32 are each rank's sums (NULL =
+ * not kept) and dgamma / dbeta (h) fp32 their sum over the ranks in rank order (the
+ * all-reduce sequence parallelism adds for the LN parameters).
+ *   dx (M, h) written;  dW1, dW1_up, dW2 as tp_mlp_bwd
+ *   ws: tp_workspace_size(TP_OP_SP_MLP_BWD, M, h, f, N, dtype, act, mode)
+ * Errors: as tp_mlp_bwd, plus TP_ERR_SHAPE when M % N != 0.
+ */
+TP_API tp_status tp_sp_mlp_bwd(const void* x, const float* gamma, const void* W1,
+                               const void* W1_up, const void* W2, const void* xn,
+                               const float* mean, const float* rstd, const void* Y,
+                               const void* Y_up, const void* H, const void* dout, void* dx,
+                               float* dgamma, float* dbeta, float* dgamma_ranks,
+                               float* dbeta_ranks, void* dW1, void* dW1_up, void* dW2, int64_t M,
+                               int64_t h, int64_t f, int32_t N, tp_dtype dtype, tp_act act,
+                               tp_reduce mode, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Pre-LN transformer layer with the tensor-parallel attention block and GELU MLP
  * [Megatron-LM 实战 04 张量并行实现, 核心实现, TPTransformerLayer]:
  *   x1 = x + Attn(LN1(x)),  out = x1 + MLP(LN2(x1)).
  * tp_layer_fwd fills every field of *saved; tp_layer_bwd reads them and writes dx and
  * every field of *grads. Sizes: M = b*s tokens, h hidden, f MLP width, n_heads, N shards.
+ * The shard sum after W_o and LN2 run as one pass (tp_row_linear_ln), so h <= 16384.
  * ws: tp_workspace_size(TP_OP_LAYER_FWD / TP_OP_LAYER_BWD, b*s, h, f, N, dtype, 0, mode).
+ * Errors: those of tp_attn_proj_fwd / _bwd and tp_mlp_fwd / _bwd.
  */
 TP_API tp_status tp_layer_fwd(const void* x, const tp_layer_weights* w, const tp_layer_saved* saved,
                               void* out, int64_t b, int64_t s, int64_t h, int64_t f,

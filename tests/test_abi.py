@@ -95,6 +95,37 @@ def test_row_and_mlp_argument_errors(L):
                                                             M=4, n=8, out_dtype=BF), **kw}))
     assert _status(s()) == T.Status.INVALID_ARG
     assert _status(s(N=2, out=A16 + 4)) == T.Status.ALIGNMENT
+    rl = lambda **kw: (lambda: T.tp_shard_reduce_ln(**{**dict(
+        partials=A16, residual=None, gamma=A16, beta=A16, sum_out=None, y=A16, mean=None,
+        rstd=None, N=2, M=4, h=64, eps=1e-5, dtype=BF), **kw}))
+    assert _status(rl(y=None)) == T.Status.INVALID_ARG
+    assert _status(rl(h=60)) == T.Status.SHAPE            # h % 8
+    assert _status(rl(h=16384 + 8)) == T.Status.SHAPE     # wider than one row group holds
+    assert _status(rl(eps=-1.0)) == T.Status.INVALID_ARG
+    assert _status(rl(gamma=A16 + 4)) == T.Status.ALIGNMENT
+    rr = lambda **kw: (lambda: T.tp_row_linear_ln(**{**dict(
+        Xs=A16, W=A16, residual=None, gamma=A16, beta=A16, sum_out=A16, y=A16, mean=None,
+        rstd=None, M=10, k=256, n=128, N=2, eps=1e-5, dtype=BF, mode=T.Reduce.BUFFERS, ws=None,
+        ws_bytes=0), **kw}))
+    assert _status(rr()) == T.Status.WORKSPACE             # buffers mode needs the partials
+    assert _status(rr(sum_out=None)) == T.Status.INVALID_ARG
+    assert _status(rr(k=250)) == T.Status.SHAPE            # k % N
+    assert _status(rr(n=100)) == T.Status.SHAPE            # bf16 tile rule / n % 8
+    spf = lambda **kw: (lambda: T.tp_sp_mlp_fwd(**{**dict(
+        x=A16, gamma=A16, beta=A16, W1=A16, W1_up=None, W2=A16, xn=A16, mean=A16, rstd=A16,
+        Y=A16, Y_up=None, H=A16, out=A16, M=12, h=128, f=256, N=4, dtype=BF, act=T.Act.GELU,
+        mode=T.Reduce.BUFFERS, ws=None, ws_bytes=0), **kw}))
+    assert _status(spf(M=10)) == T.Status.SHAPE           # M % N
+    assert _status(spf(H=None)) == T.Status.INVALID_ARG
+    assert _status(spf()) == T.Status.WORKSPACE           # buffers mode needs the partials
+    spb = lambda **kw: (lambda: T.tp_sp_mlp_bwd(**{**dict(
+        x=A16, gamma=A16, W1=A16, W1_up=None, W2=A16, xn=A16, mean=A16, rstd=A16, Y=A16,
+        Y_up=None, H=A16, dout=A16, dx=A16, dgamma=A16, dbeta=A16, dgamma_ranks=None,
+        dbeta_ranks=None, dW1=A16, dW1_up=None, dW2=A16, M=12, h=128, f=256, N=4, dtype=BF,
+        act=T.Act.GELU, mode=T.Reduce.SPLITK, ws=A16, ws_bytes=1 << 30), **kw}))
+    assert _status(spb(dgamma=None)) == T.Status.INVALID_ARG
+    assert _status(spb(ws_bytes=16)) == T.Status.WORKSPACE
+    assert _status(spb(M=14)) == T.Status.SHAPE
 
 
 def test_workspace_sizes(L):
