@@ -14,6 +14,7 @@ Generator (a published, counter-based construction, restated here):
     element 2j = r cos(theta), element 2j+1 = r sin(theta).
   * value = sigma * n, rounded to the storage type: fp32 by IEEE round-to-nearest-
     even, bf16 by round-to-nearest-even of the fp32 bit pattern.
+  * uniform tensors: lo + (hi - lo) * u_i; integers on [0, n): floor(u_i * n).
 
 The key of a tensor is mix(seed), seed = 1000 * config_id + tensor_id, so every
 tensor of every workload is its own stream, and element i of a tensor does not
@@ -35,7 +36,7 @@ _M2 = np.uint64(0x94D049BB133111EB)
 TENSOR_ID = {
     "X": 1, "W1": 2, "Wg": 2, "Wu": 3, "W2": 4, "Wd": 4, "dZ": 5,
     "Wqkv": 6, "Wo": 7, "gamma1": 8, "beta1": 9, "gamma2": 10, "beta2": 11,
-    "R": 12,
+    "R": 12, "E": 13, "ids": 14, "targets": 15, "gammaf": 16, "betaf": 17,
 }
 
 _CHUNK = 1 << 22
@@ -134,6 +135,32 @@ def normal_rows(shape, rows, seed: int, sigma: float = 1.0, dtype: str = "bf16")
             tmp[:] = _fill_row
         out[j] = tmp
     return out.reshape((len(rows),) + shape[1:])
+
+
+def _uniform01(key: np.uint64, n: int) -> np.ndarray:
+    """u_i = (SplitMix64 output i >> 11) * 2^-53 in [0, 1), i = 0 .. n-1."""
+    i = np.arange(n, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        return (_mix(key + (i + np.uint64(1)) * GAMMA) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+
+
+def uniform(shape, seed: int, lo: float, hi: float, dtype: str = "f32") -> np.ndarray:
+    """Seeded U[lo, hi) tensor: lo + (hi - lo) * u, rounded to `dtype` like `normal`."""
+    shape = tuple(int(s) for s in shape)
+    n = int(np.prod(shape)) if shape else 1
+    v = lo + (hi - lo) * _uniform01(stream_key(seed), n)
+    if dtype == "f32":
+        return v.astype(np.float32).reshape(shape)
+    if dtype == "bf16":
+        return f32_to_bf16_bits(v.astype(np.float32)).reshape(shape)
+    return v.reshape(shape)
+
+
+def integers(shape, seed: int, n: int) -> np.ndarray:
+    """Seeded integers uniform on [0, n): floor(u * n) with u of `_uniform01` (int32)."""
+    shape = tuple(int(s) for s in shape)
+    cnt = int(np.prod(shape)) if shape else 1
+    return np.floor(_uniform01(stream_key(seed), cnt) * n).astype(np.int32).reshape(shape)
 
 
 def to_f64(a: np.ndarray, dtype: str) -> np.ndarray:

@@ -121,3 +121,40 @@ def test_sp_rank_rows_swapped_is_caught(monkeypatch):
     import pytest
     with pytest.raises(AssertionError):
         pins.test_sp_mlp_block_equals_unsplit_and_fd("gelu", 2)
+
+
+def test_tied_embedding_missing_input_grad_is_caught(monkeypatch):
+    """grad_total = grad_out only (the input layer's gradient dropped)."""
+    from oracle import gpt_oracle as G
+    from tests import test_oracle_gpt_pins as gp
+    monkeypatch.setattr(G, "vocab_embed_bwd", lambda ids, dx, v, N: np.zeros((v, dx.shape[1])))
+    import pytest
+    with pytest.raises(AssertionError):
+        gp.test_gpt_backward_fd()
+
+
+def test_ce_grad_without_onehot_is_caught(monkeypatch):
+    from oracle import gpt_oracle as G
+    from tests import test_oracle_gpt_pins as gp
+
+    def bad(logits, targets, lse, N, scale):
+        return np.exp(logits - lse[:, None]) * scale
+    monkeypatch.setattr(G, "vocab_ce_bwd", bad)
+    import pytest
+    with pytest.raises(AssertionError):
+        gp.test_vocab_ce_bwd_fd(2)
+
+
+def test_adamw_without_bias_correction_is_caught(monkeypatch):
+    from oracle import gpt_oracle as G
+    from tests import test_oracle_gpt_pins as gp
+
+    def bad(p, g, m, v, t, lr, beta1, beta2, eps, weight_decay):
+        p = p * (1.0 - lr * weight_decay)
+        m = beta1 * m + (1.0 - beta1) * g
+        v = beta2 * v + (1.0 - beta2) * g * g
+        return p - lr * m / (np.sqrt(v) + eps), m, v
+    monkeypatch.setattr(G, "adamw_step", bad)
+    import pytest
+    with pytest.raises(AssertionError):
+        gp.test_adamw_first_steps_closed_form()
