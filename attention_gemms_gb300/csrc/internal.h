@@ -130,6 +130,22 @@ tp_status launch_attention_bwd(const void* qkv, const void* o, const float* lse,
                                void* dqkv, int64_t b, int64_t s, int64_t h, int heads, int causal,
                                tp_dtype dt, cudaStream_t st);
 
+// vocabulary-parallel embedding / cross-entropy and AdamW (vocab.cu)
+tp_status launch_vocab_embed_fwd(const int32_t* ids, const void* E, void* x, int64_t M, int64_t v,
+                                 int64_t h, int N, tp_dtype dt, cudaStream_t st);
+tp_status launch_vocab_embed_bwd(const int32_t* ids, const void* dx, void* dE, int64_t M,
+                                 int64_t v, int64_t h, bool accumulate, tp_dtype dt,
+                                 cudaStream_t st);
+tp_status launch_vocab_ce_fwd(const void* logits, const int32_t* targets, float* lse,
+                              float* row_loss, float* shard_loss, float* loss, int64_t M,
+                              int64_t v, int N, tp_dtype dt, cudaStream_t st);
+tp_status launch_vocab_ce_bwd(const void* logits, const int32_t* targets, const float* lse,
+                              void* dlogits, int64_t M, int64_t v, float scale, tp_dtype dt,
+                              cudaStream_t st);
+tp_status launch_adamw(float* p, const float* g, float* m, float* v, int64_t n, float lr,
+                       float b1, float b2, float eps, float wd, float bc1, float bc2,
+                       cudaStream_t st);
+
 // ------------------------------------------------------------------ API helpers (api.cu)
 
 tp_status need(bool cond, tp_status s, const char* msg);

@@ -172,3 +172,28 @@ def to_f64(a: np.ndarray, dtype: str) -> np.ndarray:
 
 def seed_of(config_id: int, name: str) -> int:
     return 1000 * int(config_id) + TENSOR_ID[name]
+
+
+def gpt_inputs(config_id: int, vocab: int, hidden: int, ffn: int, layers: int, batch: int,
+               seq: int):
+    """Seeded parameters and one batch of the small GPT, as float32 / int32 arrays:
+    E ~ U(-1/sqrt(h), 1/sqrt(h)) (the output layer's default initialisation, whose
+    tensor the embedding shares), the layers' weights ~ N(0, 0.02^2), LayerNorm gamma = 1,
+    beta = 0, token ids and targets uniform on [0, vocab). Layer l's tensors use seeds
+    offset by 100 * (l + 1)."""
+    h, f = hidden, ffn
+    bound = 1.0 / np.sqrt(h)
+    p = {"E": uniform((vocab, h), seed_of(config_id, "E"), -bound, bound, "f32"),
+         "gammaf": np.ones(h, np.float32), "betaf": np.zeros(h, np.float32)}
+    shp = {"Wqkv": (h, 3 * h), "Wo": (h, h), "W1": (h, f), "W2": (f, h)}
+    for li in range(layers):
+        off = 100 * (li + 1)
+        for k, sh in shp.items():
+            p[f"L{li}.{k}"] = normal(sh, seed_of(config_id, k) + off, 0.02, "f32")
+        for k in ("gamma1", "gamma2"):
+            p[f"L{li}.{k}"] = np.ones(h, np.float32)
+        for k in ("beta1", "beta2"):
+            p[f"L{li}.{k}"] = np.zeros(h, np.float32)
+    ids = integers((batch, seq), seed_of(config_id, "ids"), vocab)
+    targets = integers((batch, seq), seed_of(config_id, "targets"), vocab)
+    return p, ids, targets

@@ -77,6 +77,25 @@ class LayerGrads(ctypes.Structure):
                 ("dWqkv", "dWo", "dW1", "dW2", "dgamma1", "dbeta1", "dgamma2", "dbeta2")]
 
 
+class GptConfig(ctypes.Structure):
+    """tp_gpt_config"""
+    _fields_ = [("vocab", ctypes.c_int64), ("hidden", ctypes.c_int64), ("heads", ctypes.c_int64),
+                ("ffn", ctypes.c_int64), ("layers", ctypes.c_int64), ("batch", ctypes.c_int64),
+                ("seq", ctypes.c_int64), ("shards", ctypes.c_int32)]
+
+
+class GptWeights(ctypes.Structure):
+    """tp_gpt_weights"""
+    _fields_ = [("E", ctypes.c_void_p), ("gammaf", ctypes.c_void_p), ("betaf", ctypes.c_void_p),
+                ("layers", ctypes.POINTER(LayerWeights))]
+
+
+class GptGrads(ctypes.Structure):
+    """tp_gpt_grads"""
+    _fields_ = [("dE", ctypes.c_void_p), ("dgammaf", ctypes.c_void_p), ("dbetaf", ctypes.c_void_p),
+                ("layers", ctypes.POINTER(LayerGrads))]
+
+
 def make_struct(cls, **tensors):
     """Fill one of the layer structs from tensors / addresses / None by field name."""
     return cls(**{k: _ptr(v) for k, v in tensors.items()})
@@ -128,6 +147,14 @@ _SIGS = {
     "tp_layer_bwd": (_ST, [_P, ctypes.POINTER(LayerWeights), ctypes.POINTER(LayerSaved), _P, _P,
                            ctypes.POINTER(LayerGrads), _I64, _I64, _I64, _I64, _I32, _I32,
                            ctypes.c_int, _ST, _ST, _P, _SZ, _P]),
+    "tp_vocab_embed_fwd": (_ST, [_P, _P, _P, _I64, _I64, _I64, _I32, _ST, _P]),
+    "tp_vocab_embed_bwd": (_ST, [_P, _P, _P, _I64, _I64, _I64, _I32, ctypes.c_int, _ST, _P]),
+    "tp_vocab_ce_fwd": (_ST, [_P] * 6 + [_I64, _I64, _I32, _ST, _P]),
+    "tp_vocab_ce_bwd": (_ST, [_P] * 4 + [_I64, _I64, _I32, ctypes.c_float, _ST, _P]),
+    "tp_adamw_step": (_ST, [_P] * 4 + [_I64, _I64] + [ctypes.c_float] * 5 + [_P]),
+    "tp_gpt_workspace_size": (_SZ, [ctypes.POINTER(GptConfig), _ST, _ST]),
+    "tp_gpt_fwd_bwd": (_ST, [ctypes.POINTER(GptConfig), ctypes.POINTER(GptWeights),
+                             ctypes.POINTER(GptGrads), _P, _P, _P, _ST, _ST, _P, _SZ, _P]),
     "tp_row_linear_noalloc": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _ST, _P]),
     "tp_debug_inject_wait_fault": (None, [ctypes.c_int]),
 }
@@ -293,6 +320,44 @@ def tp_sp_mlp_bwd(x, gamma, W1, W1_up, W2, xn, mean, rstd, Y, Y_up, H, dout, dx,
                                                    dbeta_ranks, dW1, dW1_up, dW2)],
                                M, h, f, N, int(dtype), int(act), int(mode), _ptr(ws),
                                int(ws_bytes), _stream(stream)))
+
+
+def tp_vocab_embed_fwd(ids, E, x, M, vocab, h, N, dtype, stream=None):
+    _check(lib().tp_vocab_embed_fwd(_ptr(ids), _ptr(E), _ptr(x), M, vocab, h, N, int(dtype),
+                                    _stream(stream)))
+
+
+def tp_vocab_embed_bwd(ids, dx, dE, M, vocab, h, N, accumulate, dtype, stream=None):
+    _check(lib().tp_vocab_embed_bwd(_ptr(ids), _ptr(dx), _ptr(dE), M, vocab, h, N,
+                                    int(bool(accumulate)), int(dtype), _stream(stream)))
+
+
+def tp_vocab_ce_fwd(logits, targets, lse, row_loss, shard_loss, loss, M, vocab, N, dtype,
+                    stream=None):
+    _check(lib().tp_vocab_ce_fwd(_ptr(logits), _ptr(targets), _ptr(lse), _ptr(row_loss),
+                                 _ptr(shard_loss), _ptr(loss), M, vocab, N, int(dtype),
+                                 _stream(stream)))
+
+
+def tp_vocab_ce_bwd(logits, targets, lse, dlogits, M, vocab, N, scale, dtype, stream=None):
+    _check(lib().tp_vocab_ce_bwd(_ptr(logits), _ptr(targets), _ptr(lse), _ptr(dlogits), M, vocab,
+                                 N, float(scale), int(dtype), _stream(stream)))
+
+
+def tp_adamw_step(p, g, m, v, n, step, lr, beta1, beta2, eps, weight_decay, stream=None):
+    _check(lib().tp_adamw_step(_ptr(p), _ptr(g), _ptr(m), _ptr(v), n, step, float(lr),
+                               float(beta1), float(beta2), float(eps), float(weight_decay),
+                               _stream(stream)))
+
+
+def tp_gpt_workspace_size(cfg, dtype, mode):
+    return int(lib().tp_gpt_workspace_size(ctypes.byref(cfg), int(dtype), int(mode)))
+
+
+def tp_gpt_fwd_bwd(cfg, weights, grads, ids, targets, loss, dtype, mode, ws, ws_bytes, stream=None):
+    _check(lib().tp_gpt_fwd_bwd(ctypes.byref(cfg), ctypes.byref(weights), ctypes.byref(grads),
+                                _ptr(ids), _ptr(targets), _ptr(loss), int(dtype), int(mode),
+                                _ptr(ws), int(ws_bytes), _stream(stream)))
 
 
 def tp_row_linear_noalloc(Xs, W, residual, out, M, k, n, N, dtype, stream=None):

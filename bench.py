@@ -47,6 +47,10 @@ WORKLOADS = {
     "c3-sp": dict(desc="sequence-parallel pre-LN erf-GELU MLP block fwd+bwd (LN on each rank's "
                        "rows, reduce-scatter + all-gather): b=4 s=2048 h=4096 ffn=16384 N=8",
                   b=4, s=2048, h=4096, f=16384, N=8, act="gelu", cfg=3, sp=True),
+    "gpt": dict(desc="small tensor-parallel GPT training (vocabulary-parallel embedding and "
+                     "cross-entropy, tied output layer, AdamW): vocab=256 h=128 heads=8 ffn=512 "
+                     "layers=2 b=4 s=32 N=2, fp32", b=4, s=32, h=128, f=512, N=2, heads=8,
+                vocab=256, layers=2, act="gelu", cfg=6, gpt=True, dtype="f32"),
     # reduced-token case of c5 for ncu captures (a few GB on the device, inputs > L2)
     "c5-2k": dict(desc="profiling case: SwiGLU MLP fwd+bwd b=1 s=2048 h=8192 ffn=28672 N=4",
                   b=1, s=2048, h=8192, f=28672, N=4, act="swiglu", cfg=5),
@@ -256,6 +260,8 @@ def run_ours(args, w):
         return run_layer(args, w, T, device, rank, ws_)
     if w.get("sp"):
         return run_sp(args, w, T, device, rank, ws_)
+    if w.get("gpt"):
+        return run_gpt(args, w, T, device, rank, ws_)
     M, h, f, N = w["b"] * w["s"], w["h"], w["f"], w["N"]
     sw = w["act"] == "swiglu"
     act = T.Act.SWIGLU if sw else T.Act.GELU
@@ -516,6 +522,169 @@ def run_sp(args, w, T, device, rank, nranks):
         res["cpu_baseline"] = cpu_baseline(w, hostin, budget_s=args.cpu_budget)
     if rank == 0:
         print(json.dumps(res), flush=True)
+
+
+def gpt_flops(w):
+    """Algorithmic FLOPs of one training step: 3 x the forward's matrix products
+    (layers' linear maps and attention, output layer)."""
+    M, h, f, v, L = w["b"] * w["s"], w["h"], w["f"], w["vocab"], w["layers"]
+    per_layer = 2 * M * h * (3 * h + h + 2 * f) + 4 * w["b"] * w["s"] * w["s"] * h
+    return 3.0 * (L * per_layer + 2 * M * h * v)
+
+
+def run_vocab_ce(device, T, M=8192, v=50304, N=8, reps=20):
+    """Vocabulary-parallel cross-entropy, forward + backward (in place), bf16 logits at
+    a GPT-2-sized vocabulary: HBM-bound; algorithmic bytes = the logits read by the
+    forward, read and written by the backward (+ targets, lse, row losses)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(77)
+    L = (torch.randn((M, v), generator=g, device=device) * 2).to(torch.bfloat16)
+    tg = torch.randint(0, v, (M,), generator=g, device=device, dtype=torch.int32)
+    f = lambda *sh: torch.empty(sh, dtype=torch.float32, device=device)
+    lse, rows, shards, loss = f(M), f(M), f(N), f(1)
+    stream = torch.cuda.current_stream()
+    BF = T.DType.BF16
+
+    def fwd():
+        T.tp_vocab_ce_fwd(L, tg, lse, rows, shards, loss, M, v, N, BF, stream)
+
+    def bwd():
+        T.tp_vocab_ce_bwd(L, tg, lse, L, M, v, N, 1.0 / M, BF, stream)
+    out = {"shape": {"M": M, "vocab": v, "N": N, "dtype": "bf16"}, "unit": "GB/s"}
+    peaks, src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    for name, fn, nbytes in (("fwd", fwd, M * v * 2 + 16 * M), ("bwd", bwd, 2 * M * v * 2 + 8 * M)):
+        for _ in range(3):
+            fwd()
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            fwd()  # the backward needs the forward's lse; both rewrite nothing they read
+            a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            z.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(z))
+        us = float(np.median(ts)) * 1e3
+        out[name] = {"us": round(us, 2), "algorithmic_bytes": int(nbytes),
+                     "achieved": round(nbytes / us / 1e3, 1), "frac": round(nbytes / us / 1e3 / hbm, 4)}
+    out["peak"], out["peak_source"] = hbm, f"{src} HBM copy"
+    del L
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_gpt(args, w, T, device, rank, nranks):
+    """The small GPT's training step (forward, backward, AdamW) on one seeded batch,
+    the page's 50-step run, plus the vocabulary-parallel cross-entropy at a large
+    vocabulary for its HBM roofline."""
+    import torch
+    from attention_gemms_gb300 import gpt as GP
+    from attention_gemms_gb300 import synth
+    mode = T.Reduce.SPLITK if args.mode == "splitk" else T.Reduce.BUFFERS
+    steps_run = 50
+    t_gen = time.time()
+    p, ids, tg = synth.gpt_inputs(w["cfg"], w["vocab"], w["h"], w["f"], w["layers"], w["b"], w["s"])
+    t_gen = time.time() - t_gen
+    m = GP.SmallGPT(w["vocab"], w["h"], w["heads"], w["f"], w["layers"], w["b"], w["s"], w["N"],
+                    mode=mode, steps=steps_run, device=device)
+    m.load(p)
+    m.set_batch(ids, tg)
+    stream = torch.cuda.current_stream()
+    # the page's run from the loaded parameters: 50 steps, losses kept on the device
+    for _ in range(steps_run):
+        m.step(stream=stream)
+    torch.cuda.synchronize()
+    trajectory = m.losses.cpu().numpy().tolist()
+    for _ in range(args.warmup):
+        m.step(stream=stream)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(device.index)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    n0 = T.tp_launch_count()
+    a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        m.step(stream=stream)
+    z.record(stream)
+    torch.cuda.synchronize()
+    launches = T.tp_launch_count() - n0
+    ms = a.elapsed_time(z) / args.steps
+    # end to end: the batch's ids and targets in from pinned host memory, the loss out
+    idp = torch.from_numpy(np.asarray(ids, np.int32).reshape(-1)).pin_memory()
+    tgp = torch.from_numpy(np.asarray(tg, np.int32).reshape(-1)).pin_memory()
+    lossp = torch.empty(1, dtype=torch.float32, pin_memory=True)
+    barrier()
+    a.record(stream)
+    for _ in range(args.steps):
+        m.ids.copy_(idp, non_blocking=True)
+        m.targets.copy_(tgp, non_blocking=True)
+        slot = m.t % m.losses.numel()
+        m.step(stream=stream)
+        lossp.copy_(m.losses[slot:slot + 1], non_blocking=True)
+    z.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(z) / args.steps
+    clk = clocks.stop()
+    if T.tp_check_status(stream) != 0:
+        raise RuntimeError("device wait timeout: " + T.tp_last_error())
+    ce = run_vocab_ce(device, T)
+    ms_max, e2e_max = max_over_ranks(ms, device), max_over_ranks(e2e_ms, device)
+    M = w["b"] * w["s"]
+    tok = M * nranks / (ms_max * 1e-3)
+    res = {
+        "metric": "small GPT training tokens/s (vocabulary-parallel embedding + cross-entropy)",
+        "value": round(tok, 1), "unit": "tokens/s", "n_gpus": nranks, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded random tokens and targets; E ~ U(-1/sqrt(h), 1/sqrt(h)), "
+                "weights ~ N(0, 0.02^2))",
+        "config": {"workload": w["desc"], "tokens": M, "vocab": w["vocab"], "h": w["h"],
+                   "ffn": w["f"], "layers": w["layers"], "heads": w["heads"], "shards": w["N"],
+                   "shard_sum": args.mode, "parallelism": f"tp{w['N']} virtual ranks per GPU, "
+                   f"dp{nranks}", "l2": "whole model L2-resident (latency-bound size)"},
+        "tflops": round(gpt_flops(w) * nranks / (ms_max * 1e-3) / 1e12, 4),
+        "loss_trajectory_every_10": [round(x, 4) for x in trajectory[::10]] + [round(trajectory[-1], 4)],
+        "roofline": {"bound": "hbm", "kernel": "vocab_ce_bwd_kernel (vocabulary-parallel "
+                     "cross-entropy gradient, bf16 logits, M=8192 v=50304 N=8, timed on its own)",
+                     "achieved": ce["bwd"]["achieved"], "peak": ce["peak"], "unit": "GB/s",
+                     "frac": ce["bwd"]["frac"], "traffic": None,
+                     "note": "the GPT step itself is launch/latency-bound at this size"},
+        "vocab_ce": ce,
+        "e2e": {"value": round(M * nranks / (e2e_max * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": 2 * M * 4, "d2h_bytes_per_step": 4,
+                "ms_per_step": round(e2e_max, 4)},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "input_gen_s": round(t_gen, 1),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = gpt_cpu_baseline(w, p, ids, tg)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+def gpt_cpu_baseline(w, p, ids, tg, steps=3):
+    """The fp64 oracle's training step (forward, backward, AdamW) on the same batch."""
+    from oracle import gpt_oracle as G
+    f64 = {k: np.asarray(a, np.float64) for k, a in p.items()}
+    params = {"E": f64["E"], "gammaf": f64["gammaf"], "betaf": f64["betaf"],
+              "layers": [{k: f64[f"L{li}.{k}"] for k in G.LAYER_KEYS} for li in range(w["layers"])]}
+    cfg = dict(b=w["b"], s=w["s"], heads=w["heads"], N=w["N"])
+    c0, t0 = time.process_time(), time.perf_counter()
+    G.gpt_train(params, ids, tg, cfg, steps)
+    dt, dc = (time.perf_counter() - t0) / steps, (time.process_time() - c0) / steps
+    M = w["b"] * w["s"]
+    return {"value": round(M / dt, 1), "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+            "threads_effective": round(dc / dt, 1), "kind": "oracle",
+            "sample": f"fp64 oracle training steps (forward, backward, AdamW) on the full batch, "
+                      f"{steps} steps, {dt * 1e3:.0f} ms each"}
 
 
 # ------------------------------------------------------------------ page-2 layer
@@ -888,7 +1057,21 @@ def run_reference(args, w):
     M, h, f = w["b"] * w["s"], w["h"], w["f"]
     c = w["cfg"]
     dtp = w.get("dtype", "bf16")
-    if w.get("layer"):
+    metric, unit, scale = METRIC, "TFLOP/s", 1e12
+    if w.get("gpt"):
+        from oracle import gpt_oracle as G
+        pr, ids, tg = synth.gpt_inputs(c, w["vocab"], h, f, w["layers"], w["b"], w["s"])
+        f64 = {k: np.asarray(a, np.float64) for k, a in pr.items()}
+        params = {"E": f64["E"], "gammaf": f64["gammaf"], "betaf": f64["betaf"],
+                  "layers": [{k: f64[f"L{li}.{k}"] for k in G.LAYER_KEYS}
+                             for li in range(w["layers"])]}
+        gcfg = dict(b=w["b"], s=w["s"], heads=w["heads"], N=w["N"])
+        run = lambda: G.gpt_train(params, ids, tg, gcfg, 1)
+        flops = M  # tokens per step
+        metric = "small GPT training tokens/s (vocabulary-parallel embedding + cross-entropy)"
+        unit, scale = "tokens/s", 1.0
+        sample = "fp64 oracle training step (forward, backward, AdamW) on the whole batch"
+    elif w.get("layer"):
         from oracle import tp_oracle as O
         hin = layer_inputs(w, 0)
         f64 = lambda a: synth.to_f64(a, "bf16") if a.dtype == np.uint16 else a.astype(np.float64)
@@ -920,18 +1103,18 @@ def run_reference(args, w):
     for _ in range(args.steps):
         run()
     dt, dc = (time.perf_counter() - t0) / args.steps, (time.process_time() - c0) / args.steps
-    val = flops / dt / 1e12
+    val = flops / dt / scale
     print(json.dumps({
-        "metric": METRIC, "value": round(val, 6), "unit": "TFLOP/s", "n_gpus": ws_,
+        "metric": metric, "value": round(val, 6), "unit": unit, "n_gpus": ws_,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)", "impl": "reference",
         "config": {"workload": w["desc"], "tokens": M, "h": h, "ffn": f, "shards": w["N"],
                    "act": w["act"]},
-        "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "kind": "oracle",
+        "cpu_baseline": {"value": round(val, 6), "unit": unit, "kind": "oracle",
                          "cores": len(os.sched_getaffinity(0)),
                          "threads_effective": round(dc / dt, 1), "sample": sample},
-        "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": round(val, 6), "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "input_gen_s": round(t_gen, 1),
     }), flush=True)
@@ -944,7 +1127,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="c5", choices=sorted(WORKLOADS) + ["c4"],
                     help="c5 (default): large SwiGLU MLP; c3: GELU MLP; c2: page-2 layer; "
-                         "c1: tiny fp32 MLP; c4: decode sweep only; c5-2k: profiling case")
+                         "c1: tiny fp32 MLP; c4: decode sweep only; c5-2k: profiling case; "
+                         "c3-sp: sequence-parallel MLP block; gpt: small GPT training")
     ap.add_argument("--mode", default="splitk", choices=["splitk", "buffers"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-rows", type=int, default=64)

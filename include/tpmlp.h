@@ -144,6 +144,33 @@ typedef struct tp_layer_grads {
   float* dbeta2;
 } tp_layer_grads;
 
+/* The small tensor-parallel GPT: embedding (vocabulary-parallel, shared with the output
+ * layer), `layers` pre-LN layers, final LayerNorm, output layer, cross-entropy. */
+typedef struct tp_gpt_config {
+  int64_t vocab;   /* v, divisible by N */
+  int64_t hidden;  /* h */
+  int64_t heads;   /* attention heads (head_dim = h / heads in {16, 32, 64}) */
+  int64_t ffn;     /* f */
+  int64_t layers;
+  int64_t batch;   /* b */
+  int64_t seq;     /* s; token rows M = b*s, the s rows of one sequence consecutive */
+  int32_t shards;  /* N */
+} tp_gpt_config;
+
+typedef struct tp_gpt_weights {
+  const void* E;                   /* (vocab, h): embedding, and the output layer's weight */
+  const float* gammaf;             /* (h) final LayerNorm */
+  const float* betaf;
+  const tp_layer_weights* layers;  /* `layers` entries */
+} tp_gpt_weights;
+
+typedef struct tp_gpt_grads {
+  void* dE;                        /* (vocab, h): output layer's gradient + embedding's */
+  float* dgammaf;
+  float* dbetaf;
+  const tp_layer_grads* layers;    /* `layers` entries */
+} tp_gpt_grads;
+
 /* ------------------------------------------------------------------ utilities */
 
 /* Library version (TPMLP_VERSION). */
@@ -485,6 +512,69 @@ TP_API tp_status tp_layer_bwd(const void* x, const tp_layer_weights* w,
                               const tp_layer_grads* grads, int64_t b, int64_t s, int64_t h,
                               int64_t f, int32_t n_heads, int32_t N, int causal, tp_dtype dtype,
                               tp_reduce mode, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------ vocabulary-parallel
+ * embedding, cross-entropy, the small GPT and its optimiser. Shard i of the vocabulary
+ * owns rows [i v/N, (i+1) v/N) of E and the same columns of the logits. Token ids and
+ * targets are int32 device arrays; ids or targets outside [0, v) give a zero embedding
+ * row and a zero loss / gradient row (the mean still divides by M). */
+
+/* x[t] = sum_i (E_i[ids[t]] if shard i owns ids[t], else 0): every shard looks up the ids
+ * it owns and the all-reduce adds the results [张量并行 notes, §嵌入层的并行化, input].
+ *   ids (M) int32;  E (vocab, h) read;  x (M, h) written.
+ * Errors: TP_ERR_INVALID_ARG, TP_ERR_SHAPE (vocab % N), TP_ERR_DTYPE, TP_ERR_ALIGNMENT. */
+TP_API tp_status tp_vocab_embed_fwd(const int32_t* ids, const void* E, void* x, int64_t M,
+                                    int64_t vocab, int64_t h, int32_t N, tp_dtype dtype,
+                                    void* stream);
+
+/* dE[v] (+)= sum over tokens t with ids[t] == v of dx[t], in token order (shard i fills
+ * its own rows). accumulate != 0 adds to dE (e.g. to the output layer's gradient of a
+ * shared embedding: grad_total = grad_in + grad_out [张量并行 notes, §嵌入层的并行化]);
+ * 0 overwrites it. */
+TP_API tp_status tp_vocab_embed_bwd(const int32_t* ids, const void* dx, void* dE, int64_t M,
+                                    int64_t vocab, int64_t h, int32_t N, int accumulate,
+                                    tp_dtype dtype, void* stream);
+
+/* Cross-entropy of logits (M, vocab) against targets (M), vocabulary-parallel
+ * [张量并行 notes, §损失计算层的并行化]: m = all-reduce(max) of the shards' row maxima,
+ * S = all-reduce(sum) of the shards' sums of exp(l - m), the target's shard adds
+ * log S + m - l_target to its loss, and the loss is the sum of the N shard losses / M.
+ *   lse (M) fp32 written (m + log S, for the backward); row_loss (M) fp32 written;
+ *   shard_loss (N) fp32 written or NULL; loss (1) fp32 device written (the mean). */
+TP_API tp_status tp_vocab_ce_fwd(const void* logits, const int32_t* targets, float* lse,
+                                 float* row_loss, float* shard_loss, float* loss, int64_t M,
+                                 int64_t vocab, int32_t N, tp_dtype dtype, void* stream);
+
+/* dlogits = scale * (softmax(logits) - one_hot(targets)), from lse; dlogits may be the
+ * logits buffer itself (in place). scale = 1/M for the mean loss. */
+TP_API tp_status tp_vocab_ce_bwd(const void* logits, const int32_t* targets, const float* lse,
+                                 void* dlogits, int64_t M, int64_t vocab, int32_t N,
+                                 float scale, tp_dtype dtype, void* stream);
+
+/* AdamW with decoupled weight decay over n fp32 values, step >= 1 (bias corrections
+ * 1 - beta^step): p <- p (1 - lr wd); m <- b1 m + (1-b1) g; v <- b2 v + (1-b2) g^2;
+ * p <- p - lr (m / bc1) / (sqrt(v / bc2) + eps). The listing of the Megatron-LM 实战 04
+ * page trains its GPT with AdamW; the paper has no kernel for it. m, v start at 0. */
+TP_API tp_status tp_adamw_step(float* p, const float* g, float* m, float* v, int64_t n,
+                               int64_t step, float lr, float beta1, float beta2, float eps,
+                               float weight_decay, void* stream);
+
+/* Bytes of workspace tp_gpt_fwd_bwd needs (0 on invalid arguments). */
+TP_API size_t tp_gpt_workspace_size(const tp_gpt_config* cfg, tp_dtype dtype, tp_reduce mode);
+
+/* Loss and every gradient of the small GPT [Megatron-LM 实战 04 张量并行实现, 核心实现,
+ * SmallGPT]: embedding (vocabulary-parallel), the layers of tp_layer_fwd, final LN,
+ * output layer x_f E^T (column-parallel over the vocabulary), vocabulary-parallel
+ * cross-entropy (mean over the M rows); then the backward: the output layer's input
+ * gradient is summed over the vocabulary shards, its weight gradient written to dE, the
+ * layers' backward, and the embedding's gradient added to dE. fp32 only (the listing
+ * trains in fp32).
+ *   ids, targets (b*s) int32;  loss (1) fp32 device written.
+ * Errors: those of the parts; TP_ERR_DTYPE for bf16; TP_ERR_SHAPE (vocab % N, heads). */
+TP_API tp_status tp_gpt_fwd_bwd(const tp_gpt_config* cfg, const tp_gpt_weights* w,
+                                const tp_gpt_grads* g, const int32_t* ids,
+                                const int32_t* targets, float* loss, tp_dtype dtype,
+                                tp_reduce mode, void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------ testing */
 

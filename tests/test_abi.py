@@ -126,6 +126,22 @@ def test_row_and_mlp_argument_errors(L):
     assert _status(spb(dgamma=None)) == T.Status.INVALID_ARG
     assert _status(spb(ws_bytes=16)) == T.Status.WORKSPACE
     assert _status(spb(M=14)) == T.Status.SHAPE
+    assert _status(lambda: T.tp_vocab_embed_fwd(A16, A16, A16, 4, 10, 8, 3, BF)) == T.Status.SHAPE
+    assert _status(lambda: T.tp_vocab_ce_fwd(A16, A16, A16, A16, None, None, 4, 12, 3, BF)) == \
+        T.Status.INVALID_ARG                                # loss pointer missing
+    assert _status(lambda: T.tp_adamw_step(A16, A16, A16, A16, 10, 0, 1e-3, 0.9, 0.999, 1e-8,
+                                           0.0)) == T.Status.INVALID_ARG   # step 0
+    cfg = T.GptConfig(256, 128, 8, 512, 2, 4, 32, 2)
+    assert T.tp_gpt_workspace_size(cfg, T.DType.F32, T.Reduce.BUFFERS) > 0
+    assert T.tp_gpt_workspace_size(cfg, BF, T.Reduce.BUFFERS) == 0        # fp32 only
+    assert T.tp_gpt_workspace_size(T.GptConfig(250, 128, 8, 512, 2, 4, 32, 3), T.DType.F32,
+                                   T.Reduce.BUFFERS) == 0                 # vocab % N
+    w, g = T.GptWeights(A16, A16, A16, None), T.GptGrads(A16, A16, A16, None)
+    assert _status(lambda: T.tp_gpt_fwd_bwd(cfg, w, g, A16, A16, A16, BF, T.Reduce.BUFFERS, A16,
+                                            1 << 30)) == T.Status.DTYPE
+    assert _status(lambda: T.tp_gpt_fwd_bwd(cfg, w, g, A16, A16, A16, T.DType.F32,
+                                            T.Reduce.BUFFERS, A16, 1 << 30)) == \
+        T.Status.INVALID_ARG                                # layer arrays missing
 
 
 def test_workspace_sizes(L):
