@@ -158,3 +158,39 @@ def test_adamw_without_bias_correction_is_caught(monkeypatch):
     import pytest
     with pytest.raises(AssertionError):
         gp.test_adamw_first_steps_closed_form()
+
+
+def test_gqa_replicas_not_synchronised_is_caught(monkeypatch):
+    """Replicated key/value heads whose weight gradients are not all-reduced: each
+    replica keeps only its own query heads' share."""
+    from oracle import gqa_oracle as Q
+    from tests import test_oracle_gqa_pins as qp
+    monkeypatch.setattr(Q, "gqa_split", lambda H, Hkv, N: (H // N, 1, 1) if N > Hkv else
+                        (H // N, Hkv // N, 1))
+    import pytest
+    with pytest.raises((AssertionError, IndexError, ValueError)):
+        qp.test_gqa_bwd_fd(4, 2, 4)
+
+
+def test_gqa_wrong_group_is_caught(monkeypatch):
+    """Query head t paired with key/value head t % Hkv instead of t // (H / Hkv)."""
+    from oracle import gqa_oracle as Q
+    from oracle import tp_oracle as T0
+    from tests import test_oracle_gqa_pins as qp
+
+    def bad(xn, Wq, Wk, Wv, b, s, H, Hkv, causal=False):
+        d = Wq.shape[1] // H
+        Qm, K, V = xn @ Wq, xn @ Wk, xn @ Wv
+        O = np.zeros((xn.shape[0], H * d))
+        for t in range(H):
+            j = t % Hkv
+            for bb in range(b):
+                r = slice(bb * s, (bb + 1) * s)
+                O[r, t * d:(t + 1) * d] = T0.attention_head_fwd(
+                    Qm[r, t * d:(t + 1) * d], K[r, j * d:(j + 1) * d], V[r, j * d:(j + 1) * d],
+                    causal)[0]
+        return O
+    monkeypatch.setattr(Q, "gqa_attention_unsplit", bad)
+    import pytest
+    with pytest.raises(AssertionError):
+        qp.test_gqa_grouping_head_by_head()
