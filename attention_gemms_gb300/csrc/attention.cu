@@ -1,9 +1,14 @@
 // Per-head softmax attention of the head-sharded attention block, forward and
 // backward. Heads are independent [张量并行 notes, §Multi-Head Attention 的并行化], so
 // shard i's heads (a contiguous range of grid.y) never exchange data with other
-// shards. Layout: qkv (M, 3h) with M = b*s rows, W_qkv = [W_q | W_k | W_v] so head t
-// of Q, K, V sits at columns t*d, h + t*d, 2h + t*d; o (M, h), head t at t*d;
-// lse (b, heads, s) the log-sum-exp of each score row.
+// shards. A head map places the heads in the qkv rows (M = b*s rows):
+//  * multi-head layout: W_qkv = [W_q | W_k | W_v], head t of Q, K, V at columns t*d,
+//    h + t*d, 2h + t*d;
+//  * grouped-query layout (per-shard blocks): shard i's columns are one block of S =
+//    (hq + 2 hkv) d columns, [its hq query heads | its hkv key/value heads (K) | (V)];
+//    local query head tl uses local key/value head tl / g. With fewer key/value heads
+//    than shards, each block holds its own copy of its group's key/value head.
+// o (M, H d), head t at t*d; lse (b, H, s) the log-sum-exp of each score row.
 //   forward:  O = softmax(Q K^T / sqrt(d)) V        [Megatron-LM 实战 04, TPAttention]
 //   backward: P = exp(S - lse), Dr = rowsum(dO * O), dV = P^T dO, dP = dO V^T,
 //             dS = P * (dP - Dr), dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d)
@@ -23,6 +28,34 @@ namespace {
 
 constexpr int RB = 64;  // rows per CTA and per shared-memory block
 
+// Where query head t (0 <= t < H) and its key/value head sit in a qkv row.
+struct HeadMap {
+  int64_t ldq;     // row stride of qkv
+  int64_t S;       // columns per shard block (0 for the multi-head layout)
+  int64_t KO, VO;  // offsets of the K and V heads within a block
+  int hq;          // query heads per block
+  int g;           // query heads per key/value head within a block
+  int hkv;         // key/value heads per block
+  int H;           // query heads in total
+  int64_t ldo;     // row stride of o and dO (H * d)
+};
+
+template <int D>
+__device__ __forceinline__ int64_t qcol(const HeadMap& m, int t) {
+  const int i = t / m.hq;
+  return i * m.S + static_cast<int64_t>(t - i * m.hq) * D;
+}
+template <int D>
+__device__ __forceinline__ int64_t kcol(const HeadMap& m, int t) {
+  const int i = t / m.hq;
+  return i * m.S + m.KO + static_cast<int64_t>((t - i * m.hq) / m.g) * D;
+}
+template <int D>
+__device__ __forceinline__ int64_t vcol(const HeadMap& m, int t) {
+  const int i = t / m.hq;
+  return i * m.S + m.VO + static_cast<int64_t>((t - i * m.hq) / m.g) * D;
+}
+
 __device__ __forceinline__ float ld(const float* p, int64_t i) { return p[i]; }
 __device__ __forceinline__ float ld(const __nv_bfloat16* p, int64_t i) {
   return __bfloat162float(p[i]);
@@ -34,18 +67,18 @@ __device__ __forceinline__ void st(__nv_bfloat16* p, int64_t i, float v) {
 
 template <typename T, int D>
 __global__ void __launch_bounds__(RB) attn_fwd_kernel(const T* __restrict__ qkv, T* __restrict__ o,
-                                                      float* __restrict__ lse, int s, int h,
-                                                      int heads, float scale, int causal) {
+                                                      float* __restrict__ lse, int s,
+                                                      const HeadMap hm, float scale, int causal) {
   __shared__ float Ks[RB][D + 1], Vs[RB][D + 1];
   const int b = blockIdx.z, t = blockIdx.y;
   const int qi = blockIdx.x * RB + threadIdx.x;
-  const int64_t ldq = 3ll * h;
+  const int64_t ldq = hm.ldq, qc = qcol<D>(hm, t), kc = kcol<D>(hm, t), vc = vcol<D>(hm, t);
   const T* base = qkv + static_cast<int64_t>(b) * s * ldq;
   const bool valid = qi < s;
   float q[D], acc[D];
 #pragma unroll
   for (int d = 0; d < D; ++d) {
-    q[d] = valid ? ld(base + qi * ldq, t * D + d) * scale : 0.0f;
+    q[d] = valid ? ld(base + qi * ldq, qc + d) * scale : 0.0f;
     acc[d] = 0.0f;
   }
   float m = -INFINITY, l = 0.0f;
@@ -55,8 +88,8 @@ __global__ void __launch_bounds__(RB) attn_fwd_kernel(const T* __restrict__ qkv,
     const int kj = k0 + threadIdx.x;
 #pragma unroll
     for (int d = 0; d < D; ++d) {
-      Ks[threadIdx.x][d] = kj < s ? ld(base + kj * ldq, h + t * D + d) : 0.0f;
-      Vs[threadIdx.x][d] = kj < s ? ld(base + kj * ldq, 2 * h + t * D + d) : 0.0f;
+      Ks[threadIdx.x][d] = kj < s ? ld(base + kj * ldq, kc + d) : 0.0f;
+      Vs[threadIdx.x][d] = kj < s ? ld(base + kj * ldq, vc + d) : 0.0f;
     }
     __syncthreads();
     if (!valid) continue;
@@ -93,68 +126,78 @@ __global__ void __launch_bounds__(RB) attn_fwd_kernel(const T* __restrict__ qkv,
   }
   if (!valid) return;
   const float inv = 1.0f / l;
-  T* orow = o + (static_cast<int64_t>(b) * s + qi) * h + t * D;
+  T* orow = o + (static_cast<int64_t>(b) * s + qi) * hm.ldo + t * D;
 #pragma unroll
   for (int d = 0; d < D; ++d) st(orow, d, acc[d] * inv);
-  lse[(static_cast<int64_t>(b) * heads + t) * s + qi] = m + logf(l);
+  lse[(static_cast<int64_t>(b) * hm.H + t) * s + qi] = m + logf(l);
 }
 
-// dK, dV: one thread per key row; query rows streamed through shared memory
+// dK, dV: one thread per key row of one key/value head (grid.y runs over the blocks'
+// key/value heads, replicas included); the query rows of every query head of the block
+// that uses it are streamed through shared memory, so the head's gradient sums their
+// contributions.
 template <typename T, int D>
 __global__ void __launch_bounds__(RB) attn_bwd_dkdv_kernel(
     const T* __restrict__ qkv, const T* __restrict__ o, const float* __restrict__ lse,
-    const T* __restrict__ dO, T* __restrict__ dqkv, int s, int h, int heads, float scale,
+    const T* __restrict__ dO, T* __restrict__ dqkv, int s, const HeadMap hm, float scale,
     int causal) {
   __shared__ float Qs[RB][D + 1], dOs[RB][D + 1], Ls[RB], Ds[RB];
-  const int b = blockIdx.z, t = blockIdx.y;
+  const int b = blockIdx.z, u = blockIdx.y;
+  const int blk = u / hm.hkv, kvl = u - blk * hm.hkv;
   const int kj = blockIdx.x * RB + threadIdx.x;
-  const int64_t ldq = 3ll * h;
+  const int64_t ldq = hm.ldq;
+  const int64_t kc = blk * hm.S + hm.KO + static_cast<int64_t>(kvl) * D;
+  const int64_t vc = blk * hm.S + hm.VO + static_cast<int64_t>(kvl) * D;
   const T* base = qkv + static_cast<int64_t>(b) * s * ldq;
-  const T* obase = o + static_cast<int64_t>(b) * s * h;
-  const T* dobase = dO + static_cast<int64_t>(b) * s * h;
-  const float* lrow = lse + (static_cast<int64_t>(b) * heads + t) * s;
+  const T* obase = o + static_cast<int64_t>(b) * s * hm.ldo;
+  const T* dobase = dO + static_cast<int64_t>(b) * s * hm.ldo;
   const bool valid = kj < s;
   float k[D], v[D], dk[D], dv[D];
 #pragma unroll
   for (int d = 0; d < D; ++d) {
-    k[d] = valid ? ld(base + kj * ldq, h + t * D + d) : 0.0f;
-    v[d] = valid ? ld(base + kj * ldq, 2 * h + t * D + d) : 0.0f;
+    k[d] = valid ? ld(base + kj * ldq, kc + d) : 0.0f;
+    v[d] = valid ? ld(base + kj * ldq, vc + d) : 0.0f;
     dk[d] = 0.0f;
     dv[d] = 0.0f;
   }
   const int qstart = causal ? static_cast<int>(blockIdx.x) * RB : 0;
-  for (int q0 = qstart; q0 < s; q0 += RB) {
-    __syncthreads();
-    const int qi = q0 + threadIdx.x;
-    float dsum = 0.0f;
-#pragma unroll
-    for (int d = 0; d < D; ++d) {
-      const float qv = qi < s ? ld(base + qi * ldq, t * D + d) : 0.0f;
-      const float dov = qi < s ? ld(dobase + qi * h, t * D + d) : 0.0f;
-      const float ov = qi < s ? ld(obase + qi * h, t * D + d) : 0.0f;
-      Qs[threadIdx.x][d] = qv;
-      dOs[threadIdx.x][d] = dov;
-      dsum = fmaf(dov, ov, dsum);
-    }
-    Ls[threadIdx.x] = qi < s ? lrow[qi] : 0.0f;
-    Ds[threadIdx.x] = dsum;
-    __syncthreads();
-    if (!valid) continue;
-    const int iend = min(RB, s - q0);
-    for (int i = 0; i < iend; ++i) {
-      if (causal && kj > q0 + i) continue;
-      float sc = 0.0f, dp = 0.0f;
+  for (int tl = kvl * hm.g; tl < (kvl + 1) * hm.g; ++tl) {  // the block's query heads of this group
+    const int t = blk * hm.hq + tl;
+    const int64_t qc = blk * hm.S + static_cast<int64_t>(tl) * D;
+    const float* lrow = lse + (static_cast<int64_t>(b) * hm.H + t) * s;
+    for (int q0 = qstart; q0 < s; q0 += RB) {
+      __syncthreads();
+      const int qi = q0 + threadIdx.x;
+      float dsum = 0.0f;
 #pragma unroll
       for (int d = 0; d < D; ++d) {
-        sc = fmaf(Qs[i][d], k[d], sc);
-        dp = fmaf(dOs[i][d], v[d], dp);
+        const float qv = qi < s ? ld(base + qi * ldq, qc + d) : 0.0f;
+        const float dov = qi < s ? ld(dobase + qi * hm.ldo, t * D + d) : 0.0f;
+        const float ov = qi < s ? ld(obase + qi * hm.ldo, t * D + d) : 0.0f;
+        Qs[threadIdx.x][d] = qv;
+        dOs[threadIdx.x][d] = dov;
+        dsum = fmaf(dov, ov, dsum);
       }
-      const float p = expf(sc * scale - Ls[i]);
-      const float ds = p * (dp - Ds[i]) * scale;
+      Ls[threadIdx.x] = qi < s ? lrow[qi] : 0.0f;
+      Ds[threadIdx.x] = dsum;
+      __syncthreads();
+      if (!valid) continue;
+      const int iend = min(RB, s - q0);
+      for (int i = 0; i < iend; ++i) {
+        if (causal && kj > q0 + i) continue;
+        float sc = 0.0f, dp = 0.0f;
 #pragma unroll
-      for (int d = 0; d < D; ++d) {
-        dv[d] = fmaf(p, dOs[i][d], dv[d]);
-        dk[d] = fmaf(ds, Qs[i][d], dk[d]);
+        for (int d = 0; d < D; ++d) {
+          sc = fmaf(Qs[i][d], k[d], sc);
+          dp = fmaf(dOs[i][d], v[d], dp);
+        }
+        const float p = expf(sc * scale - Ls[i]);
+        const float ds = p * (dp - Ds[i]) * scale;
+#pragma unroll
+        for (int d = 0; d < D; ++d) {
+          dv[d] = fmaf(p, dOs[i][d], dv[d]);
+          dk[d] = fmaf(ds, Qs[i][d], dk[d]);
+        }
       }
     }
   }
@@ -162,8 +205,8 @@ __global__ void __launch_bounds__(RB) attn_bwd_dkdv_kernel(
   T* row = dqkv + (static_cast<int64_t>(b) * s + kj) * ldq;
 #pragma unroll
   for (int d = 0; d < D; ++d) {
-    st(row, h + t * D + d, dk[d]);
-    st(row, 2 * h + t * D + d, dv[d]);
+    st(row, kc + d, dk[d]);
+    st(row, vc + d, dv[d]);
   }
 }
 
@@ -171,27 +214,27 @@ __global__ void __launch_bounds__(RB) attn_bwd_dkdv_kernel(
 template <typename T, int D>
 __global__ void __launch_bounds__(RB) attn_bwd_dq_kernel(
     const T* __restrict__ qkv, const T* __restrict__ o, const float* __restrict__ lse,
-    const T* __restrict__ dO, T* __restrict__ dqkv, int s, int h, int heads, float scale,
+    const T* __restrict__ dO, T* __restrict__ dqkv, int s, const HeadMap hm, float scale,
     int causal) {
   __shared__ float Ks[RB][D + 1], Vs[RB][D + 1];
   const int b = blockIdx.z, t = blockIdx.y;
   const int qi = blockIdx.x * RB + threadIdx.x;
-  const int64_t ldq = 3ll * h;
+  const int64_t ldq = hm.ldq, qc = qcol<D>(hm, t), kc = kcol<D>(hm, t), vc = vcol<D>(hm, t);
   const T* base = qkv + static_cast<int64_t>(b) * s * ldq;
   const bool valid = qi < s;
   float q[D], dov[D], dq[D];
   float dsum = 0.0f, L = 0.0f;
   if (valid) {
-    const T* orow = o + (static_cast<int64_t>(b) * s + qi) * h + t * D;
-    const T* dorow = dO + (static_cast<int64_t>(b) * s + qi) * h + t * D;
+    const T* orow = o + (static_cast<int64_t>(b) * s + qi) * hm.ldo + t * D;
+    const T* dorow = dO + (static_cast<int64_t>(b) * s + qi) * hm.ldo + t * D;
 #pragma unroll
     for (int d = 0; d < D; ++d) {
-      q[d] = ld(base + qi * ldq, t * D + d);
+      q[d] = ld(base + qi * ldq, qc + d);
       dov[d] = ld(dorow, d);
       dsum = fmaf(dov[d], ld(orow, d), dsum);
       dq[d] = 0.0f;
     }
-    L = lse[(static_cast<int64_t>(b) * heads + t) * s + qi];
+    L = lse[(static_cast<int64_t>(b) * hm.H + t) * s + qi];
   } else {
 #pragma unroll
     for (int d = 0; d < D; ++d) q[d] = dov[d] = dq[d] = 0.0f;
@@ -202,8 +245,8 @@ __global__ void __launch_bounds__(RB) attn_bwd_dq_kernel(
     const int kj = k0 + threadIdx.x;
 #pragma unroll
     for (int d = 0; d < D; ++d) {
-      Ks[threadIdx.x][d] = kj < s ? ld(base + kj * ldq, h + t * D + d) : 0.0f;
-      Vs[threadIdx.x][d] = kj < s ? ld(base + kj * ldq, 2 * h + t * D + d) : 0.0f;
+      Ks[threadIdx.x][d] = kj < s ? ld(base + kj * ldq, kc + d) : 0.0f;
+      Vs[threadIdx.x][d] = kj < s ? ld(base + kj * ldq, vc + d) : 0.0f;
     }
     __syncthreads();
     if (!valid) continue;
@@ -225,16 +268,15 @@ __global__ void __launch_bounds__(RB) attn_bwd_dq_kernel(
   if (!valid) return;
   T* row = dqkv + (static_cast<int64_t>(b) * s + qi) * ldq;
 #pragma unroll
-  for (int d = 0; d < D; ++d) st(row, t * D + d, dq[d]);
+  for (int d = 0; d < D; ++d) st(row, qc + d, dq[d]);
 }
 
 template <typename T, int D>
-tp_status run_fwd(const void* qkv, void* o, float* lse, int b, int s, int h, int heads,
+tp_status run_fwd(const void* qkv, void* o, float* lse, int b, int s, const HeadMap& hm,
                   int causal, cudaStream_t st) {
-  const dim3 grid((s + RB - 1) / RB, heads, b);
+  const dim3 grid((s + RB - 1) / RB, hm.H, b);
   attn_fwd_kernel<T, D><<<grid, RB, 0, st>>>(static_cast<const T*>(qkv), static_cast<T*>(o), lse,
-                                              s, h, heads, 1.0f / sqrtf(static_cast<float>(D)),
-                                              causal);
+                                              s, hm, 1.0f / sqrtf(static_cast<float>(D)), causal);
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;
@@ -242,40 +284,74 @@ tp_status run_fwd(const void* qkv, void* o, float* lse, int b, int s, int h, int
 
 template <typename T, int D>
 tp_status run_bwd(const void* qkv, const void* o, const float* lse, const void* dO, void* dqkv,
-                  int b, int s, int h, int heads, int causal, cudaStream_t st) {
-  const dim3 grid((s + RB - 1) / RB, heads, b);
+                  int b, int s, const HeadMap& hm, int kv_heads, int causal, cudaStream_t st) {
   const float scale = 1.0f / sqrtf(static_cast<float>(D));
-  attn_bwd_dkdv_kernel<T, D><<<grid, RB, 0, st>>>(
+  attn_bwd_dkdv_kernel<T, D><<<dim3((s + RB - 1) / RB, kv_heads, b), RB, 0, st>>>(
       static_cast<const T*>(qkv), static_cast<const T*>(o), lse, static_cast<const T*>(dO),
-      static_cast<T*>(dqkv), s, h, heads, scale, causal);
-  attn_bwd_dq_kernel<T, D><<<grid, RB, 0, st>>>(
+      static_cast<T*>(dqkv), s, hm, scale, causal);
+  attn_bwd_dq_kernel<T, D><<<dim3((s + RB - 1) / RB, hm.H, b), RB, 0, st>>>(
       static_cast<const T*>(qkv), static_cast<const T*>(o), lse, static_cast<const T*>(dO),
-      static_cast<T*>(dqkv), s, h, heads, scale, causal);
+      static_cast<T*>(dqkv), s, hm, scale, causal);
   count_launch(2);
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;
 }
 
 template <typename T>
-tp_status fwd_d(const void* qkv, void* o, float* lse, int b, int s, int h, int heads, int causal,
-                cudaStream_t st) {
-  switch (h / heads) {
-    case 16: return run_fwd<T, 16>(qkv, o, lse, b, s, h, heads, causal, st);
-    case 32: return run_fwd<T, 32>(qkv, o, lse, b, s, h, heads, causal, st);
-    case 64: return run_fwd<T, 64>(qkv, o, lse, b, s, h, heads, causal, st);
+tp_status fwd_d(const void* qkv, void* o, float* lse, int b, int s, const HeadMap& hm, int d,
+                int causal, cudaStream_t st) {
+  switch (d) {
+    case 16: return run_fwd<T, 16>(qkv, o, lse, b, s, hm, causal, st);
+    case 32: return run_fwd<T, 32>(qkv, o, lse, b, s, hm, causal, st);
+    case 64: return run_fwd<T, 64>(qkv, o, lse, b, s, hm, causal, st);
   }
   return fail(TP_ERR_SHAPE, "head_dim must be 16, 32 or 64");
 }
 
 template <typename T>
 tp_status bwd_d(const void* qkv, const void* o, const float* lse, const void* dO, void* dqkv,
-                int b, int s, int h, int heads, int causal, cudaStream_t st) {
-  switch (h / heads) {
-    case 16: return run_bwd<T, 16>(qkv, o, lse, dO, dqkv, b, s, h, heads, causal, st);
-    case 32: return run_bwd<T, 32>(qkv, o, lse, dO, dqkv, b, s, h, heads, causal, st);
-    case 64: return run_bwd<T, 64>(qkv, o, lse, dO, dqkv, b, s, h, heads, causal, st);
+                int b, int s, const HeadMap& hm, int kv_heads, int d, int causal,
+                cudaStream_t st) {
+  switch (d) {
+    case 16: return run_bwd<T, 16>(qkv, o, lse, dO, dqkv, b, s, hm, kv_heads, causal, st);
+    case 32: return run_bwd<T, 32>(qkv, o, lse, dO, dqkv, b, s, hm, kv_heads, causal, st);
+    case 64: return run_bwd<T, 64>(qkv, o, lse, dO, dqkv, b, s, hm, kv_heads, causal, st);
   }
   return fail(TP_ERR_SHAPE, "head_dim must be 16, 32 or 64");
+}
+
+HeadMap mha_map(int64_t h, int heads) {
+  HeadMap m{};
+  m.ldq = 3 * h;
+  m.S = 0;  // one block: head t at t*d, h + t*d, 2h + t*d
+  m.KO = h;
+  m.VO = 2 * h;
+  m.hq = heads;
+  m.g = 1;
+  m.hkv = heads;
+  m.H = heads;
+  m.ldo = h;
+  return m;
+}
+
+HeadMap gqa_map(int heads, int kv_heads, int N, int d) {
+  const int hq = heads / N, hkv = kv_heads >= N ? kv_heads / N : 1;
+  HeadMap m{};
+  m.S = static_cast<int64_t>(hq + 2 * hkv) * d;
+  m.ldq = N * m.S;
+  m.KO = static_cast<int64_t>(hq) * d;
+  m.VO = static_cast<int64_t>(hq + hkv) * d;
+  m.hq = hq;
+  m.g = hq / hkv;
+  m.hkv = hkv;
+  m.H = heads;
+  m.ldo = static_cast<int64_t>(heads) * d;
+  return m;
+}
+
+tp_status check_sizes(int64_t b, int64_t s, int heads) {
+  if (b > 65535 || heads > 65535 || s > (1 << 24)) return fail(TP_ERR_SHAPE, "attention sizes out of range");
+  return TP_OK;
 }
 
 }  // namespace
@@ -283,23 +359,49 @@ tp_status bwd_d(const void* qkv, const void* o, const float* lse, const void* dO
 tp_status launch_attention_fwd(const void* qkv, void* o, float* lse, int64_t b, int64_t s,
                                int64_t h, int heads, int causal, tp_dtype dt, cudaStream_t st) {
   if (b <= 0 || s <= 0) return TP_OK;
-  if (b > 65535 || heads > 65535 || s > (1 << 24) || h > (1 << 20))
-    return fail(TP_ERR_SHAPE, "attention sizes out of range");
-  const int bi = static_cast<int>(b), si = static_cast<int>(s), hi = static_cast<int>(h);
-  return dt == TP_BF16 ? fwd_d<__nv_bfloat16>(qkv, o, lse, bi, si, hi, heads, causal, st)
-                       : fwd_d<float>(qkv, o, lse, bi, si, hi, heads, causal, st);
+  TP_TRY(check_sizes(b, s, heads));
+  if (h > (1 << 20)) return fail(TP_ERR_SHAPE, "attention sizes out of range");
+  const HeadMap m = mha_map(h, heads);
+  const int d = static_cast<int>(h / heads), bi = static_cast<int>(b), si = static_cast<int>(s);
+  return dt == TP_BF16 ? fwd_d<__nv_bfloat16>(qkv, o, lse, bi, si, m, d, causal, st)
+                       : fwd_d<float>(qkv, o, lse, bi, si, m, d, causal, st);
 }
 
 tp_status launch_attention_bwd(const void* qkv, const void* o, const float* lse, const void* dO,
                                void* dqkv, int64_t b, int64_t s, int64_t h, int heads, int causal,
                                tp_dtype dt, cudaStream_t st) {
   if (b <= 0 || s <= 0) return TP_OK;
-  if (b > 65535 || heads > 65535 || s > (1 << 24) || h > (1 << 20))
-    return fail(TP_ERR_SHAPE, "attention sizes out of range");
-  const int bi = static_cast<int>(b), si = static_cast<int>(s), hi = static_cast<int>(h);
+  TP_TRY(check_sizes(b, s, heads));
+  if (h > (1 << 20)) return fail(TP_ERR_SHAPE, "attention sizes out of range");
+  const HeadMap m = mha_map(h, heads);
+  const int d = static_cast<int>(h / heads), bi = static_cast<int>(b), si = static_cast<int>(s);
   return dt == TP_BF16
-             ? bwd_d<__nv_bfloat16>(qkv, o, lse, dO, dqkv, bi, si, hi, heads, causal, st)
-             : bwd_d<float>(qkv, o, lse, dO, dqkv, bi, si, hi, heads, causal, st);
+             ? bwd_d<__nv_bfloat16>(qkv, o, lse, dO, dqkv, bi, si, m, heads, d, causal, st)
+             : bwd_d<float>(qkv, o, lse, dO, dqkv, bi, si, m, heads, d, causal, st);
+}
+
+tp_status launch_gqa_attention_fwd(const void* qkv, void* o, float* lse, int64_t b, int64_t s,
+                                   int heads, int kv_heads, int N, int d, int causal, tp_dtype dt,
+                                   cudaStream_t st) {
+  if (b <= 0 || s <= 0) return TP_OK;
+  TP_TRY(check_sizes(b, s, heads));
+  const HeadMap m = gqa_map(heads, kv_heads, N, d);
+  const int bi = static_cast<int>(b), si = static_cast<int>(s);
+  return dt == TP_BF16 ? fwd_d<__nv_bfloat16>(qkv, o, lse, bi, si, m, d, causal, st)
+                       : fwd_d<float>(qkv, o, lse, bi, si, m, d, causal, st);
+}
+
+tp_status launch_gqa_attention_bwd(const void* qkv, const void* o, const float* lse,
+                                   const void* dO, void* dqkv, int64_t b, int64_t s, int heads,
+                                   int kv_heads, int N, int d, int causal, tp_dtype dt,
+                                   cudaStream_t st) {
+  if (b <= 0 || s <= 0) return TP_OK;
+  TP_TRY(check_sizes(b, s, heads));
+  const HeadMap m = gqa_map(heads, kv_heads, N, d);
+  const int bi = static_cast<int>(b), si = static_cast<int>(s), kvg = N * m.hkv;
+  return dt == TP_BF16
+             ? bwd_d<__nv_bfloat16>(qkv, o, lse, dO, dqkv, bi, si, m, kvg, d, causal, st)
+             : bwd_d<float>(qkv, o, lse, dO, dqkv, bi, si, m, kvg, d, causal, st);
 }
 
 }  // namespace tp

@@ -129,6 +129,15 @@ tp_status launch_attention_fwd(const void* qkv, void* o, float* lse, int64_t b, 
 tp_status launch_attention_bwd(const void* qkv, const void* o, const float* lse, const void* dO,
                                void* dqkv, int64_t b, int64_t s, int64_t h, int heads, int causal,
                                tp_dtype dt, cudaStream_t st);
+// grouped-query layout (per-shard blocks [Q heads | K heads | V heads], key/value heads
+// replicated per block when kv_heads < N); o (M, heads * d)
+tp_status launch_gqa_attention_fwd(const void* qkv, void* o, float* lse, int64_t b, int64_t s,
+                                   int heads, int kv_heads, int N, int d, int causal, tp_dtype dt,
+                                   cudaStream_t st);
+tp_status launch_gqa_attention_bwd(const void* qkv, const void* o, const float* lse,
+                                   const void* dO, void* dqkv, int64_t b, int64_t s, int heads,
+                                   int kv_heads, int N, int d, int causal, tp_dtype dt,
+                                   cudaStream_t st);
 
 // vocabulary-parallel embedding / cross-entropy and AdamW (vocab.cu)
 tp_status launch_vocab_embed_fwd(const int32_t* ids, const void* E, void* x, int64_t M, int64_t v,

@@ -140,6 +140,13 @@ _SIGS = {
                                            _P, _SZ, _P]),
     "tp_attn_proj_bwd": (_ST, [_P] * 16 + [_I64, _I64, _I64, _I32, _I32, ctypes.c_int, _ST, _ST,
                                            _P, _SZ, _P]),
+    "tp_gqa_qkv_cols": (_I64, [_I64, _I32, _I32, _I32]),
+    "tp_gqa_workspace_size": (_SZ, [ctypes.c_int, _I64, _I64, _I32, _I32, _I32, _ST, _ST]),
+    "tp_gqa_pack_qkv": (_ST, [_P] * 4 + [_I64, _I32, _I32, _I32, _ST, _P]),
+    "tp_gqa_attn_proj_fwd": (_ST, [_P] * 12 + [_I64, _I64, _I64, _I32, _I32, _I32, ctypes.c_int,
+                                               _ST, _ST, _P, _SZ, _P]),
+    "tp_gqa_attn_proj_bwd": (_ST, [_P] * 16 + [_I64, _I64, _I64, _I32, _I32, _I32, ctypes.c_int,
+                                               _ST, _ST, _P, _SZ, _P]),
     "tp_sp_mlp_fwd": (_ST, [_P] * 13 + [_I64, _I64, _I64, _I32, _ST, _ST, _ST, _P, _SZ, _P]),
     "tp_sp_mlp_bwd": (_ST, [_P] * 20 + [_I64, _I64, _I64, _I32, _ST, _ST, _ST, _P, _SZ, _P]),
     "tp_layer_fwd": (_ST, [_P, ctypes.POINTER(LayerWeights), ctypes.POINTER(LayerSaved), _P, _I64,
@@ -302,6 +309,38 @@ def tp_mlp_bwd(X, W1, W1_up, W2, Y, Y_up, H, dZ, dX, dW1, dW1_up, dW2, M, h, f, 
                             _ptr(H), _ptr(dZ), _ptr(dX), _ptr(dW1), _ptr(dW1_up), _ptr(dW2),
                             M, h, f, N, int(dtype), int(act), int(mode), _ptr(ws),
                             int(ws_bytes), _stream(stream)))
+
+
+def tp_gqa_qkv_cols(h, n_heads, n_kv_heads, N):
+    return int(lib().tp_gqa_qkv_cols(h, n_heads, n_kv_heads, N))
+
+
+def tp_gqa_workspace_size(fwd, M, h, n_heads, n_kv_heads, N, dtype, mode):
+    return int(lib().tp_gqa_workspace_size(int(bool(fwd)), M, h, n_heads, n_kv_heads, N,
+                                           int(dtype), int(mode)))
+
+
+def tp_gqa_pack_qkv(Wq, Wk, Wv, Wqkv, h, n_heads, n_kv_heads, N, dtype, stream=None):
+    _check(lib().tp_gqa_pack_qkv(_ptr(Wq), _ptr(Wk), _ptr(Wv), _ptr(Wqkv), h, n_heads,
+                                 n_kv_heads, N, int(dtype), _stream(stream)))
+
+
+def tp_gqa_attn_proj_fwd(x, gamma, beta, Wqkv, Wo, xn, mean, rstd, qkv, o, lse, out, b, s, h,
+                         n_heads, n_kv_heads, N, causal, dtype, mode, ws, ws_bytes, stream=None):
+    _check(lib().tp_gqa_attn_proj_fwd(*[_ptr(t) for t in (x, gamma, beta, Wqkv, Wo, xn, mean,
+                                                          rstd, qkv, o, lse, out)],
+                                      b, s, h, n_heads, n_kv_heads, N, int(causal), int(dtype),
+                                      int(mode), _ptr(ws), int(ws_bytes), _stream(stream)))
+
+
+def tp_gqa_attn_proj_bwd(x, gamma, Wqkv, Wo, xn, mean, rstd, qkv, o, lse, dout, dx, dgamma,
+                         dbeta, dWqkv, dWo, b, s, h, n_heads, n_kv_heads, N, causal, dtype, mode,
+                         ws, ws_bytes, stream=None):
+    _check(lib().tp_gqa_attn_proj_bwd(*[_ptr(t) for t in (x, gamma, Wqkv, Wo, xn, mean, rstd,
+                                                          qkv, o, lse, dout, dx, dgamma, dbeta,
+                                                          dWqkv, dWo)],
+                                      b, s, h, n_heads, n_kv_heads, N, int(causal), int(dtype),
+                                      int(mode), _ptr(ws), int(ws_bytes), _stream(stream)))
 
 
 def tp_sp_mlp_fwd(x, gamma, beta, W1, W1_up, W2, xn, mean, rstd, Y, Y_up, H, out, M, h, f, N,

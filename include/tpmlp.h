@@ -448,6 +448,47 @@ TP_API tp_status tp_attn_proj_bwd(const void* x, const float* gamma, const void*
                                   void* stream);
 
 /*
+ * Grouped-query attention under head sharding [张量并行 notes, §相关分析, GQA]: H =
+ * n_heads query heads share Hkv = n_kv_heads key/value heads, query head t using
+ * key/value head t / (H / Hkv). N shards (H % N == 0): when N <= Hkv (Hkv % N == 0)
+ * shard i owns H/N query heads and Hkv/N key/value heads; when N > Hkv (N % Hkv == 0)
+ * it owns H/N query heads of one group and a replica of that group's key/value head,
+ * and the replicas' weight gradients are all-reduced so the copies stay equal.
+ * head_dim = h / H in {16, 32, 64}; W_o is (H head_dim = h, h).
+ *
+ * Sharded QKV weight Wqkv (h, W), W = tp_gqa_qkv_cols(...): shard i's block of
+ * S = W / N columns is [W_q of its query heads | W_k of its key/value heads | W_v of
+ * the same] (the per-rank layout of the Megatron-LM 实战 04 listing's column-parallel
+ * QKV); tp_gqa_pack_qkv builds it from the full W_q (h, H d), W_k, W_v (h, Hkv d).
+ * qkv (M, W) is laid out the same way. bf16 also needs S % 64 == 0 and (h / N) % 64 == 0.
+ */
+TP_API int64_t tp_gqa_qkv_cols(int64_t h, int32_t n_heads, int32_t n_kv_heads, int32_t N);
+TP_API size_t tp_gqa_workspace_size(int fwd, int64_t M, int64_t h, int32_t n_heads,
+                                    int32_t n_kv_heads, int32_t N, tp_dtype dtype,
+                                    tp_reduce mode);
+TP_API tp_status tp_gqa_pack_qkv(const void* Wq, const void* Wk, const void* Wv, void* Wqkv,
+                                 int64_t h, int32_t n_heads, int32_t n_kv_heads, int32_t N,
+                                 tp_dtype dtype, void* stream);
+/* out = x + sum_i O_i W_o,i, O from LN(x) and the sharded Wqkv; saved state as
+ * tp_attn_proj_fwd with qkv (M, W) and lse (b, n_heads, s). */
+TP_API tp_status tp_gqa_attn_proj_fwd(const void* x, const float* gamma, const float* beta,
+                                      const void* Wqkv, const void* Wo, void* xn, float* mean,
+                                      float* rstd, void* qkv, void* o, float* lse, void* out,
+                                      int64_t b, int64_t s, int64_t h, int32_t n_heads,
+                                      int32_t n_kv_heads, int32_t N, int causal, tp_dtype dtype,
+                                      tp_reduce mode, void* ws, size_t ws_bytes, void* stream);
+/* Backward: dWqkv (h, W) in the sharded layout, each replicated key/value head's
+ * columns holding the sum over its replicas; dx includes the residual's dout. */
+TP_API tp_status tp_gqa_attn_proj_bwd(const void* x, const float* gamma, const void* Wqkv,
+                                      const void* Wo, const void* xn, const float* mean,
+                                      const float* rstd, const void* qkv, const void* o,
+                                      const float* lse, const void* dout, void* dx,
+                                      float* dgamma, float* dbeta, void* dWqkv, void* dWo,
+                                      int64_t b, int64_t s, int64_t h, int32_t n_heads,
+                                      int32_t n_kv_heads, int32_t N, int causal, tp_dtype dtype,
+                                      tp_reduce mode, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Sequence-parallel pre-LN MLP sub-block, out = x + MLP(LN(x))
  * [20260402-parallelism, §5 Sequence Parallelism]. The rows are split over the N
  * ranks of the tensor-parallel group along the sequence: rank r holds rows

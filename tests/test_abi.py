@@ -127,6 +127,11 @@ def test_row_and_mlp_argument_errors(L):
     assert _status(spb(ws_bytes=16)) == T.Status.WORKSPACE
     assert _status(spb(M=14)) == T.Status.SHAPE
     assert _status(lambda: T.tp_vocab_embed_fwd(A16, A16, A16, 4, 10, 8, 3, BF)) == T.Status.SHAPE
+    assert T.tp_gqa_qkv_cols(2048, 32, 8, 16) == 16 * (2 + 2) * 64 and \
+        T.tp_gqa_qkv_cols(2048, 32, 8, 12) == 0 and T.tp_gqa_qkv_cols(4096, 32, 8, 8) == 0
+    assert T.tp_gqa_workspace_size(1, 64, 256, 8, 2, 4, BF, T.Reduce.BUFFERS) == 4 * 64 * 256 * 4
+    assert _status(lambda: T.tp_gqa_pack_qkv(A16, A16, None, A16, 256, 8, 2, 4, BF)) == \
+        T.Status.INVALID_ARG
     assert _status(lambda: T.tp_vocab_ce_fwd(A16, A16, A16, A16, None, None, 4, 12, 3, BF)) == \
         T.Status.INVALID_ARG                                # loss pointer missing
     assert _status(lambda: T.tp_adamw_step(A16, A16, A16, A16, 10, 0, 1e-3, 0.9, 0.999, 1e-8,
