@@ -157,6 +157,38 @@ tp_status tp_gqa_pack_qkv(const void* Wq, const void* Wk, const void* Wv, void* 
   return TP_OK;
 }
 
+tp_status tp_gqa_attention_fwd(const void* qkv, void* o, float* lse, int64_t b, int64_t s,
+                               int64_t h, int32_t n_heads, int32_t n_kv_heads, int32_t N,
+                               int causal, tp_dtype dtype, void* stream) {
+  TP_TRY(check_dtype(dtype));
+  TP_TRY(need(qkv && o && lse, TP_ERR_INVALID_ARG, "qkv, o and lse are required"));
+  TP_TRY(need(b >= 0 && s >= 0, TP_ERR_INVALID_ARG, "need b, s >= 0"));
+  Gqa g;
+  TP_TRY(gqa_shape(h, n_heads, n_kv_heads, N, TP_F32, &g));
+  if (b * s == 0) return TP_OK;
+  TP_TRY(check_device());
+  return launch_gqa_attention_fwd(qkv, o, lse, b, s, n_heads, n_kv_heads, N,
+                                  static_cast<int>(g.d), causal, dtype,
+                                  static_cast<cudaStream_t>(stream));
+}
+
+tp_status tp_gqa_attention_bwd(const void* qkv, const void* o, const float* lse, const void* dO,
+                               void* dqkv, int64_t b, int64_t s, int64_t h, int32_t n_heads,
+                               int32_t n_kv_heads, int32_t N, int causal, tp_dtype dtype,
+                               void* stream) {
+  TP_TRY(check_dtype(dtype));
+  TP_TRY(need(qkv && o && lse && dO && dqkv, TP_ERR_INVALID_ARG,
+              "qkv, o, lse, dO and dqkv are required"));
+  TP_TRY(need(b >= 0 && s >= 0, TP_ERR_INVALID_ARG, "need b, s >= 0"));
+  Gqa g;
+  TP_TRY(gqa_shape(h, n_heads, n_kv_heads, N, TP_F32, &g));
+  if (b * s == 0) return TP_OK;
+  TP_TRY(check_device());
+  return launch_gqa_attention_bwd(qkv, o, lse, dO, dqkv, b, s, n_heads, n_kv_heads, N,
+                                  static_cast<int>(g.d), causal, dtype,
+                                  static_cast<cudaStream_t>(stream));
+}
+
 tp_status tp_gqa_attn_proj_fwd(const void* x, const float* gamma, const float* beta,
                                const void* Wqkv, const void* Wo, void* xn, float* mean,
                                float* rstd, void* qkv, void* o, float* lse, void* out, int64_t b,

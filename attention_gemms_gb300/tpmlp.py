@@ -143,6 +143,10 @@ _SIGS = {
     "tp_gqa_qkv_cols": (_I64, [_I64, _I32, _I32, _I32]),
     "tp_gqa_workspace_size": (_SZ, [ctypes.c_int, _I64, _I64, _I32, _I32, _I32, _ST, _ST]),
     "tp_gqa_pack_qkv": (_ST, [_P] * 4 + [_I64, _I32, _I32, _I32, _ST, _P]),
+    "tp_gqa_attention_fwd": (_ST, [_P] * 3 + [_I64, _I64, _I64, _I32, _I32, _I32, ctypes.c_int,
+                                              _ST, _P]),
+    "tp_gqa_attention_bwd": (_ST, [_P] * 5 + [_I64, _I64, _I64, _I32, _I32, _I32, ctypes.c_int,
+                                              _ST, _P]),
     "tp_gqa_attn_proj_fwd": (_ST, [_P] * 12 + [_I64, _I64, _I64, _I32, _I32, _I32, ctypes.c_int,
                                                _ST, _ST, _P, _SZ, _P]),
     "tp_gqa_attn_proj_bwd": (_ST, [_P] * 16 + [_I64, _I64, _I64, _I32, _I32, _I32, ctypes.c_int,
@@ -323,6 +327,19 @@ def tp_gqa_workspace_size(fwd, M, h, n_heads, n_kv_heads, N, dtype, mode):
 def tp_gqa_pack_qkv(Wq, Wk, Wv, Wqkv, h, n_heads, n_kv_heads, N, dtype, stream=None):
     _check(lib().tp_gqa_pack_qkv(_ptr(Wq), _ptr(Wk), _ptr(Wv), _ptr(Wqkv), h, n_heads,
                                  n_kv_heads, N, int(dtype), _stream(stream)))
+
+
+def tp_gqa_attention_fwd(qkv, o, lse, b, s, h, n_heads, n_kv_heads, N, causal, dtype,
+                         stream=None):
+    _check(lib().tp_gqa_attention_fwd(_ptr(qkv), _ptr(o), _ptr(lse), b, s, h, n_heads,
+                                      n_kv_heads, N, int(causal), int(dtype), _stream(stream)))
+
+
+def tp_gqa_attention_bwd(qkv, o, lse, dO, dqkv, b, s, h, n_heads, n_kv_heads, N, causal, dtype,
+                         stream=None):
+    _check(lib().tp_gqa_attention_bwd(_ptr(qkv), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dqkv), b, s,
+                                      h, n_heads, n_kv_heads, N, int(causal), int(dtype),
+                                      _stream(stream)))
 
 
 def tp_gqa_attn_proj_fwd(x, gamma, beta, Wqkv, Wo, xn, mean, rstd, qkv, o, lse, out, b, s, h,

@@ -51,6 +51,10 @@ WORKLOADS = {
                      "cross-entropy, tied output layer, AdamW): vocab=256 h=128 heads=8 ffn=512 "
                      "layers=2 b=4 s=32 N=2, fp32", b=4, s=32, h=128, f=512, N=2, heads=8,
                 vocab=256, layers=2, act="gelu", cfg=6, gpt=True, dtype="f32"),
+    "gqa": dict(desc="head-sharded grouped-query attention block fwd+bwd (LN, QKV, attention, "
+                     "W_o, shard sum): b=4 s=512 h=2048 heads=32 kv_heads=8 N=16 (each key/value "
+                     "head replicated on 2 shards)", b=4, s=512, h=2048, f=0, heads=32,
+                kv_heads=8, N=16, act="none", cfg=7, gqa=True),
     # reduced-token case of c5 for ncu captures (a few GB on the device, inputs > L2)
     "c5-2k": dict(desc="profiling case: SwiGLU MLP fwd+bwd b=1 s=2048 h=8192 ffn=28672 N=4",
                   b=1, s=2048, h=8192, f=28672, N=4, act="swiglu", cfg=5),
@@ -262,6 +266,8 @@ def run_ours(args, w):
         return run_sp(args, w, T, device, rank, ws_)
     if w.get("gpt"):
         return run_gpt(args, w, T, device, rank, ws_)
+    if w.get("gqa"):
+        return run_gqa(args, w, T, device, rank, ws_)
     M, h, f, N = w["b"] * w["s"], w["h"], w["f"], w["N"]
     sw = w["act"] == "swiglu"
     act = T.Act.SWIGLU if sw else T.Act.GELU
@@ -685,6 +691,130 @@ def gpt_cpu_baseline(w, p, ids, tg, steps=3):
             "threads_effective": round(dc / dt, 1), "kind": "oracle",
             "sample": f"fp64 oracle training steps (forward, backward, AdamW) on the full batch, "
                       f"{steps} steps, {dt * 1e3:.0f} ms each"}
+
+
+FP32_ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # SMs x FP32 lanes x FMA x max clock
+
+
+def gqa_flops(w):
+    """Algorithmic FLOPs of the GQA block forward + backward, counted on the unsharded
+    model (replicated key/value projections are redundant work, not counted):
+    projections 2 M h (H + 2 Hkv) d + 2 M h h, attention 4 b H s^2 d; backward 2x."""
+    M, h, H, Hkv, b, s = w["b"] * w["s"], w["h"], w["heads"], w["kv_heads"], w["b"], w["s"]
+    d = h // H
+    fwd = 2 * M * h * (H + 2 * Hkv) * d + 2 * M * h * h + 4 * b * H * s * s * d
+    return 3.0 * fwd, 4.0 * b * H * s * s * d
+
+
+def run_gqa(args, w, T, device, rank, nranks):
+    """The head-sharded GQA block, forward + backward per step; the attention core on
+    the sharded qkv (CUDA cores, fp32 arithmetic) is timed alone for its roofline."""
+    import torch
+    from attention_gemms_gb300 import synth
+    b, s, h, H, Hkv, N = w["b"], w["s"], w["h"], w["heads"], w["kv_heads"], w["N"]
+    M, d = b * s, h // H
+    BF = T.DType.BF16
+    mode = T.Reduce.SPLITK if args.mode == "splitk" else T.Reduce.BUFFERS
+    Wc = T.tp_gqa_qkv_cols(h, H, Hkv, N)
+    c = w["cfg"]
+    sig = 1.0 / math.sqrt(h)
+    dev = lambda shape, name, sigma: torch.from_numpy(
+        synth.normal(shape, synth.seed_of(c, name), sigma, "bf16").view(np.int16)).view(
+        torch.bfloat16).to(device)
+    t_gen = time.time()
+    x, dout = dev((M, h), "X", 1.0), dev((M, h), "dZ", 1.0)
+    Wq, Wk = dev((h, H * d), "Wqkv", sig), dev((h, Hkv * d), "Wg", sig)
+    Wv, Wo = dev((h, Hkv * d), "Wu", sig), dev((h, h), "Wo", sig)
+    t_gen = time.time() - t_gen
+    g, be = torch.ones(h, device=device), torch.zeros(h, device=device)
+    e = lambda *sh, dt=torch.bfloat16: torch.empty(sh, dtype=dt, device=device)
+    f32 = torch.float32
+    Wsh = e(h, Wc)
+    T.tp_gqa_pack_qkv(Wq, Wk, Wv, Wsh, h, H, Hkv, N, BF)
+    xn, mean, rstd, qkv, o, lse, out = (e(M, h), e(M, dt=f32), e(M, dt=f32), e(M, Wc), e(M, h),
+                                        e(b, H, s, dt=f32), e(M, h))
+    dx, dg, db, dW, dWo = e(M, h), e(h, dt=f32), e(h, dt=f32), e(h, Wc), e(h, h)
+    ws = torch.empty(max(T.tp_gqa_workspace_size(1, M, h, H, Hkv, N, BF, mode),
+                         T.tp_gqa_workspace_size(0, M, h, H, Hkv, N, BF, mode), 256),
+                     dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        T.tp_gqa_attn_proj_fwd(x, g, be, Wsh, Wo, xn, mean, rstd, qkv, o, lse, out, b, s, h, H,
+                               Hkv, N, 0, BF, mode, ws, ws.numel(), stream)
+        T.tp_gqa_attn_proj_bwd(x, g, Wsh, Wo, xn, mean, rstd, qkv, o, lse, dout, dx, dg, db, dW,
+                               dWo, b, s, h, H, Hkv, N, 0, BF, mode, ws, ws.numel(), stream)
+
+    def timed(fn, steps):
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        z.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(z) / steps
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(device.index)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    n0 = T.tp_launch_count()
+    ms = timed(step, args.steps)
+    launches = T.tp_launch_count() - n0
+    attn_ms = timed(lambda: T.tp_gqa_attention_fwd(qkv, o, lse, b, s, h, H, Hkv, N, 0, BF, stream),
+                    args.steps)
+    xp = torch.empty((M, h), dtype=torch.bfloat16, pin_memory=True)
+    dp = torch.empty((M, h), dtype=torch.bfloat16, pin_memory=True)
+    xp.copy_(x)
+    dp.copy_(dout)
+    outp = torch.empty((M, h), dtype=torch.bfloat16, pin_memory=True)
+    dxp = torch.empty((M, h), dtype=torch.bfloat16, pin_memory=True)
+
+    def e2e():
+        x.copy_(xp, non_blocking=True)
+        dout.copy_(dp, non_blocking=True)
+        step()
+        outp.copy_(out, non_blocking=True)
+        dxp.copy_(dx, non_blocking=True)
+    barrier()
+    e2e_ms = timed(e2e, args.steps)
+    clk = clocks.stop()
+    if T.tp_check_status(stream) != 0:
+        raise RuntimeError("device wait timeout: " + T.tp_last_error())
+    ms_max, e2e_max = max_over_ranks(ms, device), max_over_ranks(e2e_ms, device)
+    attn_max = max_over_ranks(attn_ms, device)
+    total, attn_fwd = gqa_flops(w)
+    attn_tf = attn_fwd / (attn_max * 1e-3) / 1e12
+    res = {
+        "metric": "head-sharded GQA attention block fwd+bwd TFLOP/s",
+        "value": round(total * nranks / (ms_max * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "n_gpus": nranks, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0, 1/h) weights; LN gamma=1, beta=0)",
+        "config": {"workload": w["desc"], "tokens": M, "h": h, "heads": H, "kv_heads": Hkv,
+                   "shards": N, "qkv_columns_sharded": Wc,
+                   "qkv_columns_unreplicated": (H + 2 * Hkv) * d, "shard_sum": args.mode,
+                   "parallelism": f"tp{N} virtual ranks per GPU, dp{nranks}",
+                   "l2": "activations larger than L2 (no flush)"},
+        "roofline": {"bound": "alu", "kernel": "attn_fwd_kernel (per-head softmax attention, "
+                     "CUDA cores, fp32 arithmetic), timed on its own", "achieved": round(attn_tf, 2),
+                     "peak": round(FP32_ALU_PEAK_TFLOPS, 1), "unit": "TFLOP/s",
+                     "frac": round(attn_tf / FP32_ALU_PEAK_TFLOPS, 4),
+                     "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 (FMA) x 2.07 GHz",
+                     "traffic": None, "algorithmic_flops_per_launch": attn_fwd,
+                     "avg_launch_ms": round(attn_max, 4)},
+        "e2e": {"value": round(total * nranks / (e2e_max * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": 2 * M * h * 2, "d2h_bytes_per_step": 2 * M * h * 2,
+                "ms_per_step": round(e2e_max, 4)},
+        "gpu_launches": int(launches), "clocks": clk, "input_gen_s": round(t_gen, 1),
+    }
+    if rank == 0:
+        print(json.dumps(res), flush=True)
 
 
 # ------------------------------------------------------------------ page-2 layer
@@ -1128,7 +1258,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="c5", choices=sorted(WORKLOADS) + ["c4"],
                     help="c5 (default): large SwiGLU MLP; c3: GELU MLP; c2: page-2 layer; "
                          "c1: tiny fp32 MLP; c4: decode sweep only; c5-2k: profiling case; "
-                         "c3-sp: sequence-parallel MLP block; gpt: small GPT training")
+                         "c3-sp: sequence-parallel MLP block; gpt: small GPT training; "
+                         "gqa: head-sharded grouped-query attention block")
     ap.add_argument("--mode", default="splitk", choices=["splitk", "buffers"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-rows", type=int, default=64)

@@ -469,6 +469,16 @@ TP_API size_t tp_gqa_workspace_size(int fwd, int64_t M, int64_t h, int32_t n_hea
 TP_API tp_status tp_gqa_pack_qkv(const void* Wq, const void* Wk, const void* Wv, void* Wqkv,
                                  int64_t h, int32_t n_heads, int32_t n_kv_heads, int32_t N,
                                  tp_dtype dtype, void* stream);
+/* The attention core alone on the sharded qkv (M, W): O (M, h) and lse (b, n_heads, s);
+ * backward: dqkv (M, W) from dO, each key/value head's gradient summing the query heads
+ * of its block that use it (a replica's share; tp_gqa_attn_proj_bwd adds the replicas). */
+TP_API tp_status tp_gqa_attention_fwd(const void* qkv, void* o, float* lse, int64_t b, int64_t s,
+                                      int64_t h, int32_t n_heads, int32_t n_kv_heads, int32_t N,
+                                      int causal, tp_dtype dtype, void* stream);
+TP_API tp_status tp_gqa_attention_bwd(const void* qkv, const void* o, const float* lse,
+                                      const void* dO, void* dqkv, int64_t b, int64_t s, int64_t h,
+                                      int32_t n_heads, int32_t n_kv_heads, int32_t N, int causal,
+                                      tp_dtype dtype, void* stream);
 /* out = x + sum_i O_i W_o,i, O from LN(x) and the sharded Wqkv; saved state as
  * tp_attn_proj_fwd with qkv (M, W) and lse (b, n_heads, s). */
 TP_API tp_status tp_gqa_attn_proj_fwd(const void* x, const float* gamma, const float* beta,
