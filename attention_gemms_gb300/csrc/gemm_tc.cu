@@ -174,18 +174,30 @@ __device__ __forceinline__ void ld8(const void* base, int64_t idx, float* v) {
   unpack8(__ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(base) + idx)), v);
 }
 
+// Inputs an epilogue reads (residual / saved activations), 8 columns at a time
+template <int EPI>
+struct EpiInputs {
+  static constexpr int n = EPI == EPI_DSWIGLU ? 2 : (EPI == EPI_DGELU || EPI == EPI_STORE ? 1 : 0);
+};
+
 // Epilogue of 8 consecutive output columns of one row. a: accumulator values,
-// b: the paired half (gate/up second operand) when the problem is paired.
+// b: the paired half (gate/up second operand) when the problem is paired. pre0/pre1:
+// the 16 bytes of in0/in1 at this position when `preloaded` (else loaded here).
 template <int EPI>
 __device__ __forceinline__ void epi8(const TcParams& p, int g, int64_t row, int64_t col,
-                                     const float* a, const float* b) {
+                                     const float* a, const float* b, bool preloaded = false,
+                                     uint4 pre0 = uint4{}, uint4 pre1 = uint4{}) {
   const int64_t idx = row * p.ldo + col;
   float v[8], w[8];
+  auto in8 = [&](const void* base, const uint4& pre, float* dst) {
+    if (preloaded) unpack8(pre, dst);
+    else ld8(base, idx, dst);
+  };
   if constexpr (EPI == EPI_STORE) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = a[i];
     if (p.in0) {
-      ld8(p.in0, idx, w);
+      in8(p.in0, pre0, w);
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] += w[i];
     }
@@ -209,14 +221,14 @@ __device__ __forceinline__ void epi8(const TcParams& p, int g, int64_t row, int6
     for (int i = 0; i < 8; ++i) v[i] = silu_f(a[i]) * b[i];
     st8(p.out2, idx, v);
   } else if constexpr (EPI == EPI_DGELU) {
-    ld8(p.in0, idx, w);
+    in8(p.in0, pre0, w);
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = a[i] * gelu_prime_f(w[i]);
     st8(p.out0, idx, v);
   } else if constexpr (EPI == EPI_DSWIGLU) {
     float gg[8], uu[8], du[8];
-    ld8(p.in0, idx, gg);
-    ld8(p.in1, idx, uu);
+    in8(p.in0, pre0, gg);
+    in8(p.in1, pre1, uu);
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = dswiglu_f(a[i], gg[i], uu[i], du[i]);
     st8(p.out0, idx, v);
@@ -519,7 +531,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 #define TP_PAIR_DUAL 1
 #endif
 // TP_PAIR_DUAL: a second producer warp (warp 6) issues the B copies while warp 0 issues A
-constexpr int kPairThreads = TP_PAIR_DUAL ? 224 : 192;
+#ifndef TP_PAIR_EPI_WARPS
+#define TP_PAIR_EPI_WARPS 4
+#endif
+// TP_PAIR_EPI_WARPS = 8: a second set of four epilogue warps (after the producer warps)
+// drains the other half of each accumulator tile's columns, halving the epilogue time
+static_assert(TP_PAIR_EPI_WARPS == 4 || TP_PAIR_EPI_WARPS == 8, "4 or 8 epilogue warps");
+constexpr int kEpiHi0 = TP_PAIR_DUAL ? 7 : 6;  // first warp of the second epilogue set
+constexpr int kPairThreads = 32 * (kEpiHi0 + (TP_PAIR_EPI_WARPS == 8 ? 4 : 0));
 constexpr int kPairStages = TP_PAIR_STAGES;
 constexpr int kPairStageBytes = 2 * 128 * BK * 2;  // A 128 x 64 + B 128 x 64, bf16
 constexpr int kPairBars = 2 * kPairStages + 7;
@@ -561,7 +580,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_tc2_kernel(const __grid_
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), leader ? 8 : 1);  // 4 epilogue warps in each CTA
+      mbar_init(tempty_bar(b), leader ? 2 * TP_PAIR_EPI_WARPS : 1);  // epilogue warps of both CTAs
     }
     mbar_init(drain_bar, 1);
     mbar_init(exit_bar, 1);
@@ -727,9 +746,12 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_tc2_kernel(const __grid_
       if (!ok) record_timeout(p.status);
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if ((warp >= 2 && warp < 6) || warp >= kEpiHi0) {
     // -------------------------------------------------------------- epilogue (both CTAs)
-    const int quad = warp & 3;
+    const int quad = warp & 3;  // a warp reaches the TMEM lanes of quarter warp % 4
+    const int nchunk = bn_logical / 32;
+    const int c_lo = warp >= kEpiHi0 ? nchunk / 2 : 0;
+    const int c_hi = TP_PAIR_EPI_WARPS == 8 && warp < 6 ? nchunk / 2 : nchunk;
     const uint32_t remote_tempty0 = mapa_shared(tempty_bar(0), 0);
     uint32_t acc = 0, acc_phase = 0;
     for (int t = pair; t < ntiles; t += npairs) {
@@ -749,10 +771,29 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_tc2_kernel(const __grid_
           static_cast<int64_t>(tc.mt) * 256 + static_cast<int>(rank) * 128 + quad * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * 256;
       const int64_t col_base = static_cast<int64_t>(tc.nt) * bn_logical;
-      for (int c = 0; c < bn_logical / 32; ++c) {
+      for (int c = c_lo; c < c_hi; ++c) {
         uint32_t ra[32], rb[32];
         tmem_ld32(t_row + c * 32, ra);
         if (p.paired) tmem_ld32(t_row + 128 + c * 32, rb);
+        // the chunk's epilogue inputs are requested together, while the TMEM load runs
+        constexpr int kIn = EpiInputs<EPI>::n;
+        uint4 pin0[4] = {}, pin1[4] = {};
+        const bool has0 = kIn >= 1 && p.in0 != nullptr;
+        if (kIn > 0 && row < p.M) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int64_t col = col_base + c * 32 + q * 8;
+            if (col < p.N) {
+              const int64_t idx = row * p.ldo + col;
+              if (has0)
+                pin0[q] = __ldg(reinterpret_cast<const uint4*>(
+                    reinterpret_cast<const __nv_bfloat16*>(p.in0) + idx));
+              if (kIn == 2)
+                pin1[q] = __ldg(reinterpret_cast<const uint4*>(
+                    reinterpret_cast<const __nv_bfloat16*>(p.in1) + idx));
+            }
+          }
+        }
         tmem_ld_wait();
         if (row < p.M) {
 #pragma unroll
@@ -765,7 +806,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_tc2_kernel(const __grid_
                 a[i] = __uint_as_float(ra[q * 8 + i]);
                 b[i] = __uint_as_float(rb[q * 8 + i]);
               }
-              epi8<EPI>(p, tc.g, row, col, a, b);
+              epi8<EPI>(p, tc.g, row, col, a, b, kIn > 0 && has0, pin0[q], pin1[q]);
             }
           }
         }

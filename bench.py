@@ -583,6 +583,34 @@ def run_vocab_ce(device, T, M=8192, v=50304, N=8, reps=20):
     return out
 
 
+def run_vocab_ce_only(args):
+    """The vocabulary-parallel cross-entropy (forward + backward) alone, for profiling."""
+    import torch
+    from attention_gemms_gb300 import build as B
+    from attention_gemms_gb300 import tpmlp as T
+    ws_, rank, local = dist_env()
+    if ws_ > 1:
+        torch.cuda.set_device(local)
+    dist_init("nccl")
+    B.build()
+    T.lib()
+    device = torch.device("cuda", torch.cuda.current_device())
+    ce = run_vocab_ce(device, T, reps=max(args.steps, 1))
+    tot_us = ce["fwd"]["us"] + ce["bwd"]["us"]
+    nbytes = ce["fwd"]["algorithmic_bytes"] + ce["bwd"]["algorithmic_bytes"]
+    if rank == 0:
+        print(json.dumps({
+            "metric": "vocabulary-parallel cross-entropy fwd+bwd GB/s", "unit": "GB/s",
+            "value": round(nbytes / tot_us / 1e3 * ws_, 1), "n_gpus": ws_, "steps": args.steps,
+            "warmup": 3, "ms_per_step": round(tot_us / 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "vocab-ce", **ce["shape"]},
+            "roofline": {"bound": "hbm", "kernel": "vocab_ce_bwd_vec_kernel",
+                         "achieved": ce["bwd"]["achieved"], "peak": ce["peak"], "unit": "GB/s",
+                         "frac": ce["bwd"]["frac"], "traffic": None},
+            "vocab_ce": ce}), flush=True)
+
+
 def run_gpt(args, w, T, device, rank, nranks):
     """The small GPT's training step (forward, backward, AdamW) on one seeded batch,
     the page's 50-step run, plus the vocabulary-parallel cross-entropy at a large
@@ -1255,11 +1283,12 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="c5", choices=sorted(WORKLOADS) + ["c4"],
+    ap.add_argument("--workload", default="c5", choices=sorted(WORKLOADS) + ["c4", "vocab-ce"],
                     help="c5 (default): large SwiGLU MLP; c3: GELU MLP; c2: page-2 layer; "
                          "c1: tiny fp32 MLP; c4: decode sweep only; c5-2k: profiling case; "
                          "c3-sp: sequence-parallel MLP block; gpt: small GPT training; "
-                         "gqa: head-sharded grouped-query attention block")
+                         "gqa: head-sharded grouped-query attention block; vocab-ce: the "
+                         "vocabulary-parallel cross-entropy alone (M=8192, v=50304, N=8)")
     ap.add_argument("--mode", default="splitk", choices=["splitk", "buffers"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-rows", type=int, default=64)
@@ -1277,6 +1306,8 @@ def main(argv=None):
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.workload == "c4":
         return run_decode_only(args)
+    if args.workload == "vocab-ce":
+        return run_vocab_ce_only(args)
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
