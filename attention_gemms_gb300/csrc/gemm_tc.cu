@@ -93,6 +93,7 @@ struct TcParams {  // CUtensorMap members carry their own 128-byte alignment
   const void* in1;
   int64_t ldo;
   int out_f32;
+  int st32;  // outputs 32-byte aligned with a pitch of 32-byte multiples: 256-bit stores
   int64_t out_group_stride;
   int* status;
   uint64_t timeout_ns;
@@ -236,6 +237,100 @@ __device__ __forceinline__ void epi8(const TcParams& p, int g, int64_t row, int6
   } else if constexpr (EPI == EPI_PAIR) {
     st8(p.out0, idx, a);
     st8(p.out1, idx, b);
+  }
+}
+
+// ---- 16 consecutive columns: one 256-bit store per output when the host found the
+// outputs 32-byte aligned (st32), else two 128-bit stores
+__device__ __forceinline__ void st_b256(void* ptr, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+__device__ __forceinline__ void st16(void* base, int64_t idx, const float* v, bool wide) {
+  __nv_bfloat16* ptr = reinterpret_cast<__nv_bfloat16*>(base) + idx;
+  if (wide) {
+    const uint4 lo = pack8(v), hi = pack8(v + 8);
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    st_b256(ptr, w);
+  } else {
+    reinterpret_cast<uint4*>(ptr)[0] = pack8(v);
+    reinterpret_cast<uint4*>(ptr)[1] = pack8(v + 8);
+  }
+}
+__device__ __forceinline__ void st16_f32(float* ptr, const float* v, bool wide) {
+  if (wide) {
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(v[i]);
+    st_b256(ptr, w);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(v[8 + i]);
+    st_b256(ptr + 8, w);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      reinterpret_cast<float4*>(ptr)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  }
+}
+__device__ __forceinline__ void in16(const void* base, int64_t idx, float* v, bool pre, uint4 x0,
+                                     uint4 x1) {
+  if (pre) {
+    unpack8(x0, v);
+    unpack8(x1, v + 8);
+  } else {
+    ld8(base, idx, v);
+    ld8(base, idx + 8, v + 8);
+  }
+}
+
+// The epilogue of epi8 over 16 consecutive columns of one row (same arithmetic).
+template <int EPI>
+__device__ __forceinline__ void epi16(const TcParams& p, int g, int64_t row, int64_t col,
+                                      const float* a, const float* b, bool pre, uint4 i0a,
+                                      uint4 i0b, uint4 i1a, uint4 i1b) {
+  const int64_t idx = row * p.ldo + col;
+  const bool wide = p.st32 != 0;
+  float v[16], w[16];
+  if constexpr (EPI == EPI_STORE) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = a[i];
+    if (p.in0) {
+      in16(p.in0, idx, w, pre, i0a, i0b);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] += w[i];
+    }
+    if (p.out_f32)
+      st16_f32(reinterpret_cast<float*>(p.out0) + g * p.out_group_stride + idx, v, wide);
+    else
+      st16(p.out0, idx, v, wide);
+  } else if constexpr (EPI == EPI_GELU) {
+    if (p.out0) st16(p.out0, idx, a, wide);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = gelu_f(a[i]);
+    st16(p.out1, idx, v, wide);
+  } else if constexpr (EPI == EPI_SWIGLU) {
+    if (p.out0) st16(p.out0, idx, a, wide);
+    if (p.out1) st16(p.out1, idx, b, wide);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = silu_f(a[i]) * b[i];
+    st16(p.out2, idx, v, wide);
+  } else if constexpr (EPI == EPI_DGELU) {
+    in16(p.in0, idx, w, pre, i0a, i0b);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = a[i] * gelu_prime_f(w[i]);
+    st16(p.out0, idx, v, wide);
+  } else if constexpr (EPI == EPI_DSWIGLU) {
+    float uu[16], du[16];
+    in16(p.in0, idx, w, pre, i0a, i0b);
+    in16(p.in1, idx, uu, pre, i1a, i1b);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = dswiglu_f(a[i], w[i], uu[i], du[i]);
+    st16(p.out0, idx, v, wide);
+    st16(p.out1, idx, du, wide);
+  } else if constexpr (EPI == EPI_PAIR) {
+    st16(p.out0, idx, a, wide);
+    st16(p.out1, idx, b, wide);
   }
 }
 
@@ -797,17 +892,19 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_tc2_kernel(const __grid_
         tmem_ld_wait();
         if (row < p.M) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int64_t col = col_base + c * 32 + q * 8;
-            if (col < p.N) {
-              float a[8], b[8];
+          for (int qq = 0; qq < 2; ++qq) {  // 16 columns at a time
+            const int64_t col = col_base + c * 32 + qq * 16;
+            float a[16], b[16];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                a[i] = __uint_as_float(ra[q * 8 + i]);
-                b[i] = __uint_as_float(rb[q * 8 + i]);
-              }
-              epi8<EPI>(p, tc.g, row, col, a, b, kIn > 0 && has0, pin0[q], pin1[q]);
+            for (int i = 0; i < 16; ++i) {
+              a[i] = __uint_as_float(ra[qq * 16 + i]);
+              b[i] = __uint_as_float(rb[qq * 16 + i]);
             }
+            if (col + 16 <= p.N)
+              epi16<EPI>(p, tc.g, row, col, a, b, kIn > 0 && has0, pin0[2 * qq], pin0[2 * qq + 1],
+                         pin1[2 * qq], pin1[2 * qq + 1]);
+            else if (col < p.N)  // N % 8 == 0: the last 8 columns
+              epi8<EPI>(p, tc.g, row, col, a, b, kIn > 0 && has0, pin0[2 * qq], pin1[2 * qq]);
           }
         }
       }
@@ -1074,6 +1171,12 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
   prm.ldo = d.ldo;
   prm.out_f32 = d.out_f32;
   prm.out_group_stride = d.out_group_stride;
+  {
+    const int64_t esz = d.out_f32 ? 4 : 2;
+    bool ok = (d.ldo * esz) % 32 == 0 && (!d.out_f32 || (d.out_group_stride * 4) % 32 == 0);
+    for (void* o : d.out) ok = ok && reinterpret_cast<uintptr_t>(o) % 32 == 0;
+    prm.st32 = ok ? 1 : 0;
+  }
   prm.status = device_status_word();
   if (!prm.status) return fail(TP_ERR_CUDA, "device status word unavailable");
   prm.timeout_ns = wait_timeout_ns();
