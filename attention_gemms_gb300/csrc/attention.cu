@@ -13,7 +13,7 @@
 //   backward: P = exp(S - lse), Dr = rowsum(dO * O), dV = P^T dO, dP = dO V^T,
 //             dS = P * (dP - Dr), dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d)
 // At the page-2 layer's sizes (s = 128, d = 16) this is a few MFLOP per head, so
-// the kernels use CUDA cores: one thread per query row (forward, dQ) or key row
+// the kernels use CUDA cores: d/16 lanes per query row (forward, dQ) or key row
 // (dK, dV), 64 rows per CTA, the other operand streamed through shared memory in
 // blocks of 64 rows; softmax statistics in fp32.
 #include <cuda_bf16.h>
@@ -65,61 +65,75 @@ __device__ __forceinline__ void st(__nv_bfloat16* p, int64_t i, float v) {
   p[i] = __float2bfloat16_rn(v);
 }
 
+// Each query (or key) row is handled by P = D / 16 adjacent lanes; lane `part` of a row
+// owns the 16 head dimensions part, part + P, part + 2P, ... (interleaved, so the P
+// lanes of a row read consecutive shared-memory words). Partial dot products are summed
+// over the P lanes with xor-shuffles. Every lane runs every shuffle: rows past the end
+// and masked keys are handled by masking values, never by skipping the loop body.
+constexpr int DP = 16;  // head dimensions per thread
+
+template <int P>
+__device__ __forceinline__ float row_sum(float v) {
+#pragma unroll
+  for (int o = 1; o < P; o <<= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
 template <typename T, int D>
-__global__ void __launch_bounds__(RB) attn_fwd_kernel(const T* __restrict__ qkv, T* __restrict__ o,
-                                                      float* __restrict__ lse, int s,
-                                                      const HeadMap hm, float scale, int causal) {
+__global__ void __launch_bounds__(RB * (D / DP)) attn_fwd_kernel(
+    const T* __restrict__ qkv, T* __restrict__ o, float* __restrict__ lse, int s,
+    const HeadMap hm, float scale, int causal) {
+  constexpr int P = D / DP;
   __shared__ float Ks[RB][D + 1], Vs[RB][D + 1];
   const int b = blockIdx.z, t = blockIdx.y;
-  const int qi = blockIdx.x * RB + threadIdx.x;
+  const int r = threadIdx.x / P, part = threadIdx.x - r * P;
+  const int qi = blockIdx.x * RB + r;
   const int64_t ldq = hm.ldq, qc = qcol<D>(hm, t), kc = kcol<D>(hm, t), vc = vcol<D>(hm, t);
   const T* base = qkv + static_cast<int64_t>(b) * s * ldq;
   const bool valid = qi < s;
-  float q[D], acc[D];
+  float q[DP], acc[DP];
 #pragma unroll
-  for (int d = 0; d < D; ++d) {
-    q[d] = valid ? ld(base + qi * ldq, qc + d) * scale : 0.0f;
-    acc[d] = 0.0f;
+  for (int k = 0; k < DP; ++k) {
+    q[k] = valid ? ld(base + qi * ldq, qc + part + P * k) * scale : 0.0f;
+    acc[k] = 0.0f;
   }
   float m = -INFINITY, l = 0.0f;
   const int kend = causal ? min(s, static_cast<int>(blockIdx.x + 1) * RB) : s;
   for (int k0 = 0; k0 < kend; k0 += RB) {
     __syncthreads();
-    const int kj = k0 + threadIdx.x;
+    const int kj = k0 + r;
 #pragma unroll
-    for (int d = 0; d < D; ++d) {
-      Ks[threadIdx.x][d] = kj < s ? ld(base + kj * ldq, kc + d) : 0.0f;
-      Vs[threadIdx.x][d] = kj < s ? ld(base + kj * ldq, vc + d) : 0.0f;
+    for (int k = 0; k < DP; ++k) {
+      Ks[r][part + P * k] = kj < s ? ld(base + kj * ldq, kc + part + P * k) : 0.0f;
+      Vs[r][part + P * k] = kj < s ? ld(base + kj * ldq, vc + part + P * k) : 0.0f;
     }
     __syncthreads();
-    if (!valid) continue;
     for (int j0 = 0; j0 < RB; j0 += 32) {
       float sc[32];
       float mb = -INFINITY;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const int key = k0 + j0 + j;
-        float v = -INFINITY;
-        if (key < s && (!causal || key <= qi)) {
-          v = 0.0f;
+        float v = 0.0f;
 #pragma unroll
-          for (int d = 0; d < D; ++d) v = fmaf(q[d], Ks[j0 + j][d], v);
-        }
+        for (int k = 0; k < DP; ++k) v = fmaf(q[k], Ks[j0 + j][part + P * k], v);
+        v = row_sum<P>(v);
+        const int key = k0 + j0 + j;
+        if (!valid || key >= s || (causal && key > qi)) v = -INFINITY;
         sc[j] = v;
         mb = fmaxf(mb, v);
       }
       const float mn = fmaxf(m, mb);
-      if (mn == -INFINITY) continue;  // every key so far masked
+      if (mn == -INFINITY) continue;  // every key so far masked (no shuffles below)
       const float corr = expf(m - mn);
       l *= corr;
 #pragma unroll
-      for (int d = 0; d < D; ++d) acc[d] *= corr;
+      for (int k = 0; k < DP; ++k) acc[k] *= corr;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const float p = expf(sc[j] - mn);
         l += p;
 #pragma unroll
-        for (int d = 0; d < D; ++d) acc[d] = fmaf(p, Vs[j0 + j][d], acc[d]);
+        for (int k = 0; k < DP; ++k) acc[k] = fmaf(p, Vs[j0 + j][part + P * k], acc[k]);
       }
       m = mn;
     }
@@ -128,23 +142,25 @@ __global__ void __launch_bounds__(RB) attn_fwd_kernel(const T* __restrict__ qkv,
   const float inv = 1.0f / l;
   T* orow = o + (static_cast<int64_t>(b) * s + qi) * hm.ldo + t * D;
 #pragma unroll
-  for (int d = 0; d < D; ++d) st(orow, d, acc[d] * inv);
-  lse[(static_cast<int64_t>(b) * hm.H + t) * s + qi] = m + logf(l);
+  for (int k = 0; k < DP; ++k) st(orow, part + P * k, acc[k] * inv);
+  if (part == 0) lse[(static_cast<int64_t>(b) * hm.H + t) * s + qi] = m + logf(l);
 }
 
-// dK, dV: one thread per key row of one key/value head (grid.y runs over the blocks'
+// dK, dV: P lanes per key row of one key/value head (grid.y runs over the blocks'
 // key/value heads, replicas included); the query rows of every query head of the block
 // that uses it are streamed through shared memory, so the head's gradient sums their
 // contributions.
 template <typename T, int D>
-__global__ void __launch_bounds__(RB) attn_bwd_dkdv_kernel(
+__global__ void __launch_bounds__(RB * (D / DP)) attn_bwd_dkdv_kernel(
     const T* __restrict__ qkv, const T* __restrict__ o, const float* __restrict__ lse,
     const T* __restrict__ dO, T* __restrict__ dqkv, int s, const HeadMap hm, float scale,
     int causal) {
+  constexpr int P = D / DP;
   __shared__ float Qs[RB][D + 1], dOs[RB][D + 1], Ls[RB], Ds[RB];
   const int b = blockIdx.z, u = blockIdx.y;
   const int blk = u / hm.hkv, kvl = u - blk * hm.hkv;
-  const int kj = blockIdx.x * RB + threadIdx.x;
+  const int r = threadIdx.x / P, part = threadIdx.x - r * P;
+  const int kj = blockIdx.x * RB + r;
   const int64_t ldq = hm.ldq;
   const int64_t kc = blk * hm.S + hm.KO + static_cast<int64_t>(kvl) * D;
   const int64_t vc = blk * hm.S + hm.VO + static_cast<int64_t>(kvl) * D;
@@ -152,13 +168,13 @@ __global__ void __launch_bounds__(RB) attn_bwd_dkdv_kernel(
   const T* obase = o + static_cast<int64_t>(b) * s * hm.ldo;
   const T* dobase = dO + static_cast<int64_t>(b) * s * hm.ldo;
   const bool valid = kj < s;
-  float k[D], v[D], dk[D], dv[D];
+  float k[DP], v[DP], dk[DP], dv[DP];
 #pragma unroll
-  for (int d = 0; d < D; ++d) {
-    k[d] = valid ? ld(base + kj * ldq, kc + d) : 0.0f;
-    v[d] = valid ? ld(base + kj * ldq, vc + d) : 0.0f;
-    dk[d] = 0.0f;
-    dv[d] = 0.0f;
+  for (int c = 0; c < DP; ++c) {
+    k[c] = valid ? ld(base + kj * ldq, kc + part + P * c) : 0.0f;
+    v[c] = valid ? ld(base + kj * ldq, vc + part + P * c) : 0.0f;
+    dk[c] = 0.0f;
+    dv[c] = 0.0f;
   }
   const int qstart = causal ? static_cast<int>(blockIdx.x) * RB : 0;
   for (int tl = kvl * hm.g; tl < (kvl + 1) * hm.g; ++tl) {  // the block's query heads of this group
@@ -167,36 +183,41 @@ __global__ void __launch_bounds__(RB) attn_bwd_dkdv_kernel(
     const float* lrow = lse + (static_cast<int64_t>(b) * hm.H + t) * s;
     for (int q0 = qstart; q0 < s; q0 += RB) {
       __syncthreads();
-      const int qi = q0 + threadIdx.x;
+      const int qi = q0 + r;
       float dsum = 0.0f;
 #pragma unroll
-      for (int d = 0; d < D; ++d) {
-        const float qv = qi < s ? ld(base + qi * ldq, qc + d) : 0.0f;
-        const float dov = qi < s ? ld(dobase + qi * hm.ldo, t * D + d) : 0.0f;
-        const float ov = qi < s ? ld(obase + qi * hm.ldo, t * D + d) : 0.0f;
-        Qs[threadIdx.x][d] = qv;
-        dOs[threadIdx.x][d] = dov;
+      for (int c = 0; c < DP; ++c) {
+        const int dd = part + P * c;
+        const float qv = qi < s ? ld(base + qi * ldq, qc + dd) : 0.0f;
+        const float dov = qi < s ? ld(dobase + qi * hm.ldo, t * D + dd) : 0.0f;
+        const float ov = qi < s ? ld(obase + qi * hm.ldo, t * D + dd) : 0.0f;
+        Qs[r][dd] = qv;
+        dOs[r][dd] = dov;
         dsum = fmaf(dov, ov, dsum);
       }
-      Ls[threadIdx.x] = qi < s ? lrow[qi] : 0.0f;
-      Ds[threadIdx.x] = dsum;
+      dsum = row_sum<P>(dsum);
+      if (part == 0) {
+        Ls[r] = qi < s ? lrow[qi] : 0.0f;
+        Ds[r] = dsum;
+      }
       __syncthreads();
-      if (!valid) continue;
       const int iend = min(RB, s - q0);
       for (int i = 0; i < iend; ++i) {
-        if (causal && kj > q0 + i) continue;
         float sc = 0.0f, dp = 0.0f;
 #pragma unroll
-        for (int d = 0; d < D; ++d) {
-          sc = fmaf(Qs[i][d], k[d], sc);
-          dp = fmaf(dOs[i][d], v[d], dp);
+        for (int c = 0; c < DP; ++c) {
+          sc = fmaf(Qs[i][part + P * c], k[c], sc);
+          dp = fmaf(dOs[i][part + P * c], v[c], dp);
         }
-        const float p = expf(sc * scale - Ls[i]);
-        const float ds = p * (dp - Ds[i]) * scale;
+        sc = row_sum<P>(sc);
+        dp = row_sum<P>(dp);
+        const bool live = valid && !(causal && kj > q0 + i);
+        const float pr = live ? expf(sc * scale - Ls[i]) : 0.0f;
+        const float ds = pr * (dp - Ds[i]) * scale;
 #pragma unroll
-        for (int d = 0; d < D; ++d) {
-          dv[d] = fmaf(p, dOs[i][d], dv[d]);
-          dk[d] = fmaf(ds, Qs[i][d], dk[d]);
+        for (int c = 0; c < DP; ++c) {
+          dv[c] = fmaf(pr, dOs[i][part + P * c], dv[c]);
+          dk[c] = fmaf(ds, Qs[i][part + P * c], dk[c]);
         }
       }
     }
@@ -204,78 +225,80 @@ __global__ void __launch_bounds__(RB) attn_bwd_dkdv_kernel(
   if (!valid) return;
   T* row = dqkv + (static_cast<int64_t>(b) * s + kj) * ldq;
 #pragma unroll
-  for (int d = 0; d < D; ++d) {
-    st(row, kc + d, dk[d]);
-    st(row, vc + d, dv[d]);
+  for (int c = 0; c < DP; ++c) {
+    st(row, kc + part + P * c, dk[c]);
+    st(row, vc + part + P * c, dv[c]);
   }
 }
 
-// dQ: one thread per query row; key rows streamed through shared memory
+// dQ: P lanes per query row; key rows streamed through shared memory
 template <typename T, int D>
-__global__ void __launch_bounds__(RB) attn_bwd_dq_kernel(
+__global__ void __launch_bounds__(RB * (D / DP)) attn_bwd_dq_kernel(
     const T* __restrict__ qkv, const T* __restrict__ o, const float* __restrict__ lse,
     const T* __restrict__ dO, T* __restrict__ dqkv, int s, const HeadMap hm, float scale,
     int causal) {
+  constexpr int P = D / DP;
   __shared__ float Ks[RB][D + 1], Vs[RB][D + 1];
   const int b = blockIdx.z, t = blockIdx.y;
-  const int qi = blockIdx.x * RB + threadIdx.x;
+  const int r = threadIdx.x / P, part = threadIdx.x - r * P;
+  const int qi = blockIdx.x * RB + r;
   const int64_t ldq = hm.ldq, qc = qcol<D>(hm, t), kc = kcol<D>(hm, t), vc = vcol<D>(hm, t);
   const T* base = qkv + static_cast<int64_t>(b) * s * ldq;
   const bool valid = qi < s;
-  float q[D], dov[D], dq[D];
+  float q[DP], dov[DP], dq[DP];
   float dsum = 0.0f, L = 0.0f;
-  if (valid) {
-    const T* orow = o + (static_cast<int64_t>(b) * s + qi) * hm.ldo + t * D;
-    const T* dorow = dO + (static_cast<int64_t>(b) * s + qi) * hm.ldo + t * D;
+  {
+    const T* orow = o + (static_cast<int64_t>(b) * s + (valid ? qi : 0)) * hm.ldo + t * D;
+    const T* dorow = dO + (static_cast<int64_t>(b) * s + (valid ? qi : 0)) * hm.ldo + t * D;
 #pragma unroll
-    for (int d = 0; d < D; ++d) {
-      q[d] = ld(base + qi * ldq, qc + d);
-      dov[d] = ld(dorow, d);
-      dsum = fmaf(dov[d], ld(orow, d), dsum);
-      dq[d] = 0.0f;
+    for (int c = 0; c < DP; ++c) {
+      const int dd = part + P * c;
+      q[c] = valid ? ld(base + qi * ldq, qc + dd) : 0.0f;
+      dov[c] = valid ? ld(dorow, dd) : 0.0f;
+      dsum = fmaf(dov[c], valid ? ld(orow, dd) : 0.0f, dsum);
+      dq[c] = 0.0f;
     }
-    L = lse[(static_cast<int64_t>(b) * hm.H + t) * s + qi];
-  } else {
-#pragma unroll
-    for (int d = 0; d < D; ++d) q[d] = dov[d] = dq[d] = 0.0f;
+    dsum = row_sum<P>(dsum);
+    L = valid ? lse[(static_cast<int64_t>(b) * hm.H + t) * s + qi] : 0.0f;
   }
   const int kend = causal ? min(s, static_cast<int>(blockIdx.x + 1) * RB) : s;
   for (int k0 = 0; k0 < kend; k0 += RB) {
     __syncthreads();
-    const int kj = k0 + threadIdx.x;
+    const int kj = k0 + r;
 #pragma unroll
-    for (int d = 0; d < D; ++d) {
-      Ks[threadIdx.x][d] = kj < s ? ld(base + kj * ldq, kc + d) : 0.0f;
-      Vs[threadIdx.x][d] = kj < s ? ld(base + kj * ldq, vc + d) : 0.0f;
+    for (int c = 0; c < DP; ++c) {
+      Ks[r][part + P * c] = kj < s ? ld(base + kj * ldq, kc + part + P * c) : 0.0f;
+      Vs[r][part + P * c] = kj < s ? ld(base + kj * ldq, vc + part + P * c) : 0.0f;
     }
     __syncthreads();
-    if (!valid) continue;
     const int jend = min(RB, s - k0);
     for (int j = 0; j < jend; ++j) {
-      if (causal && k0 + j > qi) break;
       float sc = 0.0f, dp = 0.0f;
 #pragma unroll
-      for (int d = 0; d < D; ++d) {
-        sc = fmaf(q[d], Ks[j][d], sc);
-        dp = fmaf(dov[d], Vs[j][d], dp);
+      for (int c = 0; c < DP; ++c) {
+        sc = fmaf(q[c], Ks[j][part + P * c], sc);
+        dp = fmaf(dov[c], Vs[j][part + P * c], dp);
       }
-      const float p = expf(sc * scale - L);
-      const float ds = p * (dp - dsum) * scale;
+      sc = row_sum<P>(sc);
+      dp = row_sum<P>(dp);
+      const bool live = valid && !(causal && k0 + j > qi);
+      const float pr = live ? expf(sc * scale - L) : 0.0f;
+      const float ds = pr * (dp - dsum) * scale;
 #pragma unroll
-      for (int d = 0; d < D; ++d) dq[d] = fmaf(ds, Ks[j][d], dq[d]);
+      for (int c = 0; c < DP; ++c) dq[c] = fmaf(ds, Ks[j][part + P * c], dq[c]);
     }
   }
   if (!valid) return;
   T* row = dqkv + (static_cast<int64_t>(b) * s + qi) * ldq;
 #pragma unroll
-  for (int d = 0; d < D; ++d) st(row, qc + d, dq[d]);
+  for (int c = 0; c < DP; ++c) st(row, qc + part + P * c, dq[c]);
 }
 
 template <typename T, int D>
 tp_status run_fwd(const void* qkv, void* o, float* lse, int b, int s, const HeadMap& hm,
                   int causal, cudaStream_t st) {
   const dim3 grid((s + RB - 1) / RB, hm.H, b);
-  attn_fwd_kernel<T, D><<<grid, RB, 0, st>>>(static_cast<const T*>(qkv), static_cast<T*>(o), lse,
+  attn_fwd_kernel<T, D><<<grid, RB * (D / DP), 0, st>>>(static_cast<const T*>(qkv), static_cast<T*>(o), lse,
                                               s, hm, 1.0f / sqrtf(static_cast<float>(D)), causal);
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
@@ -286,10 +309,10 @@ template <typename T, int D>
 tp_status run_bwd(const void* qkv, const void* o, const float* lse, const void* dO, void* dqkv,
                   int b, int s, const HeadMap& hm, int kv_heads, int causal, cudaStream_t st) {
   const float scale = 1.0f / sqrtf(static_cast<float>(D));
-  attn_bwd_dkdv_kernel<T, D><<<dim3((s + RB - 1) / RB, kv_heads, b), RB, 0, st>>>(
+  attn_bwd_dkdv_kernel<T, D><<<dim3((s + RB - 1) / RB, kv_heads, b), RB * (D / DP), 0, st>>>(
       static_cast<const T*>(qkv), static_cast<const T*>(o), lse, static_cast<const T*>(dO),
       static_cast<T*>(dqkv), s, hm, scale, causal);
-  attn_bwd_dq_kernel<T, D><<<dim3((s + RB - 1) / RB, hm.H, b), RB, 0, st>>>(
+  attn_bwd_dq_kernel<T, D><<<dim3((s + RB - 1) / RB, hm.H, b), RB * (D / DP), 0, st>>>(
       static_cast<const T*>(qkv), static_cast<const T*>(o), lse, static_cast<const T*>(dO),
       static_cast<T*>(dqkv), s, hm, scale, causal);
   count_launch(2);
