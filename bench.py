@@ -248,6 +248,57 @@ def make_inputs(w, rank, device):
 
 # ------------------------------------------------------------------ our arm
 
+def overlapped_e2e(stream, steps, step_on, ins, ins_host, outs, outs_host):
+    """Time `steps` end-to-end steps: every step copies its inputs in from pinned host
+    memory (ins_host -> a device input set) and its results out (a device output set ->
+    outs_host). Copies run on a second stream and overlap the neighbouring steps'
+    compute; inputs and outputs are double-buffered (ins / outs are the first sets, a
+    second set is allocated like them) and events order each copy after the step that
+    frees its buffer. step_on(in_set, out_set) enqueues one step on `stream`.
+    Returns ms per step (CUDA events on `stream`)."""
+    import torch
+    ins_b = [list(ins), [torch.empty_like(t) for t in ins]]
+    outs_b = [list(outs), [torch.empty_like(t) for t in outs]]
+    copy = torch.cuda.Stream(device=stream.device)
+    ev = torch.cuda.Event
+    torch.cuda.synchronize()
+    e0, e1 = ev(enable_timing=True), ev(enable_timing=True)
+    e0.record(stream)
+    copy.wait_event(e0)
+    in_ready, step_done, out_read = [ev(), ev()], [None, None], [None, None]
+
+    def copy_in(k):
+        with torch.cuda.stream(copy):
+            for dst, src in zip(ins_b[k], ins_host):
+                dst.copy_(src, non_blocking=True)
+        in_ready[k] = ev()
+        in_ready[k].record(copy)
+
+    copy_in(0)
+    for k in range(steps):
+        cur = k % 2
+        if k + 1 < steps:  # next step's inputs, once the step that used that buffer is done
+            if step_done[1 - cur] is not None:
+                copy.wait_event(step_done[1 - cur])
+            copy_in(1 - cur)
+        stream.wait_event(in_ready[cur])
+        if out_read[cur] is not None:
+            stream.wait_event(out_read[cur])
+        step_on(ins_b[cur], outs_b[cur])
+        step_done[cur] = ev()
+        step_done[cur].record(stream)
+        copy.wait_event(step_done[cur])
+        with torch.cuda.stream(copy):
+            for dst, src in zip(outs_host, outs_b[cur]):
+                dst.copy_(src, non_blocking=True)
+        out_read[cur] = ev()
+        out_read[cur].record(copy)
+    stream.wait_stream(copy)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
 def run_ours(args, w):
     import torch
     from attention_gemms_gb300 import build as B
@@ -288,17 +339,20 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream()
     col_ev = []
 
-    def step(record=False):
+    def step_on(Xs, dZs, Zs, dXs, record=False):
         if record:
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-        T.tp_col_linear(d["X"], d["W1"], d["W1u"], Y, Yu, H, M, h, f, N, BF, act, stream)
+        T.tp_col_linear(Xs, d["W1"], d["W1u"], Y, Yu, H, M, h, f, N, BF, act, stream)
         if record:
             b.record(stream)
             col_ev.append((a, b))
-        T.tp_row_linear(H, d["W2"], None, Z, M, f, h, N, BF, mode, ws, ws.numel(), stream)
-        T.tp_mlp_bwd(d["X"], d["W1"], d["W1u"], d["W2"], Y, Yu, H, d["dZ"], dX, dW1, dW1u, dW2,
+        T.tp_row_linear(H, d["W2"], None, Zs, M, f, h, N, BF, mode, ws, ws.numel(), stream)
+        T.tp_mlp_bwd(Xs, d["W1"], d["W1u"], d["W2"], Y, Yu, H, dZs, dXs, dW1, dW1u, dW2,
                      M, h, f, N, BF, act, mode, ws, ws.numel(), stream)
+
+    def step(record=False):
+        step_on(d["X"], d["dZ"], Z, dX, record)
 
     for _ in range(args.warmup):
         step()
@@ -325,31 +379,20 @@ def run_ours(args, w):
     if T.tp_check_status(stream) != 0:
         raise RuntimeError("device wait timeout in the timed region: " + T.tp_last_error())
 
-    # end to end: pinned host inputs in, results (Z, dX) out, every step
-    Xp = torch.empty((M, h), dtype=bf, pin_memory=True)
-    dZp = torch.empty((M, h), dtype=bf, pin_memory=True)
+    # end to end: inputs in from pinned host memory and results out, every step,
+    # copies overlapped with the neighbouring steps' compute (overlapped_e2e)
+    pin = lambda: torch.empty((M, h), dtype=bf, pin_memory=True)
+    Xp, dZp = pin(), pin()
     if f32:
         Xp.numpy()[:] = hostin["X"]
         dZp.numpy()[:] = hostin["dZ"]
     else:
         Xp.view(torch.int16).numpy()[:] = hostin["X"].view(np.int16)
         dZp.view(torch.int16).numpy()[:] = hostin["dZ"].view(np.int16)
-    Zp = torch.empty((M, h), dtype=bf, pin_memory=True)
-    dXp = torch.empty((M, h), dtype=bf, pin_memory=True)
     barrier()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        d["X"].copy_(Xp, non_blocking=True)
-        d["dZ"].copy_(dZp, non_blocking=True)
-        step()
-        Zp.copy_(Z, non_blocking=True)
-        dXp.copy_(dX, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
+    e2e_ms = overlapped_e2e(stream, args.steps, lambda i, o: step_on(i[0], i[1], o[0], o[1]),
+                            [d["X"], d["dZ"]], [Xp, dZp], [Z, dX], [pin(), pin()])
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
     clk = clocks.stop()
 
     ms_max = max_over_ranks(ms, device)
@@ -474,19 +517,19 @@ def run_sp(args, w, T, device, rank, nranks):
     col_ms = timed(lambda: T.tp_col_linear(xn, W1, W1u, Y, Yu, H, M, h, f, N, BF, A, stream),
                    args.steps)
     # end to end: x and dout in from pinned host memory, out and dx back, every step
+    # (copies overlapped with the neighbouring steps' compute)
     pin = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
     Xp, dZp = pin(hostin["X"]), pin(hostin["dZ"])
-    outp = torch.empty((M, h), dtype=bf, pin_memory=True)
-    dxp = torch.empty((M, h), dtype=bf, pin_memory=True)
+    hostbuf = lambda: torch.empty((M, h), dtype=bf, pin_memory=True)
 
-    def e2e_step():
-        X.copy_(Xp, non_blocking=True)
-        dZ.copy_(dZp, non_blocking=True)
-        sp_step()
-        outp.copy_(out, non_blocking=True)
-        dxp.copy_(dx, non_blocking=True)
+    def sp_step_on(i, o):
+        T.tp_sp_mlp_fwd(i[0], g, b, W1, W1u, W2, xn, mean, rstd, Y, Yu, H, o[0], M, h, f, N, BF,
+                        A, mode, ws, ws.numel(), stream)
+        T.tp_sp_mlp_bwd(i[0], g, W1, W1u, W2, xn, mean, rstd, Y, Yu, H, i[1], o[1], dg, db, dgr,
+                        dbr, dW1, dWu, dW2, M, h, f, N, BF, A, mode, ws, ws.numel(), stream)
     barrier()
-    e2e_ms = timed(e2e_step, args.steps)
+    e2e_ms = overlapped_e2e(stream, args.steps, sp_step_on, [X, dZ], [Xp, dZp], [out, dx],
+                            [hostbuf(), hostbuf()])
     clk = clocks.stop()
     if T.tp_check_status(stream) != 0:
         raise RuntimeError("device wait timeout: " + T.tp_last_error())
