@@ -71,6 +71,21 @@ __device__ __forceinline__ void st(__nv_bfloat16* p, int64_t i, float v) {
 // over the P lanes with xor-shuffles. Every lane runs every shuffle: rows past the end
 // and masked keys are handled by masking values, never by skipping the loop body.
 constexpr int DP = 16;  // head dimensions per thread
+// Shared-memory rows hold each lane's 16 dimensions contiguously, padded to 20 floats:
+// a lane reads them with four 128-bit loads, and the P lanes of a row (offsets 0, 80,
+// 160, 240 bytes) hit different banks.
+constexpr int DPAD = DP + 4;
+
+__device__ __forceinline__ void lds16(const float* src, float* v) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float4 t = reinterpret_cast<const float4*>(src)[u];
+    v[4 * u] = t.x;
+    v[4 * u + 1] = t.y;
+    v[4 * u + 2] = t.z;
+    v[4 * u + 3] = t.w;
+  }
+}
 
 template <int P>
 __device__ __forceinline__ float row_sum(float v) {
@@ -84,7 +99,8 @@ __global__ void __launch_bounds__(RB * (D / DP)) attn_fwd_kernel(
     const T* __restrict__ qkv, T* __restrict__ o, float* __restrict__ lse, int s,
     const HeadMap hm, float scale, int causal) {
   constexpr int P = D / DP;
-  __shared__ float Ks[RB][D + 1], Vs[RB][D + 1];
+  __shared__ __align__(16) float Ks[RB][P][DPAD];
+  __shared__ __align__(16) float Vs[RB][P][DPAD];
   const int b = blockIdx.z, t = blockIdx.y;
   const int r = threadIdx.x / P, part = threadIdx.x - r * P;
   const int qi = blockIdx.x * RB + r;
@@ -104,8 +120,8 @@ __global__ void __launch_bounds__(RB * (D / DP)) attn_fwd_kernel(
     const int kj = k0 + r;
 #pragma unroll
     for (int k = 0; k < DP; ++k) {
-      Ks[r][part + P * k] = kj < s ? ld(base + kj * ldq, kc + part + P * k) : 0.0f;
-      Vs[r][part + P * k] = kj < s ? ld(base + kj * ldq, vc + part + P * k) : 0.0f;
+      Ks[r][part][k] = kj < s ? ld(base + kj * ldq, kc + part + P * k) : 0.0f;
+      Vs[r][part][k] = kj < s ? ld(base + kj * ldq, vc + part + P * k) : 0.0f;
     }
     __syncthreads();
     for (int j0 = 0; j0 < RB; j0 += 32) {
@@ -113,9 +129,11 @@ __global__ void __launch_bounds__(RB * (D / DP)) attn_fwd_kernel(
       float mb = -INFINITY;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
+        float kv[DP];
+        lds16(&Ks[j0 + j][part][0], kv);
         float v = 0.0f;
 #pragma unroll
-        for (int k = 0; k < DP; ++k) v = fmaf(q[k], Ks[j0 + j][part + P * k], v);
+        for (int k = 0; k < DP; ++k) v = fmaf(q[k], kv[k], v);
         v = row_sum<P>(v);
         const int key = k0 + j0 + j;
         if (!valid || key >= s || (causal && key > qi)) v = -INFINITY;
@@ -132,8 +150,10 @@ __global__ void __launch_bounds__(RB * (D / DP)) attn_fwd_kernel(
       for (int j = 0; j < 32; ++j) {
         const float p = expf(sc[j] - mn);
         l += p;
+        float vv[DP];
+        lds16(&Vs[j0 + j][part][0], vv);
 #pragma unroll
-        for (int k = 0; k < DP; ++k) acc[k] = fmaf(p, Vs[j0 + j][part + P * k], acc[k]);
+        for (int k = 0; k < DP; ++k) acc[k] = fmaf(p, vv[k], acc[k]);
       }
       m = mn;
     }
@@ -156,7 +176,9 @@ __global__ void __launch_bounds__(RB * (D / DP)) attn_bwd_dkdv_kernel(
     const T* __restrict__ dO, T* __restrict__ dqkv, int s, const HeadMap hm, float scale,
     int causal) {
   constexpr int P = D / DP;
-  __shared__ float Qs[RB][D + 1], dOs[RB][D + 1], Ls[RB], Ds[RB];
+  __shared__ __align__(16) float Qs[RB][P][DPAD];
+  __shared__ __align__(16) float dOs[RB][P][DPAD];
+  __shared__ float Ls[RB], Ds[RB];
   const int b = blockIdx.z, u = blockIdx.y;
   const int blk = u / hm.hkv, kvl = u - blk * hm.hkv;
   const int r = threadIdx.x / P, part = threadIdx.x - r * P;
@@ -191,8 +213,8 @@ __global__ void __launch_bounds__(RB * (D / DP)) attn_bwd_dkdv_kernel(
         const float qv = qi < s ? ld(base + qi * ldq, qc + dd) : 0.0f;
         const float dov = qi < s ? ld(dobase + qi * hm.ldo, t * D + dd) : 0.0f;
         const float ov = qi < s ? ld(obase + qi * hm.ldo, t * D + dd) : 0.0f;
-        Qs[r][dd] = qv;
-        dOs[r][dd] = dov;
+        Qs[r][part][c] = qv;
+        dOs[r][part][c] = dov;
         dsum = fmaf(dov, ov, dsum);
       }
       dsum = row_sum<P>(dsum);
@@ -203,11 +225,14 @@ __global__ void __launch_bounds__(RB * (D / DP)) attn_bwd_dkdv_kernel(
       __syncthreads();
       const int iend = min(RB, s - q0);
       for (int i = 0; i < iend; ++i) {
+        float qv[DP], dov[DP];
+        lds16(&Qs[i][part][0], qv);
+        lds16(&dOs[i][part][0], dov);
         float sc = 0.0f, dp = 0.0f;
 #pragma unroll
         for (int c = 0; c < DP; ++c) {
-          sc = fmaf(Qs[i][part + P * c], k[c], sc);
-          dp = fmaf(dOs[i][part + P * c], v[c], dp);
+          sc = fmaf(qv[c], k[c], sc);
+          dp = fmaf(dov[c], v[c], dp);
         }
         sc = row_sum<P>(sc);
         dp = row_sum<P>(dp);
@@ -216,8 +241,8 @@ __global__ void __launch_bounds__(RB * (D / DP)) attn_bwd_dkdv_kernel(
         const float ds = pr * (dp - Ds[i]) * scale;
 #pragma unroll
         for (int c = 0; c < DP; ++c) {
-          dv[c] = fmaf(pr, dOs[i][part + P * c], dv[c]);
-          dk[c] = fmaf(ds, Qs[i][part + P * c], dk[c]);
+          dv[c] = fmaf(pr, dov[c], dv[c]);
+          dk[c] = fmaf(ds, qv[c], dk[c]);
         }
       }
     }
@@ -238,7 +263,8 @@ __global__ void __launch_bounds__(RB * (D / DP)) attn_bwd_dq_kernel(
     const T* __restrict__ dO, T* __restrict__ dqkv, int s, const HeadMap hm, float scale,
     int causal) {
   constexpr int P = D / DP;
-  __shared__ float Ks[RB][D + 1], Vs[RB][D + 1];
+  __shared__ __align__(16) float Ks[RB][P][DPAD];
+  __shared__ __align__(16) float Vs[RB][P][DPAD];
   const int b = blockIdx.z, t = blockIdx.y;
   const int r = threadIdx.x / P, part = threadIdx.x - r * P;
   const int qi = blockIdx.x * RB + r;
@@ -267,17 +293,20 @@ __global__ void __launch_bounds__(RB * (D / DP)) attn_bwd_dq_kernel(
     const int kj = k0 + r;
 #pragma unroll
     for (int c = 0; c < DP; ++c) {
-      Ks[r][part + P * c] = kj < s ? ld(base + kj * ldq, kc + part + P * c) : 0.0f;
-      Vs[r][part + P * c] = kj < s ? ld(base + kj * ldq, vc + part + P * c) : 0.0f;
+      Ks[r][part][c] = kj < s ? ld(base + kj * ldq, kc + part + P * c) : 0.0f;
+      Vs[r][part][c] = kj < s ? ld(base + kj * ldq, vc + part + P * c) : 0.0f;
     }
     __syncthreads();
     const int jend = min(RB, s - k0);
     for (int j = 0; j < jend; ++j) {
+      float kv[DP], vv[DP];
+      lds16(&Ks[j][part][0], kv);
+      lds16(&Vs[j][part][0], vv);
       float sc = 0.0f, dp = 0.0f;
 #pragma unroll
       for (int c = 0; c < DP; ++c) {
-        sc = fmaf(q[c], Ks[j][part + P * c], sc);
-        dp = fmaf(dov[c], Vs[j][part + P * c], dp);
+        sc = fmaf(q[c], kv[c], sc);
+        dp = fmaf(dov[c], vv[c], dp);
       }
       sc = row_sum<P>(sc);
       dp = row_sum<P>(dp);
@@ -285,7 +314,7 @@ __global__ void __launch_bounds__(RB * (D / DP)) attn_bwd_dq_kernel(
       const float pr = live ? expf(sc * scale - L) : 0.0f;
       const float ds = pr * (dp - dsum) * scale;
 #pragma unroll
-      for (int c = 0; c < DP; ++c) dq[c] = fmaf(ds, Ks[j][part + P * c], dq[c]);
+      for (int c = 0; c < DP; ++c) dq[c] = fmaf(ds, kv[c], dq[c]);
     }
   }
   if (!valid) return;
