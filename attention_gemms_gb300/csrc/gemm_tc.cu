@@ -1020,11 +1020,11 @@ tp_status make_map_3d(CUtensorMap* m, const Operand& op, uint32_t chunks) {
 template <int BN, int EPI, bool DEC>
 tp_status launch_bn_epi(const TcParams& prm, int grid, cudaStream_t st) {
   auto kern = gemm_tc_kernel<BN, EPI, DEC>;
-  static bool attr_set = false;  // per instantiation; benign race (idempotent)
-  if (!attr_set) {
+  static std::atomic<uint64_t> attr_set{0};  // per instantiation and device
+  if (needs_setup(attr_set)) {
     TP_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      TcCfg<BN, DEC>::SMEM_BYTES));
-    attr_set = true;
+    mark_device(attr_set);
   }
   kern<<<grid, kThreads, TcCfg<BN, DEC>::SMEM_BYTES, st>>>(prm);
   count_launch();
@@ -1048,7 +1048,10 @@ tp_status launch_bn(int epi, const TcParams& prm, int grid, cudaStream_t st) {
 template <int EPI>
 tp_status launch_pair_epi(const TcParams& prm, int64_t ntiles, cudaStream_t st) {
   auto kern = gemm_tc2_kernel<EPI>;
-  static int max_pairs = 0;  // per instantiation; benign race (idempotent)
+  static std::atomic<int> max_pairs_dev[64];  // per instantiation and device (0: unknown)
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = -1;
+  int max_pairs = dev >= 0 ? max_pairs_dev[dev].load() : 0;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1068,6 +1071,7 @@ tp_status launch_pair_epi(const TcParams& prm, int64_t ntiles, cudaStream_t st) 
     TP_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, kern, &cfg));
     if (n <= 0) return fail(TP_ERR_CUDA, "no CTA pair of the GEMM kernel fits on the device");
     max_pairs = n;
+    if (dev >= 0) max_pairs_dev[dev].store(n);
   }
   const int pairs = static_cast<int>(std::min<int64_t>(ntiles, max_pairs));
   cfg.gridDim = dim3(2 * static_cast<unsigned>(pairs), 1, 1);

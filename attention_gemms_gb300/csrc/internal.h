@@ -4,6 +4,7 @@
 #pragma once
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <initializer_list>
@@ -35,6 +36,19 @@ tp_status cuda_fail(cudaError_t e, const char* what);
 int* device_status_word();             // for the current device; nullptr on failure
 uint64_t wait_timeout_ns();
 int device_sm_count();                 // current device
+// One-time per-device set-up (kernel attributes): true when `done` has no mark for the
+// current device; mark_device(done) records it. The set-up is idempotent, so two
+// threads racing only repeat it. Devices beyond 63 are set up on every call.
+inline uint64_t device_bit() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  return 1ull << dev;
+}
+inline bool needs_setup(const std::atomic<uint64_t>& done) {
+  const uint64_t b = device_bit();
+  return b == 0 || (done.load(std::memory_order_acquire) & b) == 0;
+}
+inline void mark_device(std::atomic<uint64_t>& done) { done.fetch_or(device_bit()); }
 void count_launch(int n = 1);
 
 // ------------------------------------------------------------------ GEMM problem

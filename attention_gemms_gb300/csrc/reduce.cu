@@ -268,11 +268,11 @@ tp_status run_ln(const float* P, const void* R, const float* gamma, const float*
   while (G < chunks && G < 256) G *= 2;
   const int wpr = G / 32, rows = 8 / wpr, iters = (chunks + G - 1) / G;
   const size_t smem = static_cast<size_t>(rows) * iters * 2 * G * sizeof(float4);
-  static bool attr_set = false;  // h <= 16384: at most 64 KB
-  if (!attr_set) {
+  static std::atomic<uint64_t> attr_set{0};  // per device; h <= 16384: at most 64 KB
+  if (needs_setup(attr_set)) {
     TP_CUDA_TRY(cudaFuncSetAttribute(shard_reduce_ln_kernel<T>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024));
-    attr_set = true;
+    mark_device(attr_set);
   }
   const int64_t blocks = (M + rows - 1) / rows;
   if (blocks > 2147483647ll) return fail(TP_ERR_SHAPE, "too many rows for one launch");
