@@ -94,6 +94,7 @@ struct TcParams {  // CUtensorMap members carry their own 128-byte alignment
   int64_t ldo;
   int out_f32;
   int st32;  // outputs 32-byte aligned with a pitch of 32-byte multiples: 256-bit stores
+  int ld32;  // epilogue inputs likewise: 256-bit loads
   int64_t out_group_stride;
   int* status;
   uint64_t timeout_ns;
@@ -238,6 +239,14 @@ __device__ __forceinline__ void epi8(const TcParams& p, int g, int64_t row, int6
     st8(p.out0, idx, a);
     st8(p.out1, idx, b);
   }
+}
+
+// ---- 32 bytes (16 bf16) of an epilogue input in one non-coherent 256-bit load
+__device__ __forceinline__ void ld_b256(const void* ptr, uint4& lo, uint4& hi) {
+  asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y),
+                 "=r"(hi.z), "=r"(hi.w)
+               : "l"(ptr));
 }
 
 // ---- 16 consecutive columns: one 256-bit store per output when the host found the
@@ -876,16 +885,22 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_tc2_kernel(const __grid_
         const bool has0 = kIn >= 1 && p.in0 != nullptr;
         if (kIn > 0 && row < p.M) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int64_t col = col_base + c * 32 + q * 8;
-            if (col < p.N) {
-              const int64_t idx = row * p.ldo + col;
-              if (has0)
-                pin0[q] = __ldg(reinterpret_cast<const uint4*>(
-                    reinterpret_cast<const __nv_bfloat16*>(p.in0) + idx));
-              if (kIn == 2)
-                pin1[q] = __ldg(reinterpret_cast<const uint4*>(
-                    reinterpret_cast<const __nv_bfloat16*>(p.in1) + idx));
+          for (int qq = 0; qq < 2; ++qq) {
+            const int64_t col = col_base + c * 32 + qq * 16;
+            const int64_t idx = row * p.ldo + col;
+            const __nv_bfloat16* i0 = reinterpret_cast<const __nv_bfloat16*>(p.in0) + idx;
+            const __nv_bfloat16* i1 = reinterpret_cast<const __nv_bfloat16*>(p.in1) + idx;
+            if (p.ld32 && col + 16 <= p.N) {  // a whole 32-byte sector per load
+              if (has0) ld_b256(i0, pin0[2 * qq], pin0[2 * qq + 1]);
+              if (kIn == 2) ld_b256(i1, pin1[2 * qq], pin1[2 * qq + 1]);
+            } else {
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                if (col + 8 * hh < p.N) {
+                  if (has0) pin0[2 * qq + hh] = __ldg(reinterpret_cast<const uint4*>(i0 + 8 * hh));
+                  if (kIn == 2) pin1[2 * qq + hh] = __ldg(reinterpret_cast<const uint4*>(i1 + 8 * hh));
+                }
+              }
             }
           }
         }
@@ -1180,6 +1195,9 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
     bool ok = (d.ldo * esz) % 32 == 0 && (!d.out_f32 || (d.out_group_stride * 4) % 32 == 0);
     for (void* o : d.out) ok = ok && reinterpret_cast<uintptr_t>(o) % 32 == 0;
     prm.st32 = ok ? 1 : 0;
+    bool ok_in = (d.ldo * 2) % 32 == 0;
+    for (const void* i : d.in) ok_in = ok_in && reinterpret_cast<uintptr_t>(i) % 32 == 0;
+    prm.ld32 = ok_in ? 1 : 0;
   }
   prm.status = device_status_word();
   if (!prm.status) return fail(TP_ERR_CUDA, "device status word unavailable");
