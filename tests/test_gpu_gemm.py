@@ -53,3 +53,58 @@ def test_gemm_bf16(at, bt, MNK):
 def test_gemm_f32(at, bt):
     e, ok = _run(67, 45, 33, at, bt, dtype="f32")
     assert e <= F32_TOL and ok, e
+
+
+# ---- the CTA-pair kernel's epilogue paths: 256-bit stores / loads when the outputs
+# (inputs) are 32-byte aligned, 128-bit otherwise, and the 8-column tail when N % 16 == 8
+
+@pytest.mark.parametrize("MNK", [(384, 264, 192), (512, 520, 128)])
+def test_pair_gemm_ragged_columns(MNK):
+    M, N, K = MNK
+    e, ok = _run(M, N, K, False, False)
+    assert e <= BF16_TOL and ok, e
+
+
+def test_pair_gemm_output_only_16_byte_aligned():
+    M, N, K = 512, 512, 256
+    A = tensor((M, K), 610)[1]
+    B = tensor((K, N), 611, 0.1)[1]
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    buf = torch.empty(M * N + 16, dtype=torch.bfloat16, device="cuda")
+    C16 = buf[8:8 + M * N].view(M, N)  # 16 bytes past a 256-byte boundary
+    T.tp_gemm(A, B, C, M, N, K, False, False, T.DType.BF16)
+    T.tp_gemm(A, B, C16, M, N, K, False, False, T.DType.BF16)
+    torch.cuda.synchronize()
+    assert C16.data_ptr() % 32 == 16
+    assert torch.equal(C, C16)
+
+
+def test_pair_gemm_epilogue_inputs_only_16_byte_aligned():
+    """The GELU MLP backward reads Y in its epilogue: a Y 16 bytes off a 32-byte boundary
+    gives the same gradients bit for bit."""
+    M, h, f, N = 512, 256, 512, 2
+    BF, A = T.DType.BF16, T.Act.GELU
+    X = tensor((M, h), 620)[1]
+    W1 = tensor((h, f), 621, 0.05)[1]
+    W2 = tensor((f, h), 622, 0.05)[1]
+    dZ = tensor((M, h), 623)[1]
+    e = lambda *s: torch.empty(s, dtype=torch.bfloat16, device="cuda")
+    Y, H, Z = e(M, f), e(M, f), e(M, h)
+    ws = torch.empty(max(T.tp_workspace_size(T.Op.MLP_FWD, M, h, f, N, BF, A, T.Reduce.SPLITK),
+                         T.tp_workspace_size(T.Op.MLP_BWD, M, h, f, N, BF, A, T.Reduce.SPLITK)),
+                     dtype=torch.uint8, device="cuda")
+    T.tp_mlp_fwd(X, W1, None, W2, None, Y, None, H, Z, M, h, f, N, BF, A, T.Reduce.SPLITK, ws,
+                 ws.numel())
+    buf = e(M * f + 16)
+    Y16 = buf[8:8 + M * f].view(M, f)
+    Y16.copy_(Y)
+    outs = []
+    for Yin in (Y, Y16):
+        dX, dW1, dW2 = e(M, h), e(h, f), e(f, h)
+        T.tp_mlp_bwd(X, W1, None, W2, Yin, None, H, dZ, dX, dW1, None, dW2, M, h, f, N, BF, A,
+                     T.Reduce.SPLITK, ws, ws.numel())
+        outs.append((dX, dW1, dW2))
+    torch.cuda.synchronize()
+    assert Y16.data_ptr() % 32 == 16
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
