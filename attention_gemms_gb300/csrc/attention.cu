@@ -27,6 +27,9 @@ namespace tp {
 namespace {
 
 constexpr int RB = 64;  // rows per CTA and per shared-memory block
+#ifndef TP_ATTN_TC
+#define TP_ATTN_TC 1  // bf16, head_dim 64: the tensor-core forward of attention_tc.cu
+#endif
 
 // Where query head t (0 <= t < H) and its key/value head sit in a qkv row.
 struct HeadMap {
@@ -415,6 +418,9 @@ tp_status launch_attention_fwd(const void* qkv, void* o, float* lse, int64_t b, 
   if (h > (1 << 20)) return fail(TP_ERR_SHAPE, "attention sizes out of range");
   const HeadMap m = mha_map(h, heads);
   const int d = static_cast<int>(h / heads), bi = static_cast<int>(b), si = static_cast<int>(s);
+  if (TP_ATTN_TC && attention_tc_eligible(dt, d, m.ldq, qkv, o, m.ldo))
+    return launch_attention_fwd_tc(qkv, o, lse, b, s, heads, m.hq, m.g, m.S, m.KO, m.VO, m.ldq,
+                                   m.ldo, causal, st);
   return dt == TP_BF16 ? fwd_d<__nv_bfloat16>(qkv, o, lse, bi, si, m, d, causal, st)
                        : fwd_d<float>(qkv, o, lse, bi, si, m, d, causal, st);
 }
@@ -439,6 +445,9 @@ tp_status launch_gqa_attention_fwd(const void* qkv, void* o, float* lse, int64_t
   TP_TRY(check_sizes(b, s, heads));
   const HeadMap m = gqa_map(heads, kv_heads, N, d);
   const int bi = static_cast<int>(b), si = static_cast<int>(s);
+  if (TP_ATTN_TC && attention_tc_eligible(dt, d, m.ldq, qkv, o, m.ldo))
+    return launch_attention_fwd_tc(qkv, o, lse, b, s, heads, m.hq, m.g, m.S, m.KO, m.VO, m.ldq,
+                                   m.ldo, causal, st);
   return dt == TP_BF16 ? fwd_d<__nv_bfloat16>(qkv, o, lse, bi, si, m, d, causal, st)
                        : fwd_d<float>(qkv, o, lse, bi, si, m, d, causal, st);
 }

@@ -1,0 +1,417 @@
+// Tensor-core attention forward, head_dim 64, bf16: O = softmax(Q K^T / sqrt(d)) V per
+// query head, with the head map of the CUDA-core kernels (multi-head layout or
+// grouped-query per-shard blocks). Same outputs: O (bf16) and lse (fp32, natural log).
+//
+// One CTA per (128 query rows, query head); keys in blocks of 128:
+//   warp 4 (one lane) loads Q once and K, V blocks into two stages with TMA straight
+//     from the qkv rows (128-byte swizzle, 64 columns = one head);
+//   warp 5 (one lane) owns TMEM (S: 128 columns, O: 64) and issues
+//     S = Q K^T (M 128, N 128, K 64) and O += P V (M 128, N 64, K 128);
+//   warps 0-3, one thread per query row, read S from TMEM, keep the running maximum
+//     and sum (base 2, online softmax), write P = 2^(s - m) as bf16 into shared memory
+//     in the swizzled K-major layout the MMA reads, and rescale O in TMEM when the
+//     maximum grows.
+// Ordering: P and the O rescale wait for the previous block's P V (o_done); the next
+// S is issued once the softmax warps have handed over P (p_full), i.e. after they have
+// read the current S; a K/V stage is refilled after its P V completes (kv_empty).
+// Every wait is bounded; on a timeout the CTA records TP_ERR_TIMEOUT, stops issuing,
+// waits (bounded) for its own copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+#include <string>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tp {
+namespace {
+
+constexpr int kQ = 128;                   // query rows per CTA = TMEM lanes
+constexpr int kKB = 128;                  // keys per block
+constexpr int kTile = 128 * 64 * 2;       // a 128 x 64 bf16 tile (Q, K or V): 16 KB
+constexpr int kOffQ = 0;
+constexpr int kOffKV = kTile;             // stage st: K at kOffKV + 2 st kTile, V after it
+constexpr int kOffP = 5 * kTile;          // P: 128 rows x 128 keys = two 64-key atoms
+constexpr int kOffBar = 7 * kTile;
+constexpr int kSmem = kOffBar + 16 * 8 + 16 + 1024;  // + alignment slack
+constexpr int kThreadsTC = 192;
+constexpr uint32_t kTmemCols = 256;       // S at 0, O at 128
+constexpr uint64_t kDrainNs = 20000000ull;
+
+struct AttnTcParams {
+  CUtensorMap tm;       // qkv: (b*s rows, ldq columns), box 64 x 128, 128-byte swizzle
+  void* o;              // (b*s, ldo) bf16
+  float* lse;           // (b, H, s)
+  int s, H, hq, g;      // sequence, query heads, query heads per block, per key/value head
+  int64_t S, KO, VO, ldo;
+  float scale_log2;     // log2(e) / sqrt(64)
+  int causal;
+  int* status;
+  uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ void record_timeout_attn(int* status) {
+  atomicCAS(status, 0, static_cast<int>(TP_ERR_TIMEOUT));
+  atomicAdd(status + 1, 1);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// generic-proxy shared-memory writes (P) made visible to the tensor cores' async proxy
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(kThreadsTC, 1) attn_fwd_tc_kernel(const __grid_constant__ AttnTcParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  const uint32_t q_full = bar0, s_full = bar0 + 8 * 5, p_full = bar0 + 8 * 6,
+                 o_done = bar0 + 8 * 7, drain = bar0 + 8 * 8;
+  auto kv_full = [&](int st) { return bar0 + 8u * (1 + st); };
+  auto kv_empty = [&](int st) { return bar0 + 8u * (3 + st); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.z, t = blockIdx.y, q0 = blockIdx.x * kQ;
+  const int blk = t / p.hq, tl = t - blk * p.hq;
+  const int qc = static_cast<int>(blk * p.S + static_cast<int64_t>(tl) * 64);
+  const int kc = static_cast<int>(blk * p.S + p.KO + static_cast<int64_t>(tl / p.g) * 64);
+  const int vc = static_cast<int>(blk * p.S + p.VO + static_cast<int64_t>(tl / p.g) * 64);
+  const int row0 = b * p.s;
+  const int kend = p.causal ? min(p.s, q0 + kQ) : p.s;
+  const int nkb = (kend + kKB - 1) / kKB;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int st = 0; st < 2; ++st) {
+      mbar_init(kv_full(st), 1);
+      mbar_init(kv_empty(st), 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 4);  // one arrive per softmax warp
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  const uint32_t tS = tmem, tO = tmem + 128;
+  int issued_kv = 0;  // producer: K/V blocks issued
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      bool ok = true;
+      mbar_arrive_expect_tx(q_full, kTile);
+      tma_load_2d(sb + kOffQ, &p.tm, q_full, qc, row0 + q0);
+      for (int j = 0; j < nkb; ++j) {
+        const int st = j & 1;
+        if (j >= 2 && !mbar_wait(kv_empty(st), ((j >> 1) - 1) & 1, p.timeout_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = sb + kOffKV + st * 2 * kTile;
+        mbar_arrive_expect_tx(kv_full(st), 2 * kTile);
+        tma_load_2d(dst, &p.tm, kv_full(st), kc, row0 + j * kKB);
+        tma_load_2d(dst + kTile, &p.tm, kv_full(st), vc, row0 + j * kKB);
+        ++issued_kv;
+      }
+      if (!ok) record_timeout_attn(p.status);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
+      const uint32_t id_o = idesc_bf16_f32(128, 64, 0, 1);   // P K-major, V MN-major
+      bool ok = mbar_wait(q_full, 0, p.timeout_ns, abort_flag);
+      auto issue_s = [&](int j) -> bool {
+        const int st = j & 1;
+        if (!mbar_wait(kv_full(st), (j >> 1) & 1, p.timeout_ns, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t kaddr = sb + kOffKV + st * 2 * kTile;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_ss(tS, sw128_desc(sb + kOffQ + kk * 32, 16u, 1024u),
+                      sw128_desc(kaddr + kk * 32, 16u, 1024u), id_s, kk > 0 ? 1u : 0u);
+        mma_commit(s_full);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; j < nkb && ok; ++j) {
+        if (!mbar_wait(p_full, j & 1, p.timeout_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int st = j & 1;
+        const uint32_t vaddr = sb + kOffKV + st * 2 * kTile + kTile;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ss(tO, sw128_desc(sb + kOffP + (kk >> 2) * kTile + (kk & 3) * 32, 16u, 1024u),
+                      sw128_desc(vaddr + kk * 2048, 8192u, 1024u), id_o,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(o_done);
+        mma_commit(kv_empty(st));
+        if (j + 1 < nkb) ok = issue_s(j + 1);
+      }
+      if (!ok) record_timeout_attn(p.status);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- softmax (warps 0-3)
+    const int r = threadIdx.x;  // query row within the tile = TMEM lane
+    const int qi = q0 + r;
+    const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;
+    float m2 = -INFINITY, l = 0.0f;
+    bool ok = true;
+    auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+      int w = 1;
+      if (lane == 0) w = mbar_wait(bar, parity, p.timeout_ns, abort_flag) ? 1 : 0;
+      return __shfl_sync(0xFFFFFFFFu, w, 0) != 0;
+    };
+    for (int j = 0; j < nkb; ++j) {
+      if (!wait_all(s_full, j & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int k0 = j * kKB;
+      // pass 1: the block's row maximum (masked keys: beyond the sequence, or after the query)
+      float mb = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tS + lanes + c * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int key = k0 + c * 32 + i;
+          const bool live = key < p.s && !(p.causal && key > qi);
+          if (live) mb = fmaxf(mb, __uint_as_float(v[i]) * p.scale_log2);
+        }
+      }
+      const float m_new = fmaxf(m2, mb);
+      const float m_use = m_new == -INFINITY ? 0.0f : m_new;
+      const float corr = exp2f(m2 - m_use);  // 0 on the first block
+      // P may be overwritten and O rescaled once the previous block's P V is complete
+      if (j > 0 && !wait_all(o_done, (j - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // pass 2: P = 2^(s - m) as bf16 into the swizzled K-major P tile
+      float sum = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tS + lanes + c * 32, v);
+        tmem_ld_wait();
+        float pv[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int key = k0 + c * 32 + i;
+          const bool live = key < p.s && !(p.causal && key > qi);
+          pv[i] = live ? exp2f(__uint_as_float(v[i]) * p.scale_log2 - m_use) : 0.0f;
+          sum += pv[i];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {  // 8 keys = 16 bytes per store
+          const int chunk = c * 4 + u;  // 16-byte chunk of the 256-byte row
+          const int atom = chunk >> 3, ch = chunk & 7;
+          const uint32_t addr = sb + kOffP + atom * kTile + (r >> 3) * 1024 + (r & 7) * 128 +
+                                ((ch ^ (r & 7)) << 4);
+          const float* q8 = pv + 8 * u;
+          st_shared_v4(addr, pack_bf16x2(q8[0], q8[1]), pack_bf16x2(q8[2], q8[3]),
+                       pack_bf16x2(q8[4], q8[5]), pack_bf16x2(q8[6], q8[7]));
+        }
+      }
+      l = l * corr + sum;
+      m2 = m_new;
+      if (j > 0) {  // O *= corr (the new maximum rebases the running output)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tO + lanes + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
+          tmem_st32(tO + lanes + c * 32, v);
+        }
+        tmem_st_wait();
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    if (ok && wait_all(o_done, (nkb - 1) & 1)) {
+      tc_fence_after();
+      const float inv = 1.0f / l;
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) +
+                            (static_cast<int64_t>(row0) + qi) * p.ldo + static_cast<int64_t>(t) * 64;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tO + lanes + c * 32, v);
+        tmem_ld_wait();
+        if (qi < p.s) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(v[8 * u]) * inv, __uint_as_float(v[8 * u + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]) * inv, __uint_as_float(v[8 * u + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]) * inv, __uint_as_float(v[8 * u + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]) * inv, __uint_as_float(v[8 * u + 7]) * inv);
+            reinterpret_cast<uint4*>(orow + c * 32)[u] = w;
+          }
+        }
+      }
+      if (qi < p.s)
+        p.lse[(static_cast<int64_t>(b) * p.H + t) * p.s + qi] = (m2 + log2f(l)) * 0.6931471805599453f;
+    } else if (lane == 0) {
+      record_timeout_attn(p.status);
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  __syncthreads();
+  if (*abort_flag) {
+    volatile int no_abort = 0;
+    if (warp == 4 && lane == 0) {  // the copies this CTA issued have landed
+      mbar_wait(q_full, 0, kDrainNs, &no_abort);
+      for (int st = 0; st < 2; ++st) {
+        const int n = issued_kv > st ? (issued_kv - 1 - st) / 2 : -1;  // last block on stage st
+        if (n >= 0) mbar_wait(kv_full(st), n & 1, kDrainNs, &no_abort);
+      }
+    }
+    if (warp == 5 && lane == 0) {  // and the MMAs it issued have completed
+      mma_commit(drain);
+      mbar_wait(drain, 0, kDrainNs, &no_abort);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                             const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                             CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                             CUtensorMapFloatOOBfill);
+
+EncodeFn encoder() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(f);
+  });
+  return fn;
+}
+
+}  // namespace
+
+// Whether the tensor-core forward takes this problem: bf16, head_dim 64, and a qkv
+// row pitch TMA can address.
+bool attention_tc_eligible(tp_dtype dt, int d, int64_t ldq, const void* qkv, const void* o,
+                           int64_t ldo) {
+  return dt == TP_BF16 && d == 64 && (ldq * 2) % 16 == 0 &&
+         reinterpret_cast<uintptr_t>(qkv) % 16 == 0 && reinterpret_cast<uintptr_t>(o) % 16 == 0 &&
+         (ldo * 2) % 16 == 0;
+}
+
+tp_status launch_attention_fwd_tc(const void* qkv, void* o, float* lse, int64_t b, int64_t s,
+                                  int heads, int hq, int g, int64_t S, int64_t KO, int64_t VO,
+                                  int64_t ldq, int64_t ldo, int causal, cudaStream_t st) {
+  if (b <= 0 || s <= 0) return TP_OK;
+  if (b * s > 2147483647ll || ldq > 2147483647ll) return fail(TP_ERR_SHAPE, "attention too large");
+  EncodeFn enc = encoder();
+  if (!enc) return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
+  AttnTcParams p{};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(ldq), static_cast<cuuint64_t>(b * s)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldq) * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(&p.tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(qkv), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled failed (code " + std::to_string(r) + ")");
+  p.o = o;
+  p.lse = lse;
+  p.s = static_cast<int>(s);
+  p.H = heads;
+  p.hq = hq;
+  p.g = g;
+  p.S = S;
+  p.KO = KO;
+  p.VO = VO;
+  p.ldo = ldo;
+  p.scale_log2 = 1.4426950408889634f / 8.0f;  // log2(e) / sqrt(64)
+  p.causal = causal;
+  p.status = device_status_word();
+  if (!p.status) return fail(TP_ERR_CUDA, "device status word unavailable");
+  p.timeout_ns = wait_timeout_ns();
+  static std::atomic<uint64_t> attr_set{0};
+  if (needs_setup(attr_set)) {
+    TP_CUDA_TRY(cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmem));
+    mark_device(attr_set);
+  }
+  const dim3 grid(static_cast<unsigned>((s + kQ - 1) / kQ), static_cast<unsigned>(heads),
+                  static_cast<unsigned>(b));
+  attn_fwd_tc_kernel<<<grid, kThreadsTC, kSmem, st>>>(p);
+  count_launch();
+  TP_CUDA_TRY(cudaGetLastError());
+  return TP_OK;
+}
+
+}  // namespace tp

@@ -148,6 +148,12 @@ tp_status launch_attention_bwd(const void* qkv, const void* o, const float* lse,
 tp_status launch_gqa_attention_fwd(const void* qkv, void* o, float* lse, int64_t b, int64_t s,
                                    int heads, int kv_heads, int N, int d, int causal, tp_dtype dt,
                                    cudaStream_t st);
+// tensor-core forward (attention_tc.cu): bf16, head_dim 64
+bool attention_tc_eligible(tp_dtype dt, int d, int64_t ldq, const void* qkv, const void* o,
+                           int64_t ldo);
+tp_status launch_attention_fwd_tc(const void* qkv, void* o, float* lse, int64_t b, int64_t s,
+                                  int heads, int hq, int g, int64_t S, int64_t KO, int64_t VO,
+                                  int64_t ldq, int64_t ldo, int causal, cudaStream_t st);
 tp_status launch_gqa_attention_bwd(const void* qkv, const void* o, const float* lse,
                                    const void* dO, void* dqkv, int64_t b, int64_t s, int heads,
                                    int kv_heads, int N, int d, int causal, tp_dtype dt,

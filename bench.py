@@ -764,9 +764,6 @@ def gpt_cpu_baseline(w, p, ids, tg, steps=3):
                       f"{steps} steps, {dt * 1e3:.0f} ms each"}
 
 
-FP32_ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # SMs x FP32 lanes x FMA x max clock
-
-
 def gqa_flops(w):
     """Algorithmic FLOPs of the GQA block forward + backward, counted on the unsharded
     model (replicated key/value projections are redundant work, not counted):
@@ -860,6 +857,8 @@ def run_gqa(args, w, T, device, rank, nranks):
     attn_max = max_over_ranks(attn_ms, device)
     total, attn_fwd = gqa_flops(w)
     attn_tf = attn_fwd / (attn_max * 1e-3) / 1e12
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     res = {
         "metric": "head-sharded GQA attention block fwd+bwd TFLOP/s",
         "value": round(total * nranks / (ms_max * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
@@ -872,11 +871,11 @@ def run_gqa(args, w, T, device, rank, nranks):
                    "qkv_columns_unreplicated": (H + 2 * Hkv) * d, "shard_sum": args.mode,
                    "parallelism": f"tp{N} virtual ranks per GPU, dp{nranks}",
                    "l2": "activations larger than L2 (no flush)"},
-        "roofline": {"bound": "alu", "kernel": "attn_fwd_kernel (per-head softmax attention, "
-                     "CUDA cores, fp32 arithmetic), timed on its own", "achieved": round(attn_tf, 2),
-                     "peak": round(FP32_ALU_PEAK_TFLOPS, 1), "unit": "TFLOP/s",
-                     "frac": round(attn_tf / FP32_ALU_PEAK_TFLOPS, 4),
-                     "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 (FMA) x 2.07 GHz",
+        "roofline": {"bound": "tensor", "kernel": "attn_fwd_tc_kernel (tcgen05 attention forward: "
+                     "S = Q K^T and O += P V in TMEM, online softmax), timed on its own",
+                     "achieved": round(attn_tf, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(attn_tf / peak, 4),
+                     "peak_source": f"{src} bf16 dense (burst)",
                      "traffic": None, "algorithmic_flops_per_launch": attn_fwd,
                      "avg_launch_ms": round(attn_max, 4)},
         "e2e": {"value": round(total * nranks / (e2e_max * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
