@@ -2,11 +2,13 @@
 // query head, with the head map of the CUDA-core kernels (multi-head layout or
 // grouped-query per-shard blocks). Same outputs: O (bf16) and lse (fp32, natural log).
 //
-// One CTA per (128 query rows, query head); keys in blocks of 128:
+// One CTA per (128 query rows, query head); keys in blocks of 64 (about 66 KB of shared
+// memory and 64 + 64 TMEM columns a CTA, so two CTAs share an SM and one CTA's softmax
+// overlaps the other's MMAs; 128-key blocks with one CTA per SM took 1.5x longer):
 //   warp 4 (one lane) loads Q once and K, V blocks into two stages with TMA straight
 //     from the qkv rows (128-byte swizzle, 64 columns = one head);
-//   warp 5 (one lane) owns TMEM (S: 128 columns, O: 64) and issues
-//     S = Q K^T (M 128, N 128, K 64) and O += P V (M 128, N 64, K 128);
+//   warp 5 (one lane) owns TMEM (S: 64 columns, O: 64) and issues
+//     S = Q K^T (M 128, N 64, K 64) and O += P V (M 128, N 64, K 64);
 //   warps 0-3, one thread per query row, read S from TMEM, keep the running maximum
 //     and sum (base 2, online softmax), write P = 2^(s - m) as bf16 into shared memory
 //     in the swizzled K-major layout the MMA reads, and rescale O in TMEM when the
@@ -31,19 +33,25 @@ namespace tp {
 namespace {
 
 constexpr int kQ = 128;                   // query rows per CTA = TMEM lanes
-constexpr int kKB = 128;                  // keys per block
-constexpr int kTile = 128 * 64 * 2;       // a 128 x 64 bf16 tile (Q, K or V): 16 KB
+constexpr int kKB = 64;                   // keys per block
+constexpr int kQTile = kQ * 64 * 2;       // Q: 128 rows x 64 dims, bf16: 16 KB
+constexpr int kKVTile = kKB * 64 * 2;     // a K or V block: 64 keys x 64 dims: 8 KB
 constexpr int kOffQ = 0;
-constexpr int kOffKV = kTile;             // stage st: K at kOffKV + 2 st kTile, V after it
-constexpr int kOffP = 5 * kTile;          // P: 128 rows x 128 keys = two 64-key atoms
-constexpr int kOffBar = 7 * kTile;
+constexpr int kOffKV = kQTile;            // stage st: K at kOffKV + 2 st kKVTile, V after it
+constexpr int kOffP = kOffKV + 4 * kKVTile;  // P: 128 rows x 64 keys (one swizzle atom)
+constexpr int kOffBar = kOffP + kQ * kKB * 2;
 constexpr int kSmem = kOffBar + 16 * 8 + 16 + 1024;  // + alignment slack
 constexpr int kThreadsTC = 192;
-constexpr uint32_t kTmemCols = 256;       // S at 0, O at 128
+#ifndef TP_ATTN_CTAS
+#define TP_ATTN_CTAS 2  // CTAs per SM the register allocation must allow (3 spills)
+#endif
+constexpr int kCtasPerSm = TP_ATTN_CTAS;
+constexpr uint32_t kTmemCols = 128;       // S at 0 (64 columns), O at 64
 constexpr uint64_t kDrainNs = 20000000ull;
 
 struct AttnTcParams {
-  CUtensorMap tm;       // qkv: (b*s rows, ldq columns), box 64 x 128, 128-byte swizzle
+  CUtensorMap tm;       // qkv: (b*s rows, ldq columns), box 64 x 128, 128-byte swizzle (Q)
+  CUtensorMap tmkv;     // the same tensor, box 64 x 64 (K, V blocks)
   void* o;              // (b*s, ldo) bf16
   float* lse;           // (b, H, s)
   int s, H, hq, g;      // sequence, query heads, query heads per block, per key/value head
@@ -89,7 +97,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__global__ void __launch_bounds__(kThreadsTC, 1) attn_fwd_tc_kernel(const __grid_constant__ AttnTcParams p) {
+__global__ void __launch_bounds__(kThreadsTC, kCtasPerSm) attn_fwd_tc_kernel(const __grid_constant__ AttnTcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -134,14 +142,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_fwd_tc_kernel(const __grid
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-  const uint32_t tS = tmem, tO = tmem + 128;
+  const uint32_t tS = tmem, tO = tmem + kKB;
   int issued_kv = 0;  // producer: K/V blocks issued
 
   if (warp == 4) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       bool ok = true;
-      mbar_arrive_expect_tx(q_full, kTile);
+      mbar_arrive_expect_tx(q_full, kQTile);
       tma_load_2d(sb + kOffQ, &p.tm, q_full, qc, row0 + q0);
       for (int j = 0; j < nkb; ++j) {
         const int st = j & 1;
@@ -149,10 +157,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_fwd_tc_kernel(const __grid
           ok = false;
           break;
         }
-        const uint32_t dst = sb + kOffKV + st * 2 * kTile;
-        mbar_arrive_expect_tx(kv_full(st), 2 * kTile);
-        tma_load_2d(dst, &p.tm, kv_full(st), kc, row0 + j * kKB);
-        tma_load_2d(dst + kTile, &p.tm, kv_full(st), vc, row0 + j * kKB);
+        const uint32_t dst = sb + kOffKV + st * 2 * kKVTile;
+        mbar_arrive_expect_tx(kv_full(st), 2 * kKVTile);
+        tma_load_2d(dst, &p.tmkv, kv_full(st), kc, row0 + j * kKB);
+        tma_load_2d(dst + kKVTile, &p.tmkv, kv_full(st), vc, row0 + j * kKB);
         ++issued_kv;
       }
       if (!ok) record_timeout_attn(p.status);
@@ -161,14 +169,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_fwd_tc_kernel(const __grid
   } else if (warp == 5) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t id_s = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
+      const uint32_t id_s = idesc_bf16_f32(128, kKB, 0, 0);  // Q, K both K-major
       const uint32_t id_o = idesc_bf16_f32(128, 64, 0, 1);   // P K-major, V MN-major
       bool ok = mbar_wait(q_full, 0, p.timeout_ns, abort_flag);
       auto issue_s = [&](int j) -> bool {
         const int st = j & 1;
         if (!mbar_wait(kv_full(st), (j >> 1) & 1, p.timeout_ns, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t kaddr = sb + kOffKV + st * 2 * kTile;
+        const uint32_t kaddr = sb + kOffKV + st * 2 * kKVTile;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_bf16_ss(tS, sw128_desc(sb + kOffQ + kk * 32, 16u, 1024u),
@@ -184,10 +192,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_fwd_tc_kernel(const __grid
         }
         tc_fence_after();
         const int st = j & 1;
-        const uint32_t vaddr = sb + kOffKV + st * 2 * kTile + kTile;
+        const uint32_t vaddr = sb + kOffKV + st * 2 * kKVTile + kKVTile;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ss(tO, sw128_desc(sb + kOffP + (kk >> 2) * kTile + (kk & 3) * 32, 16u, 1024u),
+        for (int kk = 0; kk < kKB / 16; ++kk)
+          mma_bf16_ss(tO, sw128_desc(sb + kOffP + kk * 32, 16u, 1024u),
                       sw128_desc(vaddr + kk * 2048, 8192u, 1024u), id_o,
                       (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(o_done);
@@ -219,7 +227,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_fwd_tc_kernel(const __grid
       // pass 1: the block's row maximum (masked keys: beyond the sequence, or after the query)
       float mb = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < kKB / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(tS + lanes + c * 32, v);
         tmem_ld_wait();
@@ -239,30 +247,31 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_fwd_tc_kernel(const __grid
         break;
       }
       tc_fence_after();
-      // pass 2: P = 2^(s - m) as bf16 into the swizzled K-major P tile
+      // pass 2: P = 2^(s - m) as bf16 into the swizzled K-major P tile (128-byte rows)
       float sum = 0.0f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < kKB / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(tS + lanes + c * 32, v);
         tmem_ld_wait();
-        float pv[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int key = k0 + c * 32 + i;
           const bool live = key < p.s && !(p.causal && key > qi);
-          pv[i] = live ? exp2f(__uint_as_float(v[i]) * p.scale_log2 - m_use) : 0.0f;
-          sum += pv[i];
+          const float e = live ? exp2f(__uint_as_float(v[i]) * p.scale_log2 - m_use) : 0.0f;
+          sum += e;
+          v[i] = __float_as_uint(e);
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {  // 8 keys = 16 bytes per store
-          const int chunk = c * 4 + u;  // 16-byte chunk of the 256-byte row
-          const int atom = chunk >> 3, ch = chunk & 7;
-          const uint32_t addr = sb + kOffP + atom * kTile + (r >> 3) * 1024 + (r & 7) * 128 +
-                                ((ch ^ (r & 7)) << 4);
-          const float* q8 = pv + 8 * u;
-          st_shared_v4(addr, pack_bf16x2(q8[0], q8[1]), pack_bf16x2(q8[2], q8[3]),
-                       pack_bf16x2(q8[4], q8[5]), pack_bf16x2(q8[6], q8[7]));
+          const int ch = c * 4 + u;    // 16-byte chunk of the 128-byte row
+          const uint32_t addr = sb + kOffP + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4);
+          const uint32_t* q8 = v + 8 * u;
+          st_shared_v4(addr,
+                       pack_bf16x2(__uint_as_float(q8[0]), __uint_as_float(q8[1])),
+                       pack_bf16x2(__uint_as_float(q8[2]), __uint_as_float(q8[3])),
+                       pack_bf16x2(__uint_as_float(q8[4]), __uint_as_float(q8[5])),
+                       pack_bf16x2(__uint_as_float(q8[6]), __uint_as_float(q8[7])));
         }
       }
       l = l * corr + sum;
@@ -377,14 +386,16 @@ tp_status launch_attention_fwd_tc(const void* qkv, void* o, float* lse, int64_t 
   AttnTcParams p{};
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(ldq), static_cast<cuuint64_t>(b * s)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldq) * 2};
-  const cuuint32_t box[2] = {64, 128};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(&p.tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(qkv), dims,
-                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS)
-    return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled failed (code " + std::to_string(r) + ")");
+  for (int m = 0; m < 2; ++m) {
+    const cuuint32_t box[2] = {64, m == 0 ? static_cast<cuuint32_t>(kQ) : static_cast<cuuint32_t>(kKB)};
+    const CUresult r = enc(m == 0 ? &p.tm : &p.tmkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                           const_cast<void*>(qkv), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled failed (code " + std::to_string(r) + ")");
+  }
   p.o = o;
   p.lse = lse;
   p.s = static_cast<int>(s);
