@@ -90,8 +90,8 @@ def col_gemm_flops(w):
 # from an ncu capture of the full-size workload, valid only for the kernel source it
 # was taken on (sha256 of csrc/gemm_tc.cu + csrc/ptx.cuh); see profiles/.
 COL_GEMM_TRAFFIC = {
-    "c5": {"bytes": 11.27e9 + 1.40e9, "src": "3953fcc74a8f52f6"},
-    "c3": {"bytes": 1.10e9 + 508.24e6, "src": "3953fcc74a8f52f6"},
+    "c5": {"bytes": 12.08e9 + 1.40e9, "src": "1c417b636733cb5a"},
+    "c3": {"bytes": 1.10e9 + 509.49e6, "src": "1c417b636733cb5a"},
 }
 
 
