@@ -1258,7 +1258,23 @@ def run_reference(args, w):
     c = w["cfg"]
     dtp = w.get("dtype", "bf16")
     metric, unit, scale = METRIC, "TFLOP/s", 1e12
-    if w.get("gpt"):
+    if w.get("gqa"):
+        from oracle import gqa_oracle as Q
+        H, Hkv, N, d = w["heads"], w["kv_heads"], w["N"], h // w["heads"]
+        sig = 1.0 / math.sqrt(h)
+        nrm = lambda shape, name, sg: synth.to_f64(synth.normal(shape, synth.seed_of(c, name), sg,
+                                                                "bf16"), "bf16")
+        x, dout = nrm((w["s"], h), "X", 1.0), nrm((w["s"], h), "dZ", 1.0)  # one sequence
+        Wsh = Q.gqa_pack(nrm((h, H * d), "Wqkv", sig), nrm((h, Hkv * d), "Wg", sig),
+                         nrm((h, Hkv * d), "Wu", sig), H, Hkv, N)
+        Wo = nrm((h, h), "Wo", sig)
+        g1, b1 = np.ones(h), np.zeros(h)
+        run = lambda: Q.gqa_block_bwd(x, 1, w["s"], g1, b1, Wsh, Wo, H, Hkv, N, dout)
+        flops = gqa_flops(dict(w, b=1))[0]
+        metric = "head-sharded GQA attention block fwd+bwd TFLOP/s"
+        sample = (f"fp64 oracle GQA block forward+backward on 1 of {w['b']} sequences "
+                  f"(s={w['s']}); FLOPs of that sequence")
+    elif w.get("gpt"):
         from oracle import gpt_oracle as G
         pr, ids, tg = synth.gpt_inputs(c, w["vocab"], h, f, w["layers"], w["b"], w["s"])
         f64 = {k: np.asarray(a, np.float64) for k, a in pr.items()}
@@ -1320,6 +1336,74 @@ def run_reference(args, w):
     }), flush=True)
 
 
+def _ref_line(args, metric, val, unit, dt, dc, sample, config, t_gen):
+    ws_, _, _ = dist_env()
+    print(json.dumps({
+        "metric": metric, "value": round(val, 6), "unit": unit, "n_gpus": ws_,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "impl": "reference", "config": config,
+        "cpu_baseline": {"value": round(val, 6), "unit": unit, "kind": "oracle",
+                         "cores": len(os.sched_getaffinity(0)),
+                         "threads_effective": round(dc / dt, 1), "sample": sample},
+        "e2e": {"value": round(val, 6), "unit": unit, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "input_gen_s": round(t_gen, 1)}), flush=True)
+
+
+def _time_ref(args, run):
+    for _ in range(args.warmup):
+        run()
+    c0, t0 = time.process_time(), time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    return (time.perf_counter() - t0) / args.steps, (time.process_time() - c0) / args.steps
+
+
+def run_reference_hbm(args):
+    """Oracle arms of the HBM-bound lines, each on a bounded sample (rank 0 only):
+    c4 -- the fp64 SwiGLU decode forward of one token on one shard's slice of the
+    weights (1/8 of them); vocab-ce -- the vocabulary-parallel cross-entropy forward +
+    backward on 32 of the 8192 rows. GB/s of the bf16 bytes the GPU line counts, scaled
+    to the sample."""
+    _, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from attention_gemms_gb300 import synth
+    t_gen = time.time()
+    if args.workload == "c4":
+        from oracle import tp_oracle as O
+        h, f, N = DECODE["h"], DECODE["f"], DECODE["N"]
+        fs = f // N
+        c = DECODE["cfg"]
+        x = synth.to_f64(synth.normal((1, h), synth.seed_of(c, "X"), 1.0, "bf16"), "bf16")
+        Wg = synth.to_f64(synth.normal((h, fs), synth.seed_of(c, "Wg"), 0.02, "bf16"), "bf16")
+        Wu = synth.to_f64(synth.normal((h, fs), synth.seed_of(c, "Wu"), 0.02, "bf16"), "bf16")
+        Wd = synth.to_f64(synth.normal((fs, h), synth.seed_of(c, "Wd"), 0.02, "bf16"), "bf16")
+        run = lambda: O.mlp_swiglu_fwd(x, Wg, Wu, Wd, 1)
+        nbytes = 3 * h * fs * 2
+        metric = "decode GEMV HBM GB/s"
+        sample = (f"fp64 oracle SwiGLU forward of 1 token on one shard's slice ({fs} of {f} "
+                  f"columns) of the weights; bytes = that slice in bf16")
+        config = {"workload": DECODE["desc"], "tokens": 1}
+    else:
+        from oracle import gpt_oracle as G
+        rows, v, N = 32, 50304, 8
+        L = synth.to_f64(synth.normal((rows, v), 9001, 2.0, "bf16"), "bf16")
+        tg = synth.integers((rows,), 9002, v)
+
+        def run():
+            _, lse, _, _ = G.vocab_ce_fwd(L, tg, N)
+            G.vocab_ce_bwd(L, tg, lse, N, 1.0 / rows)
+        nbytes = 3 * rows * v * 2
+        metric = "vocabulary-parallel cross-entropy fwd+bwd GB/s"
+        sample = f"fp64 oracle cross-entropy forward + backward on {rows} of 8192 rows (v={v}, N={N})"
+        config = {"workload": "vocab-ce", "M": 8192, "vocab": v, "N": N}
+    t_gen = time.time() - t_gen
+    dt, dc = _time_ref(args, run)
+    _ref_line(args, metric, nbytes / dt / 1e9, "GB/s", dt, dc, sample, config, t_gen)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1346,6 +1430,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference" and args.workload in ("c4", "vocab-ce"):
+        return run_reference_hbm(args)
     if args.workload == "c4":
         return run_decode_only(args)
     if args.workload == "vocab-ce":
