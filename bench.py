@@ -1177,11 +1177,6 @@ def run_decode_only(args):
     from attention_gemms_gb300 import build as B
     from attention_gemms_gb300 import tpmlp as T
     ws_, rank, local = dist_env()
-    if args.impl == "reference":
-        if rank == 0:
-            print(json.dumps({"impl": "reference", "unavailable": "the decode sweep has no CPU "
-                              "arm of its own; time --workload c5/c3 for the oracle"}))
-        return
     if ws_ > 1:
         torch.cuda.set_device(local)
     dist_init("nccl")
@@ -1382,7 +1377,7 @@ def run_reference_hbm(args):
         Wd = synth.to_f64(synth.normal((fs, h), synth.seed_of(c, "Wd"), 0.02, "bf16"), "bf16")
         run = lambda: O.mlp_swiglu_fwd(x, Wg, Wu, Wd, 1)
         nbytes = 3 * h * fs * 2
-        metric = "decode GEMV HBM GB/s"
+        metric = METRIC  # the decode line's metric (its value is GB/s)
         sample = (f"fp64 oracle SwiGLU forward of 1 token on one shard's slice ({fs} of {f} "
                   f"columns) of the weights; bytes = that slice in bf16")
         config = {"workload": DECODE["desc"], "tokens": 1}
