@@ -25,10 +25,13 @@ tp_status check_attn_shape(int64_t b, int64_t s, int64_t h, int32_t heads, int32
 
 size_t a256(size_t x) { return align_up(x, 256); }
 
+// dO | dQKV | dxn | shard partials | LN scratch | attention (lse, D) pairs: 8 bytes per
+// (row, head), at most h / 16 heads (head_dim >= 16)
 size_t attn_bwd_ws(int64_t M, int64_t h, int32_t N, tp_dtype dt, tp_reduce mode) {
   const size_t e = elem_size(dt);
   return a256(M * h * e) + a256(M * 3 * h * e) + a256(M * h * e) +
-         a256(partial_bytes(M, h, N, mode)) + a256(layernorm_bwd_ws_bytes(M, h));
+         a256(partial_bytes(M, h, N, mode)) + a256(layernorm_bwd_ws_bytes(M, h)) +
+         a256(attention_bwd_tc_ws_bytes(M, 1, static_cast<int>(h / 16)));
 }
 
 // QKV = xn W_qkv (all shards' columns; shard i owns its heads' columns of W_q, W_k, W_v)
@@ -175,6 +178,8 @@ tp_status tp_attn_proj_bwd(const void* x, const float* gamma, const void* Wqkv, 
   void* parts = w;
   w += a256(partial_bytes(M, h, N, mode));
   void* lnws = w;
+  w += a256(layernorm_bwd_ws_bytes(M, h));
+  void* ldws = w;
 
   // dWo_i = O_i^T dout (row-parallel weight gradient; row block i of W_o)
   {
@@ -212,7 +217,7 @@ tp_status tp_attn_proj_bwd(const void* x, const float* gamma, const void* Wqkv, 
     d.shard_axis = 1;
     TP_TRY(launch_gemm(d, st));
   }
-  TP_TRY(launch_attention_bwd(qkv, o, lse, dO, dqkv, b, s, h, n_heads, causal, dtype, st));
+  TP_TRY(launch_attention_bwd(qkv, o, lse, dO, dqkv, ldws, b, s, h, n_heads, causal, dtype, st));
   // dW_qkv = xn^T dQKV (column-parallel weight gradient)
   {
     GemmDesc d;

@@ -107,7 +107,8 @@ size_t fwd_ws(int64_t M, int64_t h, int32_t N, tp_reduce mode) { return partial_
 size_t bwd_ws(int64_t M, int64_t h, const Gqa& g, int32_t N, tp_dtype dt, tp_reduce mode) {
   const size_t e = elem_size(dt);
   return a256(M * h * e) + a256(M * g.W * e) + a256(M * h * e) +
-         a256(partial_bytes(M, h, N, mode)) + a256(layernorm_bwd_ws_bytes(M, h));
+         a256(partial_bytes(M, h, N, mode)) + a256(layernorm_bwd_ws_bytes(M, h)) +
+         a256(attention_bwd_tc_ws_bytes(M, 1, static_cast<int>(h / g.d)));
 }
 
 }  // namespace
@@ -172,19 +173,30 @@ tp_status tp_gqa_attention_fwd(const void* qkv, void* o, float* lse, int64_t b, 
                                   static_cast<cudaStream_t>(stream));
 }
 
+size_t tp_gqa_attention_bwd_workspace_size(int64_t b, int64_t s, int32_t n_heads) {
+  if (b < 0 || s < 0 || n_heads < 1) return 0;
+  return std::max<size_t>(attention_bwd_tc_ws_bytes(b, s, n_heads), 256);
+}
+
 tp_status tp_gqa_attention_bwd(const void* qkv, const void* o, const float* lse, const void* dO,
                                void* dqkv, int64_t b, int64_t s, int64_t h, int32_t n_heads,
                                int32_t n_kv_heads, int32_t N, int causal, tp_dtype dtype,
-                               void* stream) {
+                               void* ws, size_t ws_bytes, void* stream) {
   TP_TRY(check_dtype(dtype));
   TP_TRY(need(qkv && o && lse && dO && dqkv, TP_ERR_INVALID_ARG,
               "qkv, o, lse, dO and dqkv are required"));
   TP_TRY(need(b >= 0 && s >= 0, TP_ERR_INVALID_ARG, "need b, s >= 0"));
   Gqa g;
   TP_TRY(gqa_shape(h, n_heads, n_kv_heads, N, TP_F32, &g));
+  if (ws) {
+    TP_TRY(need(ws_bytes >= tp_gqa_attention_bwd_workspace_size(b, s, n_heads), TP_ERR_WORKSPACE,
+                "workspace smaller than tp_gqa_attention_bwd_workspace_size"));
+    TP_TRY(need(reinterpret_cast<uintptr_t>(ws) % 16 == 0, TP_ERR_ALIGNMENT,
+                "workspace must be 16-byte aligned"));
+  }
   if (b * s == 0) return TP_OK;
   TP_TRY(check_device());
-  return launch_gqa_attention_bwd(qkv, o, lse, dO, dqkv, b, s, n_heads, n_kv_heads, N,
+  return launch_gqa_attention_bwd(qkv, o, lse, dO, dqkv, ws, b, s, n_heads, n_kv_heads, N,
                                   static_cast<int>(g.d), causal, dtype,
                                   static_cast<cudaStream_t>(stream));
 }
@@ -270,6 +282,8 @@ tp_status tp_gqa_attn_proj_bwd(const void* x, const float* gamma, const void* Wq
   void* parts = w;
   w += a256(partial_bytes(M, h, N, mode));
   void* lnws = w;
+  w += a256(layernorm_bwd_ws_bytes(M, h));
+  void* ldws = w;  // attention (lse, D) pairs
   {  // dW_o,i = O_i^T dout
     GemmDesc d;
     d.dtype = dtype;
@@ -304,7 +318,7 @@ tp_status tp_gqa_attn_proj_bwd(const void* x, const float* gamma, const void* Wq
     d.shard_axis = 1;
     TP_TRY(launch_gemm(d, st));
   }
-  TP_TRY(launch_gqa_attention_bwd(qkv, o, lse, dO, dqkv, b, s, n_heads, n_kv_heads, N,
+  TP_TRY(launch_gqa_attention_bwd(qkv, o, lse, dO, dqkv, ldws, b, s, n_heads, n_kv_heads, N,
                                   static_cast<int>(g.d), causal, dtype, st));
   {  // dWqkv = xn^T dQKV (each block: its shard's gradient, replicas' partial K/V)
     GemmDesc d;

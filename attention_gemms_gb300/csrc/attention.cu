@@ -28,7 +28,7 @@ namespace {
 
 constexpr int RB = 64;  // rows per CTA and per shared-memory block
 #ifndef TP_ATTN_TC
-#define TP_ATTN_TC 1  // bf16, head_dim 64: the tensor-core forward of attention_tc.cu
+#define TP_ATTN_TC 1  // bf16, head_dim 64: the tensor-core kernels of attention_tc.cu
 #endif
 
 // Where query head t (0 <= t < H) and its key/value head sit in a qkv row.
@@ -426,13 +426,16 @@ tp_status launch_attention_fwd(const void* qkv, void* o, float* lse, int64_t b, 
 }
 
 tp_status launch_attention_bwd(const void* qkv, const void* o, const float* lse, const void* dO,
-                               void* dqkv, int64_t b, int64_t s, int64_t h, int heads, int causal,
-                               tp_dtype dt, cudaStream_t st) {
+                               void* dqkv, void* ldws, int64_t b, int64_t s, int64_t h, int heads,
+                               int causal, tp_dtype dt, cudaStream_t st) {
   if (b <= 0 || s <= 0) return TP_OK;
   TP_TRY(check_sizes(b, s, heads));
   if (h > (1 << 20)) return fail(TP_ERR_SHAPE, "attention sizes out of range");
   const HeadMap m = mha_map(h, heads);
   const int d = static_cast<int>(h / heads), bi = static_cast<int>(b), si = static_cast<int>(s);
+  if (TP_ATTN_TC && ldws && attention_bwd_tc_eligible(dt, d, m.ldq, qkv, o, dO, dqkv, m.ldo))
+    return launch_attention_bwd_tc(qkv, o, lse, dO, dqkv, ldws, b, s, heads, m.hq, m.g, m.hkv,
+                                   heads, m.S, m.KO, m.VO, m.ldq, m.ldo, causal, st);
   return dt == TP_BF16
              ? bwd_d<__nv_bfloat16>(qkv, o, lse, dO, dqkv, bi, si, m, heads, d, causal, st)
              : bwd_d<float>(qkv, o, lse, dO, dqkv, bi, si, m, heads, d, causal, st);
@@ -453,13 +456,16 @@ tp_status launch_gqa_attention_fwd(const void* qkv, void* o, float* lse, int64_t
 }
 
 tp_status launch_gqa_attention_bwd(const void* qkv, const void* o, const float* lse,
-                                   const void* dO, void* dqkv, int64_t b, int64_t s, int heads,
-                                   int kv_heads, int N, int d, int causal, tp_dtype dt,
+                                   const void* dO, void* dqkv, void* ldws, int64_t b, int64_t s,
+                                   int heads, int kv_heads, int N, int d, int causal, tp_dtype dt,
                                    cudaStream_t st) {
   if (b <= 0 || s <= 0) return TP_OK;
   TP_TRY(check_sizes(b, s, heads));
   const HeadMap m = gqa_map(heads, kv_heads, N, d);
   const int bi = static_cast<int>(b), si = static_cast<int>(s), kvg = N * m.hkv;
+  if (TP_ATTN_TC && ldws && attention_bwd_tc_eligible(dt, d, m.ldq, qkv, o, dO, dqkv, m.ldo))
+    return launch_attention_bwd_tc(qkv, o, lse, dO, dqkv, ldws, b, s, heads, m.hq, m.g, m.hkv,
+                                   kvg, m.S, m.KO, m.VO, m.ldq, m.ldo, causal, st);
   return dt == TP_BF16
              ? bwd_d<__nv_bfloat16>(qkv, o, lse, dO, dqkv, bi, si, m, kvg, d, causal, st)
              : bwd_d<float>(qkv, o, lse, dO, dqkv, bi, si, m, kvg, d, causal, st);

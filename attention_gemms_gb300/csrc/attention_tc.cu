@@ -346,6 +346,504 @@ __global__ void __launch_bounds__(kThreadsTC, kCtasPerSm) attn_fwd_tc_kernel(con
   }
 }
 
+// ---------------------------------------------------------------------- backward
+//
+// dP = dO V^T, P = exp(S / sqrt(d) - lse), dS = P * (dP - D) / sqrt(d), D = rowsum(dO * O);
+// dQ = dS K (one CTA per 128 query rows), dK = dS^T Q and dV = P^T dO (one CTA per 128
+// key rows of a key/value head, looping over 64-query blocks of every query head of its
+// group). The Q / dO / K tiles in shared memory serve as K-major operands of S and dP and
+// as MN-major operands of the gradient products (the same 128-byte-swizzled rows read
+// along the other dimension).
+
+constexpr int kBwdQKVTile = 128 * 64 * 2;  // 16 KB
+constexpr int kBwdBlk = 64 * 64 * 2;       // 8 KB: a 64-row block
+// dQ: Q, dO, two K/V stages, dS; dK/dV: K, V, two Q/dO stages, P^T, dS^T, and a
+// per-warp table of the 64 (lse, D) pairs of the current query block. + barriers + slack
+constexpr int kBwdSmemDq = 5 * kBwdQKVTile + 256 + 1024;
+constexpr int kBwdSmemKv = 6 * kBwdQKVTile + 256 + 4 * 64 * 8 + 1024;
+
+struct AttnBwdParams {
+  CUtensorMap tq128, tq64;    // qkv, boxes 64 x 128 and 64 x 64
+  CUtensorMap tdo128, tdo64;  // dO, the same boxes
+  const float2* ld;           // (b, H, s): (lse log2(e), D)
+  void* dqkv;
+  int64_t ldq;
+  int s, H, hq, g, hkv;
+  int64_t S, KO, VO;
+  float scale_log2, scale;
+  int causal;
+  int* status;
+  uint64_t timeout_ns;
+};
+
+// ld[b, t, q] = (lse log2(e), D) with D = the sum over the head's 64 columns of dO * O;
+// one warp per (row, head)
+__global__ void __launch_bounds__(256) attn_bwd_dsum_kernel(const __nv_bfloat16* __restrict__ O,
+                                                            const __nv_bfloat16* __restrict__ dO,
+                                                            const float* __restrict__ lse,
+                                                            float2* __restrict__ ld, int64_t rows,
+                                                            int s, int H, int64_t ldo) {
+  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= rows * H) return;
+  const int64_t row = w / H;
+  const int t = static_cast<int>(w - row * H);
+  const __nv_bfloat162 o2 =
+      reinterpret_cast<const __nv_bfloat162*>(O + row * ldo + t * 64)[lane];
+  const __nv_bfloat162 d2 =
+      reinterpret_cast<const __nv_bfloat162*>(dO + row * ldo + t * 64)[lane];
+  float acc = __bfloat162float(o2.x) * __bfloat162float(d2.x) +
+              __bfloat162float(o2.y) * __bfloat162float(d2.y);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+  if (lane == 0) {
+    const int64_t b = row / s, q = row - b * s, i = (b * H + t) * s + q;
+    ld[i] = make_float2(lse[i] * 1.4426950408889634f, acc);
+  }
+}
+
+__device__ __forceinline__ void st_row_bf16(__nv_bfloat16* dst, const uint32_t* v, float mul) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    uint4 w;
+    w.x = pack_bf16x2(__uint_as_float(v[8 * u]) * mul, __uint_as_float(v[8 * u + 1]) * mul);
+    w.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]) * mul, __uint_as_float(v[8 * u + 3]) * mul);
+    w.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]) * mul, __uint_as_float(v[8 * u + 5]) * mul);
+    w.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]) * mul, __uint_as_float(v[8 * u + 7]) * mul);
+    reinterpret_cast<uint4*>(dst)[u] = w;
+  }
+}
+
+// 32 bf16 values of row r into a 128-byte-row K-major swizzled tile at column chunk 4c..4c+3
+__device__ __forceinline__ void st_tile_chunk(uint32_t tile, int r, int c, const float* x) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int ch = c * 4 + u;
+    const uint32_t addr = tile + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4);
+    const float* q8 = x + 8 * u;
+    st_shared_v4(addr, pack_bf16x2(q8[0], q8[1]), pack_bf16x2(q8[2], q8[3]),
+                 pack_bf16x2(q8[4], q8[5]), pack_bf16x2(q8[6], q8[7]));
+  }
+}
+
+// dQ: one CTA per (128 query rows, query head); keys in blocks of 64
+__global__ void __launch_bounds__(kThreadsTC, 2) attn_bwd_dq_tc_kernel(const __grid_constant__ AttnBwdParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  // Q (16 KB) | dO (16 KB) | K0 V0 K1 V1 (8 KB each) | dS (16 KB) | barriers
+  const uint32_t sQ = sb, sdO = sb + kBwdQKVTile, sKV = sb + 2 * kBwdQKVTile,
+                 sdS = sb + 4 * kBwdQKVTile;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 5 * kBwdQKVTile);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  const uint32_t qd_full = bar0, s_full = bar0 + 8 * 5, p_full = bar0 + 8 * 6,
+                 o_done = bar0 + 8 * 7, drain = bar0 + 8 * 8;
+  auto kv_full = [&](int st) { return bar0 + 8u * (1 + st); };
+  auto kv_empty = [&](int st) { return bar0 + 8u * (3 + st); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.z, t = blockIdx.y, q0 = blockIdx.x * 128;
+  const int blk = t / p.hq, tl = t - blk * p.hq;
+  const int qc = static_cast<int>(blk * p.S + static_cast<int64_t>(tl) * 64);
+  const int kc = static_cast<int>(blk * p.S + p.KO + static_cast<int64_t>(tl / p.g) * 64);
+  const int vc = static_cast<int>(blk * p.S + p.VO + static_cast<int64_t>(tl / p.g) * 64);
+  const int row0 = b * p.s;
+  const int kend = p.causal ? min(p.s, q0 + 128) : p.s;
+  const int nkb = (kend + 63) / 64;
+
+  if (threadIdx.x == 0) {
+    mbar_init(qd_full, 1);
+    for (int st = 0; st < 2; ++st) {
+      mbar_init(kv_full(st), 1);
+      mbar_init(kv_empty(st), 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 4);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  const uint32_t tS = tmem, tdP = tmem + 64, tdQ = tmem + 128;
+  int issued = 0;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      bool ok = true;
+      mbar_arrive_expect_tx(qd_full, 2 * kBwdQKVTile);
+      tma_load_2d(sQ, &p.tq128, qd_full, qc, row0 + q0);
+      tma_load_2d(sdO, &p.tdo128, qd_full, t * 64, row0 + q0);
+      for (int j = 0; j < nkb; ++j) {
+        const int st = j & 1;
+        if (j >= 2 && !mbar_wait(kv_empty(st), ((j >> 1) - 1) & 1, p.timeout_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = sKV + st * 2 * kBwdBlk;
+        mbar_arrive_expect_tx(kv_full(st), 2 * kBwdBlk);
+        tma_load_2d(dst, &p.tq64, kv_full(st), kc, row0 + j * 64);
+        tma_load_2d(dst + kBwdBlk, &p.tq64, kv_full(st), vc, row0 + j * 64);
+        ++issued;
+      }
+      if (!ok) record_timeout_attn(p.status);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(128, 64, 0, 0);
+      const uint32_t id_g = idesc_bf16_f32(128, 64, 0, 1);
+      bool ok = mbar_wait(qd_full, 0, p.timeout_ns, abort_flag);
+      auto issue_s = [&](int j) -> bool {
+        const int st = j & 1;
+        if (!mbar_wait(kv_full(st), (j >> 1) & 1, p.timeout_ns, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t k = sKV + st * 2 * kBwdBlk, v = k + kBwdBlk;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_ss(tS, sw128_desc(sQ + kk * 32, 16u, 1024u), sw128_desc(k + kk * 32, 16u, 1024u),
+                      id_s, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_ss(tdP, sw128_desc(sdO + kk * 32, 16u, 1024u), sw128_desc(v + kk * 32, 16u, 1024u),
+                      id_s, kk > 0 ? 1u : 0u);
+        mma_commit(s_full);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; j < nkb && ok; ++j) {
+        if (!mbar_wait(p_full, j & 1, p.timeout_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int st = j & 1;
+        const uint32_t k = sKV + st * 2 * kBwdBlk;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // dQ += dS K (K read MN-major: rows = keys)
+          mma_bf16_ss(tdQ, sw128_desc(sdS + kk * 32, 16u, 1024u),
+                      sw128_desc(k + kk * 2048, 8192u, 1024u), id_g, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(o_done);
+        mma_commit(kv_empty(st));
+        if (j + 1 < nkb) ok = issue_s(j + 1);
+      }
+      if (!ok) record_timeout_attn(p.status);
+    }
+    __syncwarp();
+  } else {
+    const int r = threadIdx.x, qi = q0 + r;
+    const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;
+    const bool valid = qi < p.s;
+    const float2 ld = valid ? p.ld[(static_cast<int64_t>(b) * p.H + t) * p.s + qi]
+                            : make_float2(0.0f, 0.0f);
+    const float lse2 = ld.x, Dq = ld.y;
+    bool ok = true;
+    auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+      int w = 1;
+      if (lane == 0) w = mbar_wait(bar, parity, p.timeout_ns, abort_flag) ? 1 : 0;
+      return __shfl_sync(0xFFFFFFFFu, w, 0) != 0;
+    };
+    for (int j = 0; j < nkb; ++j) {
+      if (!wait_all(s_full, j & 1) || (j > 0 && !wait_all(o_done, (j - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t sv[32], pv[32];
+        tmem_ld32(tS + lanes + c * 32, sv);
+        tmem_ld32(tdP + lanes + c * 32, pv);
+        tmem_ld_wait();
+        float ds[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int key = j * 64 + c * 32 + i;
+          const bool live = valid && key < p.s && !(p.causal && key > qi);
+          const float pr = live ? exp2f(__uint_as_float(sv[i]) * p.scale_log2 - lse2) : 0.0f;
+          ds[i] = pr * (__uint_as_float(pv[i]) - Dq) * p.scale;
+        }
+        st_tile_chunk(sdS, r, c, ds);
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    if (ok && wait_all(o_done, (nkb - 1) & 1)) {
+      tc_fence_after();
+      __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.dqkv) +
+                            (static_cast<int64_t>(row0) + qi) * p.ldq + qc;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tdQ + lanes + c * 32, v);
+        tmem_ld_wait();
+        if (valid) st_row_bf16(drow + c * 32, v, 1.0f);
+      }
+    } else if (lane == 0) {
+      record_timeout_attn(p.status);
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    volatile int no_abort = 0;
+    if (warp == 4 && lane == 0) {
+      mbar_wait(qd_full, 0, kDrainNs, &no_abort);
+      for (int st = 0; st < 2; ++st) {
+        const int n = issued > st ? (issued - 1 - st) / 2 : -1;
+        if (n >= 0) mbar_wait(kv_full(st), n & 1, kDrainNs, &no_abort);
+      }
+    }
+    if (warp == 5 && lane == 0) {
+      mma_commit(drain);
+      mbar_wait(drain, 0, kDrainNs, &no_abort);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// dK, dV: one CTA per (128 key rows, key/value head of a block)
+__global__ void __launch_bounds__(kThreadsTC, 2) attn_bwd_dkdv_tc_kernel(const __grid_constant__ AttnBwdParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  // K (16 KB) | V (16 KB) | Q0 dO0 Q1 dO1 (8 KB each) | P^T (16 KB) | dS^T (16 KB) | barriers
+  const uint32_t sK = sb, sV = sb + kBwdQKVTile, sQD = sb + 2 * kBwdQKVTile,
+                 sPT = sb + 4 * kBwdQKVTile, sdST = sb + 5 * kBwdQKVTile;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 6 * kBwdQKVTile);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float2* ldtab = reinterpret_cast<float2*>(smem + 6 * kBwdQKVTile + 256);  // [4 warps][64]
+  const uint32_t bar0 = smem_u32(bars);
+  const uint32_t kv_full = bar0, s_full = bar0 + 8 * 5, p_full = bar0 + 8 * 6,
+                 o_done = bar0 + 8 * 7, drain = bar0 + 8 * 8;
+  auto qd_full = [&](int st) { return bar0 + 8u * (1 + st); };
+  auto qd_empty = [&](int st) { return bar0 + 8u * (3 + st); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.z, u = blockIdx.y, k0 = blockIdx.x * 128;
+  const int blk = u / p.hkv, kvl = u - blk * p.hkv;
+  const int kc = static_cast<int>(blk * p.S + p.KO + static_cast<int64_t>(kvl) * 64);
+  const int vc = static_cast<int>(blk * p.S + p.VO + static_cast<int64_t>(kvl) * 64);
+  const int row0 = b * p.s;
+  const int qb0 = p.causal ? k0 / 64 : 0;      // earlier queries see none of these keys
+  const int nqb = (p.s + 63) / 64 - qb0;
+  const int nw = p.g * nqb;                    // (query head of the group, query block)
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int st = 0; st < 2; ++st) {
+      mbar_init(qd_full(st), 1);
+      mbar_init(qd_empty(st), 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 4);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  const uint32_t tST = tmem, tdPT = tmem + 64, tdV = tmem + 128, tdK = tmem + 192;
+  auto head_of = [&](int w) { return blk * p.hq + kvl * p.g + w / nqb; };
+  int issued = 0;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      bool ok = true;
+      mbar_arrive_expect_tx(kv_full, 2 * kBwdQKVTile);
+      tma_load_2d(sK, &p.tq128, kv_full, kc, row0 + k0);
+      tma_load_2d(sV, &p.tq128, kv_full, vc, row0 + k0);
+      for (int w = 0; w < nw; ++w) {
+        const int st = w & 1;
+        if (w >= 2 && !mbar_wait(qd_empty(st), ((w >> 1) - 1) & 1, p.timeout_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const int t = head_of(w), tl = t - blk * p.hq, qb = qb0 + w % nqb;
+        const int qc = static_cast<int>(blk * p.S + static_cast<int64_t>(tl) * 64);
+        const uint32_t dst = sQD + st * 2 * kBwdBlk;
+        mbar_arrive_expect_tx(qd_full(st), 2 * kBwdBlk);
+        tma_load_2d(dst, &p.tq64, qd_full(st), qc, row0 + qb * 64);
+        tma_load_2d(dst + kBwdBlk, &p.tdo64, qd_full(st), t * 64, row0 + qb * 64);
+        ++issued;
+      }
+      if (!ok) record_timeout_attn(p.status);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(128, 64, 0, 0);
+      const uint32_t id_g = idesc_bf16_f32(128, 64, 0, 1);
+      bool ok = mbar_wait(kv_full, 0, p.timeout_ns, abort_flag);
+      auto issue_s = [&](int w) -> bool {
+        const int st = w & 1;
+        if (!mbar_wait(qd_full(st), (w >> 1) & 1, p.timeout_ns, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t q = sQD + st * 2 * kBwdBlk, d = q + kBwdBlk;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // S^T = K Q^T
+          mma_bf16_ss(tST, sw128_desc(sK + kk * 32, 16u, 1024u), sw128_desc(q + kk * 32, 16u, 1024u),
+                      id_s, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // dP^T = V dO^T
+          mma_bf16_ss(tdPT, sw128_desc(sV + kk * 32, 16u, 1024u), sw128_desc(d + kk * 32, 16u, 1024u),
+                      id_s, kk > 0 ? 1u : 0u);
+        mma_commit(s_full);
+        return true;
+      };
+      if (ok && nw > 0) ok = issue_s(0);
+      for (int w = 0; w < nw && ok; ++w) {
+        if (!mbar_wait(p_full, w & 1, p.timeout_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int st = w & 1;
+        const uint32_t q = sQD + st * 2 * kBwdBlk, d = q + kBwdBlk;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // dV += P^T dO (dO read MN-major: rows = queries)
+          mma_bf16_ss(tdV, sw128_desc(sPT + kk * 32, 16u, 1024u),
+                      sw128_desc(d + kk * 2048, 8192u, 1024u), id_g, (w > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // dK += dS^T Q
+          mma_bf16_ss(tdK, sw128_desc(sdST + kk * 32, 16u, 1024u),
+                      sw128_desc(q + kk * 2048, 8192u, 1024u), id_g, (w > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(o_done);
+        mma_commit(qd_empty(st));
+        if (w + 1 < nw) ok = issue_s(w + 1);
+      }
+      if (!ok) record_timeout_attn(p.status);
+    }
+    __syncwarp();
+  } else {
+    const int r = threadIdx.x, kj = k0 + r;
+    const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;
+    const bool valid = kj < p.s;
+    bool ok = true;
+    auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+      int w = 1;
+      if (lane == 0) w = mbar_wait(bar, parity, p.timeout_ns, abort_flag) ? 1 : 0;
+      return __shfl_sync(0xFFFFFFFFu, w, 0) != 0;
+    };
+    for (int w = 0; w < nw; ++w) {
+      if (!wait_all(s_full, w & 1) || (w > 0 && !wait_all(o_done, (w - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      const int t = head_of(w), qbase = (qb0 + w % nqb) * 64;
+      {  // this warp's copy of the block's (lse, D) pairs
+        const int64_t lrow = (static_cast<int64_t>(b) * p.H + t) * p.s;
+        float2* tab = ldtab + warp * 64;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int q = qbase + c * 32 + lane;
+          tab[c * 32 + lane] = q < p.s ? p.ld[lrow + q] : make_float2(0.0f, 0.0f);
+        }
+        __syncwarp();
+      }
+      const float4* tab4 = reinterpret_cast<const float4*>(ldtab + warp * 64);
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t sv[32], pv[32];
+        tmem_ld32(tST + lanes + c * 32, sv);
+        tmem_ld32(tdPT + lanes + c * 32, pv);
+        tmem_ld_wait();
+        float pr[32], ds[32];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float4 l4 = tab4[(c * 32 + i) >> 1];  // pairs of queries i, i + 1
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int q = qbase + c * 32 + i + e;
+            const bool live = valid && q < p.s && !(p.causal && kj > q);
+            const float l2 = e ? l4.z : l4.x, dq = e ? l4.w : l4.y;
+            pr[i + e] = live ? exp2f(__uint_as_float(sv[i + e]) * p.scale_log2 - l2) : 0.0f;
+            ds[i + e] = pr[i + e] * (__uint_as_float(pv[i + e]) - dq) * p.scale;
+          }
+        }
+        st_tile_chunk(sPT, r, c, pr);
+        st_tile_chunk(sdST, r, c, ds);
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    if (ok && (nw == 0 || wait_all(o_done, (nw - 1) & 1))) {
+      tc_fence_after();
+      __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.dqkv) + (static_cast<int64_t>(row0) + kj) * p.ldq;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v[32];
+        if (nw > 0) {
+          tmem_ld32(tdV + lanes + c * 32, v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+        if (valid) st_row_bf16(drow + vc + c * 32, v, 1.0f);
+        if (nw > 0) {
+          tmem_ld32(tdK + lanes + c * 32, v);
+          tmem_ld_wait();
+        }
+        if (valid) st_row_bf16(drow + kc + c * 32, v, 1.0f);
+      }
+    } else if (lane == 0) {
+      record_timeout_attn(p.status);
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    volatile int no_abort = 0;
+    if (warp == 4 && lane == 0) {
+      mbar_wait(kv_full, 0, kDrainNs, &no_abort);
+      for (int st = 0; st < 2; ++st) {
+        const int n = issued > st ? (issued - 1 - st) / 2 : -1;
+        if (n >= 0) mbar_wait(qd_full(st), n & 1, kDrainNs, &no_abort);
+      }
+    }
+    if (warp == 5 && lane == 0) {
+      mma_commit(drain);
+      mbar_wait(drain, 0, kDrainNs, &no_abort);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
 typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
                              CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
@@ -421,6 +919,83 @@ tp_status launch_attention_fwd_tc(const void* qkv, void* o, float* lse, int64_t 
                   static_cast<unsigned>(b));
   attn_fwd_tc_kernel<<<grid, kThreadsTC, kSmem, st>>>(p);
   count_launch();
+  TP_CUDA_TRY(cudaGetLastError());
+  return TP_OK;
+}
+
+bool attention_bwd_tc_eligible(tp_dtype dt, int d, int64_t ldq, const void* qkv, const void* o,
+                               const void* dO, const void* dqkv, int64_t ldo) {
+  return attention_tc_eligible(dt, d, ldq, qkv, o, ldo) &&
+         reinterpret_cast<uintptr_t>(dO) % 16 == 0 && reinterpret_cast<uintptr_t>(dqkv) % 16 == 0;
+}
+
+size_t attention_bwd_tc_ws_bytes(int64_t b, int64_t s, int heads) {
+  return static_cast<size_t>(b) * s * heads * sizeof(float2);
+}
+
+tp_status launch_attention_bwd_tc(const void* qkv, const void* o, const float* lse, const void* dO,
+                                  void* dqkv, void* ldws, int64_t b, int64_t s, int heads, int hq,
+                                  int g, int hkv, int kv_total, int64_t S, int64_t KO, int64_t VO,
+                                  int64_t ldq, int64_t ldo, int causal, cudaStream_t st) {
+  if (b <= 0 || s <= 0) return TP_OK;
+  if (b * s > 2147483647ll || ldq > 2147483647ll) return fail(TP_ERR_SHAPE, "attention too large");
+  if (!ldws || reinterpret_cast<uintptr_t>(ldws) % 16 != 0)
+    return fail(TP_ERR_INVALID_ARG, "attention backward workspace missing or misaligned");
+  EncodeFn enc = encoder();
+  if (!enc) return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
+  AttnBwdParams p{};
+  auto encode = [&](CUtensorMap* m, const void* ptr, int64_t cols, uint32_t box_rows) -> tp_status {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(b * s)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled failed (code " + std::to_string(r) + ")");
+    return TP_OK;
+  };
+  TP_TRY(encode(&p.tq128, qkv, ldq, 128));
+  TP_TRY(encode(&p.tq64, qkv, ldq, 64));
+  TP_TRY(encode(&p.tdo128, dO, ldo, 128));
+  TP_TRY(encode(&p.tdo64, dO, ldo, 64));
+  p.ld = static_cast<const float2*>(ldws);
+  p.dqkv = dqkv;
+  p.ldq = ldq;
+  p.s = static_cast<int>(s);
+  p.H = heads;
+  p.hq = hq;
+  p.g = g;
+  p.hkv = hkv;
+  p.S = S;
+  p.KO = KO;
+  p.VO = VO;
+  p.scale_log2 = 1.4426950408889634f / 8.0f;  // log2(e) / sqrt(64)
+  p.scale = 0.125f;                           // 1 / sqrt(64)
+  p.causal = causal;
+  p.status = device_status_word();
+  if (!p.status) return fail(TP_ERR_CUDA, "device status word unavailable");
+  p.timeout_ns = wait_timeout_ns();
+  static std::atomic<uint64_t> attr_set{0};
+  if (needs_setup(attr_set)) {
+    TP_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_dq_tc_kernel,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmemDq));
+    TP_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmemKv));
+    mark_device(attr_set);
+  }
+  const int64_t pairs = b * s * heads;
+  attn_bwd_dsum_kernel<<<static_cast<unsigned>((pairs * 32 + 255) / 256), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse,
+      static_cast<float2*>(ldws), b * s, static_cast<int>(s), heads, ldo);
+  const unsigned tiles = static_cast<unsigned>((s + 127) / 128);
+  attn_bwd_dkdv_tc_kernel<<<dim3(tiles, static_cast<unsigned>(kv_total), static_cast<unsigned>(b)),
+                            kThreadsTC, kBwdSmemKv, st>>>(p);
+  attn_bwd_dq_tc_kernel<<<dim3(tiles, static_cast<unsigned>(heads), static_cast<unsigned>(b)),
+                          kThreadsTC, kBwdSmemDq, st>>>(p);
+  count_launch(3);
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;
 }

@@ -140,9 +140,11 @@ size_t layer_workspace_size(bool fwd, int64_t M, int64_t h, int64_t f, int32_t N
                             tp_reduce mode);
 tp_status launch_attention_fwd(const void* qkv, void* o, float* lse, int64_t b, int64_t s,
                                int64_t h, int heads, int causal, tp_dtype dt, cudaStream_t st);
+// ldws: nullable scratch of attention_bwd_tc_ws_bytes(b, s, heads) bytes (16-byte aligned);
+// with it, bf16 head_dim 64 takes the tensor-core backward, without it the CUDA-core one
 tp_status launch_attention_bwd(const void* qkv, const void* o, const float* lse, const void* dO,
-                               void* dqkv, int64_t b, int64_t s, int64_t h, int heads, int causal,
-                               tp_dtype dt, cudaStream_t st);
+                               void* dqkv, void* ldws, int64_t b, int64_t s, int64_t h, int heads,
+                               int causal, tp_dtype dt, cudaStream_t st);
 // grouped-query layout (per-shard blocks [Q heads | K heads | V heads], key/value heads
 // replicated per block when kv_heads < N); o (M, heads * d)
 tp_status launch_gqa_attention_fwd(const void* qkv, void* o, float* lse, int64_t b, int64_t s,
@@ -154,9 +156,17 @@ bool attention_tc_eligible(tp_dtype dt, int d, int64_t ldq, const void* qkv, con
 tp_status launch_attention_fwd_tc(const void* qkv, void* o, float* lse, int64_t b, int64_t s,
                                   int heads, int hq, int g, int64_t S, int64_t KO, int64_t VO,
                                   int64_t ldq, int64_t ldo, int causal, cudaStream_t st);
+// tensor-core backward: (lse, D) pairs into ldws, then dK/dV and dQ
+bool attention_bwd_tc_eligible(tp_dtype dt, int d, int64_t ldq, const void* qkv, const void* o,
+                               const void* dO, const void* dqkv, int64_t ldo);
+size_t attention_bwd_tc_ws_bytes(int64_t b, int64_t s, int heads);
+tp_status launch_attention_bwd_tc(const void* qkv, const void* o, const float* lse, const void* dO,
+                                  void* dqkv, void* ldws, int64_t b, int64_t s, int heads, int hq,
+                                  int g, int hkv, int kv_total, int64_t S, int64_t KO, int64_t VO,
+                                  int64_t ldq, int64_t ldo, int causal, cudaStream_t st);
 tp_status launch_gqa_attention_bwd(const void* qkv, const void* o, const float* lse,
-                                   const void* dO, void* dqkv, int64_t b, int64_t s, int heads,
-                                   int kv_heads, int N, int d, int causal, tp_dtype dt,
+                                   const void* dO, void* dqkv, void* ldws, int64_t b, int64_t s,
+                                   int heads, int kv_heads, int N, int d, int causal, tp_dtype dt,
                                    cudaStream_t st);
 
 // vocabulary-parallel embedding / cross-entropy and AdamW (vocab.cu)

@@ -145,8 +145,9 @@ _SIGS = {
     "tp_gqa_pack_qkv": (_ST, [_P] * 4 + [_I64, _I32, _I32, _I32, _ST, _P]),
     "tp_gqa_attention_fwd": (_ST, [_P] * 3 + [_I64, _I64, _I64, _I32, _I32, _I32, ctypes.c_int,
                                               _ST, _P]),
+    "tp_gqa_attention_bwd_workspace_size": (_SZ, [_I64, _I64, _I32]),
     "tp_gqa_attention_bwd": (_ST, [_P] * 5 + [_I64, _I64, _I64, _I32, _I32, _I32, ctypes.c_int,
-                                              _ST, _P]),
+                                              _ST, _P, _SZ, _P]),
     "tp_gqa_attn_proj_fwd": (_ST, [_P] * 12 + [_I64, _I64, _I64, _I32, _I32, _I32, ctypes.c_int,
                                                _ST, _ST, _P, _SZ, _P]),
     "tp_gqa_attn_proj_bwd": (_ST, [_P] * 16 + [_I64, _I64, _I64, _I32, _I32, _I32, ctypes.c_int,
@@ -335,11 +336,15 @@ def tp_gqa_attention_fwd(qkv, o, lse, b, s, h, n_heads, n_kv_heads, N, causal, d
                                       n_kv_heads, N, int(causal), int(dtype), _stream(stream)))
 
 
+def tp_gqa_attention_bwd_workspace_size(b, s, n_heads):
+    return lib().tp_gqa_attention_bwd_workspace_size(b, s, n_heads)
+
+
 def tp_gqa_attention_bwd(qkv, o, lse, dO, dqkv, b, s, h, n_heads, n_kv_heads, N, causal, dtype,
-                         stream=None):
+                         ws=None, ws_bytes=0, stream=None):
     _check(lib().tp_gqa_attention_bwd(_ptr(qkv), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dqkv), b, s,
                                       h, n_heads, n_kv_heads, N, int(causal), int(dtype),
-                                      _stream(stream)))
+                                      _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def tp_gqa_attn_proj_fwd(x, gamma, beta, Wqkv, Wo, xn, mean, rstd, qkv, o, lse, out, b, s, h,

@@ -471,14 +471,20 @@ TP_API tp_status tp_gqa_pack_qkv(const void* Wq, const void* Wk, const void* Wv,
                                  tp_dtype dtype, void* stream);
 /* The attention core alone on the sharded qkv (M, W): O (M, h) and lse (b, n_heads, s);
  * backward: dqkv (M, W) from dO, each key/value head's gradient summing the query heads
- * of its block that use it (a replica's share; tp_gqa_attn_proj_bwd adds the replicas). */
+ * of its block that use it (a replica's share; tp_gqa_attn_proj_bwd adds the replicas).
+ * Every element of dqkv's M rows is written. The backward's ws is optional scratch of at
+ * least tp_gqa_attention_bwd_workspace_size(b, s, n_heads) bytes, 16-byte aligned: with
+ * it, bf16 at head_dim 64 runs on the tensor cores (the per-row (lse, D = rowsum(dO * O))
+ * pairs are kept there); with ws == NULL every case runs on the CUDA cores. A ws that is
+ * given but too small is TP_ERR_WORKSPACE. */
+TP_API size_t tp_gqa_attention_bwd_workspace_size(int64_t b, int64_t s, int32_t n_heads);
 TP_API tp_status tp_gqa_attention_fwd(const void* qkv, void* o, float* lse, int64_t b, int64_t s,
                                       int64_t h, int32_t n_heads, int32_t n_kv_heads, int32_t N,
                                       int causal, tp_dtype dtype, void* stream);
 TP_API tp_status tp_gqa_attention_bwd(const void* qkv, const void* o, const float* lse,
                                       const void* dO, void* dqkv, int64_t b, int64_t s, int64_t h,
                                       int32_t n_heads, int32_t n_kv_heads, int32_t N, int causal,
-                                      tp_dtype dtype, void* stream);
+                                      tp_dtype dtype, void* ws, size_t ws_bytes, void* stream);
 /* out = x + sum_i O_i W_o,i, O from LN(x) and the sharded Wqkv; saved state as
  * tp_attn_proj_fwd with qkv (M, W) and lse (b, n_heads, s). */
 TP_API tp_status tp_gqa_attn_proj_fwd(const void* x, const float* gamma, const float* beta,

@@ -88,24 +88,18 @@ def _shard_views(H, Hkv, N, d):
     return hq, hkv, Ws
 
 
-def gqa_block_fwd(x, b, s, gamma, beta, Wsh, Wo, H, Hkv, N, causal=False):
-    """Head-sharded GQA block, shard by shard: QKV_i = LN(x) Wsh_i (column-parallel),
-    attention on shard i's query heads with its (possibly replicated) key/value heads,
-    Z_i = O_i W_o,i (row block i), out = x + sum_i Z_i. Returns xn, QKV (all shards'
-    blocks side by side), O (heads in order), out."""
-    M, h = x.shape
-    d = Wo.shape[0] // H
-    hq, hkv, Ws = _shard_views(H, Hkv, N, d)
+def gqa_attention_fwd(QKV, b, s, H, Hkv, N, causal=False):
+    """The attention core on the sharded QKV (M, N S): shard i's local query head tl
+    attends with its local key/value head tl // g, every batch element on its own.
+    Returns O (M, H d), the heads in order."""
+    M = QKV.shape[0]
+    hq, hkv, _ = gqa_split(H, Hkv, N)
+    d = QKV.shape[1] // (N * (hq + 2 * hkv))
+    Ws = (hq + 2 * hkv) * d
     g = hq // hkv
-    xn = T.layernorm_fwd(x, gamma, beta)[0]
-    QKV = np.zeros((M, N * Ws))
     O = np.zeros((M, H * d))
-    parts = []
     for i in range(N):
-        Wi = Wsh[:, i * Ws:(i + 1) * Ws]
-        Qi = xn @ Wi
-        QKV[:, i * Ws:(i + 1) * Ws] = Qi
-        Oi = np.zeros((M, hq * d))
+        Qi = QKV[:, i * Ws:(i + 1) * Ws]
         for tl in range(hq):
             kl = tl // g
             for bb in range(b):
@@ -113,36 +107,23 @@ def gqa_block_fwd(x, b, s, gamma, beta, Wsh, Wo, H, Hkv, N, causal=False):
                 q = Qi[r, tl * d:(tl + 1) * d]
                 k = Qi[r, (hq + kl) * d:(hq + kl + 1) * d]
                 v = Qi[r, (hq + hkv + kl) * d:(hq + hkv + kl + 1) * d]
-                Oi[r, tl * d:(tl + 1) * d] = T.attention_head_fwd(q, k, v, causal)[0]
-        O[:, i * hq * d:(i + 1) * hq * d] = Oi
-        parts.append(Oi @ Wo[i * hq * d:(i + 1) * hq * d, :])
-    return {"xn": xn, "QKV": QKV, "O": O, "out": T.shard_reduce(parts, residual=x)}
+                O[r, (i * hq + tl) * d:(i * hq + tl + 1) * d] = T.attention_head_fwd(
+                    q, k, v, causal)[0]
+    return O
 
 
-def gqa_block_bwd(x, b, s, gamma, beta, Wsh, Wo, H, Hkv, N, dout, causal=False):
-    """Backward of `gqa_block_fwd`, shard by shard. Shard i: dO_i = dout W_o,i^T;
-    attention backward over its query heads -- a key/value head's gradient sums the
-    contributions of the shard's query heads that use it; dWsh_i = xn^T dQKV_i;
-    dW_o,i = O_i^T dout. The f-backward sums dxn = sum_i dQKV_i Wsh_i^T over the shards,
-    then LN backward (+ dout). Finally the replicas of each key/value head add their
-    weight gradients and every replica takes the sum (the all-reduce that keeps the
-    copies identical)."""
-    M, h = x.shape
-    d = Wo.shape[0] // H
+def gqa_attention_bwd(QKV, dO, b, s, H, Hkv, N, causal=False):
+    """Backward of `gqa_attention_fwd`: dQKV (M, N S) in the same layout; a key/value
+    head's gradient sums the contributions of its shard's query heads that use it (a
+    replica's share when N > Hkv)."""
+    d = dO.shape[1] // H
     hq, hkv, Ws = _shard_views(H, Hkv, N, d)
-    _, _, r = gqa_split(H, Hkv, N)
     g = hq // hkv
-    f = gqa_block_fwd(x, b, s, gamma, beta, Wsh, Wo, H, Hkv, N, causal)
-    xn, QKV, O = f["xn"], f["QKV"], f["O"]
-    dWsh = np.zeros_like(Wsh)
-    dWo = np.zeros_like(Wo)
-    dxparts = []
+    dQKV = np.zeros_like(QKV)
     for i in range(N):
         Qi = QKV[:, i * Ws:(i + 1) * Ws]
-        rows = slice(i * hq * d, (i + 1) * hq * d)
-        dOi = dout @ Wo[rows, :].T
-        dWo[rows, :] = O[:, rows].T @ dout
-        dQi = np.zeros_like(Qi)
+        dQi = dQKV[:, i * Ws:(i + 1) * Ws]
+        dOi = dO[:, i * hq * d:(i + 1) * hq * d]
         for tl in range(hq):
             kl = tl // g
             qc = slice(tl * d, (tl + 1) * d)
@@ -155,6 +136,48 @@ def gqa_block_bwd(x, b, s, gamma, beta, Wsh, Wo, H, Hkv, N, dout, causal=False):
                 dQi[rr, qc] += dq
                 dQi[rr, kc] += dk
                 dQi[rr, vc] += dv
+    return dQKV
+
+
+def gqa_block_fwd(x, b, s, gamma, beta, Wsh, Wo, H, Hkv, N, causal=False):
+    """Head-sharded GQA block, shard by shard: QKV_i = LN(x) Wsh_i (column-parallel),
+    attention on shard i's query heads with its (possibly replicated) key/value heads,
+    Z_i = O_i W_o,i (row block i), out = x + sum_i Z_i. Returns xn, QKV (all shards'
+    blocks side by side), O (heads in order), out."""
+    d = Wo.shape[0] // H
+    hq, hkv, Ws = _shard_views(H, Hkv, N, d)
+    xn = T.layernorm_fwd(x, gamma, beta)[0]
+    QKV = np.concatenate([xn @ Wsh[:, i * Ws:(i + 1) * Ws] for i in range(N)], axis=1)
+    O = gqa_attention_fwd(QKV, b, s, H, Hkv, N, causal)
+    rows = lambda i: slice(i * hq * d, (i + 1) * hq * d)
+    parts = [O[:, rows(i)] @ Wo[rows(i), :] for i in range(N)]
+    return {"xn": xn, "QKV": QKV, "O": O, "out": T.shard_reduce(parts, residual=x)}
+
+
+def gqa_block_bwd(x, b, s, gamma, beta, Wsh, Wo, H, Hkv, N, dout, causal=False):
+    """Backward of `gqa_block_fwd`, shard by shard. Shard i: dO_i = dout W_o,i^T;
+    attention backward over its query heads -- a key/value head's gradient sums the
+    contributions of the shard's query heads that use it; dWsh_i = xn^T dQKV_i;
+    dW_o,i = O_i^T dout. The f-backward sums dxn = sum_i dQKV_i Wsh_i^T over the shards,
+    then LN backward (+ dout). Finally the replicas of each key/value head add their
+    weight gradients and every replica takes the sum (the all-reduce that keeps the
+    copies identical)."""
+    d = Wo.shape[0] // H
+    hq, hkv, Ws = _shard_views(H, Hkv, N, d)
+    _, _, r = gqa_split(H, Hkv, N)
+    f = gqa_block_fwd(x, b, s, gamma, beta, Wsh, Wo, H, Hkv, N, causal)
+    xn, QKV, O = f["xn"], f["QKV"], f["O"]
+    rows = lambda i: slice(i * hq * d, (i + 1) * hq * d)
+    dWo = np.zeros_like(Wo)
+    dO = np.zeros_like(O)
+    for i in range(N):
+        dO[:, rows(i)] = dout @ Wo[rows(i), :].T
+        dWo[rows(i), :] = O[:, rows(i)].T @ dout
+    dQKV = gqa_attention_bwd(QKV, dO, b, s, H, Hkv, N, causal)
+    dWsh = np.zeros_like(Wsh)
+    dxparts = []
+    for i in range(N):
+        dQi = dQKV[:, i * Ws:(i + 1) * Ws]
         dWsh[:, i * Ws:(i + 1) * Ws] = xn.T @ dQi
         dxparts.append(dQi @ Wsh[:, i * Ws:(i + 1) * Ws].T)
     dxn = T.shard_reduce(dxparts)

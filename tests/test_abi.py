@@ -149,6 +149,18 @@ def test_row_and_mlp_argument_errors(L):
         T.Status.INVALID_ARG                                # layer arrays missing
 
 
+def test_attention_core_bwd_workspace_errors(L):
+    need = T.tp_gqa_attention_bwd_workspace_size(1, 8, 4)
+    assert need >= 8 * 8 * 4 and T.tp_gqa_attention_bwd_workspace_size(1, 8, 0) == 0
+    a = lambda **kw: (lambda: T.tp_gqa_attention_bwd(**{**dict(
+        qkv=A16, o=A16, lse=A16, dO=A16, dqkv=A16, b=1, s=8, h=256, n_heads=4, n_kv_heads=4,
+        N=1, causal=0, dtype=BF, ws=A16, ws_bytes=need), **kw}))
+    assert _status(a(ws_bytes=need - 1)) == T.Status.WORKSPACE
+    assert _status(a(ws=A16 + 8)) == T.Status.ALIGNMENT
+    assert _status(a(dO=None)) == T.Status.INVALID_ARG
+    assert _status(a(n_kv_heads=3)) == T.Status.SHAPE
+
+
 def test_workspace_sizes(L):
     M, h, f, N = 1000, 256, 1024, 4
     assert T.tp_workspace_size(T.Op.COL_LINEAR, M, h, f, N, BF) == 0

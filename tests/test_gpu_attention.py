@@ -101,6 +101,14 @@ def test_attn_block_bf16(heads, causal, mode):
         assert e <= BF16_TOL, (k, e)
 
 
+@pytest.mark.parametrize("causal", [0, 1])
+def test_attn_block_bf16_multi_tile(causal):
+    """head_dim 64 (the tensor-core kernels) over three 128-row tiles, the last ragged."""
+    errs = _attn_case(b=2, s=300, h=128, heads=2, N=2, causal=causal, mode="buffers")
+    for k, e in errs.items():
+        assert e <= BF16_TOL, (k, e)
+
+
 def test_attn_block_f32():
     errs = _attn_case(b=2, s=70, h=64, heads=4, N=2, causal=0, mode="buffers", dtype="f32")
     for k, e in errs.items():

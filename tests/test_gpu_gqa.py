@@ -81,6 +81,42 @@ def test_gqa_block_bf16(h, H, Hkv, N, mode, causal):
         assert v <= BF16_TOL, (k, v)
 
 
+CORE_CASES = [(4, 4, 1), (8, 2, 2), (8, 4, 2), (8, 2, 4)]  # (H, Hkv, N) at head_dim 64
+
+
+@pytest.mark.parametrize("H,Hkv,N", CORE_CASES)
+@pytest.mark.parametrize("causal", [0, 1])
+@pytest.mark.parametrize("s", [300, 64, 1])
+def test_gqa_attention_core_bf16(H, Hkv, N, causal, s):
+    """The attention core alone at head_dim 64 in bf16, over several 128-row tiles and a
+    ragged tail: the forward, and the backward with its scratch (tensor cores) and
+    without it (CUDA cores), each against the fp64 oracle on the same bf16 qkv. (H, Hkv,
+    N) = (4, 4, 1) is the multi-head layout; (8, 2, 4) replicates each key/value head."""
+    b, d = 2, 64
+    h, M = H * d, b * s
+    W = T.tp_gqa_qkv_cols(h, H, Hkv, N)
+    BF = T.DType.BF16
+    qo, qkv = tensor((M, W), 6100 + s, dtype="bf16")
+    do, dO = tensor((M, h), 6200 + s, dtype="bf16")
+    o = torch.empty((M, h), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((b, H, s), dtype=torch.float32, device="cuda")
+    T.tp_gqa_attention_fwd(qkv, o, lse, b, s, h, H, Hkv, N, causal, BF)
+    wsb = T.tp_gqa_attention_bwd_workspace_size(b, s, H)
+    assert wsb >= 8 * b * s * H
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    nan = lambda: torch.full((M, W), float("nan"), dtype=torch.bfloat16, device="cuda")
+    d_tc, d_cc = nan(), nan()  # every element of dqkv is written
+    T.tp_gqa_attention_bwd(qkv, o, lse, dO, d_tc, b, s, h, H, Hkv, N, causal, BF, ws, wsb)
+    T.tp_gqa_attention_bwd(qkv, o, lse, dO, d_cc, b, s, h, H, Hkv, N, causal, BF)
+    torch.cuda.synchronize()
+    assert T.tp_check_status() == 0
+    O_ref = Q.gqa_attention_fwd(qo, b, s, H, Hkv, N, bool(causal))
+    d_ref = Q.gqa_attention_bwd(qo, do, b, s, H, Hkv, N, bool(causal))
+    assert rel(host(o), O_ref) <= BF16_TOL
+    assert rel(host(d_tc), d_ref) <= BF16_TOL
+    assert rel(host(d_cc), d_ref) <= BF16_TOL
+
+
 @pytest.mark.parametrize("H,Hkv,N", [(6, 3, 3), (6, 3, 6), (6, 2, 2)])
 def test_gqa_block_f32(H, Hkv, N):
     errs, *_ = _run(2, 70, 16 * H, H, Hkv, N, "f32", "buffers", 0)

@@ -83,6 +83,22 @@ def test_gqa_bwd_fd(H, Hkv, N):
                                   gr["dWqkv"][:, base * Ws + hq * d:(base + 1) * Ws])
 
 
+@pytest.mark.parametrize("H,Hkv,N", [(4, 2, 2), (4, 2, 4), (4, 4, 1)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_core_bwd_fd(H, Hkv, N, causal):
+    """The attention core alone: gqa_attention_bwd is the gradient of
+    sum(gqa_attention_fwd(QKV) * dO) with respect to every entry of the sharded QKV,
+    each replica's key/value columns being inputs of their own."""
+    r = np.random.default_rng(74)
+    b, s, d = 2, 3, 2
+    hq, hkv, _ = Q.gqa_split(H, Hkv, N)
+    QKV = r.normal(size=(b * s, N * (hq + 2 * hkv) * d))
+    dO = r.normal(size=(b * s, H * d))
+    loss = lambda: float(np.sum(Q.gqa_attention_fwd(QKV, b, s, H, Hkv, N, causal) * dO))
+    got = Q.gqa_attention_bwd(QKV, dO, b, s, H, Hkv, N, causal)
+    assert T.rel_err(got, _fd(loss, QKV)) <= 1e-7
+
+
 def test_gqa_split_rules():
     assert Q.gqa_split(32, 8, 4) == (8, 2, 1)
     assert Q.gqa_split(32, 8, 16) == (2, 1, 2)
