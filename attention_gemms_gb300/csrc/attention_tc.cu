@@ -97,6 +97,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// 2^x on the special-function unit (PTX ex2.approx.ftz: relative error about 2^-22,
+// subnormal results flushed to zero); P is rounded to bf16 right after
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __global__ void __launch_bounds__(kThreadsTC, kCtasPerSm) attn_fwd_tc_kernel(const __grid_constant__ AttnTcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -191,6 +199,11 @@ __global__ void __launch_bounds__(kThreadsTC, kCtasPerSm) attn_fwd_tc_kernel(con
           break;
         }
         tc_fence_after();
+        // S(j) has been read: the next block's scores go ahead of P V
+        if (j + 1 < nkb && !issue_s(j + 1)) {
+          ok = false;
+          break;
+        }
         const int st = j & 1;
         const uint32_t vaddr = sb + kOffKV + st * 2 * kKVTile + kKVTile;
 #pragma unroll
@@ -200,7 +213,6 @@ __global__ void __launch_bounds__(kThreadsTC, kCtasPerSm) attn_fwd_tc_kernel(con
                       (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(o_done);
         mma_commit(kv_empty(st));
-        if (j + 1 < nkb) ok = issue_s(j + 1);
       }
       if (!ok) record_timeout_attn(p.status);
     }
@@ -224,67 +236,70 @@ __global__ void __launch_bounds__(kThreadsTC, kCtasPerSm) attn_fwd_tc_kernel(con
       }
       tc_fence_after();
       const int k0 = j * kKB;
-      // pass 1: the block's row maximum (masked keys: beyond the sequence, or after the query)
+      uint32_t v[kKB];  // the row's 64 scores, read once
+      tmem_ld32(tS + lanes, *reinterpret_cast<uint32_t(*)[32]>(v));
+      tmem_ld32(tS + lanes + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      tmem_ld_wait();
+      // the block's row maximum (masked keys: beyond the sequence, or after the query)
+      const bool full = k0 + kKB <= p.s && !(p.causal && k0 + kKB - 1 > qi);
       float mb = -INFINITY;
+      if (full) {
 #pragma unroll
-      for (int c = 0; c < kKB / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS + lanes + c * 32, v);
-        tmem_ld_wait();
+        for (int i = 0; i < kKB; ++i) mb = fmaxf(mb, __uint_as_float(v[i]));
+        mb *= p.scale_log2;
+      } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int key = k0 + c * 32 + i;
+        for (int i = 0; i < kKB; ++i) {
+          const int key = k0 + i;
           const bool live = key < p.s && !(p.causal && key > qi);
-          if (live) mb = fmaxf(mb, __uint_as_float(v[i]) * p.scale_log2);
+          if (!live) v[i] = __float_as_uint(-INFINITY);
+          mb = fmaxf(mb, __uint_as_float(v[i]));
         }
+        mb *= p.scale_log2;
       }
-      const float m_new = fmaxf(m2, mb);
+      // Lazy rescaling: the running maximum m2 moves only when the block's maximum
+      // exceeds it by more than 8 (a factor 256 in P, harmless in bf16 and the fp32
+      // sums); otherwise P = 2^(s - m2) with the stale m2 and O needs no rescale.
+      // O / l and the log-sum-exp use the same m2, so the result does not change.
+      const bool move = mb > m2 + 8.0f;
+      const float m_new = move ? mb : m2;
       const float m_use = m_new == -INFINITY ? 0.0f : m_new;
-      const float corr = exp2f(m2 - m_use);  // 0 on the first block
+      const float corr = move ? ex2_approx(m2 - m_use) : 1.0f;  // 0 on the first block
       // P may be overwritten and O rescaled once the previous block's P V is complete
       if (j > 0 && !wait_all(o_done, (j - 1) & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // pass 2: P = 2^(s - m) as bf16 into the swizzled K-major P tile (128-byte rows)
+      // P = 2^(s - m) as bf16 into the swizzled K-major P tile (128-byte rows)
       float sum = 0.0f;
 #pragma unroll
-      for (int c = 0; c < kKB / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS + lanes + c * 32, v);
-        tmem_ld_wait();
+      for (int i = 0; i < kKB; ++i) {
+        const float e = ex2_approx(fmaf(__uint_as_float(v[i]), p.scale_log2, -m_use));
+        sum += e;
+        v[i] = __float_as_uint(e);
+      }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int key = k0 + c * 32 + i;
-          const bool live = key < p.s && !(p.causal && key > qi);
-          const float e = live ? exp2f(__uint_as_float(v[i]) * p.scale_log2 - m_use) : 0.0f;
-          sum += e;
-          v[i] = __float_as_uint(e);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {  // 8 keys = 16 bytes per store
-          const int ch = c * 4 + u;    // 16-byte chunk of the 128-byte row
-          const uint32_t addr = sb + kOffP + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4);
-          const uint32_t* q8 = v + 8 * u;
-          st_shared_v4(addr,
-                       pack_bf16x2(__uint_as_float(q8[0]), __uint_as_float(q8[1])),
-                       pack_bf16x2(__uint_as_float(q8[2]), __uint_as_float(q8[3])),
-                       pack_bf16x2(__uint_as_float(q8[4]), __uint_as_float(q8[5])),
-                       pack_bf16x2(__uint_as_float(q8[6]), __uint_as_float(q8[7])));
-        }
+      for (int ch = 0; ch < kKB / 8; ++ch) {  // 8 keys = 16 bytes per store
+        const uint32_t addr = sb + kOffP + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4);
+        const uint32_t* q8 = v + 8 * ch;
+        st_shared_v4(addr,
+                     pack_bf16x2(__uint_as_float(q8[0]), __uint_as_float(q8[1])),
+                     pack_bf16x2(__uint_as_float(q8[2]), __uint_as_float(q8[3])),
+                     pack_bf16x2(__uint_as_float(q8[4]), __uint_as_float(q8[5])),
+                     pack_bf16x2(__uint_as_float(q8[6]), __uint_as_float(q8[7])));
       }
       l = l * corr + sum;
       m2 = m_new;
-      if (j > 0) {  // O *= corr (the new maximum rebases the running output)
+      if (j > 0 && __any_sync(0xFFFFFFFFu, move)) {  // O *= corr (a warp-wide TMEM access)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tO + lanes + c * 32, v);
+          uint32_t o[32];
+          tmem_ld32(tO + lanes + c * 32, o);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
-          tmem_st32(tO + lanes + c * 32, v);
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+          tmem_st32(tO + lanes + c * 32, o);
         }
         tmem_st_wait();
       }
@@ -360,7 +375,7 @@ constexpr int kBwdBlk = 64 * 64 * 2;       // 8 KB: a 64-row block
 // dQ: Q, dO, two K/V stages, dS; dK/dV: K, V, two Q/dO stages, P^T, dS^T, and a
 // per-warp table of the 64 (lse, D) pairs of the current query block. + barriers + slack
 constexpr int kBwdSmemDq = 5 * kBwdQKVTile + 256 + 1024;
-constexpr int kBwdSmemKv = 6 * kBwdQKVTile + 256 + 4 * 64 * 8 + 1024;
+constexpr int kBwdSmemKv = 6 * kBwdQKVTile + 256 + 8 * 32 * 8 + 1024;
 
 struct AttnBwdParams {
   CUtensorMap tq128, tq64;    // qkv, boxes 64 x 128 and 64 x 64
@@ -426,8 +441,22 @@ __device__ __forceinline__ void st_tile_chunk(uint32_t tile, int r, int c, const
   }
 }
 
-// dQ: one CTA per (128 query rows, query head); keys in blocks of 64
-__global__ void __launch_bounds__(kThreadsTC, 2) attn_bwd_dq_tc_kernel(const __grid_constant__ AttnBwdParams p) {
+constexpr int kThreadsBwd = 320;  // warps 0-7 element-wise, 8 TMA, 9 MMA
+
+// Element-wise warps of the backward kernels: warp w reads TMEM lanes 32 (w % 4) ..
+// + 31 (one row each) and the w / 4-th 32-column half of every 64-column block.
+struct BwdLane {
+  int quarter, half, r;
+  uint32_t lanes;
+  __device__ explicit BwdLane(int warp, int lane)
+      : quarter(warp & 3), half(warp >> 2), r((warp & 3) * 32 + lane),
+        lanes(static_cast<uint32_t>((warp & 3) * 32) << 16) {}
+};
+
+// dQ: one CTA per (128 query rows, query head); keys in blocks of 64.
+// MMA order per block j: [S(j + 1), dP(j + 1)] then dQ(j) += dS(j) K(j), so the
+// element-wise warps work on block j + 1 while dQ(j) runs.
+__global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dq_tc_kernel(const __grid_constant__ AttnBwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -461,13 +490,13 @@ __global__ void __launch_bounds__(kThreadsTC, 2) attn_bwd_dq_tc_kernel(const __g
       mbar_init(kv_empty(st), 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, 4);
+    mbar_init(p_full, 8);  // one arrive per element-wise warp
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), 256);
     tmem_relinquish();
   }
@@ -478,7 +507,7 @@ __global__ void __launch_bounds__(kThreadsTC, 2) attn_bwd_dq_tc_kernel(const __g
   const uint32_t tS = tmem, tdP = tmem + 64, tdQ = tmem + 128;
   int issued = 0;
 
-  if (warp == 4) {
+  if (warp == 8) {
     if (lane == 0) {
       bool ok = true;
       mbar_arrive_expect_tx(qd_full, 2 * kBwdQKVTile);
@@ -499,12 +528,12 @@ __global__ void __launch_bounds__(kThreadsTC, 2) attn_bwd_dq_tc_kernel(const __g
       if (!ok) record_timeout_attn(p.status);
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(128, 64, 0, 0);
       const uint32_t id_g = idesc_bf16_f32(128, 64, 0, 1);
       bool ok = mbar_wait(qd_full, 0, p.timeout_ns, abort_flag);
-      auto issue_s = [&](int j) -> bool {
+      auto issue_s = [&](int j) -> bool {  // S = Q K^T and dP = dO V^T of key block j
         const int st = j & 1;
         if (!mbar_wait(kv_full(st), (j >> 1) & 1, p.timeout_ns, abort_flag)) return false;
         tc_fence_after();
@@ -527,6 +556,11 @@ __global__ void __launch_bounds__(kThreadsTC, 2) attn_bwd_dq_tc_kernel(const __g
           break;
         }
         tc_fence_after();
+        // S and dP of block j have been read: the next block's go first
+        if (j + 1 < nkb && !issue_s(j + 1)) {
+          ok = false;
+          break;
+        }
         const int st = j & 1;
         const uint32_t k = sKV + st * 2 * kBwdBlk;
 #pragma unroll
@@ -535,14 +569,13 @@ __global__ void __launch_bounds__(kThreadsTC, 2) attn_bwd_dq_tc_kernel(const __g
                       sw128_desc(k + kk * 2048, 8192u, 1024u), id_g, (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(o_done);
         mma_commit(kv_empty(st));
-        if (j + 1 < nkb) ok = issue_s(j + 1);
       }
       if (!ok) record_timeout_attn(p.status);
     }
     __syncwarp();
   } else {
-    const int r = threadIdx.x, qi = q0 + r;
-    const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;
+    const BwdLane L(warp, lane);
+    const int qi = q0 + L.r;
     const bool valid = qi < p.s;
     const float2 ld = valid ? p.ld[(static_cast<int64_t>(b) * p.H + t) * p.s + qi]
                             : make_float2(0.0f, 0.0f);
@@ -554,27 +587,37 @@ __global__ void __launch_bounds__(kThreadsTC, 2) attn_bwd_dq_tc_kernel(const __g
       return __shfl_sync(0xFFFFFFFFu, w, 0) != 0;
     };
     for (int j = 0; j < nkb; ++j) {
-      if (!wait_all(s_full, j & 1) || (j > 0 && !wait_all(o_done, (j - 1) & 1))) {
+      if (!wait_all(s_full, j & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      uint32_t sv[32], pv[32];
+      tmem_ld32(tS + L.lanes + L.half * 32, sv);
+      tmem_ld32(tdP + L.lanes + L.half * 32, pv);
+      tmem_ld_wait();
+      const int k0 = j * 64 + L.half * 32;
+      float ds[32];  // P (dP - D); the 1 / sqrt(d) is applied to dQ at the end
+      if (valid && k0 + 32 <= p.s && !(p.causal && k0 + 31 > qi)) {
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t sv[32], pv[32];
-        tmem_ld32(tS + lanes + c * 32, sv);
-        tmem_ld32(tdP + lanes + c * 32, pv);
-        tmem_ld_wait();
-        float ds[32];
+        for (int i = 0; i < 32; ++i)
+          ds[i] = ex2_approx(fmaf(__uint_as_float(sv[i]), p.scale_log2, -lse2)) *
+                  (__uint_as_float(pv[i]) - Dq);
+      } else {  // keys beyond the sequence or after the query, rows beyond the sequence
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const int key = j * 64 + c * 32 + i;
+          const int key = k0 + i;
           const bool live = valid && key < p.s && !(p.causal && key > qi);
-          const float pr = live ? exp2f(__uint_as_float(sv[i]) * p.scale_log2 - lse2) : 0.0f;
-          ds[i] = pr * (__uint_as_float(pv[i]) - Dq) * p.scale;
+          const float pr = live ? ex2_approx(fmaf(__uint_as_float(sv[i]), p.scale_log2, -lse2)) : 0.0f;
+          ds[i] = pr * (__uint_as_float(pv[i]) - Dq);
         }
-        st_tile_chunk(sdS, r, c, ds);
       }
+      // the dS tile is free once the previous block's dQ MMA has completed
+      if (j > 0 && !wait_all(o_done, (j - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      st_tile_chunk(sdS, L.r, L.half, ds);
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -582,15 +625,13 @@ __global__ void __launch_bounds__(kThreadsTC, 2) attn_bwd_dq_tc_kernel(const __g
     }
     if (ok && wait_all(o_done, (nkb - 1) & 1)) {
       tc_fence_after();
-      __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.dqkv) +
-                            (static_cast<int64_t>(row0) + qi) * p.ldq + qc;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tdQ + lanes + c * 32, v);
-        tmem_ld_wait();
-        if (valid) st_row_bf16(drow + c * 32, v, 1.0f);
-      }
+      uint32_t v[32];
+      tmem_ld32(tdQ + L.lanes + L.half * 32, v);
+      tmem_ld_wait();
+      if (valid)
+        st_row_bf16(static_cast<__nv_bfloat16*>(p.dqkv) + (static_cast<int64_t>(row0) + qi) * p.ldq +
+                        qc + L.half * 32,
+                    v, p.scale);
     } else if (lane == 0) {
       record_timeout_attn(p.status);
     }
@@ -599,28 +640,30 @@ __global__ void __launch_bounds__(kThreadsTC, 2) attn_bwd_dq_tc_kernel(const __g
   __syncthreads();
   if (*abort_flag) {
     volatile int no_abort = 0;
-    if (warp == 4 && lane == 0) {
+    if (warp == 8 && lane == 0) {
       mbar_wait(qd_full, 0, kDrainNs, &no_abort);
       for (int st = 0; st < 2; ++st) {
         const int n = issued > st ? (issued - 1 - st) / 2 : -1;
         if (n >= 0) mbar_wait(kv_full(st), n & 1, kDrainNs, &no_abort);
       }
     }
-    if (warp == 5 && lane == 0) {
+    if (warp == 9 && lane == 0) {
       mma_commit(drain);
       mbar_wait(drain, 0, kDrainNs, &no_abort);
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 256);
   }
 }
 
-// dK, dV: one CTA per (128 key rows, key/value head of a block)
-__global__ void __launch_bounds__(kThreadsTC, 2) attn_bwd_dkdv_tc_kernel(const __grid_constant__ AttnBwdParams p) {
+// dK, dV: one CTA per (128 key rows, key/value head of a block); work items = (query
+// head of the group, 64-query block). MMA order per item w: [S^T(w + 1), dP^T(w + 1)]
+// then dV += P^T(w) dO(w), dK += dS^T(w) Q(w).
+__global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dkdv_tc_kernel(const __grid_constant__ AttnBwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -631,7 +674,7 @@ __global__ void __launch_bounds__(kThreadsTC, 2) attn_bwd_dkdv_tc_kernel(const _
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 6 * kBwdQKVTile);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float2* ldtab = reinterpret_cast<float2*>(smem + 6 * kBwdQKVTile + 256);  // [4 warps][64]
+  float2* ldtab = reinterpret_cast<float2*>(smem + 6 * kBwdQKVTile + 256);  // [8 warps][32]
   const uint32_t bar0 = smem_u32(bars);
   const uint32_t kv_full = bar0, s_full = bar0 + 8 * 5, p_full = bar0 + 8 * 6,
                  o_done = bar0 + 8 * 7, drain = bar0 + 8 * 8;
@@ -655,13 +698,13 @@ __global__ void __launch_bounds__(kThreadsTC, 2) attn_bwd_dkdv_tc_kernel(const _
       mbar_init(qd_empty(st), 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, 4);
+    mbar_init(p_full, 8);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), 256);
     tmem_relinquish();
   }
@@ -673,7 +716,7 @@ __global__ void __launch_bounds__(kThreadsTC, 2) attn_bwd_dkdv_tc_kernel(const _
   auto head_of = [&](int w) { return blk * p.hq + kvl * p.g + w / nqb; };
   int issued = 0;
 
-  if (warp == 4) {
+  if (warp == 8) {
     if (lane == 0) {
       bool ok = true;
       mbar_arrive_expect_tx(kv_full, 2 * kBwdQKVTile);
@@ -696,22 +739,22 @@ __global__ void __launch_bounds__(kThreadsTC, 2) attn_bwd_dkdv_tc_kernel(const _
       if (!ok) record_timeout_attn(p.status);
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(128, 64, 0, 0);
       const uint32_t id_g = idesc_bf16_f32(128, 64, 0, 1);
       bool ok = mbar_wait(kv_full, 0, p.timeout_ns, abort_flag);
-      auto issue_s = [&](int w) -> bool {
+      auto issue_s = [&](int w) -> bool {  // S^T = K Q^T and dP^T = V dO^T of item w
         const int st = w & 1;
         if (!mbar_wait(qd_full(st), (w >> 1) & 1, p.timeout_ns, abort_flag)) return false;
         tc_fence_after();
         const uint32_t q = sQD + st * 2 * kBwdBlk, d = q + kBwdBlk;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // S^T = K Q^T
+        for (int kk = 0; kk < 4; ++kk)
           mma_bf16_ss(tST, sw128_desc(sK + kk * 32, 16u, 1024u), sw128_desc(q + kk * 32, 16u, 1024u),
                       id_s, kk > 0 ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // dP^T = V dO^T
+        for (int kk = 0; kk < 4; ++kk)
           mma_bf16_ss(tdPT, sw128_desc(sV + kk * 32, 16u, 1024u), sw128_desc(d + kk * 32, 16u, 1024u),
                       id_s, kk > 0 ? 1u : 0u);
         mma_commit(s_full);
@@ -724,6 +767,10 @@ __global__ void __launch_bounds__(kThreadsTC, 2) attn_bwd_dkdv_tc_kernel(const _
           break;
         }
         tc_fence_after();
+        if (w + 1 < nw && !issue_s(w + 1)) {
+          ok = false;
+          break;
+        }
         const int st = w & 1;
         const uint32_t q = sQD + st * 2 * kBwdBlk, d = q + kBwdBlk;
 #pragma unroll
@@ -736,14 +783,13 @@ __global__ void __launch_bounds__(kThreadsTC, 2) attn_bwd_dkdv_tc_kernel(const _
                       sw128_desc(q + kk * 2048, 8192u, 1024u), id_g, (w > 0 || kk > 0) ? 1u : 0u);
         mma_commit(o_done);
         mma_commit(qd_empty(st));
-        if (w + 1 < nw) ok = issue_s(w + 1);
       }
       if (!ok) record_timeout_attn(p.status);
     }
     __syncwarp();
   } else {
-    const int r = threadIdx.x, kj = k0 + r;
-    const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;
+    const BwdLane L(warp, lane);
+    const int kj = k0 + L.r;
     const bool valid = kj < p.s;
     bool ok = true;
     auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
@@ -751,46 +797,58 @@ __global__ void __launch_bounds__(kThreadsTC, 2) attn_bwd_dkdv_tc_kernel(const _
       if (lane == 0) w = mbar_wait(bar, parity, p.timeout_ns, abort_flag) ? 1 : 0;
       return __shfl_sync(0xFFFFFFFFu, w, 0) != 0;
     };
+    float2* tab = ldtab + warp * 32;
+    const float4* tab4 = reinterpret_cast<const float4*>(tab);
     for (int w = 0; w < nw; ++w) {
-      if (!wait_all(s_full, w & 1) || (w > 0 && !wait_all(o_done, (w - 1) & 1))) {
+      if (!wait_all(s_full, w & 1)) {
         ok = false;
         break;
       }
-      const int t = head_of(w), qbase = (qb0 + w % nqb) * 64;
-      {  // this warp's copy of the block's (lse, D) pairs
-        const int64_t lrow = (static_cast<int64_t>(b) * p.H + t) * p.s;
-        float2* tab = ldtab + warp * 64;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int q = qbase + c * 32 + lane;
-          tab[c * 32 + lane] = q < p.s ? p.ld[lrow + q] : make_float2(0.0f, 0.0f);
-        }
+      const int t = head_of(w);
+      const int qh = (qb0 + w % nqb) * 64 + L.half * 32;  // this warp's 32 queries
+      {  // the (lse, D) pairs of those queries (the previous item's reads ended at its
+         // __syncwarp)
+        const int q = qh + lane;
+        tab[lane] = q < p.s ? p.ld[(static_cast<int64_t>(b) * p.H + t) * p.s + q]
+                            : make_float2(0.0f, 0.0f);
         __syncwarp();
       }
-      const float4* tab4 = reinterpret_cast<const float4*>(ldtab + warp * 64);
       tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t sv[32], pv[32];
-        tmem_ld32(tST + lanes + c * 32, sv);
-        tmem_ld32(tdPT + lanes + c * 32, pv);
-        tmem_ld_wait();
-        float pr[32], ds[32];
+      uint32_t sv[32], pv[32];
+      tmem_ld32(tST + L.lanes + L.half * 32, sv);
+      tmem_ld32(tdPT + L.lanes + L.half * 32, pv);
+      tmem_ld_wait();
+      float pr[32], ds[32];  // P^T and P^T (dP^T - D); 1 / sqrt(d) applied to dK at the end
+      if (valid && qh + 32 <= p.s && !(p.causal && kj > qh)) {
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float4 l4 = tab4[(c * 32 + i) >> 1];  // pairs of queries i, i + 1
+          const float4 l4 = tab4[i >> 1];
+          pr[i] = ex2_approx(fmaf(__uint_as_float(sv[i]), p.scale_log2, -l4.x));
+          pr[i + 1] = ex2_approx(fmaf(__uint_as_float(sv[i + 1]), p.scale_log2, -l4.z));
+          ds[i] = pr[i] * (__uint_as_float(pv[i]) - l4.y);
+          ds[i + 1] = pr[i + 1] * (__uint_as_float(pv[i + 1]) - l4.w);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float4 l4 = tab4[i >> 1];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int q = qbase + c * 32 + i + e;
+            const int q = qh + i + e;
             const bool live = valid && q < p.s && !(p.causal && kj > q);
             const float l2 = e ? l4.z : l4.x, dq = e ? l4.w : l4.y;
-            pr[i + e] = live ? exp2f(__uint_as_float(sv[i + e]) * p.scale_log2 - l2) : 0.0f;
-            ds[i + e] = pr[i + e] * (__uint_as_float(pv[i + e]) - dq) * p.scale;
+            pr[i + e] = live ? ex2_approx(fmaf(__uint_as_float(sv[i + e]), p.scale_log2, -l2)) : 0.0f;
+            ds[i + e] = pr[i + e] * (__uint_as_float(pv[i + e]) - dq);
           }
         }
-        st_tile_chunk(sPT, r, c, pr);
-        st_tile_chunk(sdST, r, c, ds);
       }
+      // the P^T and dS^T tiles are free once the previous item's dV, dK MMAs completed
+      if (w > 0 && !wait_all(o_done, (w - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      st_tile_chunk(sPT, L.r, L.half, pr);
+      st_tile_chunk(sdST, L.r, L.half, ds);
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -799,23 +857,20 @@ __global__ void __launch_bounds__(kThreadsTC, 2) attn_bwd_dkdv_tc_kernel(const _
     if (ok && (nw == 0 || wait_all(o_done, (nw - 1) & 1))) {
       tc_fence_after();
       __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.dqkv) + (static_cast<int64_t>(row0) + kj) * p.ldq;
+      uint32_t v[32];
+      if (nw > 0) {
+        tmem_ld32(tdV + L.lanes + L.half * 32, v);
+        tmem_ld_wait();
+      } else {
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t v[32];
-        if (nw > 0) {
-          tmem_ld32(tdV + lanes + c * 32, v);
-          tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0u;
-        }
-        if (valid) st_row_bf16(drow + vc + c * 32, v, 1.0f);
-        if (nw > 0) {
-          tmem_ld32(tdK + lanes + c * 32, v);
-          tmem_ld_wait();
-        }
-        if (valid) st_row_bf16(drow + kc + c * 32, v, 1.0f);
+        for (int i = 0; i < 32; ++i) v[i] = 0u;
       }
+      if (valid) st_row_bf16(drow + vc + L.half * 32, v, 1.0f);
+      if (nw > 0) {
+        tmem_ld32(tdK + L.lanes + L.half * 32, v);
+        tmem_ld_wait();
+      }
+      if (valid) st_row_bf16(drow + kc + L.half * 32, v, p.scale);
     } else if (lane == 0) {
       record_timeout_attn(p.status);
     }
@@ -824,21 +879,21 @@ __global__ void __launch_bounds__(kThreadsTC, 2) attn_bwd_dkdv_tc_kernel(const _
   __syncthreads();
   if (*abort_flag) {
     volatile int no_abort = 0;
-    if (warp == 4 && lane == 0) {
+    if (warp == 8 && lane == 0) {
       mbar_wait(kv_full, 0, kDrainNs, &no_abort);
       for (int st = 0; st < 2; ++st) {
         const int n = issued > st ? (issued - 1 - st) / 2 : -1;
         if (n >= 0) mbar_wait(qd_full(st), n & 1, kDrainNs, &no_abort);
       }
     }
-    if (warp == 5 && lane == 0) {
+    if (warp == 9 && lane == 0) {
       mma_commit(drain);
       mbar_wait(drain, 0, kDrainNs, &no_abort);
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 256);
   }
@@ -992,9 +1047,9 @@ tp_status launch_attention_bwd_tc(const void* qkv, const void* o, const float* l
       static_cast<float2*>(ldws), b * s, static_cast<int>(s), heads, ldo);
   const unsigned tiles = static_cast<unsigned>((s + 127) / 128);
   attn_bwd_dkdv_tc_kernel<<<dim3(tiles, static_cast<unsigned>(kv_total), static_cast<unsigned>(b)),
-                            kThreadsTC, kBwdSmemKv, st>>>(p);
+                            kThreadsBwd, kBwdSmemKv, st>>>(p);
   attn_bwd_dq_tc_kernel<<<dim3(tiles, static_cast<unsigned>(heads), static_cast<unsigned>(b)),
-                          kThreadsTC, kBwdSmemDq, st>>>(p);
+                          kThreadsBwd, kBwdSmemDq, st>>>(p);
   count_launch(3);
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;

@@ -807,11 +807,14 @@ def run_gqa(args, w, T, device, rank, nranks):
                      dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
 
-    def step():
+    def step_on(x, dout, out, dx):
         T.tp_gqa_attn_proj_fwd(x, g, be, Wsh, Wo, xn, mean, rstd, qkv, o, lse, out, b, s, h, H,
                                Hkv, N, 0, BF, mode, ws, ws.numel(), stream)
         T.tp_gqa_attn_proj_bwd(x, g, Wsh, Wo, xn, mean, rstd, qkv, o, lse, dout, dx, dg, db, dW,
                                dWo, b, s, h, H, Hkv, N, 0, BF, mode, ws, ws.numel(), stream)
+
+    def step():
+        step_on(x, dout, out, dx)
 
     def timed(fn, steps):
         a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -842,14 +845,9 @@ def run_gqa(args, w, T, device, rank, nranks):
     outp = torch.empty((M, h), dtype=torch.bfloat16, pin_memory=True)
     dxp = torch.empty((M, h), dtype=torch.bfloat16, pin_memory=True)
 
-    def e2e():
-        x.copy_(xp, non_blocking=True)
-        dout.copy_(dp, non_blocking=True)
-        step()
-        outp.copy_(out, non_blocking=True)
-        dxp.copy_(dx, non_blocking=True)
     barrier()
-    e2e_ms = timed(e2e, args.steps)
+    e2e_ms = overlapped_e2e(stream, args.steps, lambda i, o: step_on(i[0], i[1], o[0], o[1]),
+                            [x, dout], [xp, dp], [out, dx], [outp, dxp])
     clk = clocks.stop()
     if T.tp_check_status(stream) != 0:
         raise RuntimeError("device wait timeout: " + T.tp_last_error())
