@@ -7,7 +7,10 @@
 // width, which is why the shard sum precedes it.)
 // Row kernels use one warp per row; the parameter gradients are column sums taken
 // in a fixed order (per-chunk partials, then a second pass over the chunks), so
-// results are deterministic.
+// results are deterministic. When a row is a whole number of 16-byte vectors
+// (h * sizeof(T) % 16 == 0, every buffer 16-byte aligned) the kernels move 16 bytes
+// per lane and access; the row's later passes hit L1 / L2, so x and dy are read from
+// DRAM once. Other widths take the scalar kernels.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -90,8 +93,212 @@ __global__ void __launch_bounds__(32 * kRowWarps) ln_bwd_dx_kernel(
   }
 }
 
+// 16 bytes of T as floats
+template <typename T>
+struct Vec;
+template <>
+struct Vec<float> {
+  static constexpr int N = 4;
+  using Raw = float4;
+  __device__ static void unpack(const Raw& r, float (&f)[4]) {
+    f[0] = r.x;
+    f[1] = r.y;
+    f[2] = r.z;
+    f[3] = r.w;
+  }
+  __device__ static Raw pack(const float (&f)[4]) { return make_float4(f[0], f[1], f[2], f[3]); }
+};
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int N = 8;
+  using Raw = uint4;
+  __device__ static void unpack(const Raw& r, float (&f)[8]) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+  __device__ static Raw pack(const float (&f)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 t = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&t);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+// N consecutive fp32 parameters starting at a multiple of N
+template <int N>
+__device__ __forceinline__ void ld_params(const float* __restrict__ p, int64_t v, float (&f)[N]) {
+  const float4* p4 = reinterpret_cast<const float4*>(p) + v * (N / 4);
+#pragma unroll
+  for (int k = 0; k < N / 4; ++k) {
+    const float4 t = __ldg(p4 + k);
+    f[4 * k] = t.x;
+    f[4 * k + 1] = t.y;
+    f[4 * k + 2] = t.z;
+    f[4 * k + 3] = t.w;
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(32 * kRowWarps) ln_fwd_vec_kernel(
+    const T* __restrict__ x, const float* __restrict__ gamma, const float* __restrict__ beta,
+    T* __restrict__ y, float* mean, float* rstd, int64_t M, int h, float eps) {
+  using V = Vec<T>;
+  constexpr int E = V::N;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= M) return;
+  const int nv = h / E;
+  const typename V::Raw* xr = reinterpret_cast<const typename V::Raw*>(x + row * h);
+  float s = 0.0f;
+#pragma unroll 4
+  for (int v = lane; v < nv; v += 32) {
+    float f[E];
+    V::unpack(xr[v], f);
+#pragma unroll
+    for (int e = 0; e < E; ++e) s += f[e];
+  }
+  const float mu = warp_sum(s) / h;
+  float q = 0.0f;
+#pragma unroll 4
+  for (int v = lane; v < nv; v += 32) {
+    float f[E];
+    V::unpack(xr[v], f);
+#pragma unroll
+    for (int e = 0; e < E; ++e) q += (f[e] - mu) * (f[e] - mu);
+  }
+  const float rs = 1.0f / sqrtf(warp_sum(q) / h + eps);
+  typename V::Raw* yr = reinterpret_cast<typename V::Raw*>(y + row * h);
+#pragma unroll 4
+  for (int v = lane; v < nv; v += 32) {
+    float f[E], g[E], b[E];
+    V::unpack(xr[v], f);
+    ld_params<E>(gamma, v, g);
+    ld_params<E>(beta, v, b);
+#pragma unroll
+    for (int e = 0; e < E; ++e) f[e] = g[e] * ((f[e] - mu) * rs) + b[e];
+    yr[v] = V::pack(f);
+  }
+  if (lane == 0) {
+    if (mean) mean[row] = mu;
+    if (rstd) rstd[row] = rs;
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(32 * kRowWarps) ln_bwd_dx_vec_kernel(
+    const T* __restrict__ x, const float* __restrict__ gamma, const float* __restrict__ mean,
+    const float* __restrict__ rstd, const T* __restrict__ dy, const T* __restrict__ dres,
+    T* __restrict__ dx, int64_t M, int h) {
+  using V = Vec<T>;
+  constexpr int E = V::N;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= M) return;
+  const float mu = mean[row], rs = rstd[row];
+  const int nv = h / E;
+  const typename V::Raw* xr = reinterpret_cast<const typename V::Raw*>(x + row * h);
+  const typename V::Raw* dyr = reinterpret_cast<const typename V::Raw*>(dy + row * h);
+  float s1 = 0.0f, s2 = 0.0f;
+#pragma unroll 4
+  for (int v = lane; v < nv; v += 32) {
+    float a[E], d[E], g[E];
+    V::unpack(xr[v], a);
+    V::unpack(dyr[v], d);
+    ld_params<E>(gamma, v, g);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float gg = d[e] * g[e];
+      s1 += gg;
+      s2 += gg * (a[e] - mu) * rs;
+    }
+  }
+  s1 = warp_sum(s1) / h;
+  s2 = warp_sum(s2) / h;
+  const typename V::Raw* rr = dres ? reinterpret_cast<const typename V::Raw*>(dres + row * h) : nullptr;
+  typename V::Raw* out = reinterpret_cast<typename V::Raw*>(dx + row * h);
+#pragma unroll 4
+  for (int v = lane; v < nv; v += 32) {
+    float a[E], d[E], g[E], r[E];
+    V::unpack(xr[v], a);
+    V::unpack(dyr[v], d);
+    ld_params<E>(gamma, v, g);
+    if (rr) {
+      V::unpack(rr[v], r);
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) r[e] = 0.0f;
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float xh = (a[e] - mu) * rs;
+      a[e] = rs * (d[e] * g[e] - s1 - xh * s2) + r[e];
+    }
+    out[v] = V::pack(a);
+  }
+}
+
 constexpr int kColThreads = 256;
 constexpr int kRowsPerChunk = 64;
+
+// The parameter-gradient partials of one chunk of rows, vectorised: lane j of every
+// warp owns the 16-byte column vector blockIdx.x * 32 + j; warp w sums rows
+// w, w + 8, ... of the chunk in order, then the eight warps' sums are added in warp
+// order (fixed, so deterministic). Same chunking and output as the scalar kernel below.
+template <typename T>
+__global__ void __launch_bounds__(32 * kRowWarps) ln_bwd_param_partial_vec_kernel(
+    const T* __restrict__ x, const float* __restrict__ mean, const float* __restrict__ rstd,
+    const T* __restrict__ dy, float* __restrict__ partial, int64_t M, int h, int64_t rank_rows,
+    int cpr) {
+  using V = Vec<T>;
+  constexpr int E = V::N;
+  __shared__ float red[kRowWarps][32][2 * E + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int v = blockIdx.x * 32 + lane, nv = h / E;
+  const int rank = blockIdx.y / cpr, chunk = blockIdx.y - rank * cpr;
+  const int64_t rank_end = min(M, (rank + 1) * rank_rows);
+  const int64_t r0 = rank * rank_rows + static_cast<int64_t>(chunk) * kRowsPerChunk;
+  const int64_t r1 = min(rank_end, r0 + kRowsPerChunk);
+  float sg[E], sb[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) sg[e] = sb[e] = 0.0f;
+  if (v < nv) {
+#pragma unroll 2
+    for (int64_t r = r0 + warp; r < r1; r += kRowWarps) {
+      float a[E], d[E];
+      V::unpack(reinterpret_cast<const typename V::Raw*>(x + r * h)[v], a);
+      V::unpack(reinterpret_cast<const typename V::Raw*>(dy + r * h)[v], d);
+      const float mu = mean[r], rs = rstd[r];
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        sg[e] += d[e] * (a[e] - mu) * rs;
+        sb[e] += d[e];
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    red[warp][lane][e] = sg[e];
+    red[warp][lane][E + e] = sb[e];
+  }
+  __syncthreads();
+  // thread (warp w, lane j): output element w of the 2E values of column vector j
+  for (int k = warp; k < 2 * E; k += kRowWarps) {
+    float t = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kRowWarps; ++w) t += red[w][lane][k];
+    if (v < nv) {
+      const int e = k < E ? k : k - E;
+      partial[blockIdx.y * 2ll * h + (k < E ? 0 : h) + static_cast<int64_t>(v) * E + e] = t;
+    }
+  }
+}
 
 // partial[chunk][0:h] = sum over the chunk's rows of dy * xhat, partial[chunk][h:2h] = of dy.
 // Rows are grouped by rank (rank r owns rows [r * rank_rows, (r + 1) * rank_rows), one
@@ -118,12 +325,14 @@ __global__ void __launch_bounds__(kColThreads) ln_bwd_param_partial_kernel(
   partial[blockIdx.y * 2ll * h + h + c] = sb;
 }
 
+constexpr int kFinalThreads = 64;  // narrow CTAs: h / 64 of them share the chunk sums
+
 // per rank: the sum of its chunks in order (written to dgamma_ranks / dbeta_ranks
 // (ranks, h) when given); then the sum over the ranks in rank order
-__global__ void __launch_bounds__(kColThreads) ln_bwd_param_final_kernel(
+__global__ void __launch_bounds__(kFinalThreads) ln_bwd_param_final_kernel(
     const float* __restrict__ partial, int ranks, int cpr, int h, float* dgamma, float* dbeta,
     float* dgamma_ranks, float* dbeta_ranks) {
-  const int c = blockIdx.x * kColThreads + threadIdx.x;
+  const int c = blockIdx.x * kFinalThreads + threadIdx.x;
   if (c >= h) return;
   float tg = 0.0f, tb = 0.0f;
   for (int r = 0; r < ranks; ++r) {
@@ -141,12 +350,22 @@ __global__ void __launch_bounds__(kColThreads) ln_bwd_param_final_kernel(
   if (dbeta) dbeta[c] = tb;
 }
 
+// whole 16-byte vectors per row (the buffers themselves are 16-byte aligned)
+template <typename T>
+bool vec_rows(int h) {
+  return (static_cast<int64_t>(h) * sizeof(T)) % 16 == 0;
+}
+
 template <typename T>
 tp_status fwd_t(const void* x, const float* gamma, const float* beta, void* y, float* mean,
                 float* rstd, int64_t M, int h, float eps, cudaStream_t st) {
   const unsigned blocks = static_cast<unsigned>((M + kRowWarps - 1) / kRowWarps);
-  ln_fwd_kernel<T><<<blocks, 32 * kRowWarps, 0, st>>>(static_cast<const T*>(x), gamma, beta,
-                                                       static_cast<T*>(y), mean, rstd, M, h, eps);
+  if (vec_rows<T>(h))
+    ln_fwd_vec_kernel<T><<<blocks, 32 * kRowWarps, 0, st>>>(
+        static_cast<const T*>(x), gamma, beta, static_cast<T*>(y), mean, rstd, M, h, eps);
+  else
+    ln_fwd_kernel<T><<<blocks, 32 * kRowWarps, 0, st>>>(static_cast<const T*>(x), gamma, beta,
+                                                         static_cast<T*>(y), mean, rstd, M, h, eps);
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;
@@ -158,18 +377,31 @@ tp_status bwd_t(const void* x, const float* gamma, const float* mean, const floa
                 float* dgamma_ranks, float* dbeta_ranks, int64_t M, int h, int ranks, float* ws,
                 cudaStream_t st) {
   const unsigned rblocks = static_cast<unsigned>((M + kRowWarps - 1) / kRowWarps);
-  ln_bwd_dx_kernel<T><<<rblocks, 32 * kRowWarps, 0, st>>>(
-      static_cast<const T*>(x), gamma, mean, rstd, static_cast<const T*>(dy),
-      static_cast<const T*>(dres), static_cast<T*>(dx), M, h);
+  const bool vec = vec_rows<T>(h);
+  if (vec)
+    ln_bwd_dx_vec_kernel<T><<<rblocks, 32 * kRowWarps, 0, st>>>(
+        static_cast<const T*>(x), gamma, mean, rstd, static_cast<const T*>(dy),
+        static_cast<const T*>(dres), static_cast<T*>(dx), M, h);
+  else
+    ln_bwd_dx_kernel<T><<<rblocks, 32 * kRowWarps, 0, st>>>(
+        static_cast<const T*>(x), gamma, mean, rstd, static_cast<const T*>(dy),
+        static_cast<const T*>(dres), static_cast<T*>(dx), M, h);
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
   if (!dgamma && !dbeta && !dgamma_ranks && !dbeta_ranks) return TP_OK;
   const int64_t rank_rows = M / ranks;
   const int cpr = static_cast<int>((rank_rows + kRowsPerChunk - 1) / kRowsPerChunk);
-  const dim3 g1((h + kColThreads - 1) / kColThreads, ranks * cpr);
-  ln_bwd_param_partial_kernel<T><<<g1, kColThreads, 0, st>>>(
-      static_cast<const T*>(x), mean, rstd, static_cast<const T*>(dy), ws, M, h, rank_rows, cpr);
-  ln_bwd_param_final_kernel<<<(h + kColThreads - 1) / kColThreads, kColThreads, 0, st>>>(
+  if (vec) {
+    constexpr int cols = 32 * Vec<T>::N;  // columns per CTA
+    const dim3 g1((h + cols - 1) / cols, ranks * cpr);
+    ln_bwd_param_partial_vec_kernel<T><<<g1, 32 * kRowWarps, 0, st>>>(
+        static_cast<const T*>(x), mean, rstd, static_cast<const T*>(dy), ws, M, h, rank_rows, cpr);
+  } else {
+    const dim3 g1((h + kColThreads - 1) / kColThreads, ranks * cpr);
+    ln_bwd_param_partial_kernel<T><<<g1, kColThreads, 0, st>>>(
+        static_cast<const T*>(x), mean, rstd, static_cast<const T*>(dy), ws, M, h, rank_rows, cpr);
+  }
+  ln_bwd_param_final_kernel<<<(h + kFinalThreads - 1) / kFinalThreads, kFinalThreads, 0, st>>>(
       ws, ranks, cpr, h, dgamma, dbeta, dgamma_ranks, dbeta_ranks);
   count_launch(2);
   TP_CUDA_TRY(cudaGetLastError());
