@@ -392,26 +392,33 @@ struct AttnBwdParams {
 };
 
 // ld[b, t, q] = (lse log2(e), D) with D = the sum over the head's 64 columns of dO * O;
-// one warp per (row, head)
+// eight lanes per (row, head), 16 bytes of O and of dO each
 __global__ void __launch_bounds__(256) attn_bwd_dsum_kernel(const __nv_bfloat16* __restrict__ O,
                                                             const __nv_bfloat16* __restrict__ dO,
                                                             const float* __restrict__ lse,
                                                             float2* __restrict__ ld, int64_t rows,
                                                             int s, int H, int64_t ldo) {
-  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (w >= rows * H) return;
-  const int64_t row = w / H;
-  const int t = static_cast<int>(w - row * H);
-  const __nv_bfloat162 o2 =
-      reinterpret_cast<const __nv_bfloat162*>(O + row * ldo + t * 64)[lane];
-  const __nv_bfloat162 d2 =
-      reinterpret_cast<const __nv_bfloat162*>(dO + row * ldo + t * 64)[lane];
-  float acc = __bfloat162float(o2.x) * __bfloat162float(d2.x) +
-              __bfloat162float(o2.y) * __bfloat162float(d2.y);
+  const int64_t gt = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t w = gt >> 3;
+  const int sub = static_cast<int>(gt & 7);
+  const bool live = w < rows * H;  // the whole group of eight agrees
+  const int64_t row = live ? w / H : 0;
+  const int t = live ? static_cast<int>(w - row * H) : 0;
+  float acc = 0.0f;
+  if (live) {
+    const uint4 o4 = *reinterpret_cast<const uint4*>(O + row * ldo + t * 64 + sub * 8);
+    const uint4 d4 = *reinterpret_cast<const uint4*>(dO + row * ldo + t * 64 + sub * 8);
+    const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w}, dw[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
-  if (lane == 0) {
+    for (int i = 0; i < 4; ++i) {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[i]));
+      const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dw[i]));
+      acc = fmaf(a.x, c.x, fmaf(a.y, c.y, acc));
+    }
+  }
+#pragma unroll
+  for (int off = 4; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+  if (live && sub == 0) {
     const int64_t b = row / s, q = row - b * s, i = (b * H + t) * s + q;
     ld[i] = make_float2(lse[i] * 1.4426950408889634f, acc);
   }
@@ -429,18 +436,6 @@ __device__ __forceinline__ void st_row_bf16(__nv_bfloat16* dst, const uint32_t* 
   }
 }
 
-// 32 bf16 values of row r into a 128-byte-row K-major swizzled tile at column chunk 4c..4c+3
-__device__ __forceinline__ void st_tile_chunk(uint32_t tile, int r, int c, const float* x) {
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int ch = c * 4 + u;
-    const uint32_t addr = tile + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4);
-    const float* q8 = x + 8 * u;
-    st_shared_v4(addr, pack_bf16x2(q8[0], q8[1]), pack_bf16x2(q8[2], q8[3]),
-                 pack_bf16x2(q8[4], q8[5]), pack_bf16x2(q8[6], q8[7]));
-  }
-}
-
 constexpr int kThreadsBwd = 320;  // warps 0-7 element-wise, 8 TMA, 9 MMA
 
 // Element-wise warps of the backward kernels: warp w reads TMEM lanes 32 (w % 4) ..
@@ -452,6 +447,17 @@ struct BwdLane {
       : quarter(warp & 3), half(warp >> 2), r((warp & 3) * 32 + lane),
         lanes(static_cast<uint32_t>((warp & 3) * 32) << 16) {}
 };
+
+// 32 bf16 values, packed in pairs (16 words), of row r into the swizzled tile at column
+// half c (16-byte chunks 4c .. 4c + 3)
+__device__ __forceinline__ void st_tile_packed(uint32_t tile, int r, int c, const uint32_t* w) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int ch = c * 4 + u;
+    const uint32_t addr = tile + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4);
+    st_shared_v4(addr, w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+  }
+}
 
 // dQ: one CTA per (128 query rows, query head); keys in blocks of 64.
 // MMA order per block j: [S(j + 1), dP(j + 1)] then dQ(j) += dS(j) K(j), so the
@@ -597,19 +603,28 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dq_tc_kernel(const __
       tmem_ld32(tdP + L.lanes + L.half * 32, pv);
       tmem_ld_wait();
       const int k0 = j * 64 + L.half * 32;
-      float ds[32];  // P (dP - D); the 1 / sqrt(d) is applied to dQ at the end
+      uint32_t dk[16];  // P (dP - D) as packed bf16 pairs; 1 / sqrt(d) applied to dQ at the end
       if (valid && k0 + 32 <= p.s && !(p.causal && k0 + 31 > qi)) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          ds[i] = ex2_approx(fmaf(__uint_as_float(sv[i]), p.scale_log2, -lse2)) *
-                  (__uint_as_float(pv[i]) - Dq);
+        for (int i = 0; i < 32; i += 2)
+          dk[i >> 1] = pack_bf16x2(
+              ex2_approx(fmaf(__uint_as_float(sv[i]), p.scale_log2, -lse2)) *
+                  (__uint_as_float(pv[i]) - Dq),
+              ex2_approx(fmaf(__uint_as_float(sv[i + 1]), p.scale_log2, -lse2)) *
+                  (__uint_as_float(pv[i + 1]) - Dq));
       } else {  // keys beyond the sequence or after the query, rows beyond the sequence
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int key = k0 + i;
-          const bool live = valid && key < p.s && !(p.causal && key > qi);
-          const float pr = live ? ex2_approx(fmaf(__uint_as_float(sv[i]), p.scale_log2, -lse2)) : 0.0f;
-          ds[i] = pr * (__uint_as_float(pv[i]) - Dq);
+        for (int i = 0; i < 32; i += 2) {
+          float ds[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int key = k0 + i + e;
+            const bool live = valid && key < p.s && !(p.causal && key > qi);
+            const float pr =
+                live ? ex2_approx(fmaf(__uint_as_float(sv[i + e]), p.scale_log2, -lse2)) : 0.0f;
+            ds[e] = pr * (__uint_as_float(pv[i + e]) - Dq);
+          }
+          dk[i >> 1] = pack_bf16x2(ds[0], ds[1]);
         }
       }
       // the dS tile is free once the previous block's dQ MMA has completed
@@ -617,7 +632,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dq_tc_kernel(const __
         ok = false;
         break;
       }
-      st_tile_chunk(sdS, L.r, L.half, ds);
+      st_tile_packed(sdS, L.r, L.half, dk);
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -799,56 +814,55 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dkdv_tc_kernel(const 
     };
     float2* tab = ldtab + warp * 32;
     const float4* tab4 = reinterpret_cast<const float4*>(tab);
+    // the (lse, D) pair of this lane's query in item w (this warp's 32 queries); loaded
+    // one item ahead so the global load's latency overlaps the current item
+    auto ld_pair = [&](int w) -> float2 {
+      const int q = (qb0 + w % nqb) * 64 + L.half * 32 + lane;
+      return q < p.s ? p.ld[(static_cast<int64_t>(b) * p.H + head_of(w)) * p.s + q]
+                     : make_float2(0.0f, 0.0f);
+    };
+    float2 ld_next = nw > 0 ? ld_pair(0) : make_float2(0.0f, 0.0f);
     for (int w = 0; w < nw; ++w) {
       if (!wait_all(s_full, w & 1)) {
         ok = false;
         break;
       }
-      const int t = head_of(w);
       const int qh = (qb0 + w % nqb) * 64 + L.half * 32;  // this warp's 32 queries
-      {  // the (lse, D) pairs of those queries (the previous item's reads ended at its
-         // __syncwarp)
-        const int q = qh + lane;
-        tab[lane] = q < p.s ? p.ld[(static_cast<int64_t>(b) * p.H + t) * p.s + q]
-                            : make_float2(0.0f, 0.0f);
-        __syncwarp();
-      }
+      tab[lane] = ld_next;  // the previous item's reads of the table ended at its __syncwarp
+      __syncwarp();
+      if (w + 1 < nw) ld_next = ld_pair(w + 1);
       tc_fence_after();
       uint32_t sv[32], pv[32];
       tmem_ld32(tST + L.lanes + L.half * 32, sv);
       tmem_ld32(tdPT + L.lanes + L.half * 32, pv);
       tmem_ld_wait();
-      float pr[32], ds[32];  // P^T and P^T (dP^T - D); 1 / sqrt(d) applied to dK at the end
-      if (valid && qh + 32 <= p.s && !(p.causal && kj > qh)) {
+      // P^T and P^T (dP^T - D) as packed bf16 pairs; 1 / sqrt(d) applied to dK at the end
+      uint32_t pk[16], dk[16];
+      // one loop for full and masked items (two specialised loops exceed the register
+      // budget of two 320-thread CTAs per SM)
+      const bool full = valid && qh + 32 <= p.s && !(p.causal && kj > qh);
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float4 l4 = tab4[i >> 1];
-          pr[i] = ex2_approx(fmaf(__uint_as_float(sv[i]), p.scale_log2, -l4.x));
-          pr[i + 1] = ex2_approx(fmaf(__uint_as_float(sv[i + 1]), p.scale_log2, -l4.z));
-          ds[i] = pr[i] * (__uint_as_float(pv[i]) - l4.y);
-          ds[i + 1] = pr[i + 1] * (__uint_as_float(pv[i + 1]) - l4.w);
+      for (int i = 0; i < 32; i += 2) {
+        const float4 l4 = tab4[i >> 1];  // (lse, D) of queries qh + i, qh + i + 1
+        float pr[2], ds[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int q = qh + i + e;
+          const bool live = full || (valid && q < p.s && !(p.causal && kj > q));
+          const float l2 = e ? l4.z : l4.x, dq = e ? l4.w : l4.y;
+          pr[e] = live ? ex2_approx(fmaf(__uint_as_float(sv[i + e]), p.scale_log2, -l2)) : 0.0f;
+          ds[e] = pr[e] * (__uint_as_float(pv[i + e]) - dq);
         }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float4 l4 = tab4[i >> 1];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int q = qh + i + e;
-            const bool live = valid && q < p.s && !(p.causal && kj > q);
-            const float l2 = e ? l4.z : l4.x, dq = e ? l4.w : l4.y;
-            pr[i + e] = live ? ex2_approx(fmaf(__uint_as_float(sv[i + e]), p.scale_log2, -l2)) : 0.0f;
-            ds[i + e] = pr[i + e] * (__uint_as_float(pv[i + e]) - dq);
-          }
-        }
+        pk[i >> 1] = pack_bf16x2(pr[0], pr[1]);
+        dk[i >> 1] = pack_bf16x2(ds[0], ds[1]);
       }
       // the P^T and dS^T tiles are free once the previous item's dV, dK MMAs completed
       if (w > 0 && !wait_all(o_done, (w - 1) & 1)) {
         ok = false;
         break;
       }
-      st_tile_chunk(sPT, L.r, L.half, pr);
-      st_tile_chunk(sdST, L.r, L.half, ds);
+      st_tile_packed(sPT, L.r, L.half, pk);
+      st_tile_packed(sdST, L.r, L.half, dk);
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -1042,7 +1056,7 @@ tp_status launch_attention_bwd_tc(const void* qkv, const void* o, const float* l
     mark_device(attr_set);
   }
   const int64_t pairs = b * s * heads;
-  attn_bwd_dsum_kernel<<<static_cast<unsigned>((pairs * 32 + 255) / 256), 256, 0, st>>>(
+  attn_bwd_dsum_kernel<<<static_cast<unsigned>((pairs * 8 + 255) / 256), 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse,
       static_cast<float2*>(ldws), b * s, static_cast<int>(s), heads, ldo);
   const unsigned tiles = static_cast<unsigned>((s + 127) / 128);

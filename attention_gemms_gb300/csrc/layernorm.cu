@@ -337,6 +337,7 @@ __global__ void __launch_bounds__(kFinalThreads) ln_bwd_param_final_kernel(
   float tg = 0.0f, tb = 0.0f;
   for (int r = 0; r < ranks; ++r) {
     float sg = 0.0f, sb = 0.0f;
+#pragma unroll 8
     for (int k = r * cpr; k < (r + 1) * cpr; ++k) {
       sg += partial[k * 2ll * h + c];
       sb += partial[k * 2ll * h + h + c];

@@ -92,6 +92,9 @@ def col_gemm_flops(w):
 COL_GEMM_TRAFFIC = {
     "c5": {"bytes": 12.08e9 + 1.40e9, "src": "1c417b636733cb5a"},
     "c3": {"bytes": 1.10e9 + 509.49e6, "src": "1c417b636733cb5a"},
+    # the GQA line's roofline launch: the dO GEMM (2048 x 2048 x 2048) through tp_gemm;
+    # its 8.4 MB output is still in L2 when the launch ends, so no DRAM write is counted
+    "gqa-dO": {"bytes": 16.82e6 + 0.0, "src": "1c417b636733cb5a"},
 }
 
 
@@ -775,8 +778,11 @@ def gqa_flops(w):
 
 
 def run_gqa(args, w, T, device, rank, nranks):
-    """The head-sharded GQA block, forward + backward per step; the attention core on
-    the sharded qkv (CUDA cores, fp32 arithmetic) is timed alone for its roofline."""
+    """The head-sharded GQA block, forward + backward per step. The dominant kernel of
+    the step is the pair GEMM (four 2048-wide launches: W_o forward, dO, dW_o, dx_n);
+    its roofline is taken on the dO GEMM (M x h x h) timed alone through tp_gemm. The
+    tensor-core attention core (forward, and backward with its scratch) is timed alone
+    as well and reported under "attention"."""
     import torch
     from attention_gemms_gb300 import synth
     b, s, h, H, Hkv, N = w["b"], w["s"], w["h"], w["heads"], w["kv_heads"], w["N"]
@@ -838,6 +844,13 @@ def run_gqa(args, w, T, device, rank, nranks):
     launches = T.tp_launch_count() - n0
     attn_ms = timed(lambda: T.tp_gqa_attention_fwd(qkv, o, lse, b, s, h, H, Hkv, N, 0, BF, stream),
                     args.steps)
+    dO_t, dqkv_t = e(M, h), e(M, Wc)
+    dO_t.copy_(dout)
+    awsb = T.tp_gqa_attention_bwd_workspace_size(b, s, H)
+    aws = torch.empty(awsb, dtype=torch.uint8, device=device)
+    attn_bwd_ms = timed(lambda: T.tp_gqa_attention_bwd(qkv, o, lse, dO_t, dqkv_t, b, s, h, H, Hkv,
+                                                       N, 0, BF, aws, awsb, stream), args.steps)
+    gemm_ms = timed(lambda: T.tp_gemm(dout, Wo, dO_t, M, h, h, 0, 1, BF, stream), args.steps)
     xp = torch.empty((M, h), dtype=torch.bfloat16, pin_memory=True)
     dp = torch.empty((M, h), dtype=torch.bfloat16, pin_memory=True)
     xp.copy_(x)
@@ -853,8 +866,13 @@ def run_gqa(args, w, T, device, rank, nranks):
         raise RuntimeError("device wait timeout: " + T.tp_last_error())
     ms_max, e2e_max = max_over_ranks(ms, device), max_over_ranks(e2e_ms, device)
     attn_max = max_over_ranks(attn_ms, device)
+    attn_bwd_max = max_over_ranks(attn_bwd_ms, device)
+    gemm_max = max_over_ranks(gemm_ms, device)
     total, attn_fwd = gqa_flops(w)
     attn_tf = attn_fwd / (attn_max * 1e-3) / 1e12
+    attn_bwd_tf = 2.0 * attn_fwd / (attn_bwd_max * 1e-3) / 1e12
+    gemm_flops = 2.0 * M * h * h
+    gemm_tf = gemm_flops / (gemm_max * 1e-3) / 1e12
     peaks, src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     res = {
@@ -869,13 +887,23 @@ def run_gqa(args, w, T, device, rank, nranks):
                    "qkv_columns_unreplicated": (H + 2 * Hkv) * d, "shard_sum": args.mode,
                    "parallelism": f"tp{N} virtual ranks per GPU, dp{nranks}",
                    "l2": "activations larger than L2 (no flush)"},
-        "roofline": {"bound": "tensor", "kernel": "attn_fwd_tc_kernel (tcgen05 attention forward: "
-                     "S = Q K^T and O += P V in TMEM, online softmax), timed on its own",
-                     "achieved": round(attn_tf, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(attn_tf / peak, 4),
+        "roofline": {"bound": "tensor", "kernel": "gemm_tc2_kernel (pair tcgen05 GEMM, 256 x 256 "
+                     "tiles on CTA pairs; 43 % of the step's GPU time, its four 2048-wide "
+                     "launches 26 %), timed on its own as the dO GEMM "
+                     f"(M {M} x N {h} x K {h}) through tp_gemm",
+                     "achieved": round(gemm_tf, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(gemm_tf / peak, 4),
                      "peak_source": f"{src} bf16 dense (burst)",
-                     "traffic": None, "algorithmic_flops_per_launch": attn_fwd,
-                     "avg_launch_ms": round(attn_max, 4)},
+                     "traffic": col_gemm_traffic("gqa-dO"),
+                     "algorithmic_flops_per_launch": gemm_flops,
+                     "avg_launch_ms": round(gemm_max, 4)},
+        "attention": {"kernels": "attn_fwd_tc_kernel; attn_bwd_dsum_kernel + attn_bwd_dkdv_tc_kernel "
+                      "+ attn_bwd_dq_tc_kernel (tcgen05, bf16 head_dim 64), each pass timed on "
+                      "its own, non-causal",
+                      "fwd_tflops": round(attn_tf, 2), "fwd_frac": round(attn_tf / peak, 4),
+                      "fwd_ms": round(attn_max, 4), "bwd_tflops": round(attn_bwd_tf, 2),
+                      "bwd_frac": round(attn_bwd_tf / peak, 4), "bwd_ms": round(attn_bwd_max, 4),
+                      "flops": {"fwd": attn_fwd, "bwd": 2.0 * attn_fwd}},
         "e2e": {"value": round(total * nranks / (e2e_max * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": 2 * M * h * 2, "d2h_bytes_per_step": 2 * M * h * 2,
                 "ms_per_step": round(e2e_max, 4)},
