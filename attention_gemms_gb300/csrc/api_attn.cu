@@ -180,6 +180,9 @@ tp_status tp_attn_proj_bwd(const void* x, const float* gamma, const void* Wqkv, 
   void* lnws = w;
   w += a256(layernorm_bwd_ws_bytes(M, h));
   void* ldws = w;
+  // The weight gradients are off the critical path: dW_o runs on a side stream beside
+  // dO and the attention backward, dW_qkv beside dx_n and the LayerNorm backward.
+  SideBranch br(st);
 
   // dWo_i = O_i^T dout (row-parallel weight gradient; row block i of W_o)
   {
@@ -198,7 +201,7 @@ tp_status tp_attn_proj_bwd(const void* x, const float* gamma, const void* Wqkv, 
     d.out_f32 = dtype == TP_F32;
     d.shards = N;
     d.shard_axis = 0;
-    TP_TRY(launch_gemm(d, st));
+    TP_TRY(launch_gemm(d, br.stream()));
   }
   // dO_i = dout W_o,i^T (g-backward is the identity: every shard reads all of dout)
   {
@@ -218,7 +221,8 @@ tp_status tp_attn_proj_bwd(const void* x, const float* gamma, const void* Wqkv, 
     TP_TRY(launch_gemm(d, st));
   }
   TP_TRY(launch_attention_bwd(qkv, o, lse, dO, dqkv, ldws, b, s, h, n_heads, causal, dtype, st));
-  // dW_qkv = xn^T dQKV (column-parallel weight gradient)
+  // dW_qkv = xn^T dQKV (column-parallel weight gradient), once dQKV is complete
+  TP_TRY(br.fork());
   {
     GemmDesc d;
     d.dtype = dtype;
@@ -233,7 +237,7 @@ tp_status tp_attn_proj_bwd(const void* x, const float* gamma, const void* Wqkv, 
     d.epi = EPI_STORE;
     d.out[0] = dWqkv;
     d.out_f32 = dtype == TP_F32;
-    TP_TRY(launch_gemm(d, st));
+    TP_TRY(launch_gemm(d, br.stream()));
   }
   // f-backward: dxn = sum_i dQKV_i W_qkv,i^T. Shard i's K range is its heads' columns
   // of the Q, K and V blocks: three K segments at offsets 0, h, 2h.
@@ -269,8 +273,9 @@ tp_status tp_attn_proj_bwd(const void* x, const float* gamma, const void* Wqkv, 
     }
   }
   // LN backward plus the residual branch: dx = dout + LN'(dxn)
-  return launch_layernorm_bwd(x, gamma, mean, rstd, dxn, dout, dx, dgamma, dbeta, M, h, lnws,
-                              dtype, st);
+  TP_TRY(launch_layernorm_bwd(x, gamma, mean, rstd, dxn, dout, dx, dgamma, dbeta, M, h, lnws,
+                              dtype, st));
+  return br.join();
 }
 
 tp_status tp_layer_fwd(const void* x, const tp_layer_weights* w, const tp_layer_saved* sv,

@@ -345,6 +345,10 @@ tp_status tp_gqa_attn_proj_bwd(const void* x, const float* gamma, const void* Wq
   void* lnws = w;
   w += a256(layernorm_bwd_ws_bytes(M, h));
   void* ldws = w;  // attention (lse, D) pairs
+  // The weight gradients are off the critical path: dW_o runs on a side stream beside
+  // dO and the attention backward, dW_qkv and the replicas' sum beside dx_n and the
+  // LayerNorm backward.
+  SideBranch br(st);
   {  // dW_o,i = O_i^T dout
     GemmDesc d;
     d.dtype = dtype;
@@ -361,7 +365,7 @@ tp_status tp_gqa_attn_proj_bwd(const void* x, const float* gamma, const void* Wq
     d.out_f32 = dtype == TP_F32;
     d.shards = N;
     d.shard_axis = 0;
-    TP_TRY(launch_gemm(d, st));
+    TP_TRY(launch_gemm(d, br.stream()));
   }
   {  // dO_i = dout W_o,i^T (every shard reads all of dout)
     GemmDesc d;
@@ -381,6 +385,7 @@ tp_status tp_gqa_attn_proj_bwd(const void* x, const float* gamma, const void* Wq
   }
   TP_TRY(launch_gqa_attention_bwd(qkv, o, lse, dO, dqkv, ldws, b, s, n_heads, n_kv_heads, N,
                                   static_cast<int>(g.d), causal, dtype, st));
+  TP_TRY(br.fork());  // dQKV is complete
   {  // dWqkv = xn^T dQKV (each block: its shard's gradient, replicas' partial K/V)
     GemmDesc d;
     d.dtype = dtype;
@@ -395,7 +400,7 @@ tp_status tp_gqa_attn_proj_bwd(const void* x, const float* gamma, const void* Wq
     d.epi = EPI_STORE;
     d.out[0] = dWqkv;
     d.out_f32 = dtype == TP_F32;
-    TP_TRY(launch_gemm(d, st));
+    TP_TRY(launch_gemm(d, br.stream()));
   }
   if (g.r > 1) {  // all-reduce among each key/value head's replicas
     // d, S and W are multiples of 16 columns (head_dim 16, 32 or 64) and dWqkv is
@@ -404,18 +409,18 @@ tp_status tp_gqa_attn_proj_bwd(const void* x, const float* gamma, const void* Wq
     const bool vec = g.d % E == 0 && g.S % E == 0 && g.W % E == 0;
     const unsigned grid = grid_for(h * n_kv_heads * 2 * g.d / (vec ? E : 1));
     if (dtype == TP_BF16 && vec)
-      gqa_replica_sum_vec_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
+      gqa_replica_sum_vec_kernel<__nv_bfloat16><<<grid, 256, 0, br.stream()>>>(
           static_cast<__nv_bfloat16*>(dWqkv), h, n_kv_heads, g.hq, g.r, static_cast<int>(g.d),
           g.S, g.W);
     else if (dtype == TP_BF16)
-      gqa_replica_sum_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
+      gqa_replica_sum_kernel<__nv_bfloat16><<<grid, 256, 0, br.stream()>>>(
           static_cast<__nv_bfloat16*>(dWqkv), h, n_kv_heads, g.hq, g.r, static_cast<int>(g.d),
           g.S, g.W);
     else if (vec)
-      gqa_replica_sum_vec_kernel<float><<<grid, 256, 0, st>>>(
+      gqa_replica_sum_vec_kernel<float><<<grid, 256, 0, br.stream()>>>(
           static_cast<float*>(dWqkv), h, n_kv_heads, g.hq, g.r, static_cast<int>(g.d), g.S, g.W);
     else
-      gqa_replica_sum_kernel<float><<<grid, 256, 0, st>>>(
+      gqa_replica_sum_kernel<float><<<grid, 256, 0, br.stream()>>>(
           static_cast<float*>(dWqkv), h, n_kv_heads, g.hq, g.r, static_cast<int>(g.d), g.S, g.W);
     count_launch();
     TP_CUDA_TRY(cudaGetLastError());
@@ -445,8 +450,9 @@ tp_status tp_gqa_attn_proj_bwd(const void* x, const float* gamma, const void* Wq
                                  st));
     }
   }
-  return launch_layernorm_bwd(x, gamma, mean, rstd, dxn, dout, dx, dgamma, dbeta, M, h, lnws,
-                              dtype, st);
+  TP_TRY(launch_layernorm_bwd(x, gamma, mean, rstd, dxn, dout, dx, dgamma, dbeta, M, h, lnws,
+                              dtype, st));
+  return br.join();
 }
 
 }  // extern "C"

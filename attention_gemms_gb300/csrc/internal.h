@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <mutex>
 #include <cstddef>
 #include <cstdint>
 #include <initializer_list>
@@ -50,6 +51,31 @@ inline bool needs_setup(const std::atomic<uint64_t>& done) {
 }
 inline void mark_device(std::atomic<uint64_t>& done) { done.fetch_or(device_bit()); }
 void count_launch(int n = 1);
+
+// An independent branch of one library call on a per-device side stream: the
+// constructor forks it off `main` (an event recorded on `main`, waited for by the side
+// stream), fork() re-forks it at a later point of `main`, join() makes `main` wait for
+// everything enqueued on stream() (the destructor joins when the caller did not). A
+// recursive mutex per device is held from construction to the join, so branches of
+// concurrent calls do not interleave on the shared stream (a nested branch on the same
+// thread shares it and only adds ordering). While `main` is being captured into a
+// graph before the side stream exists, or if it cannot be created, stream() is `main`
+// and the branch runs in order.
+class SideBranch {
+ public:
+  explicit SideBranch(cudaStream_t main);
+  ~SideBranch();
+  SideBranch(const SideBranch&) = delete;
+  SideBranch& operator=(const SideBranch&) = delete;
+  cudaStream_t stream() const;
+  tp_status fork();
+  tp_status join();
+
+ private:
+  cudaStream_t main_;
+  void* side_ = nullptr;
+  std::unique_lock<std::recursive_mutex> lock_;
+};
 
 // ------------------------------------------------------------------ GEMM problem
 

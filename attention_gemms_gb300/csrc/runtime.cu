@@ -1,6 +1,6 @@
 // Runtime plumbing of libtpmlp: thread-local error detail, the per-device sticky
-// status word that bounded device waits report into, the wait limit, SM counts
-// and the launch counter.
+// status word that bounded device waits report into, the wait limit, SM counts,
+// the launch counter and the per-device side stream of SideBranch.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -23,7 +23,71 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int* g_status_ptr[kMaxDevices] = {};
 int g_sm_count[kMaxDevices] = {};
+
+struct Side {
+  std::recursive_mutex mu;  // held from a branch's fork to its join (nesting allowed)
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool ready = false, failed = false;
+};
+Side g_side[kMaxDevices];
 }  // namespace
+
+SideBranch::SideBranch(cudaStream_t main) : main_(main) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return;
+  Side& sd = g_side[dev];
+  std::unique_lock<std::recursive_mutex> lk(sd.mu);
+  if (!sd.ready) {
+    // created outside stream capture only; while the caller's stream is being captured
+    // (or after a failed creation) the branch runs on the caller's stream
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (sd.failed || cudaStreamIsCapturing(main, &cs) != cudaSuccess ||
+        cs != cudaStreamCaptureStatusNone)
+      return;
+    if (cudaStreamCreateWithFlags(&sd.stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) != cudaSuccess) {
+      sd.failed = true;
+      cudaGetLastError();
+      return;
+    }
+    sd.ready = true;
+  }
+  side_ = &sd;
+  lock_ = std::move(lk);
+  if (fork() != TP_OK) {  // a failed fork: run on the caller's stream instead
+    side_ = nullptr;
+    lock_ = std::unique_lock<std::recursive_mutex>();
+  }
+}
+
+cudaStream_t SideBranch::stream() const {
+  return side_ ? static_cast<Side*>(side_)->stream : main_;
+}
+
+tp_status SideBranch::fork() {
+  if (!side_) return TP_OK;
+  Side& sd = *static_cast<Side*>(side_);
+  TP_CUDA_TRY(cudaEventRecord(sd.fork, main_));
+  TP_CUDA_TRY(cudaStreamWaitEvent(sd.stream, sd.fork, 0));
+  return TP_OK;
+}
+
+tp_status SideBranch::join() {
+  if (!side_) return TP_OK;
+  Side& sd = *static_cast<Side*>(side_);
+  side_ = nullptr;
+  const cudaError_t a = cudaEventRecord(sd.join, sd.stream);
+  const cudaError_t b = a == cudaSuccess ? cudaStreamWaitEvent(main_, sd.join, 0) : a;
+  lock_ = std::unique_lock<std::recursive_mutex>();
+  if (b != cudaSuccess) return cuda_fail(b, "joining the side stream");
+  return TP_OK;
+}
+
+SideBranch::~SideBranch() {
+  if (side_) join();
+}
 
 void set_error(const std::string& msg) { t_err = msg; }
 

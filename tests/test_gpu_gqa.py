@@ -146,3 +146,61 @@ def test_gqa_shape_errors():
         T.tp_gqa_attn_proj_fwd(t, g, g, t, t, t, g, g, t, t, g, t, 1, 4, 256, 8, 2, 8, 0,
                                T.DType.BF16, T.Reduce.SPLITK, None, 0)
     assert e.value.status == T.Status.SHAPE
+
+
+def test_gqa_block_graph_replay_matches_eager():
+    """The backward runs its weight gradients on a side stream forked from and joined
+    back to the caller's stream with events. Captured into a CUDA graph (after an eager
+    call created that stream) and replayed, the block gives the eager call's outputs
+    bit for bit, and so does a second eager call."""
+    b, s, h, H, Hkv, N = 2, 200, 512, 8, 2, 4          # head_dim 64, replicated K/V heads
+    BF, md = T.DType.BF16, T.Reduce.BUFFERS
+    d, M, W = h // H, b * s, T.tp_gqa_qkv_cols(h, H, Hkv, N)
+    _, x = tensor((M, h), 6301)
+    g = torch.ones(h, device="cuda")
+    be = torch.zeros(h, device="cuda")
+    sig = 1.0 / np.sqrt(h)
+    _, Wq = tensor((h, H * d), 6302, sig)
+    _, Wk = tensor((h, Hkv * d), 6303, sig)
+    _, Wv = tensor((h, Hkv * d), 6304, sig)
+    _, Wo = tensor((h, h), 6305, sig)
+    _, dout = tensor((M, h), 6306)
+    e = lambda *sh, dty=torch.bfloat16: torch.zeros(sh, dtype=dty, device="cuda")
+    f32 = torch.float32
+    Wsh = e(h, W)
+    T.tp_gqa_pack_qkv(Wq, Wk, Wv, Wsh, h, H, Hkv, N, BF)
+    ws = torch.empty(max(T.tp_gqa_workspace_size(1, M, h, H, Hkv, N, BF, md),
+                         T.tp_gqa_workspace_size(0, M, h, H, Hkv, N, BF, md)),
+                     dtype=torch.uint8, device="cuda")
+    outs = dict(xn=e(M, h), mean=e(M, dty=f32), rstd=e(M, dty=f32), qkv=e(M, W), o=e(M, h),
+                lse=e(b, H, s, dty=f32), out=e(M, h), dx=e(M, h), dg=e(h, dty=f32),
+                db=e(h, dty=f32), dW=e(h, W), dWo=e(h, h))
+
+    def step(stream):
+        q = outs
+        T.tp_gqa_attn_proj_fwd(x, g, be, Wsh, Wo, q["xn"], q["mean"], q["rstd"], q["qkv"], q["o"],
+                               q["lse"], q["out"], b, s, h, H, Hkv, N, 0, BF, md, ws, ws.numel(),
+                               stream)
+        T.tp_gqa_attn_proj_bwd(x, g, Wsh, Wo, q["xn"], q["mean"], q["rstd"], q["qkv"], q["o"],
+                               q["lse"], dout, q["dx"], q["dg"], q["db"], q["dW"], q["dWo"], b, s,
+                               h, H, Hkv, N, 0, BF, md, ws, ws.numel(), stream)
+
+    step(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    ref = {k: v.clone() for k, v in outs.items()}
+    for v in outs.values():
+        v.zero_()
+    step(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    for k in outs:
+        assert torch.equal(outs[k], ref[k]), k
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(torch.cuda.current_stream())
+    for v in outs.values():
+        v.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert T.tp_check_status() == 0
+    for k in outs:
+        assert torch.equal(outs[k], ref[k]), k
