@@ -1060,12 +1060,19 @@ tp_status launch_attention_bwd_tc(const void* qkv, const void* o, const float* l
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse,
       static_cast<float2*>(ldws), b * s, static_cast<int>(s), heads, ldo);
   const unsigned tiles = static_cast<unsigned>((s + 127) / 128);
+  // dQ and dK/dV are independent: dQ runs on a side stream beside dK/dV, whose grid
+  // (one CTA per 128 key rows of a key/value head) often leaves CTA slots free
+  SideBranch br(st, 1);
+  attn_bwd_dq_tc_kernel<<<dim3(tiles, static_cast<unsigned>(heads), static_cast<unsigned>(b)),
+                          kThreadsBwd, kBwdSmemDq, br.stream()>>>(p);
+  const cudaError_t e1 = cudaGetLastError();
   attn_bwd_dkdv_tc_kernel<<<dim3(tiles, static_cast<unsigned>(kv_total), static_cast<unsigned>(b)),
                             kThreadsBwd, kBwdSmemKv, st>>>(p);
-  attn_bwd_dq_tc_kernel<<<dim3(tiles, static_cast<unsigned>(heads), static_cast<unsigned>(b)),
-                          kThreadsBwd, kBwdSmemDq, st>>>(p);
   count_launch(3);
-  TP_CUDA_TRY(cudaGetLastError());
+  const cudaError_t e2 = cudaGetLastError();
+  TP_TRY(br.join());
+  if (e1 != cudaSuccess) return cuda_fail(e1, "attn_bwd_dq_tc_kernel launch");
+  TP_CUDA_TRY(e2);
   return TP_OK;
 }
 

@@ -60,10 +60,12 @@ void count_launch(int n = 1);
 // concurrent calls do not interleave on the shared stream (a nested branch on the same
 // thread shares it and only adds ordering). While `main` is being captured into a
 // graph before the side stream exists, or if it cannot be created, stream() is `main`
-// and the branch runs in order.
+// and the branch runs in order. Slots are separate side streams, for branches that may
+// nest (the attention backward's inside the attention block's).
 class SideBranch {
  public:
-  explicit SideBranch(cudaStream_t main);
+  static constexpr int kSlots = 2;
+  explicit SideBranch(cudaStream_t main, int slot = 0);
   ~SideBranch();
   SideBranch(const SideBranch&) = delete;
   SideBranch& operator=(const SideBranch&) = delete;

@@ -30,13 +30,15 @@ struct Side {
   cudaEvent_t fork = nullptr, join = nullptr;
   bool ready = false, failed = false;
 };
-Side g_side[kMaxDevices];
+Side g_side[kMaxDevices][SideBranch::kSlots];
 }  // namespace
 
-SideBranch::SideBranch(cudaStream_t main) : main_(main) {
+SideBranch::SideBranch(cudaStream_t main, int slot) : main_(main) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return;
-  Side& sd = g_side[dev];
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || slot < 0 ||
+      slot >= kSlots)
+    return;
+  Side& sd = g_side[dev][slot];
   std::unique_lock<std::recursive_mutex> lk(sd.mu);
   if (!sd.ready) {
     // created outside stream capture only; while the caller's stream is being captured
