@@ -1,6 +1,10 @@
 // fp32 GEMM engine on CUDA cores (FFMA, no TF32: TF32's 10-bit mantissa would not
 // hold the fp32 path to 1e-5). Same problem descriptor and epilogues as the
-// tensor-core engine; 64 x 64 output tile per CTA, 4 x 4 per thread, K in steps of 16.
+// tensor-core engine; 64 x 64 output tile per CTA, 4 x 4 per thread, K in steps of 32.
+// Each thread gathers a whole K step of A and B into registers before storing it to
+// shared memory, and the next step's loads are issued before the current step's FMAs,
+// so one load latency per step is hidden behind the arithmetic instead of several
+// being paid in a row (the small fp32 GEMMs are latency-bound).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -11,7 +15,8 @@
 namespace tp {
 namespace {
 
-constexpr int TM = 64, TN = 64, TK = 16;
+constexpr int TM = 64, TN = 64, TK = 32;
+constexpr int kPer = TM * TK / 256;  // elements of A (and of each B) per thread per K step
 
 struct SimtParams {
   const float* A[3];
@@ -54,58 +59,85 @@ __device__ __forceinline__ void epi1(const SimtParams& p, int g, int64_t r, int6
 
 template <int EPI, bool PAIRED>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(const SimtParams p) {
+  constexpr int NB = PAIRED ? 2 : 1;
   __shared__ float As[TK][TM + 4];
-  __shared__ float Bs[PAIRED ? 2 : 1][TK][TN + 4];
+  __shared__ float Bs[NB][TK][TN + 4];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int64_t m0 = static_cast<int64_t>(blockIdx.y) * TM;
   const int64_t n0 = static_cast<int64_t>(blockIdx.x) * TN;
   const int g = blockIdx.z;
   float acc[4][4] = {}, acc2[4][4] = {};
-  for (int s = 0; s < p.nseg; ++s) {
+  float ra[kPer], rb[NB][kPer];
+  // element e of a step: consecutive threads walk the contiguous storage dimension
+  auto a_idx = [&](int e, int& mm, int& kk) {
+    mm = p.a_mn ? e % TM : e / TK;
+    kk = p.a_mn ? e / TM : e % TK;
+  };
+  auto b_idx = [&](int e, int& nn, int& kk) {
+    nn = p.b_mn ? e % TN : e / TK;
+    kk = p.b_mn ? e / TN : e % TK;
+  };
+  auto load = [&](int s, int64_t k0) {  // one K step of segment s: global -> registers
     const float* A = p.A[s];
     const int64_t lda = p.lda[s];
-    for (int64_t k0 = 0; k0 < p.K; k0 += TK) {
-      for (int e = threadIdx.x; e < TM * TK; e += 256) {
-        // consecutive threads walk the contiguous storage dimension
-        const int mm = p.a_mn ? e % TM : e / TK;
-        const int kk = p.a_mn ? e / TM : e % TK;
-        const int64_t gm = m0 + mm, lk = k0 + kk, gk = p.k0[s] + g * p.K + lk;
-        float v = 0.0f;
-        if (gm < p.M && lk < p.K) v = p.a_mn ? A[gk * lda + gm] : A[gm * lda + gk];
-        As[kk][mm] = v;
-      }
-      for (int h = 0; h < (PAIRED ? 2 : 1); ++h) {
-        const float* B = p.B[PAIRED ? h : s];
-        const int64_t ldb = p.ldb[PAIRED ? h : s];
-        for (int e = threadIdx.x; e < TN * TK; e += 256) {
-          const int nn = p.b_mn ? e % TN : e / TK;
-          const int kk = p.b_mn ? e / TN : e % TK;
-          const int64_t gn = n0 + nn, lk = k0 + kk, gk = p.k0[s] + g * p.K + lk;
-          float v = 0.0f;
-          if (gn < p.N && lk < p.K) v = p.b_mn ? B[gk * ldb + gn] : B[gn * ldb + gk];
-          Bs[h][kk][nn] = v;
-        }
-      }
-      __syncthreads();
 #pragma unroll
-      for (int kk = 0; kk < TK; ++kk) {
-        float a[4], b[4], b2[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          a[i] = As[kk][ty * 4 + i];
-          b[i] = Bs[0][kk][tx * 4 + i];
-          if constexpr (PAIRED) b2[i] = Bs[PAIRED ? 1 : 0][kk][tx * 4 + i];
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-            if constexpr (PAIRED) acc2[i][j] = fmaf(a[i], b2[j], acc2[i][j]);
-          }
-      }
-      __syncthreads();
+    for (int i = 0; i < kPer; ++i) {
+      int mm, kk;
+      a_idx(threadIdx.x + i * 256, mm, kk);
+      const int64_t gm = m0 + mm, lk = k0 + kk, gk = p.k0[s] + g * p.K + lk;
+      ra[i] = (gm < p.M && lk < p.K) ? (p.a_mn ? A[gk * lda + gm] : A[gm * lda + gk]) : 0.0f;
     }
+#pragma unroll
+    for (int h = 0; h < NB; ++h) {
+      const float* B = p.B[PAIRED ? h : s];
+      const int64_t ldb = p.ldb[PAIRED ? h : s];
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        int nn, kk;
+        b_idx(threadIdx.x + i * 256, nn, kk);
+        const int64_t gn = n0 + nn, lk = k0 + kk, gk = p.k0[s] + g * p.K + lk;
+        rb[h][i] = (gn < p.N && lk < p.K) ? (p.b_mn ? B[gk * ldb + gn] : B[gn * ldb + gk]) : 0.0f;
+      }
+    }
+  };
+  const int64_t steps = (p.K + TK - 1) / TK, total = steps * p.nseg;
+  if (total > 0) load(0, 0);
+  for (int64_t it = 0; it < total; ++it) {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {  // registers -> shared (the previous step's reads ended
+      int mm, kk;                     // at the __syncthreads below)
+      a_idx(threadIdx.x + i * 256, mm, kk);
+      As[kk][mm] = ra[i];
+#pragma unroll
+      for (int h = 0; h < NB; ++h) {
+        int nn, kb;
+        b_idx(threadIdx.x + i * 256, nn, kb);
+        Bs[h][kb][nn] = rb[h][i];
+      }
+    }
+    __syncthreads();
+    if (it + 1 < total) {  // the next step's loads fly while this step's FMAs run
+      const int64_t nx = it + 1;
+      load(static_cast<int>(nx / steps), (nx % steps) * TK);
+    }
+#pragma unroll
+    for (int kk = 0; kk < TK; ++kk) {
+      float a[4], b[4], b2[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        a[i] = As[kk][ty * 4 + i];
+        b[i] = Bs[0][kk][tx * 4 + i];
+        if constexpr (PAIRED) b2[i] = Bs[NB - 1][kk][tx * 4 + i];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+          if constexpr (PAIRED) acc2[i][j] = fmaf(a[i], b2[j], acc2[i][j]);
+        }
+    }
+    __syncthreads();
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i)
