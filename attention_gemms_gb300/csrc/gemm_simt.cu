@@ -5,12 +5,19 @@
 // shared memory, and the next step's loads are issued before the current step's FMAs,
 // so one load latency per step is hidden behind the arithmetic instead of several
 // being paid in a row (the small fp32 GEMMs are latency-bound).
+// When the output has few tiles (fewer than half the SMs), the K steps of a tile are
+// split over the CTAs of a thread-block cluster (2, 4 or 8): each CTA accumulates its
+// share, parks the partial tile in shared memory, and after a cluster barrier CTA r
+// sums row slice r of the tile over the cluster's CTAs in rank order (distributed
+// shared memory) and runs the epilogue on it. The order of the sum is fixed, so the
+// result is deterministic; no workspace is needed.
 #include <cuda_runtime.h>
 
 #include <algorithm>
 
 #include "epi_math.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace tp {
 namespace {
@@ -30,7 +37,14 @@ struct SimtParams {
   const float* in0;
   const float* in1;
   int64_t ldo, out_group_stride;
+  int split;  // CTAs of a cluster sharing one output tile's K steps (1: no split)
 };
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
 
 template <int EPI>
 __device__ __forceinline__ void epi1(const SimtParams& p, int g, int64_t r, int64_t c, float a,
@@ -60,11 +74,17 @@ __device__ __forceinline__ void epi1(const SimtParams& p, int g, int64_t r, int6
 template <int EPI, bool PAIRED>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(const SimtParams p) {
   constexpr int NB = PAIRED ? 2 : 1;
-  __shared__ float As[TK][TM + 4];
-  __shared__ float Bs[NB][TK][TN + 4];
+  // A and B staging; reused for the partial tile of a split (unpaired only: TM x TN fits)
+  constexpr int kFloats = TK * (TM + 4) + NB * TK * (TN + 4);
+  static_assert(PAIRED || kFloats >= TM * TN, "partial tile must fit the staging buffers");
+  __shared__ __align__(16) float sm[kFloats];
+  auto As = reinterpret_cast<float(*)[TM + 4]>(sm);
+  auto Bs = reinterpret_cast<float(*)[TK][TN + 4]>(sm + TK * (TM + 4));
+  const int split = p.split;
+  const int rank = split > 1 ? static_cast<int>(cluster_ctarank()) : 0;  // blockIdx.x % split
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int64_t m0 = static_cast<int64_t>(blockIdx.y) * TM;
-  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * TN;
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x / split) * TN;
   const int g = blockIdx.z;
   float acc[4][4] = {}, acc2[4][4] = {};
   float ra[kPer], rb[NB][kPer];
@@ -101,8 +121,10 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const SimtParams p) {
     }
   };
   const int64_t steps = (p.K + TK - 1) / TK, total = steps * p.nseg;
-  if (total > 0) load(0, 0);
-  for (int64_t it = 0; it < total; ++it) {
+  const int64_t per = (total + split - 1) / split;  // this CTA's K steps: [it0, it1)
+  const int64_t it0 = rank * per, it1 = it0 + per < total ? it0 + per : total;
+  if (it0 < it1) load(static_cast<int>(it0 / steps), (it0 % steps) * TK);
+  for (int64_t it = it0; it < it1; ++it) {
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {  // registers -> shared (the previous step's reads ended
       int mm, kk;                     // at the __syncthreads below)
@@ -116,7 +138,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const SimtParams p) {
       }
     }
     __syncthreads();
-    if (it + 1 < total) {  // the next step's loads fly while this step's FMAs run
+    if (it + 1 < it1) {  // the next step's loads fly while this step's FMAs run
       const int64_t nx = it + 1;
       load(static_cast<int>(nx / steps), (nx % steps) * TK);
     }
@@ -139,18 +161,53 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const SimtParams p) {
     }
     __syncthreads();
   }
+  if (split == 1) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int64_t r = m0 + ty * 4 + i, c = n0 + tx * 4 + j;
-      if (r < p.M && c < p.N) epi1<EPI>(p, g, r, c, acc[i][j], acc2[i][j]);
+      for (int j = 0; j < 4; ++j) {
+        const int64_t r = m0 + ty * 4 + i, c = n0 + tx * 4 + j;
+        if (r < p.M && c < p.N) epi1<EPI>(p, g, r, c, acc[i][j], acc2[i][j]);
+      }
+    return;
+  }
+  if constexpr (!PAIRED) {  // split K (the host splits unpaired problems only)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sm[(ty * 4 + i) * TN + tx * 4 + j] = acc[i][j];
+    cluster_sync_all();  // every CTA's partial tile is in its shared memory
+    const int rows = TM / split;
+    for (int e = threadIdx.x; e < rows * TN; e += 256) {
+      const int rr = rank * rows + e / TN, cc = e % TN;
+      const uint32_t off = smem_u32(sm + rr * TN + cc);
+      float v = 0.0f;
+      for (int q = 0; q < split; ++q) v += ld_cluster_f32(mapa_shared(off, static_cast<uint32_t>(q)));
+      const int64_t r = m0 + rr, c = n0 + cc;
+      if (r < p.M && c < p.N) epi1<EPI>(p, g, r, c, v, 0.0f);
     }
+    cluster_sync_all();  // no CTA leaves while another still reads its tile
+  }
 }
 
 template <int EPI, bool PAIRED>
-void launch_k(const SimtParams& p, dim3 grid, cudaStream_t st) {
-  gemm_simt_kernel<EPI, PAIRED><<<grid, 256, 0, st>>>(p);
+cudaError_t launch_k(const SimtParams& p, dim3 grid, cudaStream_t st) {
+  if (p.split == 1) {
+    gemm_simt_kernel<EPI, PAIRED><<<grid, 256, 0, st>>>(p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(p.split);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(grid.x * static_cast<unsigned>(p.split), grid.y, grid.z);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_simt_kernel<EPI, PAIRED>, p);
 }
 
 }  // namespace
@@ -187,23 +244,31 @@ tp_status launch_gemm_simt(const GemmDesc& d, cudaStream_t st) {
     return fail(TP_ERR_SHAPE, "fp32 GEMM grid too large");
   dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(d.groups));
   const bool pr = d.paired;
+  // split K over a cluster while the tiles (times the split) stay within half the SMs
+  // and every CTA keeps at least two K steps
+  const int64_t tiles = gx * gy * d.groups, ksteps = (d.K + TK - 1) / TK * d.nseg;
+  p.split = 1;
+  while (!pr && p.split < 8 && tiles * p.split * 4 <= device_sm_count() &&
+         ksteps >= 4 * p.split)
+    p.split *= 2;
+  cudaError_t e = cudaSuccess;
   switch (d.epi) {
-    case EPI_STORE: launch_k<EPI_STORE, false>(p, grid, st); break;
-    case EPI_GELU: launch_k<EPI_GELU, false>(p, grid, st); break;
+    case EPI_STORE: e = launch_k<EPI_STORE, false>(p, grid, st); break;
+    case EPI_GELU: e = launch_k<EPI_GELU, false>(p, grid, st); break;
     case EPI_SWIGLU:
       if (!pr) return fail(TP_ERR_INVALID_ARG, "SwiGLU epilogue needs a paired problem");
-      launch_k<EPI_SWIGLU, true>(p, grid, st);
+      e = launch_k<EPI_SWIGLU, true>(p, grid, st);
       break;
-    case EPI_DGELU: launch_k<EPI_DGELU, false>(p, grid, st); break;
-    case EPI_DSWIGLU: launch_k<EPI_DSWIGLU, false>(p, grid, st); break;
+    case EPI_DGELU: e = launch_k<EPI_DGELU, false>(p, grid, st); break;
+    case EPI_DSWIGLU: e = launch_k<EPI_DSWIGLU, false>(p, grid, st); break;
     case EPI_PAIR:
       if (!pr) return fail(TP_ERR_INVALID_ARG, "pair epilogue needs a paired problem");
-      launch_k<EPI_PAIR, true>(p, grid, st);
+      e = launch_k<EPI_PAIR, true>(p, grid, st);
       break;
     default: return fail(TP_ERR_INVALID_ARG, "unknown epilogue");
   }
   count_launch();
-  TP_CUDA_TRY(cudaGetLastError());
+  TP_CUDA_TRY(e);
   return TP_OK;
 }
 
