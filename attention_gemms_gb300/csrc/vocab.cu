@@ -184,26 +184,35 @@ __device__ __forceinline__ void st8(float* p, const float* v) {
 constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
 constexpr float kLn2 = 0.6931471805599453f;    // ln(2)
 
+// 2^x on the special-function unit (PTX ex2.approx.ftz: relative error about 2^-22,
+// results below 2^-126 flushed to zero, which only drops terms that cannot move a sum
+// that already holds 2^0 = 1 from the row maximum); 2^-inf = 0
+__device__ __forceinline__ float ex2_sfu(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // (m2, s) running maximum (base-2 scaled) and sum of 2^(y - m2), updated with 8 logits
+// (the maximum is taken on the raw logits and scaled once: rounding is monotonic, so
+// it equals the maximum of the scaled logits; each exponent is one fused multiply-add)
 __device__ __forceinline__ void online8(float& m2, float& s, const float* x) {
-  float y[8];
+  float mx = x[0];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) y[k] = x[k] * kLog2e;
-  float mx = y[0];
-#pragma unroll
-  for (int k = 1; k < 8; ++k) mx = fmaxf(mx, y[k]);
+  for (int k = 1; k < 8; ++k) mx = fmaxf(mx, x[k]);
+  mx *= kLog2e;
   if (mx > m2) {
-    s *= exp2f(m2 - mx);  // m2 = -inf at first: s = 0 stays 0
+    s *= ex2_sfu(m2 - mx);  // m2 = -inf at first: s = 0 stays 0
     m2 = mx;
   }
 #pragma unroll
-  for (int k = 0; k < 8; ++k) s += exp2f(y[k] - m2);
+  for (int k = 0; k < 8; ++k) s += ex2_sfu(fmaf(x[k], kLog2e, -m2));
 }
 
 // (m2, s) pairs combined: max of the two, sums re-based to it
 __device__ __forceinline__ void combine(float& m, float& s, float m2, float s2) {
   const float mm = fmaxf(m, m2);
-  s = (m == -INFINITY ? 0.0f : s * exp2f(m - mm)) + (m2 == -INFINITY ? 0.0f : s2 * exp2f(m2 - mm));
+  s = (m == -INFINITY ? 0.0f : s * ex2_sfu(m - mm)) + (m2 == -INFINITY ? 0.0f : s2 * ex2_sfu(m2 - mm));
   m = mm;
 }
 
