@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(32 * kRowWarps) ln_fwd_vec_kernel(
   const int nv = h / E;
   const typename V::Raw* xr = reinterpret_cast<const typename V::Raw*>(x + row * h);
   float s = 0.0f;
-#pragma unroll 4
+#pragma unroll 8
   for (int v = lane; v < nv; v += 32) {
     float f[E];
     V::unpack(xr[v], f);
@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(32 * kRowWarps) ln_bwd_dx_vec_kernel(
   const typename V::Raw* xr = reinterpret_cast<const typename V::Raw*>(x + row * h);
   const typename V::Raw* dyr = reinterpret_cast<const typename V::Raw*>(dy + row * h);
   float s1 = 0.0f, s2 = 0.0f;
-#pragma unroll 4
+#pragma unroll 8
   for (int v = lane; v < nv; v += 32) {
     float a[E], d[E], g[E];
     V::unpack(xr[v], a);
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(32 * kRowWarps) ln_bwd_param_partial_vec_kerne
 #pragma unroll
   for (int e = 0; e < E; ++e) sg[e] = sb[e] = 0.0f;
   if (v < nv) {
-#pragma unroll 2
+#pragma unroll 8
     for (int64_t r = r0 + warp; r < r1; r += kRowWarps) {
       float a[E], d[E];
       V::unpack(reinterpret_cast<const typename V::Raw*>(x + r * h)[v], a);
@@ -325,30 +325,51 @@ __global__ void __launch_bounds__(kColThreads) ln_bwd_param_partial_kernel(
   partial[blockIdx.y * 2ll * h + h + c] = sb;
 }
 
-constexpr int kFinalThreads = 64;  // narrow CTAs: h / 64 of them share the chunk sums
+constexpr int kFinalCols = 64, kFinalGroups = 4;  // columns per CTA, chunk groups per column
 
-// per rank: the sum of its chunks in order (written to dgamma_ranks / dbeta_ranks
-// (ranks, h) when given); then the sum over the ranks in rank order
-__global__ void __launch_bounds__(kFinalThreads) ln_bwd_param_final_kernel(
+// per rank: the sum of its chunks (written to dgamma_ranks / dbeta_ranks (ranks, h)
+// when given); then the sum over the ranks in rank order. A rank's chunks are split
+// into kFinalGroups consecutive groups summed in parallel, each in chunk order, and
+// the group sums are added in group order: a fixed order, so results are deterministic.
+__global__ void __launch_bounds__(kFinalCols * kFinalGroups) ln_bwd_param_final_kernel(
     const float* __restrict__ partial, int ranks, int cpr, int h, float* dgamma, float* dbeta,
     float* dgamma_ranks, float* dbeta_ranks) {
-  const int c = blockIdx.x * kFinalThreads + threadIdx.x;
-  if (c >= h) return;
+  __shared__ float red[kFinalGroups][2][kFinalCols];
+  const int cl = threadIdx.x % kFinalCols, q = threadIdx.x / kFinalCols;
+  const int c = blockIdx.x * kFinalCols + cl;
+  const int per = (cpr + kFinalGroups - 1) / kFinalGroups;
   float tg = 0.0f, tb = 0.0f;
   for (int r = 0; r < ranks; ++r) {
+    const int k0 = r * cpr + q * per, k1 = min((r + 1) * cpr, k0 + per);
     float sg = 0.0f, sb = 0.0f;
+    if (c < h) {
 #pragma unroll 8
-    for (int k = r * cpr; k < (r + 1) * cpr; ++k) {
-      sg += partial[k * 2ll * h + c];
-      sb += partial[k * 2ll * h + h + c];
+      for (int k = k0; k < k1; ++k) {
+        sg += partial[k * 2ll * h + c];
+        sb += partial[k * 2ll * h + h + c];
+      }
     }
-    if (dgamma_ranks) dgamma_ranks[static_cast<int64_t>(r) * h + c] = sg;
-    if (dbeta_ranks) dbeta_ranks[static_cast<int64_t>(r) * h + c] = sb;
-    tg += sg;
-    tb += sb;
+    red[q][0][cl] = sg;
+    red[q][1][cl] = sb;
+    __syncthreads();
+    if (q == 0 && c < h) {
+      float g = 0.0f, b = 0.0f;
+#pragma unroll
+      for (int i = 0; i < kFinalGroups; ++i) {
+        g += red[i][0][cl];
+        b += red[i][1][cl];
+      }
+      if (dgamma_ranks) dgamma_ranks[static_cast<int64_t>(r) * h + c] = g;
+      if (dbeta_ranks) dbeta_ranks[static_cast<int64_t>(r) * h + c] = b;
+      tg += g;
+      tb += b;
+    }
+    __syncthreads();
   }
-  if (dgamma) dgamma[c] = tg;
-  if (dbeta) dbeta[c] = tb;
+  if (q == 0 && c < h) {
+    if (dgamma) dgamma[c] = tg;
+    if (dbeta) dbeta[c] = tb;
+  }
 }
 
 // whole 16-byte vectors per row (the buffers themselves are 16-byte aligned)
@@ -402,7 +423,7 @@ tp_status bwd_t(const void* x, const float* gamma, const float* mean, const floa
     ln_bwd_param_partial_kernel<T><<<g1, kColThreads, 0, st>>>(
         static_cast<const T*>(x), mean, rstd, static_cast<const T*>(dy), ws, M, h, rank_rows, cpr);
   }
-  ln_bwd_param_final_kernel<<<(h + kFinalThreads - 1) / kFinalThreads, kFinalThreads, 0, st>>>(
+  ln_bwd_param_final_kernel<<<(h + kFinalCols - 1) / kFinalCols, kFinalCols * kFinalGroups, 0, st>>>(
       ws, ranks, cpr, h, dgamma, dbeta, dgamma_ranks, dbeta_ranks);
   count_launch(2);
   TP_CUDA_TRY(cudaGetLastError());
