@@ -68,12 +68,16 @@ __device__ __forceinline__ void st(__nv_bfloat16* p, int64_t i, float v) {
   p[i] = __float2bfloat16_rn(v);
 }
 
-// Each query (or key) row is handled by P = D / 16 adjacent lanes; lane `part` of a row
-// owns the 16 head dimensions part, part + P, part + 2P, ... (interleaved, so the P
-// lanes of a row read consecutive shared-memory words). Partial dot products are summed
-// over the P lanes with xor-shuffles. Every lane runs every shuffle: rows past the end
-// and masked keys are handled by masking values, never by skipping the loop body.
-constexpr int DP = 16;  // head dimensions per thread
+// Each query (or key) row is handled by four adjacent lanes: P = D / 16 of them split
+// the head dimensions (lane `part` owns dimensions part, part + P, part + 2P, ...,
+// interleaved so the P lanes of a row read consecutive shared-memory words) and
+// KS = 4 / P of them split the other operand's rows (lane `ks` takes rows ks, ks + KS,
+// ...), each keeping its own partial state that the KS lanes merge at the end. Partial
+// dot products are summed over the P lanes with xor-shuffles. Every lane runs every
+// shuffle: all lanes of a warp run the same number of loop steps, and rows past the end
+// and masked entries are handled by masking values, never by skipping the loop body.
+constexpr int DP = 16;  // head dimensions per lane
+constexpr int LPR = 4;  // lanes per row
 // Shared-memory rows hold each lane's 16 dimensions contiguously, padded to 20 floats:
 // a lane reads them with four 128-bit loads, and the P lanes of a row (offsets 0, 80,
 // 160, 240 bytes) hit different banks.
@@ -90,22 +94,36 @@ __device__ __forceinline__ void lds16(const float* src, float* v) {
   }
 }
 
-template <int P>
-__device__ __forceinline__ float row_sum(float v) {
+// sum over the lanes whose index differs in bits [lo, hi) (xor-shuffle tree)
+template <int LO, int HI>
+__device__ __forceinline__ float lane_sum(float v) {
 #pragma unroll
-  for (int o = 1; o < P; o <<= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  for (int o = LO; o < HI; o <<= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
   return v;
 }
+template <int P>
+__device__ __forceinline__ float row_sum(float v) {
+  return lane_sum<1, P>(v);
+}
+
+template <int D>
+struct Lanes {
+  static constexpr int P = D / DP, KS = LPR / P;  // dimension lanes, row-split lanes
+  int r, part, ks;
+  __device__ explicit Lanes(int tid) : r(tid / LPR), part((tid % LPR) % P), ks((tid % LPR) / P) {}
+};
 
 template <typename T, int D>
-__global__ void __launch_bounds__(RB * (D / DP)) attn_fwd_kernel(
+__global__ void __launch_bounds__(RB * LPR) attn_fwd_kernel(
     const T* __restrict__ qkv, T* __restrict__ o, float* __restrict__ lse, int s,
     const HeadMap hm, float scale, int causal) {
-  constexpr int P = D / DP;
+  using Ln = Lanes<D>;
+  constexpr int P = Ln::P, KS = Ln::KS;
   __shared__ __align__(16) float Ks[RB][P][DPAD];
   __shared__ __align__(16) float Vs[RB][P][DPAD];
   const int b = blockIdx.z, t = blockIdx.y;
-  const int r = threadIdx.x / P, part = threadIdx.x - r * P;
+  const Ln L(threadIdx.x);
+  const int r = L.r, part = L.part, ks = L.ks;
   const int qi = blockIdx.x * RB + r;
   const int64_t ldq = hm.ldq, qc = qcol<D>(hm, t), kc = kcol<D>(hm, t), vc = vcol<D>(hm, t);
   const T* base = qkv + static_cast<int64_t>(b) * s * ldq;
@@ -120,48 +138,65 @@ __global__ void __launch_bounds__(RB * (D / DP)) attn_fwd_kernel(
   const int kend = causal ? min(s, static_cast<int>(blockIdx.x + 1) * RB) : s;
   for (int k0 = 0; k0 < kend; k0 += RB) {
     __syncthreads();
-    const int kj = k0 + r;
+    const int kj = k0 + r;  // this row's key; the KS lanes of a part load slices of it
 #pragma unroll
-    for (int k = 0; k < DP; ++k) {
+    for (int k = ks * (DP / KS); k < (ks + 1) * (DP / KS); ++k) {
       Ks[r][part][k] = kj < s ? ld(base + kj * ldq, kc + part + P * k) : 0.0f;
       Vs[r][part][k] = kj < s ? ld(base + kj * ldq, vc + part + P * k) : 0.0f;
     }
     __syncthreads();
     for (int j0 = 0; j0 < RB; j0 += 32) {
-      float sc[32];
+      float sc[32 / KS];
       float mb = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
+      for (int jj = 0; jj < 32 / KS; ++jj) {
+        const int j = j0 + jj * KS + ks;
         float kv[DP];
-        lds16(&Ks[j0 + j][part][0], kv);
+        lds16(&Ks[j][part][0], kv);
         float v = 0.0f;
 #pragma unroll
         for (int k = 0; k < DP; ++k) v = fmaf(q[k], kv[k], v);
         v = row_sum<P>(v);
-        const int key = k0 + j0 + j;
+        const int key = k0 + j;
         if (!valid || key >= s || (causal && key > qi)) v = -INFINITY;
-        sc[j] = v;
+        sc[jj] = v;
         mb = fmaxf(mb, v);
       }
       const float mn = fmaxf(m, mb);
-      if (mn == -INFINITY) continue;  // every key so far masked (no shuffles below)
+      if (mn == -INFINITY) continue;  // every key of this lane so far masked (no shuffles below)
       const float corr = expf(m - mn);
       l *= corr;
 #pragma unroll
       for (int k = 0; k < DP; ++k) acc[k] *= corr;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float p = expf(sc[j] - mn);
+      for (int jj = 0; jj < 32 / KS; ++jj) {
+        const float p = expf(sc[jj] - mn);
         l += p;
         float vv[DP];
-        lds16(&Vs[j0 + j][part][0], vv);
+        lds16(&Vs[j0 + jj * KS + ks][part][0], vv);
 #pragma unroll
         for (int k = 0; k < DP; ++k) acc[k] = fmaf(p, vv[k], acc[k]);
       }
       m = mn;
     }
   }
-  if (!valid) return;
+  // merge the KS lanes' (max, sum, output) states (symmetric: every lane ends equal)
+#pragma unroll
+  for (int off = P; off < LPR; off <<= 1) {
+    const float mo = __shfl_xor_sync(0xFFFFFFFFu, m, off);
+    const float lo = __shfl_xor_sync(0xFFFFFFFFu, l, off);
+    const float mn = fmaxf(m, mo);
+    const float a = m == -INFINITY ? 0.0f : expf(m - mn);
+    const float c = mo == -INFINITY ? 0.0f : expf(mo - mn);
+    l = l * a + lo * c;
+#pragma unroll
+    for (int k = 0; k < DP; ++k) {
+      const float ao = __shfl_xor_sync(0xFFFFFFFFu, acc[k], off);
+      acc[k] = acc[k] * a + ao * c;
+    }
+    m = mn;
+  }
+  if (!valid || ks != 0) return;
   const float inv = 1.0f / l;
   T* orow = o + (static_cast<int64_t>(b) * s + qi) * hm.ldo + t * D;
 #pragma unroll
@@ -169,22 +204,24 @@ __global__ void __launch_bounds__(RB * (D / DP)) attn_fwd_kernel(
   if (part == 0) lse[(static_cast<int64_t>(b) * hm.H + t) * s + qi] = m + logf(l);
 }
 
-// dK, dV: P lanes per key row of one key/value head (grid.y runs over the blocks'
+// dK, dV: four lanes per key row of one key/value head (grid.y runs over the blocks'
 // key/value heads, replicas included); the query rows of every query head of the block
 // that uses it are streamed through shared memory, so the head's gradient sums their
-// contributions.
+// contributions; the KS lanes of a part take every KS-th query and sum at the end.
 template <typename T, int D>
-__global__ void __launch_bounds__(RB * (D / DP)) attn_bwd_dkdv_kernel(
+__global__ void __launch_bounds__(RB * LPR) attn_bwd_dkdv_kernel(
     const T* __restrict__ qkv, const T* __restrict__ o, const float* __restrict__ lse,
     const T* __restrict__ dO, T* __restrict__ dqkv, int s, const HeadMap hm, float scale,
     int causal) {
-  constexpr int P = D / DP;
+  using Ln = Lanes<D>;
+  constexpr int P = Ln::P, KS = Ln::KS;
   __shared__ __align__(16) float Qs[RB][P][DPAD];
   __shared__ __align__(16) float dOs[RB][P][DPAD];
   __shared__ float Ls[RB], Ds[RB];
   const int b = blockIdx.z, u = blockIdx.y;
   const int blk = u / hm.hkv, kvl = u - blk * hm.hkv;
-  const int r = threadIdx.x / P, part = threadIdx.x - r * P;
+  const Ln L(threadIdx.x);
+  const int r = L.r, part = L.part, ks = L.ks;
   const int kj = blockIdx.x * RB + r;
   const int64_t ldq = hm.ldq;
   const int64_t kc = blk * hm.S + hm.KO + static_cast<int64_t>(kvl) * D;
@@ -208,10 +245,10 @@ __global__ void __launch_bounds__(RB * (D / DP)) attn_bwd_dkdv_kernel(
     const float* lrow = lse + (static_cast<int64_t>(b) * hm.H + t) * s;
     for (int q0 = qstart; q0 < s; q0 += RB) {
       __syncthreads();
-      const int qi = q0 + r;
+      const int qi = q0 + r;  // this row's query; the KS lanes of a part load slices of it
       float dsum = 0.0f;
 #pragma unroll
-      for (int c = 0; c < DP; ++c) {
+      for (int c = ks * (DP / KS); c < (ks + 1) * (DP / KS); ++c) {
         const int dd = part + P * c;
         const float qv = qi < s ? ld(base + qi * ldq, qc + dd) : 0.0f;
         const float dov = qi < s ? ld(dobase + qi * hm.ldo, t * D + dd) : 0.0f;
@@ -220,17 +257,20 @@ __global__ void __launch_bounds__(RB * (D / DP)) attn_bwd_dkdv_kernel(
         dOs[r][part][c] = dov;
         dsum = fmaf(dov, ov, dsum);
       }
-      dsum = row_sum<P>(dsum);
-      if (part == 0) {
+      dsum = lane_sum<1, LPR>(dsum);  // over every dimension slice of the row
+      if (part == 0 && ks == 0) {
         Ls[r] = qi < s ? lrow[qi] : 0.0f;
         Ds[r] = dsum;
       }
       __syncthreads();
       const int iend = min(RB, s - q0);
-      for (int i = 0; i < iend; ++i) {
+      for (int i0 = 0; i0 < iend; i0 += KS) {  // the same step count on every lane
+        const int i = i0 + ks;
+        const bool in = i < iend;
+        const int ii = in ? i : 0;
         float qv[DP], dov[DP];
-        lds16(&Qs[i][part][0], qv);
-        lds16(&dOs[i][part][0], dov);
+        lds16(&Qs[ii][part][0], qv);
+        lds16(&dOs[ii][part][0], dov);
         float sc = 0.0f, dp = 0.0f;
 #pragma unroll
         for (int c = 0; c < DP; ++c) {
@@ -239,9 +279,9 @@ __global__ void __launch_bounds__(RB * (D / DP)) attn_bwd_dkdv_kernel(
         }
         sc = row_sum<P>(sc);
         dp = row_sum<P>(dp);
-        const bool live = valid && !(causal && kj > q0 + i);
-        const float pr = live ? expf(sc * scale - Ls[i]) : 0.0f;
-        const float ds = pr * (dp - Ds[i]) * scale;
+        const bool live = in && valid && !(causal && kj > q0 + i);
+        const float pr = live ? expf(sc * scale - Ls[ii]) : 0.0f;
+        const float ds = pr * (dp - Ds[ii]) * scale;
 #pragma unroll
         for (int c = 0; c < DP; ++c) {
           dv[c] = fmaf(pr, dov[c], dv[c]);
@@ -250,7 +290,12 @@ __global__ void __launch_bounds__(RB * (D / DP)) attn_bwd_dkdv_kernel(
       }
     }
   }
-  if (!valid) return;
+#pragma unroll
+  for (int c = 0; c < DP; ++c) {  // the KS lanes' partial sums (a fixed xor tree)
+    dk[c] = lane_sum<P, LPR>(dk[c]);
+    dv[c] = lane_sum<P, LPR>(dv[c]);
+  }
+  if (!valid || ks != 0) return;
   T* row = dqkv + (static_cast<int64_t>(b) * s + kj) * ldq;
 #pragma unroll
   for (int c = 0; c < DP; ++c) {
@@ -259,23 +304,26 @@ __global__ void __launch_bounds__(RB * (D / DP)) attn_bwd_dkdv_kernel(
   }
 }
 
-// dQ: P lanes per query row; key rows streamed through shared memory
+// dQ: four lanes per query row; key rows streamed through shared memory, every KS-th
+// key to each of a part's KS lanes
 template <typename T, int D>
-__global__ void __launch_bounds__(RB * (D / DP)) attn_bwd_dq_kernel(
+__global__ void __launch_bounds__(RB * LPR) attn_bwd_dq_kernel(
     const T* __restrict__ qkv, const T* __restrict__ o, const float* __restrict__ lse,
     const T* __restrict__ dO, T* __restrict__ dqkv, int s, const HeadMap hm, float scale,
     int causal) {
-  constexpr int P = D / DP;
+  using Ln = Lanes<D>;
+  constexpr int P = Ln::P, KS = Ln::KS;
   __shared__ __align__(16) float Ks[RB][P][DPAD];
   __shared__ __align__(16) float Vs[RB][P][DPAD];
   const int b = blockIdx.z, t = blockIdx.y;
-  const int r = threadIdx.x / P, part = threadIdx.x - r * P;
+  const Ln L(threadIdx.x);
+  const int r = L.r, part = L.part, ks = L.ks;
   const int qi = blockIdx.x * RB + r;
   const int64_t ldq = hm.ldq, qc = qcol<D>(hm, t), kc = kcol<D>(hm, t), vc = vcol<D>(hm, t);
   const T* base = qkv + static_cast<int64_t>(b) * s * ldq;
   const bool valid = qi < s;
   float q[DP], dov[DP], dq[DP];
-  float dsum = 0.0f, L = 0.0f;
+  float dsum = 0.0f, Lq = 0.0f;
   {
     const T* orow = o + (static_cast<int64_t>(b) * s + (valid ? qi : 0)) * hm.ldo + t * D;
     const T* dorow = dO + (static_cast<int64_t>(b) * s + (valid ? qi : 0)) * hm.ldo + t * D;
@@ -288,23 +336,26 @@ __global__ void __launch_bounds__(RB * (D / DP)) attn_bwd_dq_kernel(
       dq[c] = 0.0f;
     }
     dsum = row_sum<P>(dsum);
-    L = valid ? lse[(static_cast<int64_t>(b) * hm.H + t) * s + qi] : 0.0f;
+    Lq = valid ? lse[(static_cast<int64_t>(b) * hm.H + t) * s + qi] : 0.0f;
   }
   const int kend = causal ? min(s, static_cast<int>(blockIdx.x + 1) * RB) : s;
   for (int k0 = 0; k0 < kend; k0 += RB) {
     __syncthreads();
     const int kj = k0 + r;
 #pragma unroll
-    for (int c = 0; c < DP; ++c) {
+    for (int c = ks * (DP / KS); c < (ks + 1) * (DP / KS); ++c) {
       Ks[r][part][c] = kj < s ? ld(base + kj * ldq, kc + part + P * c) : 0.0f;
       Vs[r][part][c] = kj < s ? ld(base + kj * ldq, vc + part + P * c) : 0.0f;
     }
     __syncthreads();
     const int jend = min(RB, s - k0);
-    for (int j = 0; j < jend; ++j) {
+    for (int j0 = 0; j0 < jend; j0 += KS) {  // the same step count on every lane
+      const int j = j0 + ks;
+      const bool in = j < jend;
+      const int jj = in ? j : 0;
       float kv[DP], vv[DP];
-      lds16(&Ks[j][part][0], kv);
-      lds16(&Vs[j][part][0], vv);
+      lds16(&Ks[jj][part][0], kv);
+      lds16(&Vs[jj][part][0], vv);
       float sc = 0.0f, dp = 0.0f;
 #pragma unroll
       for (int c = 0; c < DP; ++c) {
@@ -313,14 +364,16 @@ __global__ void __launch_bounds__(RB * (D / DP)) attn_bwd_dq_kernel(
       }
       sc = row_sum<P>(sc);
       dp = row_sum<P>(dp);
-      const bool live = valid && !(causal && k0 + j > qi);
-      const float pr = live ? expf(sc * scale - L) : 0.0f;
+      const bool live = in && valid && !(causal && k0 + j > qi);
+      const float pr = live ? expf(sc * scale - Lq) : 0.0f;
       const float ds = pr * (dp - dsum) * scale;
 #pragma unroll
       for (int c = 0; c < DP; ++c) dq[c] = fmaf(ds, kv[c], dq[c]);
     }
   }
-  if (!valid) return;
+#pragma unroll
+  for (int c = 0; c < DP; ++c) dq[c] = lane_sum<P, LPR>(dq[c]);  // the KS lanes' partials
+  if (!valid || ks != 0) return;
   T* row = dqkv + (static_cast<int64_t>(b) * s + qi) * ldq;
 #pragma unroll
   for (int c = 0; c < DP; ++c) st(row, qc + part + P * c, dq[c]);
@@ -330,7 +383,7 @@ template <typename T, int D>
 tp_status run_fwd(const void* qkv, void* o, float* lse, int b, int s, const HeadMap& hm,
                   int causal, cudaStream_t st) {
   const dim3 grid((s + RB - 1) / RB, hm.H, b);
-  attn_fwd_kernel<T, D><<<grid, RB * (D / DP), 0, st>>>(static_cast<const T*>(qkv), static_cast<T*>(o), lse,
+  attn_fwd_kernel<T, D><<<grid, RB * LPR, 0, st>>>(static_cast<const T*>(qkv), static_cast<T*>(o), lse,
                                               s, hm, 1.0f / sqrtf(static_cast<float>(D)), causal);
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
@@ -341,10 +394,10 @@ template <typename T, int D>
 tp_status run_bwd(const void* qkv, const void* o, const float* lse, const void* dO, void* dqkv,
                   int b, int s, const HeadMap& hm, int kv_heads, int causal, cudaStream_t st) {
   const float scale = 1.0f / sqrtf(static_cast<float>(D));
-  attn_bwd_dkdv_kernel<T, D><<<dim3((s + RB - 1) / RB, kv_heads, b), RB * (D / DP), 0, st>>>(
+  attn_bwd_dkdv_kernel<T, D><<<dim3((s + RB - 1) / RB, kv_heads, b), RB * LPR, 0, st>>>(
       static_cast<const T*>(qkv), static_cast<const T*>(o), lse, static_cast<const T*>(dO),
       static_cast<T*>(dqkv), s, hm, scale, causal);
-  attn_bwd_dq_kernel<T, D><<<dim3((s + RB - 1) / RB, hm.H, b), RB * (D / DP), 0, st>>>(
+  attn_bwd_dq_kernel<T, D><<<dim3((s + RB - 1) / RB, hm.H, b), RB * LPR, 0, st>>>(
       static_cast<const T*>(qkv), static_cast<const T*>(o), lse, static_cast<const T*>(dO),
       static_cast<T*>(dqkv), s, hm, scale, causal);
   count_launch(2);
