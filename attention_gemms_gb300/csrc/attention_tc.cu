@@ -36,17 +36,22 @@ constexpr int kQ = 128;                   // query rows per CTA = TMEM lanes
 constexpr int kKB = 64;                   // keys per block
 constexpr int kQTile = kQ * 64 * 2;       // Q: 128 rows x 64 dims, bf16: 16 KB
 constexpr int kKVTile = kKB * 64 * 2;     // a K or V block: 64 keys x 64 dims: 8 KB
-constexpr int kOffQ = 0;
-constexpr int kOffKV = kQTile;            // stage st: K at kOffKV + 2 st kKVTile, V after it
-constexpr int kOffP = kOffKV + 4 * kKVTile;  // P: 128 rows x 64 keys (one swizzle atom)
-constexpr int kOffBar = kOffP + kQ * kKB * 2;
-constexpr int kSmem = kOffBar + 16 * 8 + 16 + 1024;  // + alignment slack
-constexpr int kThreadsTC = 192;
+// Forward layout for NH query heads per CTA (1, or 2 heads sharing a key/value head):
+// Q tiles | K/V stages | P tiles | barriers. TMEM: S of head h at 64 h, O at 64 NH + 64 h.
+template <int NH>
+struct FwdLayout {
+  static constexpr int kOffQ = 0;                      // head h: kOffQ + h kQTile
+  static constexpr int kOffKV = NH * kQTile;           // stage st: K at kOffKV + 2 st kKVTile, V after
+  static constexpr int kOffP = kOffKV + 4 * kKVTile;   // head h: 128 rows x 64 keys (one swizzle atom)
+  static constexpr int kOffBar = kOffP + NH * kQ * kKB * 2;
+  static constexpr int kSmem = kOffBar + 16 * 8 + 16 + 1024;  // + alignment slack
+  static constexpr int kThreads = (4 * NH + 2) * 32;  // 4 softmax warps per head, TMA, MMA
+  static constexpr uint32_t kTmemCols = 128 * NH;
+};
 #ifndef TP_ATTN_CTAS
 #define TP_ATTN_CTAS 2  // CTAs per SM the register allocation must allow (3 spills)
 #endif
 constexpr int kCtasPerSm = TP_ATTN_CTAS;
-constexpr uint32_t kTmemCols = 128;       // S at 0 (64 columns), O at 64
 constexpr uint64_t kDrainNs = 20000000ull;
 
 struct AttnTcParams {
@@ -105,26 +110,46 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-__global__ void __launch_bounds__(kThreadsTC, kCtasPerSm) attn_fwd_tc_kernel(const __grid_constant__ AttnTcParams p) {
+// 32 fp32 values times `mul` as bf16 to global memory (16-byte aligned)
+__device__ __forceinline__ void st_row_bf16(__nv_bfloat16* dst, const uint32_t* v, float mul) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    uint4 w;
+    w.x = pack_bf16x2(__uint_as_float(v[8 * u]) * mul, __uint_as_float(v[8 * u + 1]) * mul);
+    w.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]) * mul, __uint_as_float(v[8 * u + 3]) * mul);
+    w.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]) * mul, __uint_as_float(v[8 * u + 5]) * mul);
+    w.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]) * mul, __uint_as_float(v[8 * u + 7]) * mul);
+    reinterpret_cast<uint4*>(dst)[u] = w;
+  }
+}
+
+template <int NH>
+__global__ void __launch_bounds__(FwdLayout<NH>::kThreads, kCtasPerSm) attn_fwd_tc_kernel(const __grid_constant__ AttnTcParams p) {
+  using Lay = FwdLayout<NH>;
+  constexpr int kProd = 4 * NH, kMma = 4 * NH + 1;  // warp roles
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_u32(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
-  const uint32_t q_full = bar0, s_full = bar0 + 8 * 5, p_full = bar0 + 8 * 6,
-                 o_done = bar0 + 8 * 7, drain = bar0 + 8 * 8;
+  const uint32_t q_full = bar0, drain = bar0 + 8 * 11;
   auto kv_full = [&](int st) { return bar0 + 8u * (1 + st); };
   auto kv_empty = [&](int st) { return bar0 + 8u * (3 + st); };
+  auto s_full = [&](int h) { return bar0 + 8u * (5 + h); };
+  auto p_full = [&](int h) { return bar0 + 8u * (7 + h); };
+  auto o_done = [&](int h) { return bar0 + 8u * (9 + h); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.z, t = blockIdx.y, q0 = blockIdx.x * kQ;
-  const int blk = t / p.hq, tl = t - blk * p.hq;
-  const int qc = static_cast<int>(blk * p.S + static_cast<int64_t>(tl) * 64);
-  const int kc = static_cast<int>(blk * p.S + p.KO + static_cast<int64_t>(tl / p.g) * 64);
-  const int vc = static_cast<int>(blk * p.S + p.VO + static_cast<int64_t>(tl / p.g) * 64);
+  const int b = blockIdx.z, t0 = blockIdx.y * NH, q0 = blockIdx.x * kQ;  // heads t0 .. t0 + NH - 1
+  const int blk = t0 / p.hq, tl0 = t0 - blk * p.hq;                     // same key/value head
+  auto qcol_of = [&](int h) {
+    return static_cast<int>(blk * p.S + static_cast<int64_t>(tl0 + h) * 64);
+  };
+  const int kc = static_cast<int>(blk * p.S + p.KO + static_cast<int64_t>(tl0 / p.g) * 64);
+  const int vc = static_cast<int>(blk * p.S + p.VO + static_cast<int64_t>(tl0 / p.g) * 64);
   const int row0 = b * p.s;
   const int kend = p.causal ? min(p.s, q0 + kQ) : p.s;
   const int nkb = (kend + kKB - 1) / kKB;
@@ -135,37 +160,41 @@ __global__ void __launch_bounds__(kThreadsTC, kCtasPerSm) attn_fwd_tc_kernel(con
       mbar_init(kv_full(st), 1);
       mbar_init(kv_empty(st), 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_full, 4);  // one arrive per softmax warp
-    mbar_init(o_done, 1);
+    for (int h = 0; h < NH; ++h) {
+      mbar_init(s_full(h), 1);
+      mbar_init(p_full(h), 4);  // one arrive per softmax warp of the head
+      mbar_init(o_done(h), 1);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  if (warp == kMma) {
+    tmem_alloc(smem_u32(tmem_slot), Lay::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-  const uint32_t tS = tmem, tO = tmem + kKB;
+  auto tS = [&](int h) { return tmem + 64u * h; };
+  auto tO = [&](int h) { return tmem + 64u * NH + 64u * h; };
   int issued_kv = 0;  // producer: K/V blocks issued
 
-  if (warp == 4) {
+  if (warp == kProd) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       bool ok = true;
-      mbar_arrive_expect_tx(q_full, kQTile);
-      tma_load_2d(sb + kOffQ, &p.tm, q_full, qc, row0 + q0);
+      mbar_arrive_expect_tx(q_full, NH * kQTile);
+      for (int h = 0; h < NH; ++h)
+        tma_load_2d(sb + Lay::kOffQ + h * kQTile, &p.tm, q_full, qcol_of(h), row0 + q0);
       for (int j = 0; j < nkb; ++j) {
         const int st = j & 1;
         if (j >= 2 && !mbar_wait(kv_empty(st), ((j >> 1) - 1) & 1, p.timeout_ns, abort_flag)) {
           ok = false;
           break;
         }
-        const uint32_t dst = sb + kOffKV + st * 2 * kKVTile;
+        const uint32_t dst = sb + Lay::kOffKV + st * 2 * kKVTile;
         mbar_arrive_expect_tx(kv_full(st), 2 * kKVTile);
         tma_load_2d(dst, &p.tmkv, kv_full(st), kc, row0 + j * kKB);
         tma_load_2d(dst + kKVTile, &p.tmkv, kv_full(st), vc, row0 + j * kKB);
@@ -174,54 +203,61 @@ __global__ void __launch_bounds__(kThreadsTC, kCtasPerSm) attn_fwd_tc_kernel(con
       if (!ok) record_timeout_attn(p.status);
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == kMma) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(128, kKB, 0, 0);  // Q, K both K-major
       const uint32_t id_o = idesc_bf16_f32(128, 64, 0, 1);   // P K-major, V MN-major
       bool ok = mbar_wait(q_full, 0, p.timeout_ns, abort_flag);
-      auto issue_s = [&](int j) -> bool {
+      // S_h = Q_h K^T of key block j (the block's K/V stage must have landed)
+      auto issue_s = [&](int j, int h) -> bool {
         const int st = j & 1;
         if (!mbar_wait(kv_full(st), (j >> 1) & 1, p.timeout_ns, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t kaddr = sb + kOffKV + st * 2 * kKVTile;
+        const uint32_t kaddr = sb + Lay::kOffKV + st * 2 * kKVTile;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_bf16_ss(tS, sw128_desc(sb + kOffQ + kk * 32, 16u, 1024u),
+          mma_bf16_ss(tS(h), sw128_desc(sb + Lay::kOffQ + h * kQTile + kk * 32, 16u, 1024u),
                       sw128_desc(kaddr + kk * 32, 16u, 1024u), id_s, kk > 0 ? 1u : 0u);
-        mma_commit(s_full);
+        mma_commit(s_full(h));
         return true;
       };
-      if (ok) ok = issue_s(0);
+      for (int h = 0; h < NH && ok; ++h) ok = issue_s(0, h);
       for (int j = 0; j < nkb && ok; ++j) {
-        if (!mbar_wait(p_full, j & 1, p.timeout_ns, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // S(j) has been read: the next block's scores go ahead of P V
-        if (j + 1 < nkb && !issue_s(j + 1)) {
-          ok = false;
-          break;
-        }
         const int st = j & 1;
-        const uint32_t vaddr = sb + kOffKV + st * 2 * kKVTile + kKVTile;
+        const uint32_t vaddr = sb + Lay::kOffKV + st * 2 * kKVTile + kKVTile;
+        // the heads in turn: while one head's softmax runs, the other's MMAs do
+        for (int h = 0; h < NH && ok; ++h) {
+          if (!mbar_wait(p_full(h), j & 1, p.timeout_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // S_h(j) has been read: the next block's scores go ahead of P V
+          if (j + 1 < nkb && !issue_s(j + 1, h)) {
+            ok = false;
+            break;
+          }
 #pragma unroll
-        for (int kk = 0; kk < kKB / 16; ++kk)
-          mma_bf16_ss(tO, sw128_desc(sb + kOffP + kk * 32, 16u, 1024u),
-                      sw128_desc(vaddr + kk * 2048, 8192u, 1024u), id_o,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(o_done);
-        mma_commit(kv_empty(st));
+          for (int kk = 0; kk < kKB / 16; ++kk)
+            mma_bf16_ss(tO(h), sw128_desc(sb + Lay::kOffP + h * (kQ * kKB * 2) + kk * 32, 16u, 1024u),
+                        sw128_desc(vaddr + kk * 2048, 8192u, 1024u), id_o,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(o_done(h));
+        }
+        if (ok) mma_commit(kv_empty(st));  // after every head's P V of block j
       }
       if (!ok) record_timeout_attn(p.status);
     }
     __syncwarp();
   } else {
-    // ---------------------------------------------------------------- softmax (warps 0-3)
-    const int r = threadIdx.x;  // query row within the tile = TMEM lane
+    // ---------------------------------------------------------------- softmax (4 warps per head)
+    const int hh = warp >> 2, quarter = warp & 3;
+    const int t = t0 + hh;
+    const int r = quarter * 32 + lane;  // query row within the tile = TMEM lane
     const int qi = q0 + r;
-    const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lanes = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t sP = sb + Lay::kOffP + hh * (kQ * kKB * 2);
     float m2 = -INFINITY, l = 0.0f;
     bool ok = true;
     auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
@@ -230,15 +266,15 @@ __global__ void __launch_bounds__(kThreadsTC, kCtasPerSm) attn_fwd_tc_kernel(con
       return __shfl_sync(0xFFFFFFFFu, w, 0) != 0;
     };
     for (int j = 0; j < nkb; ++j) {
-      if (!wait_all(s_full, j & 1)) {
+      if (!wait_all(s_full(hh), j & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const int k0 = j * kKB;
       uint32_t v[kKB];  // the row's 64 scores, read once
-      tmem_ld32(tS + lanes, *reinterpret_cast<uint32_t(*)[32]>(v));
-      tmem_ld32(tS + lanes + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      tmem_ld32(tS(hh) + lanes, *reinterpret_cast<uint32_t(*)[32]>(v));
+      tmem_ld32(tS(hh) + lanes + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
       tmem_ld_wait();
       // the block's row maximum (masked keys: beyond the sequence, or after the query)
       const bool full = k0 + kKB <= p.s && !(p.causal && k0 + kKB - 1 > qi);
@@ -266,7 +302,7 @@ __global__ void __launch_bounds__(kThreadsTC, kCtasPerSm) attn_fwd_tc_kernel(con
       const float m_use = m_new == -INFINITY ? 0.0f : m_new;
       const float corr = move ? ex2_approx(m2 - m_use) : 1.0f;  // 0 on the first block
       // P may be overwritten and O rescaled once the previous block's P V is complete
-      if (j > 0 && !wait_all(o_done, (j - 1) & 1)) {
+      if (j > 0 && !wait_all(o_done(hh), (j - 1) & 1)) {
         ok = false;
         break;
       }
@@ -281,7 +317,7 @@ __global__ void __launch_bounds__(kThreadsTC, kCtasPerSm) attn_fwd_tc_kernel(con
       }
 #pragma unroll
       for (int ch = 0; ch < kKB / 8; ++ch) {  // 8 keys = 16 bytes per store
-        const uint32_t addr = sb + kOffP + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4);
+        const uint32_t addr = sP + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4);
         const uint32_t* q8 = v + 8 * ch;
         st_shared_v4(addr,
                      pack_bf16x2(__uint_as_float(q8[0]), __uint_as_float(q8[1])),
@@ -295,40 +331,30 @@ __global__ void __launch_bounds__(kThreadsTC, kCtasPerSm) attn_fwd_tc_kernel(con
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t o[32];
-          tmem_ld32(tO + lanes + c * 32, o);
+          tmem_ld32(tO(hh) + lanes + c * 32, o);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
-          tmem_st32(tO + lanes + c * 32, o);
+          tmem_st32(tO(hh) + lanes + c * 32, o);
         }
         tmem_st_wait();
       }
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(p_full(hh));
     }
-    if (ok && wait_all(o_done, (nkb - 1) & 1)) {
+    if (ok && wait_all(o_done(hh), (nkb - 1) & 1)) {
       tc_fence_after();
       const float inv = 1.0f / l;
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) +
                             (static_cast<int64_t>(row0) + qi) * p.ldo + static_cast<int64_t>(t) * 64;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tO + lanes + c * 32, v);
+        uint32_t o[32];
+        tmem_ld32(tO(hh) + lanes + c * 32, o);
         tmem_ld_wait();
-        if (qi < p.s) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(v[8 * u]) * inv, __uint_as_float(v[8 * u + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]) * inv, __uint_as_float(v[8 * u + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]) * inv, __uint_as_float(v[8 * u + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]) * inv, __uint_as_float(v[8 * u + 7]) * inv);
-            reinterpret_cast<uint4*>(orow + c * 32)[u] = w;
-          }
-        }
+        if (qi < p.s) st_row_bf16(orow + c * 32, o, inv);
       }
       if (qi < p.s)
         p.lse[(static_cast<int64_t>(b) * p.H + t) * p.s + qi] = (m2 + log2f(l)) * 0.6931471805599453f;
@@ -341,23 +367,23 @@ __global__ void __launch_bounds__(kThreadsTC, kCtasPerSm) attn_fwd_tc_kernel(con
   __syncthreads();
   if (*abort_flag) {
     volatile int no_abort = 0;
-    if (warp == 4 && lane == 0) {  // the copies this CTA issued have landed
+    if (warp == kProd && lane == 0) {  // the copies this CTA issued have landed
       mbar_wait(q_full, 0, kDrainNs, &no_abort);
       for (int st = 0; st < 2; ++st) {
         const int n = issued_kv > st ? (issued_kv - 1 - st) / 2 : -1;  // last block on stage st
         if (n >= 0) mbar_wait(kv_full(st), n & 1, kDrainNs, &no_abort);
       }
     }
-    if (warp == 5 && lane == 0) {  // and the MMAs it issued have completed
+    if (warp == kMma && lane == 0) {  // and the MMAs it issued have completed
       mma_commit(drain);
       mbar_wait(drain, 0, kDrainNs, &no_abort);
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMma) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, Lay::kTmemCols);
   }
 }
 
@@ -424,17 +450,6 @@ __global__ void __launch_bounds__(256) attn_bwd_dsum_kernel(const __nv_bfloat16*
   }
 }
 
-__device__ __forceinline__ void st_row_bf16(__nv_bfloat16* dst, const uint32_t* v, float mul) {
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    uint4 w;
-    w.x = pack_bf16x2(__uint_as_float(v[8 * u]) * mul, __uint_as_float(v[8 * u + 1]) * mul);
-    w.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]) * mul, __uint_as_float(v[8 * u + 3]) * mul);
-    w.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]) * mul, __uint_as_float(v[8 * u + 5]) * mul);
-    w.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]) * mul, __uint_as_float(v[8 * u + 7]) * mul);
-    reinterpret_cast<uint4*>(dst)[u] = w;
-  }
-}
 
 constexpr int kThreadsBwd = 320;  // warps 0-7 element-wise, 8 TMA, 9 MMA
 
@@ -980,13 +995,23 @@ tp_status launch_attention_fwd_tc(const void* qkv, void* o, float* lse, int64_t 
   p.timeout_ns = wait_timeout_ns();
   static std::atomic<uint64_t> attr_set{0};
   if (needs_setup(attr_set)) {
-    TP_CUDA_TRY(cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kSmem));
+    TP_CUDA_TRY(cudaFuncSetAttribute(attn_fwd_tc_kernel<1>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     FwdLayout<1>::kSmem));
+    TP_CUDA_TRY(cudaFuncSetAttribute(attn_fwd_tc_kernel<2>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     FwdLayout<2>::kSmem));
     mark_device(attr_set);
   }
-  const dim3 grid(static_cast<unsigned>((s + kQ - 1) / kQ), static_cast<unsigned>(heads),
+  // two query heads per CTA when a key/value head's query heads come in pairs (the
+  // pair shares every K/V block, and one head's softmax overlaps the other's MMAs)
+  const int nh = g % 2 == 0 ? 2 : 1;
+  const dim3 grid(static_cast<unsigned>((s + kQ - 1) / kQ), static_cast<unsigned>(heads / nh),
                   static_cast<unsigned>(b));
-  attn_fwd_tc_kernel<<<grid, kThreadsTC, kSmem, st>>>(p);
+  if (nh == 2)
+    attn_fwd_tc_kernel<2><<<grid, FwdLayout<2>::kThreads, FwdLayout<2>::kSmem, st>>>(p);
+  else
+    attn_fwd_tc_kernel<1><<<grid, FwdLayout<1>::kThreads, FwdLayout<1>::kSmem, st>>>(p);
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;
