@@ -1,21 +1,26 @@
-// Tensor-core attention forward, head_dim 64, bf16: O = softmax(Q K^T / sqrt(d)) V per
-// query head, with the head map of the CUDA-core kernels (multi-head layout or
-// grouped-query per-shard blocks). Same outputs: O (bf16) and lse (fp32, natural log).
+// Tensor-core attention, head_dim 64, bf16, forward and backward, with the head map of
+// the CUDA-core kernels (multi-head layout or grouped-query per-shard blocks). Same
+// outputs: O (bf16) and lse (fp32, natural log); dqkv (bf16).
 //
-// One CTA per (128 query rows, query head); keys in blocks of 64 (about 66 KB of shared
-// memory and 64 + 64 TMEM columns a CTA, so two CTAs share an SM and one CTA's softmax
-// overlaps the other's MMAs; 128-key blocks with one CTA per SM took 1.5x longer):
-//   warp 4 (one lane) loads Q once and K, V blocks into two stages with TMA straight
-//     from the qkv rows (128-byte swizzle, 64 columns = one head);
-//   warp 5 (one lane) owns TMEM (S: 64 columns, O: 64) and issues
-//     S = Q K^T (M 128, N 64, K 64) and O += P V (M 128, N 64, K 64);
-//   warps 0-3, one thread per query row, read S from TMEM, keep the running maximum
-//     and sum (base 2, online softmax), write P = 2^(s - m) as bf16 into shared memory
-//     in the swizzled K-major layout the MMA reads, and rescale O in TMEM when the
-//     maximum grows.
-// Ordering: P and the O rescale wait for the previous block's P V (o_done); the next
-// S is issued once the softmax warps have handed over P (p_full), i.e. after they have
-// read the current S; a K/V stage is refilled after its P V completes (kv_empty).
+// Forward: O = softmax(Q K^T / sqrt(d)) V. One CTA per (128 query rows, NH query heads),
+// NH = 2 when a key/value head's query heads come in pairs (they share every K/V block),
+// else 1; keys in blocks of 64; two CTAs per SM, so one CTA's softmax overlaps the
+// other's MMAs (128-key blocks with one CTA per SM took 1.5x longer):
+//   the TMA warp (one lane) loads the NH Q tiles once and K, V blocks into two stages
+//     straight from the qkv rows (128-byte swizzle, 64 columns = one head);
+//   the MMA warp (one lane) owns TMEM (per head S: 64 columns, O: 64) and issues
+//     S = Q K^T (M 128, N 64, K 64) and O += P V (M 128, N 64, K 64), serving the
+//     heads in turn;
+//   four softmax warps per head, one thread per query row, read a block's scores from
+//     TMEM once, keep the running maximum (moved lazily) and sum (base 2), write
+//     P = 2^(s - m) as bf16 into shared memory in the swizzled K-major layout the MMA
+//     reads, and rescale O in TMEM when the maximum moves.
+// Ordering: P and the O rescale wait for the head's previous P V (o_done); once the
+// softmax warps hand over P (p_full) -- after reading the current S -- the next block's
+// S is issued ahead of this block's P V; a K/V stage is refilled after every head's P V
+// of it completes (kv_empty).
+// Backward (below): a D / lse pair kernel, then dK/dV and dQ kernels that recompute S
+// and dP in TMEM.
 // Every wait is bounded; on a timeout the CTA records TP_ERR_TIMEOUT, stops issuing,
 // waits (bounded) for its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
