@@ -888,8 +888,8 @@ def run_gqa(args, w, T, device, rank, nranks):
                    "parallelism": f"tp{N} virtual ranks per GPU, dp{nranks}",
                    "l2": "activations larger than L2 (no flush)"},
         "roofline": {"bound": "tensor", "kernel": "gemm_tc2_kernel (pair tcgen05 GEMM, 256 x 256 "
-                     "tiles on CTA pairs; 43 % of the step's GPU time, its four 2048-wide "
-                     "launches 26 %), timed on its own as the dO GEMM "
+                     "tiles on CTA pairs; 44 % of the step's GPU time, its four 2048-wide "
+                     "launches 27 %), timed on its own as the dO GEMM "
                      f"(M {M} x N {h} x K {h}) through tp_gemm",
                      "achieved": round(gemm_tf, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(gemm_tf / peak, 4),
