@@ -194,3 +194,65 @@ def test_gqa_wrong_group_is_caught(monkeypatch):
     import pytest
     with pytest.raises(AssertionError):
         qp.test_gqa_grouping_head_by_head()
+
+
+def test_gqa_core_kv_grad_not_summed_over_group_is_caught(monkeypatch):
+    """The attention core's key/value gradient overwritten by each query head of its
+    group instead of summed over them."""
+    from oracle import gqa_oracle as Q
+    from oracle import tp_oracle as T0
+    from tests import test_oracle_gqa_pins as qp
+
+    def bad(QKV, dO, b, s, H, Hkv, N, causal=False):
+        d = dO.shape[1] // H
+        hq, hkv, Ws = Q._shard_views(H, Hkv, N, d)
+        g = hq // hkv
+        dQKV = np.zeros_like(QKV)
+        for i in range(N):
+            Qi, dQi = QKV[:, i * Ws:(i + 1) * Ws], dQKV[:, i * Ws:(i + 1) * Ws]
+            dOi = dO[:, i * hq * d:(i + 1) * hq * d]
+            for tl in range(hq):
+                kl = tl // g
+                qc = slice(tl * d, (tl + 1) * d)
+                kc = slice((hq + kl) * d, (hq + kl + 1) * d)
+                vc = slice((hq + hkv + kl) * d, (hq + hkv + kl + 1) * d)
+                for bb in range(b):
+                    rr = slice(bb * s, (bb + 1) * s)
+                    dq, dk, dv = T0.attention_head_bwd(Qi[rr, qc], Qi[rr, kc], Qi[rr, vc],
+                                                       dOi[rr, qc], causal)
+                    dQi[rr, qc] += dq
+                    dQi[rr, kc] = dk   # the mistake: the group's heads overwrite each other
+                    dQi[rr, vc] = dv
+        return dQKV
+    monkeypatch.setattr(Q, "gqa_attention_bwd", bad)
+    import pytest
+    with pytest.raises(AssertionError):
+        qp.test_gqa_core_bwd_fd(4, 2, 2, False)
+
+
+def test_gqa_core_wrong_local_kv_head_is_caught(monkeypatch):
+    """Inside a shard, local query head tl paired with local key/value head tl % hkv
+    instead of tl // g."""
+    from oracle import gqa_oracle as Q
+    from oracle import tp_oracle as T0
+    from tests import test_oracle_gqa_pins as qp
+
+    def bad(QKV, b, s, H, Hkv, N, causal=False):
+        hq, hkv, _ = Q.gqa_split(H, Hkv, N)
+        d = QKV.shape[1] // (N * (hq + 2 * hkv))
+        Ws = (hq + 2 * hkv) * d
+        O = np.zeros((QKV.shape[0], H * d))
+        for i in range(N):
+            Qi = QKV[:, i * Ws:(i + 1) * Ws]
+            for tl in range(hq):
+                kl = tl % hkv  # the mistake
+                for bb in range(b):
+                    r = slice(bb * s, (bb + 1) * s)
+                    O[r, (i * hq + tl) * d:(i * hq + tl + 1) * d] = T0.attention_head_fwd(
+                        Qi[r, tl * d:(tl + 1) * d], Qi[r, (hq + kl) * d:(hq + kl + 1) * d],
+                        Qi[r, (hq + hkv + kl) * d:(hq + hkv + kl + 1) * d], causal)[0]
+        return O
+    monkeypatch.setattr(Q, "gqa_attention_fwd", bad)
+    import pytest
+    with pytest.raises(AssertionError):
+        qp.test_gqa_sharded_equals_unsplit(8, 2, 1, False)   # hq = 8, hkv = 2: g = 4
