@@ -207,7 +207,14 @@ cudaError_t launch_k(const SimtParams& p, dim3 grid, cudaStream_t st) {
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_simt_kernel<EPI, PAIRED>, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_simt_kernel<EPI, PAIRED>, p);
+  if (e == cudaSuccess) return e;
+  // a cluster the device cannot place (e.g. too few SMs in a partition): run unsplit
+  cudaGetLastError();
+  SimtParams q = p;
+  q.split = 1;
+  gemm_simt_kernel<EPI, PAIRED><<<grid, 256, 0, st>>>(q);
+  return cudaGetLastError();
 }
 
 }  // namespace
