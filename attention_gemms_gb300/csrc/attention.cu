@@ -13,9 +13,11 @@
 //   backward: P = exp(S - lse), Dr = rowsum(dO * O), dV = P^T dO, dP = dO V^T,
 //             dS = P * (dP - Dr), dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d)
 // At the page-2 layer's sizes (s = 128, d = 16) this is a few MFLOP per head, so
-// the kernels use CUDA cores: d/16 lanes per query row (forward, dQ) or key row
-// (dK, dV), 64 rows per CTA, the other operand streamed through shared memory in
-// blocks of 64 rows; softmax statistics in fp32.
+// these kernels use CUDA cores: four lanes per query row (forward, dQ) or key row
+// (dK, dV), which split the head dimensions and the streamed rows between them; 64
+// rows per CTA, the other operand streamed through shared memory in blocks of 64
+// rows; softmax statistics in fp32. bf16 at head_dim 64 runs on the tensor cores
+// (attention_tc.cu).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
