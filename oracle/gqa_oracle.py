@@ -90,8 +90,9 @@ def _shard_views(H, Hkv, N, d):
 
 def gqa_attention_fwd(QKV, b, s, H, Hkv, N, causal=False):
     """The attention core on the sharded QKV (M, N S): shard i's local query head tl
-    attends with its local key/value head tl // g, every batch element on its own.
-    Returns O (M, H d), the heads in order."""
+    attends with its local key/value head tl // g, every batch element on its own, each
+    head by `tp_oracle.attention_head_fwd` [Megatron-LM 实战 04, TPAttention; 张量并行
+    notes, §相关分析, GQA]. Returns O (M, H d), the heads in order."""
     M = QKV.shape[0]
     hq, hkv, _ = gqa_split(H, Hkv, N)
     d = QKV.shape[1] // (N * (hq + 2 * hkv))
@@ -113,9 +114,10 @@ def gqa_attention_fwd(QKV, b, s, H, Hkv, N, causal=False):
 
 
 def gqa_attention_bwd(QKV, dO, b, s, H, Hkv, N, causal=False):
-    """Backward of `gqa_attention_fwd`: dQKV (M, N S) in the same layout; a key/value
-    head's gradient sums the contributions of its shard's query heads that use it (a
-    replica's share when N > Hkv)."""
+    """Backward of `gqa_attention_fwd`: dQKV (M, N S) in the same layout, each head by
+    `tp_oracle.attention_head_bwd`; a key/value head's gradient sums the contributions
+    of its shard's query heads that use it (a replica's share when N > Hkv; the
+    replicas' all-reduce is the block's, in `gqa_block_bwd`)."""
     d = dO.shape[1] // H
     hq, hkv, Ws = _shard_views(H, Hkv, N, d)
     g = hq // hkv
