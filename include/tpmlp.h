@@ -476,7 +476,7 @@ TP_API tp_status tp_gqa_pack_qkv(const void* Wq, const void* Wk, const void* Wv,
  * least tp_gqa_attention_bwd_workspace_size(b, s, n_heads) bytes, 16-byte aligned: with
  * it, bf16 at head_dim 64 runs on the tensor cores (the per-row (lse, D = rowsum(dO * O))
  * pairs are kept there); with ws == NULL every case runs on the CUDA cores. A ws that is
- * given but too small is TP_ERR_WORKSPACE. */
+ * given but too small is TP_ERR_WORKSPACE, one not 16-byte aligned TP_ERR_ALIGNMENT. */
 TP_API size_t tp_gqa_attention_bwd_workspace_size(int64_t b, int64_t s, int32_t n_heads);
 TP_API tp_status tp_gqa_attention_fwd(const void* qkv, void* o, float* lse, int64_t b, int64_t s,
                                       int64_t h, int32_t n_heads, int32_t n_kv_heads, int32_t N,
