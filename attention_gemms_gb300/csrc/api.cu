@@ -30,10 +30,27 @@ tp_status check_dtype(tp_dtype dt) {
   return need(dt == TP_BF16 || dt == TP_F32, TP_ERR_DTYPE, "dtype must be TP_BF16 or TP_F32");
 }
 
+// Extents of buffers that can exist in device memory: every extent below 2^31, a
+// matrix below 2^40 elements, at most 65536 shards. Sizes past these limits are
+// rejected before any byte count is formed, so N * rows * cols * 4 and the workspace
+// sums built from such products cannot wrap around in 64 bits.
+bool extents_ok(int64_t rows, int64_t cols, int64_t N) {
+  constexpr int64_t kMaxExtent = int64_t(1) << 31, kMaxElems = int64_t(1) << 40;
+  return rows >= 0 && cols >= 0 && rows < kMaxExtent && cols < kMaxExtent && N >= 1 &&
+         N <= 65536 && rows * cols < kMaxElems;
+}
+tp_status check_extents(int64_t rows, int64_t cols, int64_t N) {
+  return need(extents_ok(rows, cols, N), TP_ERR_SHAPE,
+              "sizes too large (an extent >= 2^31, a matrix >= 2^40 elements or N > 65536)");
+}
+
 // bf16 tile rules: reduced widths and per-shard widths are whole 64-column blocks
 tp_status check_mlp_shape(int64_t M, int64_t h, int64_t f, int32_t N, tp_dtype dt) {
   TP_TRY(need(N >= 1, TP_ERR_INVALID_ARG, "shard count N must be >= 1"));
   TP_TRY(need(M >= 0 && h >= 1 && f >= 1, TP_ERR_INVALID_ARG, "sizes must be positive (M >= 0)"));
+  TP_TRY(check_extents(M, h, N));
+  TP_TRY(check_extents(M, f, N));
+  TP_TRY(check_extents(h, f, 1));
   TP_TRY(need(f % N == 0, TP_ERR_SHAPE, "h' (f) must be divisible by the shard count N"));
   if (dt == TP_BF16) {
     TP_TRY(need(h % 64 == 0, TP_ERR_SHAPE, "bf16 path: h must be a multiple of 64"));
@@ -42,8 +59,16 @@ tp_status check_mlp_shape(int64_t M, int64_t h, int64_t f, int32_t N, tp_dtype d
   return TP_OK;
 }
 
+// fp32 shard partials of variant A; saturates at 2^62 bytes (no wrap-around) for sizes
+// that check_extents would reject
 size_t partial_bytes(int64_t M, int64_t n, int32_t N, tp_reduce mode) {
-  return mode == TP_REDUCE_BUFFERS ? static_cast<size_t>(N) * M * n * sizeof(float) : 0;
+  if (mode != TP_REDUCE_BUFFERS || M <= 0 || n <= 0 || N <= 0) return 0;
+  constexpr size_t kCap = size_t(1) << 62;
+  const size_t rows = static_cast<size_t>(M), cols = static_cast<size_t>(n);
+  if (cols > kCap / rows) return kCap;
+  const size_t elems = rows * cols;
+  if (elems > kCap / (sizeof(float) * static_cast<size_t>(N))) return kCap;
+  return elems * static_cast<size_t>(N) * sizeof(float);
 }
 
 tp_status col_impl(const void* X, const void* W, const void* Wu, void* Y, void* Yu, void* out,
@@ -183,6 +208,8 @@ size_t tp_workspace_size(tp_op op, int64_t M, int64_t h, int64_t f, int32_t N, t
                                    op != TP_OP_LAYERNORM_BWD))
     return 0;
   if (dtype != TP_BF16 && dtype != TP_F32) return 0;
+  // sizes the entry points reject (check_extents) need no workspace either
+  if (!extents_ok(M, 3 * h, N) || !extents_ok(M, f, N) || !extents_ok(h, f, 1)) return 0;
   const size_t elt = elem_size(dtype);
   switch (op) {
     case TP_OP_COL_LINEAR: return 0;
@@ -255,6 +282,9 @@ tp_status tp_row_linear(const void* Xs, const void* W, const void* residual, voi
   TP_TRY(need(Xs && W && out, TP_ERR_INVALID_ARG, "Xs, W and out are required"));
   TP_TRY(need(N >= 1, TP_ERR_INVALID_ARG, "shard count N must be >= 1"));
   TP_TRY(need(M >= 0 && k >= 1 && n >= 1, TP_ERR_INVALID_ARG, "sizes must be positive (M >= 0)"));
+  TP_TRY(check_extents(M, n, N));
+  TP_TRY(check_extents(M, k, 1));
+  TP_TRY(check_extents(k, n, 1));
   TP_TRY(need(k % N == 0, TP_ERR_SHAPE, "k must be divisible by the shard count N"));
   if (dtype == TP_BF16) {
     TP_TRY(need((k / N) % 64 == 0, TP_ERR_SHAPE, "bf16 path: k/N must be a multiple of 64"));
@@ -275,6 +305,7 @@ tp_status tp_shard_reduce(const float* partials, const void* residual, void* out
   TP_TRY(check_dtype(out_dtype));
   TP_TRY(need(partials && out, TP_ERR_INVALID_ARG, "partials and out are required"));
   TP_TRY(need(N >= 1 && M >= 0 && n >= 1, TP_ERR_INVALID_ARG, "need N >= 1, M >= 0, n >= 1"));
+  TP_TRY(check_extents(M, n, N));
   TP_TRY(check_aligned({partials, residual, out}));
   if (M == 0) return TP_OK;
   TP_TRY(check_device());
@@ -291,6 +322,7 @@ tp_status tp_shard_reduce_ln(const float* partials, const void* residual, const 
               "partials, gamma, beta and y are required"));
   TP_TRY(need(N >= 1 && M >= 0 && h >= 1 && eps >= 0.0f, TP_ERR_INVALID_ARG,
               "need N >= 1, M >= 0, h >= 1, eps >= 0"));
+  TP_TRY(check_extents(M, h, N));
   TP_TRY(need(h % 8 == 0 && h <= kReduceLnMaxH, TP_ERR_SHAPE,
               "fused reduce + LayerNorm: h must be a multiple of 8 and at most 16384"));
   TP_TRY(check_aligned({partials, residual, gamma, beta, sum_out, y, mean, rstd}));
@@ -313,6 +345,9 @@ tp_status tp_row_linear_ln(const void* Xs, const void* W, const void* residual,
   TP_TRY(need(N >= 1, TP_ERR_INVALID_ARG, "shard count N must be >= 1"));
   TP_TRY(need(M >= 0 && k >= 1 && n >= 1 && eps >= 0.0f, TP_ERR_INVALID_ARG,
               "sizes must be positive (M >= 0) and eps >= 0"));
+  TP_TRY(check_extents(M, n, N));
+  TP_TRY(check_extents(M, k, 1));
+  TP_TRY(check_extents(k, n, 1));
   TP_TRY(need(k % N == 0, TP_ERR_SHAPE, "k must be divisible by the shard count N"));
   TP_TRY(need(n % 8 == 0 && n <= kReduceLnMaxH, TP_ERR_SHAPE,
               "fused reduce + LayerNorm: n must be a multiple of 8 and at most 16384"));
@@ -492,7 +527,7 @@ void* g_noalloc_ptr[64] = {};
 // Device address of g_noalloc_scratch on the current device. In host code the
 // symbol's name is only a host-side stand-in, so the address must come from
 // cudaGetSymbolAddress, called with that device current; it is looked up once per
-// device and cached.
+// device and cached (a cudaDeviceReset of the device invalidates the cached address).
 tp_status noalloc_scratch(void** out) {
   int dev = 0;
   TP_CUDA_TRY(cudaGetDevice(&dev));
@@ -516,6 +551,9 @@ extern "C" tp_status tp_row_linear_noalloc(const void* Xs, const void* W, const 
   TP_TRY(need(Xs && W && out, TP_ERR_INVALID_ARG, "Xs, W and out are required"));
   TP_TRY(need(N >= 1, TP_ERR_INVALID_ARG, "shard count N must be >= 1"));
   TP_TRY(need(M >= 0 && k >= 1 && n >= 1, TP_ERR_INVALID_ARG, "sizes must be positive (M >= 0)"));
+  TP_TRY(check_extents(M, n, N));
+  TP_TRY(check_extents(M, k, 1));
+  TP_TRY(check_extents(k, n, 1));
   TP_TRY(need(k % N == 0, TP_ERR_SHAPE, "k must be divisible by the shard count N"));
   if (dtype == TP_BF16) {
     TP_TRY(need((k / N) % 64 == 0, TP_ERR_SHAPE, "bf16 path: k/N must be a multiple of 64"));

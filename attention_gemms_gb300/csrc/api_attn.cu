@@ -13,6 +13,8 @@ tp_status check_attn_shape(int64_t b, int64_t s, int64_t h, int32_t heads, int32
                            tp_dtype dt) {
   TP_TRY(need(b >= 0 && s >= 0 && h >= 1 && heads >= 1 && N >= 1, TP_ERR_INVALID_ARG,
               "need b, s >= 0 and h, n_heads, N >= 1"));
+  TP_TRY(need(b < (int64_t(1) << 31) && s < (int64_t(1) << 31), TP_ERR_SHAPE, "b or s too large"));
+  TP_TRY(check_extents(b * s, 3 * h, N));
   TP_TRY(need(h % heads == 0, TP_ERR_SHAPE, "h must be divisible by n_heads"));
   // heads are split across shards: TP degree <= heads and heads % N == 0
   TP_TRY(need(heads % N == 0, TP_ERR_SHAPE, "n_heads must be divisible by the shard count N"));

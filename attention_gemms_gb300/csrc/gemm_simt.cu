@@ -13,6 +13,8 @@
 // result is deterministic; no workspace is needed.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include <algorithm>
 
 #include "epi_math.cuh"
@@ -190,10 +192,40 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const SimtParams p) {
   }
 }
 
+// Whether the device can place a cluster of `split` CTAs of this kernel: asked once per
+// device and cluster size (cudaOccupancyMaxActiveClusters), before the first launch.
+template <int EPI, bool PAIRED>
+bool cluster_fits(int split) {
+  static std::atomic<int> known[64][4];  // 0 unknown, 1 fits, 2 does not
+  const int slot = split == 2 ? 0 : split == 4 ? 1 : split == 8 ? 2 : 3;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = -1;
+  if (dev >= 0 && known[dev][slot].load() != 0) return known[dev][slot].load() == 1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(split);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(split), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  const bool fits = cudaOccupancyMaxActiveClusters(&n, gemm_simt_kernel<EPI, PAIRED>, &cfg) ==
+                        cudaSuccess && n > 0;
+  if (!fits) cudaGetLastError();  // the query's own error, not a launch's
+  if (dev >= 0) known[dev][slot].store(fits ? 1 : 2);
+  return fits;
+}
+
 template <int EPI, bool PAIRED>
 cudaError_t launch_k(const SimtParams& p, dim3 grid, cudaStream_t st) {
-  if (p.split == 1) {
-    gemm_simt_kernel<EPI, PAIRED><<<grid, 256, 0, st>>>(p);
+  if (p.split == 1 || !cluster_fits<EPI, PAIRED>(p.split)) {
+    // unsplit: one CTA per tile (also when the device cannot place the cluster)
+    SimtParams q = p;
+    q.split = 1;
+    gemm_simt_kernel<EPI, PAIRED><<<grid, 256, 0, st>>>(q);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -207,14 +239,7 @@ cudaError_t launch_k(const SimtParams& p, dim3 grid, cudaStream_t st) {
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_simt_kernel<EPI, PAIRED>, p);
-  if (e == cudaSuccess) return e;
-  // a cluster the device cannot place (e.g. too few SMs in a partition): run unsplit
-  cudaGetLastError();
-  SimtParams q = p;
-  q.split = 1;
-  gemm_simt_kernel<EPI, PAIRED><<<grid, 256, 0, st>>>(q);
-  return cudaGetLastError();
+  return cudaLaunchKernelEx(&cfg, gemm_simt_kernel<EPI, PAIRED>, p);
 }
 
 }  // namespace

@@ -220,6 +220,8 @@ tp_status check_aligned(std::initializer_list<const void*> ptrs);
 tp_status check_dtype(tp_dtype dt);
 tp_status check_device();
 size_t partial_bytes(int64_t M, int64_t n, int32_t N, tp_reduce mode);
+bool extents_ok(int64_t rows, int64_t cols, int64_t N);  // see check_extents
+tp_status check_extents(int64_t rows, int64_t cols, int64_t N);
 tp_status check_mlp_shape(int64_t M, int64_t h, int64_t f, int32_t N, tp_dtype dt);
 size_t sp_mlp_workspace_size(bool fwd, int64_t M, int64_t h, int64_t f, int32_t N, tp_dtype dt,
                              tp_act act, tp_reduce mode);

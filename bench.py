@@ -136,10 +136,15 @@ def dist_env():
 
 
 def dist_init(backend):
+    """One process group over the ranks, with a bounded timeout (TP_DIST_TIMEOUT_S,
+    default 300 s): a rank that has left makes the others' next barrier or timing
+    reduction raise instead of waiting forever."""
+    import datetime
     import torch.distributed as dist
     ws, rank, _ = dist_env()
     if ws > 1 and not dist.is_initialized():
-        dist.init_process_group(backend=backend)
+        timeout = datetime.timedelta(seconds=float(os.environ.get("TP_DIST_TIMEOUT_S", "300")))
+        dist.init_process_group(backend=backend, timeout=timeout)
     return ws, rank
 
 
@@ -302,6 +307,29 @@ def overlapped_e2e(stream, steps, step_on, ins, ins_host, outs, outs_host):
     return e0.elapsed_time(e1) / steps
 
 
+VENDOR_PEAKS = {"bf16_tflops": 2250.0, "hbm_gbs": 7900.0,
+                "label": "nominal dense bf16 2.25 PFLOP/s and HBM3e 7.9 TB/s (vendor class)"}
+
+
+def timed_steps(stream, steps, step):
+    """Time `steps` calls of step(i) on `stream`: one event pair brackets all of them
+    (the mean) and one pair per step gives the per-step distribution (the median).
+    Returns (mean ms, median ms)."""
+    import torch
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    t0, t1 = ev(), ev()
+    per = [(ev(), ev()) for _ in range(steps)]
+    t0.record(stream)
+    for i in range(steps):
+        per[i][0].record(stream)
+        step(i)
+        per[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    med = float(np.median([a.elapsed_time(b) for a, b in per]))
+    return t0.elapsed_time(t1) / steps, med
+
+
 def run_ours(args, w):
     import torch
     from attention_gemms_gb300 import build as B
@@ -325,7 +353,7 @@ def run_ours(args, w):
     M, h, f, N = w["b"] * w["s"], w["h"], w["f"], w["N"]
     sw = w["act"] == "swiglu"
     act = T.Act.SWIGLU if sw else T.Act.GELU
-    mode = T.Reduce.SPLITK if args.mode == "splitk" else T.Reduce.BUFFERS
+    modes = {"splitk": T.Reduce.SPLITK, "buffers": T.Reduce.BUFFERS}
     f32 = w.get("dtype") == "f32"
     BF = T.DType.F32 if f32 else T.DType.BF16
     bf = torch.float32 if f32 else torch.bfloat16
@@ -336,54 +364,16 @@ def run_ours(args, w):
     Y, Yu, H = e(M, f), (e(M, f) if sw else None), e(M, f)
     Z, dX = e(M, h), e(M, h)
     dW1, dW1u, dW2 = e(h, f), (e(h, f) if sw else None), e(f, h)
-    wsb = max(T.tp_workspace_size(T.Op.ROW_LINEAR, M, f, h, N, BF, T.Act.NONE, mode),
-              T.tp_workspace_size(T.Op.MLP_BWD, M, h, f, N, BF, act, mode))
+    wsb = max(T.tp_workspace_size(T.Op.ROW_LINEAR, M, f, h, N, BF, T.Act.NONE, m)
+              for m in modes.values())
+    wsb = max([wsb] + [T.tp_workspace_size(T.Op.MLP_BWD, M, h, f, N, BF, act, m)
+                       for m in modes.values()])
     ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
-    col_ev = []
-
-    def step_on(Xs, dZs, Zs, dXs, record=False):
-        if record:
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-        T.tp_col_linear(Xs, d["W1"], d["W1u"], Y, Yu, H, M, h, f, N, BF, act, stream)
-        if record:
-            b.record(stream)
-            col_ev.append((a, b))
-        T.tp_row_linear(H, d["W2"], None, Zs, M, f, h, N, BF, mode, ws, ws.numel(), stream)
-        T.tp_mlp_bwd(Xs, d["W1"], d["W1u"], d["W2"], Y, Yu, H, dZs, dXs, dW1, dW1u, dW2,
-                     M, h, f, N, BF, act, mode, ws, ws.numel(), stream)
-
-    def step(record=False):
-        step_on(d["X"], d["dZ"], Z, dX, record)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if T.tp_check_status(stream) != 0:
-        raise RuntimeError("device wait timeout during warm-up: " + T.tp_last_error())
-
-    clocks = ClockSampler(device.index)
-    clocks.start()
-    time.sleep(0.3)
-    barrier()
-    torch.cuda.synchronize()
-    n0 = T.tp_launch_count()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        step(record=True)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    launches = T.tp_launch_count() - n0
-    ms = t0.elapsed_time(t1) / args.steps
-    col_ms = sum(a.elapsed_time(b) for a, b in col_ev) / len(col_ev)
-    if T.tp_check_status(stream) != 0:
-        raise RuntimeError("device wait timeout in the timed region: " + T.tp_last_error())
-
-    # end to end: inputs in from pinned host memory and results out, every step,
-    # copies overlapped with the neighbouring steps' compute (overlapped_e2e)
+    flops = mlp_flops(w)
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_s = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     pin = lambda: torch.empty((M, h), dtype=bf, pin_memory=True)
     Xp, dZp = pin(), pin()
     if f32:
@@ -392,26 +382,74 @@ def run_ours(args, w):
     else:
         Xp.view(torch.int16).numpy()[:] = hostin["X"].view(np.int16)
         dZp.view(torch.int16).numpy()[:] = hostin["dZ"].view(np.int16)
-    barrier()
-    e2e_ms = overlapped_e2e(stream, args.steps, lambda i, o: step_on(i[0], i[1], o[0], o[1]),
-                            [d["X"], d["dZ"]], [Xp, dZp], [Z, dX], [pin(), pin()])
-    barrier()
+    outs_host = [pin(), pin()]
+
+    def measure(mode_name):
+        """Warm-up, the timed steps (device-resident inputs) and the end-to-end steps of
+        one shard-sum variant; per-rank ms, the column GEMM's ms and the launch count."""
+        mode = modes[mode_name]
+        col_ev = []
+
+        def step_on(Xs, dZs, Zs, dXs, record=False):
+            if record:
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+            T.tp_col_linear(Xs, d["W1"], d["W1u"], Y, Yu, H, M, h, f, N, BF, act, stream)
+            if record:
+                b.record(stream)
+                col_ev.append((a, b))
+            T.tp_row_linear(H, d["W2"], None, Zs, M, f, h, N, BF, mode, ws, ws.numel(), stream)
+            T.tp_mlp_bwd(Xs, d["W1"], d["W1u"], d["W2"], Y, Yu, H, dZs, dXs, dW1, dW1u, dW2,
+                         M, h, f, N, BF, act, mode, ws, ws.numel(), stream)
+
+        for _ in range(args.warmup):
+            step_on(d["X"], d["dZ"], Z, dX)
+        torch.cuda.synchronize()
+        if T.tp_check_status(stream) != 0:
+            raise RuntimeError("device wait timeout during warm-up: " + T.tp_last_error())
+        barrier()
+        torch.cuda.synchronize()
+        n0 = T.tp_launch_count()
+        ms, med = timed_steps(stream, args.steps,
+                              lambda i: step_on(d["X"], d["dZ"], Z, dX, record=True))
+        barrier()
+        launches = T.tp_launch_count() - n0
+        col_ms = sum(a.elapsed_time(b) for a, b in col_ev) / len(col_ev)
+        if T.tp_check_status(stream) != 0:
+            raise RuntimeError("device wait timeout in the timed region: " + T.tp_last_error())
+        # end to end: inputs in from pinned host memory and results out, every step,
+        # copies overlapped with the neighbouring steps' compute (overlapped_e2e)
+        barrier()
+        e2e_ms = overlapped_e2e(stream, args.steps, lambda i, o: step_on(i[0], i[1], o[0], o[1]),
+                                [d["X"], d["dZ"]], [Xp, dZp], [Z, dX], outs_host)
+        barrier()
+        if T.tp_check_status(stream) != 0:
+            raise RuntimeError("device wait timeout in the end-to-end steps: " + T.tp_last_error())
+        return {"ms": max_over_ranks(ms, device), "median": max_over_ranks(med, device),
+                "col": max_over_ranks(col_ms, device), "e2e": max_over_ranks(e2e_ms, device),
+                "launches": launches}
+
+    clocks = ClockSampler(device.index)
+    clocks.start()
+    time.sleep(0.3)
+    main_r = measure(args.mode)
+    others = {}
+    if args.variants and not f32:
+        for name in modes:
+            if name != args.mode:
+                others[name] = measure(name)
     clk = clocks.stop()
 
-    ms_max = max_over_ranks(ms, device)
-    e2e_max = max_over_ranks(e2e_ms, device)
-    col_max = max_over_ranks(col_ms, device)
-    flops = mlp_flops(w)
+    ms_max, e2e_max, col_max = main_r["ms"], main_r["e2e"], main_r["col"]
     value = flops * ws_ / (ms_max * 1e-3) / 1e12
     e2e_val = flops * ws_ / (e2e_max * 1e-3) / 1e12
-    peaks, src = load_peaks()
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    peak_s = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     col_tf = col_gemm_flops(w) / (col_max * 1e-3) / 1e12
     traffic = col_gemm_traffic(args.workload)
+    vp = VENDOR_PEAKS["bf16_tflops"]
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws_,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+        "ms_per_step_median": round(main_r["median"], 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if f32 else "bf16",
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights; random init)",
@@ -420,21 +458,37 @@ def run_ours(args, w):
                    "seq_len": w["s"], "parallelism": f"tp{N} virtual ranks per GPU, dp{ws_}",
                    "l2": "inputs larger than L2 (no flush)"},
         "pct_of_peak": round(100 * value / ws_ / peak, 2),
-        "roofline": {"bound": "tensor", "kernel": "gemm_tc_kernel (column-parallel GEMM + fused "
+        "pct_of_vendor_peak": round(100 * value / ws_ / vp, 2),
+        "roofline": {"bound": "tensor", "kernel": "gemm_tc2_kernel (column-parallel GEMM + fused "
                      + ("SwiGLU" if sw else "GELU") + " epilogue)",
                      "achieved": round(col_tf, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(col_tf / peak, 4), "frac_of_sustained": round(col_tf / peak_s, 4),
-                     "peak_source": f"{src} bf16 dense (burst)", "traffic": traffic,
+                     "frac_of_vendor": round(col_tf / vp, 4),
+                     "peak_source": f"{src} bf16 dense (burst)",
+                     "vendor_peak": {"value": vp, "label": VENDOR_PEAKS["label"]},
+                     "traffic": traffic,
                      "algorithmic_flops_per_launch": col_gemm_flops(w),
                      "avg_launch_ms": round(col_max, 4)},
         "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": 2 * M * h * (4 if f32 else 2),
                 "d2h_bytes_per_step": 2 * M * h * (4 if f32 else 2),
                 "ms_per_step": round(e2e_max, 4)},
-        "gpu_launches": int(launches),
+        "gpu_launches": int(main_r["launches"]),
         "clocks": clk,
         "input_gen_s": round(t_gen, 1),
     }
+    if others:
+        var = {}
+        for name, r in [(args.mode, main_r)] + list(others.items()):
+            tf = flops * ws_ / (r["ms"] * 1e-3) / 1e12
+            var[name] = {"ms_per_step": round(r["ms"], 4), "ms_per_step_median": round(r["median"], 4),
+                         "TFLOPs": round(tf, 2), "pct_of_peak": round(100 * tf / ws_ / peak, 2),
+                         "e2e_TFLOPs": round(flops * ws_ / (r["e2e"] * 1e-3) / 1e12, 2),
+                         "column_gemm_ms": round(r["col"], 4), "gpu_launches": int(r["launches"])}
+        var["note"] = ("splitk: the row-parallel sums folded as split-K into one accumulator; "
+                       "buffers: per-shard fp32 partials summed by the shard-reduce kernel; "
+                       "both timed in this process, same steps and warm-up")
+        out["shard_sum_variants"] = var
     if f32:
         out["roofline"] = {"bound": "alu", "note": "fp32 FFMA path at a latency-bound size; "
                            "no roofline fraction is claimed", "achieved": None, "peak": None,
@@ -1188,7 +1242,9 @@ def run_decode(args, device, T):
             "pct_of_peak": round(100 * gbs / hbm, 1),
             "weight_GBps": round(wbytes / (ms * 1e-3) / 1e9, 1),
             "TFLOPs": round(2 * nt * 3 * h * f / (ms * 1e-3) / 1e12, 2),
-            "roofline": {"bound": "hbm", "kernel": "gemm_tc_kernel (gate/up + SwiGLU)",
+            "roofline": {"bound": "hbm",
+                         "kernel": ("gemv_kernel<1, EPI_SWIGLU, paired> (gate/up + SwiGLU)" if nt == 1
+                                    else "gemm_tc_kernel<128, EPI_SWIGLU, decode> (gate/up + SwiGLU)"),
                          "achieved": round(col_bytes / (col * 1e-3) / 1e9, 1), "peak": hbm,
                          "unit": "GB/s", "frac": round(col_bytes / (col * 1e-3) / 1e9 / hbm, 4),
                          "avg_launch_ms": round(col, 4), "algorithmic_bytes": col_bytes},
@@ -1436,7 +1492,10 @@ def main(argv=None):
                          "c3-sp: sequence-parallel MLP block; gpt: small GPT training; "
                          "gqa: head-sharded grouped-query attention block; vocab-ce: the "
                          "vocabulary-parallel cross-entropy alone (M=8192, v=50304, N=8)")
-    ap.add_argument("--mode", default="splitk", choices=["splitk", "buffers"])
+    ap.add_argument("--mode", default="splitk", choices=["splitk", "buffers"],
+                    help="shard-sum variant of the main line (the other is timed beside it)")
+    ap.add_argument("--no-variants", dest="variants", action="store_false", default=True,
+                    help="time only --mode, not the other shard-sum variant")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--cpu-budget", type=float, default=15.0)

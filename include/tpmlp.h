@@ -371,6 +371,9 @@ TP_API tp_status tp_mlp_bwd(const void* X, const void* W1, const void* W1_up, co
  *   - Every device that loads the library holds the 32 MiB until the process exits.
  *   - The first call on each device looks up the array's device address (with that
  *     device current) and caches it; make that first call before any stream capture.
+ *     The cached address does not survive cudaDeviceReset (the reset discards the
+ *     array, which may come back elsewhere): do not call this entry point on a
+ *     device after resetting it in the same process.
  *   - All calls share the one array: calls that overlap on the GPU (e.g. on two
  *     streams at once) race. Nothing in it needs to start at zero: every partial
  *     that is read is written first by the same call.

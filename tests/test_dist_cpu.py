@@ -70,3 +70,54 @@ def test_reference_arm_only_on_rank0(monkeypatch):
     line = json.loads(buf.getvalue().strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def _dropout_worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank), TP_DIST_TIMEOUT_S="10")
+    import time
+    bench.dist_init("gloo")
+    bench.barrier()                     # step 1, both ranks
+    bench.max_over_ranks(1.0)
+    if rank == 1:                       # leaves between steps, nothing in flight
+        q.put((1, "left", 0.0))
+        q.close()
+        q.join_thread()                 # the message is out before the process ends
+        os._exit(0)
+    time.sleep(0.5)
+    for name, call in (("barrier", bench.barrier), ("max_over_ranks", lambda: bench.max_over_ranks(2.0))):
+        t0 = time.monotonic()
+        try:
+            call()
+            q.put((0, name + ": no error", time.monotonic() - t0))
+        except Exception as e:         # noqa: BLE001 -- any error is the expected outcome
+            q.put((0, name + ": " + type(e).__name__, time.monotonic() - t0))
+    q.close()
+    q.join_thread()
+    os._exit(0)
+
+
+def test_rank_leaving_between_steps_fails_the_survivor_in_bounded_time():
+    """A rank leaves between two steps (the launch of `torchrun --nproc_per_node=2` on
+    the pages); the other rank's next barrier and timing reduction must raise within
+    the process-group timeout rather than wait forever."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_dropout_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    try:
+        got = [q.get(timeout=120) for _ in range(3)]
+    finally:
+        for p in procs:
+            p.join(timeout=30)
+            if p.is_alive():
+                p.kill()
+    left = [g for g in got if g[0] == 1]
+    surv = {g[1].split(":")[0]: g for g in got if g[0] == 0}
+    assert left and left[0][1] == "left"
+    for name in ("barrier", "max_over_ranks"):
+        _, msg, dt = surv[name]
+        assert "no error" not in msg, msg
+        assert dt < 60.0, (name, dt)
