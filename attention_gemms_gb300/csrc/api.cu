@@ -71,17 +71,42 @@ size_t partial_bytes(int64_t M, int64_t n, int32_t N, tp_reduce mode) {
   return elems * static_cast<size_t>(N) * sizeof(float);
 }
 
+// A weight of the linear map from `in` to `out` features as the B operand B(k, n) of
+// D = A B (k over `in`, n over `out`): stored (in, out) it is read MN-major, stored
+// (out, in) K-major -- in place either way.
+void weight_operand(GemmDesc& d, int s, const void* W, int64_t in, int64_t out, bool w_out_in) {
+  if (w_out_in) {
+    d.B[s] = {W, out, in, in};
+    d.b_mn = false;
+  } else {
+    d.B[s] = {W, in, out, out};
+    d.b_mn = true;
+  }
+}
+
+// The transpose W^T of such a weight as the B operand (k over `out`, n over `in`), for
+// the backward's dH = dZ W^T: stored (in, out) it is read K-major, stored (out, in)
+// MN-major.
+void weight_t_operand(GemmDesc& d, int s, const void* W, int64_t in, int64_t out, bool w_out_in) {
+  if (w_out_in) {
+    d.B[s] = {W, out, in, in};
+    d.b_mn = true;
+  } else {
+    d.B[s] = {W, in, out, out};
+    d.b_mn = false;
+  }
+}
+
 tp_status col_impl(const void* X, const void* W, const void* Wu, void* Y, void* Yu, void* out,
                    int64_t M, int64_t h, int64_t f, int32_t N, tp_dtype dt, tp_act act,
-                   cudaStream_t st) {
+                   cudaStream_t st, bool w_out_in) {
   GemmDesc d;
   d.dtype = dt;
   d.M = M;
   d.N = f;
   d.K = h;
   d.A[0] = {X, M, h, h};
-  d.B[0] = {W, h, f, f};
-  d.b_mn = true;
+  weight_operand(d, 0, W, h, f, w_out_in);
   d.ldo = f;
   d.shards = N;
   d.shard_axis = 1;
@@ -95,7 +120,7 @@ tp_status col_impl(const void* X, const void* W, const void* Wu, void* Y, void* 
     d.out[1] = out;
   } else {
     d.paired = true;
-    d.B[1] = {Wu, h, f, f};
+    weight_operand(d, 1, Wu, h, f, w_out_in);
     d.epi = EPI_SWIGLU;
     d.out[0] = Y;
     d.out[1] = Yu;
@@ -107,14 +132,13 @@ tp_status col_impl(const void* X, const void* W, const void* Wu, void* Y, void* 
 // out = sum_i Xs_i W_i (+ residual): variant A (partials + reduce) or B (split-K fold)
 tp_status row_impl(const void* Xs, const void* W, const void* residual, void* out, int64_t M,
                    int64_t k, int64_t n, int32_t N, tp_dtype dt, tp_reduce mode, void* ws,
-                   cudaStream_t st) {
+                   cudaStream_t st, bool w_out_in) {
   GemmDesc d;
   d.dtype = dt;
   d.M = M;
   d.N = n;
   d.A[0] = {Xs, M, k, k};
-  d.B[0] = {W, k, n, n};
-  d.b_mn = true;
+  weight_operand(d, 0, W, k, n, w_out_in);
   d.ldo = n;
   d.epi = EPI_STORE;
   if (mode == TP_REDUCE_SPLITK) {
@@ -162,34 +186,34 @@ tp_status row_ln_impl(const void* Xs, const void* W, const void* residual, const
                                 mean, rstd, N, M, n, eps, dt, st);
 }
 
-// dX = sum_i sum_s dA_s,i B_s,i^T over nseg operand pairs (dY with W1, or dG/dU with Wg/Wu)
-tp_status dx_impl(const void* const* dA, const void* const* Wt, int nseg, void* dX, int64_t M,
-                  int64_t h, int64_t f, int32_t N, tp_dtype dt, tp_reduce mode, void* ws,
-                  cudaStream_t st) {
+// The GEMM of dX = sum_i sum_s dA_s,i B_s,i^T over nseg operand pairs (dY with W1, or
+// dG/dU with Wg/Wu): split-K writes dX itself into `dst`; buffers writes the N fp32
+// partials (M x h each) into `dst`
+tp_status dx_gemm(const void* const* dA, const void* const* Wt, int nseg, void* dst, int64_t M,
+                  int64_t h, int64_t f, int32_t N, tp_dtype dt, tp_reduce mode, cudaStream_t st,
+                  bool w_out_in) {
   GemmDesc d;
   d.dtype = dt;
   d.M = M;
   d.N = h;
   d.nseg = nseg;
   for (int s = 0; s < nseg; ++s) {
-    d.A[s] = {dA[s], M, f, f};   // dY (M, f), K-major
-    d.B[s] = {Wt[s], h, f, f};   // W1 (h, f) read as B(k = f, n = h): K-major
+    d.A[s] = {dA[s], M, f, f};                       // dY (M, f), K-major
+    weight_t_operand(d, s, Wt[s], h, f, w_out_in);   // W1^T as B(k = f, n = h)
   }
   d.ldo = h;
   d.epi = EPI_STORE;
+  d.out[0] = dst;
   if (mode == TP_REDUCE_SPLITK) {
     d.K = f;
-    d.out[0] = dX;
     d.out_f32 = dt == TP_F32;
     return launch_gemm(d, st);
   }
   d.K = f / N;
   d.groups = N;
-  d.out[0] = ws;
   d.out_f32 = true;
   d.out_group_stride = M * h;
-  TP_TRY(launch_gemm(d, st));
-  return launch_shard_reduce(static_cast<const float*>(ws), nullptr, dX, N, M, h, dt, st);
+  return launch_gemm(d, st);
 }
 
 }  // namespace tp
@@ -258,10 +282,16 @@ tp_status tp_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, i
   return launch_gemm(d, static_cast<cudaStream_t>(stream));
 }
 
+tp_status check_wlayout(tp_wlayout wl) {
+  return need(wl == TP_W_IN_OUT || wl == TP_W_OUT_IN, TP_ERR_INVALID_ARG,
+              "w_layout must be TP_W_IN_OUT or TP_W_OUT_IN");
+}
+
 tp_status tp_col_linear(const void* X, const void* W, const void* W_up, void* Y, void* Y_up,
                         void* out, int64_t M, int64_t h, int64_t f, int32_t N, tp_dtype dtype,
-                        tp_act act, void* stream) {
+                        tp_act act, tp_wlayout w_layout, void* stream) {
   TP_TRY(check_dtype(dtype));
+  TP_TRY(check_wlayout(w_layout));
   TP_TRY(need(act >= TP_ACT_NONE && act <= TP_ACT_SWIGLU, TP_ERR_INVALID_ARG, "unknown act"));
   TP_TRY(need(X && W && out, TP_ERR_INVALID_ARG, "X, W and out are required"));
   TP_TRY(need(act != TP_ACT_SWIGLU || W_up, TP_ERR_INVALID_ARG, "SwiGLU needs W_up"));
@@ -270,13 +300,14 @@ tp_status tp_col_linear(const void* X, const void* W, const void* W_up, void* Y,
   if (M == 0) return TP_OK;
   TP_TRY(check_device());
   return col_impl(X, W, W_up, Y, Y_up, out, M, h, f, N, dtype, act,
-                  static_cast<cudaStream_t>(stream));
+                  static_cast<cudaStream_t>(stream), w_layout == TP_W_OUT_IN);
 }
 
 tp_status tp_row_linear(const void* Xs, const void* W, const void* residual, void* out, int64_t M,
                         int64_t k, int64_t n, int32_t N, tp_dtype dtype, tp_reduce mode, void* ws,
-                        size_t ws_bytes, void* stream) {
+                        size_t ws_bytes, tp_wlayout w_layout, void* stream) {
   TP_TRY(check_dtype(dtype));
+  TP_TRY(check_wlayout(w_layout));
   TP_TRY(need(mode == TP_REDUCE_BUFFERS || mode == TP_REDUCE_SPLITK, TP_ERR_INVALID_ARG,
               "unknown reduce mode"));
   TP_TRY(need(Xs && W && out, TP_ERR_INVALID_ARG, "Xs, W and out are required"));
@@ -297,7 +328,7 @@ tp_status tp_row_linear(const void* Xs, const void* W, const void* residual, voi
               "workspace smaller than tp_workspace_size"));
   TP_TRY(check_device());
   return row_impl(Xs, W, residual, out, M, k, n, N, dtype, mode, ws,
-                  static_cast<cudaStream_t>(stream));
+                  static_cast<cudaStream_t>(stream), w_layout == TP_W_OUT_IN);
 }
 
 tp_status tp_shard_reduce(const float* partials, const void* residual, void* out, int32_t N,
@@ -368,8 +399,9 @@ tp_status tp_row_linear_ln(const void* Xs, const void* W, const void* residual,
 tp_status tp_mlp_fwd(const void* X, const void* W1, const void* W1_up, const void* W2,
                      const void* residual, void* Y, void* Y_up, void* H, void* Z, int64_t M,
                      int64_t h, int64_t f, int32_t N, tp_dtype dtype, tp_act act, tp_reduce mode,
-                     void* ws, size_t ws_bytes, void* stream) {
+                     void* ws, size_t ws_bytes, tp_wlayout w_layout, void* stream) {
   TP_TRY(check_dtype(dtype));
+  TP_TRY(check_wlayout(w_layout));
   TP_TRY(need(act == TP_ACT_GELU || act == TP_ACT_SWIGLU, TP_ERR_INVALID_ARG,
               "MLP act must be TP_ACT_GELU or TP_ACT_SWIGLU"));
   TP_TRY(need(mode == TP_REDUCE_BUFFERS || mode == TP_REDUCE_SPLITK, TP_ERR_INVALID_ARG,
@@ -387,16 +419,18 @@ tp_status tp_mlp_fwd(const void* X, const void* W1, const void* W1_up, const voi
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   void* Hb = H ? H : ws;
   void* parts = static_cast<char*>(ws) + h_bytes;
-  TP_TRY(col_impl(X, W1, W1_up, Y, Y_up, Hb, M, h, f, N, dtype, act, st));
-  return row_impl(Hb, W2, residual, Z, M, f, h, N, dtype, mode, parts, st);
+  const bool wt = w_layout == TP_W_OUT_IN;
+  TP_TRY(col_impl(X, W1, W1_up, Y, Y_up, Hb, M, h, f, N, dtype, act, st, wt));
+  return row_impl(Hb, W2, residual, Z, M, f, h, N, dtype, mode, parts, st, wt);
 }
 
 tp_status tp_mlp_bwd(const void* X, const void* W1, const void* W1_up, const void* W2,
                      const void* Y, const void* Y_up, const void* H, const void* dZ, void* dX,
                      void* dW1, void* dW1_up, void* dW2, int64_t M, int64_t h, int64_t f,
                      int32_t N, tp_dtype dtype, tp_act act, tp_reduce mode, void* ws,
-                     size_t ws_bytes, void* stream) {
+                     size_t ws_bytes, tp_wlayout w_layout, void* stream) {
   TP_TRY(check_dtype(dtype));
+  TP_TRY(check_wlayout(w_layout));
   TP_TRY(need(act == TP_ACT_GELU || act == TP_ACT_SWIGLU, TP_ERR_INVALID_ARG,
               "MLP act must be TP_ACT_GELU or TP_ACT_SWIGLU"));
   TP_TRY(need(mode == TP_REDUCE_BUFFERS || mode == TP_REDUCE_SPLITK, TP_ERR_INVALID_ARG,
@@ -417,6 +451,7 @@ tp_status tp_mlp_bwd(const void* X, const void* W1, const void* W1_up, const voi
               "workspace smaller than tp_workspace_size"));
   TP_TRY(check_device());
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool wt = w_layout == TP_W_OUT_IN;
   void* dY = ws;  // GELU: dY; SwiGLU: dG then dU
   void* dU = static_cast<char*>(ws) + g_one;
   void* parts = static_cast<char*>(ws) + g_bytes;
@@ -430,7 +465,7 @@ tp_status tp_mlp_bwd(const void* X, const void* W1, const void* W1_up, const voi
     d.N = f;
     d.K = h;
     d.A[0] = {dZ, M, h, h};
-    d.B[0] = {W2, f, h, h};  // W2 (f, h) read as B(k = h, n = f): K-major
+    weight_t_operand(d, 0, W2, f, h, wt);  // W2^T as B(k = h, n = f)
     d.ldo = f;
     d.shards = N;
     d.shard_axis = 1;
@@ -447,38 +482,65 @@ tp_status tp_mlp_bwd(const void* X, const void* W1, const void* W1_up, const voi
     }
     TP_TRY(launch_gemm(d, st));
   }
-  // 2. dW2_i = H_i^T dZ (row-parallel weight gradient; shard i = row block i)
-  {
+  // 2. dW2_i = H_i^T dZ (row-parallel weight gradient; shard i = row block i of the
+  //    (f, h) gradient), or in (out, in) storage dW2_i^T = dZ^T H_i (column block i)
+  auto dw2 = [&]() -> tp_status {
     GemmDesc d;
     d.dtype = dtype;
-    d.M = f;
-    d.N = h;
     d.K = M;
-    d.A[0] = {H, M, f, f};
     d.a_mn = true;
-    d.B[0] = {dZ, M, h, h};
     d.b_mn = true;
-    d.ldo = h;
     d.epi = EPI_STORE;
     d.out[0] = dW2;
     d.out_f32 = dtype == TP_F32;
     d.shards = N;
-    d.shard_axis = 0;
-    TP_TRY(launch_gemm(d, st));
-  }
-  // 3. dW1_i = X^T dY_i (column-parallel weight gradient; shard i = column block i)
-  {
+    if (wt) {
+      d.M = h;
+      d.N = f;
+      d.A[0] = {dZ, M, h, h};
+      d.B[0] = {H, M, f, f};
+      d.ldo = f;
+      d.shard_axis = 1;
+    } else {
+      d.M = f;
+      d.N = h;
+      d.A[0] = {H, M, f, f};
+      d.B[0] = {dZ, M, h, h};
+      d.ldo = h;
+      d.shard_axis = 0;
+    }
+    return launch_gemm(d, st);
+  };
+  // 3. dW1_i = X^T dY_i (column-parallel weight gradient; shard i = column block i), or
+  //    in (out, in) storage dW1_i^T = dY_i^T X (row block i); SwiGLU also dW1up from dU
+  auto dw1 = [&]() -> tp_status {
     GemmDesc d;
     d.dtype = dtype;
+    d.K = M;
+    d.a_mn = true;
+    d.b_mn = true;
+    d.shards = N;
+    if (wt) {  // one GEMM per projection: the gate's and the up's gradients are row blocks
+      d.M = f;
+      d.N = h;
+      d.B[0] = {X, M, h, h};
+      d.ldo = h;
+      d.shard_axis = 0;
+      d.epi = EPI_STORE;
+      d.out_f32 = dtype == TP_F32;
+      d.A[0] = {dY, M, f, f};
+      d.out[0] = dW1;
+      TP_TRY(launch_gemm(d, st));
+      if (!sw) return TP_OK;
+      d.A[0] = {dU, M, f, f};
+      d.out[0] = dW1_up;
+      return launch_gemm(d, st);
+    }
     d.M = h;
     d.N = f;
-    d.K = M;
     d.A[0] = {X, M, h, h};
-    d.a_mn = true;
     d.B[0] = {dY, M, f, f};
-    d.b_mn = true;
     d.ldo = f;
-    d.shards = N;
     d.shard_axis = 1;
     if (sw) {
       d.paired = true;
@@ -491,17 +553,29 @@ tp_status tp_mlp_bwd(const void* X, const void* W1, const void* W1_up, const voi
       d.out[0] = dW1;
       d.out_f32 = dtype == TP_F32;
     }
-    TP_TRY(launch_gemm(d, st));
-  }
+    return launch_gemm(d, st);
+  };
   // 4. f-backward: dX = sum_i dY_i W1_i^T (SwiGLU: + dU_i W1up_i^T)
-  if (sw) {
-    const void* dA[2] = {dY, dU};
-    const void* Wt[2] = {W1, W1_up};
-    return dx_impl(dA, Wt, 2, dX, M, h, f, N, dtype, mode, parts, st);
+  const void* dA[2] = {dY, dU};
+  const void* Wt[2] = {W1, W1_up};
+  const int nseg = sw ? 2 : 1;
+  if (mode == TP_REDUCE_SPLITK) {
+    TP_TRY(dw2());
+    TP_TRY(dw1());
+    return dx_gemm(dA, Wt, nseg, dX, M, h, f, N, dtype, mode, st, wt);
   }
-  const void* dA[1] = {dY};
-  const void* Wt[1] = {W1};
-  return dx_impl(dA, Wt, 1, dX, M, h, f, N, dtype, mode, parts, st);
+  // Per-shard partials: dX's GEMM comes first, and the shard sum of its partials (the
+  // all-reduce stand-in, HBM-bound) runs on a side stream beside the two weight-gradient
+  // GEMMs (tensor-core-bound), which do not read dX. A grid of two reduce CTAs per SM
+  // leaves every SM room for the GEMM's persistent CTA.
+  TP_TRY(dx_gemm(dA, Wt, nseg, parts, M, h, f, N, dtype, mode, st, wt));
+  SideBranch sum(st);
+  const bool beside = sum.stream() != st;
+  TP_TRY(launch_shard_reduce(static_cast<const float*>(parts), nullptr, dX, N, M, h, dtype,
+                             sum.stream(), beside ? 2 : 8));
+  TP_TRY(dw2());
+  TP_TRY(dw1());
+  return sum.join();
 }
 
 }  // extern "C"

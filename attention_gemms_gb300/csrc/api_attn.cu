@@ -306,7 +306,7 @@ tp_status tp_layer_fwd(const void* x, const tp_layer_weights* w, const tp_layer_
                        static_cast<cudaStream_t>(stream)));
   // out = x1 + sum_i GELU(xn2 W1_i) W2_i
   return tp_mlp_fwd(sv->xn2, w->W1, nullptr, w->W2, sv->x1, sv->y, nullptr, sv->hh, out, b * s,
-                    h, f, N, dtype, TP_ACT_GELU, mode, ws, ws_bytes, stream);
+                    h, f, N, dtype, TP_ACT_GELU, mode, ws, ws_bytes, TP_W_IN_OUT, stream);
 }
 
 tp_status tp_layer_bwd(const void* x, const tp_layer_weights* w, const tp_layer_saved* sv,
@@ -331,7 +331,7 @@ tp_status tp_layer_bwd(const void* x, const tp_layer_weights* w, const tp_layer_
   const size_t rest_bytes = ws_bytes - 2 * a256(M * h * e);
   TP_TRY(tp_mlp_bwd(sv->xn2, w->W1, nullptr, w->W2, sv->y, nullptr, sv->hh, dout, dxn2, g->dW1,
                     nullptr, g->dW2, M, h, f, N, dtype, TP_ACT_GELU, mode, rest, rest_bytes,
-                    stream));
+                    TP_W_IN_OUT, stream));
   TP_TRY(tp_layernorm_bwd(sv->x1, w->gamma2, sv->mean2, sv->rstd2, dxn2, dout, dx1, g->dgamma2,
                           g->dbeta2, M, h, dtype, rest, rest_bytes, stream));
   return tp_attn_proj_bwd(x, w->gamma1, w->Wqkv, w->Wo, sv->xn1, sv->mean1, sv->rstd1, sv->qkv,

@@ -78,7 +78,7 @@ tp_status tp_sp_mlp_fwd(const void* x, const float* gamma, const float* beta, co
                               static_cast<cudaStream_t>(stream)));
   // all-gather = the adjacent rank blocks of xn; the TP MLP; reduce-scatter + x_r
   return tp_mlp_fwd(xn, W1, W1_up, W2, x, Y, Y_up, H, out, M, h, f, N, dtype, act, mode, ws,
-                    ws_bytes, stream);
+                    ws_bytes, TP_W_IN_OUT, stream);
 }
 
 tp_status tp_sp_mlp_bwd(const void* x, const float* gamma, const void* W1, const void* W1_up,
@@ -105,7 +105,7 @@ tp_status tp_sp_mlp_bwd(const void* x, const float* gamma, const void* W1, const
   const size_t rest_bytes = ws_bytes - (rest - p);
   // all-gather of dout (the buffer itself) -> MLP backward -> reduce-scatter of dX
   TP_TRY(tp_mlp_bwd(xn, W1, W1_up, W2, Y, Y_up, H, dout, dxn, dW1, dW1_up, dW2, M, h, f, N,
-                    dtype, act, mode, rest, rest_bytes, stream));
+                    dtype, act, mode, rest, rest_bytes, TP_W_IN_OUT, stream));
   // LN backward on each rank's rows + the residual's dout_r; LN parameter gradients
   // per rank, then summed over the ranks
   return launch_layernorm_bwd_ranks(x, gamma, mean, rstd, dxn, dout, dx, dgamma, dbeta,

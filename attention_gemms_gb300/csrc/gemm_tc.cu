@@ -445,7 +445,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           } else {
             tma_load_2d(a_dst, &p.tmA[seg], full_bar(stage), k0, m0);
           }
-          if (p.paired) {
+          if (p.paired && !p.b_mn) {
+            // K-major halves ((out, in) weights): BN/2 gate rows, then BN/2 up rows
+            tma_load_2d(b_dst, &p.tmB[0], full_bar(stage), k0, n0);
+            tma_load_2d(b_dst + (BN / 2) * 128, &p.tmB[1], full_bar(stage), k0, n0);
+          } else if (p.paired) {
             constexpr int HALF = BN / 128;  // 64-wide boxes per half
             if (p.b3d) {
               tma_load_3d(b_dst, &p.tmB[0], full_bar(stage), 0, k0, n0 / 64);
@@ -762,6 +766,9 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_tc2_kernel(const __grid_
             tma_load_2d_pair(a_dst, &p.tmA[seg], fb, k0, m0);
           }
           if (!load_b) {
+          } else if (p.paired && !p.b_mn) {
+            // K-major ((out, in) weights): even CTA 128 gate rows, odd CTA the same up rows
+            tma_load_2d_pair(b_dst, &p.tmB[rank], fb, k0, n0);
           } else if (p.paired) {
             // even CTA: 128 gate columns, odd CTA: the same 128 up columns
             if (p.b3d) {
@@ -1117,8 +1124,7 @@ void set_pair_mode(int v) { g_pair_mode.store(v); }
 
 tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
   if (d.M <= 0 || d.N <= 0 || d.K <= 0) return TP_OK;
-  if (d.paired && (!d.b_mn || d.nseg != 1))
-    return fail(TP_ERR_INVALID_ARG, "paired GEMM needs MN-major B and one K segment");
+  if (d.paired && d.nseg != 1) return fail(TP_ERR_INVALID_ARG, "paired GEMM needs one K segment");
   if (d.N % 8 != 0) return fail(TP_ERR_SHAPE, "GEMM output width must be a multiple of 8");
   if (d.groups > 1 && d.K % BK != 0)
     return fail(TP_ERR_SHAPE, "per-shard K must be a multiple of 64");
@@ -1157,7 +1163,8 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
   for (int s = 0; s < nb; ++s) {
     if (b3d) TP_TRY(make_map_3d(&prm.tmB[s], d.B[s], b_chunks));
     else if (d.b_mn) TP_TRY(make_map(&prm.tmB[s], d.B[s], 64, 64));
-    else TP_TRY(make_map(&prm.tmB[s], d.B[s], 64, static_cast<uint32_t>(pair ? 128 : BN)));
+    else TP_TRY(make_map(&prm.tmB[s], d.B[s], 64,
+                         static_cast<uint32_t>(pair ? 128 : (d.paired ? BN / 2 : BN))));
   }
   prm.a3d = a3d;
   prm.b3d = b3d;

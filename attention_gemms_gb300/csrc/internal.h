@@ -130,8 +130,11 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st);    // bf16, tcgen0
 bool gemv_eligible(const GemmDesc& d);                             // bf16, M <= 4
 tp_status launch_gemv(const GemmDesc& d, cudaStream_t st);
 tp_status launch_gemm_simt(const GemmDesc& d, cudaStream_t st);  // fp32, CUDA cores
+// blocks_per_sm: CTAs of 256 threads per SM of the grid-stride grid (8 saturates HBM
+// alone; 2 leaves room on every SM for a persistent GEMM CTA running beside it)
 tp_status launch_shard_reduce(const float* P, const void* residual, void* out, int N,
-                              int64_t M, int64_t n, tp_dtype out_dtype, cudaStream_t st);
+                              int64_t M, int64_t n, tp_dtype out_dtype, cudaStream_t st,
+                              int blocks_per_sm = 8);
 // sum + residual, rounded to dt, then LayerNorm of the rounded row: h % 8 == 0,
 // h <= kReduceLnMaxH, 16-byte aligned buffers
 constexpr int64_t kReduceLnMaxH = 16384;
@@ -225,9 +228,10 @@ tp_status check_extents(int64_t rows, int64_t cols, int64_t N);
 tp_status check_mlp_shape(int64_t M, int64_t h, int64_t f, int32_t N, tp_dtype dt);
 size_t sp_mlp_workspace_size(bool fwd, int64_t M, int64_t h, int64_t f, int32_t N, tp_dtype dt,
                              tp_act act, tp_reduce mode);
+// w_out_in: W stored (n, k) (TP_W_OUT_IN) instead of (k, n)
 tp_status row_impl(const void* Xs, const void* W, const void* residual, void* out, int64_t M,
                    int64_t k, int64_t n, int32_t N, tp_dtype dt, tp_reduce mode, void* ws,
-                   cudaStream_t st);
+                   cudaStream_t st, bool w_out_in = false);
 tp_status row_ln_impl(const void* Xs, const void* W, const void* residual, const float* gamma,
                       const float* beta, void* sum_out, void* y, float* mean, float* rstd,
                       int64_t M, int64_t k, int64_t n, int32_t N, float eps, tp_dtype dt,

@@ -125,12 +125,14 @@ __global__ void __launch_bounds__(256) shard_reduce_scalar(const float* __restri
 }
 
 template <typename OutT>
-tp_status run(const float* P, const void* R, void* O, int N, int64_t E, cudaStream_t st) {
+tp_status run(const float* P, const void* R, void* O, int N, int64_t E, int blocks_per_sm,
+              cudaStream_t st) {
   const bool vec = (E % 8 == 0) && (reinterpret_cast<uintptr_t>(P) % 16 == 0) &&
                    (reinterpret_cast<uintptr_t>(O) % 16 == 0) &&
                    (R == nullptr || reinterpret_cast<uintptr_t>(R) % 16 == 0);
   const int64_t work = vec ? E / 8 : E;
-  const int64_t blocks = std::min<int64_t>((work + 255) / 256, 8ll * device_sm_count());
+  const int64_t blocks =
+      std::min<int64_t>((work + 255) / 256, static_cast<int64_t>(blocks_per_sm) * device_sm_count());
   if (vec)
     shard_reduce_vec8<OutT><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
         P, static_cast<const OutT*>(R), static_cast<OutT*>(O), N, work, E);
@@ -287,11 +289,12 @@ tp_status run_ln(const float* P, const void* R, const float* gamma, const float*
 }  // namespace
 
 tp_status launch_shard_reduce(const float* P, const void* residual, void* out, int N, int64_t M,
-                              int64_t n, tp_dtype out_dtype, cudaStream_t st) {
+                              int64_t n, tp_dtype out_dtype, cudaStream_t st, int blocks_per_sm) {
   const int64_t E = M * n;
   if (E <= 0) return TP_OK;
-  return out_dtype == TP_BF16 ? run<__nv_bfloat16>(P, residual, out, N, E, st)
-                              : run<float>(P, residual, out, N, E, st);
+  blocks_per_sm = std::max(1, std::min(blocks_per_sm, 8));
+  return out_dtype == TP_BF16 ? run<__nv_bfloat16>(P, residual, out, N, E, blocks_per_sm, st)
+                              : run<float>(P, residual, out, N, E, blocks_per_sm, st);
 }
 
 tp_status launch_shard_reduce_ln(const float* P, const void* residual, const float* gamma,

@@ -44,6 +44,12 @@ class Reduce(enum.IntEnum):
     SPLITK = 1
 
 
+class WLayout(enum.IntEnum):
+    """tp_wlayout: weights stored (in, out) -- the pages' W -- or (out, in)."""
+    IN_OUT = 0
+    OUT_IN = 1
+
+
 class Op(enum.IntEnum):
     COL_LINEAR = 0
     ROW_LINEAR = 1
@@ -124,16 +130,16 @@ _SIGS = {
     "tp_launch_count": (ctypes.c_uint64, []),
     "tp_workspace_size": (_SZ, [_ST, _I64, _I64, _I64, _I32, _ST, _ST, _ST]),
     "tp_gemm": (_ST, [_P, _P, _P, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, _ST, _P]),
-    "tp_col_linear": (_ST, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _ST, _ST, _P]),
-    "tp_row_linear": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _ST, _ST, _P, _SZ, _P]),
+    "tp_col_linear": (_ST, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _ST, _ST, _ST, _P]),
+    "tp_row_linear": (_ST, [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _ST, _ST, _P, _SZ, _ST, _P]),
     "tp_shard_reduce": (_ST, [_P, _P, _P, _I32, _I64, _I64, _ST, _P]),
     "tp_shard_reduce_ln": (_ST, [_P] * 8 + [_I32, _I64, _I64, ctypes.c_float, _ST, _P]),
     "tp_row_linear_ln": (_ST, [_P] * 9 + [_I64, _I64, _I64, _I32, ctypes.c_float, _ST, _ST, _P,
                                           _SZ, _P]),
     "tp_mlp_fwd": (_ST, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _ST, _ST,
-                         _ST, _P, _SZ, _P]),
+                         _ST, _P, _SZ, _ST, _P]),
     "tp_mlp_bwd": (_ST, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32,
-                         _ST, _ST, _ST, _P, _SZ, _P]),
+                         _ST, _ST, _ST, _P, _SZ, _ST, _P]),
     "tp_layernorm_fwd": (_ST, [_P, _P, _P, _P, _P, _P, _I64, _I64, ctypes.c_float, _ST, _P]),
     "tp_layernorm_bwd": (_ST, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _ST, _P, _SZ, _P]),
     "tp_attn_proj_fwd": (_ST, [_P] * 12 + [_I64, _I64, _I64, _I32, _I32, ctypes.c_int, _ST, _ST,
@@ -271,14 +277,17 @@ def tp_gemm(A, B, C, M, N, K, a_trans, b_trans, dtype, stream=None):
                          int(bool(b_trans)), int(dtype), _stream(stream)))
 
 
-def tp_col_linear(X, W, W_up, Y, Y_up, out, M, h, f, N, dtype, act, stream=None):
+def tp_col_linear(X, W, W_up, Y, Y_up, out, M, h, f, N, dtype, act, stream=None,
+                  w_layout=WLayout.IN_OUT):
     _check(lib().tp_col_linear(_ptr(X), _ptr(W), _ptr(W_up), _ptr(Y), _ptr(Y_up), _ptr(out),
-                               M, h, f, N, int(dtype), int(act), _stream(stream)))
+                               M, h, f, N, int(dtype), int(act), int(w_layout), _stream(stream)))
 
 
-def tp_row_linear(Xs, W, residual, out, M, k, n, N, dtype, mode, ws, ws_bytes, stream=None):
+def tp_row_linear(Xs, W, residual, out, M, k, n, N, dtype, mode, ws, ws_bytes, stream=None,
+                  w_layout=WLayout.IN_OUT):
     _check(lib().tp_row_linear(_ptr(Xs), _ptr(W), _ptr(residual), _ptr(out), M, k, n, N,
-                               int(dtype), int(mode), _ptr(ws), int(ws_bytes), _stream(stream)))
+                               int(dtype), int(mode), _ptr(ws), int(ws_bytes), int(w_layout),
+                               _stream(stream)))
 
 
 def tp_shard_reduce(partials, residual, out, N, M, n, out_dtype, stream=None):
@@ -302,18 +311,18 @@ def tp_row_linear_ln(Xs, W, residual, gamma, beta, sum_out, y, mean, rstd, M, k,
 
 
 def tp_mlp_fwd(X, W1, W1_up, W2, residual, Y, Y_up, H, Z, M, h, f, N, dtype, act, mode, ws,
-               ws_bytes, stream=None):
+               ws_bytes, stream=None, w_layout=WLayout.IN_OUT):
     _check(lib().tp_mlp_fwd(_ptr(X), _ptr(W1), _ptr(W1_up), _ptr(W2), _ptr(residual), _ptr(Y),
                             _ptr(Y_up), _ptr(H), _ptr(Z), M, h, f, N, int(dtype), int(act),
-                            int(mode), _ptr(ws), int(ws_bytes), _stream(stream)))
+                            int(mode), _ptr(ws), int(ws_bytes), int(w_layout), _stream(stream)))
 
 
 def tp_mlp_bwd(X, W1, W1_up, W2, Y, Y_up, H, dZ, dX, dW1, dW1_up, dW2, M, h, f, N, dtype, act,
-               mode, ws, ws_bytes, stream=None):
+               mode, ws, ws_bytes, stream=None, w_layout=WLayout.IN_OUT):
     _check(lib().tp_mlp_bwd(_ptr(X), _ptr(W1), _ptr(W1_up), _ptr(W2), _ptr(Y), _ptr(Y_up),
                             _ptr(H), _ptr(dZ), _ptr(dX), _ptr(dW1), _ptr(dW1_up), _ptr(dW2),
                             M, h, f, N, int(dtype), int(act), int(mode), _ptr(ws),
-                            int(ws_bytes), _stream(stream)))
+                            int(ws_bytes), int(w_layout), _stream(stream)))
 
 
 def tp_gqa_qkv_cols(h, n_heads, n_kv_heads, N):

@@ -429,15 +429,38 @@ def run_ours(args, w):
                 "col": max_over_ranks(col_ms, device), "e2e": max_over_ranks(e2e_ms, device),
                 "launches": launches}
 
+    def interleaved():
+        """Steps of the two variants alternated (per-step CUDA events), so that clock
+        drift under the power cap weighs on both alike: per-variant median ms."""
+        ev = lambda: torch.cuda.Event(enable_timing=True)
+        per = {name: [] for name in modes}
+        barrier()
+        torch.cuda.synchronize()
+        for _ in range(args.steps):
+            for name, mode in modes.items():
+                a, b = ev(), ev()
+                a.record(stream)
+                T.tp_col_linear(d["X"], d["W1"], d["W1u"], Y, Yu, H, M, h, f, N, BF, act, stream)
+                T.tp_row_linear(H, d["W2"], None, Z, M, f, h, N, BF, mode, ws, ws.numel(), stream)
+                T.tp_mlp_bwd(d["X"], d["W1"], d["W1u"], d["W2"], Y, Yu, H, d["dZ"], dX, dW1, dW1u,
+                             dW2, M, h, f, N, BF, act, mode, ws, ws.numel(), stream)
+                b.record(stream)
+                per[name].append((a, b))
+        torch.cuda.synchronize()
+        barrier()
+        return {name: max_over_ranks(float(np.median([a.elapsed_time(b) for a, b in v])), device)
+                for name, v in per.items()}
+
     clocks = ClockSampler(device.index)
     clocks.start()
     time.sleep(0.3)
     main_r = measure(args.mode)
-    others = {}
+    others, inter = {}, {}
     if args.variants and not f32:
         for name in modes:
             if name != args.mode:
                 others[name] = measure(name)
+        inter = interleaved()
     clk = clocks.stop()
 
     ms_max, e2e_max, col_max = main_r["ms"], main_r["e2e"], main_r["col"]
@@ -485,9 +508,16 @@ def run_ours(args, w):
                          "TFLOPs": round(tf, 2), "pct_of_peak": round(100 * tf / ws_ / peak, 2),
                          "e2e_TFLOPs": round(flops * ws_ / (r["e2e"] * 1e-3) / 1e12, 2),
                          "column_gemm_ms": round(r["col"], 4), "gpu_launches": int(r["launches"])}
+            if name in inter:
+                tf_i = flops * ws_ / (inter[name] * 1e-3) / 1e12
+                var[name]["interleaved_ms_median"] = round(inter[name], 4)
+                var[name]["interleaved_TFLOPs"] = round(tf_i, 2)
+                var[name]["interleaved_pct_of_peak"] = round(100 * tf_i / ws_ / peak, 2)
         var["note"] = ("splitk: the row-parallel sums folded as split-K into one accumulator; "
-                       "buffers: per-shard fp32 partials summed by the shard-reduce kernel; "
-                       "both timed in this process, same steps and warm-up")
+                       "buffers: per-shard fp32 partials summed by the shard-reduce kernel (the "
+                       "backward's dX sum on a side stream beside the weight-gradient GEMMs); "
+                       "each timed in its own bracketed run, then in one run of alternating "
+                       "steps (interleaved_*, per-step medians)")
         out["shard_sum_variants"] = var
     if f32:
         out["roofline"] = {"bound": "alu", "note": "fp32 FFMA path at a latency-bound size; "

@@ -22,7 +22,8 @@
  * Conventions for every entry point
  *   - Tensors are dense and row-major. X is (M, h) with M = b*s tokens (the pages'
  *     X:(b, s, h)); a weight W is (h, h') = (in, out) so that Y = X W (the pages'
- *     W:(h, h')) [张量并行 notes, §基本思想].
+ *     W:(h, h')) [张量并行 notes, §基本思想]. The linear entry points also take
+ *     (out, in) weights (tp_wlayout).
  *   - Column shard i of a weight = columns [i*h'/N, (i+1)*h'/N); row shard i = rows
  *     [i*h/N, (i+1)*h/N). Shards are blocks of one allocation, in shard order.
  *   - Element types: TP_BF16 (bf16 storage, fp32 accumulation, tensor cores) or
@@ -59,7 +60,7 @@
 extern "C" {
 #endif
 
-#define TPMLP_VERSION 1
+#define TPMLP_VERSION 2
 
 typedef enum tp_status {
   TP_OK = 0,
@@ -89,6 +90,23 @@ typedef enum tp_reduce {
   TP_REDUCE_SPLITK = 1   /* the K-slices of all shards are folded into one on-chip fp32
                             accumulator, shard 0 first; no partial buffers               */
 } tp_reduce;
+
+/*
+ * Storage order of the weights of the linear entry points (tp_col_linear, tp_row_linear,
+ * tp_mlp_fwd, tp_mlp_bwd). The pages write Y = X W with W:(h, h') [张量并行 notes,
+ * §基本思想; Infra: Tensor Parallel]; the Megatron listing keeps each shard's weight as
+ * (out, in) for F.linear, Y = X W^T [Megatron-LM 分布式大模型训练实战 04, 核心实现,
+ * ColumnParallelLinear / RowParallelLinear].
+ *   TP_W_IN_OUT: a weight is stored (in, out) row-major, the pages' W itself. A column
+ *                shard is a column block of the stored matrix, a row shard a row block.
+ *   TP_W_OUT_IN: a weight is stored (out, in) row-major, i.e. W^T. A column shard
+ *                (out features [i out/N, (i+1) out/N)) is then a ROW block of the stored
+ *                matrix, and a row shard (in features [i in/N, (i+1) in/N)) a COLUMN
+ *                block; weight gradients are written in the same (out, in) order.
+ * Either way the tensor cores read the stored matrix in place (K-major or MN-major
+ * operand), with no transpose copy.
+ */
+typedef enum tp_wlayout { TP_W_IN_OUT = 0, TP_W_OUT_IN = 1 } tp_wlayout;
 
 typedef enum tp_op {
   TP_OP_COL_LINEAR = 0,
@@ -234,13 +252,16 @@ TP_API tp_status tp_gemm(const void* A, const void* B, void* C, int64_t M, int64
  *   out  (M, f)  device, written     act(Y): Y itself (NONE), GELU(Y), or SiLU(Y) * Y_up;
  *                                    shard i's output is column block i (the all-gather
  *                                    is this layout, no copy)
- * Errors: TP_ERR_INVALID_ARG (null X/W/out, N < 1, SwiGLU without W_up),
- *         TP_ERR_SHAPE (f % N, bf16 tile rules), TP_ERR_ALIGNMENT, TP_ERR_CUDA.
+ *   w_layout                         TP_W_IN_OUT: W, W_up as above; TP_W_OUT_IN: W, W_up
+ *                                    stored (f, h), shard i = row block i (the
+ *                                    Megatron listing's ColumnParallelLinear weight)
+ * Errors: TP_ERR_INVALID_ARG (null X/W/out, N < 1, SwiGLU without W_up, unknown
+ *         w_layout), TP_ERR_SHAPE (f % N, bf16 tile rules), TP_ERR_ALIGNMENT, TP_ERR_CUDA.
  */
 TP_API tp_status tp_col_linear(const void* X, const void* W, const void* W_up,
                         void* Y, void* Y_up, void* out,
                         int64_t M, int64_t h, int64_t f, int32_t N,
-                        tp_dtype dtype, tp_act act, void* stream);
+                        tp_dtype dtype, tp_act act, tp_wlayout w_layout, void* stream);
 
 /*
  * Row-parallel linear followed by the shard sum (the all-reduce stand-in).
@@ -252,12 +273,15 @@ TP_API tp_status tp_col_linear(const void* X, const void* W, const void* W_up,
  *   out      (M, n) device, written  sum_i X_i W_i (+ residual), element type `dtype`
  *   ws, ws_bytes                     TP_REDUCE_BUFFERS needs N*M*n*4 bytes
  *                                    (tp_workspace_size(TP_OP_ROW_LINEAR, M, k, n, ...))
+ *   w_layout                         TP_W_IN_OUT: W as above; TP_W_OUT_IN: W stored
+ *                                    (n, k), W_i = column block i (the Megatron
+ *                                    listing's RowParallelLinear weight)
  * Errors: as tp_col_linear, plus TP_ERR_WORKSPACE.
  */
 TP_API tp_status tp_row_linear(const void* Xs, const void* W, const void* residual, void* out,
                         int64_t M, int64_t k, int64_t n, int32_t N,
                         tp_dtype dtype, tp_reduce mode, void* ws, size_t ws_bytes,
-                        void* stream);
+                        tp_wlayout w_layout, void* stream);
 
 /*
  * The shard sum on its own: out = sum_{i=0}^{N-1} partials[i] (+ residual), in
@@ -323,6 +347,8 @@ TP_API tp_status tp_row_linear_ln(const void* Xs, const void* W, const void* res
  *                NULL = kept in the workspace instead.
  *   Z     (M, h) written.
  *   act   TP_ACT_GELU or TP_ACT_SWIGLU.  mode: the shard sum variant.
+ *   w_layout  TP_W_IN_OUT as above; TP_W_OUT_IN: W1, W1_up stored (f, h) and W2 stored
+ *             (h, f), the Megatron listing's (out, in) weights.
  * For bf16 and M <= 64 (decode) a weight-streaming kernel family is used.
  * Errors: as tp_row_linear.
  */
@@ -330,7 +356,7 @@ TP_API tp_status tp_mlp_fwd(const void* X, const void* W1, const void* W1_up, co
                      const void* residual, void* Y, void* Y_up, void* H, void* Z,
                      int64_t M, int64_t h, int64_t f, int32_t N,
                      tp_dtype dtype, tp_act act, tp_reduce mode,
-                     void* ws, size_t ws_bytes, void* stream);
+                     void* ws, size_t ws_bytes, tp_wlayout w_layout, void* stream);
 
 /*
  * Tensor-parallel MLP backward. g-backward is the identity (every shard reads all
@@ -347,6 +373,12 @@ TP_API tp_status tp_mlp_fwd(const void* X, const void* W1, const void* W1_up, co
  *   dZ    (M, h) read
  *   dX    (M, h) written;  dW1 (h, f), dW1_up (h, f, SwiGLU), dW2 (f, h) written
  *   ws    dY (or dG and dU) plus, for TP_REDUCE_BUFFERS, N*M*h fp32 partials
+ *   w_layout  as tp_mlp_fwd; with TP_W_OUT_IN the gradients are written (out, in)
+ *             like their weights: dW1, dW1_up (f, h) = dY^T X, dU^T X and dW2 (h, f) =
+ *             dZ^T H.
+ * With TP_REDUCE_BUFFERS the dX GEMM runs before the weight-gradient GEMMs and the
+ * shard sum of its partials runs on a side stream beside them (they do not read dX);
+ * the call is still one ordered unit on `stream`.
  * Errors: as tp_row_linear.
  */
 TP_API tp_status tp_mlp_bwd(const void* X, const void* W1, const void* W1_up, const void* W2,
@@ -354,7 +386,7 @@ TP_API tp_status tp_mlp_bwd(const void* X, const void* W1, const void* W1_up, co
                      void* dX, void* dW1, void* dW1_up, void* dW2,
                      int64_t M, int64_t h, int64_t f, int32_t N,
                      tp_dtype dtype, tp_act act, tp_reduce mode,
-                     void* ws, size_t ws_bytes, void* stream);
+                     void* ws, size_t ws_bytes, tp_wlayout w_layout, void* stream);
 
 /*
  * Row-parallel linear + shard sum with per-shard partial buffers, allocating

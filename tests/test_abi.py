@@ -32,7 +32,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_version_and_strings(L):
-    assert T.tp_version() == 1
+    assert T.tp_version() == 2
     for s in T.Status:
         assert T.tp_status_string(s) == "TP_" + ("OK" if s == 0 else "ERR_" + s.name)
 
@@ -178,3 +178,44 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(T, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         T.lib()
+
+
+def test_weight_layout_and_size_errors(L):
+    """The (out, in) weight layout of the Megatron listing (ColumnParallelLinear /
+    RowParallelLinear store W for F.linear) is an argument of the four linear entry
+    points; an unknown value, and sizes whose byte counts would not fit in 64 bits, are
+    rejected before anything is launched."""
+    OUT_IN = T.WLayout.OUT_IN
+    c = lambda **kw: (lambda: T.tp_col_linear(**{**dict(X=A16, W=A16, W_up=None, Y=None, Y_up=None,
+                                                           out=A16, M=10, h=128, f=256, N=2,
+                                                           dtype=BF, act=T.Act.GELU), **kw}))
+    assert _status(c(w_layout=2)) == T.Status.INVALID_ARG
+    assert _status(c(w_layout=OUT_IN, f=250)) == T.Status.SHAPE        # f % N in either layout
+    assert _status(c(w_layout=OUT_IN, act=T.Act.SWIGLU)) == T.Status.INVALID_ARG
+    assert _status(c(w_layout=OUT_IN, M=0)) == T.Status.OK
+    assert _status(c(M=1 << 40)) == T.Status.SHAPE                     # extent >= 2^31
+    r = lambda **kw: (lambda: T.tp_row_linear(**{**dict(Xs=A16, W=A16, residual=None, out=A16, M=10,
+                                                          k=256, n=128, N=2, dtype=BF,
+                                                          mode=T.Reduce.BUFFERS, ws=None,
+                                                          ws_bytes=0), **kw}))
+    assert _status(r(w_layout=-1)) == T.Status.INVALID_ARG
+    assert _status(r(w_layout=OUT_IN, k=200)) == T.Status.SHAPE
+    assert _status(r(w_layout=OUT_IN)) == T.Status.WORKSPACE
+    # N*M*n*4 with M*n = 2^40 elements and N = 2^16 would pass 2^64 in a plain product
+    assert _status(r(M=1 << 30, n=1 << 10, k=1 << 16, N=1 << 16)) == T.Status.SHAPE
+    assert T.tp_workspace_size(T.Op.ROW_LINEAR, 1 << 40, 128, 128, 2, BF) == 0
+    m = lambda **kw: (lambda: T.tp_mlp_fwd(**{**dict(X=A16, W1=A16, W1_up=None, W2=A16, residual=None,
+                                                       Y=None, Y_up=None, H=A16, Z=A16, M=10, h=128,
+                                                       f=256, N=2, dtype=BF, act=T.Act.GELU,
+                                                       mode=T.Reduce.SPLITK, ws=None, ws_bytes=0),
+                                                  **kw}))
+    assert _status(m(w_layout=3)) == T.Status.INVALID_ARG
+    assert _status(m(w_layout=OUT_IN, M=0)) == T.Status.OK
+    b = lambda **kw: (lambda: T.tp_mlp_bwd(**{**dict(X=A16, W1=A16, W1_up=None, W2=A16, Y=A16, Y_up=None,
+                                                       H=A16, dZ=A16, dX=A16, dW1=A16, dW1_up=None,
+                                                       dW2=A16, M=10, h=128, f=256, N=2, dtype=BF,
+                                                       act=T.Act.GELU, mode=T.Reduce.SPLITK,
+                                                       ws=A16, ws_bytes=10), **kw}))
+    assert _status(b(w_layout=7)) == T.Status.INVALID_ARG
+    assert _status(b(w_layout=OUT_IN)) == T.Status.WORKSPACE
+    assert _status(b(w_layout=OUT_IN, act=T.Act.SWIGLU)) == T.Status.INVALID_ARG
