@@ -70,6 +70,7 @@ struct AttnTcParams {
   int causal;
   int* status;
   uint64_t timeout_ns;
+  int debug_hang;       // test hook: the MMA thread first waits on a barrier nothing arrives on
 };
 
 __device__ __forceinline__ void record_timeout_attn(int* status) {
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(FwdLayout<NH>::kThreads, kCtasPerSm) attn_fwd_
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
-  const uint32_t q_full = bar0, drain = bar0 + 8 * 11;
+  const uint32_t q_full = bar0, drain = bar0 + 8 * 11, never = bar0 + 8 * 12;
   auto kv_full = [&](int st) { return bar0 + 8u * (1 + st); };
   auto kv_empty = [&](int st) { return bar0 + 8u * (3 + st); };
   auto s_full = [&](int h) { return bar0 + 8u * (5 + h); };
@@ -171,6 +172,7 @@ __global__ void __launch_bounds__(FwdLayout<NH>::kThreads, kCtasPerSm) attn_fwd_
       mbar_init(o_done(h), 1);
     }
     mbar_init(drain, 1);
+    mbar_init(never, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -214,6 +216,7 @@ __global__ void __launch_bounds__(FwdLayout<NH>::kThreads, kCtasPerSm) attn_fwd_
       const uint32_t id_s = idesc_bf16_f32(128, kKB, 0, 0);  // Q, K both K-major
       const uint32_t id_o = idesc_bf16_f32(128, 64, 0, 1);   // P K-major, V MN-major
       bool ok = mbar_wait(q_full, 0, p.timeout_ns, abort_flag);
+      if (ok && p.debug_hang) ok = mbar_wait(never, 0, p.timeout_ns, abort_flag);
       // S_h = Q_h K^T of key block j (the block's K/V stage must have landed)
       auto issue_s = [&](int j, int h) -> bool {
         const int st = j & 1;
@@ -420,6 +423,7 @@ struct AttnBwdParams {
   int causal;
   int* status;
   uint64_t timeout_ns;
+  int debug_hang;  // test hook, as in the forward's parameters
 };
 
 // ld[b, t, q] = (lse log2(e), D) with D = the sum over the head's 64 columns of dO * O;
@@ -495,7 +499,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dq_tc_kernel(const __
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
   const uint32_t qd_full = bar0, s_full = bar0 + 8 * 5, p_full = bar0 + 8 * 6,
-                 o_done = bar0 + 8 * 7, drain = bar0 + 8 * 8;
+                 o_done = bar0 + 8 * 7, drain = bar0 + 8 * 8, never = bar0 + 8 * 9;
   auto kv_full = [&](int st) { return bar0 + 8u * (1 + st); };
   auto kv_empty = [&](int st) { return bar0 + 8u * (3 + st); };
 
@@ -519,6 +523,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dq_tc_kernel(const __
     mbar_init(p_full, 8);  // one arrive per element-wise warp
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
+    mbar_init(never, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -559,6 +564,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dq_tc_kernel(const __
       const uint32_t id_s = idesc_bf16_f32(128, 64, 0, 0);
       const uint32_t id_g = idesc_bf16_f32(128, 64, 0, 1);
       bool ok = mbar_wait(qd_full, 0, p.timeout_ns, abort_flag);
+      if (ok && p.debug_hang) ok = mbar_wait(never, 0, p.timeout_ns, abort_flag);
       auto issue_s = [&](int j) -> bool {  // S = Q K^T and dP = dO V^T of key block j
         const int st = j & 1;
         if (!mbar_wait(kv_full(st), (j >> 1) & 1, p.timeout_ns, abort_flag)) return false;
@@ -712,7 +718,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dkdv_tc_kernel(const 
   float2* ldtab = reinterpret_cast<float2*>(smem + 6 * kBwdQKVTile + 256);  // [8 warps][32]
   const uint32_t bar0 = smem_u32(bars);
   const uint32_t kv_full = bar0, s_full = bar0 + 8 * 5, p_full = bar0 + 8 * 6,
-                 o_done = bar0 + 8 * 7, drain = bar0 + 8 * 8;
+                 o_done = bar0 + 8 * 7, drain = bar0 + 8 * 8, never = bar0 + 8 * 9;
   auto qd_full = [&](int st) { return bar0 + 8u * (1 + st); };
   auto qd_empty = [&](int st) { return bar0 + 8u * (3 + st); };
 
@@ -736,6 +742,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dkdv_tc_kernel(const 
     mbar_init(p_full, 8);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
+    mbar_init(never, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -779,6 +786,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dkdv_tc_kernel(const 
       const uint32_t id_s = idesc_bf16_f32(128, 64, 0, 0);
       const uint32_t id_g = idesc_bf16_f32(128, 64, 0, 1);
       bool ok = mbar_wait(kv_full, 0, p.timeout_ns, abort_flag);
+      if (ok && p.debug_hang) ok = mbar_wait(never, 0, p.timeout_ns, abort_flag);
       auto issue_s = [&](int w) -> bool {  // S^T = K Q^T and dP^T = V dO^T of item w
         const int st = w & 1;
         if (!mbar_wait(qd_full(st), (w >> 1) & 1, p.timeout_ns, abort_flag)) return false;
@@ -998,6 +1006,7 @@ tp_status launch_attention_fwd_tc(const void* qkv, void* o, float* lse, int64_t 
   p.status = device_status_word();
   if (!p.status) return fail(TP_ERR_CUDA, "device status word unavailable");
   p.timeout_ns = wait_timeout_ns();
+  p.debug_hang = debug_hang_flag();
   static std::atomic<uint64_t> attr_set{0};
   if (needs_setup(attr_set)) {
     TP_CUDA_TRY(cudaFuncSetAttribute(attn_fwd_tc_kernel<1>,
@@ -1077,6 +1086,7 @@ tp_status launch_attention_bwd_tc(const void* qkv, const void* o, const float* l
   p.status = device_status_word();
   if (!p.status) return fail(TP_ERR_CUDA, "device status word unavailable");
   p.timeout_ns = wait_timeout_ns();
+  p.debug_hang = debug_hang_flag();
   static std::atomic<uint64_t> attr_set{0};
   if (needs_setup(attr_set)) {
     TP_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_dq_tc_kernel,

@@ -1120,6 +1120,7 @@ std::atomic<int> g_pair_mode{1};  // 1: CTA-pair kernel for large tiles, 0: one-
 }  // namespace
 
 void set_debug_hang(int v) { g_debug_hang.store(v); }
+int debug_hang_flag() { return g_debug_hang.load(); }
 void set_pair_mode(int v) { g_pair_mode.store(v); }
 
 tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {

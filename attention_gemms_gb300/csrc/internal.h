@@ -51,6 +51,9 @@ inline bool needs_setup(const std::atomic<uint64_t>& done) {
 }
 inline void mark_device(std::atomic<uint64_t>& done) { done.fetch_or(device_bit()); }
 void count_launch(int n = 1);
+// test hook (tp_debug_inject_wait_fault): kernels launched while it is set make their
+// MMA thread wait on a barrier nothing arrives on, so the bounded wait runs out
+int debug_hang_flag();
 
 // An independent branch of one library call on a per-device side stream: the
 // constructor forks it off `main` (an event recorded on `main`, waited for by the side

@@ -98,6 +98,17 @@ COL_GEMM_TRAFFIC = {
 }
 
 
+# Tensor-pipe activity of the same launch (sm__pipe_tensor_cycles_active and
+# sm__pipe_tc_cycles_active, % of peak over the elapsed cycles) from an ncu capture,
+# under the same source-hash rule; c5's is taken on the c5-2k case (2048 of the 8192
+# tokens: the same kernel instance, tile shapes and per-tile K). See profiles/.
+COL_GEMM_TENSOR_PIPE = {
+    "c5": {"tensor": 77.7, "tc": 85.5, "case": "c5-2k", "src": "b0ab4dd1afc6ba5c"},
+    "c5-2k": {"tensor": 77.7, "tc": 85.5, "case": "c5-2k", "src": "b0ab4dd1afc6ba5c"},
+    "c3": {"tensor": 66.3, "tc": 74.1, "case": "c3", "src": "b0ab4dd1afc6ba5c"},
+}
+
+
 def _kernel_source_hash():
     """Hash of the tensor-core GEMM's source (kernel and its PTX wrappers): a stored
     traffic figure is reported only while the kernel it was measured on is unchanged."""
@@ -114,6 +125,14 @@ def col_gemm_traffic(workload):
     if not t or t["src"] != _kernel_source_hash():
         return None
     return t["bytes"]
+
+
+def col_gemm_tensor_pipe(workload):
+    t = COL_GEMM_TENSOR_PIPE.get(workload)
+    if not t or t["src"] != _kernel_source_hash():
+        return None
+    return {"sm__pipe_tensor_cycles_active_pct": t["tensor"],
+            "sm__pipe_tc_cycles_active_pct": t["tc"], "captured_on": t["case"]}
 
 
 def load_peaks():
@@ -490,6 +509,7 @@ def run_ours(args, w):
                      "peak_source": f"{src} bf16 dense (burst)",
                      "vendor_peak": {"value": vp, "label": VENDOR_PEAKS["label"]},
                      "traffic": traffic,
+                     "tensor_pipe_active": col_gemm_tensor_pipe(args.workload),
                      "algorithmic_flops_per_launch": col_gemm_flops(w),
                      "avg_launch_ms": round(col_max, 4)},
         "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s",

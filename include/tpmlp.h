@@ -670,8 +670,10 @@ TP_API tp_status tp_gpt_fwd_bwd(const tp_gpt_config* cfg, const tp_gpt_weights* 
 
 /* ------------------------------------------------------------------ testing */
 
-/* Failure injection for tests. While enabled (non-zero), every tensor-core GEMM
- * launch makes its MMA warp first wait on a barrier that nothing arrives on, so the
+/* Failure injection for tests. While enabled (non-zero), every launch of a kernel with
+ * bounded barrier waits -- the tensor-core GEMMs (CTA-pair, one-CTA and decode
+ * configurations) and the tensor-core attention forward, dQ and dK/dV kernels --
+ * makes its MMA thread first wait on a barrier that nothing arrives on, so the
  * bounded wait expires; the kernel then stops cleanly (its copies and MMAs drained,
  * TMEM freed) and tp_check_status reports TP_ERR_TIMEOUT. Nothing faults on the
  * device. Off by default; outputs of launches made while it is on are undefined. */
