@@ -147,6 +147,7 @@ __global__ void __launch_bounds__(FwdLayout<NH>::kThreads, kCtasPerSm) attn_fwd_
   auto s_full = [&](int h) { return bar0 + 8u * (5 + h); };
   auto p_full = [&](int h) { return bar0 + 8u * (7 + h); };
   auto o_done = [&](int h) { return bar0 + 8u * (9 + h); };
+  auto s_free = [&](int h) { return bar0 + 8u * (13 + h); };  // slot 12: the test hook's
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.z, t0 = blockIdx.y * NH, q0 = blockIdx.x * kQ;  // heads t0 .. t0 + NH - 1
@@ -169,6 +170,7 @@ __global__ void __launch_bounds__(FwdLayout<NH>::kThreads, kCtasPerSm) attn_fwd_
     for (int h = 0; h < NH; ++h) {
       mbar_init(s_full(h), 1);
       mbar_init(p_full(h), 4);  // one arrive per softmax warp of the head
+      mbar_init(s_free(h), 4);  // likewise, once a warp has read the head's S out of TMEM
       mbar_init(o_done(h), 1);
     }
     mbar_init(drain, 1);
@@ -234,6 +236,19 @@ __global__ void __launch_bounds__(FwdLayout<NH>::kThreads, kCtasPerSm) attn_fwd_
       for (int j = 0; j < nkb && ok; ++j) {
         const int st = j & 1;
         const uint32_t vaddr = sb + Lay::kOffKV + st * 2 * kKVTile + kKVTile;
+        // S_h(j) has been read out of TMEM: the next block's scores are issued while the
+        // softmax warps still form P_h(j), and go ahead of P V
+        for (int h = 0; h < NH && ok; ++h) {
+          if (!mbar_wait(s_free(h), j & 1, p.timeout_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (j + 1 < nkb && !issue_s(j + 1, h)) {
+            ok = false;
+            break;
+          }
+        }
         // the heads in turn: while one head's softmax runs, the other's MMAs do
         for (int h = 0; h < NH && ok; ++h) {
           if (!mbar_wait(p_full(h), j & 1, p.timeout_ns, abort_flag)) {
@@ -241,11 +256,6 @@ __global__ void __launch_bounds__(FwdLayout<NH>::kThreads, kCtasPerSm) attn_fwd_
             break;
           }
           tc_fence_after();
-          // S_h(j) has been read: the next block's scores go ahead of P V
-          if (j + 1 < nkb && !issue_s(j + 1, h)) {
-            ok = false;
-            break;
-          }
 #pragma unroll
           for (int kk = 0; kk < kKB / 16; ++kk)
             mma_bf16_ss(tO(h), sw128_desc(sb + Lay::kOffP + h * (kQ * kKB * 2) + kk * 32, 16u, 1024u),
@@ -284,6 +294,9 @@ __global__ void __launch_bounds__(FwdLayout<NH>::kThreads, kCtasPerSm) attn_fwd_
       tmem_ld32(tS(hh) + lanes, *reinterpret_cast<uint32_t(*)[32]>(v));
       tmem_ld32(tS(hh) + lanes + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
       tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free(hh));
       // the block's row maximum (masked keys: beyond the sequence, or after the query)
       const bool full = k0 + kKB <= p.s && !(p.causal && k0 + kKB - 1 > qi);
       float mb = -INFINITY;
@@ -499,7 +512,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dq_tc_kernel(const __
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
   const uint32_t qd_full = bar0, s_full = bar0 + 8 * 5, p_full = bar0 + 8 * 6,
-                 o_done = bar0 + 8 * 7, drain = bar0 + 8 * 8, never = bar0 + 8 * 9;
+                 o_done = bar0 + 8 * 7, drain = bar0 + 8 * 8, never = bar0 + 8 * 9,
+                 s_free = bar0 + 8 * 10;
   auto kv_full = [&](int st) { return bar0 + 8u * (1 + st); };
   auto kv_empty = [&](int st) { return bar0 + 8u * (3 + st); };
 
@@ -521,6 +535,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dq_tc_kernel(const __
     }
     mbar_init(s_full, 1);
     mbar_init(p_full, 8);  // one arrive per element-wise warp
+    mbar_init(s_free, 8);  // likewise, once a warp has read S and dP out of TMEM
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     mbar_init(never, 1);
@@ -583,16 +598,22 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dq_tc_kernel(const __
       };
       if (ok) ok = issue_s(0);
       for (int j = 0; j < nkb && ok; ++j) {
+        // S and dP of block j have been read out of TMEM: the next block's are issued
+        // while the element-wise warps still form dS of block j
+        if (!mbar_wait(s_free, j & 1, p.timeout_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (j + 1 < nkb && !issue_s(j + 1)) {
+          ok = false;
+          break;
+        }
         if (!mbar_wait(p_full, j & 1, p.timeout_ns, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        // S and dP of block j have been read: the next block's go first
-        if (j + 1 < nkb && !issue_s(j + 1)) {
-          ok = false;
-          break;
-        }
         const int st = j & 1;
         const uint32_t k = sKV + st * 2 * kBwdBlk;
 #pragma unroll
@@ -628,6 +649,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dq_tc_kernel(const __
       tmem_ld32(tS + L.lanes + L.half * 32, sv);
       tmem_ld32(tdP + L.lanes + L.half * 32, pv);
       tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free);
       const int k0 = j * 64 + L.half * 32;
       uint32_t dk[16];  // P (dP - D) as packed bf16 pairs; 1 / sqrt(d) applied to dQ at the end
       if (valid && k0 + 32 <= p.s && !(p.causal && k0 + 31 > qi)) {
@@ -718,7 +742,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dkdv_tc_kernel(const 
   float2* ldtab = reinterpret_cast<float2*>(smem + 6 * kBwdQKVTile + 256);  // [8 warps][32]
   const uint32_t bar0 = smem_u32(bars);
   const uint32_t kv_full = bar0, s_full = bar0 + 8 * 5, p_full = bar0 + 8 * 6,
-                 o_done = bar0 + 8 * 7, drain = bar0 + 8 * 8, never = bar0 + 8 * 9;
+                 o_done = bar0 + 8 * 7, drain = bar0 + 8 * 8, never = bar0 + 8 * 9,
+                 s_free = bar0 + 8 * 10;
   auto qd_full = [&](int st) { return bar0 + 8u * (1 + st); };
   auto qd_empty = [&](int st) { return bar0 + 8u * (3 + st); };
 
@@ -740,6 +765,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dkdv_tc_kernel(const 
     }
     mbar_init(s_full, 1);
     mbar_init(p_full, 8);
+    mbar_init(s_free, 8);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     mbar_init(never, 1);
@@ -805,7 +831,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dkdv_tc_kernel(const 
       };
       if (ok && nw > 0) ok = issue_s(0);
       for (int w = 0; w < nw && ok; ++w) {
-        if (!mbar_wait(p_full, w & 1, p.timeout_ns, abort_flag)) {
+        // S^T and dP^T of item w have been read out of TMEM: the next item's are issued
+        // while the element-wise warps still form P^T and dS^T of item w
+        if (!mbar_wait(s_free, w & 1, p.timeout_ns, abort_flag)) {
           ok = false;
           break;
         }
@@ -814,6 +842,11 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dkdv_tc_kernel(const 
           ok = false;
           break;
         }
+        if (!mbar_wait(p_full, w & 1, p.timeout_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
         const int st = w & 1;
         const uint32_t q = sQD + st * 2 * kBwdBlk, d = q + kBwdBlk;
 #pragma unroll
@@ -864,6 +897,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dkdv_tc_kernel(const 
       tmem_ld32(tST + L.lanes + L.half * 32, sv);
       tmem_ld32(tdPT + L.lanes + L.half * 32, pv);
       tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free);
       // P^T and P^T (dP^T - D) as packed bf16 pairs; 1 / sqrt(d) applied to dK at the end
       uint32_t pk[16], dk[16];
       // one loop for full and masked items (two specialised loops exceed the register
