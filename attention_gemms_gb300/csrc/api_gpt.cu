@@ -146,6 +146,38 @@ tp_status tp_adamw_step(float* p, const float* g, float* m, float* v, int64_t n,
                       static_cast<cudaStream_t>(stream));
 }
 
+tp_status tp_train_step_advance(int32_t* step, const float* loss, float* loss_hist,
+                                int64_t hist_len, void* stream) {
+  TP_TRY(need(step != nullptr, TP_ERR_INVALID_ARG, "step is required"));
+  TP_TRY(need((loss == nullptr) == (loss_hist == nullptr), TP_ERR_INVALID_ARG,
+              "loss and loss_hist go together"));
+  TP_TRY(need(!loss_hist || hist_len >= 1, TP_ERR_INVALID_ARG, "hist_len must be >= 1"));
+  for (const void* q : {static_cast<const void*>(step), static_cast<const void*>(loss),
+                        static_cast<const void*>(loss_hist)})
+    TP_TRY(need(reinterpret_cast<uintptr_t>(q) % 4 == 0, TP_ERR_ALIGNMENT,
+                "step, loss and loss_hist must be 4-byte aligned"));
+  TP_TRY(check_device());
+  return launch_step_advance(step, loss, loss_hist, hist_len, static_cast<cudaStream_t>(stream));
+}
+
+tp_status tp_adamw_step_device(float* p, const float* g, float* m, float* v, int64_t n,
+                               const int32_t* step, float lr, float beta1, float beta2, float eps,
+                               float weight_decay, void* stream) {
+  TP_TRY(need(p && g && m && v && step, TP_ERR_INVALID_ARG, "p, g, m, v and step are required"));
+  TP_TRY(need(n >= 0, TP_ERR_INVALID_ARG, "need n >= 0"));
+  TP_TRY(need(beta1 >= 0.0f && beta1 < 1.0f && beta2 >= 0.0f && beta2 < 1.0f && eps > 0.0f,
+              TP_ERR_INVALID_ARG, "need 0 <= beta < 1 and eps > 0"));
+  for (const void* q : {static_cast<const void*>(p), static_cast<const void*>(g),
+                        static_cast<const void*>(m), static_cast<const void*>(v),
+                        static_cast<const void*>(step)})
+    TP_TRY(need(reinterpret_cast<uintptr_t>(q) % 4 == 0, TP_ERR_ALIGNMENT,
+                "p, g, m, v and step must be 4-byte aligned"));
+  if (n == 0) return TP_OK;
+  TP_TRY(check_device());
+  return launch_adamw_dev(p, g, m, v, n, step, lr, beta1, beta2, eps, weight_decay,
+                          static_cast<cudaStream_t>(stream));
+}
+
 size_t tp_gpt_workspace_size(const tp_gpt_config* cfg, tp_dtype dtype, tp_reduce mode) {
   if (!cfg || dtype != TP_F32 || cfg->shards < 1 || cfg->vocab % cfg->shards) return 0;
   return gpt_layout(*cfg, dtype, mode).total;

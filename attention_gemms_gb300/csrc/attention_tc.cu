@@ -236,9 +236,10 @@ __global__ void __launch_bounds__(FwdLayout<NH>::kThreads, kCtasPerSm) attn_fwd_
       for (int j = 0; j < nkb && ok; ++j) {
         const int st = j & 1;
         const uint32_t vaddr = sb + Lay::kOffKV + st * 2 * kKVTile + kKVTile;
-        // S_h(j) has been read out of TMEM: the next block's scores are issued while the
-        // softmax warps still form P_h(j), and go ahead of P V
+        // the heads in turn: while one head's softmax runs, the other's MMAs do
         for (int h = 0; h < NH && ok; ++h) {
+          // S_h(j) has been read out of TMEM: the next block's scores are issued while
+          // the softmax warps still form P_h(j), and go ahead of P V
           if (!mbar_wait(s_free(h), j & 1, p.timeout_ns, abort_flag)) {
             ok = false;
             break;
@@ -248,9 +249,6 @@ __global__ void __launch_bounds__(FwdLayout<NH>::kThreads, kCtasPerSm) attn_fwd_
             ok = false;
             break;
           }
-        }
-        // the heads in turn: while one head's softmax runs, the other's MMAs do
-        for (int h = 0; h < NH && ok; ++h) {
           if (!mbar_wait(p_full(h), j & 1, p.timeout_ns, abort_flag)) {
             ok = false;
             break;
@@ -278,10 +276,12 @@ __global__ void __launch_bounds__(FwdLayout<NH>::kThreads, kCtasPerSm) attn_fwd_
     const uint32_t sP = sb + Lay::kOffP + hh * (kQ * kKB * 2);
     float m2 = -INFINITY, l = 0.0f;
     bool ok = true;
+    // every lane polls the barrier (one warp-wide instruction per poll), so the warp does
+    // not split into a waiting lane and 31 lanes parked at a shuffle; the lanes agree on
+    // the outcome before any warp-wide TMEM access
     auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
-      int w = 1;
-      if (lane == 0) w = mbar_wait(bar, parity, p.timeout_ns, abort_flag) ? 1 : 0;
-      return __shfl_sync(0xFFFFFFFFu, w, 0) != 0;
+      const bool w = mbar_wait(bar, parity, p.timeout_ns, abort_flag);
+      return __all_sync(0xFFFFFFFFu, w) != 0;
     };
     for (int j = 0; j < nkb; ++j) {
       if (!wait_all(s_full(hh), j & 1)) {
@@ -634,10 +634,12 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dq_tc_kernel(const __
                             : make_float2(0.0f, 0.0f);
     const float lse2 = ld.x, Dq = ld.y;
     bool ok = true;
+    // every lane polls the barrier (one warp-wide instruction per poll), so the warp does
+    // not split into a waiting lane and 31 lanes parked at a shuffle; the lanes agree on
+    // the outcome before any warp-wide TMEM access
     auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
-      int w = 1;
-      if (lane == 0) w = mbar_wait(bar, parity, p.timeout_ns, abort_flag) ? 1 : 0;
-      return __shfl_sync(0xFFFFFFFFu, w, 0) != 0;
+      const bool w = mbar_wait(bar, parity, p.timeout_ns, abort_flag);
+      return __all_sync(0xFFFFFFFFu, w) != 0;
     };
     for (int j = 0; j < nkb; ++j) {
       if (!wait_all(s_full, j & 1)) {
@@ -868,10 +870,12 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dkdv_tc_kernel(const 
     const int kj = k0 + L.r;
     const bool valid = kj < p.s;
     bool ok = true;
+    // every lane polls the barrier (one warp-wide instruction per poll), so the warp does
+    // not split into a waiting lane and 31 lanes parked at a shuffle; the lanes agree on
+    // the outcome before any warp-wide TMEM access
     auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
-      int w = 1;
-      if (lane == 0) w = mbar_wait(bar, parity, p.timeout_ns, abort_flag) ? 1 : 0;
-      return __shfl_sync(0xFFFFFFFFu, w, 0) != 0;
+      const bool w = mbar_wait(bar, parity, p.timeout_ns, abort_flag);
+      return __all_sync(0xFFFFFFFFu, w) != 0;
     };
     float2* tab = ldtab + warp * 32;
     const float4* tab4 = reinterpret_cast<const float4*>(tab);

@@ -218,6 +218,13 @@ tp_status launch_vocab_ce_bwd(const void* logits, const int32_t* targets, const 
 tp_status launch_adamw(float* p, const float* g, float* m, float* v, int64_t n, float lr,
                        float b1, float b2, float eps, float wd, float bc1, float bc2,
                        cudaStream_t st);
+// AdamW whose step count (for the bias corrections) is read from device memory
+tp_status launch_adamw_dev(float* p, const float* g, float* m, float* v, int64_t n,
+                           const int32_t* step, float lr, float b1, float b2, float eps, float wd,
+                           cudaStream_t st);
+// *step += 1; hist[(*step - 1) % hist_len] = *loss (when loss and hist are given)
+tp_status launch_step_advance(int32_t* step, const float* loss, float* hist, int64_t hist_len,
+                              cudaStream_t st);
 
 // ------------------------------------------------------------------ API helpers (api.cu)
 

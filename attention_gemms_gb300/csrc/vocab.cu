@@ -366,6 +366,43 @@ __global__ void __launch_bounds__(kThreads) adamw_kernel(
   }
 }
 
+// The same update with the step count read from device memory: thread 0 of every CTA
+// forms the bias corrections 1 - beta^step (in double, as the host path does) for the
+// CTA, so the launch has no per-step argument and can replay from a CUDA graph.
+__global__ void __launch_bounds__(kThreads) adamw_dev_kernel(
+    float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
+    float* __restrict__ v, int64_t n, const int32_t* __restrict__ step, float lr, float b1,
+    float b2, float eps, float wd) {
+  __shared__ float bc[2];
+  if (threadIdx.x == 0) {
+    const double t = static_cast<double>(*step);
+    bc[0] = static_cast<float>(1.0 - pow(static_cast<double>(b1), t));
+    bc[1] = static_cast<float>(1.0 - pow(static_cast<double>(b2), t));
+  }
+  __syncthreads();
+  const float bc1 = bc[0], bc2 = bc[1];
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += stride) {
+    const float gi = g[i];
+    const float mi = b1 * m[i] + (1.0f - b1) * gi;
+    const float vi = b2 * v[i] + (1.0f - b2) * gi * gi;
+    m[i] = mi;
+    v[i] = vi;
+    const float pi = p[i] * (1.0f - lr * wd);
+    p[i] = pi - lr * (mi / bc1) / (sqrtf(vi / bc2) + eps);
+  }
+}
+
+// One step of a training loop's device-side bookkeeping: the step counter advances by
+// one, and the step's loss goes to its slot of the loss history.
+__global__ void step_advance_kernel(int32_t* step, const float* loss, float* hist,
+                                    int64_t hist_len) {
+  const int32_t t = *step + 1;
+  *step = t;
+  if (loss && hist) hist[static_cast<int64_t>(t - 1) % hist_len] = *loss;
+}
+
 template <typename T>
 tp_status embed_fwd_t(const int32_t* ids, const void* E, void* x, int64_t M, int64_t v, int h,
                       int N, cudaStream_t st) {
@@ -460,6 +497,26 @@ tp_status launch_adamw(float* p, const float* g, float* m, float* v, int64_t n, 
   const int64_t blocks = std::min<int64_t>((n + kThreads - 1) / kThreads, 8ll * device_sm_count());
   adamw_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, st>>>(p, g, m, v, n, lr, b1, b2,
                                                                     eps, wd, bc1, bc2);
+  count_launch();
+  TP_CUDA_TRY(cudaGetLastError());
+  return TP_OK;
+}
+
+tp_status launch_adamw_dev(float* p, const float* g, float* m, float* v, int64_t n,
+                           const int32_t* step, float lr, float b1, float b2, float eps, float wd,
+                           cudaStream_t st) {
+  if (n <= 0) return TP_OK;
+  const int64_t blocks = std::min<int64_t>((n + kThreads - 1) / kThreads, 8ll * device_sm_count());
+  adamw_dev_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, st>>>(p, g, m, v, n, step, lr,
+                                                                        b1, b2, eps, wd);
+  count_launch();
+  TP_CUDA_TRY(cudaGetLastError());
+  return TP_OK;
+}
+
+tp_status launch_step_advance(int32_t* step, const float* loss, float* hist, int64_t hist_len,
+                              cudaStream_t st) {
+  step_advance_kernel<<<1, 1, 0, st>>>(step, loss, hist, hist_len);
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;

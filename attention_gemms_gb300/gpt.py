@@ -3,8 +3,10 @@
 Allocates the parameters, their gradients and the AdamW moments as four flat fp32
 device buffers (every tensor at a 64-element-aligned offset), points the library's
 tp_gpt_weights / tp_gpt_grads structs into them, and sequences one training step as
-two library calls: tp_gpt_fwd_bwd (loss and every gradient) and tp_adamw_step over
-the whole flat buffer. No arithmetic of the model runs here.
+three library calls: tp_gpt_fwd_bwd (loss and every gradient), tp_train_step_advance
+(the device-side step counter and loss history) and tp_adamw_step_device over the whole
+flat buffer. No host argument changes from one step to the next, so capture() records a
+step once as a CUDA graph and replay() runs it. No arithmetic of the model runs here.
 
 Parameter order (also the flat layout): E, then per layer gamma1, beta1, Wqkv, Wo,
 gamma2, beta2, W1, W2, then gammaf, betaf -- the layer and weight shapes of
@@ -47,6 +49,9 @@ class SmallGPT:
         z = lambda: torch.zeros(off, dtype=torch.float32, device=device)
         self.p, self.g, self.m, self.v = z(), z(), z(), z()
         self.losses = torch.zeros(max(steps, 1), dtype=torch.float32, device=device)
+        self.loss_now = torch.zeros(1, dtype=torch.float32, device=device)
+        self.step_dev = torch.zeros(1, dtype=torch.int32, device=device)
+        self.graph = None
         wsb = T.tp_gpt_workspace_size(self.cfg, T.DType.F32, mode)
         if wsb == 0:
             raise ValueError("invalid GPT configuration")
@@ -78,6 +83,7 @@ class SmallGPT:
             self.view(self.p, name).copy_(torch.from_numpy(np.asarray(params[name], np.float32)))
         self.m.zero_()
         self.v.zero_()
+        self.step_dev.zero_()
         self.t = 0
 
     def set_batch(self, ids, targets):
@@ -90,9 +96,29 @@ class SmallGPT:
                          self.losses[loss_slot:loss_slot + 1], T.DType.F32, self.mode, self.ws,
                          self.ws.numel(), stream)
 
+    def _enqueue_step(self, opt, stream):
+        T.tp_gpt_fwd_bwd(self.cfg, self.weights, self.grads, self.ids, self.targets,
+                         self.loss_now, T.DType.F32, self.mode, self.ws, self.ws.numel(), stream)
+        T.tp_train_step_advance(self.step_dev, self.loss_now, self.losses, self.losses.numel(),
+                                stream)
+        T.tp_adamw_step_device(self.p, self.g, self.m, self.v, self.n, self.step_dev, opt["lr"],
+                               opt["beta1"], opt["beta2"], opt["eps"], opt["weight_decay"], stream)
+
     def step(self, opt=ADAMW, stream=None):
         """One training step on the loaded batch: loss into losses[t], then AdamW."""
-        self.fwd_bwd(self.t % self.losses.numel(), stream)
+        self._enqueue_step(opt, stream)
         self.t += 1
-        T.tp_adamw_step(self.p, self.g, self.m, self.v, self.n, self.t, opt["lr"], opt["beta1"],
-                        opt["beta2"], opt["eps"], opt["weight_decay"], stream)
+
+    def capture(self, opt=ADAMW):
+        """Record one training step (the launches of step()) as a CUDA graph. Make at least
+        one eager step first: the library sets its kernels' attributes and creates its side
+        streams outside a capture."""
+        import torch
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self._enqueue_step(opt, None)
+
+    def replay(self):
+        """One training step from the captured graph (its stream is torch's current one)."""
+        self.graph.replay()
+        self.t += 1

@@ -170,6 +170,8 @@ _SIGS = {
     "tp_vocab_ce_fwd": (_ST, [_P] * 6 + [_I64, _I64, _I32, _ST, _P]),
     "tp_vocab_ce_bwd": (_ST, [_P] * 4 + [_I64, _I64, _I32, ctypes.c_float, _ST, _P]),
     "tp_adamw_step": (_ST, [_P] * 4 + [_I64, _I64] + [ctypes.c_float] * 5 + [_P]),
+    "tp_train_step_advance": (_ST, [_P, _P, _P, _I64, _P]),
+    "tp_adamw_step_device": (_ST, [_P] * 4 + [_I64, _P] + [ctypes.c_float] * 5 + [_P]),
     "tp_gpt_workspace_size": (_SZ, [ctypes.POINTER(GptConfig), _ST, _ST]),
     "tp_gpt_fwd_bwd": (_ST, [ctypes.POINTER(GptConfig), ctypes.POINTER(GptWeights),
                              ctypes.POINTER(GptGrads), _P, _P, _P, _ST, _ST, _P, _SZ, _P]),
@@ -418,6 +420,17 @@ def tp_adamw_step(p, g, m, v, n, step, lr, beta1, beta2, eps, weight_decay, stre
     _check(lib().tp_adamw_step(_ptr(p), _ptr(g), _ptr(m), _ptr(v), n, step, float(lr),
                                float(beta1), float(beta2), float(eps), float(weight_decay),
                                _stream(stream)))
+
+
+def tp_train_step_advance(step, loss, loss_hist, hist_len, stream=None):
+    _check(lib().tp_train_step_advance(_ptr(step), _ptr(loss), _ptr(loss_hist), int(hist_len),
+                                       _stream(stream)))
+
+
+def tp_adamw_step_device(p, g, m, v, n, step, lr, beta1, beta2, eps, weight_decay, stream=None):
+    _check(lib().tp_adamw_step_device(_ptr(p), _ptr(g), _ptr(m), _ptr(v), n, _ptr(step),
+                                      float(lr), float(beta1), float(beta2), float(eps),
+                                      float(weight_decay), _stream(stream)))
 
 
 def tp_gpt_workspace_size(cfg, dtype, mode):

@@ -651,6 +651,24 @@ TP_API tp_status tp_adamw_step(float* p, const float* g, float* m, float* v, int
                                int64_t step, float lr, float beta1, float beta2, float eps,
                                float weight_decay, void* stream);
 
+/* The device-side bookkeeping of one training step, for a loop whose steps replay from a
+ * CUDA graph (a graph cannot take a new host argument per replay): *step (one int32 in
+ * device memory, 0 before the first step) advances by one, and when loss and loss_hist
+ * are given (both or neither), loss_hist[(*step - 1) % hist_len] = *loss. Enqueue it after
+ * the step's loss is written and before tp_adamw_step_device. (The pages' training loop,
+ * Megatron-LM 实战 04, 训练入口, keeps its step count and losses on the host.)
+ * Errors: TP_ERR_INVALID_ARG, TP_ERR_ALIGNMENT (4-byte), TP_ERR_CUDA. */
+TP_API tp_status tp_train_step_advance(int32_t* step, const float* loss, float* loss_hist,
+                                       int64_t hist_len, void* stream);
+
+/* tp_adamw_step with the step count read from device memory (*step >= 1, the counter that
+ * tp_train_step_advance keeps) instead of a host argument; the same arithmetic, with the
+ * bias corrections 1 - beta^step formed in double precision on the device. p, g, m, v and
+ * step must be 4-byte aligned. */
+TP_API tp_status tp_adamw_step_device(float* p, const float* g, float* m, float* v, int64_t n,
+                                      const int32_t* step, float lr, float beta1, float beta2,
+                                      float eps, float weight_decay, void* stream);
+
 /* Bytes of workspace tp_gpt_fwd_bwd needs (0 on invalid arguments). */
 TP_API size_t tp_gpt_workspace_size(const tp_gpt_config* cfg, tp_dtype dtype, tp_reduce mode);
 

@@ -219,3 +219,23 @@ def test_weight_layout_and_size_errors(L):
     assert _status(b(w_layout=7)) == T.Status.INVALID_ARG
     assert _status(b(w_layout=OUT_IN)) == T.Status.WORKSPACE
     assert _status(b(w_layout=OUT_IN, act=T.Act.SWIGLU)) == T.Status.INVALID_ARG
+
+
+def test_device_step_argument_errors(L):
+    """The device-side step counter and the AdamW that reads it: argument errors come back
+    before any launch."""
+    adv = lambda **kw: (lambda: T.tp_train_step_advance(**{**dict(step=A16, loss=A16, loss_hist=A16,
+                                                                   hist_len=50), **kw}))
+    assert _status(adv(step=None)) == T.Status.INVALID_ARG
+    assert _status(adv(loss=None)) == T.Status.INVALID_ARG        # loss and loss_hist go together
+    assert _status(adv(hist_len=0)) == T.Status.INVALID_ARG
+    assert _status(adv(step=A16 + 2)) == T.Status.ALIGNMENT
+    ad = lambda **kw: (lambda: T.tp_adamw_step_device(**{**dict(p=A16, g=A16, m=A16, v=A16, n=10,
+                                                                step=A16, lr=1e-3, beta1=0.9,
+                                                                beta2=0.999, eps=1e-8,
+                                                                weight_decay=0.01), **kw}))
+    assert _status(ad(step=None)) == T.Status.INVALID_ARG
+    assert _status(ad(beta1=1.0)) == T.Status.INVALID_ARG
+    assert _status(ad(n=-1)) == T.Status.INVALID_ARG
+    assert _status(ad(m=A16 + 1)) == T.Status.ALIGNMENT
+    assert _status(ad(n=0)) == T.Status.OK

@@ -156,3 +156,29 @@ def test_gpt_50_step_training_matches_oracle_and_one_shard():
     assert np.max(np.abs(runs[2] - ref) / ref) <= 2e-3, np.max(np.abs(runs[2] - ref) / ref)
     assert np.max(np.abs(runs[2] - runs[1])) <= 1e-4
     assert runs[2][-1] < 0.5 * runs[2][0]        # the loss falls (the page's convergence check)
+
+
+@pytest.mark.parametrize("mode", [T.Reduce.BUFFERS, T.Reduce.SPLITK])
+def test_gpt_training_step_replays_from_a_cuda_graph(mode):
+    """The training step captured once as a CUDA graph (the step count and the loss
+    history live in device memory, so no launch argument changes between steps) and
+    replayed: the 50-step loss trajectory and the final parameters equal the eager
+    run's bit for bit, and the trajectory tracks the fp64 oracle's."""
+    steps = 50
+    eager, p, ids, tg = _model(2, mode, steps=steps)
+    for _ in range(steps):
+        eager.step()
+    graphed, *_ = _model(2, mode, steps=steps)
+    graphed.step()                     # first step eagerly: kernel attributes, side streams
+    graphed.capture()
+    for _ in range(steps - 1):
+        graphed.replay()
+    torch.cuda.synchronize()
+    assert T.tp_check_status() == 0
+    assert int(graphed.step_dev.item()) == steps
+    assert torch.equal(graphed.losses, eager.losses)
+    assert torch.equal(graphed.p, eager.p)
+    cfg = dict(b=CFG["batch"], s=CFG["seq"], heads=CFG["heads"], N=2)
+    ref, _ = G.gpt_train(_oracle_params(p, CFG["layers"]), ids, tg, cfg, steps)
+    got = graphed.losses.cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(got - np.array(ref)) / np.array(ref)) <= 2e-3
