@@ -57,6 +57,8 @@ template <typename T>
 __global__ void gqa_pack_kernel(const T* __restrict__ Wq, const T* __restrict__ Wk,
                                 const T* __restrict__ Wv, T* __restrict__ Wsh, int64_t h, int H,
                                 int Hkv, int hq, int hkv, int r, int d, int64_t S, int64_t W) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   const int64_t n = h * W;
   for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < n;
        e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -81,6 +83,8 @@ __global__ void gqa_pack_kernel(const T* __restrict__ Wq, const T* __restrict__ 
 template <typename T>
 __global__ void gqa_replica_sum_kernel(T* __restrict__ dW, int64_t h, int Hkv, int hq, int r,
                                        int d, int64_t S, int64_t W) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   const int64_t per_row = static_cast<int64_t>(Hkv) * 2 * d;
   const int64_t n = h * per_row;
   for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < n;
@@ -135,6 +139,8 @@ __device__ __forceinline__ uint4 pack16(const float (&f)[16 / sizeof(T)]) {
 template <typename T>
 __global__ void gqa_replica_sum_vec_kernel(T* __restrict__ dW, int64_t h, int Hkv, int hq, int r,
                                            int d, int64_t S, int64_t W) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   constexpr int E = 16 / sizeof(T);
   const int dv = d / E;
   const int64_t per_row = static_cast<int64_t>(Hkv) * 2 * dv;
@@ -205,15 +211,15 @@ tp_status tp_gqa_pack_qkv(const void* Wq, const void* Wk, const void* Wv, void* 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const unsigned grid = grid_for(h * g.W);
   if (dtype == TP_BF16)
-    gqa_pack_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
+    TP_CUDA_TRY(launch_kernel(gqa_pack_kernel<__nv_bfloat16>, grid, 256, 0, st,
         static_cast<const __nv_bfloat16*>(Wq), static_cast<const __nv_bfloat16*>(Wk),
         static_cast<const __nv_bfloat16*>(Wv), static_cast<__nv_bfloat16*>(Wqkv), h, n_heads,
-        n_kv_heads, g.hq, g.hkv, g.r, static_cast<int>(g.d), g.S, g.W);
+        n_kv_heads, g.hq, g.hkv, g.r, static_cast<int>(g.d), g.S, g.W));
   else
-    gqa_pack_kernel<float><<<grid, 256, 0, st>>>(
+    TP_CUDA_TRY(launch_kernel(gqa_pack_kernel<float>, grid, 256, 0, st,
         static_cast<const float*>(Wq), static_cast<const float*>(Wk),
         static_cast<const float*>(Wv), static_cast<float*>(Wqkv), h, n_heads, n_kv_heads, g.hq,
-        g.hkv, g.r, static_cast<int>(g.d), g.S, g.W);
+        g.hkv, g.r, static_cast<int>(g.d), g.S, g.W));
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;
@@ -409,19 +415,19 @@ tp_status tp_gqa_attn_proj_bwd(const void* x, const float* gamma, const void* Wq
     const bool vec = g.d % E == 0 && g.S % E == 0 && g.W % E == 0;
     const unsigned grid = grid_for(h * n_kv_heads * 2 * g.d / (vec ? E : 1));
     if (dtype == TP_BF16 && vec)
-      gqa_replica_sum_vec_kernel<__nv_bfloat16><<<grid, 256, 0, br.stream()>>>(
+      TP_CUDA_TRY(launch_kernel(gqa_replica_sum_vec_kernel<__nv_bfloat16>, grid, 256, 0, br.stream(),
           static_cast<__nv_bfloat16*>(dWqkv), h, n_kv_heads, g.hq, g.r, static_cast<int>(g.d),
-          g.S, g.W);
+          g.S, g.W));
     else if (dtype == TP_BF16)
-      gqa_replica_sum_kernel<__nv_bfloat16><<<grid, 256, 0, br.stream()>>>(
+      TP_CUDA_TRY(launch_kernel(gqa_replica_sum_kernel<__nv_bfloat16>, grid, 256, 0, br.stream(),
           static_cast<__nv_bfloat16*>(dWqkv), h, n_kv_heads, g.hq, g.r, static_cast<int>(g.d),
-          g.S, g.W);
+          g.S, g.W));
     else if (vec)
-      gqa_replica_sum_vec_kernel<float><<<grid, 256, 0, br.stream()>>>(
-          static_cast<float*>(dWqkv), h, n_kv_heads, g.hq, g.r, static_cast<int>(g.d), g.S, g.W);
+      TP_CUDA_TRY(launch_kernel(gqa_replica_sum_vec_kernel<float>, grid, 256, 0, br.stream(),
+          static_cast<float*>(dWqkv), h, n_kv_heads, g.hq, g.r, static_cast<int>(g.d), g.S, g.W));
     else
-      gqa_replica_sum_kernel<float><<<grid, 256, 0, br.stream()>>>(
-          static_cast<float*>(dWqkv), h, n_kv_heads, g.hq, g.r, static_cast<int>(g.d), g.S, g.W);
+      TP_CUDA_TRY(launch_kernel(gqa_replica_sum_kernel<float>, grid, 256, 0, br.stream(),
+          static_cast<float*>(dWqkv), h, n_kv_heads, g.hq, g.r, static_cast<int>(g.d), g.S, g.W));
     count_launch();
     TP_CUDA_TRY(cudaGetLastError());
   }

@@ -119,6 +119,8 @@ template <typename T, int D>
 __global__ void __launch_bounds__(RB * LPR) attn_fwd_kernel(
     const T* __restrict__ qkv, T* __restrict__ o, float* __restrict__ lse, int s,
     const HeadMap hm, float scale, int causal) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   using Ln = Lanes<D>;
   constexpr int P = Ln::P, KS = Ln::KS;
   __shared__ __align__(16) float Ks[RB][P][DPAD];
@@ -215,6 +217,8 @@ __global__ void __launch_bounds__(RB * LPR) attn_bwd_dkdv_kernel(
     const T* __restrict__ qkv, const T* __restrict__ o, const float* __restrict__ lse,
     const T* __restrict__ dO, T* __restrict__ dqkv, int s, const HeadMap hm, float scale,
     int causal) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   using Ln = Lanes<D>;
   constexpr int P = Ln::P, KS = Ln::KS;
   __shared__ __align__(16) float Qs[RB][P][DPAD];
@@ -313,6 +317,8 @@ __global__ void __launch_bounds__(RB * LPR) attn_bwd_dq_kernel(
     const T* __restrict__ qkv, const T* __restrict__ o, const float* __restrict__ lse,
     const T* __restrict__ dO, T* __restrict__ dqkv, int s, const HeadMap hm, float scale,
     int causal) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   using Ln = Lanes<D>;
   constexpr int P = Ln::P, KS = Ln::KS;
   __shared__ __align__(16) float Ks[RB][P][DPAD];
@@ -385,8 +391,8 @@ template <typename T, int D>
 tp_status run_fwd(const void* qkv, void* o, float* lse, int b, int s, const HeadMap& hm,
                   int causal, cudaStream_t st) {
   const dim3 grid((s + RB - 1) / RB, hm.H, b);
-  attn_fwd_kernel<T, D><<<grid, RB * LPR, 0, st>>>(static_cast<const T*>(qkv), static_cast<T*>(o), lse,
-                                              s, hm, 1.0f / sqrtf(static_cast<float>(D)), causal);
+  TP_CUDA_TRY(launch_kernel(attn_fwd_kernel<T, D>, grid, RB * LPR, 0, st, static_cast<const T*>(qkv), static_cast<T*>(o), lse,
+                                              s, hm, 1.0f / sqrtf(static_cast<float>(D)), causal));
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;
@@ -396,12 +402,12 @@ template <typename T, int D>
 tp_status run_bwd(const void* qkv, const void* o, const float* lse, const void* dO, void* dqkv,
                   int b, int s, const HeadMap& hm, int kv_heads, int causal, cudaStream_t st) {
   const float scale = 1.0f / sqrtf(static_cast<float>(D));
-  attn_bwd_dkdv_kernel<T, D><<<dim3((s + RB - 1) / RB, kv_heads, b), RB * LPR, 0, st>>>(
-      static_cast<const T*>(qkv), static_cast<const T*>(o), lse, static_cast<const T*>(dO),
-      static_cast<T*>(dqkv), s, hm, scale, causal);
-  attn_bwd_dq_kernel<T, D><<<dim3((s + RB - 1) / RB, hm.H, b), RB * LPR, 0, st>>>(
-      static_cast<const T*>(qkv), static_cast<const T*>(o), lse, static_cast<const T*>(dO),
-      static_cast<T*>(dqkv), s, hm, scale, causal);
+  TP_CUDA_TRY(launch_kernel(attn_bwd_dkdv_kernel<T, D>, dim3((s + RB - 1) / RB, kv_heads, b),
+      RB * LPR, 0, st, static_cast<const T*>(qkv), static_cast<const T*>(o), lse, static_cast<const T*>(dO),
+      static_cast<T*>(dqkv), s, hm, scale, causal));
+  TP_CUDA_TRY(launch_kernel(attn_bwd_dq_kernel<T, D>, dim3((s + RB - 1) / RB, hm.H, b),
+      RB * LPR, 0, st, static_cast<const T*>(qkv), static_cast<const T*>(o), lse, static_cast<const T*>(dO),
+      static_cast<T*>(dqkv), s, hm, scale, causal));
   count_launch(2);
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;

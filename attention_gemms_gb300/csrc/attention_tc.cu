@@ -186,6 +186,8 @@ __global__ void __launch_bounds__(FwdLayout<NH>::kThreads, kCtasPerSm) attn_fwd_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  pdl_wait();  // the set-up above overlaps the previous kernel
+  pdl_trigger();
   auto tS = [&](int h) { return tmem + 64u * h; };
   auto tO = [&](int h) { return tmem + 64u * NH + 64u * h; };
   int issued_kv = 0;  // producer: K/V blocks issued
@@ -446,6 +448,8 @@ __global__ void __launch_bounds__(256) attn_bwd_dsum_kernel(const __nv_bfloat16*
                                                             const float* __restrict__ lse,
                                                             float2* __restrict__ ld, int64_t rows,
                                                             int s, int H, int64_t ldo) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   const int64_t gt = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t w = gt >> 3;
   const int sub = static_cast<int>(gt & 7);
@@ -550,6 +554,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dq_tc_kernel(const __
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  pdl_wait();  // the set-up above overlaps the previous kernel
+  pdl_trigger();
   const uint32_t tS = tmem, tdP = tmem + 64, tdQ = tmem + 128;
   int issued = 0;
 
@@ -782,6 +788,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dkdv_tc_kernel(const 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  pdl_wait();  // the set-up above overlaps the previous kernel
+  pdl_trigger();
   const uint32_t tST = tmem, tdPT = tmem + 64, tdV = tmem + 128, tdK = tmem + 192;
   auto head_of = [&](int w) { return blk * p.hq + kvl * p.g + w / nqb; };
   int issued = 0;
@@ -906,19 +914,23 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dkdv_tc_kernel(const 
       if (lane == 0) mbar_arrive(s_free);
       // P^T and P^T (dP^T - D) as packed bf16 pairs; 1 / sqrt(d) applied to dK at the end
       uint32_t pk[16], dk[16];
-      // one loop for full and masked items (two specialised loops exceed the register
-      // budget of two 320-thread CTAs per SM)
-      const bool full = valid && qh + 32 <= p.s && !(p.causal && kj > qh);
+      // bit c set: query qh + c sees this lane's key (it is in the sequence, the key row
+      // is, and, causal, the key does not come after it); one loop for full and masked
+      // items (two specialised loops exceed the register budget of two 320-thread CTAs
+      // per SM), so the test per entry is one bit of this word
+      const int hi = valid ? min(p.s - qh, 32) : 0;
+      const int lo = p.causal ? max(kj - qh, 0) : 0;
+      const uint32_t live_bits =
+          hi <= lo ? 0u : ((hi - lo == 32 ? 0xFFFFFFFFu : ((1u << (hi - lo)) - 1u)) << lo);
 #pragma unroll
       for (int i = 0; i < 32; i += 2) {
         const float4 l4 = tab4[i >> 1];  // (lse, D) of queries qh + i, qh + i + 1
         float pr[2], ds[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int q = qh + i + e;
-          const bool live = full || (valid && q < p.s && !(p.causal && kj > q));
           const float l2 = e ? l4.z : l4.x, dq = e ? l4.w : l4.y;
-          pr[e] = live ? ex2_approx(fmaf(__uint_as_float(sv[i + e]), p.scale_log2, -l2)) : 0.0f;
+          const float x = fmaf(__uint_as_float(sv[i + e]), p.scale_log2, -l2);
+          pr[e] = ex2_approx((live_bits & (1u << (i + e))) ? x : -INFINITY);  // 2^-inf = 0
           ds[e] = pr[e] * (__uint_as_float(pv[i + e]) - dq);
         }
         pk[i >> 1] = pack_bf16x2(pr[0], pr[1]);
@@ -1063,11 +1075,12 @@ tp_status launch_attention_fwd_tc(const void* qkv, void* o, float* lse, int64_t 
   const dim3 grid(static_cast<unsigned>((s + kQ - 1) / kQ), static_cast<unsigned>(heads / nh),
                   static_cast<unsigned>(b));
   if (nh == 2)
-    attn_fwd_tc_kernel<2><<<grid, FwdLayout<2>::kThreads, FwdLayout<2>::kSmem, st>>>(p);
+    TP_CUDA_TRY(launch_kernel(attn_fwd_tc_kernel<2>, grid, FwdLayout<2>::kThreads,
+                              FwdLayout<2>::kSmem, st, p));
   else
-    attn_fwd_tc_kernel<1><<<grid, FwdLayout<1>::kThreads, FwdLayout<1>::kSmem, st>>>(p);
+    TP_CUDA_TRY(launch_kernel(attn_fwd_tc_kernel<1>, grid, FwdLayout<1>::kThreads,
+                              FwdLayout<1>::kSmem, st, p));
   count_launch();
-  TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;
 }
 
@@ -1136,20 +1149,22 @@ tp_status launch_attention_bwd_tc(const void* qkv, const void* o, const float* l
     mark_device(attr_set);
   }
   const int64_t pairs = b * s * heads;
-  attn_bwd_dsum_kernel<<<static_cast<unsigned>((pairs * 8 + 255) / 256), 256, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse,
-      static_cast<float2*>(ldws), b * s, static_cast<int>(s), heads, ldo);
+  TP_CUDA_TRY(launch_kernel(attn_bwd_dsum_kernel, static_cast<unsigned>((pairs * 8 + 255) / 256),
+                            256, 0, st, static_cast<const __nv_bfloat16*>(o),
+                            static_cast<const __nv_bfloat16*>(dO), lse, static_cast<float2*>(ldws),
+                            b * s, static_cast<int>(s), heads, ldo));
   const unsigned tiles = static_cast<unsigned>((s + 127) / 128);
   // dQ and dK/dV are independent: dQ runs on a side stream beside dK/dV, whose grid
   // (one CTA per 128 key rows of a key/value head) often leaves CTA slots free
   SideBranch br(st, 1);
-  attn_bwd_dq_tc_kernel<<<dim3(tiles, static_cast<unsigned>(heads), static_cast<unsigned>(b)),
-                          kThreadsBwd, kBwdSmemDq, br.stream()>>>(p);
-  const cudaError_t e1 = cudaGetLastError();
-  attn_bwd_dkdv_tc_kernel<<<dim3(tiles, static_cast<unsigned>(kv_total), static_cast<unsigned>(b)),
-                            kThreadsBwd, kBwdSmemKv, st>>>(p);
+  const cudaError_t e1 = launch_kernel(
+      attn_bwd_dq_tc_kernel, dim3(tiles, static_cast<unsigned>(heads), static_cast<unsigned>(b)),
+      kThreadsBwd, kBwdSmemDq, br.stream(), p);
+  const cudaError_t e2 = launch_kernel(
+      attn_bwd_dkdv_tc_kernel,
+      dim3(tiles, static_cast<unsigned>(kv_total), static_cast<unsigned>(b)), kThreadsBwd,
+      kBwdSmemKv, st, p);
   count_launch(3);
-  const cudaError_t e2 = cudaGetLastError();
   TP_TRY(br.join());
   if (e1 != cudaSuccess) return cuda_fail(e1, "attn_bwd_dq_tc_kernel launch");
   TP_CUDA_TRY(e2);

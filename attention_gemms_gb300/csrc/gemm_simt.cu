@@ -75,6 +75,8 @@ __device__ __forceinline__ void epi1(const SimtParams& p, int g, int64_t r, int6
 
 template <int EPI, bool PAIRED>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(const SimtParams p) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   constexpr int NB = PAIRED ? 2 : 1;
   // A and B staging; reused for the partial tile of a split (unpaired only: TM x TN fits)
   constexpr int kFloats = TK * (TM + 4) + NB * TK * (TN + 4);
@@ -225,20 +227,21 @@ cudaError_t launch_k(const SimtParams& p, dim3 grid, cudaStream_t st) {
     // unsplit: one CTA per tile (also when the device cannot place the cluster)
     SimtParams q = p;
     q.split = 1;
-    gemm_simt_kernel<EPI, PAIRED><<<grid, 256, 0, st>>>(q);
-    return cudaGetLastError();
+    return launch_kernel(gemm_simt_kernel<EPI, PAIRED>, grid, 256, 0, st, q);
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(p.split);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_kernel
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(grid.x * static_cast<unsigned>(p.split), grid.y, grid.z);
   cfg.blockDim = dim3(256, 1, 1);
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, gemm_simt_kernel<EPI, PAIRED>, p);
 }
 

@@ -399,6 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  // the set-up above overlaps the previous kernel; operands and outputs are touched after
+  pdl_wait();
+  pdl_trigger();
 
   const int ntiles = p.tiles_m * p.tiles_n * p.groups;
   const int nkb = p.nseg * p.kb_per_seg;
@@ -714,6 +717,9 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_tc2_kernel(const __grid_
   cluster_sync_all();  // the peer's barriers are initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  // the set-up above overlaps the previous kernel; operands and outputs are touched after
+  pdl_wait();
+  pdl_trigger();
 
   const int pair = blockIdx.x >> 1;
   const int npairs = gridDim.x >> 1;
@@ -1048,9 +1054,8 @@ tp_status launch_bn_epi(const TcParams& prm, int grid, cudaStream_t st) {
                                      TcCfg<BN, DEC>::SMEM_BYTES));
     mark_device(attr_set);
   }
-  kern<<<grid, kThreads, TcCfg<BN, DEC>::SMEM_BYTES, st>>>(prm);
+  TP_CUDA_TRY(launch_kernel(kern, grid, kThreads, TcCfg<BN, DEC>::SMEM_BYTES, st, prm));
   count_launch();
-  TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;
 }
 
@@ -1075,16 +1080,18 @@ tp_status launch_pair_epi(const TcParams& prm, int64_t ntiles, cudaStream_t st) 
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = -1;
   int max_pairs = dev >= 0 ? max_pairs_dev[dev].load() : 0;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_kernel
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(kPairThreads, 1, 1);
   cfg.dynamicSmemBytes = kPairSmem;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;  // the occupancy query below takes the cluster shape only
   if (max_pairs == 0) {
     TP_CUDA_TRY(
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem));
@@ -1097,6 +1104,7 @@ tp_status launch_pair_epi(const TcParams& prm, int64_t ntiles, cudaStream_t st) 
   }
   const int pairs = static_cast<int>(std::min<int64_t>(ntiles, max_pairs));
   cfg.gridDim = dim3(2 * static_cast<unsigned>(pairs), 1, 1);
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
   TP_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, prm));
   count_launch();
   return TP_OK;

@@ -58,6 +58,8 @@ __device__ __forceinline__ void st_bf16(void* base, int64_t i, float v) {
 
 template <int T, int EPI, bool PAIRED>
 __global__ void __launch_bounds__(32 * kWarps) gemv_kernel(const GemvParams p) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   // rows in flight per thread: the paired (gate/up) kernel streams two weights
   constexpr int kUnroll = PAIRED ? 4 : 8;
   __shared__ float red[PAIRED ? 2 : 1][kWarps][T][kStrip];
@@ -164,9 +166,9 @@ __global__ void __launch_bounds__(32 * kWarps) gemv_kernel(const GemvParams p) {
 
 template <int T>
 tp_status launch_t(int epi, bool paired, const GemvParams& p, dim3 grid, cudaStream_t st) {
-  if (epi == EPI_SWIGLU && paired) gemv_kernel<T, EPI_SWIGLU, true><<<grid, 32 * kWarps, 0, st>>>(p);
-  else if (epi == EPI_GELU) gemv_kernel<T, EPI_GELU, false><<<grid, 32 * kWarps, 0, st>>>(p);
-  else if (epi == EPI_STORE) gemv_kernel<T, EPI_STORE, false><<<grid, 32 * kWarps, 0, st>>>(p);
+  if (epi == EPI_SWIGLU && paired) TP_CUDA_TRY(launch_kernel(gemv_kernel<T, EPI_SWIGLU, true>, grid, 32 * kWarps, 0, st, p));
+  else if (epi == EPI_GELU) TP_CUDA_TRY(launch_kernel(gemv_kernel<T, EPI_GELU, false>, grid, 32 * kWarps, 0, st, p));
+  else if (epi == EPI_STORE) TP_CUDA_TRY(launch_kernel(gemv_kernel<T, EPI_STORE, false>, grid, 32 * kWarps, 0, st, p));
   else return fail(TP_ERR_INVALID_ARG, "GEMV epilogue not supported");
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());

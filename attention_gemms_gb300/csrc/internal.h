@@ -10,6 +10,7 @@
 #include <cstdint>
 #include <initializer_list>
 #include <string>
+#include <utility>
 
 #include "../../include/tpmlp.h"
 
@@ -81,6 +82,42 @@ class SideBranch {
   void* side_ = nullptr;
   std::unique_lock<std::recursive_mutex> lock_;
 };
+
+// ------------------------------------------------------------------ launches
+//
+// Programmatic dependent launch: every kernel of the library is launched (launch_kernel)
+// so that its CTAs may start while the kernel before it on the stream is finishing. A
+// kernel calls pdl_wait() before its first access to global memory -- everything the
+// earlier kernels of the stream wrote is then complete and visible, and nothing they
+// still read is overwritten -- and pdl_trigger() right after, which lets the next
+// kernel's CTAs start their own set-up (barrier init, TMEM allocation, tensor-map
+// prefetch) in turn. The next kernel launches only once every CTA of this one has
+// passed its trigger, so a waiting CTA never holds resources an earlier kernel's CTA
+// still needs. Without the attribute (the environment variable TP_NO_PDL=1) the
+// instructions return at once and the stream serialises the kernels as usual.
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+#endif
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // ------------------------------------------------------------------ GEMM problem
 

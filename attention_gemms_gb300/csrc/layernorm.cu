@@ -45,6 +45,8 @@ __global__ void __launch_bounds__(32 * kRowWarps) ln_fwd_kernel(const T* __restr
                                                                 T* __restrict__ y, float* mean,
                                                                 float* rstd, int64_t M, int h,
                                                                 float eps) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= M) return;
@@ -71,6 +73,8 @@ __global__ void __launch_bounds__(32 * kRowWarps) ln_bwd_dx_kernel(
     const T* __restrict__ x, const float* __restrict__ gamma, const float* __restrict__ mean,
     const float* __restrict__ rstd, const T* __restrict__ dy, const T* __restrict__ dres,
     T* __restrict__ dx, int64_t M, int h) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= M) return;
@@ -149,6 +153,8 @@ template <typename T>
 __global__ void __launch_bounds__(32 * kRowWarps) ln_fwd_vec_kernel(
     const T* __restrict__ x, const float* __restrict__ gamma, const float* __restrict__ beta,
     T* __restrict__ y, float* mean, float* rstd, int64_t M, int h, float eps) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   using V = Vec<T>;
   constexpr int E = V::N;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
@@ -196,6 +202,8 @@ __global__ void __launch_bounds__(32 * kRowWarps) ln_bwd_dx_vec_kernel(
     const T* __restrict__ x, const float* __restrict__ gamma, const float* __restrict__ mean,
     const float* __restrict__ rstd, const T* __restrict__ dy, const T* __restrict__ dres,
     T* __restrict__ dx, int64_t M, int h) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   using V = Vec<T>;
   constexpr int E = V::N;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
@@ -256,6 +264,8 @@ __global__ void __launch_bounds__(32 * kRowWarps) ln_bwd_param_partial_vec_kerne
     const T* __restrict__ x, const float* __restrict__ mean, const float* __restrict__ rstd,
     const T* __restrict__ dy, float* __restrict__ partial, int64_t M, int h, int64_t rank_rows,
     int cpr) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   using V = Vec<T>;
   constexpr int E = V::N;
   __shared__ float red[kRowWarps][32][2 * E + 1];
@@ -309,6 +319,8 @@ __global__ void __launch_bounds__(kColThreads) ln_bwd_param_partial_kernel(
     const T* __restrict__ x, const float* __restrict__ mean, const float* __restrict__ rstd,
     const T* __restrict__ dy, float* __restrict__ partial, int64_t M, int h, int64_t rank_rows,
     int cpr) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   const int c = blockIdx.x * kColThreads + threadIdx.x;
   const int rank = blockIdx.y / cpr, chunk = blockIdx.y - rank * cpr;
   const int64_t rank_end = min(M, (rank + 1) * rank_rows);
@@ -334,6 +346,8 @@ constexpr int kFinalCols = 64, kFinalGroups = 4;  // columns per CTA, chunk grou
 __global__ void __launch_bounds__(kFinalCols * kFinalGroups) ln_bwd_param_final_kernel(
     const float* __restrict__ partial, int ranks, int cpr, int h, float* dgamma, float* dbeta,
     float* dgamma_ranks, float* dbeta_ranks) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   __shared__ float red[kFinalGroups][2][kFinalCols];
   const int cl = threadIdx.x % kFinalCols, q = threadIdx.x / kFinalCols;
   const int c = blockIdx.x * kFinalCols + cl;
@@ -383,11 +397,11 @@ tp_status fwd_t(const void* x, const float* gamma, const float* beta, void* y, f
                 float* rstd, int64_t M, int h, float eps, cudaStream_t st) {
   const unsigned blocks = static_cast<unsigned>((M + kRowWarps - 1) / kRowWarps);
   if (vec_rows<T>(h))
-    ln_fwd_vec_kernel<T><<<blocks, 32 * kRowWarps, 0, st>>>(
-        static_cast<const T*>(x), gamma, beta, static_cast<T*>(y), mean, rstd, M, h, eps);
+    TP_CUDA_TRY(launch_kernel(ln_fwd_vec_kernel<T>, blocks, 32 * kRowWarps, 0, st,
+        static_cast<const T*>(x), gamma, beta, static_cast<T*>(y), mean, rstd, M, h, eps));
   else
-    ln_fwd_kernel<T><<<blocks, 32 * kRowWarps, 0, st>>>(static_cast<const T*>(x), gamma, beta,
-                                                         static_cast<T*>(y), mean, rstd, M, h, eps);
+    TP_CUDA_TRY(launch_kernel(ln_fwd_kernel<T>, blocks, 32 * kRowWarps, 0, st, static_cast<const T*>(x), gamma, beta,
+                                                         static_cast<T*>(y), mean, rstd, M, h, eps));
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;
@@ -401,13 +415,13 @@ tp_status bwd_t(const void* x, const float* gamma, const float* mean, const floa
   const unsigned rblocks = static_cast<unsigned>((M + kRowWarps - 1) / kRowWarps);
   const bool vec = vec_rows<T>(h);
   if (vec)
-    ln_bwd_dx_vec_kernel<T><<<rblocks, 32 * kRowWarps, 0, st>>>(
+    TP_CUDA_TRY(launch_kernel(ln_bwd_dx_vec_kernel<T>, rblocks, 32 * kRowWarps, 0, st,
         static_cast<const T*>(x), gamma, mean, rstd, static_cast<const T*>(dy),
-        static_cast<const T*>(dres), static_cast<T*>(dx), M, h);
+        static_cast<const T*>(dres), static_cast<T*>(dx), M, h));
   else
-    ln_bwd_dx_kernel<T><<<rblocks, 32 * kRowWarps, 0, st>>>(
+    TP_CUDA_TRY(launch_kernel(ln_bwd_dx_kernel<T>, rblocks, 32 * kRowWarps, 0, st,
         static_cast<const T*>(x), gamma, mean, rstd, static_cast<const T*>(dy),
-        static_cast<const T*>(dres), static_cast<T*>(dx), M, h);
+        static_cast<const T*>(dres), static_cast<T*>(dx), M, h));
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
   if (!dgamma && !dbeta && !dgamma_ranks && !dbeta_ranks) return TP_OK;
@@ -416,15 +430,15 @@ tp_status bwd_t(const void* x, const float* gamma, const float* mean, const floa
   if (vec) {
     constexpr int cols = 32 * Vec<T>::N;  // columns per CTA
     const dim3 g1((h + cols - 1) / cols, ranks * cpr);
-    ln_bwd_param_partial_vec_kernel<T><<<g1, 32 * kRowWarps, 0, st>>>(
-        static_cast<const T*>(x), mean, rstd, static_cast<const T*>(dy), ws, M, h, rank_rows, cpr);
+    TP_CUDA_TRY(launch_kernel(ln_bwd_param_partial_vec_kernel<T>, g1, 32 * kRowWarps, 0, st,
+        static_cast<const T*>(x), mean, rstd, static_cast<const T*>(dy), ws, M, h, rank_rows, cpr));
   } else {
     const dim3 g1((h + kColThreads - 1) / kColThreads, ranks * cpr);
-    ln_bwd_param_partial_kernel<T><<<g1, kColThreads, 0, st>>>(
-        static_cast<const T*>(x), mean, rstd, static_cast<const T*>(dy), ws, M, h, rank_rows, cpr);
+    TP_CUDA_TRY(launch_kernel(ln_bwd_param_partial_kernel<T>, g1, kColThreads, 0, st,
+        static_cast<const T*>(x), mean, rstd, static_cast<const T*>(dy), ws, M, h, rank_rows, cpr));
   }
-  ln_bwd_param_final_kernel<<<(h + kFinalCols - 1) / kFinalCols, kFinalCols * kFinalGroups, 0, st>>>(
-      ws, ranks, cpr, h, dgamma, dbeta, dgamma_ranks, dbeta_ranks);
+  TP_CUDA_TRY(launch_kernel(ln_bwd_param_final_kernel, (h + kFinalCols - 1) / kFinalCols, kFinalCols * kFinalGroups, 0, st,
+      ws, ranks, cpr, h, dgamma, dbeta, dgamma_ranks, dbeta_ranks));
   count_launch(2);
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;

@@ -63,6 +63,8 @@ __global__ void __launch_bounds__(256) shard_reduce_vec8(const float* __restrict
                                                          const OutT* __restrict__ R,
                                                          OutT* __restrict__ O, int N,
                                                          int64_t items, int64_t E) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t it = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; it < items;
        it += stride) {
@@ -114,6 +116,8 @@ __global__ void __launch_bounds__(256) shard_reduce_scalar(const float* __restri
                                                            const OutT* __restrict__ R,
                                                            OutT* __restrict__ O, int N,
                                                            int64_t E) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < E;
        e += stride) {
@@ -134,11 +138,11 @@ tp_status run(const float* P, const void* R, void* O, int N, int64_t E, int bloc
   const int64_t blocks =
       std::min<int64_t>((work + 255) / 256, static_cast<int64_t>(blocks_per_sm) * device_sm_count());
   if (vec)
-    shard_reduce_vec8<OutT><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-        P, static_cast<const OutT*>(R), static_cast<OutT*>(O), N, work, E);
+    TP_CUDA_TRY(launch_kernel(shard_reduce_vec8<OutT>, static_cast<unsigned>(blocks), 256, 0, st,
+        P, static_cast<const OutT*>(R), static_cast<OutT*>(O), N, work, E));
   else
-    shard_reduce_scalar<OutT><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-        P, static_cast<const OutT*>(R), static_cast<OutT*>(O), N, E);
+    TP_CUDA_TRY(launch_kernel(shard_reduce_scalar<OutT>, static_cast<unsigned>(blocks), 256, 0, st,
+        P, static_cast<const OutT*>(R), static_cast<OutT*>(O), N, E));
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;
@@ -187,6 +191,8 @@ __global__ void __launch_bounds__(256, TP_RLN_MINB) shard_reduce_ln_kernel(
     const float* __restrict__ P, const T* __restrict__ R, const float* __restrict__ gamma,
     const float* __restrict__ beta, T* __restrict__ S, T* __restrict__ Y, float* __restrict__ mean,
     float* __restrict__ rstd, int N, int64_t M, int h, float eps, int wpr, int iters) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   extern __shared__ float4 rowbuf[];
   __shared__ float red[2][8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -278,9 +284,9 @@ tp_status run_ln(const float* P, const void* R, const float* gamma, const float*
   }
   const int64_t blocks = (M + rows - 1) / rows;
   if (blocks > 2147483647ll) return fail(TP_ERR_SHAPE, "too many rows for one launch");
-  shard_reduce_ln_kernel<T><<<static_cast<unsigned>(blocks), 256, smem, st>>>(
+  TP_CUDA_TRY(launch_kernel(shard_reduce_ln_kernel<T>, static_cast<unsigned>(blocks), 256, smem, st,
       P, static_cast<const T*>(R), gamma, beta, static_cast<T*>(S), static_cast<T*>(Y), mean,
-      rstd, N, M, h, eps, wpr, iters);
+      rstd, N, M, h, eps, wpr, iters));
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;

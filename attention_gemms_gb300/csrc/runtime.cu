@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstdlib>
 #include <mutex>
 #include <string>
 
@@ -134,6 +135,14 @@ uint64_t wait_timeout_ns() {
 }
 
 void count_launch(int n) { g_launches.fetch_add(static_cast<uint64_t>(n)); }
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("TP_NO_PDL");
+    return !(e && e[0] == '1');
+  }();
+  return on;
+}
 
 // The kernels are built for sm_103a only.
 tp_status check_device() {

@@ -78,6 +78,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) vocab_embed_fwd_kernel(
     const int32_t* __restrict__ ids, const T* __restrict__ E, T* __restrict__ x, int64_t M,
     int64_t v, int h, int N) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= M) return;
@@ -98,6 +100,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) vocab_embed_bwd_kernel(
     const int32_t* __restrict__ ids, const T* __restrict__ dx, T* __restrict__ dE, int64_t M,
     int h, int accumulate) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   __shared__ int32_t tile[kIdTile];
   const int64_t vrow = blockIdx.x;  // a vocabulary row lies in exactly one shard's block
   for (int c0 = 0; c0 < h; c0 += kThreads) {
@@ -122,6 +126,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) vocab_ce_fwd_kernel(
     const T* __restrict__ logits, const int32_t* __restrict__ targets, float* __restrict__ lse,
     float* __restrict__ row_loss, int64_t v, int N) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   __shared__ float red[kThreads / 32];
   const int64_t row = blockIdx.x;
   const T* L = logits + row * v;
@@ -228,6 +234,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) vocab_ce_fwd_vec_kernel(
     const T* __restrict__ logits, const int32_t* __restrict__ targets, float* __restrict__ lse,
     float* __restrict__ row_loss, int64_t M, int64_t v, int N) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= M) return;
@@ -286,6 +294,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) vocab_ce_bwd_vec_kernel(
     const T* logits, const int32_t* __restrict__ targets, const float* __restrict__ lse,
     T* dlogits, int64_t v, float scale) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   const int64_t row = blockIdx.x;
   const float l2 = lse[row] * kLog2e;
   const int64_t t = targets[row];
@@ -310,6 +320,8 @@ __global__ void __launch_bounds__(kThreads) vocab_ce_bwd_vec_kernel(
 __global__ void __launch_bounds__(1024) vocab_ce_loss_kernel(
     const float* __restrict__ row_loss, const int32_t* __restrict__ targets,
     float* __restrict__ shard_loss, float* __restrict__ loss, int64_t M, int64_t v, int N) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   __shared__ float red[32];
   const int64_t vs = v / N;
   float total = 0.0f;
@@ -337,6 +349,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) vocab_ce_bwd_kernel(
     const T* logits, const int32_t* __restrict__ targets, const float* __restrict__ lse,
     T* dlogits, int64_t v, float scale) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   const int64_t row = blockIdx.x;
   const float l = lse[row];
   const int64_t t = targets[row];
@@ -353,6 +367,8 @@ __global__ void __launch_bounds__(kThreads) adamw_kernel(
     float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
     float* __restrict__ v, int64_t n, float lr, float b1, float b2, float eps, float wd,
     float bc1, float bc2) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += stride) {
@@ -373,6 +389,8 @@ __global__ void __launch_bounds__(kThreads) adamw_dev_kernel(
     float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
     float* __restrict__ v, int64_t n, const int32_t* __restrict__ step, float lr, float b1,
     float b2, float eps, float wd) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   __shared__ float bc[2];
   if (threadIdx.x == 0) {
     const double t = static_cast<double>(*step);
@@ -398,6 +416,8 @@ __global__ void __launch_bounds__(kThreads) adamw_dev_kernel(
 // one, and the step's loss goes to its slot of the loss history.
 __global__ void step_advance_kernel(int32_t* step, const float* loss, float* hist,
                                     int64_t hist_len) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
   const int32_t t = *step + 1;
   *step = t;
   if (loss && hist) hist[static_cast<int64_t>(t - 1) % hist_len] = *loss;
@@ -407,8 +427,8 @@ template <typename T>
 tp_status embed_fwd_t(const int32_t* ids, const void* E, void* x, int64_t M, int64_t v, int h,
                       int N, cudaStream_t st) {
   const int64_t blocks = (M + kThreads / 32 - 1) / (kThreads / 32);
-  vocab_embed_fwd_kernel<T><<<static_cast<unsigned>(blocks), kThreads, 0, st>>>(
-      ids, static_cast<const T*>(E), static_cast<T*>(x), M, v, h, N);
+  TP_CUDA_TRY(launch_kernel(vocab_embed_fwd_kernel<T>, static_cast<unsigned>(blocks), kThreads, 0, st,
+      ids, static_cast<const T*>(E), static_cast<T*>(x), M, v, h, N));
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;
@@ -431,12 +451,12 @@ tp_status launch_vocab_embed_bwd(const int32_t* ids, const void* dx, void* dE, i
   if (v > 2147483647ll || h > (1 << 30)) return fail(TP_ERR_SHAPE, "embedding too large");
   const int hh = static_cast<int>(h);
   if (dt == TP_BF16)
-    vocab_embed_bwd_kernel<__nv_bfloat16><<<static_cast<unsigned>(v), kThreads, 0, st>>>(
+    TP_CUDA_TRY(launch_kernel(vocab_embed_bwd_kernel<__nv_bfloat16>, static_cast<unsigned>(v), kThreads, 0, st,
         ids, static_cast<const __nv_bfloat16*>(dx), static_cast<__nv_bfloat16*>(dE), M, hh,
-        accumulate ? 1 : 0);
+        accumulate ? 1 : 0));
   else
-    vocab_embed_bwd_kernel<float><<<static_cast<unsigned>(v), kThreads, 0, st>>>(
-        ids, static_cast<const float*>(dx), static_cast<float*>(dE), M, hh, accumulate ? 1 : 0);
+    TP_CUDA_TRY(launch_kernel(vocab_embed_bwd_kernel<float>, static_cast<unsigned>(v), kThreads, 0, st,
+        ids, static_cast<const float*>(dx), static_cast<float*>(dE), M, hh, accumulate ? 1 : 0));
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;
@@ -453,14 +473,14 @@ tp_status launch_vocab_ce_fwd(const void* logits, const int32_t* targets, float*
   const unsigned gw = static_cast<unsigned>((M + kThreads / 32 - 1) / (kThreads / 32));
   if (dt == TP_BF16) {
     const auto* L = static_cast<const __nv_bfloat16*>(logits);
-    if (vec) vocab_ce_fwd_vec_kernel<__nv_bfloat16><<<gw, kThreads, 0, st>>>(L, targets, lse, row_loss, M, v, N);
-    else vocab_ce_fwd_kernel<__nv_bfloat16><<<g, kThreads, 0, st>>>(L, targets, lse, row_loss, v, N);
+    if (vec) TP_CUDA_TRY(launch_kernel(vocab_ce_fwd_vec_kernel<__nv_bfloat16>, gw, kThreads, 0, st, L, targets, lse, row_loss, M, v, N));
+    else TP_CUDA_TRY(launch_kernel(vocab_ce_fwd_kernel<__nv_bfloat16>, g, kThreads, 0, st, L, targets, lse, row_loss, v, N));
   } else {
     const auto* L = static_cast<const float*>(logits);
-    if (vec) vocab_ce_fwd_vec_kernel<float><<<gw, kThreads, 0, st>>>(L, targets, lse, row_loss, M, v, N);
-    else vocab_ce_fwd_kernel<float><<<g, kThreads, 0, st>>>(L, targets, lse, row_loss, v, N);
+    if (vec) TP_CUDA_TRY(launch_kernel(vocab_ce_fwd_vec_kernel<float>, gw, kThreads, 0, st, L, targets, lse, row_loss, M, v, N));
+    else TP_CUDA_TRY(launch_kernel(vocab_ce_fwd_kernel<float>, g, kThreads, 0, st, L, targets, lse, row_loss, v, N));
   }
-  vocab_ce_loss_kernel<<<1, 1024, 0, st>>>(row_loss, targets, shard_loss, loss, M, v, N);
+  TP_CUDA_TRY(launch_kernel(vocab_ce_loss_kernel, 1, 1024, 0, st, row_loss, targets, shard_loss, loss, M, v, N));
   count_launch(2);
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;
@@ -477,13 +497,13 @@ tp_status launch_vocab_ce_bwd(const void* logits, const int32_t* targets, const 
   if (dt == TP_BF16) {
     const auto* L = static_cast<const __nv_bfloat16*>(logits);
     auto* D = static_cast<__nv_bfloat16*>(dlogits);
-    if (vec) vocab_ce_bwd_vec_kernel<__nv_bfloat16><<<g, kThreads, 0, st>>>(L, targets, lse, D, v, scale);
-    else vocab_ce_bwd_kernel<__nv_bfloat16><<<g, kThreads, 0, st>>>(L, targets, lse, D, v, scale);
+    if (vec) TP_CUDA_TRY(launch_kernel(vocab_ce_bwd_vec_kernel<__nv_bfloat16>, g, kThreads, 0, st, L, targets, lse, D, v, scale));
+    else TP_CUDA_TRY(launch_kernel(vocab_ce_bwd_kernel<__nv_bfloat16>, g, kThreads, 0, st, L, targets, lse, D, v, scale));
   } else {
     const auto* L = static_cast<const float*>(logits);
     auto* D = static_cast<float*>(dlogits);
-    if (vec) vocab_ce_bwd_vec_kernel<float><<<g, kThreads, 0, st>>>(L, targets, lse, D, v, scale);
-    else vocab_ce_bwd_kernel<float><<<g, kThreads, 0, st>>>(L, targets, lse, D, v, scale);
+    if (vec) TP_CUDA_TRY(launch_kernel(vocab_ce_bwd_vec_kernel<float>, g, kThreads, 0, st, L, targets, lse, D, v, scale));
+    else TP_CUDA_TRY(launch_kernel(vocab_ce_bwd_kernel<float>, g, kThreads, 0, st, L, targets, lse, D, v, scale));
   }
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
@@ -495,8 +515,8 @@ tp_status launch_adamw(float* p, const float* g, float* m, float* v, int64_t n, 
                        cudaStream_t st) {
   if (n <= 0) return TP_OK;
   const int64_t blocks = std::min<int64_t>((n + kThreads - 1) / kThreads, 8ll * device_sm_count());
-  adamw_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, st>>>(p, g, m, v, n, lr, b1, b2,
-                                                                    eps, wd, bc1, bc2);
+  TP_CUDA_TRY(launch_kernel(adamw_kernel, static_cast<unsigned>(blocks), kThreads, 0, st, p, g, m, v, n, lr, b1, b2,
+                                                                    eps, wd, bc1, bc2));
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;
@@ -507,8 +527,8 @@ tp_status launch_adamw_dev(float* p, const float* g, float* m, float* v, int64_t
                            cudaStream_t st) {
   if (n <= 0) return TP_OK;
   const int64_t blocks = std::min<int64_t>((n + kThreads - 1) / kThreads, 8ll * device_sm_count());
-  adamw_dev_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, st>>>(p, g, m, v, n, step, lr,
-                                                                        b1, b2, eps, wd);
+  TP_CUDA_TRY(launch_kernel(adamw_dev_kernel, static_cast<unsigned>(blocks), kThreads, 0, st, p, g, m, v, n, step, lr,
+                                                                        b1, b2, eps, wd));
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;
@@ -516,7 +536,7 @@ tp_status launch_adamw_dev(float* p, const float* g, float* m, float* v, int64_t
 
 tp_status launch_step_advance(int32_t* step, const float* loss, float* hist, int64_t hist_len,
                               cudaStream_t st) {
-  step_advance_kernel<<<1, 1, 0, st>>>(step, loss, hist, hist_len);
+  TP_CUDA_TRY(launch_kernel(step_advance_kernel, 1, 1, 0, st, step, loss, hist, hist_len));
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;
