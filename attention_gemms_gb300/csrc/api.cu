@@ -153,6 +153,31 @@ tp_status row_impl(const void* Xs, const void* W, const void* residual, void* ou
   d.out[0] = ws;
   d.out_f32 = true;
   d.out_group_stride = M * n;
+  // Many rows: two row blocks, each a GEMM writing its rows of every shard's partial and
+  // a shard sum of those rows; the first block's sum (HBM-bound) runs on a side stream
+  // beside the second block's GEMM (tensor-bound), so only the second sum is exposed.
+  const int64_t half = M >= 2048 ? (M / 2 + 255) / 256 * 256 : 0;  // whole 256-row tiles
+  if (half > 0 && half < M) {
+    const size_t elt = elem_size(dt);
+    float* P = static_cast<float*>(ws);
+    GemmDesc d0 = d;
+    d0.M = half;
+    TP_TRY(launch_gemm(d0, st));
+    SideBranch first(st);
+    const bool beside = first.stream() != st;
+    TP_TRY(launch_shard_reduce(P, residual, out, N, half, n, dt, first.stream(), beside ? 2 : 8,
+                               M * n));
+    GemmDesc d1 = d;
+    d1.M = M - half;
+    d1.A[0] = {static_cast<const char*>(Xs) + half * k * elt, M - half, k, k};
+    d1.out[0] = P + half * n;
+    TP_TRY(launch_gemm(d1, st));
+    TP_TRY(launch_shard_reduce(P + half * n,
+                               residual ? static_cast<const char*>(residual) + half * n * elt : nullptr,
+                               static_cast<char*>(out) + half * n * elt, N, M - half, n, dt, st, 8,
+                               M * n));
+    return first.join();
+  }
   TP_TRY(launch_gemm(d, st));
   return launch_shard_reduce(static_cast<const float*>(ws), residual, out, N, M, n, dt, st);
 }

@@ -280,11 +280,12 @@ tp_status launch_gemm_simt(const GemmDesc& d, cudaStream_t st) {
   dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(d.groups));
   const bool pr = d.paired;
   // split K over a cluster while the tiles (times the split) stay within half the SMs
-  // and every CTA keeps at least two K steps
+  // and every CTA keeps at least one K step: at these sizes a K step is a global-load
+  // latency, so fewer steps per CTA is a shorter launch
   const int64_t tiles = gx * gy * d.groups, ksteps = (d.K + TK - 1) / TK * d.nseg;
   p.split = 1;
   while (!pr && p.split < 8 && tiles * p.split * 4 <= device_sm_count() &&
-         ksteps >= 4 * p.split)
+         ksteps >= 2 * p.split)
     p.split *= 2;
   cudaError_t e = cudaSuccess;
   switch (d.epi) {

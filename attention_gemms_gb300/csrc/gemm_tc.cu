@@ -1146,10 +1146,21 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
   // (decode: M <= 64 tokens, one M-tile) that 128-wide tiles are needed to give
   // every SM its share of the weight stream
   const int64_t n_tmem = d.paired ? 2 * d.N : d.N;
-  const int BN = (n_tmem >= 256 && d.M > 64) ? 256 : 128;
-  const int bn_logical = d.paired ? BN / 2 : BN;
+  int BN = (n_tmem >= 256 && d.M > 64) ? 256 : 128;
   // 256 x 256 tiles on CTA pairs once there are at least 256 rows
-  const bool pair = BN == 256 && d.M >= 256 && g_pair_mode.load() != 0;
+  bool pair = BN == 256 && d.M >= 256 && g_pair_mode.load() != 0;
+  // small problems (a handful of tiles, e.g. M = 1024 tokens at h = 128): narrower
+  // one-CTA tiles, down to 128 x 64, while that leaves at most half the SMs busy, so
+  // more SMs share the operand loads and the epilogue (unpaired, not the decode form)
+  if (!d.paired && d.M > 64) {
+    const int64_t sms = device_sm_count();
+    auto ctas = [&](int64_t tm, int64_t bn) {
+      return (d.M + tm - 1) / tm * ((d.N + bn - 1) / bn) * d.groups;
+    };
+    if (pair && 2 * ctas(256, 256) * 2 <= sms) pair = false;
+    while (!pair && BN > 64 && 2 * ctas(BM, BN) <= sms) BN /= 2;
+  }
+  const int bn_logical = d.paired ? BN / 2 : BN;
   const int tile_m = pair ? 256 : BM;
   // decode configuration: at most 64 K-major rows of A
   const bool dec = !pair && BN == 128 && !d.a_mn && d.M <= 64;
@@ -1226,6 +1237,7 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
   const int grid = static_cast<int>(
       std::min<int64_t>(ntiles, static_cast<int64_t>(device_sm_count()) * (dec ? TP_DEC_CTAS_PER_SM : 1)));
   if (dec) return launch_bn<128, true>(epi, prm, grid, st);
+  if (BN == 64) return launch_bn<64, false>(epi, prm, grid, st);
   return BN == 256 ? launch_bn<256, false>(epi, prm, grid, st)
                    : launch_bn<128, false>(epi, prm, grid, st);
 }

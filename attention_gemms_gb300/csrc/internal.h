@@ -171,10 +171,12 @@ bool gemv_eligible(const GemmDesc& d);                             // bf16, M <=
 tp_status launch_gemv(const GemmDesc& d, cudaStream_t st);
 tp_status launch_gemm_simt(const GemmDesc& d, cudaStream_t st);  // fp32, CUDA cores
 // blocks_per_sm: CTAs of 256 threads per SM of the grid-stride grid (8 saturates HBM
-// alone; 2 leaves room on every SM for a persistent GEMM CTA running beside it)
+// alone; 2 leaves room on every SM for a persistent GEMM CTA running beside it).
+// group_stride: elements from one shard's partial to the next (0: M * n), so that a
+// block of rows of larger partial buffers can be summed on its own
 tp_status launch_shard_reduce(const float* P, const void* residual, void* out, int N,
                               int64_t M, int64_t n, tp_dtype out_dtype, cudaStream_t st,
-                              int blocks_per_sm = 8);
+                              int blocks_per_sm = 8, int64_t group_stride = 0);
 // sum + residual, rounded to dt, then LayerNorm of the rounded row: h % 8 == 0,
 // h <= kReduceLnMaxH, 16-byte aligned buffers
 constexpr int64_t kReduceLnMaxH = 16384;

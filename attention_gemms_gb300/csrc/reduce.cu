@@ -115,23 +115,24 @@ template <typename OutT>
 __global__ void __launch_bounds__(256) shard_reduce_scalar(const float* __restrict__ P,
                                                            const OutT* __restrict__ R,
                                                            OutT* __restrict__ O, int N,
-                                                           int64_t E) {
+                                                           int64_t E, int64_t gs) {
   pdl_wait();  // the previous kernel's results are complete and visible
   pdl_trigger();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < E;
        e += stride) {
     float s = P[e];
-    for (int i = 1; i < N; ++i) s += P[i * E + e];
+    for (int i = 1; i < N; ++i) s += P[i * gs + e];
     if (R) s += to_f(R[e]);
     from_f(O[e], s);
   }
 }
 
+// E elements of each partial (shard i's at P + i gs) summed into O
 template <typename OutT>
-tp_status run(const float* P, const void* R, void* O, int N, int64_t E, int blocks_per_sm,
-              cudaStream_t st) {
-  const bool vec = (E % 8 == 0) && (reinterpret_cast<uintptr_t>(P) % 16 == 0) &&
+tp_status run(const float* P, const void* R, void* O, int N, int64_t E, int64_t gs,
+              int blocks_per_sm, cudaStream_t st) {
+  const bool vec = (E % 8 == 0) && (gs % 8 == 0) && (reinterpret_cast<uintptr_t>(P) % 16 == 0) &&
                    (reinterpret_cast<uintptr_t>(O) % 16 == 0) &&
                    (R == nullptr || reinterpret_cast<uintptr_t>(R) % 16 == 0);
   const int64_t work = vec ? E / 8 : E;
@@ -139,10 +140,10 @@ tp_status run(const float* P, const void* R, void* O, int N, int64_t E, int bloc
       std::min<int64_t>((work + 255) / 256, static_cast<int64_t>(blocks_per_sm) * device_sm_count());
   if (vec)
     TP_CUDA_TRY(launch_kernel(shard_reduce_vec8<OutT>, static_cast<unsigned>(blocks), 256, 0, st,
-        P, static_cast<const OutT*>(R), static_cast<OutT*>(O), N, work, E));
+        P, static_cast<const OutT*>(R), static_cast<OutT*>(O), N, work, gs));
   else
     TP_CUDA_TRY(launch_kernel(shard_reduce_scalar<OutT>, static_cast<unsigned>(blocks), 256, 0, st,
-        P, static_cast<const OutT*>(R), static_cast<OutT*>(O), N, E));
+        P, static_cast<const OutT*>(R), static_cast<OutT*>(O), N, E, gs));
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
   return TP_OK;
@@ -295,12 +296,14 @@ tp_status run_ln(const float* P, const void* R, const float* gamma, const float*
 }  // namespace
 
 tp_status launch_shard_reduce(const float* P, const void* residual, void* out, int N, int64_t M,
-                              int64_t n, tp_dtype out_dtype, cudaStream_t st, int blocks_per_sm) {
+                              int64_t n, tp_dtype out_dtype, cudaStream_t st, int blocks_per_sm,
+                              int64_t group_stride) {
   const int64_t E = M * n;
   if (E <= 0) return TP_OK;
+  const int64_t gs = group_stride > 0 ? group_stride : E;
   blocks_per_sm = std::max(1, std::min(blocks_per_sm, 8));
-  return out_dtype == TP_BF16 ? run<__nv_bfloat16>(P, residual, out, N, E, blocks_per_sm, st)
-                              : run<float>(P, residual, out, N, E, blocks_per_sm, st);
+  return out_dtype == TP_BF16 ? run<__nv_bfloat16>(P, residual, out, N, E, gs, blocks_per_sm, st)
+                              : run<float>(P, residual, out, N, E, gs, blocks_per_sm, st);
 }
 
 tp_status launch_shard_reduce_ln(const float* P, const void* residual, const float* gamma,

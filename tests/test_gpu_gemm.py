@@ -35,7 +35,10 @@ def _run(M, N, K, at, bt, dtype="bf16", seed=600):
 @pytest.mark.parametrize("at", [False, True])
 @pytest.mark.parametrize("bt", [False, True])
 @pytest.mark.parametrize("MNK", [(128, 128, 64), (128, 256, 64), (256, 512, 192), (200, 264, 136),
-                                 (1, 64, 64), (77, 1000, 520)])
+                                 (1, 64, 64), (77, 1000, 520),
+                                 # few tiles at M >= 256: one-CTA 128 x 64 tiles instead of
+                                 # 256 x 256 pairs (the page-2 layer's QKV and MLP shapes)
+                                 (1024, 384, 128), (1024, 512, 128), (1000, 136, 520)])
 def test_gemm_bf16(at, bt, MNK):
     M, N, K = MNK
     if at and M % 8:

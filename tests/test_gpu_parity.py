@@ -96,6 +96,29 @@ def test_row_linear(mode, N, with_res):
     assert guard_intact(full, M)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_row_linear_buffers_in_two_row_blocks(dtype):
+    """From 2048 rows on, variant A runs the row GEMM as two row blocks (whole 256-row
+    tiles, then the ragged rest) and sums the first block's partials beside the second
+    block's GEMM: every row of the sum, residual included, against the oracle."""
+    M, k, n, N = 2100, 256, 192, 4
+    dt = BF if dtype == "bf16" else T.DType.F32
+    tdt = bf16 if dtype == "bf16" else torch.float32
+    Xo, X = tensor((M, k), 311, dtype=dtype)
+    Wo, W = tensor((k, n), 312, 0.05, dtype=dtype)
+    Ro, R = tensor((M, n), 313, dtype=dtype)
+    out, full = guarded((M, n), tdt)
+    ws = _ws(T.tp_workspace_size(T.Op.ROW_LINEAR, M, k, n, N, dt, T.Act.NONE, T.Reduce.BUFFERS))
+    T.tp_row_linear(X, W, R, out, M, k, n, N, dt, T.Reduce.BUFFERS, ws, ws.numel())
+    torch.cuda.synchronize()
+    assert T.tp_check_status() == 0
+    ref = O.row_linear(Xo, Wo, N, Ro)
+    tol = BF16_TOL if dtype == "bf16" else F32_TOL
+    assert rel(host(out), ref) <= tol
+    assert rel(host(out)[1280:], ref[1280:]) <= tol    # the second block on its own
+    assert guard_intact(full, M)
+
+
 # ---------------------------------------------------------------- MLP forward + backward
 
 def _mlp_run(act, mode, N, M, h, f, dtype="bf16", seed0=400, sigma=0.05):
