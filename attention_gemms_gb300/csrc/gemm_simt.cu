@@ -42,11 +42,6 @@ struct SimtParams {
   int split;  // CTAs of a cluster sharing one output tile's K steps (1: no split)
 };
 
-__device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
-  return v;
-}
 
 template <int EPI>
 __device__ __forceinline__ void epi1(const SimtParams& p, int g, int64_t r, int64_t c, float a,

@@ -17,6 +17,7 @@
 #include <algorithm>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace tp {
 namespace {
@@ -310,6 +311,78 @@ __global__ void __launch_bounds__(32 * kRowWarps) ln_bwd_param_partial_vec_kerne
   }
 }
 
+// The partials and their final sum in one launch, for the replicated LN (one rank) with
+// at most kClusterChunks chunks of at most kRowsPerChunk rows (larger inputs keep the
+// partial and final kernels, whose grid has more CTAs): the CTAs of a cluster (1 x chunks) take the chunks of
+// one block of 32 column vectors, each keeps its chunk's sums in shared memory, and
+// after a cluster barrier CTA c adds up its share of the block's 2E x 32 outputs over
+// the cluster's CTAs in chunk order (distributed shared memory) and writes dgamma and
+// dbeta. A fixed order, so deterministic; no workspace and no second launch.
+constexpr int kClusterChunks = 8;
+
+template <typename T>
+__global__ void __launch_bounds__(32 * kRowWarps) ln_bwd_param_cluster_vec_kernel(
+    const T* __restrict__ x, const float* __restrict__ mean, const float* __restrict__ rstd,
+    const T* __restrict__ dy, float* __restrict__ dgamma, float* __restrict__ dbeta, int64_t M,
+    int h, int64_t rows_per_chunk) {
+  pdl_wait();  // the previous kernel's results are complete and visible
+  pdl_trigger();
+  using V = Vec<T>;
+  constexpr int E = V::N;
+  __shared__ float red[kRowWarps][32][2 * E + 1];
+  __shared__ float tot[2 * E][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int v = blockIdx.x * 32 + lane, nv = h / E;
+  const int chunk = static_cast<int>(cluster_ctarank()), chunks = gridDim.y;
+  const int64_t r0 = static_cast<int64_t>(chunk) * rows_per_chunk;
+  const int64_t r1 = min(M, r0 + rows_per_chunk);
+  float sg[E], sb[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) sg[e] = sb[e] = 0.0f;
+  if (v < nv) {
+#pragma unroll 8
+    for (int64_t r = r0 + warp; r < r1; r += kRowWarps) {
+      float a[E], d[E];
+      V::unpack(reinterpret_cast<const typename V::Raw*>(x + r * h)[v], a);
+      V::unpack(reinterpret_cast<const typename V::Raw*>(dy + r * h)[v], d);
+      const float mu = mean[r], rs = rstd[r];
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        sg[e] += d[e] * (a[e] - mu) * rs;
+        sb[e] += d[e];
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    red[warp][lane][e] = sg[e];
+    red[warp][lane][E + e] = sb[e];
+  }
+  __syncthreads();
+  for (int k = warp; k < 2 * E; k += kRowWarps) {  // the chunk's sums, warps in order
+    float t = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kRowWarps; ++w) t += red[w][lane][k];
+    tot[k][lane] = t;
+  }
+  cluster_sync_all();  // every chunk's sums are in its CTA's shared memory
+  const int per = (2 * E * 32 + chunks - 1) / chunks;
+  for (int o = chunk * per + static_cast<int>(threadIdx.x); o < min(2 * E * 32, (chunk + 1) * per);
+       o += blockDim.x) {
+    const int k = o / 32, j = o % 32;
+    const uint32_t addr = smem_u32(&tot[k][j]);
+    float t = 0.0f;
+    for (int q = 0; q < chunks; ++q) t += ld_cluster_f32(mapa_shared(addr, static_cast<uint32_t>(q)));
+    const int vv = blockIdx.x * 32 + j;
+    if (vv < nv) {
+      const int e = k < E ? k : k - E;
+      float* dst = k < E ? dgamma : dbeta;
+      if (dst) dst[static_cast<int64_t>(vv) * E + e] = t;
+    }
+  }
+  cluster_sync_all();  // no CTA leaves while another still reads its sums
+}
+
 // partial[chunk][0:h] = sum over the chunk's rows of dy * xhat, partial[chunk][h:2h] = of dy.
 // Rows are grouped by rank (rank r owns rows [r * rank_rows, (r + 1) * rank_rows), one
 // rank when the LN input is replicated) and each rank's rows are cut into cpr chunks
@@ -425,6 +498,30 @@ tp_status bwd_t(const void* x, const float* gamma, const float* mean, const floa
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
   if (!dgamma && !dbeta && !dgamma_ranks && !dbeta_ranks) return TP_OK;
+  if (vec && ranks == 1 && !dgamma_ranks && !dbeta_ranks && M <= kClusterChunks * kRowsPerChunk) {
+    const int chunks = static_cast<int>(
+        std::min<int64_t>(kClusterChunks, (M + kRowsPerChunk - 1) / kRowsPerChunk));
+    const int64_t rows_per_chunk = (M + chunks - 1) / chunks;
+    constexpr int cols = 32 * Vec<T>::N;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = static_cast<unsigned>(chunks);
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_kernel
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>((h + cols - 1) / cols), static_cast<unsigned>(chunks), 1);
+    cfg.blockDim = dim3(32 * kRowWarps, 1, 1);
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
+    TP_CUDA_TRY(cudaLaunchKernelEx(&cfg, ln_bwd_param_cluster_vec_kernel<T>,
+                                   static_cast<const T*>(x), mean, rstd, static_cast<const T*>(dy),
+                                   dgamma, dbeta, M, h, rows_per_chunk));
+    count_launch();
+    return TP_OK;
+  }
   const int64_t rank_rows = M / ranks;
   const int cpr = static_cast<int>((rank_rows + kRowsPerChunk - 1) / kRowsPerChunk);
   if (vec) {

@@ -663,8 +663,9 @@ TP_API tp_status tp_train_step_advance(int32_t* step, const float* loss, float* 
 
 /* tp_adamw_step with the step count read from device memory (*step >= 1, the counter that
  * tp_train_step_advance keeps) instead of a host argument; the same arithmetic, with the
- * bias corrections 1 - beta^step formed in double precision on the device. p, g, m, v and
- * step must be 4-byte aligned. */
+ * bias corrections 1 - beta^step formed in fp32 on the device (the host entry point forms
+ * them in double: results may differ in the last bits). p, g, m, v and step must be 4-byte
+ * aligned. */
 TP_API tp_status tp_adamw_step_device(float* p, const float* g, float* m, float* v, int64_t n,
                                       const int32_t* step, float lr, float beta1, float beta2,
                                       float eps, float weight_decay, void* stream);
