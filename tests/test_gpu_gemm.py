@@ -38,7 +38,10 @@ def _run(M, N, K, at, bt, dtype="bf16", seed=600):
                                  (1, 64, 64), (77, 1000, 520),
                                  # few tiles at M >= 256: one-CTA 128 x 64 tiles instead of
                                  # 256 x 256 pairs (the page-2 layer's QKV and MLP shapes)
-                                 (1024, 384, 128), (1024, 512, 128), (1000, 136, 520)])
+                                 (1024, 384, 128), (1024, 512, 128), (1000, 136, 520),
+                                 # few narrow tiles with a long K (weight-gradient shapes of small layers)
+                                 # (ragged M, N and K in the second)
+                                 (128, 128, 1024), (200, 192, 680)])
 def test_gemm_bf16(at, bt, MNK):
     M, N, K = MNK
     if at and M % 8:
