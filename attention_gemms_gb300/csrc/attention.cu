@@ -402,14 +402,21 @@ template <typename T, int D>
 tp_status run_bwd(const void* qkv, const void* o, const float* lse, const void* dO, void* dqkv,
                   int b, int s, const HeadMap& hm, int kv_heads, int causal, cudaStream_t st) {
   const float scale = 1.0f / sqrtf(static_cast<float>(D));
-  TP_CUDA_TRY(launch_kernel(attn_bwd_dkdv_kernel<T, D>, dim3((s + RB - 1) / RB, kv_heads, b),
-      RB * LPR, 0, st, static_cast<const T*>(qkv), static_cast<const T*>(o), lse, static_cast<const T*>(dO),
-      static_cast<T*>(dqkv), s, hm, scale, causal));
-  TP_CUDA_TRY(launch_kernel(attn_bwd_dq_kernel<T, D>, dim3((s + RB - 1) / RB, hm.H, b),
-      RB * LPR, 0, st, static_cast<const T*>(qkv), static_cast<const T*>(o), lse, static_cast<const T*>(dO),
-      static_cast<T*>(dqkv), s, hm, scale, causal));
+  // dQ and dK/dV read the same inputs and write disjoint columns of dqkv: dQ runs on a
+  // side stream beside dK/dV (the grids are small at these sizes)
+  SideBranch br(st, 1);
+  const cudaError_t e1 = launch_kernel(
+      attn_bwd_dq_kernel<T, D>, dim3((s + RB - 1) / RB, hm.H, b), RB * LPR, 0, br.stream(),
+      static_cast<const T*>(qkv), static_cast<const T*>(o), lse, static_cast<const T*>(dO),
+      static_cast<T*>(dqkv), s, hm, scale, causal);
+  const cudaError_t e2 = launch_kernel(
+      attn_bwd_dkdv_kernel<T, D>, dim3((s + RB - 1) / RB, kv_heads, b), RB * LPR, 0, st,
+      static_cast<const T*>(qkv), static_cast<const T*>(o), lse, static_cast<const T*>(dO),
+      static_cast<T*>(dqkv), s, hm, scale, causal);
   count_launch(2);
-  TP_CUDA_TRY(cudaGetLastError());
+  TP_TRY(br.join());
+  if (e1 != cudaSuccess) return cuda_fail(e1, "attn_bwd_dq_kernel launch");
+  TP_CUDA_TRY(e2);
   return TP_OK;
 }
 

@@ -15,6 +15,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -312,13 +313,15 @@ __global__ void __launch_bounds__(32 * kRowWarps) ln_bwd_param_partial_vec_kerne
 }
 
 // The partials and their final sum in one launch, for the replicated LN (one rank) with
-// at most kClusterChunks chunks of at most kRowsPerChunk rows (larger inputs keep the
-// partial and final kernels, whose grid has more CTAs): the CTAs of a cluster (1 x chunks) take the chunks of
+// at most kClusterChunks chunks of at most kRowsPerChunk rows, or kMaxClusterChunks where
+// the device places such clusters (larger inputs keep the partial and final kernels,
+// whose grid has more CTAs): the CTAs of a cluster (1 x chunks) take the chunks of
 // one block of 32 column vectors, each keeps its chunk's sums in shared memory, and
 // after a cluster barrier CTA c adds up its share of the block's 2E x 32 outputs over
 // the cluster's CTAs in chunk order (distributed shared memory) and writes dgamma and
 // dbeta. A fixed order, so deterministic; no workspace and no second launch.
-constexpr int kClusterChunks = 8;
+constexpr int kClusterChunks = 8;      // portable cluster size
+constexpr int kMaxClusterChunks = 16;  // with the non-portable opt-in, where it can be placed
 
 template <typename T>
 __global__ void __launch_bounds__(32 * kRowWarps) ln_bwd_param_cluster_vec_kernel(
@@ -459,6 +462,36 @@ __global__ void __launch_bounds__(kFinalCols * kFinalGroups) ln_bwd_param_final_
   }
 }
 
+// Whether the device places clusters of `chunks` CTAs of the parameter-sum kernel (16
+// needs the non-portable opt-in): asked once per device, before the first such launch.
+template <typename T>
+bool cluster_fits(int chunks) {
+  static std::atomic<int> known[64];  // 0 unknown, 1 fits, 2 does not
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  if (known[dev].load() != 0) return known[dev].load() == 1;
+  auto kern = ln_bwd_param_cluster_vec_kernel<T>;
+  bool fits = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+              cudaSuccess;
+  if (fits) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = static_cast<unsigned>(chunks);
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(1, static_cast<unsigned>(chunks), 1);
+    cfg.blockDim = dim3(32 * kRowWarps, 1, 1);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    fits = cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0;
+  }
+  if (!fits) cudaGetLastError();  // the query's own error, not a launch's
+  known[dev].store(fits ? 1 : 2);
+  return fits;
+}
+
 // whole 16-byte vectors per row (the buffers themselves are 16-byte aligned)
 template <typename T>
 bool vec_rows(int h) {
@@ -498,9 +531,12 @@ tp_status bwd_t(const void* x, const float* gamma, const float* mean, const floa
   count_launch();
   TP_CUDA_TRY(cudaGetLastError());
   if (!dgamma && !dbeta && !dgamma_ranks && !dbeta_ranks) return TP_OK;
-  if (vec && ranks == 1 && !dgamma_ranks && !dbeta_ranks && M <= kClusterChunks * kRowsPerChunk) {
+  const int64_t want_chunks = (M + kRowsPerChunk - 1) / kRowsPerChunk;
+  if (vec && ranks == 1 && !dgamma_ranks && !dbeta_ranks &&
+      (want_chunks <= kClusterChunks ||
+       (want_chunks <= kMaxClusterChunks && cluster_fits<T>(kMaxClusterChunks)))) {
     const int chunks = static_cast<int>(
-        std::min<int64_t>(kClusterChunks, (M + kRowsPerChunk - 1) / kRowsPerChunk));
+        want_chunks <= kClusterChunks ? std::max<int64_t>(1, want_chunks) : kMaxClusterChunks);
     const int64_t rows_per_chunk = (M + chunks - 1) / chunks;
     constexpr int cols = 32 * Vec<T>::N;
     cudaLaunchConfig_t cfg = {};

@@ -34,8 +34,10 @@ def _gb(h, seed):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 # up to 512 rows the parameter gradients are summed in one cluster launch (512: eight
-# chunks of 64 rows), above it by the partial + final kernels
-@pytest.mark.parametrize("Mh", [(100, 128), (33, 200), (1, 8192), (512, 256), (513, 64)])
+# chunks of 64 rows), up to 1024 in a 16-CTA cluster where the device places one, above
+# it by the partial + final kernels
+@pytest.mark.parametrize("Mh", [(100, 128), (33, 200), (1, 8192), (512, 256), (513, 64),
+                                (1024, 128), (1025, 64)])
 def test_layernorm(dtype, Mh):
     M, h = Mh
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
