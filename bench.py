@@ -90,11 +90,8 @@ def col_gemm_flops(w):
 # from an ncu capture of the full-size workload, valid only for the kernel source it
 # was taken on (sha256 of csrc/gemm_tc.cu + csrc/ptx.cuh); see profiles/.
 COL_GEMM_TRAFFIC = {
-    "c5": {"bytes": 12.08e9 + 1.40e9, "src": "1c417b636733cb5a"},
-    "c3": {"bytes": 1.10e9 + 509.49e6, "src": "1c417b636733cb5a"},
-    # the GQA line's roofline launch: the dO GEMM (2048 x 2048 x 2048) through tp_gemm;
-    # its 8.4 MB output is still in L2 when the launch ends, so no DRAM write is counted
-    "gqa-dO": {"bytes": 16.82e6 + 0.0, "src": "1c417b636733cb5a"},
+    "c5": {"bytes": 11.041e9 + 1.401e9, "src": "d8b91c5e88db8c22"},
+    "c3": {"bytes": 1.068e9 + 0.509e9, "src": "d8b91c5e88db8c22"},
 }
 
 
@@ -103,9 +100,9 @@ COL_GEMM_TRAFFIC = {
 # under the same source-hash rule; c5's is taken on the c5-2k case (2048 of the 8192
 # tokens: the same kernel instance, tile shapes and per-tile K). See profiles/.
 COL_GEMM_TENSOR_PIPE = {
-    "c5": {"tensor": 77.7, "tc": 85.5, "case": "c5-2k", "src": "b0ab4dd1afc6ba5c"},
-    "c5-2k": {"tensor": 77.7, "tc": 85.5, "case": "c5-2k", "src": "b0ab4dd1afc6ba5c"},
-    "c3": {"tensor": 66.3, "tc": 74.1, "case": "c3", "src": "b0ab4dd1afc6ba5c"},
+    "c5": {"tensor": 76.1, "tc": 82.9, "case": "c5-2k", "src": "d8b91c5e88db8c22"},
+    "c5-2k": {"tensor": 76.1, "tc": 82.9, "case": "c5-2k", "src": "d8b91c5e88db8c22"},
+    "c3": {"tensor": 65.2, "tc": 73.1, "case": "c3", "src": "d8b91c5e88db8c22"},
 }
 
 
