@@ -13,6 +13,7 @@ namespace tp {
 tp_status check_device();
 void set_debug_hang(int v);
 void set_pair_mode(int v);
+void set_wide_mode(int v);
 
 namespace {
 bool al16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
@@ -249,7 +250,9 @@ extern "C" {
 
 void tp_debug_inject_wait_fault(int enable) { set_debug_hang(enable); }
 
-void tp_set_gemm_pair_mode(int enable) { set_pair_mode(enable); }
+void tp_set_gemm_pair_mode(int enable) { set_pair_mode(enable == 0 || enable == 2 ? enable : 1); }
+
+void tp_set_gemm_wide_mode(int mode) { set_wide_mode(mode == 0 || mode == 2 ? mode : 1); }
 
 size_t tp_workspace_size(tp_op op, int64_t M, int64_t h, int64_t f, int32_t N, tp_dtype dtype,
                          tp_act act, tp_reduce mode) {

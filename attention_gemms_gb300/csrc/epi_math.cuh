@@ -24,10 +24,29 @@ __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf
 __device__ __forceinline__ float silu_f(float x) { return x * sigmoid_f(x); }
 
 // returns dG, writes dU:  a = dA, g = gate pre-activation, u = up pre-activation
-__device__ __forceinline__ float dswiglu_f(float a, float g, float u, float& du) {
-  const float s = sigmoid_f(g);
+__device__ __forceinline__ float dswiglu_of(float a, float g, float u, float s, float& du) {
   du = a * g * s;
   return a * u * s * (1.0f + g * (1.0f - s));
+}
+__device__ __forceinline__ float dswiglu_f(float a, float g, float u, float& du) {
+  return dswiglu_of(a, g, u, sigmoid_f(g), du);
+}
+
+// The same on the special-function unit, for epilogues whose results are rounded to
+// bf16: e^-x = 2^(-x log2 e) by ex2.approx and the reciprocal by rcp.approx, each
+// within a few fp32 ulp (about 1e-6 relative in all), where bf16 keeps 8 bits. The
+// full-precision forms above cost an accurate exponential and an IEEE division per
+// element, which made the epilogue warps, not the tensor core, the limit of the
+// SwiGLU GEMMs. Large |x| saturate correctly: e^-x = inf gives 0, e^-x = 0 gives 1.
+__device__ __forceinline__ float sigmoid_sfu(float x) {
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * -1.4426950408889634f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+  return r;
+}
+__device__ __forceinline__ float silu_sfu(float x) { return x * sigmoid_sfu(x); }
+__device__ __forceinline__ float dswiglu_sfu(float a, float g, float u, float& du) {
+  return dswiglu_of(a, g, u, sigmoid_sfu(g), du);
 }
 
 }  // namespace tp

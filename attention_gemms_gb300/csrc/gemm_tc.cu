@@ -220,7 +220,7 @@ __device__ __forceinline__ void epi8(const TcParams& p, int g, int64_t row, int6
     if (p.out0) st8(p.out0, idx, a);
     if (p.out1) st8(p.out1, idx, b);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = silu_f(a[i]) * b[i];
+    for (int i = 0; i < 8; ++i) v[i] = silu_sfu(a[i]) * b[i];
     st8(p.out2, idx, v);
   } else if constexpr (EPI == EPI_DGELU) {
     in8(p.in0, pre0, w);
@@ -232,7 +232,7 @@ __device__ __forceinline__ void epi8(const TcParams& p, int g, int64_t row, int6
     in8(p.in0, pre0, gg);
     in8(p.in1, pre1, uu);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = dswiglu_f(a[i], gg[i], uu[i], du[i]);
+    for (int i = 0; i < 8; ++i) v[i] = dswiglu_sfu(a[i], gg[i], uu[i], du[i]);
     st8(p.out0, idx, v);
     st8(p.out1, idx, du);
   } else if constexpr (EPI == EPI_PAIR) {
@@ -322,7 +322,7 @@ __device__ __forceinline__ void epi16(const TcParams& p, int g, int64_t row, int
     if (p.out0) st16(p.out0, idx, a, wide);
     if (p.out1) st16(p.out1, idx, b, wide);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = silu_f(a[i]) * b[i];
+    for (int i = 0; i < 16; ++i) v[i] = silu_sfu(a[i]) * b[i];
     st16(p.out2, idx, v, wide);
   } else if constexpr (EPI == EPI_DGELU) {
     in16(p.in0, idx, w, pre, i0a, i0b);
@@ -334,7 +334,7 @@ __device__ __forceinline__ void epi16(const TcParams& p, int g, int64_t row, int
     in16(p.in0, idx, w, pre, i0a, i0b);
     in16(p.in1, idx, uu, pre, i1a, i1b);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = dswiglu_f(a[i], w[i], uu[i], du[i]);
+    for (int i = 0; i < 16; ++i) v[i] = dswiglu_sfu(a[i], w[i], uu[i], du[i]);
     st16(p.out0, idx, v, wide);
     st16(p.out1, idx, du, wide);
   } else if constexpr (EPI == EPI_PAIR) {
@@ -649,25 +649,46 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 // drains the other half of each accumulator tile's columns, halving the epilogue time
 static_assert(TP_PAIR_EPI_WARPS == 4 || TP_PAIR_EPI_WARPS == 8, "4 or 8 epilogue warps");
 constexpr int kEpiHi0 = TP_PAIR_DUAL ? 7 : 6;  // first warp of the second epilogue set
-constexpr int kPairThreads = 32 * (kEpiHi0 + (TP_PAIR_EPI_WARPS == 8 ? 4 : 0));
-constexpr int kPairStages = TP_PAIR_STAGES;
-constexpr int kPairStageBytes = 2 * 128 * BK * 2;  // A 128 x 64 + B 128 x 64, bf16
-constexpr int kPairBars = 2 * kPairStages + 7;
-constexpr int kPairSmem = kPairStages * kPairStageBytes + 1024 + kPairBars * 8 + 16;
 constexpr uint64_t kPairDrainNs = 20000000ull;
 
-template <int EPI>
-__global__ void __launch_bounds__(kPairThreads, 1) gemm_tc2_kernel(const __grid_constant__ TcParams p) {
-  constexpr int S = kPairStages;
+// Wide form (WN = 2): the pair computes a 256 x 512 tile -- two N = 256 MMAs per K
+// step into one 128 x 512 fp32 accumulator per CTA, all 512 TMEM columns. A stage
+// holds A 128 x 64 and two B halves of 128 x 64 per CTA (48 KB), four stages deep.
+// Per FLOP it moves 3/4 of the operand bytes of the 256 x 256 tile from L2 into
+// shared memory, which is what bounds the narrow form's issue rate. With a single
+// accumulator the epilogue drains the first 256 columns, hands them back
+// (tempty 0) and then drains the second half (tempty 1); meanwhile the next tile's
+// first stages already run their first-half MMAs.
+#ifndef TP_WIDE_STAGES
+#define TP_WIDE_STAGES 4
+#endif
+template <int WN>
+struct PairCfg {
+  static constexpr int EPI_WARPS = WN == 2 ? 8 : TP_PAIR_EPI_WARPS;
+  static constexpr int THREADS = 32 * (kEpiHi0 + (EPI_WARPS == 8 ? 4 : 0));
+  static constexpr int STAGES = WN == 2 ? TP_WIDE_STAGES : TP_PAIR_STAGES;
+  static constexpr int B_HALF_BYTES = 128 * BK * 2;                // 128 x 64 bf16
+  static constexpr int STAGE_BYTES = (1 + WN) * B_HALF_BYTES;      // A + WN B halves
+  static constexpr int NACC = WN == 2 ? 1 : 2;                     // TMEM accumulators
+  static constexpr int NBARS = 2 * STAGES + 7;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + NBARS * 8 + 16;
+};
+static_assert(PairCfg<2>::SMEM <= 232448 && PairCfg<1>::SMEM <= 232448, "shared memory per CTA");
+
+template <int EPI, int WN>
+__global__ void __launch_bounds__(PairCfg<WN>::THREADS, 1)
+    gemm_tc2_kernel(const __grid_constant__ TcParams p) {
+  using C = PairCfg<WN>;
+  constexpr int S = C::STAGES;
   constexpr int A_BYTES = 128 * BK * 2;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * kPairStageBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kPairBars);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 #ifdef TP_GEMM_STATS
-  __shared__ volatile long long issue_clk[kPairStages], commit_clk[kPairStages];
+  __shared__ volatile long long issue_clk[S], commit_clk[S];
 #endif
 
   const int warp = threadIdx.x >> 5;
@@ -691,7 +712,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_tc2_kernel(const __grid_
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), leader ? 2 * TP_PAIR_EPI_WARPS : 1);  // epilogue warps of both CTAs
+      mbar_init(tempty_bar(b), leader ? 2 * C::EPI_WARPS : 1);  // epilogue warps of both CTAs
     }
     mbar_init(drain_bar, 1);
     mbar_init(exit_bar, 1);
@@ -740,7 +761,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_tc2_kernel(const __grid_
       for (int t = pair; t < ntiles && ok; t += npairs) {
         const TileCoord tc = tile_coord(p, t);
         const int m0 = tc.mt * 256 + static_cast<int>(rank) * 128;
-        const int n0 = tc.nt * bn_logical;
+        const int n0 = tc.nt * bn_logical * WN;
         for (int kb = 0; kb < nkb; ++kb) {
           [[maybe_unused]] const long long tw = TP_CLK();
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag)) {
@@ -751,7 +772,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_tc2_kernel(const __grid_
           const int seg = kb / p.kb_per_seg;
           const int k0 =
               p.seg_k0[seg] + static_cast<int>(tc.g * p.K) + (kb - seg * p.kb_per_seg) * BK;
-          const uint32_t a_dst = sbase + stage * kPairStageBytes;
+          const uint32_t a_dst = sbase + stage * C::STAGE_BYTES;
           const uint32_t b_dst = a_dst + A_BYTES;
           const uint32_t fb = lead_full0 + 8u * stage;  // the even CTA's barrier
 #ifdef TP_GEMM_STATS
@@ -761,7 +782,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_tc2_kernel(const __grid_
             issue_clk[stage] = now;
           }
 #endif
-          if (leader && load_a) mbar_arrive_expect_tx(full_bar(stage), 2 * kPairStageBytes);
+          if (leader && load_a) mbar_arrive_expect_tx(full_bar(stage), 2 * C::STAGE_BYTES);
           if (!load_a) {
           } else if (p.a_mn && p.a3d) {
             tma_load_3d_pair(a_dst, &p.tmA[seg], fb, 0, k0, m0 / 64);
@@ -771,28 +792,35 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_tc2_kernel(const __grid_
           } else {
             tma_load_2d_pair(a_dst, &p.tmA[seg], fb, k0, m0);
           }
-          if (!load_b) {
-          } else if (p.paired && !p.b_mn) {
-            // K-major ((out, in) weights): even CTA 128 gate rows, odd CTA the same up rows
-            tma_load_2d_pair(b_dst, &p.tmB[rank], fb, k0, n0);
-          } else if (p.paired) {
-            // even CTA: 128 gate columns, odd CTA: the same 128 up columns
-            if (p.b3d) {
-              tma_load_3d_pair(b_dst, &p.tmB[rank], fb, 0, k0, n0 / 64);
+          // B: WN halves of the tile's MMA width, each split between the two CTAs
+#pragma unroll
+          for (int h = 0; h < WN; ++h) {
+            const uint32_t bh = b_dst + h * C::B_HALF_BYTES;
+            if (!load_b) {
+            } else if (p.paired && !p.b_mn) {
+              // K-major ((out, in) weights): even CTA 128 gate rows, odd CTA the same up rows
+              tma_load_2d_pair(bh, &p.tmB[rank], fb, k0, n0 + h * 128);
+            } else if (p.paired) {
+              // even CTA: 128 gate columns, odd CTA: the same 128 up columns
+              const int nb = n0 + h * 128;
+              if (p.b3d) {
+                tma_load_3d_pair(bh, &p.tmB[rank], fb, 0, k0, nb / 64);
+              } else {
+                tma_load_2d_pair(bh, &p.tmB[rank], fb, nb, k0);
+                tma_load_2d_pair(bh + 8192, &p.tmB[rank], fb, nb + 64, k0);
+              }
+            } else if (p.b_mn) {
+              const int nb = n0 + h * 256 + static_cast<int>(rank) * 128;
+              if (p.b3d) {
+                tma_load_3d_pair(bh, &p.tmB[seg], fb, 0, k0, nb / 64);
+              } else {
+                tma_load_2d_pair(bh, &p.tmB[seg], fb, nb, k0);
+                tma_load_2d_pair(bh + 8192, &p.tmB[seg], fb, nb + 64, k0);
+              }
             } else {
-              tma_load_2d_pair(b_dst, &p.tmB[rank], fb, n0, k0);
-              tma_load_2d_pair(b_dst + 8192, &p.tmB[rank], fb, n0 + 64, k0);
+              tma_load_2d_pair(bh, &p.tmB[seg], fb, k0,
+                               n0 + h * 256 + static_cast<int>(rank) * 128);
             }
-          } else if (p.b_mn) {
-            const int nb = n0 + static_cast<int>(rank) * 128;
-            if (p.b3d) {
-              tma_load_3d_pair(b_dst, &p.tmB[seg], fb, 0, k0, nb / 64);
-            } else {
-              tma_load_2d_pair(b_dst, &p.tmB[seg], fb, nb, k0);
-              tma_load_2d_pair(b_dst + 8192, &p.tmB[seg], fb, nb + 64, k0);
-            }
-          } else {
-            tma_load_2d_pair(b_dst, &p.tmB[seg], fb, k0, n0 + static_cast<int>(rank) * 128);
           }
           ++issued;
           if (++stage == S) {
@@ -815,9 +843,47 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_tc2_kernel(const __grid_
       bool ok = true;
       if (p.debug_hang) ok = mbar_wait(never_bar, 0, p.timeout_ns, abort_flag);
       [[maybe_unused]] const long long t_start = TP_CLK();
+      // the MMAs of one stage for the tile halves [h0, h1), K block kb of the tile
+      auto issue = [&](uint32_t d_tmem, int h0, int h1, int kb) {
+        const uint32_t a_addr = sbase + stage * C::STAGE_BYTES;
+        const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint64_t ad = sw128_desc(a_addr + kk * a_kstep, a_lbo, 1024u);
+#pragma unroll
+          for (int h = 0; h < WN; ++h) {
+            if (h < h0 || h >= h1) continue;
+            const uint64_t bd =
+                sw128_desc(b_addr + h * C::B_HALF_BYTES + kk * b_kstep, b_lbo, 1024u);
+            mma_bf16_ss_pair(d_tmem + h * 256, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+        }
+      };
+      auto wait_full = [&]() {
+        [[maybe_unused]] const long long tw = TP_CLK();
+        if (!mbar_wait(full_bar(stage), phase, p.timeout_ns, abort_flag)) return false;
+        TP_STAT(1, TP_CLK() - tw);
+#ifdef TP_GEMM_STATS
+        TP_STAT(8, clock64() - issue_clk[stage]);
+        TP_STAT(10, 1);
+#endif
+        if (TP_KLOOP_FENCE) tc_fence_after();
+        return true;
+      };
+      auto release = [&]() {
+        mma_commit_pair(empty_bar(stage), 0x3);
+#ifdef TP_GEMM_STATS
+        commit_clk[stage] = clock64();
+#endif
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      };
       for (int t = pair; t < ntiles && ok; t += npairs) {
         [[maybe_unused]] long long tw = TP_CLK();
-        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
+        // narrow: accumulator `acc` drained; wide: the first half of the accumulator
+        if (!mbar_wait(tempty_bar(WN == 2 ? 0 : acc), acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
           ok = false;
           break;
         }
@@ -825,39 +891,51 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_tc2_kernel(const __grid_
         TP_STAT(6, 1);
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * 256;
-        for (int kb = 0; kb < nkb; ++kb) {
-          tw = TP_CLK();
-          if (!mbar_wait(full_bar(stage), phase, p.timeout_ns, abort_flag)) {
+        int kb = 0;
+        if constexpr (WN == 2) {
+          // the first stages' first-half MMAs run while the epilogue drains the second
+          // half of the previous tile; then the same stages' second-half MMAs
+          const int pre = min(S, nkb);
+          const uint32_t stage0 = stage, phase0 = phase;
+          for (int j = 0; j < pre && ok; ++j) {
+            ok = wait_full();
+            if (!ok) break;
+            issue(d_tmem, 0, 1, j);
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          if (!mbar_wait(tempty_bar(1), acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
             ok = false;
             break;
           }
-          TP_STAT(1, TP_CLK() - tw);
-#ifdef TP_GEMM_STATS
-          TP_STAT(8, clock64() - issue_clk[stage]);
-          TP_STAT(10, 1);
-#endif
-          if (TP_KLOOP_FENCE) tc_fence_after();
-          const uint32_t a_addr = sbase + stage * kPairStageBytes;
-          const uint32_t b_addr = a_addr + A_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = sw128_desc(a_addr + kk * a_kstep, a_lbo, 1024u);
-            const uint64_t bd = sw128_desc(b_addr + kk * b_kstep, b_lbo, 1024u);
-            mma_bf16_ss_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          tc_fence_after();
+          stage = stage0;
+          phase = phase0;
+          for (int j = 0; j < pre; ++j) {
+            issue(d_tmem, 1, 2, j);
+            release();
           }
-          mma_commit_pair(empty_bar(stage), 0x3);
-#ifdef TP_GEMM_STATS
-          commit_clk[stage] = clock64();
-#endif
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
+          kb = pre;
+        }
+        for (; kb < nkb; ++kb) {
+          if (!wait_full()) {
+            ok = false;
+            break;
           }
+          issue(d_tmem, 0, WN, kb);
+          release();
         }
         if (!ok) break;
         mma_commit_pair(tfull_bar(acc), 0x3);
-        acc ^= 1u;
-        if (acc == 0) acc_phase ^= 1u;
+        if (C::NACC == 2) {
+          acc ^= 1u;
+          if (acc == 0) acc_phase ^= 1u;
+        } else {
+          acc_phase ^= 1u;
+        }
       }
       TP_STAT(5, TP_CLK() - t_start);
       if (!ok) record_timeout(p.status);
@@ -867,8 +945,10 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_tc2_kernel(const __grid_
     // -------------------------------------------------------------- epilogue (both CTAs)
     const int quad = warp & 3;  // a warp reaches the TMEM lanes of quarter warp % 4
     const int nchunk = bn_logical / 32;
-    const int c_lo = warp >= kEpiHi0 ? nchunk / 2 : 0;
-    const int c_hi = TP_PAIR_EPI_WARPS == 8 && warp < 6 ? nchunk / 2 : nchunk;
+    // with eight epilogue warps each set drains half of every accumulator half's chunks
+    constexpr int kEW = C::EPI_WARPS;
+    const int c_lo = kEW == 8 && warp >= kEpiHi0 ? nchunk / 2 : 0;
+    const int c_hi = kEW == 8 && warp < 6 ? nchunk / 2 : nchunk;
     const uint32_t remote_tempty0 = mapa_shared(tempty_bar(0), 0);
     uint32_t acc = 0, acc_phase = 0;
     for (int t = pair; t < ntiles; t += npairs) {
@@ -887,64 +967,80 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_tc2_kernel(const __grid_
       const int64_t row =
           static_cast<int64_t>(tc.mt) * 256 + static_cast<int>(rank) * 128 + quad * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * 256;
-      const int64_t col_base = static_cast<int64_t>(tc.nt) * bn_logical;
-      for (int c = c_lo; c < c_hi; ++c) {
-        uint32_t ra[32], rb[32];
-        tmem_ld32(t_row + c * 32, ra);
-        if (p.paired) tmem_ld32(t_row + 128 + c * 32, rb);
-        // the chunk's epilogue inputs are requested together, while the TMEM load runs
-        constexpr int kIn = EpiInputs<EPI>::n;
-        uint4 pin0[4] = {}, pin1[4] = {};
-        const bool has0 = kIn >= 1 && p.in0 != nullptr;
-        if (kIn > 0 && row < p.M) {
-#pragma unroll
-          for (int qq = 0; qq < 2; ++qq) {
-            const int64_t col = col_base + c * 32 + qq * 16;
-            const int64_t idx = row * p.ldo + col;
-            const __nv_bfloat16* i0 = reinterpret_cast<const __nv_bfloat16*>(p.in0) + idx;
-            const __nv_bfloat16* i1 = reinterpret_cast<const __nv_bfloat16*>(p.in1) + idx;
-            if (p.ld32 && col + 16 <= p.N) {  // a whole 32-byte sector per load
-              if (has0) ld_b256(i0, pin0[2 * qq], pin0[2 * qq + 1]);
-              if (kIn == 2) ld_b256(i1, pin1[2 * qq], pin1[2 * qq + 1]);
-            } else {
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                if (col + 8 * hh < p.N) {
-                  if (has0) pin0[2 * qq + hh] = __ldg(reinterpret_cast<const uint4*>(i0 + 8 * hh));
-                  if (kIn == 2) pin1[2 * qq + hh] = __ldg(reinterpret_cast<const uint4*>(i1 + 8 * hh));
+      for (int h = 0; h < WN; ++h) {
+        const int64_t col_base = (static_cast<int64_t>(tc.nt) * WN + h) * bn_logical;
+        const uint32_t t_half = t_row + h * 256;
+        for (int c = c_lo; c < c_hi; ++c) {
+          uint32_t ra[32], rb[32];
+          tmem_ld32(t_half + c * 32, ra);
+          if (p.paired) tmem_ld32(t_half + 128 + c * 32, rb);
+          // the chunk's epilogue inputs are requested together, while the TMEM load runs
+          constexpr int kIn = EpiInputs<EPI>::n;
+          uint4 pin0[4] = {}, pin1[4] = {};
+          const bool has0 = kIn >= 1 && p.in0 != nullptr;
+          if (kIn > 0 && row < p.M) {
+  #pragma unroll
+            for (int qq = 0; qq < 2; ++qq) {
+              const int64_t col = col_base + c * 32 + qq * 16;
+              const int64_t idx = row * p.ldo + col;
+              const __nv_bfloat16* i0 = reinterpret_cast<const __nv_bfloat16*>(p.in0) + idx;
+              const __nv_bfloat16* i1 = reinterpret_cast<const __nv_bfloat16*>(p.in1) + idx;
+              if (p.ld32 && col + 16 <= p.N) {  // a whole 32-byte sector per load
+                if (has0) ld_b256(i0, pin0[2 * qq], pin0[2 * qq + 1]);
+                if (kIn == 2) ld_b256(i1, pin1[2 * qq], pin1[2 * qq + 1]);
+              } else {
+  #pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                  if (col + 8 * hh < p.N) {
+                    if (has0) pin0[2 * qq + hh] = __ldg(reinterpret_cast<const uint4*>(i0 + 8 * hh));
+                    if (kIn == 2) pin1[2 * qq + hh] = __ldg(reinterpret_cast<const uint4*>(i1 + 8 * hh));
+                  }
                 }
               }
             }
           }
-        }
-        tmem_ld_wait();
-        if (row < p.M) {
-#pragma unroll
-          for (int qq = 0; qq < 2; ++qq) {  // 16 columns at a time
-            const int64_t col = col_base + c * 32 + qq * 16;
-            float a[16], b[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              a[i] = __uint_as_float(ra[qq * 16 + i]);
-              b[i] = __uint_as_float(rb[qq * 16 + i]);
+          tmem_ld_wait();
+          if (row < p.M) {
+  #pragma unroll
+            for (int qq = 0; qq < 2; ++qq) {  // 16 columns at a time
+              const int64_t col = col_base + c * 32 + qq * 16;
+              float a[16], b[16];
+  #pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                a[i] = __uint_as_float(ra[qq * 16 + i]);
+                b[i] = __uint_as_float(rb[qq * 16 + i]);
+              }
+              if (col + 16 <= p.N)
+                epi16<EPI>(p, tc.g, row, col, a, b, kIn > 0 && has0, pin0[2 * qq], pin0[2 * qq + 1],
+                           pin1[2 * qq], pin1[2 * qq + 1]);
+              else if (col < p.N)  // N % 8 == 0: the last 8 columns
+                epi8<EPI>(p, tc.g, row, col, a, b, kIn > 0 && has0, pin0[2 * qq], pin1[2 * qq]);
             }
-            if (col + 16 <= p.N)
-              epi16<EPI>(p, tc.g, row, col, a, b, kIn > 0 && has0, pin0[2 * qq], pin0[2 * qq + 1],
-                         pin1[2 * qq], pin1[2 * qq + 1]);
-            else if (col < p.N)  // N % 8 == 0: the last 8 columns
-              epi8<EPI>(p, tc.g, row, col, a, b, kIn > 0 && has0, pin0[2 * qq], pin1[2 * qq]);
+          }
+        }
+        // wide tile: this half of the accumulator is free for the next tile's MMAs
+        if (WN == 2) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (leader) mbar_arrive(tempty_bar(h));
+            else mbar_arrive_remote(remote_tempty0 + 8u * h);
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
       if (warp == 2 && lane == 0) TP_STAT(4, TP_CLK() - tb);
-      if (lane == 0) {
-        if (leader) mbar_arrive(tempty_bar(acc));
-        else mbar_arrive_remote(remote_tempty0 + 8u * acc);
+      if (C::NACC == 2) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(tempty_bar(acc));
+          else mbar_arrive_remote(remote_tempty0 + 8u * acc);
+        }
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      } else {
+        acc_phase ^= 1u;
       }
-      acc ^= 1u;
-      if (acc == 0) acc_phase ^= 1u;
     }
   }
 
@@ -1072,9 +1168,10 @@ tp_status launch_bn(int epi, const TcParams& prm, int grid, cudaStream_t st) {
   return fail(TP_ERR_INVALID_ARG, "unknown epilogue");
 }
 
-template <int EPI>
+template <int EPI, int WN>
 tp_status launch_pair_epi(const TcParams& prm, int64_t ntiles, cudaStream_t st) {
-  auto kern = gemm_tc2_kernel<EPI>;
+  auto kern = gemm_tc2_kernel<EPI, WN>;
+  constexpr int kSmem = PairCfg<WN>::SMEM;
   static std::atomic<int> max_pairs_dev[64];  // per instantiation and device (0: unknown)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = -1;
@@ -1087,14 +1184,14 @@ tp_status launch_pair_epi(const TcParams& prm, int64_t ntiles, cudaStream_t st) 
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_kernel
   attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.blockDim = dim3(kPairThreads, 1, 1);
-  cfg.dynamicSmemBytes = kPairSmem;
+  cfg.blockDim = dim3(PairCfg<WN>::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = kSmem;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;  // the occupancy query below takes the cluster shape only
   if (max_pairs == 0) {
     TP_CUDA_TRY(
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem));
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem));
     cfg.gridDim = dim3(2 * static_cast<unsigned>(device_sm_count() / 2), 1, 1);
     int n = 0;
     TP_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, kern, &cfg));
@@ -1110,26 +1207,47 @@ tp_status launch_pair_epi(const TcParams& prm, int64_t ntiles, cudaStream_t st) 
   return TP_OK;
 }
 
-tp_status launch_pair(int epi, const TcParams& prm, int64_t ntiles, cudaStream_t st) {
+template <int WN>
+tp_status launch_pair_wn(int epi, const TcParams& prm, int64_t ntiles, cudaStream_t st) {
   switch (epi) {
-    case EPI_STORE: return launch_pair_epi<EPI_STORE>(prm, ntiles, st);
-    case EPI_GELU: return launch_pair_epi<EPI_GELU>(prm, ntiles, st);
-    case EPI_SWIGLU: return launch_pair_epi<EPI_SWIGLU>(prm, ntiles, st);
-    case EPI_DGELU: return launch_pair_epi<EPI_DGELU>(prm, ntiles, st);
-    case EPI_DSWIGLU: return launch_pair_epi<EPI_DSWIGLU>(prm, ntiles, st);
-    case EPI_PAIR: return launch_pair_epi<EPI_PAIR>(prm, ntiles, st);
+    case EPI_STORE: return launch_pair_epi<EPI_STORE, WN>(prm, ntiles, st);
+    case EPI_GELU: return launch_pair_epi<EPI_GELU, WN>(prm, ntiles, st);
+    case EPI_SWIGLU: return launch_pair_epi<EPI_SWIGLU, WN>(prm, ntiles, st);
+    case EPI_DGELU: return launch_pair_epi<EPI_DGELU, WN>(prm, ntiles, st);
+    case EPI_DSWIGLU: return launch_pair_epi<EPI_DSWIGLU, WN>(prm, ntiles, st);
+    case EPI_PAIR: return launch_pair_epi<EPI_PAIR, WN>(prm, ntiles, st);
   }
   return fail(TP_ERR_INVALID_ARG, "unknown epilogue");
 }
 
+tp_status launch_pair(int epi, bool wide, const TcParams& prm, int64_t ntiles, cudaStream_t st) {
+  return wide ? launch_pair_wn<2>(epi, prm, ntiles, st) : launch_pair_wn<1>(epi, prm, ntiles, st);
+}
+
 std::atomic<int> g_debug_hang{0};
-std::atomic<int> g_pair_mode{1};  // 1: CTA-pair kernel for large tiles, 0: one-CTA kernel only
+// 1: CTA-pair kernel for large problems, 0: one-CTA kernel only, 2: the pair kernel for
+// every GEMM it can run (at least 256 rows and 256 TMEM columns), small ones included
+std::atomic<int> g_pair_mode{1};
+// 256 x 512 pair tiles: 0 never, 1 where the width is whole wide tiles and there are
+// at least four per SM pair, 2 whenever the pair kernel runs (tests of the wide form)
+std::atomic<int> g_wide_mode{1};
 
 }  // namespace
 
 void set_debug_hang(int v) { g_debug_hang.store(v); }
 int debug_hang_flag() { return g_debug_hang.load(); }
 void set_pair_mode(int v) { g_pair_mode.store(v); }
+void set_wide_mode(int v) { g_wide_mode.store(v); }
+
+// bytes the epilogue writes per output element (logical column) of a row
+#ifndef TP_WIDE_K_PER_BYTE
+#define TP_WIDE_K_PER_BYTE 1024
+#endif
+int epi_out_bytes(const GemmDesc& d) {
+  int n = 0;
+  for (void* o : d.out) n += o != nullptr;
+  return std::max(n, 1) * (d.out_f32 ? 4 : 2);
+}
 
 tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
   if (d.M <= 0 || d.N <= 0 || d.K <= 0) return TP_OK;
@@ -1152,7 +1270,7 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
   // small problems (a handful of tiles, e.g. M = 1024 tokens at h = 128): narrower
   // one-CTA tiles, down to 128 x 64, while that leaves at most half the SMs busy, so
   // more SMs share the operand loads and the epilogue (unpaired, not the decode form)
-  if (!d.paired && d.M > 64) {
+  if (!d.paired && d.M > 64 && g_pair_mode.load() != 2) {
     const int64_t sms = device_sm_count();
     auto ctas = [&](int64_t tm, int64_t bn) {
       return (d.M + tm - 1) / tm * ((d.N + bn - 1) / bn) * d.groups;
@@ -1162,6 +1280,20 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
   }
   const int bn_logical = d.paired ? BN / 2 : BN;
   const int tile_m = pair ? 256 : BM;
+  // pair tiles twice as wide (256 x 512): 3/4 of the operand bytes per FLOP, but one
+  // accumulator, so most of each tile's epilogue is not hidden behind MMAs: taken
+  // where the width is whole wide tiles, there are at least four per SM pair, and
+  // the tile's K is long beside the bytes its epilogue writes per output element
+  bool wide = false;
+  if (pair) {
+    const int64_t ww = 2 * bn_logical;
+    const int64_t wtiles = (d.M + 255) / 256 * ((d.N + ww - 1) / ww) * d.groups;
+    const int64_t k_tile = static_cast<int64_t>(d.nseg) * d.K;
+    const int mode = g_wide_mode.load();
+    wide = mode == 2 || (mode == 1 && d.N % ww == 0 && wtiles >= 2 * device_sm_count() &&
+                         k_tile >= static_cast<int64_t>(TP_WIDE_K_PER_BYTE) * epi_out_bytes(d));
+  }
+  const int tile_w = bn_logical * (wide ? 2 : 1);  // logical output columns of a tile
   // decode configuration: at most 64 K-major rows of A
   const bool dec = !pair && BN == 128 && !d.a_mn && d.M <= 64;
   const int a_rows = dec ? static_cast<int>((d.M + 7) / 8 * 8) : BM;
@@ -1201,7 +1333,7 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
   prm.paired = d.paired;
   prm.groups = d.groups;
   prm.tiles_m = static_cast<int>((d.M + tile_m - 1) / tile_m);
-  prm.tiles_n = static_cast<int>((d.N + bn_logical - 1) / bn_logical);
+  prm.tiles_n = static_cast<int>((d.N + tile_w - 1) / tile_w);
   prm.kb_per_seg = static_cast<int>((d.K + BK - 1) / BK);
   prm.shards = 1;
   prm.shard_axis = d.shard_axis;
@@ -1233,7 +1365,7 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
 
   const int64_t ntiles = static_cast<int64_t>(prm.tiles_m) * prm.tiles_n * prm.groups;
   if (ntiles > (1ll << 30)) return fail(TP_ERR_SHAPE, "problem too large");
-  if (pair) return launch_pair(epi, prm, ntiles, st);
+  if (pair) return launch_pair(epi, wide, prm, ntiles, st);
   const int grid = static_cast<int>(
       std::min<int64_t>(ntiles, static_cast<int64_t>(device_sm_count()) * (dec ? TP_DEC_CTAS_PER_SM : 1)));
   if (dec) return launch_bn<128, true>(epi, prm, grid, st);

@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(32 * kWarps) gemv_kernel(const GemvParams p) {
     if constexpr (EPI == EPI_SWIGLU) {
       if (p.out0) st_bf16(p.out0, i, a);
       if (p.out1) st_bf16(p.out1, i, b);
-      st_bf16(p.out2, i, silu_f(a) * b);
+      st_bf16(p.out2, i, silu_sfu(a) * b);
     } else if constexpr (EPI == EPI_GELU) {
       if (p.out0) st_bf16(p.out0, i, a);
       st_bf16(p.out1, i, gelu_f(a));

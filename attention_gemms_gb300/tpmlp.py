@@ -127,6 +127,7 @@ _SIGS = {
     "tp_check_status": (_ST, [_P]),
     "tp_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "tp_set_gemm_pair_mode": (None, [ctypes.c_int]),
+    "tp_set_gemm_wide_mode": (None, [ctypes.c_int]),
     "tp_launch_count": (ctypes.c_uint64, []),
     "tp_workspace_size": (_SZ, [_ST, _I64, _I64, _I64, _I32, _ST, _ST, _ST]),
     "tp_gemm": (_ST, [_P, _P, _P, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, _ST, _P]),
@@ -256,8 +257,13 @@ def tp_set_wait_timeout_ns(ns: int) -> None:
     lib().tp_set_wait_timeout_ns(int(ns))
 
 
-def tp_set_gemm_pair_mode(enable: bool) -> None:
-    lib().tp_set_gemm_pair_mode(1 if enable else 0)
+def tp_set_gemm_pair_mode(enable) -> None:
+    """False/0: one-CTA kernel only; True/1: automatic; 2: pair kernel whenever it can run."""
+    lib().tp_set_gemm_pair_mode(int(enable))
+
+
+def tp_set_gemm_wide_mode(mode: int) -> None:
+    lib().tp_set_gemm_wide_mode(int(mode))
 
 
 def tp_launch_count() -> int:

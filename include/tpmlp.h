@@ -210,10 +210,22 @@ TP_API tp_status tp_check_status(void* stream);
 TP_API void tp_set_wait_timeout_ns(uint64_t ns);
 
 /* Large GEMM tiles (M >= 256 rows, 256 columns) run on CTA pairs (two SMs sharing one
- * 256 x 256 tile through tcgen05 pair MMAs) when enabled (default 1); 0 restricts every
- * GEMM to the one-CTA 128 x 256 kernel. Results agree within rounding either way;
- * this switch exists to compare the two kernels. Applies to launches made after it. */
+ * 256 x 256 tile through tcgen05 pair MMAs) when enabled (default 1), except on
+ * problems so small that narrower one-CTA tiles spread them over more SMs; 0 restricts
+ * every GEMM to the one-CTA kernel; 2 runs the pair kernel for every GEMM it can take,
+ * small ones included (to test it on small shapes). Any other value is treated as 1.
+ * Results agree within rounding in every mode; this switch exists to compare the
+ * kernels. Applies to launches made after it. */
 TP_API void tp_set_gemm_pair_mode(int enable);
+
+/* Width of the CTA-pair tiles: 1 (default) uses 256 x 512 tiles -- two pair MMAs per
+ * K step into one 128 x 512 accumulator per CTA, 3/4 of the operand bytes per FLOP of
+ * 256 x 256 -- where the output width is whole 512-column tiles (256 for the paired
+ * gate/up form) and there are at least four tiles per SM pair; 0 keeps 256 x 256
+ * tiles; 2 takes the wide tiles for every pair-kernel GEMM (to test that form on
+ * small shapes). Results agree within rounding in every mode. Applies to launches
+ * made after the call; any other value is treated as 1. */
+TP_API void tp_set_gemm_wide_mode(int mode);
 
 /* Number of kernel launches this library has made in this process (all threads). */
 TP_API uint64_t tp_launch_count(void);

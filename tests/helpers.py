@@ -44,3 +44,24 @@ def guarded(shape, dtype, guard_rows=2, device="cuda"):
 
 def guard_intact(full, rows):
     return bool(torch.all(full[rows:] == -768.0).item())
+
+
+class gemm_tiles:
+    """Context manager: GEMM kernel selection for a test (pair: 0 one-CTA only,
+    1 automatic, 2 the CTA-pair kernel wherever it can run; wide: 0 256 x 256 pair
+    tiles, 1 automatic, 2 256 x 512 pair tiles), restored to automatic on exit."""
+
+    def __init__(self, pair, wide):
+        self.pair, self.wide = pair, wide
+
+    def __enter__(self):
+        from attention_gemms_gb300 import tpmlp as T
+        T.tp_set_gemm_pair_mode(self.pair)
+        T.tp_set_gemm_wide_mode(self.wide)
+        return self
+
+    def __exit__(self, *exc):
+        from attention_gemms_gb300 import tpmlp as T
+        T.tp_set_gemm_pair_mode(1)
+        T.tp_set_gemm_wide_mode(1)
+        return False

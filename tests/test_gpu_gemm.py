@@ -6,7 +6,7 @@ import pytest
 import torch
 
 from attention_gemms_gb300 import tpmlp as T
-from tests.helpers import BF16_TOL, F32_TOL, guard_intact, guarded, host, rel, tensor
+from tests.helpers import BF16_TOL, F32_TOL, gemm_tiles, guard_intact, guarded, host, rel, tensor
 
 pytestmark = pytest.mark.gpu
 
@@ -61,17 +61,42 @@ def test_gemm_f32(at, bt):
     assert e <= F32_TOL and ok, e
 
 
-# ---- the CTA-pair kernel's epilogue paths: 256-bit stores / loads when the outputs
-# (inputs) are 32-byte aligned, 128-bit otherwise, and the 8-column tail when N % 16 == 8
+# ---- the CTA-pair kernel in both tile widths (256 x 256 and 256 x 512), forced onto
+# small shapes: every operand-major combination; one K block, fewer K blocks than the
+# wide form's four stages, more of them, and ragged M / N / K; a second tile half that
+# lies wholly or partly past N
 
-@pytest.mark.parametrize("MNK", [(384, 264, 192), (512, 520, 128)])
-def test_pair_gemm_ragged_columns(MNK):
+@pytest.mark.parametrize("wide", [0, 2], ids=["pair256", "pair512"])
+@pytest.mark.parametrize("at", [False, True])
+@pytest.mark.parametrize("bt", [False, True])
+@pytest.mark.parametrize("MNK", [(256, 512, 64), (256, 512, 128), (512, 1024, 320),
+                                 (600, 1288, 520), (768, 264, 192), (256, 256, 512)])
+def test_pair_gemm_forms(wide, at, bt, MNK):
     M, N, K = MNK
-    e, ok = _run(M, N, K, False, False)
+    with gemm_tiles(2, wide):
+        e, ok = _run(M, N, K, at, bt, seed=640)
     assert e <= BF16_TOL and ok, e
 
 
-def test_pair_gemm_output_only_16_byte_aligned():
+# ---- the CTA-pair kernel's epilogue paths: 256-bit stores / loads when the outputs
+# (inputs) are 32-byte aligned, 128-bit otherwise, and the 8-column tail when N % 16 == 8
+
+@pytest.mark.parametrize("wide", [0, 2], ids=["pair256", "pair512"])
+@pytest.mark.parametrize("MNK", [(384, 264, 192), (512, 520, 128)])
+def test_pair_gemm_ragged_columns(MNK, wide):
+    M, N, K = MNK
+    with gemm_tiles(2, wide):
+        e, ok = _run(M, N, K, False, False)
+    assert e <= BF16_TOL and ok, e
+
+
+@pytest.mark.parametrize("wide", [0, 2], ids=["pair256", "pair512"])
+def test_pair_gemm_output_only_16_byte_aligned(wide):
+    with gemm_tiles(2, wide):
+        _output_only_16_byte_aligned()
+
+
+def _output_only_16_byte_aligned():
     M, N, K = 512, 512, 256
     A = tensor((M, K), 610)[1]
     B = tensor((K, N), 611, 0.1)[1]
@@ -85,9 +110,15 @@ def test_pair_gemm_output_only_16_byte_aligned():
     assert torch.equal(C, C16)
 
 
-def test_pair_gemm_epilogue_inputs_only_16_byte_aligned():
+@pytest.mark.parametrize("wide", [0, 2], ids=["pair256", "pair512"])
+def test_pair_gemm_epilogue_inputs_only_16_byte_aligned(wide):
     """The GELU MLP backward reads Y in its epilogue: a Y 16 bytes off a 32-byte boundary
     gives the same gradients bit for bit."""
+    with gemm_tiles(2, wide):
+        _epilogue_inputs_only_16_byte_aligned()
+
+
+def _epilogue_inputs_only_16_byte_aligned():
     M, h, f, N = 512, 256, 512, 2
     BF, A = T.DType.BF16, T.Act.GELU
     X = tensor((M, h), 620)[1]

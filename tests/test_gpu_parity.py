@@ -9,7 +9,8 @@ import torch
 
 from attention_gemms_gb300 import tpmlp as T
 from oracle import tp_oracle as O
-from tests.helpers import BF16_TOL, F32_TOL, empty, guard_intact, guarded, host, rel, tensor
+from tests.helpers import (BF16_TOL, F32_TOL, empty, gemm_tiles, guard_intact, guarded, host,
+                           rel, tensor)
 
 pytestmark = pytest.mark.gpu
 BF = T.DType.BF16
@@ -163,6 +164,19 @@ def _mlp_run(act, mode, N, M, h, f, dtype="bf16", seed0=400, sigma=0.05):
 @pytest.mark.parametrize("N", [1, 2, 4])
 def test_mlp_bf16(act, mode, N):
     errs, _ = _mlp_run(act, mode, N, M=333, h=192, f=512)
+    for k, e in errs.items():
+        assert e <= BF16_TOL, (k, e)
+
+
+@pytest.mark.parametrize("wide", [0, 2], ids=["pair256", "pair512"])
+@pytest.mark.parametrize("act", [T.Act.GELU, T.Act.SWIGLU])
+@pytest.mark.parametrize("mode", [T.Reduce.BUFFERS, T.Reduce.SPLITK])
+def test_mlp_bf16_pair_tiles(act, mode, wide):
+    """Every GEMM of the step on the CTA-pair kernel in one tile width: the paired
+    gate/up operands, MN-major weight-gradient operands, the two-segment dX, per-shard
+    K-groups and the epilogues that read saved activations."""
+    with gemm_tiles(2, wide):
+        errs, _ = _mlp_run(act, mode, 2, M=600, h=512, f=1024)
     for k, e in errs.items():
         assert e <= BF16_TOL, (k, e)
 

@@ -5,7 +5,7 @@ tp_debug_inject_wait_fault makes each launch's MMA thread wait on a barrier noth
 arrives on, with a short limit. The kernel must stop by itself (no fault, no trap),
 report TP_ERR_TIMEOUT through tp_check_status, and leave the context usable: a clean
 call right after must match the fp64 oracle. Families: the one-CTA 128 x 256 GEMM,
-its decode configuration (M <= 64), the CTA-pair GEMM, the tensor-core attention
+its decode configuration (M <= 64), the CTA-pair GEMM in both tile widths, the tensor-core attention
 forward, and the tensor-core attention backward (dK/dV and dQ kernels).
 
 The header promises that calls may come from several host threads: two threads run
@@ -22,7 +22,7 @@ import torch
 from attention_gemms_gb300 import tpmlp as T
 from oracle import gqa_oracle as Q
 from oracle import tp_oracle as O
-from tests.helpers import BF16_TOL, empty, host, rel, tensor
+from tests.helpers import BF16_TOL, empty, gemm_tiles, host, rel, tensor
 
 pytestmark = pytest.mark.gpu
 BF = T.DType.BF16
@@ -73,15 +73,17 @@ def _col_case(M, act, seed):
     return call, out, ref
 
 
-@pytest.mark.parametrize("M,act", [(128, T.Act.GELU),     # one-CTA 128 x 256 tile
-                                   (8, T.Act.SWIGLU),     # decode configuration
-                                   (40, T.Act.GELU),      # decode configuration
-                                   (512, T.Act.SWIGLU)])  # CTA pair
-def test_gemm_wait_timeout_reports_and_recovers(M, act):
+@pytest.mark.parametrize("M,act,wide", [(128, T.Act.GELU, 1),     # one-CTA 128 x 256 tile
+                                        (8, T.Act.SWIGLU, 1),     # decode configuration
+                                        (40, T.Act.GELU, 1),      # decode configuration
+                                        (512, T.Act.SWIGLU, 0),   # CTA pair, 256 x 256
+                                        (512, T.Act.SWIGLU, 2)])  # CTA pair, 256 x 512
+def test_gemm_wait_timeout_reports_and_recovers(M, act, wide):
     call, out, ref = _col_case(M, act, 7300 + M)
-    _expect_timeout(call)
-    call()
-    torch.cuda.synchronize()
+    with gemm_tiles(1, wide):
+        _expect_timeout(call)
+        call()
+        torch.cuda.synchronize()
     assert T.tp_check_status() == 0
     assert rel(host(out), ref) <= BF16_TOL
 
