@@ -79,6 +79,7 @@ struct TcCfg {
 struct TcParams {  // CUtensorMap members carry their own 128-byte alignment
   CUtensorMap tmA[3];
   CUtensorMap tmB[3];
+  CUtensorMap tmO[3];  // pair kernel, tma_out: maps of out0..out2 for TMA stores
   int64_t M, N, K;  // N counts logical output columns
   int a_mn, b_mn, nseg, paired, groups;
   int a3d, b3d;  // MN-major operand maps are 3-D (x: 64 columns, y: k, z: 64-column chunk)
@@ -96,6 +97,7 @@ struct TcParams {  // CUtensorMap members carry their own 128-byte alignment
   int st32;  // outputs 32-byte aligned with a pitch of 32-byte multiples: 256-bit stores
   int ld32;  // epilogue inputs likewise: 256-bit loads
   int64_t out_group_stride;
+  int tma_out;  // pair kernel: the epilogue stages outputs in shared memory, TMA stores them
   int* status;
   uint64_t timeout_ns;
   int debug_hang;
@@ -340,6 +342,129 @@ __device__ __forceinline__ void epi16(const TcParams& p, int g, int64_t row, int
   } else if constexpr (EPI == EPI_PAIR) {
     st16(p.out0, idx, a, wide);
     st16(p.out1, idx, b, wide);
+  }
+}
+
+// ---- pair-kernel epilogue through shared memory: a warp's 32 rows x 32 columns of
+// one output go to a 2 KB staging box (row r from lane r, 64 bytes, its 16-byte
+// granules permuted by the 64-byte swizzle the output map names -- which also keeps
+// the 32 lanes' writes free of bank conflicts) and leave by one TMA store, instead of
+// 32 scattered 32-byte stores per instruction. Each warp owns two boxes and reuses
+// one once the store issued from it two outputs ago has read it.
+struct EpiStager {
+  uint32_t base;  // this warp's two boxes (shared::cta address)
+  uint32_t k;     // the box the next output goes to
+  int lane;
+  __device__ __forceinline__ uint32_t box(uint32_t i) const { return base + i * 2048u; }
+  __device__ __forceinline__ uint32_t at(uint32_t i, int q) const {
+    return box(i) + lane * 64 + 16 * (q ^ ((lane >> 1) & 3));
+  }
+  // wait until at most `free_boxes` earlier stores still read this warp's boxes
+  template <int N>
+  __device__ __forceinline__ void acquire() {
+    if (lane == 0) bulk_wait_read<N>();
+    __syncwarp();
+  }
+  __device__ __forceinline__ void store(uint32_t i, const CUtensorMap* m, int x, int y, int z) {
+    if (lane == 0) {
+      tma_store_3d(m, box(i), x, y, z);
+      bulk_commit();
+    }
+  }
+  __device__ __forceinline__ void publish() {  // the lanes' box writes, visible to TMA
+    fence_proxy_async_smem();
+    __syncwarp();
+  }
+};
+
+__device__ __forceinline__ uint32_t bf2(float lo, float hi) {
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
+// 32 bf16 values val(0..31) of this lane's row, stored as one box at (x, y)
+template <class F>
+__device__ __forceinline__ void stage_bf16(EpiStager& st, const CUtensorMap* m, int x, int y,
+                                           F&& val) {
+  st.acquire<1>();
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    st_shared_v4(st.at(st.k, q), bf2(val(8 * q), val(8 * q + 1)), bf2(val(8 * q + 2), val(8 * q + 3)),
+                 bf2(val(8 * q + 4), val(8 * q + 5)), bf2(val(8 * q + 6), val(8 * q + 7)));
+  st.publish();
+  st.store(st.k, m, x, y, 0);
+  st.k ^= 1u;
+}
+
+// 32 fp32 values as two boxes of 16 columns: (x, y, z) and (x + 16, y, z)
+template <class F>
+__device__ __forceinline__ void stage_f32(EpiStager& st, const CUtensorMap* m, int x, int y, int z,
+                                          F&& val) {
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    st.acquire<1>();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = 16 * hf + 4 * q;
+      st_shared_v4(st.at(st.k, q), __float_as_uint(val(j)), __float_as_uint(val(j + 1)),
+                   __float_as_uint(val(j + 2)), __float_as_uint(val(j + 3)));
+    }
+    st.publish();
+    st.store(st.k, m, x + 16 * hf, y, z);
+    st.k ^= 1u;
+  }
+}
+
+// element j (0..31) of 32 bf16 inputs preloaded as four 16-byte words
+__device__ __forceinline__ float in_at(const uint4* pin, int j) {
+  const uint4 v = pin[j >> 3];
+  const int w = (j & 7) >> 1;
+  const uint32_t u = w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
+  return __uint_as_float((j & 1) ? (u & 0xFFFF0000u) : (u << 16));
+}
+
+// The epilogue of one 32-column chunk of the warp's 32 rows (same arithmetic as
+// epi16), outputs staged and TMA-stored; rows >= M and columns >= N of a box are not
+// written by the store.
+template <int EPI>
+__device__ __forceinline__ void epi_chunk_tma(const TcParams& p, EpiStager& st, int g, int x, int y,
+                                              const uint32_t* ra, const uint32_t* rb,
+                                              const uint4* pin0, const uint4* pin1, bool has0) {
+  auto A = [&](int j) { return __uint_as_float(ra[j]); };
+  auto B = [&](int j) { return __uint_as_float(rb[j]); };
+  if constexpr (EPI == EPI_STORE) {
+    auto v = [&](int j) { return has0 ? A(j) + in_at(pin0, j) : A(j); };
+    if (p.out_f32) stage_f32(st, &p.tmO[0], x, y, g, v);
+    else stage_bf16(st, &p.tmO[0], x, y, v);
+  } else if constexpr (EPI == EPI_GELU) {
+    if (p.out0) stage_bf16(st, &p.tmO[0], x, y, A);
+    stage_bf16(st, &p.tmO[1], x, y, [&](int j) { return gelu_f(A(j)); });
+  } else if constexpr (EPI == EPI_SWIGLU) {
+    if (p.out0) stage_bf16(st, &p.tmO[0], x, y, A);
+    if (p.out1) stage_bf16(st, &p.tmO[1], x, y, B);
+    stage_bf16(st, &p.tmO[2], x, y, [&](int j) { return silu_sfu(A(j)) * B(j); });
+  } else if constexpr (EPI == EPI_DGELU) {
+    stage_bf16(st, &p.tmO[0], x, y, [&](int j) { return A(j) * gelu_prime_f(in_at(pin0, j)); });
+  } else if constexpr (EPI == EPI_DSWIGLU) {
+    // dG and dU share the gate's sigmoid: both boxes are filled in one pass
+    st.acquire<0>();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float dg[8], du[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        dg[i] = dswiglu_sfu(A(8 * q + i), in_at(pin0, 8 * q + i), in_at(pin1, 8 * q + i), du[i]);
+      st_shared_v4(st.at(st.k, q), bf2(dg[0], dg[1]), bf2(dg[2], dg[3]), bf2(dg[4], dg[5]),
+                   bf2(dg[6], dg[7]));
+      st_shared_v4(st.at(st.k ^ 1u, q), bf2(du[0], du[1]), bf2(du[2], du[3]), bf2(du[4], du[5]),
+                   bf2(du[6], du[7]));
+    }
+    st.publish();
+    st.store(st.k, &p.tmO[0], x, y, 0);
+    st.store(st.k ^ 1u, &p.tmO[1], x, y, 0);  // the older of the two groups is box k's
+  } else if constexpr (EPI == EPI_PAIR) {
+    stage_bf16(st, &p.tmO[0], x, y, A);
+    stage_bf16(st, &p.tmO[1], x, y, B);
   }
 }
 
@@ -671,7 +796,9 @@ struct PairCfg {
   static constexpr int STAGE_BYTES = (1 + WN) * B_HALF_BYTES;      // A + WN B halves
   static constexpr int NACC = WN == 2 ? 1 : 2;                     // TMEM accumulators
   static constexpr int NBARS = 2 * STAGES + 7;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + NBARS * 8 + 16;
+  // epilogue staging: two 2 KB boxes (32 rows x 64 bytes) per epilogue warp
+  static constexpr int STAGING_BYTES = EPI_WARPS * 2 * 2048;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 + NBARS * 8 + 16;
 };
 static_assert(PairCfg<2>::SMEM <= 232448 && PairCfg<1>::SMEM <= 232448, "shared memory per CTA");
 
@@ -684,7 +811,8 @@ __global__ void __launch_bounds__(PairCfg<WN>::THREADS, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::STAGE_BYTES);
+  uint8_t* staging = smem + S * C::STAGE_BYTES;  // 1024-byte aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + C::STAGING_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 #ifdef TP_GEMM_STATS
@@ -950,6 +1078,8 @@ __global__ void __launch_bounds__(PairCfg<WN>::THREADS, 1)
     const int c_lo = kEW == 8 && warp >= kEpiHi0 ? nchunk / 2 : 0;
     const int c_hi = kEW == 8 && warp < 6 ? nchunk / 2 : nchunk;
     const uint32_t remote_tempty0 = mapa_shared(tempty_bar(0), 0);
+    const int epi_slot = warp < 6 ? warp - 2 : warp - kEpiHi0 + 4;
+    EpiStager stg{smem_u32(staging) + static_cast<uint32_t>(epi_slot) * 4096u, 0u, lane};
     uint32_t acc = 0, acc_phase = 0;
     for (int t = pair; t < ntiles; t += npairs) {
       const TileCoord tc = tile_coord(p, t);
@@ -979,7 +1109,7 @@ __global__ void __launch_bounds__(PairCfg<WN>::THREADS, 1)
           uint4 pin0[4] = {}, pin1[4] = {};
           const bool has0 = kIn >= 1 && p.in0 != nullptr;
           if (kIn > 0 && row < p.M) {
-  #pragma unroll
+#pragma unroll
             for (int qq = 0; qq < 2; ++qq) {
               const int64_t col = col_base + c * 32 + qq * 16;
               const int64_t idx = row * p.ldo + col;
@@ -989,7 +1119,7 @@ __global__ void __launch_bounds__(PairCfg<WN>::THREADS, 1)
                 if (has0) ld_b256(i0, pin0[2 * qq], pin0[2 * qq + 1]);
                 if (kIn == 2) ld_b256(i1, pin1[2 * qq], pin1[2 * qq + 1]);
               } else {
-  #pragma unroll
+#pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                   if (col + 8 * hh < p.N) {
                     if (has0) pin0[2 * qq + hh] = __ldg(reinterpret_cast<const uint4*>(i0 + 8 * hh));
@@ -1000,12 +1130,17 @@ __global__ void __launch_bounds__(PairCfg<WN>::THREADS, 1)
             }
           }
           tmem_ld_wait();
-          if (row < p.M) {
-  #pragma unroll
+          if (p.tma_out) {
+            const int64_t x = col_base + c * 32, y = row - lane;  // the warp's first row
+            if (y < p.M && x < p.N)
+              epi_chunk_tma<EPI>(p, stg, tc.g, static_cast<int>(x), static_cast<int>(y), ra, rb,
+                                 pin0, pin1, kIn > 0 && has0);
+          } else if (row < p.M) {
+#pragma unroll
             for (int qq = 0; qq < 2; ++qq) {  // 16 columns at a time
               const int64_t col = col_base + c * 32 + qq * 16;
               float a[16], b[16];
-  #pragma unroll
+#pragma unroll
               for (int i = 0; i < 16; ++i) {
                 a[i] = __uint_as_float(ra[qq * 16 + i]);
                 b[i] = __uint_as_float(rb[qq * 16 + i]);
@@ -1041,6 +1176,11 @@ __global__ void __launch_bounds__(PairCfg<WN>::THREADS, 1)
       } else {
         acc_phase ^= 1u;
       }
+    }
+    // the staged stores have read shared memory and written their outputs before exit
+    if (p.tma_out) {
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
     }
   }
 
@@ -1138,6 +1278,29 @@ tp_status make_map_3d(CUtensorMap* m, const Operand& op, uint32_t chunks) {
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed (code " + std::to_string(r) + ")");
+  return TP_OK;
+}
+
+// Store map of an output for the pair kernel's staged epilogue: 3-D (columns, rows,
+// groups), box 32 rows x 64 bytes (32 bf16 or 16 fp32 columns) x 1, 64-byte swizzle
+// (the staging boxes' layout). Groups stride `gstride` elements (fp32 partials).
+tp_status make_out_map(CUtensorMap* m, void* ptr, bool f32, int64_t N, int64_t M, int64_t ldo,
+                       int64_t groups, int64_t gstride) {
+  EncodeTiledFn enc = get_encoder();
+  if (!enc) return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
+  const int64_t esz = f32 ? 4 : 2;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M),
+                              static_cast<cuuint64_t>(groups)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ldo * esz),
+                                 static_cast<cuuint64_t>(gstride * esz)};
+  const cuuint32_t box[3] = {f32 ? 16u : 32u, 32u, 1u};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                   ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled (output) failed (code " + std::to_string(r) + ")");
   return TP_OK;
 }
 
@@ -1240,6 +1403,9 @@ void set_pair_mode(int v) { g_pair_mode.store(v); }
 void set_wide_mode(int v) { g_wide_mode.store(v); }
 
 // bytes the epilogue writes per output element (logical column) of a row
+#ifndef TP_TMA_STORE
+#define TP_TMA_STORE 1  // 0: the pair kernel's epilogue stores straight from registers
+#endif
 #ifndef TP_WIDE_K_PER_BYTE
 #define TP_WIDE_K_PER_BYTE 1024
 #endif
@@ -1357,6 +1523,21 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
     bool ok_in = (d.ldo * 2) % 32 == 0;
     for (const void* i : d.in) ok_in = ok_in && reinterpret_cast<uintptr_t>(i) % 32 == 0;
     prm.ld32 = ok_in ? 1 : 0;
+  }
+  // pair kernel: outputs staged in shared memory and TMA-stored, where every output's
+  // base, pitch and group stride are 16-byte multiples (else direct stores)
+  prm.tma_out = 0;
+  if (pair && TP_TMA_STORE) {
+    const int64_t esz = d.out_f32 ? 4 : 2;
+    const int64_t groups = d.out_f32 && d.groups > 1 ? d.groups : 1;
+    const int64_t gstride = groups > 1 ? d.out_group_stride : d.ldo * d.M;
+    bool ok = (d.ldo * esz) % 16 == 0 && (gstride * esz) % 16 == 0 && gstride > 0;
+    for (void* o : d.out) ok = ok && reinterpret_cast<uintptr_t>(o) % 16 == 0;
+    if (ok) {
+      for (int o = 0; o < 3; ++o)
+        if (d.out[o]) TP_TRY(make_out_map(&prm.tmO[o], d.out[o], d.out_f32, d.N, d.M, d.ldo, groups, gstride));
+      prm.tma_out = 1;
+    }
   }
   prm.status = device_status_word();
   if (!prm.status) return fail(TP_ERR_CUDA, "device status word unavailable");
