@@ -88,7 +88,7 @@ def col_gemm_flops(w):
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one column-GEMM launch,
 # from an ncu capture of the full-size workload, valid only for the kernel source it
-# was taken on (sha256 of csrc/gemm_tc.cu + csrc/ptx.cuh); see profiles/.
+# was taken on (sha256 of csrc/gemm_tc.cu + csrc/ptx.cuh + csrc/epi_math.cuh); see profiles/.
 COL_GEMM_TRAFFIC = {
     "c5": {"bytes": 11.041e9 + 1.401e9, "src": "d8b91c5e88db8c22"},
     "c3": {"bytes": 1.068e9 + 0.509e9, "src": "d8b91c5e88db8c22"},
@@ -111,7 +111,7 @@ def _kernel_source_hash():
     traffic figure is reported only while the kernel it was measured on is unchanged."""
     import hashlib
     h = hashlib.sha256()
-    for name in ("gemm_tc.cu", "ptx.cuh"):
+    for name in ("gemm_tc.cu", "ptx.cuh", "epi_math.cuh"):
         with open(os.path.join(ROOT, "attention_gemms_gb300", "csrc", name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
