@@ -90,19 +90,17 @@ def col_gemm_flops(w):
 # from an ncu capture of the full-size workload, valid only for the kernel source it
 # was taken on (sha256 of csrc/gemm_tc.cu + csrc/ptx.cuh + csrc/epi_math.cuh); see profiles/.
 COL_GEMM_TRAFFIC = {
-    "c5": {"bytes": 11.041e9 + 1.401e9, "src": "d8b91c5e88db8c22"},
-    "c3": {"bytes": 1.068e9 + 0.509e9, "src": "d8b91c5e88db8c22"},
+    "c5": {"bytes": 8.754e9 + 1.395e9, "src": "1ad9bce0f4ac71ff"},
+    "c3": {"bytes": 1.124e9 + 0.503e9, "src": "1ad9bce0f4ac71ff"},
 }
 
 
 # Tensor-pipe activity of the same launch (sm__pipe_tensor_cycles_active and
-# sm__pipe_tc_cycles_active, % of peak over the elapsed cycles) from an ncu capture,
-# under the same source-hash rule; c5's is taken on the c5-2k case (2048 of the 8192
-# tokens: the same kernel instance, tile shapes and per-tile K). See profiles/.
+# sm__pipe_tc_cycles_active, % of peak over the elapsed cycles) from a one-pass ncu
+# capture of the full-size workload, under the same source-hash rule. See profiles/.
 COL_GEMM_TENSOR_PIPE = {
-    "c5": {"tensor": 76.1, "tc": 82.9, "case": "c5-2k", "src": "d8b91c5e88db8c22"},
-    "c5-2k": {"tensor": 76.1, "tc": 82.9, "case": "c5-2k", "src": "d8b91c5e88db8c22"},
-    "c3": {"tensor": 65.2, "tc": 73.1, "case": "c3", "src": "d8b91c5e88db8c22"},
+    "c5": {"tensor": 90.03, "tc": 90.18, "case": "c5", "src": "1ad9bce0f4ac71ff"},
+    "c3": {"tensor": 67.32, "tc": 68.15, "case": "c3", "src": "1ad9bce0f4ac71ff"},
 }
 
 

@@ -70,7 +70,10 @@ def test_gemm_f32(at, bt):
 @pytest.mark.parametrize("at", [False, True])
 @pytest.mark.parametrize("bt", [False, True])
 @pytest.mark.parametrize("MNK", [(256, 512, 64), (256, 512, 128), (512, 1024, 320),
-                                 (600, 1288, 520), (768, 264, 192), (256, 256, 512)])
+                                 (600, 1288, 520), (768, 264, 192), (256, 256, 512),
+                                 # at least two tiles per SM pair: the epilogue's
+                                 # TMA-store path, ragged rows and columns
+                                 (4000, 5128, 200)])
 def test_pair_gemm_forms(wide, at, bt, MNK):
     M, N, K = MNK
     with gemm_tiles(2, wide):

@@ -181,6 +181,17 @@ def test_mlp_bf16_pair_tiles(act, mode, wide):
         assert e <= BF16_TOL, (k, e)
 
 
+@pytest.mark.parametrize("wide", [0, 2], ids=["pair256", "pair512"])
+@pytest.mark.parametrize("act", [T.Act.GELU, T.Act.SWIGLU])
+def test_mlp_bf16_pair_tiles_many(act, wide):
+    """Enough tiles per SM pair that the column GEMM and dA take the TMA-store epilogue
+    (at least two tiles per pair), with a ragged M."""
+    with gemm_tiles(2, wide):
+        errs, _ = _mlp_run(act, T.Reduce.SPLITK, 2, M=2600, h=256, f=4096)
+    for k, e in errs.items():
+        assert e <= BF16_TOL, (k, e)
+
+
 def test_mlp_bf16_multi_tile_k():
     """Several 64-wide K blocks per shard and several M/N tiles with a ragged M tail."""
     errs, _ = _mlp_run(T.Act.GELU, T.Reduce.BUFFERS, 2, M=700, h=384, f=1024)
