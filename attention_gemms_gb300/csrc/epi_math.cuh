@@ -45,6 +45,35 @@ __device__ __forceinline__ float sigmoid_sfu(float x) {
   return r;
 }
 __device__ __forceinline__ float silu_sfu(float x) { return x * sigmoid_sfu(x); }
+
+// Phi and phi for the bf16 epilogues, after Abramowitz & Stegun, Handbook of
+// Mathematical Functions, 7.1.26 (Hastings' approximation):
+//   erfc(z) = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) e^(-z^2),  t = 1 / (1 + p z),  z >= 0,
+// absolute error below 1.5e-7 (CUDA's erff is within ~1e-7). With z = |x| / sqrt 2,
+// e^(-z^2) = e^(-x^2 / 2) = sqrt(2 pi) phi(x), so GELU' = Phi + x phi takes one
+// exponential for both terms; the exponential (2^(-x^2 log2(e) / 2)) and the reciprocal
+// run on the SFU. Phi is formed from the small tail erfc(|x| / sqrt 2) / 2 on either side.
+__device__ __forceinline__ void normal_sfu(float x, float& Phi, float& phi) {
+  float t, e;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(fmaf(0.3275911f * 0.70710678118654752f, fabsf(x), 1.0f)));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * x * -0.72134752044448170f));
+  const float poly =
+      t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f), -0.284496736f),
+               0.254829592f);
+  const float tail = 0.5f * poly * e;  // P(N(0,1) > |x|)
+  Phi = x >= 0.0f ? 1.0f - tail : tail;
+  phi = 0.39894228040143268f * e;
+}
+__device__ __forceinline__ float gelu_sfu(float x) {
+  float Phi, phi;
+  normal_sfu(x, Phi, phi);
+  return x * Phi;
+}
+__device__ __forceinline__ float gelu_prime_sfu(float x) {
+  float Phi, phi;
+  normal_sfu(x, Phi, phi);
+  return fmaf(x, phi, Phi);
+}
 __device__ __forceinline__ float dswiglu_sfu(float a, float g, float u, float& du) {
   return dswiglu_of(a, g, u, sigmoid_sfu(g), du);
 }

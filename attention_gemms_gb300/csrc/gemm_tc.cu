@@ -27,6 +27,18 @@
 #include "internal.h"
 #include "ptx.cuh"
 
+// GELU and GELU' of the bf16 epilogues: the SFU forms (1), or erff / expf (0)
+#ifndef TP_GELU_SFU
+#define TP_GELU_SFU 1
+#endif
+#if TP_GELU_SFU
+#define TP_GELU gelu_sfu
+#define TP_GELU_PRIME gelu_prime_sfu
+#else
+#define TP_GELU gelu_f
+#define TP_GELU_PRIME gelu_prime_f
+#endif
+
 namespace tp {
 namespace {
 
@@ -216,7 +228,7 @@ __device__ __forceinline__ void epi8(const TcParams& p, int g, int64_t row, int6
   } else if constexpr (EPI == EPI_GELU) {
     if (p.out0) st8(p.out0, idx, a);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = gelu_f(a[i]);
+    for (int i = 0; i < 8; ++i) v[i] = TP_GELU(a[i]);
     st8(p.out1, idx, v);
   } else if constexpr (EPI == EPI_SWIGLU) {
     if (p.out0) st8(p.out0, idx, a);
@@ -227,7 +239,7 @@ __device__ __forceinline__ void epi8(const TcParams& p, int g, int64_t row, int6
   } else if constexpr (EPI == EPI_DGELU) {
     in8(p.in0, pre0, w);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = a[i] * gelu_prime_f(w[i]);
+    for (int i = 0; i < 8; ++i) v[i] = a[i] * TP_GELU_PRIME(w[i]);
     st8(p.out0, idx, v);
   } else if constexpr (EPI == EPI_DSWIGLU) {
     float gg[8], uu[8], du[8];
@@ -318,7 +330,7 @@ __device__ __forceinline__ void epi16(const TcParams& p, int g, int64_t row, int
   } else if constexpr (EPI == EPI_GELU) {
     if (p.out0) st16(p.out0, idx, a, wide);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = gelu_f(a[i]);
+    for (int i = 0; i < 16; ++i) v[i] = TP_GELU(a[i]);
     st16(p.out1, idx, v, wide);
   } else if constexpr (EPI == EPI_SWIGLU) {
     if (p.out0) st16(p.out0, idx, a, wide);
@@ -329,7 +341,7 @@ __device__ __forceinline__ void epi16(const TcParams& p, int g, int64_t row, int
   } else if constexpr (EPI == EPI_DGELU) {
     in16(p.in0, idx, w, pre, i0a, i0b);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = a[i] * gelu_prime_f(w[i]);
+    for (int i = 0; i < 16; ++i) v[i] = a[i] * TP_GELU_PRIME(w[i]);
     st16(p.out0, idx, v, wide);
   } else if constexpr (EPI == EPI_DSWIGLU) {
     float uu[16], du[16];
@@ -438,13 +450,13 @@ __device__ __forceinline__ void epi_chunk_tma(const TcParams& p, EpiStager& st, 
     else stage_bf16(st, &p.tmO[0], x, y, v);
   } else if constexpr (EPI == EPI_GELU) {
     if (p.out0) stage_bf16(st, &p.tmO[0], x, y, A);
-    stage_bf16(st, &p.tmO[1], x, y, [&](int j) { return gelu_f(A(j)); });
+    stage_bf16(st, &p.tmO[1], x, y, [&](int j) { return TP_GELU(A(j)); });
   } else if constexpr (EPI == EPI_SWIGLU) {
     if (p.out0) stage_bf16(st, &p.tmO[0], x, y, A);
     if (p.out1) stage_bf16(st, &p.tmO[1], x, y, B);
     stage_bf16(st, &p.tmO[2], x, y, [&](int j) { return silu_sfu(A(j)) * B(j); });
   } else if constexpr (EPI == EPI_DGELU) {
-    stage_bf16(st, &p.tmO[0], x, y, [&](int j) { return A(j) * gelu_prime_f(in_at(pin0, j)); });
+    stage_bf16(st, &p.tmO[0], x, y, [&](int j) { return A(j) * TP_GELU_PRIME(in_at(pin0, j)); });
   } else if constexpr (EPI == EPI_DSWIGLU) {
     // dG and dU share the gate's sigmoid: both boxes are filled in one pass
     st.acquire<0>();

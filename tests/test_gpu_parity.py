@@ -275,3 +275,52 @@ def test_decode_forward(T_, act, mode):
     assert rel(host(H), ref["A"] if sw else ref["H"]) <= BF16_TOL
     assert rel(host(Z), ref["Z"]) <= BF16_TOL
     assert guard_intact(full, M)
+
+
+# ---------------------------------------------------------------- GELU epilogue precision
+#
+# The bf16 epilogues compute Phi by an approximation of erf with an absolute error below
+# 1.5e-7 on the special-function unit. These inputs make the accumulator of every output
+# exactly one chosen bf16 value v (X = a column of ones, W1 holding v in its first row), so
+# the epilogue's result can be held to the bf16 rounding of the exact value: |got - ref|
+# <= 2^-8 |ref| + 1e-6 (bf16 keeps 8 significant bits; round to nearest). The backward's
+# dY = dH * GELU'(Y) reaches dW1 = X^T dY unrounded for M a power of two (dH = 1
+# exactly: dZ and W2 hold ones in their first column).
+
+def _gelu_sweep_inputs(M, h, f):
+    v = torch.linspace(-9.0, 9.0, f).to(torch.bfloat16)
+    X = torch.zeros(M, h, dtype=torch.bfloat16)
+    X[:, 0] = 1.0
+    W1 = torch.zeros(h, f, dtype=torch.bfloat16)
+    W1[0] = v
+    W2 = torch.zeros(f, h, dtype=torch.bfloat16)
+    W2[:, 0] = 1.0
+    dZ = torch.zeros(M, h, dtype=torch.bfloat16)
+    dZ[:, 0] = 1.0
+    return v.double().numpy(), X.cuda(), W1.cuda(), W2.cuda(), dZ.cuda()
+
+
+@pytest.mark.parametrize("M,pair,wide", [(128, 1, 1), (256, 2, 0), (256, 2, 2), (4096, 2, 0)],
+                         ids=["one-cta", "pair256", "pair512", "pair256-tma"])
+def test_gelu_epilogue_precision(M, pair, wide):
+    h, f = 64, 4096
+    v, X, W1, W2, dZ = _gelu_sweep_inputs(M, h, f)
+    e = lambda *s: torch.empty(*s, dtype=bf16, device="cuda")
+    Y, H, Z, dX, dW1, dW2 = e(M, f), e(M, f), e(M, h), e(M, h), e(h, f), e(f, h)
+    md = T.Reduce.SPLITK
+    ws = _ws(max(T.tp_workspace_size(T.Op.MLP_FWD, M, h, f, 1, BF, T.Act.GELU, md),
+                 T.tp_workspace_size(T.Op.MLP_BWD, M, h, f, 1, BF, T.Act.GELU, md)))
+    with gemm_tiles(pair, wide):
+        T.tp_mlp_fwd(X, W1, None, W2, None, Y, None, H, Z, M, h, f, 1, BF, T.Act.GELU, md, ws,
+                     ws.numel())
+        T.tp_mlp_bwd(X, W1, None, W2, Y, None, H, dZ, dX, dW1, None, dW2, M, h, f, 1, BF,
+                     T.Act.GELU, md, ws, ws.numel())
+        torch.cuda.synchronize()
+    assert T.tp_check_status() == 0
+    assert np.array_equal(host(Y[[0, M - 1]]), np.stack([v, v]))
+    g, gp = O.gelu(v), O.gelu_prime(v)
+    for got in (host(H[0]), host(H[M - 1])):
+        assert np.all(np.abs(got - g) <= 2.0 ** -8 * np.abs(g) + 1e-6), np.max(np.abs(got - g))
+    if M & (M - 1) == 0:
+        got = host(dW1[0]) / M
+        assert np.all(np.abs(got - gp) <= 2.0 ** -8 * np.abs(gp) + 1e-6), np.max(np.abs(got - gp))
