@@ -654,7 +654,7 @@ def run_sp(args, w, T, device, rank, nranks):
                    "l2": "inputs larger than L2 (no flush)"},
         "pct_of_peak": round(100 * value / nranks / peak, 2),
         "without_sp_ms_per_step": round(tp_max, 4),
-        "roofline": {"bound": "tensor", "kernel": "gemm_tc_kernel (column-parallel GEMM + fused "
+        "roofline": {"bound": "tensor", "kernel": "gemm_tc2_kernel (column-parallel GEMM + fused "
                      + ("SwiGLU" if sw else "GELU") + " epilogue), timed on its own at the "
                      "block's shape", "achieved": round(col_tf, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(col_tf / peak, 4),
