@@ -1047,6 +1047,7 @@ __global__ void __launch_bounds__(PairCfg<WN>::THREADS, 1)
             }
           }
           if (!ok) break;
+          if (pre == nkb) mma_commit_pair(tfull_bar(0), 0x3);  // the first half is complete
           if (!mbar_wait(tempty_bar(1), acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
             ok = false;
             break;
@@ -1060,7 +1061,11 @@ __global__ void __launch_bounds__(PairCfg<WN>::THREADS, 1)
           }
           kb = pre;
         }
-        for (; kb < nkb; ++kb) {
+        // wide: the last `post` stages run their first-half MMAs first, so that the first
+        // half of the accumulator is complete (tfull 0) and drains while their second-half
+        // MMAs run (tfull 1)
+        const int post = WN == 2 ? min(S, nkb - kb) : 0;
+        for (; kb < nkb - post; ++kb) {
           if (!wait_full()) {
             ok = false;
             break;
@@ -1069,7 +1074,32 @@ __global__ void __launch_bounds__(PairCfg<WN>::THREADS, 1)
           release();
         }
         if (!ok) break;
-        mma_commit_pair(tfull_bar(acc), 0x3);
+        if constexpr (WN == 2) {
+          if (post > 0) {
+            const uint32_t stage0 = stage, phase0 = phase;
+            for (int j = 0; j < post && ok; ++j) {
+              ok = wait_full();
+              if (!ok) break;
+              issue(d_tmem, 0, 1, kb + j);
+              if (++stage == S) {
+                stage = 0;
+                phase ^= 1u;
+              }
+            }
+            if (!ok) break;
+            mma_commit_pair(tfull_bar(0), 0x3);
+            stage = stage0;
+            phase = phase0;
+            for (int j = 0; j < post; ++j) {
+              issue(d_tmem, 1, 2, kb + j);
+              release();
+            }
+            kb += post;
+          }
+          mma_commit_pair(tfull_bar(1), 0x3);
+        } else {
+          mma_commit_pair(tfull_bar(acc), 0x3);
+        }
         if (C::NACC == 2) {
           acc ^= 1u;
           if (acc == 0) acc_phase ^= 1u;
@@ -1097,7 +1127,9 @@ __global__ void __launch_bounds__(PairCfg<WN>::THREADS, 1)
       const TileCoord tc = tile_coord(p, t);
       int ok = 1;
       [[maybe_unused]] const long long tw = TP_CLK();
-      if (lane == 0) ok = mbar_wait(tfull_bar(acc), acc_phase, p.timeout_ns, abort_flag) ? 1 : 0;
+      // narrow: the whole accumulator; wide: each half is waited for below
+      if (lane == 0 && WN == 1)
+        ok = mbar_wait(tfull_bar(acc), acc_phase, p.timeout_ns, abort_flag) ? 1 : 0;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       [[maybe_unused]] const long long tb = TP_CLK();
       if (warp == 2 && lane == 0) TP_STAT(3, tb - tw);
@@ -1109,7 +1141,16 @@ __global__ void __launch_bounds__(PairCfg<WN>::THREADS, 1)
       const int64_t row =
           static_cast<int64_t>(tc.mt) * 256 + static_cast<int>(rank) * 128 + quad * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * 256;
-      for (int h = 0; h < WN; ++h) {
+      for (int h = 0; h < WN && ok; ++h) {
+        if (WN == 2) {
+          if (lane == 0) ok = mbar_wait(tfull_bar(h), acc_phase, p.timeout_ns, abort_flag) ? 1 : 0;
+          ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+          if (!ok) {
+            if (lane == 0) record_timeout(p.status);
+            break;
+          }
+          tc_fence_after();
+        }
         const int64_t col_base = (static_cast<int64_t>(tc.nt) * WN + h) * bn_logical;
         const uint32_t t_half = t_row + h * 256;
         for (int c = c_lo; c < c_hi; ++c) {
@@ -1175,6 +1216,7 @@ __global__ void __launch_bounds__(PairCfg<WN>::THREADS, 1)
           }
         }
       }
+      if (!ok) break;
       if (warp == 2 && lane == 0) TP_STAT(4, TP_CLK() - tb);
       if (C::NACC == 2) {
         tc_fence_before();
