@@ -421,9 +421,10 @@ __global__ void __launch_bounds__(FwdLayout<NH>::kThreads, kCtasPerSm) attn_fwd_
 
 constexpr int kBwdQKVTile = 128 * 64 * 2;  // 16 KB
 constexpr int kBwdBlk = 64 * 64 * 2;       // 8 KB: a 64-row block
-// dQ: Q, dO, two K/V stages, dS; dK/dV: K, V, two Q/dO stages, P^T, dS^T, and a
+// dQ: Q, dO, three K/V stages, dS; dK/dV: K, V, two Q/dO stages, P^T, dS^T, and a
 // per-warp table of the 64 (lse, D) pairs of the current query block. + barriers + slack
-constexpr int kBwdSmemDq = 5 * kBwdQKVTile + 256 + 1024;
+constexpr int kKvStagesDq = 3;
+constexpr int kBwdSmemDq = (3 + kKvStagesDq) * kBwdQKVTile + 256 + 1024;
 constexpr int kBwdSmemKv = 6 * kBwdQKVTile + 256 + 8 * 32 * 8 + 1024;
 
 struct AttnBwdParams {
@@ -508,18 +509,25 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dq_tc_kernel(const __
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_u32(smem);
-  // Q (16 KB) | dO (16 KB) | K0 V0 K1 V1 (8 KB each) | dS (16 KB) | barriers
+  // Q (16 KB) | dO (16 KB) | K/V stages (K 8 KB, V 8 KB each) | dS (16 KB) | barriers.
+  // Three stages: a stage is released once dQ of its key block completes, which comes
+  // just before S of the block after next is wanted; the third stage lets its load start
+  // a block earlier
+  constexpr int NS = kKvStagesDq;
   const uint32_t sQ = sb, sdO = sb + kBwdQKVTile, sKV = sb + 2 * kBwdQKVTile,
-                 sdS = sb + 4 * kBwdQKVTile;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 5 * kBwdQKVTile);
+                 sdS = sb + (2 + NS) * kBwdQKVTile;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (3 + NS) * kBwdQKVTile);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
-  const uint32_t qd_full = bar0, s_full = bar0 + 8 * 5, p_full = bar0 + 8 * 6,
-                 o_done = bar0 + 8 * 7, drain = bar0 + 8 * 8, never = bar0 + 8 * 9,
-                 s_free = bar0 + 8 * 10;
+  // barriers: qd_full | kv_full[NS] | kv_empty[NS] | s_full p_full o_done drain never s_free
+  constexpr int kB = 1 + 2 * NS;
+  static_assert(kB + 6 <= 16, "barriers overlap the TMEM slot");
+  const uint32_t qd_full = bar0, s_full = bar0 + 8 * kB, p_full = bar0 + 8 * (kB + 1),
+                 o_done = bar0 + 8 * (kB + 2), drain = bar0 + 8 * (kB + 3),
+                 never = bar0 + 8 * (kB + 4), s_free = bar0 + 8 * (kB + 5);
   auto kv_full = [&](int st) { return bar0 + 8u * (1 + st); };
-  auto kv_empty = [&](int st) { return bar0 + 8u * (3 + st); };
+  auto kv_empty = [&](int st) { return bar0 + 8u * (1 + NS + st); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.z, t = blockIdx.y, q0 = blockIdx.x * 128;
@@ -533,7 +541,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dq_tc_kernel(const __
 
   if (threadIdx.x == 0) {
     mbar_init(qd_full, 1);
-    for (int st = 0; st < 2; ++st) {
+    for (int st = 0; st < NS; ++st) {
       mbar_init(kv_full(st), 1);
       mbar_init(kv_empty(st), 1);
     }
@@ -566,8 +574,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dq_tc_kernel(const __
       tma_load_2d(sQ, &p.tq128, qd_full, qc, row0 + q0);
       tma_load_2d(sdO, &p.tdo128, qd_full, t * 64, row0 + q0);
       for (int j = 0; j < nkb; ++j) {
-        const int st = j & 1;
-        if (j >= 2 && !mbar_wait(kv_empty(st), ((j >> 1) - 1) & 1, p.timeout_ns, abort_flag)) {
+        const int st = j % NS;
+        if (j >= NS && !mbar_wait(kv_empty(st), (j / NS - 1) & 1, p.timeout_ns, abort_flag)) {
           ok = false;
           break;
         }
@@ -587,8 +595,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dq_tc_kernel(const __
       bool ok = mbar_wait(qd_full, 0, p.timeout_ns, abort_flag);
       if (ok && p.debug_hang) ok = mbar_wait(never, 0, p.timeout_ns, abort_flag);
       auto issue_s = [&](int j) -> bool {  // S = Q K^T and dP = dO V^T of key block j
-        const int st = j & 1;
-        if (!mbar_wait(kv_full(st), (j >> 1) & 1, p.timeout_ns, abort_flag)) return false;
+        const int st = j % NS;
+        if (!mbar_wait(kv_full(st), (j / NS) & 1, p.timeout_ns, abort_flag)) return false;
         tc_fence_after();
         const uint32_t k = sKV + st * 2 * kBwdBlk, v = k + kBwdBlk;
 #pragma unroll
@@ -620,7 +628,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dq_tc_kernel(const __
           break;
         }
         tc_fence_after();
-        const int st = j & 1;
+        const int st = j % NS;
         const uint32_t k = sKV + st * 2 * kBwdBlk;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // dQ += dS K (K read MN-major: rows = keys)
@@ -715,8 +723,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 2) attn_bwd_dq_tc_kernel(const __
     volatile int no_abort = 0;
     if (warp == 8 && lane == 0) {
       mbar_wait(qd_full, 0, kDrainNs, &no_abort);
-      for (int st = 0; st < 2; ++st) {
-        const int n = issued > st ? (issued - 1 - st) / 2 : -1;
+      for (int st = 0; st < NS; ++st) {
+        const int n = issued > st ? (issued - 1 - st) / NS : -1;
         if (n >= 0) mbar_wait(kv_full(st), n & 1, kDrainNs, &no_abort);
       }
     }
