@@ -1502,15 +1502,23 @@ tp_status launch_gemm_tc(const GemmDesc& d, cudaStream_t st) {
   const int tile_m = pair ? 256 : BM;
   // pair tiles twice as wide (256 x 512): 3/4 of the operand bytes per FLOP, but one
   // accumulator, so most of each tile's epilogue is not hidden behind MMAs: taken
-  // where the width is whole wide tiles, there are at least four per SM pair, and
-  // the tile's K is long beside the bytes its epilogue writes per output element
+  // where the width is whole wide tiles, the tile's K is long beside the bytes its
+  // epilogue writes per output element, and either there are at least four wide tiles
+  // per SM pair or the wide tiles need so many fewer waves of the 76 pairs that a wave
+  // of them (2 narrow tiles' work at ~10 % more per cycle) still ends first
+  // (2048 x 4096 x 2048: 64 wide tiles in one wave, not 128 narrow ones in two)
   bool wide = false;
   if (pair) {
     const int64_t ww = 2 * bn_logical;
-    const int64_t wtiles = (d.M + 255) / 256 * ((d.N + ww - 1) / ww) * d.groups;
+    const int64_t rows = (d.M + 255) / 256 * d.groups;
+    const int64_t wtiles = rows * ((d.N + ww - 1) / ww);
+    const int64_t ntiles = rows * ((d.N + bn_logical - 1) / bn_logical);
+    const int64_t pairs_n = std::max<int64_t>(device_sm_count() / 2, 1);
+    auto waves = [&](int64_t t) { return (t + pairs_n - 1) / pairs_n; };
+    const bool many = wtiles >= 4 * pairs_n || 18 * waves(wtiles) < 10 * waves(ntiles);
     const int64_t k_tile = static_cast<int64_t>(d.nseg) * d.K;
     const int mode = g_wide_mode.load();
-    wide = mode == 2 || (mode == 1 && d.N % ww == 0 && wtiles >= 2 * device_sm_count() &&
+    wide = mode == 2 || (mode == 1 && d.N % ww == 0 && many &&
                          k_tile >= static_cast<int64_t>(TP_WIDE_K_PER_BYTE) * epi_out_bytes(d));
   }
   const int tile_w = bn_logical * (wide ? 2 : 1);  // logical output columns of a tile
