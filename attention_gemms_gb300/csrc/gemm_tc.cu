@@ -11,6 +11,11 @@
 // and inside a slab in groups of 16 M-tiles so that concurrently running CTAs
 // share operand tiles through L2.
 //
+// Large GEMMs run on the CTA-pair kernel further down (gemm_tc2_kernel): two CTAs of a
+// cluster share 256 x 256 tiles through cta_group::2 MMAs, or 256 x 512 tiles with one
+// 128 x 512 accumulator per CTA, and stage the epilogue's outputs in shared memory for
+// TMA stores.
+//
 // Every mbarrier wait is bounded by a time limit; on expiry the CTA records
 // TP_ERR_TIMEOUT in the device status word, waits for its own copies and MMAs
 // in flight, frees its TMEM and returns.
