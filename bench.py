@@ -90,8 +90,8 @@ def col_gemm_flops(w):
 # from an ncu capture of the full-size workload, valid only for the kernel source it
 # was taken on (sha256 of csrc/gemm_tc.cu + csrc/ptx.cuh + csrc/epi_math.cuh); see profiles/.
 COL_GEMM_TRAFFIC = {
-    "c5": {"bytes": 5.802e9 + 1.392e9, "src": "563550b4021e94e1"},
-    "c3": {"bytes": 1.125e9 + 0.501e9, "src": "563550b4021e94e1"},
+    "c5": {"bytes": 6.647e9 + 1.398e9, "src": "d417b4ec8df59967"},
+    "c3": {"bytes": 1.123e9 + 0.502e9, "src": "d417b4ec8df59967"},
 }
 
 
@@ -99,8 +99,8 @@ COL_GEMM_TRAFFIC = {
 # sm__pipe_tc_cycles_active, % of peak over the elapsed cycles) from a one-pass ncu
 # capture of the full-size workload, under the same source-hash rule. See profiles/.
 COL_GEMM_TENSOR_PIPE = {
-    "c5": {"tensor": 90.38, "tc": 90.58, "case": "c5", "src": "563550b4021e94e1"},
-    "c3": {"tensor": 74.63, "tc": 75.42, "case": "c3", "src": "563550b4021e94e1"},
+    "c5": {"tensor": 90.03, "tc": 90.24, "case": "c5", "src": "d417b4ec8df59967"},
+    "c3": {"tensor": 74.10, "tc": 74.92, "case": "c3", "src": "d417b4ec8df59967"},
 }
 
 
