@@ -221,10 +221,11 @@ TP_API void tp_set_gemm_pair_mode(int enable);
 /* Width of the CTA-pair tiles: 1 (default) uses 256 x 512 tiles -- two pair MMAs per
  * K step into one 128 x 512 accumulator per CTA, 3/4 of the operand bytes per FLOP of
  * 256 x 256 -- where the output width is whole 512-column tiles (256 for the paired
- * gate/up form) and there are at least four tiles per SM pair; 0 keeps 256 x 256
- * tiles; 2 takes the wide tiles for every pair-kernel GEMM (to test that form on
- * small shapes). Results agree within rounding in every mode. Applies to launches
- * made after the call; any other value is treated as 1. */
+ * gate/up form), K is long beside the bytes the epilogue writes, and there are at
+ * least four tiles per SM pair or the wide tiles need enough fewer waves of the SM
+ * pairs; 0 keeps 256 x 256 tiles; 2 takes the wide tiles for every pair-kernel GEMM
+ * (to test that form on small shapes). Results agree within rounding in every mode.
+ * Applies to launches made after the call; any other value is treated as 1. */
 TP_API void tp_set_gemm_wide_mode(int mode);
 
 /* Number of kernel launches this library has made in this process (all threads). */
