@@ -192,6 +192,17 @@ def test_mlp_bf16_pair_tiles_many(act, wide):
         assert e <= BF16_TOL, (k, e)
 
 
+@pytest.mark.parametrize("act", [T.Act.GELU, T.Act.SWIGLU])
+def test_mlp_bf16_buffers_staged_partials(act):
+    """Per-shard fp32 partials (variant A) through the staged TMA-store epilogue: the row
+    GEMM and dX have enough tiles (K-groups x 11 x 8) for it, with a ragged M, so the
+    partials' 3-D store map (columns, rows, shard) and its clipped last row tile are
+    exercised."""
+    errs, _ = _mlp_run(act, T.Reduce.BUFFERS, 2, M=2600, h=2048, f=1024)
+    for k, e in errs.items():
+        assert e <= BF16_TOL, (k, e)
+
+
 def test_mlp_bf16_multi_tile_k():
     """Several 64-wide K blocks per shard and several M/N tiles with a ragged M tail."""
     errs, _ = _mlp_run(T.Act.GELU, T.Reduce.BUFFERS, 2, M=700, h=384, f=1024)
